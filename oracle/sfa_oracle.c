@@ -1,0 +1,262 @@
+/*
+ * sfa_oracle.c -- the parity oracle for indexer-selected block-sparse attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this file:
+ * only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg do.  It shares no
+ * code, header, table or helper with the CUDA library.
+ *
+ * Plain, slow and obviously correct: every quantity is computed in double precision from
+ * the (exactly representable) input values, straight from the definition, with no
+ * blocking, fusion or reordering beyond what the definition states.
+ *
+ * Sources (the pages this restates):
+ *  [QSA]  llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", the paragraphs on
+ *         the QSA indexer: "An indexer scores one mean-pooled key per block of
+ *         compress_ratio tokens and keeps a budget of the best blocks, plus the tail of
+ *         tokens that do not yet form a complete block"; the indexer key cache holds raw
+ *         keys (pooling precedes norm and rotation); each head's dot product is rectified
+ *         before the sum over heads; the graph expands block scores to tokens so the cut
+ *         lands on a block boundary.
+ *  [SFA]  llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM": attention over a
+ *         sparse K/V set with V a view of the first DV dims of K, no ALiBi, no softcap,
+ *         index rows padded with -1.
+ *
+ * Readings where the pages are silent (each one is listed with its reason in the design
+ * notes): indexer_top_k counts blocks; a block counts for query i only when all of its
+ * tokens are at positions <= p_i; the tail is [B_i*cr, p_i]; ties at the cut go to the
+ * lower block index; the indexer has no extra scale; head h reads KV head h / (H_q/H_kv).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------ */
+/* Step 1 -- block mean pooling of the raw index keys [QSA, indexer paragraph].
+ *   kbar_b[d] = (1/cr) * sum_{t = b*cr}^{b*cr + cr - 1} X[t][d],   b = 0 .. n_blk-1
+ * X is one sequence's index-key cache, row-major [n_tok][d_idx]; n_blk*cr <= n_tok.     */
+void sfa_oracle_pool(const float *X, int64_t n_blk, int d_idx, int cr, double *kbar)
+{
+    for (int64_t b = 0; b < n_blk; ++b) {
+        for (int d = 0; d < d_idx; ++d) {
+            double sum = 0.0;
+            for (int t = 0; t < cr; ++t)
+                sum += (double)X[(b * cr + t) * (int64_t)d_idx + d];
+            kbar[b * d_idx + d] = sum / (double)cr;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Step 2 -- indexer score of every complete block [QSA, ReLU paragraph].
+ *   s_b = sum_j w_j * max(0, q_j . kbar_b)
+ * q_idx is [h_idx][d_idx] for one query token, w is [h_idx].                              */
+void sfa_oracle_index_scores(const float *q_idx, const float *w, int h_idx, int d_idx,
+                             const double *kbar, int64_t n_blk, double *score)
+{
+    for (int64_t b = 0; b < n_blk; ++b) {
+        double s = 0.0;
+        for (int j = 0; j < h_idx; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < d_idx; ++d)
+                dot += (double)q_idx[j * d_idx + d] * kbar[b * d_idx + d];
+            double relu = dot > 0.0 ? dot : 0.0;
+            s += (double)w[j] * relu;
+        }
+        score[b] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Step 3 -- the budget rule [QSA, budget paragraph].
+ * If every block fits the budget (n_blk <= top_k) all blocks are kept.  Otherwise all
+ * blocks are fully sorted by (score descending, block index ascending) and the first
+ * top_k are kept.  The kept ids are written ascending and the row is padded with -1
+ * (the padding convention of [SFA]).  Returns the number kept.                           */
+struct scored_block { double s; int64_t b; };
+
+static int by_score_then_index(const void *pa, const void *pb)
+{
+    const struct scored_block *a = pa, *b = pb;
+    if (a->s > b->s) return -1;
+    if (a->s < b->s) return 1;
+    return (a->b < b->b) ? -1 : (a->b > b->b);
+}
+
+static int ascending_i32(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+int sfa_oracle_select(const double *score, int64_t n_blk, int top_k, int32_t *sel)
+{
+    int n_sel;
+    if (n_blk <= top_k) {
+        n_sel = (int)n_blk;
+        for (int i = 0; i < n_sel; ++i) sel[i] = i;
+    } else {
+        struct scored_block *all = malloc(sizeof(*all) * (size_t)n_blk);
+        for (int64_t b = 0; b < n_blk; ++b) { all[b].s = score[b]; all[b].b = b; }
+        qsort(all, (size_t)n_blk, sizeof(*all), by_score_then_index);
+        n_sel = top_k;
+        for (int i = 0; i < n_sel; ++i) sel[i] = (int32_t)all[i].b;
+        free(all);
+        qsort(sel, (size_t)n_sel, sizeof(int32_t), ascending_i32);
+    }
+    for (int i = n_sel; i < top_k; ++i) sel[i] = -1;
+    return n_sel;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Step 4 -- the attended set as an explicit mask over positions 0..p [QSA, budget
+ * paragraph]: every token of a kept block, plus the tail [B*cr, p] of tokens that do not
+ * form a complete block, B = floor((p+1)/cr).  top_k <= 0 means dense: all of 0..p.      */
+void sfa_oracle_mask(int64_t p, int cr, const int32_t *sel, int n_sel, int dense,
+                     uint8_t *mask)
+{
+    const int64_t n_vis = p + 1;
+    if (dense) {
+        for (int64_t t = 0; t < n_vis; ++t) mask[t] = 1;
+        return;
+    }
+    const int64_t n_blk = n_vis / cr;
+    for (int64_t t = 0; t < n_vis; ++t) mask[t] = 0;
+    for (int i = 0; i < n_sel; ++i)
+        for (int64_t t = (int64_t)sel[i] * cr; t < (int64_t)sel[i] * cr + cr; ++t) mask[t] = 1;
+    for (int64_t t = n_blk * cr; t < n_vis; ++t) mask[t] = 1;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Step 5 -- exact softmax attention over the masked tokens [SFA].
+ * For head h (KV head g = h / (h_q / h_kv)):
+ *   l_t = scale * q_h . K[t][g],   O_h = sum_t exp(l_t - m) V[t][g] / sum_t exp(l_t - m),
+ *   lse_h = m + log(sum_t exp(l_t - m)),   m = max over masked t of l_t.
+ * Token t's K row is K + row(t)*k_row_stride + g*dkq where row(t) = t, or tok_row[t] when
+ * tok_row is given (so callers may pass only the rows that the mask touches).  V == NULL
+ * means V[t][g] is the first dv entries of K[t][g].                                      */
+void sfa_oracle_attend(const float *q, int h_q, int h_kv, int dkq, int dv, double scale,
+                       const float *K, int64_t k_row_stride, const float *V,
+                       int64_t v_row_stride, const int64_t *tok_row, const uint8_t *mask,
+                       int64_t n_vis, double *out, double *lse)
+{
+    const int group = h_q / h_kv;
+    double *logit = malloc(sizeof(double) * (size_t)(n_vis > 0 ? n_vis : 1));
+    for (int h = 0; h < h_q; ++h) {
+        const int g = h / group;
+        const float *qh = q + (int64_t)h * dkq;
+        double m = -INFINITY;
+        for (int64_t t = 0; t < n_vis; ++t) {
+            if (!mask[t]) continue;
+            const int64_t r = tok_row ? tok_row[t] : t;
+            const float *kt = K + r * k_row_stride + (int64_t)g * dkq;
+            double dot = 0.0;
+            for (int d = 0; d < dkq; ++d) dot += (double)qh[d] * (double)kt[d];
+            logit[t] = scale * dot;
+            if (logit[t] > m) m = logit[t];
+        }
+        double denom = 0.0;
+        double *oh = out + (int64_t)h * dv;
+        for (int d = 0; d < dv; ++d) oh[d] = 0.0;
+        for (int64_t t = 0; t < n_vis; ++t) {
+            if (!mask[t]) continue;
+            const int64_t r = tok_row ? tok_row[t] : t;
+            const float *vt = V ? V + r * v_row_stride + (int64_t)g * dv
+                                : K + r * k_row_stride + (int64_t)g * dkq;
+            const double e = exp(logit[t] - m);
+            denom += e;
+            for (int d = 0; d < dv; ++d) oh[d] += e * (double)vt[d];
+        }
+        for (int d = 0; d < dv; ++d) oh[d] /= denom;
+        if (lse) lse[h] = m + log(denom);
+    }
+    free(logit);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* The whole method for a batch of query tokens, one query per task over n_threads
+ * host threads.  Each query i belongs to sequence q_seq[i] at position q_pos[i] and sees
+ * that sequence's tokens 0..q_pos[i] only.
+ *
+ * Layouts (row-major, contiguous):
+ *   X     [n_seq][n_tok][d_idx]         raw index keys
+ *   q_idx [n_q][h_idx][d_idx], w [n_q][h_idx]
+ *   Q     [n_q][h_q][dkq]
+ *   K     [n_seq][n_tok][h_kv][dkq],  V [n_seq][n_tok][h_kv][dv] or NULL
+ * Outputs: sel [n_q][top_k] (-1 padded), n_sel [n_q], O [n_q][h_q][dv], lse [n_q][h_q],
+ *   and, when score != NULL, score [n_q][score_stride] (entries b >= B_i untouched).
+ * top_k <= 0 runs dense attention (sel / n_sel / score are then not written).            */
+struct run_args {
+    const float *X, *q_idx, *w, *Q, *K, *V;
+    const int32_t *q_seq, *q_pos;
+    int n_q, n_tok, h_idx, d_idx, cr, top_k, h_q, h_kv, dkq, dv;
+    double scale;
+    int32_t *sel, *n_sel;
+    double *score;
+    int64_t score_stride;
+    double *O, *lse;
+    int next;
+    pthread_mutex_t lock;
+};
+
+static void run_one_query(struct run_args *a, int i)
+{
+    const int64_t s = a->q_seq[i], p = a->q_pos[i], n_vis = p + 1;
+    const int dense = a->top_k <= 0;
+    uint8_t *mask = malloc((size_t)n_vis);
+    const float *Ks = a->K + s * (int64_t)a->n_tok * a->h_kv * a->dkq;
+    const float *Vs = a->V ? a->V + s * (int64_t)a->n_tok * a->h_kv * a->dv : NULL;
+    if (dense) {
+        sfa_oracle_mask(p, a->cr, NULL, 0, 1, mask);
+    } else {
+        const int64_t n_blk = n_vis / a->cr;
+        double *kbar = malloc(sizeof(double) * (size_t)(n_blk > 0 ? n_blk : 1) * a->d_idx);
+        double *score = malloc(sizeof(double) * (size_t)(n_blk > 0 ? n_blk : 1));
+        sfa_oracle_pool(a->X + s * (int64_t)a->n_tok * a->d_idx, n_blk, a->d_idx, a->cr, kbar);
+        sfa_oracle_index_scores(a->q_idx + (int64_t)i * a->h_idx * a->d_idx,
+                                a->w + (int64_t)i * a->h_idx, a->h_idx, a->d_idx, kbar, n_blk,
+                                score);
+        int32_t *sel = a->sel + (int64_t)i * a->top_k;
+        a->n_sel[i] = sfa_oracle_select(score, n_blk, a->top_k, sel);
+        if (a->score)
+            for (int64_t b = 0; b < n_blk; ++b) a->score[i * a->score_stride + b] = score[b];
+        sfa_oracle_mask(p, a->cr, sel, a->n_sel[i], 0, mask);
+        free(kbar);
+        free(score);
+    }
+    sfa_oracle_attend(a->Q + (int64_t)i * a->h_q * a->dkq, a->h_q, a->h_kv, a->dkq, a->dv,
+                      a->scale, Ks, (int64_t)a->h_kv * a->dkq, Vs, (int64_t)a->h_kv * a->dv,
+                      NULL, mask, n_vis, a->O + (int64_t)i * a->h_q * a->dv,
+                      a->lse + (int64_t)i * a->h_q);
+    free(mask);
+}
+
+static void *run_worker(void *p)
+{
+    struct run_args *a = p;
+    for (;;) {
+        pthread_mutex_lock(&a->lock);
+        const int i = a->next++;
+        pthread_mutex_unlock(&a->lock);
+        if (i >= a->n_q) return NULL;
+        run_one_query(a, i);
+    }
+}
+
+void sfa_oracle_run(const float *X, const float *q_idx, const float *w, const float *Q,
+                    const float *K, const float *V, const int32_t *q_seq, const int32_t *q_pos,
+                    int n_q, int n_tok, int h_idx, int d_idx, int cr, int top_k, int h_q,
+                    int h_kv, int dkq, int dv, double scale, int32_t *sel, int32_t *n_sel,
+                    double *score, int64_t score_stride, double *O, double *lse, int n_threads)
+{
+    struct run_args a = {X, q_idx, w, Q, K, V, q_seq, q_pos, n_q, n_tok, h_idx, d_idx, cr,
+                         top_k, h_q, h_kv, dkq, dv, scale, sel, n_sel, score, score_stride,
+                         O, lse, 0, PTHREAD_MUTEX_INITIALIZER};
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > n_q) n_threads = n_q > 0 ? n_q : 1;
+    pthread_t *tid = malloc(sizeof(pthread_t) * (size_t)n_threads);
+    for (int t = 0; t < n_threads; ++t) pthread_create(&tid[t], NULL, run_worker, &a);
+    for (int t = 0; t < n_threads; ++t) pthread_join(tid[t], NULL);
+    free(tid);
+}
