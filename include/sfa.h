@@ -1,0 +1,181 @@
+/*
+ * sfa.h -- C ABI of libsfa: indexer-selected block-sparse attention on one GB300 (sm_103a).
+ *
+ * The method (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", the QSA indexer
+ * paragraphs; llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM"): for each query
+ * token i of sequence s_i at position p_i, an indexer scores one mean-pooled key per block of
+ * compress_ratio (cr) cached tokens, as the weighted sum over index heads of the rectified dot
+ * product; the best indexer_top_k blocks plus the tail of tokens that do not form a complete
+ * block are kept; softmax attention then runs over those cells only.
+ *
+ *   B_i    = floor((p_i + 1) / cr)                complete blocks visible to query i
+ *   tail_i = [B_i*cr, p_i]                        always attended
+ *   kbar_b = (1/cr) sum_{t in block b} X[s_i][t]  raw index keys, pooled   (sfa_pool_index_keys)
+ *   s_ib   = sum_j w_ij * max(0, qidx_ij . kbar_b),  b < B_i                (sfa_index_scores)
+ *   Sel_i  = all b < B_i if B_i <= top_k, else the top_k best by (score desc, block asc)
+ *                                                                           (sfa_topk_blocks)
+ *   O_ih   = softmax_t(scale * Q_ih . K[s_i][t][g]) V[s_i][t][g] over t in Sel_i-blocks + tail,
+ *            g = h / (h_q / h_kv)                                           (sfa_gather_attend)
+ *   below the budget (every B_i <= top_k) this is dense causal attention    (sfa_dense_attend)
+ *
+ * Conventions shared by every entry point:
+ *  - Returns an sfa status (SFA_OK = 0).  Never aborts, never synchronises the stream, never
+ *    allocates device memory.  Invalid arguments are rejected on the host before anything is
+ *    enqueued.  A CUDA launch error returns SFA_ERR_CUDA.
+ *  - All data pointers are caller-owned DEVICE pointers; work is enqueued on `stream` (a
+ *    cudaStream_t; NULL is the legacy default stream).  The library keeps no state between
+ *    calls except a per-device cache of the SM count and of the driver's tensor-map encoder.
+ *  - Strides are in elements of the buffer's own type.  Buffers must be 16-byte aligned.
+ *  - `dev_status` (nullable) is a device int32 the kernels OR bits into (SFA_DEV_*) when they
+ *    meet data they cannot use (a block id outside [0, B_i), a non-ascending list, n_sel out
+ *    of range, a query outside the caches, a bounded wait that ran out).  The offending entry
+ *    is skipped; nothing traps.  The caller clears it and reads it when it wishes
+ *    (sfa_read_device_status).
+ */
+#ifndef SFA_H
+#define SFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *sfa_stream_t; /* identical to cudaStream_t */
+
+enum sfa_status {
+    SFA_OK = 0,
+    SFA_ERR_INVALID_ARG = 1, /* a pointer, size, stride or alignment the call cannot accept */
+    SFA_ERR_UNSUPPORTED = 2, /* a valid shape this build has no kernel for                */
+    SFA_ERR_CUDA = 3,        /* the CUDA runtime reported an error while enqueuing         */
+    SFA_ERR_WORKSPACE = 4    /* the workspace is NULL or smaller than the size query says  */
+};
+
+enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
+
+/* bits of the device status word */
+#define SFA_DEV_BAD_BLOCK 0x1 /* a selected block id outside [0, B_i) or not ascending      */
+#define SFA_DEV_BAD_NSEL 0x2  /* n_sel[i] < 0 or > top_k (clamped)                         */
+#define SFA_DEV_BAD_QUERY 0x4 /* q_seq/q_pos outside the caches, or a query group that
+                                 spans sequences (that query is skipped)                  */
+#define SFA_DEV_TIMEOUT 0x8   /* a bounded wait inside a kernel ran out; the kernel
+                                 released its resources and returned early                */
+
+/*
+ * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, over
+ * the RAW index keys ("pooling happens before the norm and the rotation": QSA commit, indexer
+ * key cache paragraph; "one mean-pooled key per block of compress_ratio tokens": QSA budget
+ * paragraph).  Blocks are cut on positions: block b holds tokens [b*cr, b*cr + cr).
+ *
+ *   X      [n_seq][x_seq_stride / d_idx][d_idx], x_dtype SFA_BF16 or SFA_F32 (raw keys)
+ *   Kbar   [n_seq][kbar_seq_stride / (2*d_idx)][2*d_idx] bf16 (uint16 storage): row b of
+ *          sequence s holds the pooled key split in two bf16 halves,
+ *            m      = fl32(sum_t X[s][t]) / cr   (fp32 sum in token order, IEEE division)
+ *            hi     = bf16_rn(m),  lo = bf16_rn(m - hi)
+ *            row b  = (hi[0..d_idx), lo[0..d_idx))
+ *          so that hi + lo carries m to about 2^-17 relative while the tensor cores read it
+ *          as plain bf16.
+ * Writes rows [blk_begin, blk_end) of every sequence; reads tokens [blk_begin*cr, blk_end*cr).
+ * Limits: 1 <= cr <= 64, d_idx in {32, 64, 96, 128}, 0 <= blk_begin <= blk_end.
+ */
+int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq, int d_idx,
+                        int compress_ratio, int64_t blk_begin, int64_t blk_end, void *Kbar,
+                        int64_t kbar_seq_stride, sfa_stream_t stream);
+
+/*
+ * sfa_index_scores -- the indexer score of every complete block visible to each query
+ * ("rectifies each head's dot product before summing over heads": QSA commit, index
+ * comparison paragraph; scoring is batched over streams so that stream s's queries meet
+ * only stream s's blocks: QSA commit, multi-stream scoring).
+ *
+ *   q_idx   [n_q][h_idx][d_idx] bf16 index queries;   w [n_q][h_idx] fp32 head weights
+ *   q_seq, q_pos [n_q] int32: sequence and position of each query
+ *   Kbar    pooled keys as written by sfa_pool_index_keys (rows >= B_i are not read for i)
+ *   scores  [n_q][score_stride] fp32: scores[i][b] = s_ib for b < min(B_i, n_blk_max);
+ *           entries at b >= B_i are left untouched.
+ *   q_group: the caller's promise that queries [k*q_group, (k+1)*q_group) share one sequence
+ *           (1 for decode batches of independent sequences; n_q for one prefill ubatch).
+ *           Tiles of queries that share a sequence share every pooled-key load.  A query that
+ *           breaks the promise is skipped and SFA_DEV_BAD_QUERY is set.
+ *   n_blk_max: host bound on max_i B_i (<= blk_cap = kbar_seq_stride / (2*d_idx), and
+ *           <= score_stride).
+ * The q.kbar contraction runs on tcgen05 tensor cores (bf16 x (hi, lo) into an fp32 TMEM
+ * accumulator); the ReLU, weights and head sum run in the TMEM read-back.
+ * Limits: d_idx in {64, 128}; h_idx in [1, 32]; h_idx * 16 <= 256.
+ */
+int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
+                     const int32_t *q_pos, int n_q, int q_group, int h_idx, int d_idx,
+                     int compress_ratio, const void *Kbar, int64_t kbar_seq_stride, int n_seq,
+                     int64_t n_blk_max, float *scores, int64_t score_stride,
+                     int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_topk_blocks -- the budget rule ("keeps a budget of the best blocks, plus the tail ...
+ * Below indexer_top_k + compress_ratio - 1 cached tokens every block fits in the budget":
+ * QSA commit, budget paragraph; the cut lands on a block boundary: QSA commit, expansion
+ * paragraph).  Ties at the cut go to the lower block index (the pages do not order equal
+ * scores; this is the stated reading).  -0.0 counts as +0.0; a NaN score ranks lowest.
+ *
+ *   scores  as written by sfa_index_scores; row i is read at [0, B_i)
+ *   blk_idx [n_q][top_k] int32: the kept block ids of query i, ascending, padded with -1
+ *           (the padding convention of PR #27970's sparse index rows)
+ *   n_sel   [n_q] int32: min(top_k, B_i)
+ *   workspace: sfa_topk_workspace_bytes(n_q, n_blk_max, top_k) bytes of device memory.
+ * The tail is not listed: it is implied by q_pos and cr and always attended.
+ * Limits: 1 <= top_k <= 2048; n_blk_max <= 2^21.
+ */
+size_t sfa_topk_workspace_bytes(int n_q, int64_t n_blk_max, int top_k);
+int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_pos, int n_q,
+                    int compress_ratio, int top_k, int64_t n_blk_max, int32_t *blk_idx,
+                    int32_t *n_sel, void *workspace, size_t workspace_bytes,
+                    int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_gather_attend -- softmax attention of each query over the cells of its kept blocks plus
+ * its tail (PR #27970: flash attention whose K/V tile loads are gathered through a per-query
+ * index list; V may be a view of the first DV dims of K; no ALiBi, no softcap).
+ *
+ *   Q    [n_q][h_q][dkq]                       dtype (SFA_BF16 or SFA_F32)
+ *   K    [n_seq][n_tok_cap][h_kv][dkq]         dtype
+ *   V    [n_seq][n_tok_cap][h_kv][dv] dtype, or NULL: V = K[..., :dv] (MLA layout)
+ *   blk_idx, n_sel: as written by sfa_topk_blocks (any ascending subset of [0, B_i) works)
+ *   O    [n_q][h_q][dv] fp32;  lse [n_q][h_q] fp32 natural-log sum of exp(logits), nullable
+ *   workspace: sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, top_k*cr + cr - 1) bytes
+ *           (split-KV partial results; may be NULL when that size is 0).
+ * Query head h reads KV head h / (h_q / h_kv).  p_i < n_tok_cap is required.
+ * Limits (bf16): dkq in {64, 128, 512, 576}, dv in {64, 128, 512}, dv <= dkq, h_q/h_kv <= 16.
+ *        (fp32): dkq, dv <= 576 and multiples of 4, h_q/h_kv <= 16.
+ */
+size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max);
+int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
+                      int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv,
+                      float scale, const int32_t *q_seq, const int32_t *q_pos,
+                      const int32_t *blk_idx, const int32_t *n_sel, int top_k,
+                      int compress_ratio, float *O, float *lse, void *workspace,
+                      size_t workspace_bytes, int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_dense_attend -- causal attention of each query over all of its sequence's tokens
+ * 0..p_i: the below-budget case, where the sparse result is exactly dense (QSA commit, budget
+ * paragraph; "a layer with no ratio falls back to dense").  n_kv_max must bound p_i + 1 for
+ * every query (the role of PR #27970's n_kv_max hint); it sizes the split-KV work.
+ * Arguments otherwise as sfa_gather_attend.
+ */
+int sfa_dense_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
+                     int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv,
+                     float scale, const int32_t *q_seq, const int32_t *q_pos, int64_t n_kv_max,
+                     float *O, float *lse, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, sfa_stream_t stream);
+
+/* Copies *dev_status to *host_out after the work already enqueued on `stream` (this call
+ * synchronises the stream). */
+int sfa_read_device_status(const int32_t *dev_status, int32_t *host_out, sfa_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+const char *sfa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SFA_H */

@@ -1,0 +1,16 @@
+"""indexer_selected_sparse_block_gb300: indexer-selected block-sparse attention on GB300.
+
+The product is libsfa.so (C ABI in include/sfa.h, CUDA kernels for sm_103a in csrc/); this
+package is its Python binding (argument marshalling only), the step runner that chains the
+entry points, and the seeded synthetic input generators.
+"""
+from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY,
+                       SFA_DEV_TIMEOUT, SFA_ERR_CUDA, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED,
+                       SFA_ERR_WORKSPACE, SFA_F32, SFA_OK, SfaError, kbar_shape, lib,
+                       sfa_attend_workspace_bytes, sfa_dense_attend, sfa_gather_attend,
+                       sfa_index_scores, sfa_pool_index_keys, sfa_read_device_status,
+                       sfa_topk_blocks, sfa_topk_workspace_bytes)
+from .inputs import WORKLOADS, Workload, make_case
+from .pipeline import SfaStep
+
+__all__ = [n for n in dir() if not n.startswith("_")]

@@ -1,0 +1,192 @@
+"""ctypes binding of libsfa (the C ABI in include/sfa.h).
+
+Argument marshalling only: every step of the method runs in libsfa's CUDA kernels.  Tensors
+are torch CUDA tensors (torch provides device memory and streams); each function passes
+their raw pointers, sizes and the current stream to the C entry point of the same name and
+raises ``SfaError`` on a non-zero status.  There is no CPU fallback: if libsfa.so is not
+built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsfa.so")
+
+SFA_OK, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA, SFA_ERR_WORKSPACE = range(5)
+SFA_BF16, SFA_F32 = 0, 1
+SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT = 1, 2, 4, 8
+
+_lib = None
+_vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                              ctypes.c_size_t)
+
+# name -> (restype, argtypes); mirrors include/sfa.h
+SIGNATURES = {
+    "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp]),
+    "sfa_index_scores": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _i64,
+                                _int, _i64, _vp, _i64, _vp, _vp]),
+    "sfa_topk_workspace_bytes": (_sz, [_int, _i64, _int]),
+    "sfa_topk_blocks": (_int, [_vp, _i64, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp,
+                               _vp]),
+    "sfa_attend_workspace_bytes": (_sz, [_int, _int, _int, _int, _i64]),
+    "sfa_gather_attend": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int, _int, _int,
+                                 _f32, _vp, _vp, _vp, _vp, _int, _int, _vp, _vp, _vp, _sz, _vp,
+                                 _vp]),
+    "sfa_dense_attend": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int, _int, _int,
+                                _f32, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
+    "sfa_status_string": (ctypes.c_char_p, [_int]),
+}
+
+
+class SfaError(RuntimeError):
+    """A non-zero status returned by libsfa."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib().sfa_status_string(status).decode()}")
+
+
+def lib(path: str | None = None):
+    """Loads libsfa.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libsfa.so is not built ({p}); run __graft_entry__.build() first")
+    L = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    if path is None:
+        _lib = L
+    return L
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libsfa takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libsfa takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != SFA_OK:
+        raise SfaError(fn, rc)
+
+
+def _dtype_code(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return SFA_BF16
+    if t.dtype == torch.float32:
+        return SFA_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def kbar_shape(n_seq: int, blk_cap: int, d_idx: int):
+    """Shape of the pooled-key table: [n_seq][blk_cap][2*d_idx] bf16 (hi, lo halves)."""
+    return (n_seq, blk_cap, 2 * d_idx)
+
+
+def sfa_pool_index_keys(X, compress_ratio: int, blk_begin: int, blk_end: int, Kbar, stream=None):
+    """X [n_seq][n_tok_cap][d_idx] (bf16/f32) -> rows [blk_begin, blk_end) of Kbar."""
+    n_seq, _, d_idx = X.shape
+    rc = lib().sfa_pool_index_keys(_p(X), _dtype_code(X), X.stride(0), n_seq, d_idx,
+                                   compress_ratio, blk_begin, blk_end, _p(Kbar), Kbar.stride(0),
+                                   _stream(stream))
+    _check("sfa_pool_index_keys", rc)
+
+
+def sfa_index_scores(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_max: int, scores,
+                     q_group: int = 1, dev_status=None, stream=None):
+    """scores[i][b] = sum_j w[i][j] * relu(q_idx[i][j] . kbar_b) for b < B_i."""
+    n_q, h_idx, d_idx = q_idx.shape
+    rc = lib().sfa_index_scores(_p(q_idx), _p(w), _p(q_seq), _p(q_pos), n_q, q_group, h_idx,
+                                d_idx, compress_ratio, _p(Kbar), Kbar.stride(0), Kbar.shape[0],
+                                n_blk_max, _p(scores), scores.stride(0), _p(dev_status),
+                                _stream(stream))
+    _check("sfa_index_scores", rc)
+
+
+def sfa_topk_workspace_bytes(n_q: int, n_blk_max: int, top_k: int) -> int:
+    return int(lib().sfa_topk_workspace_bytes(n_q, n_blk_max, top_k))
+
+
+def sfa_topk_blocks(scores, q_pos, compress_ratio: int, top_k: int, n_blk_max: int, blk_idx,
+                    n_sel, workspace=None, dev_status=None, stream=None):
+    """The top_k best blocks of each query (ascending, -1 padded) and their count."""
+    n_q = q_pos.shape[0]
+    need = sfa_topk_workspace_bytes(n_q, n_blk_max, top_k)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_pos.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_topk_blocks(_p(scores), scores.stride(0), _p(q_pos), n_q, compress_ratio,
+                               top_k, n_blk_max, _p(blk_idx), _p(n_sel), _p(workspace),
+                               ws_bytes, _p(dev_status), _stream(stream))
+    _check("sfa_topk_blocks", rc)
+
+
+def sfa_attend_workspace_bytes(n_q: int, h_q: int, h_kv: int, dv: int, n_kv_max: int) -> int:
+    return int(lib().sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max))
+
+
+def _attn_dims(Q, K, V, O):
+    n_q, h_q, dkq = Q.shape
+    n_seq, n_tok_cap, h_kv, _ = K.shape
+    dv = O.shape[-1]
+    if V is not None and K.dtype != V.dtype:
+        raise ValueError("K and V must share a dtype")
+    if Q.dtype != K.dtype:
+        raise ValueError("Q and K must share a dtype")
+    return n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv
+
+
+def sfa_gather_attend(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int, compress_ratio: int,
+                      scale: float, O, lse=None, workspace=None, dev_status=None, stream=None):
+    """Attention of each query over its kept blocks plus its tail."""
+    n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv = _attn_dims(Q, K, V, O)
+    n_kv_max = top_k * compress_ratio + compress_ratio - 1
+    need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_gather_attend(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap, n_q, h_q,
+                                 h_kv, dkq, dv, float(scale), _p(q_seq), _p(q_pos), _p(blk_idx),
+                                 _p(n_sel), top_k, compress_ratio, _p(O), _p(lse), _p(workspace),
+                                 ws_bytes, _p(dev_status), _stream(stream))
+    _check("sfa_gather_attend", rc)
+
+
+def sfa_dense_attend(Q, K, V, q_seq, q_pos, n_kv_max: int, scale: float, O, lse=None,
+                     workspace=None, dev_status=None, stream=None):
+    """Causal attention of each query over all of its sequence's tokens 0..p_i."""
+    n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv = _attn_dims(Q, K, V, O)
+    need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_dense_attend(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap, n_q, h_q,
+                                h_kv, dkq, dv, float(scale), _p(q_seq), _p(q_pos), n_kv_max,
+                                _p(O), _p(lse), _p(workspace), ws_bytes, _p(dev_status),
+                                _stream(stream))
+    _check("sfa_dense_attend", rc)
+
+
+def sfa_read_device_status(dev_status, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    rc = lib().sfa_read_device_status(_p(dev_status), ctypes.byref(out), _stream(stream))
+    _check("sfa_read_device_status", rc)
+    return int(out.value)

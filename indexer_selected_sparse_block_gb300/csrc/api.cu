@@ -1,0 +1,44 @@
+// api.cu -- status strings, the device status read-back, and the per-device SM count cache.
+#include <mutex>
+
+#include "sfa_common.cuh"
+
+namespace sfa {
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace sfa
+
+extern "C" const char *sfa_status_string(int status) {
+    switch (status) {
+        case SFA_OK: return "SFA_OK";
+        case SFA_ERR_INVALID_ARG: return "SFA_ERR_INVALID_ARG: an argument the call cannot accept";
+        case SFA_ERR_UNSUPPORTED: return "SFA_ERR_UNSUPPORTED: a shape this build has no kernel for";
+        case SFA_ERR_CUDA: return "SFA_ERR_CUDA: the CUDA runtime reported an error";
+        case SFA_ERR_WORKSPACE: return "SFA_ERR_WORKSPACE: workspace missing or too small";
+        default: return "unknown sfa status";
+    }
+}
+
+extern "C" int sfa_read_device_status(const int32_t *dev_status, int32_t *host_out,
+                                      sfa_stream_t stream) {
+    if (!dev_status || !host_out) return SFA_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        (cudaStream_t)stream) != cudaSuccess)
+        return SFA_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SFA_ERR_CUDA;
+    return SFA_OK;
+}

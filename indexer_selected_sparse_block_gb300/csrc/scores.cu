@@ -1,0 +1,363 @@
+// scores.cu -- the indexer score of every visible block (sfa_index_scores).
+//
+//   s_ib = sum_j w_ij * max(0, qidx_ij . kbar_b)
+// ("The reference rectifies each head's dot product before summing over heads"; scoring is
+// batched over streams so that stream s's queries only meet stream s's blocks: llama.cpp
+// commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs.)
+//
+// Design (sm_103a): the q.kbar contraction is a GEMM D[blocks x (queries*heads)] on the
+// tcgen05 tensor cores with the fp32 accumulator in tensor memory.  The pooled key is stored
+// as two bf16 halves (hi, lo) per row, so one bf16 MMA chain over K' = 2*d_idx against the
+// duplicated query [q | q] yields q.(hi + lo) in fp32: selection-grade accuracy at bf16
+// tensor-core rates.  The ReLU, the head weights and the head sum are applied while the
+// accumulator is read back from tensor memory, so only the final score is written.
+//
+// One CTA = one tile of q_tile queries of one sequence x a run of 128-block tiles.
+//   warp 0      TMA producer: 128 rows x 128 B slabs of Kbar, 128-byte swizzle, S stages
+//   warp 1      tensor-memory owner and single-thread MMA issuer (M = 128, N = q_tile*H pad 16)
+//   warps 2..5  epilogue: tcgen05.ld (lane = block), ReLU . w, head sum, coalesced stores
+// Two accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs of
+// tile t + 1.  Every wait is bounded (SFA_DEV_TIMEOUT) and tensor memory is always released.
+#include <mutex>
+
+#include "sfa_common.cuh"
+
+namespace sfa {
+namespace {
+
+constexpr int kBM = 128;               // blocks per tile (MMA M)
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kSmemBudget = 200 * 1024;
+
+struct ScoreParams {
+    const __nv_bfloat16 *q_idx;
+    const float *w;
+    const int32_t *q_seq;
+    const int32_t *q_pos;
+    float *scores;
+    int32_t *status;
+    int64_t score_stride;
+    int64_t blk_cap;
+    int64_t n_blk_max;
+    int n_q, q_tile, n_seq, cr, N, stages, tiles_per_cta, tmem_cols;
+};
+
+template <int KP>
+struct Layout {
+    static constexpr int kSlabs = KP / 64;
+    static constexpr int kABytes = kBM * KP * 2;
+};
+
+template <int KP, int H>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_score_kernel(const __grid_constant__ CUtensorMap kbar_map, const ScoreParams p) {
+    using L = Layout<KP>;
+    constexpr int D = KP / 2;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const int S = p.stages, N = p.N;
+    uint8_t *sA = smem;                                    // S x kABytes
+    uint8_t *sB = sA + (size_t)S * L::kABytes;             // N x KP bf16, swizzled
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KP * 2);
+    uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S,
+             *acc_empty = bars + 2 * S + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *s_nblk = reinterpret_cast<int *>(tmem_slot + 2);  // [q_tile] visible blocks, -1 skip
+    float *s_w = reinterpret_cast<float *>(s_nblk + 256);  // [q_tile * H]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q0 = blockIdx.y * p.q_tile;
+    const int nq_tile = min(p.q_tile, p.n_q - q0);
+    const int seq0 = p.q_seq[q0];
+    const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+
+    // ---------------------------------------------------------------- set-up (all warps)
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) prefetch_tensormap(&kbar_map);
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    for (int qq = threadIdx.x; qq < p.q_tile; qq += kThreads) {
+        int nb = -1;
+        if (qq < nq_tile) {
+            const int qi = q0 + qq;
+            const int s = p.q_seq[qi], pos = p.q_pos[qi];
+            if (s != seq0 || s < 0 || s >= p.n_seq || pos < 0) {
+                set_status(p.status, SFA_DEV_BAD_QUERY);
+            } else {
+                const int64_t b = min((int64_t)(pos + 1) / p.cr, p.n_blk_max);
+                nb = (int)min(b, p.blk_cap);
+            }
+        }
+        s_nblk[qq] = nb;
+    }
+    for (int e = threadIdx.x; e < p.q_tile * H; e += kThreads) {
+        const int qq = e / H;
+        s_w[e] = qq < nq_tile ? p.w[(int64_t)(q0 + qq) * H + (e % H)] : 0.f;
+    }
+    // B operand: row n = (query qq, head j), K' = [q | q]; 16-byte chunks, 128-byte swizzle.
+    for (int e = threadIdx.x; e < N * (KP / 8); e += kThreads) {
+        const int n = e / (KP / 8), c = e % (KP / 8);
+        const int qq = n / H, j = n % H;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (qq < nq_tile && n < p.q_tile * H) {
+            const int src_c = c % (D / 8);
+            v = *reinterpret_cast<const uint4 *>(p.q_idx + ((int64_t)(q0 + qq) * H + j) * D +
+                                                 src_c * 8);
+        }
+        const int slab = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4 *>(sB + (size_t)slab * N * 128 + n * 128 + ((cc ^ (n & 7)) << 4)) =
+            v;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int max_nb = 0;
+    for (int qq = 0; qq < nq_tile; ++qq) max_nb = max(max_nb, s_nblk[qq]);
+    const int n_tiles_q = (max_nb + kBM - 1) / kBM;
+    const int t_begin = blockIdx.x * p.tiles_per_cta;
+    const int my_tiles = max(0, min(p.tiles_per_cta, n_tiles_q - t_begin));
+    const int64_t row0 = (int64_t)seq0 * p.blk_cap;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && my_tiles > 0) {
+            int issued = 0;
+            for (int it = 0; it < my_tiles && !*abort_flag; ++it) {
+                const int st = it % S;
+                if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, deadline)) {
+                    set_status(p.status, SFA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[st], L::kABytes);
+                const int32_t y = (int32_t)(row0 + (int64_t)(t_begin + it) * kBM);
+                uint8_t *dst = sA + (size_t)st * L::kABytes;
+#pragma unroll
+                for (int sl = 0; sl < L::kSlabs; ++sl)
+                    tma_load_2d(dst + sl * (kBM * 128), &kbar_map, sl * 64, y, &full[st]);
+                ++issued;
+            }
+            // never leave a copy in flight: wait (bounded) for the last load of each stage
+            for (int it = max(0, issued - S); it < issued; ++it)
+                mbar_wait(&full[it % S], (it / S) & 1, deadline + kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && my_tiles > 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, N);
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            int issued = 0;
+            for (int it = 0; it < my_tiles && !*abort_flag; ++it) {
+                const int st = it % S, acc = it & 1;
+                if (!mbar_wait(&full[st], (it / S) & 1, deadline) ||
+                    !mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, deadline)) {
+                    set_status(p.status, SFA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * N);
+                const uint32_t a_st = a0 + st * L::kABytes;
+#pragma unroll
+                for (int kk = 0; kk < KP / 16; ++kk) {
+                    const uint64_t ad = sw128_kmajor_desc(a_st + (kk >> 2) * (kBM * 128) + (kk & 3) * 32);
+                    const uint64_t bd = sw128_kmajor_desc(b0 + (kk >> 2) * (N * 128) + (kk & 3) * 32);
+                    tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&empty[st]);
+                tc_commit(&acc_full[acc]);
+                ++issued;
+            }
+            if (issued > 0) {  // tensor memory may only be released once the MMAs are done
+                const int last = issued - 1;
+                mbar_wait(&acc_full[last & 1], (last >> 1) & 1, deadline + kWaitLimitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (4 warps)
+        const int quarter = warp & 3;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const int ncols = nq_tile * H;
+        for (int it = 0; it < my_tiles; ++it) {
+            const int acc = it & 1;
+            if (*abort_flag) break;
+            if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, deadline)) {
+                set_status(p.status, SFA_DEV_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
+            for (int c0 = 0; c0 < ncols; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tmem_base + lane_addr + (uint32_t)(acc * N + c0), r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 16 / H; ++g) {
+                    const int qq = (c0 / H) + g;
+                    if (qq >= nq_tile) break;
+                    float s = 0.f;
+#pragma unroll
+                    for (int j = 0; j < H; ++j)
+                        s = fmaf(s_w[qq * H + j], fmaxf(__uint_as_float(r[g * H + j]), 0.f), s);
+                    if (b < s_nblk[qq]) p.scores[(int64_t)(q0 + qq) * p.score_stride + b] = s;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+int pow2_at_least(int v) {
+    int r = 32;
+    while (r < v) r <<= 1;
+    return r;
+}
+
+template <int KP, int H>
+int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
+           cudaStream_t stream) {
+    using L = Layout<KP>;
+    const size_t b_bytes = (size_t)p.N * KP * 2;
+    int stages = (int)((kSmemBudget - b_bytes) / L::kABytes);
+    stages = stages > 4 ? 4 : stages;
+    if (stages < 1) return SFA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    const size_t smem = 1024 + (size_t)stages * L::kABytes + b_bytes + 8 * (2 * stages + 4) + 16 +
+                        256 * 4 + (size_t)p.q_tile * H * 4;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(index_score_kernel<KP, H>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024) != cudaSuccess)
+            return SFA_ERR_CUDA;
+        attr_set = true;
+    }
+    // Spread the block tiles of each query tile over enough CTAs to fill the GPU.
+    const int sms = device_sm_count();
+    int cta_per_qtile = (2 * sms + n_qtiles - 1) / n_qtiles;
+    if (cta_per_qtile > n_blk_tiles) cta_per_qtile = n_blk_tiles;
+    if (cta_per_qtile < 1) cta_per_qtile = 1;
+    p.tiles_per_cta = (n_blk_tiles + cta_per_qtile - 1) / cta_per_qtile;
+    const int grid_x = (n_blk_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    index_score_kernel<KP, H><<<dim3(grid_x, n_qtiles), kThreads, smem, stream>>>(map, p);
+    SFA_CHECK_LAUNCH();
+    return SFA_OK;
+}
+
+}  // namespace
+}  // namespace sfa
+
+extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
+                                const int32_t *q_pos, int n_q, int q_group, int h_idx,
+                                int d_idx, int compress_ratio, const void *Kbar,
+                                int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max,
+                                float *scores, int64_t score_stride, int32_t *dev_status,
+                                sfa_stream_t stream) {
+    using namespace sfa;
+    if (!q_idx || !w || !q_seq || !q_pos || !Kbar || !scores) return SFA_ERR_INVALID_ARG;
+    if (n_q < 0 || q_group < 1 || n_seq < 1 || compress_ratio < 1 || n_blk_max < 0)
+        return SFA_ERR_INVALID_ARG;
+    if (d_idx != 64 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
+    if (h_idx != 4 && h_idx != 8 && h_idx != 16) return SFA_ERR_UNSUPPORTED;
+    const int KP = 2 * d_idx;
+    if (kbar_seq_stride % KP != 0 || kbar_seq_stride <= 0) return SFA_ERR_INVALID_ARG;
+    const int64_t blk_cap = kbar_seq_stride / KP;
+    if (n_blk_max > blk_cap || n_blk_max > score_stride) return SFA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(Kbar) || !aligned16(scores)) return SFA_ERR_INVALID_ARG;
+    if (n_q == 0 || n_blk_max == 0) return SFA_OK;
+    if ((int64_t)n_seq * blk_cap > 0x7FFFFFFFll) return SFA_ERR_UNSUPPORTED;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return SFA_ERR_CUDA;
+
+    // Queries per tile: the largest power of two that divides q_group and fits N <= 256 (and
+    // the B tile fits next to the pooled-key stages).
+    const int n_cap = (KP == 256) ? 128 : 256;
+    int q_tile = 1;
+    while (q_tile * 2 * h_idx <= n_cap && q_group % (q_tile * 2) == 0) q_tile *= 2;
+    ScoreParams p{};
+    p.q_idx = reinterpret_cast<const __nv_bfloat16 *>(q_idx);
+    p.w = w;
+    p.q_seq = q_seq;
+    p.q_pos = q_pos;
+    p.scores = scores;
+    p.status = dev_status;
+    p.score_stride = score_stride;
+    p.blk_cap = blk_cap;
+    p.n_blk_max = n_blk_max;
+    p.n_q = n_q;
+    p.q_tile = q_tile;
+    p.n_seq = n_seq;
+    p.cr = compress_ratio;
+    p.N = ((q_tile * h_idx + 15) / 16) * 16;
+    p.tmem_cols = pow2_at_least(2 * p.N);
+
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)KP, (cuuint64_t)(n_seq * blk_cap)};
+    const cuuint64_t gstride[1] = {(cuuint64_t)KP * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(Kbar), gdim, gstride,
+            box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SFA_ERR_INVALID_ARG;
+
+    const int n_qtiles = (n_q + q_tile - 1) / q_tile;
+    if (n_qtiles > 65535) return SFA_ERR_UNSUPPORTED;
+    const int n_blk_tiles = (int)((n_blk_max + kBM - 1) / kBM);
+    const cudaStream_t st = (cudaStream_t)stream;
+    if (d_idx == 64 && h_idx == 4) return launch<128, 4>(map, p, n_qtiles, n_blk_tiles, st);
+    if (d_idx == 64 && h_idx == 8) return launch<128, 8>(map, p, n_qtiles, n_blk_tiles, st);
+    if (d_idx == 64 && h_idx == 16) return launch<128, 16>(map, p, n_qtiles, n_blk_tiles, st);
+    if (d_idx == 128 && h_idx == 4) return launch<256, 4>(map, p, n_qtiles, n_blk_tiles, st);
+    if (d_idx == 128 && h_idx == 8) return launch<256, 8>(map, p, n_qtiles, n_blk_tiles, st);
+    return launch<256, 16>(map, p, n_qtiles, n_blk_tiles, st);
+}

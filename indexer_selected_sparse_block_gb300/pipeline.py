@@ -1,0 +1,76 @@
+"""One step of indexer-selected block-sparse attention through the C ABI, with its buffers.
+
+``SfaStep`` owns the intermediate device buffers of the method (pooled keys, block scores,
+kept block lists, workspaces, outputs) and runs the stages as the C entry points:
+
+  sfa_pool_index_keys -> sfa_index_scores -> sfa_topk_blocks -> sfa_gather_attend
+
+or, when every query is below the budget (B_i <= indexer_top_k for all i), the exact dense
+case ``sfa_dense_attend`` ("Below indexer_top_k + compress_ratio - 1 cached tokens every
+block fits in the budget, so the result is exactly dense": llama.cpp commit "model: add
+Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+class SfaStep:
+    def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
+                 dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
+                 n_blk_max: int, q_group: int = 1, device="cuda"):
+        self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
+                             dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
+                             top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
+        dev = torch.device(device)
+        self.blk_cap = n_tok_cap // compress_ratio
+        assert n_blk_max <= self.blk_cap
+        self.Kbar = torch.zeros(B.kbar_shape(n_seq, self.blk_cap, d_idx), dtype=torch.bfloat16,
+                                device=dev)
+        self.dense = n_blk_max <= indexer_top_k
+        self.scores = torch.empty((n_q, max(n_blk_max, 1)), dtype=torch.float32, device=dev)
+        self.blk_idx = torch.empty((n_q, indexer_top_k), dtype=torch.int32, device=dev)
+        self.n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+        nt = B.sfa_topk_workspace_bytes(n_q, max(n_blk_max, 1), indexer_top_k)
+        self.topk_ws = torch.empty(max(nt, 16), dtype=torch.uint8, device=dev)
+        self.n_kv_dense = n_tok_cap
+        n_kv = (n_tok_cap if self.dense else
+                indexer_top_k * compress_ratio + compress_ratio - 1)
+        na = B.sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv)
+        self.attn_ws = torch.empty(max(na, 16), dtype=torch.uint8, device=dev)
+        self.O = torch.empty((n_q, h_q, dv), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((n_q, h_q), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def pool(self, X, blk_begin: int, blk_end: int, stream=None):
+        if blk_end > blk_begin:
+            B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, stream=stream)
+
+    def select(self, q_idx, w, q_seq, q_pos, stream=None):
+        B.sfa_index_scores(q_idx, w, q_seq, q_pos, self.Kbar, self.cr, self.n_blk_max,
+                           self.scores, q_group=self.q_group, dev_status=self.status,
+                           stream=stream)
+        B.sfa_topk_blocks(self.scores, q_pos, self.cr, self.top_k, self.n_blk_max, self.blk_idx,
+                          self.n_sel, workspace=self.topk_ws, dev_status=self.status,
+                          stream=stream)
+
+    def attend(self, Q, K, V, q_seq, q_pos, scale: float, stream=None):
+        if self.dense:
+            B.sfa_dense_attend(Q, K, V, q_seq, q_pos, self.n_kv_dense, scale, self.O,
+                               lse=self.lse, workspace=self.attn_ws, dev_status=self.status,
+                               stream=stream)
+        else:
+            B.sfa_gather_attend(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel, self.top_k,
+                                self.cr, scale, self.O, lse=self.lse, workspace=self.attn_ws,
+                                dev_status=self.status, stream=stream)
+
+    def run(self, X, K, V, Q, q_idx, w, q_seq, q_pos, scale: float, new_blocks=(0, 0),
+            stream=None):
+        """One step: pool the blocks completed by this step's tokens, score, select, attend."""
+        self.pool(X, new_blocks[0], new_blocks[1], stream=stream)
+        if not self.dense:
+            self.select(q_idx, w, q_seq, q_pos, stream=stream)
+        self.attend(Q, K, V, q_seq, q_pos, scale, stream=stream)
+        return self.O

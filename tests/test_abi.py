@@ -1,0 +1,104 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every entry point that
+include/sfa.h declares, and rejects invalid arguments before enqueuing anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from indexer_selected_sparse_block_gb300 import _binding
+    return _binding.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sfa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sfa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    from indexer_selected_sparse_block_gb300 import _binding
+    assert set(names) <= set(_binding.SIGNATURES)
+
+
+def test_status_strings(L):
+    for code in range(5):
+        assert L.sfa_status_string(code).startswith(b"SFA_")
+    assert b"unknown" in L.sfa_status_string(99)
+
+
+FAKE = ctypes.c_void_p(0x10000)     # never dereferenced: every call below is rejected first
+ODD = ctypes.c_void_p(0x10008)      # not 16-byte aligned
+
+
+def test_pool_rejects_bad_arguments(L):
+    f = L.sfa_pool_index_keys
+    assert f(None, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1
+    assert f(FAKE, 2, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1          # dtype
+    assert f(FAKE, 0, 1024, 1, 48, 4, 0, 4, FAKE, 1024, None) == 2          # d_idx
+    assert f(FAKE, 0, 1024, 1, 64, 0, 0, 4, FAKE, 1024, None) == 1          # cr
+    assert f(FAKE, 0, 1024, 1, 64, 4, 5, 4, FAKE, 1024, None) == 1          # begin > end
+    assert f(ODD, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1           # alignment
+    assert f(FAKE, 0, 100, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1           # X too short
+    assert f(FAKE, 0, 1024, 1, 64, 4, 0, 0, FAKE, 1024, None) == 0          # empty: no work
+
+
+def test_scores_reject_bad_arguments(L):
+    f = L.sfa_index_scores
+    ok = [FAKE, FAKE, FAKE, FAKE, 4, 1, 8, 128, 4, FAKE, 256 * 100, 1, 100, FAKE, 100, None, None]
+    bad = list(ok); bad[7] = 96
+    assert f(*bad) == 2                                                    # d_idx
+    bad = list(ok); bad[6] = 5
+    assert f(*bad) == 2                                                    # h_idx
+    bad = list(ok); bad[12] = 101
+    assert f(*bad) == 1                                                    # n_blk_max > cap
+    bad = list(ok); bad[5] = 0
+    assert f(*bad) == 1                                                    # q_group
+    bad = list(ok); bad[10] = 250
+    assert f(*bad) == 1                                                    # stride % 2*d_idx
+
+
+def test_topk_rejects_bad_arguments(L):
+    f = L.sfa_topk_blocks
+    assert f(FAKE, 100, FAKE, 4, 4, 0, 100, FAKE, FAKE, None, 0, None, None) == 2     # top_k 0
+    assert f(FAKE, 100, FAKE, 4, 4, 4096, 100, FAKE, FAKE, None, 0, None, None) == 2  # > 2048
+    assert f(FAKE, 50, FAKE, 4, 4, 16, 100, FAKE, FAKE, None, 0, None, None) == 1     # stride
+    assert f(FAKE, 100, FAKE, 4, 0, 16, 100, FAKE, FAKE, None, 0, None, None) == 1    # cr
+    need = L.sfa_topk_workspace_bytes(4, 100000, 512)
+    assert need > 0
+    assert f(FAKE, 100000, FAKE, 4, 4, 512, 100000, FAKE, FAKE, None, 0, None, None) == 4
+    assert L.sfa_topk_workspace_bytes(4, 1000, 512) == 0                  # one chunk: none
+
+
+def test_attend_rejects_bad_arguments(L):
+    f = L.sfa_gather_attend
+    base = [FAKE, FAKE, None, 0, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04), FAKE, FAKE,
+            FAKE, FAKE, 256, 4, FAKE, None, None, 0, None, None]
+    a = list(base); a[9], a[10] = 320, 256
+    assert f(*a) == 2                                                      # head dim
+    a = list(base); a[7], a[8] = 12, 5
+    assert f(*a) == 1                                                      # h_q % h_kv
+    a = list(base); a[7], a[8] = 32, 1
+    assert f(*a) == 2                                                      # 32 heads per KV head
+    a = list(base); a[11] = ctypes.c_float(float("nan"))
+    assert f(*a) == 1                                                      # scale
+    a = list(base); a[16] = 0
+    assert f(*a) == 1                                                      # top_k
+    a = list(base); a[0] = ODD
+    assert f(*a) == 1                                                      # alignment
+    a = list(base); a[10] = 576; a[9] = 512
+    assert f(*a) == 1                                                      # dv > dkq, V NULL
+    g = L.sfa_dense_attend
+    assert g(FAKE, FAKE, None, 0, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04), FAKE, FAKE,
+             0, FAKE, None, None, 0, None, None) == 1                      # n_kv_max 0

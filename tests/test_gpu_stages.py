@@ -1,0 +1,261 @@
+"""Stage-by-stage parity of the CUDA path (through the C ABI) against the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_BF16, TOL_F32, np32, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+sfa = pytest.importorskip("indexer_selected_sparse_block_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _randn_bf16(shape, gen, dev, scale=1.0):
+    return (torch.randn(shape, generator=gen, device="cpu") * scale).to(torch.bfloat16).to(dev)
+
+
+# -------------------------------------------------------------------------------- pooling
+@pytest.mark.parametrize("cr", [1, 3, 4, 8])
+@pytest.mark.parametrize("d_idx", [32, 64, 128])
+@pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float32])
+def test_pool_matches_oracle(dev, cr, d_idx, xdtype):
+    g = torch.Generator().manual_seed(cr * 1000 + d_idx)
+    n_seq, n_tok = 3, 1000 + cr
+    X = _randn_bf16((n_seq, n_tok, d_idx), g, dev).to(xdtype)
+    blk_cap = n_tok // cr + 5
+    Kbar = torch.full(sfa.kbar_shape(n_seq, blk_cap, d_idx), 7.0, dtype=torch.bfloat16, device=dev)
+    b0, b1 = 3, n_tok // cr
+    sfa.sfa_pool_index_keys(X, cr, b0, b1, Kbar)
+    torch.cuda.synchronize()
+    kb = np32(Kbar).astype(np.float64)
+    got = kb[..., :d_idx] + kb[..., d_idx:]
+    Xn = np32(X)
+    for s in range(n_seq):
+        ref = oracle.pool(Xn[s], b1, cr)
+        mag = np.abs(Xn[s, : b1 * cr].astype(np.float64)).reshape(b1, cr, d_idx).mean(1)
+        err = np.abs(got[s, b0:b1] - ref[b0:b1])
+        assert np.all(err <= 2.0 ** -16 * mag[b0:b1] + 1e-30), err.max()
+    assert np.all(kb[:, :b0] == 7.0) and np.all(kb[:, b1:] == 7.0)  # other rows untouched
+
+
+# ---------------------------------------------------------------------------------- scores
+def _oracle_scores(Xn, qi, w, q_seq, q_pos, cr):
+    out = []
+    for i in range(len(q_seq)):
+        B = (int(q_pos[i]) + 1) // cr
+        kb = oracle.pool(Xn[q_seq[i]], B, cr)
+        s = oracle.index_scores(qi[i], w[i], kb)
+        mag = np.abs(kb) @ np.abs(qi[i].astype(np.float64)).T @ np.abs(w[i].astype(np.float64))
+        out.append((s, mag))
+    return out
+
+
+@pytest.mark.parametrize("d_idx,h_idx", [(64, 4), (128, 8), (64, 16), (128, 4)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_scores_match_oracle(dev, d_idx, h_idx, mode):
+    g = torch.Generator().manual_seed(d_idx + h_idx)
+    cr = 4
+    if mode == "decode":
+        n_seq, n_tok, n_q, q_group = 5, 1500, 5, 1
+        q_seq = torch.arange(5, dtype=torch.int32)
+        q_pos = torch.tensor([1499, 700, 3, 1023, 511], dtype=torch.int32)
+    else:
+        n_seq, n_tok, n_q, q_group = 1, 2100, 70, 70
+        q_seq = torch.zeros(n_q, dtype=torch.int32)
+        q_pos = torch.arange(2100 - n_q, 2100, dtype=torch.int32)
+    X = _randn_bf16((n_seq, n_tok, d_idx), g, dev)
+    qi = _randn_bf16((n_q, h_idx, d_idx), g, dev)
+    w = torch.rand((n_q, h_idx), generator=g).to(dev)
+    blk_cap = n_tok // cr
+    Kbar = torch.zeros(sfa.kbar_shape(n_seq, blk_cap, d_idx), dtype=torch.bfloat16, device=dev)
+    sfa.sfa_pool_index_keys(X, cr, 0, blk_cap, Kbar)
+    n_blk_max = int((q_pos.max() + 1) // cr)
+    scores = torch.full((n_q, n_blk_max + 3), float("nan"), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores(qi, w, q_seq.to(dev), q_pos.to(dev), Kbar, cr, n_blk_max, scores,
+                         q_group=q_group, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    got = np32(scores)
+    ref = _oracle_scores(np32(X), np32(qi), np32(w), q_seq.numpy(), q_pos.numpy(), cr)
+    for i, (s, mag) in enumerate(ref):
+        B = s.shape[0]
+        err = np.abs(got[i, :B] - s)
+        assert np.all(err <= 1e-5 * mag + 1e-30), (i, err.max(), mag.max())
+        assert np.all(np.isnan(got[i, B:])), i   # entries at b >= B_i untouched
+
+
+def test_scores_flag_query_group_violation(dev):
+    """A query that breaks the q_group promise is skipped and flagged, never misread."""
+    g = torch.Generator().manual_seed(5)
+    X = _randn_bf16((2, 600, 64), g, dev)
+    Kbar = torch.zeros(sfa.kbar_shape(2, 150, 64), dtype=torch.bfloat16, device=dev)
+    sfa.sfa_pool_index_keys(X, 4, 0, 150, Kbar)
+    qi = _randn_bf16((4, 4, 64), g, dev)
+    w = torch.rand((4, 4), generator=g).to(dev)
+    q_seq = torch.tensor([0, 0, 0, 1], dtype=torch.int32, device=dev)
+    q_pos = torch.full((4,), 599, dtype=torch.int32, device=dev)
+    scores = torch.full((4, 150), float("nan"), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kbar, 4, 150, scores, q_group=4, dev_status=status)
+    st = sfa.sfa_read_device_status(status)
+    assert st & sfa.SFA_DEV_BAD_QUERY
+    got = np32(scores)
+    assert np.all(np.isnan(got[3])) and not np.any(np.isnan(got[:3]))
+
+
+# ------------------------------------------------------------------------------------ top-k
+@pytest.mark.parametrize("top_k", [1, 7, 256, 512, 2048])
+def test_topk_bit_exact(dev, top_k):
+    g = torch.Generator().manual_seed(top_k)
+    cr = 4
+    Bs = [0, 1, top_k - 1, top_k, top_k + 1, 3000, 8192, 8193, 20000, 70000]
+    Bs = [b for b in Bs if b >= 0]
+    n_q = len(Bs)
+    q_pos = torch.tensor([b * cr + (i % (cr - 1)) for i, b in enumerate(Bs)], dtype=torch.int32)
+    n_blk_max = max(Bs)
+    raw = torch.randn((n_q, n_blk_max), generator=g)
+    coarse = torch.round(raw * 4) / 4          # many exact ties
+    coarse[coarse == 0] = -0.0                 # signed zeros must tie with +0.0
+    coarse[1::2, ::3] = 0.0
+    scores = coarse.to(dev)
+    blk = torch.full((n_q, top_k), -9, dtype=torch.int32, device=dev)
+    n_sel = torch.full((n_q,), -9, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_topk_blocks(scores, q_pos.to(dev), cr, top_k, n_blk_max, blk, n_sel,
+                        dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    got, got_n = np32(blk), np32(n_sel)
+    sc = coarse.double().numpy()
+    for i in range(n_q):
+        B = (int(q_pos[i]) + 1) // cr
+        ref, n = oracle.select(sc[i, :B], top_k)
+        assert got_n[i] == n, (i, got_n[i], n)
+        assert np.array_equal(got[i], ref), (i, B)
+
+
+# ----------------------------------------------------------------------------------- attend
+def _attend_case(dev, dkq, dv, v_is_k, h_q, h_kv, n_seq, n_tok, q_seq, q_pos, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    K = _randn_bf16((n_seq, n_tok, h_kv, dkq), g, dev).to(dtype)
+    V = None if v_is_k else _randn_bf16((n_seq, n_tok, h_kv, dv), g, dev).to(dtype)
+    Q = _randn_bf16((len(q_seq), h_q, dkq), g, dev).to(dtype)
+    return Q, K, V
+
+
+def _random_selection(q_pos, cr, top_k, seed):
+    rng = np.random.default_rng(seed)
+    sel = np.full((len(q_pos), top_k), -1, np.int32)
+    n_sel = np.zeros(len(q_pos), np.int32)
+    for i, p in enumerate(q_pos):
+        B = (int(p) + 1) // cr
+        n = min(top_k, B)
+        pick = np.sort(rng.choice(B, size=n, replace=False)) if n else np.zeros(0, np.int64)
+        sel[i, :n] = pick
+        n_sel[i] = n
+    return sel, n_sel
+
+
+ATTN_SHAPES = [(576, 512, True, 16, 1), (512, 512, False, 16, 2), (128, 128, False, 8, 2),
+               (64, 64, True, 4, 1)]
+
+
+@pytest.mark.parametrize("dkq,dv,v_is_k,h_q,h_kv", ATTN_SHAPES)
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_gather_attend_matches_oracle(dev, dkq, dv, v_is_k, h_q, h_kv, mode, dtype):
+    cr, top_k = 4, 40
+    if mode == "decode":
+        n_seq, n_tok = 3, 900
+        q_seq = np.array([0, 1, 2], np.int32)
+        q_pos = np.array([899, 161, 2], np.int32)    # long list, just over budget, tail only
+    else:
+        n_seq, n_tok = 1, 700
+        q_seq = np.zeros(150, np.int32)
+        q_pos = np.arange(550, 700, dtype=np.int32)
+    Q, K, V = _attend_case(dev, dkq, dv, v_is_k, h_q, h_kv, n_seq, n_tok, q_seq, q_pos, dtype,
+                           dkq + h_q)
+    sel, n_sel = _random_selection(q_pos, cr, top_k, 3)
+    scale = 1.0 / math.sqrt(dkq)
+    O = torch.empty((len(q_seq), h_q, dv), device=dev)
+    lse = torch.empty((len(q_seq), h_q), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_gather_attend(Q, K, V, torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_pos).to(dev),
+                          torch.from_numpy(sel).to(dev), torch.from_numpy(n_sel).to(dev), top_k,
+                          cr, scale, O, lse=lse, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Kn, Vn, Qn = np32(K), np32(V), np32(Q)
+    tol = TOL_BF16 if dtype == torch.bfloat16 else TOL_F32
+    On, Ln = np32(O), np32(lse)
+    for i in range(len(q_seq)):
+        s, p = q_seq[i], int(q_pos[i])
+        msk = oracle.mask(p, cr, sel[i], int(n_sel[i]))
+        ref, rlse = oracle.attend(Qn[i], Kn[s], None if Vn is None else Vn[s], msk, scale, h_kv,
+                                  dv=dv)
+        err = row_rel_err(On[i], ref)
+        assert err.max() < tol, (i, err.max())
+        assert np.abs(Ln[i] - rlse).max() < (2e-3 if dtype == torch.bfloat16 else 1e-5)
+
+
+@pytest.mark.parametrize("dkq,dv,v_is_k,h_q,h_kv", ATTN_SHAPES[:2])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_dense_attend_matches_oracle(dev, dkq, dv, v_is_k, h_q, h_kv, dtype):
+    n_seq, n_tok = 2, 1100
+    q_seq = np.array([0, 1, 1, 0], np.int32)
+    q_pos = np.array([1099, 0, 517, 64], np.int32)
+    Q, K, V = _attend_case(dev, dkq, dv, v_is_k, h_q, h_kv, n_seq, n_tok, q_seq, q_pos, dtype, 9)
+    scale = 1.0 / math.sqrt(dkq)
+    O = torch.empty((len(q_seq), h_q, dv), device=dev)
+    sfa.sfa_dense_attend(Q, K, V, torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_pos).to(dev),
+                         n_tok, scale, O)
+    torch.cuda.synchronize()
+    Kn, Vn, Qn, On = np32(K), np32(V), np32(Q), np32(O)
+    tol = TOL_BF16 if dtype == torch.bfloat16 else TOL_F32
+    for i in range(len(q_seq)):
+        s, p = q_seq[i], int(q_pos[i])
+        ref, _ = oracle.attend(Qn[i], Kn[s], None if Vn is None else Vn[s],
+                               oracle.mask(p, 4, dense=True), scale, h_kv, dv=dv)
+        assert row_rel_err(On[i], ref).max() < tol
+
+
+def test_attend_flags_bad_block_lists(dev):
+    """Out-of-range, repeated or descending block ids and bad n_sel are skipped and flagged;
+    the result equals attention over the valid part of the list."""
+    dkq, dv, h_q, h_kv, cr, top_k = 64, 64, 4, 1, 4, 6
+    q_seq = np.array([0, 0, 0], np.int32)
+    q_pos = np.array([99, 99, 99], np.int32)   # B = 25
+    Q, K, V = _attend_case(dev, dkq, dv, True, h_q, h_kv, 1, 100, q_seq, q_pos, torch.bfloat16, 4)
+    sel = np.array([[2, 5, 30, 7, -1, -1], [3, 3, 9, 12, -1, -1], [1, 2, 3, 4, 5, 6]], np.int32)
+    n_sel = np.array([4, 4, 9], np.int32)
+    O = torch.empty((3, h_q, dv), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_gather_attend(Q, K, None, torch.from_numpy(q_seq).to(dev),
+                          torch.from_numpy(q_pos).to(dev), torch.from_numpy(sel).to(dev),
+                          torch.from_numpy(n_sel).to(dev), top_k, cr, 0.125, O, dev_status=status)
+    st = sfa.sfa_read_device_status(status)
+    assert st & sfa.SFA_DEV_BAD_BLOCK and st & sfa.SFA_DEV_BAD_NSEL
+    Kn, Qn, On = np32(K), np32(Q), np32(O)
+    for i in range(3):
+        valid = []
+        for j in range(min(int(n_sel[i]), top_k)):
+            b = int(sel[i, j])
+            ok = 0 <= b < 25 and (j == 0 or b > int(sel[i, j - 1]))
+            if ok:
+                valid.append(b)
+        msk = oracle.mask(99, cr, np.array(valid, np.int32), len(valid))
+        ref, _ = oracle.attend(Qn[i], Kn[0], None, msk, 0.125, h_kv, dv=dv)
+        assert row_rel_err(On[i], ref).max() < TOL_BF16
