@@ -1,0 +1,492 @@
+"""Benchmark of indexer-selected block-sparse attention on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole method over one batch of queries: pool the index-key blocks
+that this step's tokens complete, score every visible block, keep the top-k blocks plus the
+tail, and attend over the kept cells (sfa_pool_index_keys -> sfa_index_scores ->
+sfa_topk_blocks -> sfa_gather_attend).  Inputs are seeded synthetic tensors resident in HBM;
+L2 is flushed (a 512 MB write) before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 C implementation) on the host cores on
+a bounded sample of the same workload.  Under torchrun each rank runs its own replica of the
+workload on its own GPU (weak scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import indexer_selected_sparse_block_gb300 as sfa  # noqa: E402
+from indexer_selected_sparse_block_gb300 import _binding as B  # noqa: E402
+
+METRIC = "sparse-attn tokens/s (decode, pp2048) at depth; gathered-KV HBM GB/s vs peak"
+DEFAULT_WORKLOAD = "decode_32x131072"
+SECOND_WORKLOAD = "pp2048_131072"
+L2_FLUSH_BYTES = 512 << 20
+CSRC = os.path.join(ROOT, "indexer_selected_sparse_block_gb300", "csrc")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def src_hash(name):
+    with open(os.path.join(CSRC, name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """dram bytes per launch from a committed ncu summary, if taken on the current source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{kernel}@{workload}")
+    except Exception:
+        return None
+    if not rec or rec.get("src_sha256_16") != src_hash(rec["source"]):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ------------------------------------------------------------------ algorithmic work per step
+def algorithmic(w, attended):
+    """Bytes / FLOPs each stage must move / do for one step of workload w (one rank).
+
+    attended[i] = |A_i|, the number of cells query i attends (kept blocks * cr + tail).
+    Pooled keys are 4*d_idx bytes per block (bf16 hi + lo halves); a query tile of one
+    sequence reads that sequence's pooled keys once, so decode reads them once per query and
+    a prefill ubatch once per sequence.
+    """
+    cr = w.compress_ratio
+    nb = [(w.depth + j + 1) // cr for j in range(w.n_q_per_seq)] * w.n_seq
+    kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
+    if w.kind == "decode":
+        kbar_bytes = sum(b * 4 * w.d_idx for b in nb)
+    else:
+        kbar_bytes = w.n_seq * max(nb) * 4 * w.d_idx
+    return {
+        "kbar_bytes": kbar_bytes,
+        "score_bytes": sum(b * 4 for b in nb),
+        "score_flops": sum(b * 2 * w.h_idx * w.d_idx for b in nb),
+        "gathered_kv_bytes": sum(a * kv_row for a in attended),
+        "attend_flops": sum(a * 2 * w.h_q * (w.dkq + w.dv) for a in attended),
+    }
+
+
+# ------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ GPU arm
+class Workbench:
+    """Inputs, buffers and one step of the method for workload w on the current device."""
+
+    def __init__(self, w, dev):
+        self.w, self.dev = w, dev
+        self.case = sfa.make_case(w, device=dev)
+        self.n_blk_max = w.n_tok // w.compress_ratio
+        self.step = sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q,
+                                h_kv=w.h_kv, dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
+                                compress_ratio=w.compress_ratio,
+                                indexer_top_k=w.indexer_top_k, n_blk_max=self.n_blk_max,
+                                q_group=w.n_q_per_seq, device=dev)
+        # the cache state before the step: every block completed by earlier tokens is pooled
+        self.first_new_blk = w.depth // w.compress_ratio
+        self.step.pool(self.case["X"], 0, self.first_new_blk)
+        # blocks completed by this step's tokens (depth .. depth + n_q_per_seq - 1)
+        self.new_blocks = (self.first_new_blk, self.n_blk_max)
+        torch.cuda.synchronize()
+
+    def launches_per_step(self):
+        w, st = self.w, self.step
+        n = 1 if self.new_blocks[1] > self.new_blocks[0] else 0
+        if not st.dense:
+            n += 1  # scores
+            n += 1 + (B.sfa_topk_workspace_bytes(w.n_q, self.n_blk_max, w.indexer_top_k) > 0)
+            n_kv = w.indexer_top_k * w.compress_ratio + w.compress_ratio - 1
+        else:
+            n_kv = st.n_kv_dense
+        n += 1 + (B.sfa_attend_workspace_bytes(w.n_q, w.h_q, w.h_kv, w.dv, n_kv) > 0)
+        return n
+
+    def run_step(self, events=None):
+        c, st, w = self.case, self.step, self.w
+        ev = events or {}
+        if "pool" in ev:
+            ev["pool"][0].record()
+        st.pool(c["X"], *self.new_blocks)
+        if "pool" in ev:
+            ev["pool"][1].record()
+        if not st.dense:
+            if "scores" in ev:
+                ev["scores"][0].record()
+            B.sfa_index_scores(c["q_idx"], c["w"], c["q_seq"], c["q_pos"], st.Kbar,
+                               w.compress_ratio, st.n_blk_max, st.scores, q_group=st.q_group,
+                               dev_status=st.status)
+            if "scores" in ev:
+                ev["scores"][1].record()
+                ev["topk"][0].record()
+            B.sfa_topk_blocks(st.scores, c["q_pos"], w.compress_ratio, w.indexer_top_k,
+                              st.n_blk_max, st.blk_idx, st.n_sel, workspace=st.topk_ws,
+                              dev_status=st.status)
+            if "topk" in ev:
+                ev["topk"][1].record()
+        if "attend" in ev:
+            ev["attend"][0].record()
+        st.attend(c["Q"], c["K"], c["V"], c["q_seq"], c["q_pos"], w.scale)
+        if "attend" in ev:
+            ev["attend"][1].record()
+
+
+def measure(wb, steps, warmup, flush, per_stage=True):
+    """Device time of `steps` steps (L2 flushed before each), plus per-stage averages."""
+    for _ in range(warmup):
+        flush.zero_()
+        wb.run_step()
+    torch.cuda.synchronize()
+    stages = ["pool", "scores", "topk", "attend"]
+    step_ms, stage_ms = [], {s: [] for s in stages}
+    for _ in range(steps):
+        flush.zero_()
+        ev = {s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for s in stages} if per_stage else {}
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        wb.run_step(ev)
+        e1.record()
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        for s, (a, b) in ev.items():
+            try:
+                stage_ms[s].append(a.elapsed_time(b))
+            except RuntimeError:
+                pass
+    return step_ms, {s: (sum(v) / len(v) if v else 0.0) for s, v in stage_ms.items()}
+
+
+def measure_e2e(wb, steps, warmup):
+    """Same step through the public API with host inputs: each step copies this step's query
+    inputs and new cache rows from pinned host memory, runs, and reads O back."""
+    c, w = wb.case, wb.w
+    names = ["Q", "q_idx", "w", "q_seq", "q_pos"]
+    host = {n: c[n].cpu().pin_memory() for n in names}
+    # the step's new cache rows (positions depth .. depth + n_q_per_seq - 1 of each sequence)
+    sl = slice(w.depth, w.n_tok)
+    host["K_new"] = c["K"][:, sl].cpu().pin_memory()
+    host["X_new"] = c["X"][:, sl].cpu().pin_memory()
+    if c["V"] is not None:
+        host["V_new"] = c["V"][:, sl].cpu().pin_memory()
+    out = torch.empty(wb.step.O.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def one():
+        for n in names:
+            c[n].copy_(host[n], non_blocking=True)
+        c["K"][:, sl].copy_(host["K_new"], non_blocking=True)
+        c["X"][:, sl].copy_(host["X_new"], non_blocking=True)
+        if c["V"] is not None:
+            c["V"][:, sl].copy_(host["V_new"], non_blocking=True)
+        wb.run_step()
+        out.copy_(wb.step.O, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def oracle_sample(w, dev_case, n_queries, n_threads):
+    """Host copies of a bounded sample (the first n_queries queries) for the CPU oracle."""
+    import numpy as np
+
+    qi = list(range(min(n_queries, w.n_q)))
+    seqs = sorted({int(dev_case["q_seq"][i]) for i in qi})
+    remap = {s: k for k, s in enumerate(seqs)}
+    npf = lambda t: t.float().cpu().numpy()  # noqa: E731
+    st = torch.tensor(seqs, device=dev_case["X"].device)
+    X = npf(dev_case["X"].index_select(0, st))
+    K = npf(dev_case["K"].index_select(0, st))
+    V = None if dev_case["V"] is None else npf(dev_case["V"].index_select(0, st))
+    sel = torch.tensor(qi, device=dev_case["X"].device)
+    q = {n: dev_case[n].index_select(0, sel) for n in ["Q", "q_idx", "w", "q_pos", "q_seq"]}
+    q_seq = np.array([remap[int(s)] for s in q["q_seq"].cpu()], np.int32)
+    return dict(X=X, q_idx=npf(q["q_idx"]), w=npf(q["w"]), Q=npf(q["Q"]), K=K, V=V,
+                q_seq=q_seq, q_pos=q["q_pos"].cpu().numpy().astype(np.int32)), len(qi)
+
+
+def time_oracle(w, sample, n_q, n_threads, min_seconds=3.0, max_reps=50):
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        out = oracle.run(sample["X"], sample["q_idx"], sample["w"], sample["Q"], sample["K"],
+                         sample["V"], sample["q_seq"], sample["q_pos"], cr=w.compress_ratio,
+                         top_k=w.indexer_top_k, scale=w.scale, dv=w.dv, n_threads=n_threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return n_q * reps / el, out["threads"], el
+
+
+def run_reference(args, w, rank, world):
+    """--impl reference: the CPU oracle on the host cores, on bounded samples of w."""
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    cores = os.cpu_count() or 1
+    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    case = sfa.make_case(w, device=dev)
+    sample, nq = oracle_sample(w, case, min(cores, w.n_q), cores)
+    del case
+    vals, used = [], 1
+    for _ in range(args.warmup):
+        time_oracle(w, sample, nq, cores, min_seconds=0.0, max_reps=1)
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        v, used, _ = time_oracle(w, sample, nq, cores, min_seconds=0.0, max_reps=1)
+        vals.append(v)
+    el = time.perf_counter() - t_all
+    value = nq * args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "queries_per_step_sample": nq},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "sample": f"first {nq} of {w.n_q} queries of {w.name}, whole "
+                                       "method (pool, score, sort, mask, attend) per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(sfa.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-second", action="store_true", help="skip the pp2048 companion line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = sfa.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, w, rank, world)
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        dist.barrier()
+        __graft_entry__.build()
+    hbm_peak, tf_peak, peak_kind = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    wb = Workbench(w, dev)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms, stage_ms = measure(wb, args.steps, args.warmup, flush)
+        total_ms = sum(step_ms)
+        if dist is not None:
+            t = torch.tensor([total_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+    torch.cuda.synchronize()
+    status = B.sfa_read_device_status(wb.step.status)
+    ms_per_step = total_ms / args.steps
+    n_q_total = w.n_q * world
+    value = n_q_total / (ms_per_step / 1000.0)
+
+    n_sel = wb.step.n_sel.cpu()
+    tail = [(int(p) + 1) % w.compress_ratio for p in wb.case["q_pos"].cpu()]
+    attended = [int(n) * w.compress_ratio + t for n, t in zip(n_sel, tail)] if not wb.step.dense \
+        else [int(p) + 1 for p in wb.case["q_pos"].cpu()]
+    alg = algorithmic(w, attended)
+    kernels = {}
+    for name, ms in stage_ms.items():
+        if ms <= 0 or (name == "pool" and wb.new_blocks[1] <= wb.new_blocks[0]):
+            continue
+        if name in ("scores", "topk") and wb.step.dense:
+            continue
+        k = {"ms": ms}
+        if name == "scores":
+            k.update(bound="hbm", bytes=alg["kbar_bytes"] + alg["score_bytes"])
+        elif name == "attend":
+            k.update(bound="hbm" if w.kind == "decode" else "tensor", bytes=alg["gathered_kv_bytes"],
+                     flops=alg["attend_flops"])
+        elif name == "topk":
+            k.update(bound="hbm", bytes=alg["score_bytes"])
+        elif name == "pool":
+            nb = wb.new_blocks[1] - wb.new_blocks[0]
+            k.update(bound="hbm", bytes=w.n_seq * nb * (w.compress_ratio * 2 + 4) * w.d_idx)
+        if "bytes" in k:
+            k["GBps"] = k["bytes"] / (ms * 1e6)
+            k["hbm_frac"] = k["GBps"] / hbm_peak
+        if "flops" in k:
+            k["TFLOPs"] = k["flops"] / (ms * 1e9)
+            k["tensor_frac"] = k["TFLOPs"] / tf_peak
+        kernels[name] = k
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dk = kernels[dom]
+    src = {"scores": "scores.cu", "attend": "attend.cu", "topk": "topk.cu", "pool": "pool.cu"}[dom]
+    if dk.get("bound") == "tensor":
+        roof = {"bound": "tensor", "achieved": dk["TFLOPs"], "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": dk["TFLOPs"] / tf_peak}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["GBps"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": dk["GBps"] / hbm_peak}
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" \
+        else "fallback"
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["source"] = src
+
+    e2e_ms, h2d, d2h = measure_e2e(wb, max(3, args.steps // 2), 3)
+    launches = wb.launches_per_step() * args.steps
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) K/Q/index keys, U(0,1) head weights)",
+            "config": {"workload": w.name, "kind": w.kind, "n_seq": w.n_seq,
+                       "queries_per_step": w.n_q, "depth": w.depth, "h_q": w.h_q,
+                       "h_kv": w.h_kv, "dkq": w.dkq, "dv": w.dv, "v_is_k": w.v_is_k,
+                       "h_idx": w.h_idx, "d_idx": w.d_idx, "compress_ratio": w.compress_ratio,
+                       "indexer_top_k": w.indexer_top_k, "l2": "flushed (512 MB write) "
+                       "before every timed step, outside the timed events"},
+            "gathered_kv_GBps": kernels.get("attend", {}).get("GBps"),
+            "gathered_kv_hbm_frac": kernels.get("attend", {}).get("hbm_frac"),
+            "roofline": roof, "kernels": kernels,
+            "e2e": {"value": n_q_total / (e2e_ms / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches, "clocks": clk.summary(), "device_status": status}
+    del wb
+    torch.cuda.empty_cache()
+
+    if not args.no_second and rank == 0 and world == 1:
+        w2 = sfa.WORKLOADS[SECOND_WORKLOAD]
+        wb2 = Workbench(w2, dev)
+        s2, st2 = measure(wb2, max(3, args.steps // 4), 3, flush)
+        ms2 = sum(s2) / len(s2)
+        n_sel2 = wb2.step.n_sel.cpu()
+        att2 = [int(n) * w2.compress_ratio + (int(p) + 1) % w2.compress_ratio
+                for n, p in zip(n_sel2, wb2.case["q_pos"].cpu())]
+        a2 = algorithmic(w2, att2)
+        line["pp2048"] = {
+            "workload": w2.name, "value": w2.n_q / (ms2 / 1000.0), "unit": "tokens/s",
+            "ms_per_step": ms2, "stage_ms": st2,
+            "attend_TFLOPs": a2["attend_flops"] / (st2["attend"] * 1e9),
+            "attend_tensor_frac": a2["attend_flops"] / (st2["attend"] * 1e9) / tf_peak,
+            "scores_TFLOPs": a2["score_flops"] / (st2["scores"] * 1e9),
+            "scores_tensor_frac": a2["score_flops"] / (st2["scores"] * 1e9) / tf_peak}
+        del wb2
+        torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        case = sfa.make_case(w, device=dev)
+        sample, nq = oracle_sample(w, case, min(cores, w.n_q), cores)
+        del case
+        v, used, el = time_oracle(w, sample, nq, cores)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                                "sample": f"first {nq} of {w.n_q} queries of {w.name} "
+                                          f"(whole method per query), repeated for {el:.1f} s"}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

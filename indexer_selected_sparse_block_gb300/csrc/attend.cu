@@ -14,9 +14,11 @@
 //     contiguous rows), XOR-swizzled rows so that ldmatrix is conflict-free, 2-4 stages;
 //   * S = Q K^T on tensor cores (mma.sync m16n8k16, M = the 16 query heads of the KV head),
 //     the head dim split over the 4 warps and the partial sums reduced through shared memory;
-//   * online softmax (base 2) over the 32 tokens, P rounded to bf16;
-//   * O += P V on tensor cores, the 512 value dims split over the 4 warps; V = K reuses the
-//     K tile in shared memory.
+//   * online softmax (base 2) over the 32 tokens; P is carried as two bf16 halves
+//     (hi = bf16(p), lo = bf16(p - hi)), so P V is accurate to ~2^-17 instead of the 2^-9 of
+//     a single bf16 rounding (which alone uses up a 2e-3 output tolerance);
+//   * O += P_hi V + P_lo V on tensor cores, the 512 value dims split over the 4 warps; V = K
+//     reuses the K tile in shared memory.
 // Decode has few queries, so each list is split over several CTAs (flash-decoding) and the
 // partial (O, m, l) are merged by combine_kernel.  fp32 inputs take a plain SIMT kernel with
 // the same split/merge structure (accuracy reference path).
@@ -125,8 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     uint8_t *sStage = smem;                                              // stages x STAGE_BYTES
     uint8_t *sQ = sStage + (size_t)p.stages * STAGE_BYTES;               // 16 x KROW
     float *sSP = reinterpret_cast<float *>(sQ + 16 * KROW);              // 4 x 16 x SP_PITCH
-    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(sSP + 4 * 16 * SP_PITCH);
-    float *sAlpha = reinterpret_cast<float *>(sP + 16 * P_PITCH);        // 16
+    __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(sSP + 4 * 16 * SP_PITCH);  // hi, lo
+    float *sAlpha = reinterpret_cast<float *>(sP + 2 * 16 * P_PITCH);    // 16
     float *sL = sAlpha + 16;                                             // 16
     float *sM = sL + 16;                                                 // 16
     int *sTok = reinterpret_cast<int *>(sM + 16);                        // stages x kT
@@ -283,20 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
             const float m_new = fmaxf(m_run, mx);
             const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-            float pr[4], rs = 0.f;
+            float ph[4], pl[4], rs = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
-                pr[e] = __bfloat162float(__float2bfloat16_rn(pe));
-                rs += pr[e];
+                ph[e] = __bfloat162float(__float2bfloat16_rn(pe));
+                pl[e] = pe - ph[e];
+                rs += pe;
             }
             rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
             rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
             rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
             l_run = l_run * alpha + rs;
             m_run = m_new;
-            uint2 pk = make_uint2(pack_bf16(pr[0], pr[1]), pack_bf16(pr[2], pr[3]));
-            *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) = pk;
+            *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
+                make_uint2(pack_bf16(ph[0], ph[1]), pack_bf16(ph[2], ph[3]));
+            *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
+                make_uint2(pack_bf16(pl[0], pl[1]), pack_bf16(pl[2], pl[3]));
             if ((tid & 7) == 0) sAlpha[row] = alpha;
         }
         __syncthreads();
@@ -311,10 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
             const uint32_t pbase = smem_u32(sP);
 #pragma unroll
             for (int ks = 0; ks < kT / 16; ++ks) {
-                uint32_t pa[4];
+                uint32_t pa[4], pb[4];
                 {
                     const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
-                    ldsm_x4(pbase + r * (P_PITCH * 2) + col * 2, pa[0], pa[1], pa[2], pa[3]);
+                    const uint32_t a = pbase + r * (P_PITCH * 2) + col * 2;
+                    ldsm_x4(a, pa[0], pa[1], pa[2], pa[3]);
+                    ldsm_x4(a + 16 * P_PITCH * 2, pb[0], pb[1], pb[2], pb[3]);
                 }
 #pragma unroll
                 for (int np = 0; np < NTV / 2; ++np) {
@@ -325,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
                     ldsm_x4_t(vbase + k * VROW + swz(c, k) * 16, b0, b1, b2, b3);
                     mma_bf16_16816(o[2 * np], pa, b0, b1);
                     mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                    mma_bf16_16816(o[2 * np], pb, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pb, b2, b3);
                 }
             }
         }
@@ -491,7 +500,7 @@ template <int DKQ, int DV, bool VK>
 int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st) {
     constexpr int KROW = DKQ * 2, VROW = VK ? KROW : DV * 2;
     constexpr int STAGE = kT * KROW + (VK ? 0 : kT * VROW);
-    const size_t fixed = 16 * KROW + 4 * 16 * (kT + 8) * 4 + 16 * (kT + 8) * 2 + 48 * 4 +
+    const size_t fixed = 16 * KROW + 4 * 16 * (kT + 8) * 4 + 2 * 16 * (kT + 8) * 2 + 48 * 4 +
                         kMaxBlkList * 4 + 4 * kT * 4 + 256;
     int stages = (int)((227 * 1024 - fixed) / STAGE);
     if (stages > 4) stages = 4;
@@ -501,9 +510,7 @@ int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st) {
     const size_t smem = fixed + (size_t)stages * STAGE;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(attend_bf16_kernel<DKQ, DV, VK>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return SFA_ERR_CUDA;
+        if (!allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
         attr = true;
     }
     attend_bf16_kernel<DKQ, DV, VK><<<grid, kThreads, smem, st>>>(q);

@@ -275,10 +275,7 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
                         256 * 4 + (size_t)p.q_tile * H * 4;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(index_score_kernel<KP, H>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
-            return SFA_ERR_CUDA;
+        if (!allow_max_dynamic_smem(index_score_kernel<KP, H>)) return SFA_ERR_CUDA;
         attr_set = true;
     }
     // Spread the block tiles of each query tile over enough CTAs to fill the GPU.

@@ -30,6 +30,24 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int device_sm_count();  // cached per device (api.cu)
 
+// Opts `fn` into the largest dynamic shared memory its static usage leaves (227 KB per CTA on
+// sm_103a in total).  Clears the runtime's last error on failure.
+template <typename F>
+inline bool allow_max_dynamic_smem(F *fn) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, fn) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const int avail = 227 * 1024 - (int)a.sharedSizeBytes;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, avail) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 // 1.5 s: the longest any bounded wait in a kernel may spin before giving up.
 constexpr uint64_t kWaitLimitNs = 1500000000ull;
 

@@ -326,10 +326,7 @@ extern "C" int sfa_topk_blocks(const float *scores, int64_t score_stride, const 
     const size_t smem1 = sizeof(SelShared) + (size_t)ch * 4;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess ||
-            cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
+        if (!allow_max_dynamic_smem(topk_chunk_kernel) || !allow_max_dynamic_smem(topk_merge_kernel))
             return SFA_ERR_CUDA;
         attr = true;
     }

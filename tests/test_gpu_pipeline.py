@@ -1,0 +1,185 @@
+"""End-to-end parity of the whole method on the five synthetic workloads, at full size, in the
+launch configuration the benchmark times (SfaStep through the C ABI).
+
+Small workloads are checked on every query; the large ones on sampled queries that the
+oracle recomputes one by one (pool -> scores -> select -> mask -> attention over the kept
+rows only).  Selections follow the agreement rule: identical wherever the oracle's gap at the
+cut exceeds 1e-4 relative; outputs are compared with the oracle attending the GPU's own set.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_BF16, check_selection, np32, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+sfa = pytest.importorskip("indexer_selected_sparse_block_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _step_for(w, dev, top_k=None):
+    n_blk_max = w.n_tok // w.compress_ratio
+    return sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
+                       dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
+                       compress_ratio=w.compress_ratio,
+                       indexer_top_k=top_k or w.indexer_top_k, n_blk_max=n_blk_max,
+                       q_group=w.n_q_per_seq, device=dev)
+
+
+def _run(w, dev, top_k=None):
+    case = sfa.make_case(w, device=dev)
+    step = _step_for(w, dev, top_k)
+    step.pool(case["X"], 0, step.n_blk_max)
+    step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
+             case["q_seq"], case["q_pos"], w.scale)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(step.status) == 0
+    return case, step
+
+
+def _oracle_one(w, case, i, X_host, got_sel, got_n, top_k):
+    """Oracle for query i, attending its own set and, if the GPU's differs within the rule,
+    the GPU's set too.  Returns (selection ok, exact-rule applied, rel error vs oracle)."""
+    cr = w.compress_ratio
+    s = int(case["q_seq"][i])
+    p = int(case["q_pos"][i])
+    B = (p + 1) // cr
+    kb = oracle.pool(X_host, B, cr)
+    sc = oracle.index_scores(np32(case["q_idx"][i]), np32(case["w"][i]), kb)
+    ok, exact = check_selection(got_sel, got_n, sc, top_k)
+    sel, n = oracle.select(sc, top_k)
+    if not exact and ok:      # attend the GPU's own set
+        sel, n = np.asarray(got_sel, np.int32), int(got_n)
+    msk = oracle.mask(p, cr, sel, n)
+    toks = np.nonzero(msk)[0]
+    rows = np.full(p + 1, -1, np.int64)
+    rows[toks] = np.arange(len(toks))
+    tk = torch.from_numpy(toks).to(case["K"].device)
+    Ks = np32(case["K"][s].index_select(0, tk))
+    Vs = None if case["V"] is None else np32(case["V"][s].index_select(0, tk))
+    ref, lse = oracle.attend(np32(case["Q"][i]), Ks, Vs, msk, w.scale, w.h_kv, dv=w.dv,
+                             tok_row=rows)
+    return ok, exact, ref, lse
+
+
+def _check_sampled(w, case, step, queries):
+    got_sel = np32(step.blk_idx)
+    got_n = np32(step.n_sel)
+    O = np32(step.O)
+    L = np32(step.lse)
+    x_cache = {}
+    n_exact = 0
+    for i in queries:
+        s = int(case["q_seq"][i])
+        if s not in x_cache:
+            x_cache = {s: np32(case["X"][s])}
+        ok, exact, ref, lse = _oracle_one(w, case, i, x_cache[s], got_sel[i], got_n[i],
+                                          step.top_k)
+        assert ok, f"query {i}: kept blocks violate the agreement rule"
+        n_exact += exact
+        err = row_rel_err(O[i], ref).max()
+        assert err < TOL_BF16, (i, err)
+        assert np.abs(L[i] - lse).max() < 2e-3
+    return n_exact
+
+
+def test_decode_1x4096_all(dev):
+    w = sfa.WORKLOADS["decode_1x4096"]
+    case, step = _run(w, dev)
+    assert _check_sampled(w, case, step, range(w.n_q)) >= 0
+
+
+def test_prefill_512x8192_all(dev):
+    w = sfa.WORKLOADS["prefill_512x8192"]
+    case, step = _run(w, dev)
+    c = {k: np32(v) for k, v in case.items()}
+    ref = oracle.run(c["X"], c["q_idx"], c["w"], c["Q"], c["K"], c["V"], c["q_seq"], c["q_pos"],
+                     cr=w.compress_ratio, top_k=w.indexer_top_k, scale=w.scale, dv=w.dv,
+                     want_scores=True)
+    got_sel, got_n = np32(step.blk_idx), np32(step.n_sel)
+    O = np32(step.O)
+    n_exact = 0
+    for i in range(w.n_q):
+        B = (int(c["q_pos"][i]) + 1) // w.compress_ratio
+        ok, exact = check_selection(got_sel[i], got_n[i], ref["score"][i, :B], w.indexer_top_k)
+        assert ok, i
+        n_exact += exact
+        if exact:
+            assert row_rel_err(O[i], ref["O"][i]).max() < TOL_BF16, i
+    assert n_exact > 0.9 * w.n_q
+
+
+def test_prefill_512x1000_below_budget_is_dense(dev):
+    """Every query has B_i <= indexer_top_k: the step takes the dense path; the oracle's
+    sparse and dense results are identical, and the GPU's sparse path agrees with both."""
+    w = sfa.WORKLOADS["prefill_512x1000"]
+    case, step = _run(w, dev)
+    assert step.dense
+    c = {k: np32(v) for k, v in case.items()}
+    kw = dict(cr=w.compress_ratio, scale=w.scale, dv=w.dv)
+    sp = oracle.run(c["X"], c["q_idx"], c["w"], c["Q"], c["K"], c["V"], c["q_seq"], c["q_pos"],
+                    top_k=w.indexer_top_k, **kw)
+    de = oracle.run(c["X"], c["q_idx"], c["w"], c["Q"], c["K"], c["V"], c["q_seq"], c["q_pos"],
+                    top_k=0, **kw)
+    assert np.array_equal(sp["O"], de["O"])
+    assert row_rel_err(np32(step.O), de["O"]).max() < TOL_BF16
+    # the sparse kernels on the same inputs (every block kept) agree with the dense kernel
+    n_blk_max = w.n_tok // w.compress_ratio
+    scores = torch.empty((w.n_q, n_blk_max), device=dev)
+    blk = torch.empty((w.n_q, w.indexer_top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(w.n_q, dtype=torch.int32, device=dev)
+    Kbar = step.Kbar
+    sfa.sfa_index_scores(case["q_idx"], case["w"], case["q_seq"], case["q_pos"], Kbar,
+                         w.compress_ratio, n_blk_max, scores, q_group=w.n_q)
+    sfa.sfa_topk_blocks(scores, case["q_pos"], w.compress_ratio, w.indexer_top_k, n_blk_max,
+                        blk, n_sel)
+    O = torch.empty_like(step.O)
+    sfa.sfa_gather_attend(case["Q"], case["K"], case["V"], case["q_seq"], case["q_pos"], blk,
+                          n_sel, w.indexer_top_k, w.compress_ratio, w.scale, O)
+    torch.cuda.synchronize()
+    nb = (np32(case["q_pos"]) + 1) // w.compress_ratio
+    assert np.array_equal(np32(n_sel), nb)
+    assert row_rel_err(np32(O), de["O"]).max() < TOL_BF16
+
+
+def test_decode_32x131072_sampled(dev):
+    w = sfa.WORKLOADS["decode_32x131072"]
+    case, step = _run(w, dev)
+    _check_sampled(w, case, step, [0, 7, 19, 31])
+
+
+def test_pp2048_131072_sampled(dev):
+    w = sfa.WORKLOADS["pp2048_131072"]
+    case, step = _run(w, dev)
+    _check_sampled(w, case, step, [0, 1, 511, 1024, 1500, 2046, 2047])
+
+
+def test_decode_4x1048576_sampled(dev):
+    w = sfa.WORKLOADS["decode_4x1048576"]
+    case, step = _run(w, dev)
+    _check_sampled(w, case, step, [0, 3])
+
+
+def test_stream_isolation(dev):
+    """Changing one sequence's caches leaves the other sequences' outputs bit-identical."""
+    w = sfa.WORKLOADS["decode_1x4096"].with_(n_seq=4, depth=3000, seed=77)
+    case, step = _run(w, dev)
+    O1 = step.O.clone()
+    case["K"][2].mul_(-1)
+    case["X"][2].mul_(-1)
+    step.pool(case["X"], 0, step.n_blk_max)
+    step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
+             case["q_seq"], case["q_pos"], w.scale)
+    torch.cuda.synchronize()
+    same = [bool(torch.equal(O1[i], step.O[i])) for i in range(4)]
+    assert same == [True, True, False, True]
