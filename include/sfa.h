@@ -168,6 +168,40 @@ int sfa_dense_attend(const void *Q, const void *K, const void *V, int dtype, int
                      float *O, float *lse, void *workspace, size_t workspace_bytes,
                      int32_t *dev_status, sfa_stream_t stream);
 
+/*
+ * sfa_gather_attend_noalloc -- sfa_gather_attend for callers that cannot allocate device
+ * memory.  (No counterpart in the pages: it is a property of this library's interface.)
+ *
+ * Some callers have no way to hand the library a workspace at the point of the call: a host
+ * application that owns every byte of device memory through its own allocator and exposes
+ * none of it, or a latency-critical decode loop that must never call cudaMalloc/cudaFree
+ * (cudaFree synchronises the whole device and would stall every other stream).  This entry
+ * point computes exactly what sfa_gather_attend computes, with the same kernels, but takes its
+ * split-KV scratch from a fixed array compiled into libsfa (SFA_NOALLOC_SCRATCH_BYTES per GPU,
+ * held by every GPU that loads the library until the process exits) instead of `workspace`.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  - Arguments and results are those of sfa_gather_attend without the workspace pair; the
+ *    caller still owns Q, K, V, the block lists, O and lse.
+ *  - If the scratch that this shape needs (sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv,
+ *    top_k*cr + cr - 1)) exceeds SFA_NOALLOC_SCRATCH_BYTES the call returns
+ *    SFA_ERR_WORKSPACE and enqueues nothing; use sfa_gather_attend with a workspace instead.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *    capture begins.
+ *  - Every call on a device shares the one array and leaves the last call's partial results
+ *    in it.  Nothing in it needs to start at zero: every split writes its partial before the
+ *    merge reads it.  Calls whose work overlaps on the GPU (for example on two streams at
+ *    once) race on the array: order them on one stream or with events.
+ */
+#define SFA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int sfa_gather_attend_noalloc(const void *Q, const void *K, const void *V, int dtype, int n_seq,
+                              int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv,
+                              float scale, const int32_t *q_seq, const int32_t *q_pos,
+                              const int32_t *blk_idx, const int32_t *n_sel, int top_k,
+                              int compress_ratio, float *O, float *lse, int32_t *dev_status,
+                              sfa_stream_t stream);
+
 /* Copies *dev_status to *host_out after the work already enqueued on `stream` (this call
  * synchronises the stream). */
 int sfa_read_device_status(const int32_t *dev_status, int32_t *host_out, sfa_stream_t stream);

@@ -38,6 +38,9 @@ SIGNATURES = {
                                  _vp]),
     "sfa_dense_attend": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int, _int, _int,
                                 _f32, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "sfa_gather_attend_noalloc": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int,
+                                         _int, _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _vp,
+                                         _vp, _vp, _vp]),
     "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
     "sfa_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -168,6 +171,21 @@ def sfa_gather_attend(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int, compres
                                  _p(n_sel), top_k, compress_ratio, _p(O), _p(lse), _p(workspace),
                                  ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_gather_attend", rc)
+
+
+def sfa_gather_attend_noalloc(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,
+                              compress_ratio: int, scale: float, O, lse=None, dev_status=None,
+                              stream=None):
+    """sfa_gather_attend without a workspace: for callers that cannot allocate device memory
+    when they call (their split-KV scratch is a fixed 16 MiB array inside libsfa, shared by
+    every call on the device; overlapping calls on the GPU race on it)."""
+    n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv = _attn_dims(Q, K, V, O)
+    rc = lib().sfa_gather_attend_noalloc(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap,
+                                         n_q, h_q, h_kv, dkq, dv, float(scale), _p(q_seq),
+                                         _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
+                                         compress_ratio, _p(O), _p(lse), _p(dev_status),
+                                         _stream(stream))
+    _check("sfa_gather_attend_noalloc", rc)
 
 
 def sfa_dense_attend(Q, K, V, q_seq, q_pos, n_kv_max: int, scale: float, O, lse=None,

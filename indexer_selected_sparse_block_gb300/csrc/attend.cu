@@ -24,6 +24,8 @@
 // the same split/merge structure (accuracy reference path).
 #include <math.h>
 
+#include <mutex>
+
 #include "sfa_common.cuh"
 
 namespace sfa {
@@ -615,4 +617,55 @@ extern "C" int sfa_dense_attend(const void *Q, const void *K, const void *V, int
     return sfa::run_attend(Q, K, V, dtype, n_seq, n_tok_cap, n_q, h_q, h_kv, dkq, dv, scale,
                            q_seq, q_pos, nullptr, nullptr, 0, 1, 1, n_kv_max, O, lse, workspace,
                            workspace_bytes, dev_status, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// sfa_gather_attend_noalloc: the split-KV scratch lives in this file-scope device array, so
+// the call allocates nothing.  Host code may not use the array's name as a device address:
+// the address is looked up once per device with cudaGetSymbolAddress and cached.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SFA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+void *noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+extern "C" int sfa_gather_attend_noalloc(const void *Q, const void *K, const void *V, int dtype,
+                                         int n_seq, int64_t n_tok_cap, int n_q, int h_q,
+                                         int h_kv, int dkq, int dv, float scale,
+                                         const int32_t *q_seq, const int32_t *q_pos,
+                                         const int32_t *blk_idx, const int32_t *n_sel,
+                                         int top_k, int compress_ratio, float *O, float *lse,
+                                         int32_t *dev_status, sfa_stream_t stream) {
+    if (compress_ratio < 1 || top_k < 1) return SFA_ERR_INVALID_ARG;
+    const int64_t n_kv_max = (int64_t)top_k * compress_ratio + compress_ratio - 1;
+    const size_t need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max);
+    if (need > SFA_NOALLOC_SCRATCH_BYTES) return SFA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch();
+        if (!scratch) return SFA_ERR_CUDA;
+    }
+    return sfa::run_attend(Q, K, V, dtype, n_seq, n_tok_cap, n_q, h_q, h_kv, dkq, dv, scale,
+                           q_seq, q_pos, blk_idx, n_sel, top_k, compress_ratio, 0, n_kv_max, O,
+                           lse, scratch, need, dev_status, (cudaStream_t)stream);
 }
