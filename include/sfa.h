@@ -63,10 +63,10 @@ enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
                                  released its resources and returned early                */
 
 /*
- * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, over
- * the RAW index keys ("pooling happens before the norm and the rotation": QSA commit, indexer
- * key cache paragraph; "one mean-pooled key per block of compress_ratio tokens": QSA budget
- * paragraph).  Blocks are cut on positions: block b holds tokens [b*cr, b*cr + cr).
+ * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, taken
+ * over the RAW index keys, since the model pools before it normalises and rotates them (QSA
+ * commit, indexer key cache paragraph; block pooling: QSA commit, budget paragraph).  Blocks
+ * are cut on positions: block b holds tokens [b*cr, b*cr + cr).
  *
  *   X      [n_seq][x_seq_stride / d_idx][d_idx], x_dtype SFA_BF16 or SFA_F32 (raw keys)
  *   Kbar   [n_seq][kbar_seq_stride / (2*d_idx)][2*d_idx] bf16 (uint16 storage): row b of
@@ -84,10 +84,10 @@ int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_
                         int64_t kbar_seq_stride, sfa_stream_t stream);
 
 /*
- * sfa_index_scores -- the indexer score of every complete block visible to each query
- * ("rectifies each head's dot product before summing over heads": QSA commit, index
- * comparison paragraph; scoring is batched over streams so that stream s's queries meet
- * only stream s's blocks: QSA commit, multi-stream scoring).
+ * sfa_index_scores -- the indexer score of every complete block visible to each query: each
+ * index head's dot product passes through a ReLU before the weighted sum over heads (QSA
+ * commit, index comparison paragraph); a query is scored only against the blocks of its own
+ * sequence (QSA commit, multi-stream scoring).
  *
  *   q_idx   [n_q][h_idx][d_idx] bf16 index queries;   w [n_q][h_idx] fp32 head weights
  *   q_seq, q_pos [n_q] int32: sequence and position of each query
@@ -111,11 +111,12 @@ int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
                      int32_t *dev_status, sfa_stream_t stream);
 
 /*
- * sfa_topk_blocks -- the budget rule ("keeps a budget of the best blocks, plus the tail ...
- * Below indexer_top_k + compress_ratio - 1 cached tokens every block fits in the budget":
- * QSA commit, budget paragraph; the cut lands on a block boundary: QSA commit, expansion
- * paragraph).  Ties at the cut go to the lower block index (the pages do not order equal
- * scores; this is the stated reading).  -0.0 counts as +0.0; a NaN score ranks lowest.
+ * sfa_topk_blocks -- the budget rule: the indexer_top_k best blocks are kept, and the tail of
+ * tokens that do not yet fill a block is always attended; when a query sees no more blocks
+ * than the budget, every block is kept and the result is dense (QSA commit, budget
+ * paragraph).  The budget is whole blocks, so the cut falls on a block boundary (QSA commit,
+ * expansion paragraph).  Ties at the cut go to the lower block index (the pages do not order
+ * equal scores; this is the stated reading).  -0.0 counts as +0.0; a NaN score ranks lowest.
  *
  *   scores  as written by sfa_index_scores; row i is read at [0, B_i)
  *   blk_idx [n_q][top_k] int32: the kept block ids of query i, ascending, padded with -1
@@ -158,7 +159,7 @@ int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype, in
 /*
  * sfa_dense_attend -- causal attention of each query over all of its sequence's tokens
  * 0..p_i: the below-budget case, where the sparse result is exactly dense (QSA commit, budget
- * paragraph; "a layer with no ratio falls back to dense").  n_kv_max must bound p_i + 1 for
+ * paragraph); a layer without a compression ratio also attends densely.  n_kv_max must bound p_i + 1 for
  * every query (the role of PR #27970's n_kv_max hint); it sizes the split-KV work.
  * Arguments otherwise as sfa_gather_attend.
  */

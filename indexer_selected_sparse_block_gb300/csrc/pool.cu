@@ -1,8 +1,8 @@
 // pool.cu -- block mean pooling of the raw index keys (sfa_pool_index_keys).
 //
-// "An indexer scores one mean-pooled key per block of compress_ratio tokens"; the indexer
-// key cache "holds raw keys, because pooling happens before the norm and the rotation"
-// (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+// The indexer works on one mean-pooled key per block of compress_ratio tokens, pooled from the
+// raw index keys: the model pools before it normalises and rotates them (llama.cpp commit
+// "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
 //
 // HBM-bound streaming kernel: each thread owns one 16-byte chunk of one pooled row, reads the
 // chunk of the block's cr raw rows with 16-byte loads (a warp covers whole 128/256-byte rows),

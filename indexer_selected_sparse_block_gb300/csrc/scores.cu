@@ -1,9 +1,9 @@
 // scores.cu -- the indexer score of every visible block (sfa_index_scores).
 //
 //   s_ib = sum_j w_ij * max(0, qidx_ij . kbar_b)
-// ("The reference rectifies each head's dot product before summing over heads"; scoring is
-// batched over streams so that stream s's queries only meet stream s's blocks: llama.cpp
-// commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs.)
+// (each head's dot product is rectified before the sum over heads, and a query meets only
+// the blocks of its own sequence: llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)",
+// QSA paragraphs.)
 //
 // Design (sm_103a): the q.kbar contraction is a GEMM D[blocks x (queries*heads)] on the
 // tcgen05 tensor cores with the fp32 accumulator in tensor memory.  The pooled key is stored

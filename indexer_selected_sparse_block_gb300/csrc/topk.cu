@@ -1,8 +1,8 @@
 // topk.cu -- the budget rule: the indexer_top_k best blocks of each query (sfa_topk_blocks).
 //
-// "keeps a budget of the best blocks, plus the tail of tokens that do not yet form a complete
-// block.  Below indexer_top_k + compress_ratio - 1 cached tokens every block fits in the
-// budget" (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+// The budget holds the indexer_top_k best blocks; the tail that does not fill a block is
+// attended anyway, and a query that sees no more blocks than the budget keeps them all
+// (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
 // Order: score descending, then block index ascending (the tie rule of this library).  The
 // kept ids are written ascending and the row is padded with -1 (the sparse index rows of
 // llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM" are padded the same way).

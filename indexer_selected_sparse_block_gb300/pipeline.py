@@ -5,10 +5,9 @@ kept block lists, workspaces, outputs) and runs the stages as the C entry points
 
   sfa_pool_index_keys -> sfa_index_scores -> sfa_topk_blocks -> sfa_gather_attend
 
-or, when every query is below the budget (B_i <= indexer_top_k for all i), the exact dense
-case ``sfa_dense_attend`` ("Below indexer_top_k + compress_ratio - 1 cached tokens every
-block fits in the budget, so the result is exactly dense": llama.cpp commit "model: add
-Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+or, when every query is below the budget (B_i <= indexer_top_k for all i), the dense case
+``sfa_dense_attend``: every block then fits the budget, so the method is exactly dense
+attention (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
 """
 from __future__ import annotations
 

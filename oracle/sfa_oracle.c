@@ -11,12 +11,11 @@
  *
  * Sources (the pages this restates):
  *  [QSA]  llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", the paragraphs on
- *         the QSA indexer: "An indexer scores one mean-pooled key per block of
- *         compress_ratio tokens and keeps a budget of the best blocks, plus the tail of
- *         tokens that do not yet form a complete block"; the indexer key cache holds raw
- *         keys (pooling precedes norm and rotation); each head's dot product is rectified
- *         before the sum over heads; the graph expands block scores to tokens so the cut
- *         lands on a block boundary.
+ *         the QSA indexer: one mean-pooled key per block of compress_ratio tokens is scored,
+ *         the best blocks within a budget are kept together with the tail that does not
+ *         fill a block; the indexer key cache holds raw keys (pooling precedes norm and
+ *         rotation); each head's dot product is rectified before the sum over heads; the
+ *         graph expands block scores to tokens so the cut lands on a block boundary.
  *  [SFA]  llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM": attention over a
  *         sparse K/V set with V a view of the first DV dims of K, no ALiBi, no softcap,
  *         index rows padded with -1.
