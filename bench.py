@@ -35,6 +35,7 @@ METRIC = "sparse-attn tokens/s (decode, pp2048) at depth; gathered-KV HBM GB/s v
 DEFAULT_WORKLOAD = "decode_32x131072"
 SECOND_WORKLOAD = "pp2048_131072"
 L2_FLUSH_BYTES = 512 << 20
+HOLD_CYCLES = 2_000_000        # ~1 ms GPU spin that covers the host's enqueue of one step
 CSRC = os.path.join(ROOT, "indexer_selected_sparse_block_gb300", "csrc")
 
 
@@ -203,7 +204,11 @@ class Workbench:
 
 
 def measure(wb, steps, warmup, flush, per_stage=True):
-    """Device time of `steps` steps (L2 flushed before each), plus per-stage averages."""
+    """Device time of `steps` steps (L2 flushed before each), plus per-stage averages.
+
+    Before each timed step the stream is held by a short GPU spin (outside the timed events)
+    so that the host has enqueued the whole step before the first timed event runs: the
+    events then see GPU execution only, not host launch latency."""
     for _ in range(warmup):
         flush.zero_()
         wb.run_step()
@@ -212,6 +217,7 @@ def measure(wb, steps, warmup, flush, per_stage=True):
     step_ms, stage_ms = [], {s: [] for s in stages}
     for _ in range(steps):
         flush.zero_()
+        torch.cuda._sleep(HOLD_CYCLES)
         ev = {s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for s in stages} if per_stage else {}
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -341,6 +347,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-second", action="store_true", help="skip the pp2048 companion line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="override the number of sequences (smaller runs for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -348,6 +356,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = sfa.WORKLOADS[args.workload]
+    if args.seqs:
+        w = w.with_(n_seq=args.seqs, name=f"{w.name}[seqs={args.seqs}]")
     if args.impl == "reference":
         if world > 1:
             import torch.distributed as dist

@@ -162,19 +162,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
         }
         return;
     }
-    const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
-
-    // Q rows of this KV head (rows >= G are zero), swizzled like the K tile.
+    // Q rows of this KV head (rows >= G zero-filled), swizzled like the K tile: copied
+    // asynchronously as the oldest cp.async group, so the copy overlaps the block-list reads
+    // and the first K/V tiles.
     {
         const __nv_bfloat16 *Qg = reinterpret_cast<const __nv_bfloat16 *>(p.Q) +
                                   ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ;
+        const uint32_t qs = smem_u32(sQ);
         for (int e = tid; e < 16 * KCH; e += kThreads) {
             const int r = e / KCH, c = e % KCH;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < G) v = *reinterpret_cast<const uint4 *>(Qg + (int64_t)r * DKQ + c * 8);
-            *reinterpret_cast<uint4 *>(sQ + r * KROW + swz(c, r) * 16) = v;
+            const bool live = r < G;
+            cp_async16(qs + r * KROW + swz(c, r) * 16, live ? Qg + (int64_t)r * DKQ + c * 8 : Qg,
+                       live ? 16u : 0u);
         }
+        cp_async_commit();
     }
+    const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
     __syncthreads();
 
     const __nv_bfloat16 *Kseq = reinterpret_cast<const __nv_bfloat16 *>(p.K) +
@@ -204,11 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
         }
     };
 
-    // prologue: stages-1 tiles in flight
+    // prologue: stages-1 tiles in flight (behind the Q group)
     for (int t = 0; t < p.stages - 1; ++t) {
         if (t < n_tiles) issue_tile(t);
         cp_async_commit();
     }
+    // Q has landed once at most stages-1 younger groups are pending
+    if (p.stages == 2) cp_async_wait<1>();
+    else if (p.stages == 3) cp_async_wait<2>();
+    else cp_async_wait<3>();
+    __syncthreads();
 
     // Q fragments of this warp's head-dim slice (A operand, kept in registers)
     uint32_t qa[KS][4];
@@ -446,31 +454,55 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
     }
 }
 
-// Merges the split partials of one (query, head): grid (n_q * h_q).
+// Merges the split partials of one (query, head): grid (n_q * h_q), 128 threads.  Warp 0
+// turns the splits' (m, l) into merge weights in shared memory; then each thread owns 4
+// consecutive value dims and sums the weighted partials with 16-byte loads.
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p, int dv) {
+    extern __shared__ float s_w[];  // [n_split] weights, then 1/L and M
     const int i = blockIdx.x / p.h_q, h = blockIdx.x % p.h_q;
     const int g = h / p.G, row = h % p.G;
     const int64_t base0 = ((int64_t)i * p.h_kv + g) * p.n_split * p.G + row;
-    float M = -INFINITY;
-    for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, p.part_ml[(base0 + (int64_t)s * p.G) * 2]);
-    float Lsum = 0.f;
-    for (int s = 0; s < p.n_split; ++s) {
-        const int64_t b = base0 + (int64_t)s * p.G;
-        const float m = p.part_ml[b * 2];
-        if (m != -INFINITY) Lsum += exp2f(m - M) * p.part_ml[b * 2 + 1];
-    }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    for (int d = threadIdx.x; d < dv; d += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < p.n_split; ++s) {
+    const int ns = p.n_split;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float M = -INFINITY;
+        for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.part_ml[(base0 + (int64_t)s * p.G) * 2]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float L = 0.f;
+        for (int s = lane; s < ns; s += 32) {
             const int64_t b = base0 + (int64_t)s * p.G;
             const float m = p.part_ml[b * 2];
-            if (m != -INFINITY) acc = fmaf(exp2f(m - M), p.part_o[b * dv + d], acc);
+            const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+            s_w[s] = w;
+            L += w * p.part_ml[b * 2 + 1];
         }
-        p.O[((int64_t)i * p.h_q + h) * dv + d] = acc * inv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        if (lane == 0) {
+            s_w[ns] = L > 0.f ? 1.f / L : 0.f;
+            s_w[ns + 1] = M;
+            if (p.lse) p.lse[(int64_t)i * p.h_q + h] = L > 0.f ? (M + log2f(L)) / kLog2e : -INFINITY;
+        }
     }
-    if (threadIdx.x == 0 && p.lse)
-        p.lse[(int64_t)i * p.h_q + h] = Lsum > 0.f ? (M + log2f(Lsum)) / kLog2e : -INFINITY;
+    __syncthreads();
+    const float inv = s_w[ns];
+    const int64_t stride4 = (int64_t)p.G * dv / 4;   // float4 step between splits
+    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + base0 * dv);
+    float4 *dst = reinterpret_cast<float4 *>(p.O + ((int64_t)i * p.h_q + h) * dv);
+    for (int d4 = threadIdx.x; d4 < dv / 4; d4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int s = 0; s < ns; ++s) {
+            const float w = s_w[s];
+            const float4 v = __ldg(src + s * stride4 + d4);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        dst[d4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -478,11 +510,14 @@ struct SplitPlan {
     int n_split, split_tokens;
 };
 
+// Few (query, KV head) items -> split each list so that the CTAs fill one wave (one CTA per
+// SM: each streams a long run of tiles, so its fixed start-up cost is amortised); many items
+// -> one CTA per item.
 SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max) {
     const int64_t items = (int64_t)n_q * h_kv;
     const int64_t tiles = (n_kv_max + kT - 1) / kT;
-    const int64_t target = 2 * (int64_t)device_sm_count();
-    int64_t ns = (target + items - 1) / items;
+    const int64_t target = (int64_t)device_sm_count();
+    int64_t ns = target / items;
     if (ns > tiles) ns = tiles;
     if (ns < 1) ns = 1;
     const int64_t per = (tiles + ns - 1) / ns;
@@ -578,7 +613,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     }
     if (rc != SFA_OK) return rc;
     if (sp.n_split > 1) {
-        combine_kernel<<<n_q * h_q, 128, 0, st>>>(p, dv);
+        combine_kernel<<<n_q * h_q, 128, (sp.n_split + 2) * sizeof(float), st>>>(p, dv);
         SFA_CHECK_LAUNCH();
     }
     return SFA_OK;

@@ -13,7 +13,8 @@
 // accumulator is read back from tensor memory, so only the final score is written.
 //
 // One CTA = one tile of q_tile queries of one sequence x a run of 128-block tiles.
-//   warp 0      TMA producer: 128 rows x 128 B slabs of Kbar, 128-byte swizzle, S stages
+//   warp 0      TMA producer: one pipeline stage = one 128-row x 128-byte slab of Kbar
+//               (16 KB, 128-byte swizzle); a tile is 2 (d_idx 64) or 4 (d_idx 128) slabs
 //   warp 1      tensor-memory owner and single-thread MMA issuer (M = 128, N = q_tile*H pad 16)
 //   warps 2..5  epilogue: tcgen05.ld (lane = block), ReLU . w, head sum, coalesced stores
 // Two accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs of
@@ -27,7 +28,7 @@ namespace {
 
 constexpr int kBM = 128;               // blocks per tile (MMA M)
 constexpr int kThreads = 192;          // 6 warps
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSlabBytes = kBM * 128;  // one pipeline stage
 
 struct ScoreParams {
     const __nv_bfloat16 *q_idx;
@@ -45,7 +46,7 @@ struct ScoreParams {
 template <int KP>
 struct Layout {
     static constexpr int kSlabs = KP / 64;
-    static constexpr int kABytes = kBM * KP * 2;
+    static constexpr int kABytes = kBM * KP * 2;  // one tile = kSlabs stages
 };
 
 template <int KP, int H>
@@ -57,12 +58,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int S = p.stages, N = p.N;
-    uint8_t *sA = smem;                                    // S x kABytes
-    uint8_t *sB = sA + (size_t)S * L::kABytes;             // N x KP bf16, swizzled
+    uint8_t *sA = smem;                                    // S x kSlabBytes
+    uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x KP bf16, swizzled
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KP * 2);
     uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S,
-             *acc_empty = bars + 2 * S + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+             *acc_empty = bars + 2 * S + 2, *drain = bars + 2 * S + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_nblk = reinterpret_cast<int *>(tmem_slot + 2);  // [q_tile] visible blocks, -1 skip
     float *s_w = reinterpret_cast<float *>(s_nblk + 256);  // [q_tile * H]
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -140,19 +142,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && my_tiles > 0) {
             int issued = 0;
-            for (int it = 0; it < my_tiles && !*abort_flag; ++it) {
+            const int n_loads = my_tiles * L::kSlabs;
+            for (int it = 0; it < n_loads && !*abort_flag; ++it) {
                 const int st = it % S;
                 if (!mbar_wait(&empty[st], ((it / S) & 1) ^ 1, deadline)) {
                     set_status(p.status, SFA_DEV_TIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[st], L::kABytes);
-                const int32_t y = (int32_t)(row0 + (int64_t)(t_begin + it) * kBM);
-                uint8_t *dst = sA + (size_t)st * L::kABytes;
-#pragma unroll
-                for (int sl = 0; sl < L::kSlabs; ++sl)
-                    tma_load_2d(dst + sl * (kBM * 128), &kbar_map, sl * 64, y, &full[st]);
+                mbar_arrive_expect_tx(&full[st], kSlabBytes);
+                const int tile = it / L::kSlabs, sl = it % L::kSlabs;
+                const int32_t y = (int32_t)(row0 + (int64_t)(t_begin + tile) * kBM);
+                tma_load_2d(sA + (size_t)st * kSlabBytes, &kbar_map, sl * 64, y, &full[st]);
                 ++issued;
             }
             // never leave a copy in flight: wait (bounded) for the last load of each stage
@@ -164,29 +165,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && my_tiles > 0) {
             const uint32_t idesc = idesc_bf16_f32(kBM, N);
             const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-            int issued = 0;
-            for (int it = 0; it < my_tiles && !*abort_flag; ++it) {
-                const int st = it % S, acc = it & 1;
-                if (!mbar_wait(&full[st], (it / S) & 1, deadline) ||
-                    !mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, deadline)) {
-                    set_status(p.status, SFA_DEV_TIMEOUT);
-                    *abort_flag = 1;
+            int issued = 0, ld = 0;
+            bool ok = true;
+            for (int it = 0; it < my_tiles && ok && !*abort_flag; ++it) {
+                const int acc = it & 1;
+                if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, deadline)) {
+                    ok = false;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * N);
-                const uint32_t a_st = a0 + st * L::kABytes;
+                for (int sl = 0; sl < L::kSlabs; ++sl, ++ld) {
+                    const int st = ld % S;
+                    if (!mbar_wait(&full[st], (ld / S) & 1, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_st = a0 + st * kSlabBytes;
+                    const uint32_t b_sl = b0 + sl * (N * 128);
 #pragma unroll
-                for (int kk = 0; kk < KP / 16; ++kk) {
-                    const uint64_t ad = sw128_kmajor_desc(a_st + (kk >> 2) * (kBM * 128) + (kk & 3) * 32);
-                    const uint64_t bd = sw128_kmajor_desc(b0 + (kk >> 2) * (N * 128) + (kk & 3) * 32);
-                    tc_mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(d, sw128_kmajor_desc(a_st + kk * 32),
+                                    sw128_kmajor_desc(b_sl + kk * 32), idesc,
+                                    (sl > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty[st]);
                 }
-                tc_commit(&empty[st]);
+                if (!ok) break;
                 tc_commit(&acc_full[acc]);
                 ++issued;
             }
-            if (issued > 0) {  // tensor memory may only be released once the MMAs are done
+            if (!ok) {
+                set_status(p.status, SFA_DEV_TIMEOUT);
+                *abort_flag = 1;
+                tc_commit(drain);  // arrives once every MMA issued so far is done
+                mbar_wait(drain, 0, deadline + kWaitLimitNs);
+            } else if (issued > 0) {  // tensor memory may only be released once the MMAs are done
                 const int last = issued - 1;
                 mbar_wait(&acc_full[last & 1], (last >> 1) & 1, deadline + kWaitLimitNs);
             }
@@ -265,22 +278,27 @@ int pow2_at_least(int v) {
 template <int KP, int H>
 int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
            cudaStream_t stream) {
-    using L = Layout<KP>;
     const size_t b_bytes = (size_t)p.N * KP * 2;
-    int stages = (int)((kSmemBudget - b_bytes) / L::kABytes);
-    stages = stages > 4 ? 4 : stages;
-    if (stages < 1) return SFA_ERR_UNSUPPORTED;
+    // Narrow B tiles (decode) are HBM-bound streams: two CTAs per SM keep more slabs in
+    // flight; wide ones (prefill) are tensor-bound: one CTA per SM with a deep pipeline.
+    const int per_sm = p.N <= 32 ? 2 : 1;
+    const size_t budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
+    const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * H * 4;
+    if (budget < b_bytes + misc + kSlabBytes) return SFA_ERR_UNSUPPORTED;
+    int stages = (int)((budget - b_bytes - misc) / kSlabBytes);
+    if (stages > 16) stages = 16;
     p.stages = stages;
-    const size_t smem = 1024 + (size_t)stages * L::kABytes + b_bytes + 8 * (2 * stages + 4) + 16 +
+    const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes + 8 * (2 * stages + 5) + 8 +
                         256 * 4 + (size_t)p.q_tile * H * 4;
     static bool attr_set = false;
     if (!attr_set) {
         if (!allow_max_dynamic_smem(index_score_kernel<KP, H>)) return SFA_ERR_CUDA;
         attr_set = true;
     }
-    // Spread the block tiles of each query tile over enough CTAs to fill the GPU.
-    const int sms = device_sm_count();
-    int cta_per_qtile = (2 * sms + n_qtiles - 1) / n_qtiles;
+    // One wave: the block tiles of each query tile are split over as many CTAs as the
+    // resident slots allow.
+    const int slots = per_sm * device_sm_count();
+    int cta_per_qtile = slots / n_qtiles;
     if (cta_per_qtile > n_blk_tiles) cta_per_qtile = n_blk_tiles;
     if (cta_per_qtile < 1) cta_per_qtile = 1;
     p.tiles_per_cta = (n_blk_tiles + cta_per_qtile - 1) / cta_per_qtile;

@@ -118,8 +118,13 @@ def test_scores_flag_query_group_violation(dev):
 
 # ------------------------------------------------------------------------------------ top-k
 @pytest.mark.parametrize("top_k", [1, 7, 256, 512, 2048])
-def test_topk_bit_exact(dev, top_k):
-    g = torch.Generator().manual_seed(top_k)
+@pytest.mark.parametrize("pattern", ["coarse", "continuous", "dup_at_cut"])
+def test_topk_bit_exact(dev, top_k, pattern):
+    """Kept sets equal the oracle's full sort exactly, for rows that fit the budget, rows of
+    one chunk and rows cut into chunks; coarse values (many ties: the fallback radix select),
+    continuous values (the two-digit path) and continuous values with a run of exact ties
+    across the cut (ranked by index)."""
+    g = torch.Generator().manual_seed(top_k * 3 + len(pattern))
     cr = 4
     Bs = [0, 1, top_k - 1, top_k, top_k + 1, 3000, 8192, 8193, 20000, 70000]
     Bs = [b for b in Bs if b >= 0]
@@ -127,10 +132,21 @@ def test_topk_bit_exact(dev, top_k):
     q_pos = torch.tensor([b * cr + (i % (cr - 1)) for i, b in enumerate(Bs)], dtype=torch.int32)
     n_blk_max = max(Bs)
     raw = torch.randn((n_q, n_blk_max), generator=g)
-    coarse = torch.round(raw * 4) / 4          # many exact ties
-    coarse[coarse == 0] = -0.0                 # signed zeros must tie with +0.0
-    coarse[1::2, ::3] = 0.0
-    scores = coarse.to(dev)
+    if pattern == "coarse":
+        vals = torch.round(raw * 4) / 4          # many exact ties
+        vals[vals == 0] = -0.0                   # signed zeros must tie with +0.0
+        vals[1::2, ::3] = 0.0
+    elif pattern == "continuous":
+        vals = torch.relu(raw) * 3 + torch.rand((n_q, n_blk_max), generator=g)
+    else:
+        vals = torch.relu(raw) * 3 + torch.rand((n_q, n_blk_max), generator=g)
+        for i, b in enumerate(Bs):
+            if b > top_k:
+                row = vals[i, :b]
+                cut = torch.sort(row, descending=True).values[top_k - 1].item()
+                idx = torch.randperm(b, generator=g)[:40]
+                row[idx] = cut                   # 40 exact copies of the cut value
+    scores = vals.to(dev)
     blk = torch.full((n_q, top_k), -9, dtype=torch.int32, device=dev)
     n_sel = torch.full((n_q,), -9, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -139,7 +155,7 @@ def test_topk_bit_exact(dev, top_k):
     torch.cuda.synchronize()
     assert sfa.sfa_read_device_status(status) == 0
     got, got_n = np32(blk), np32(n_sel)
-    sc = coarse.double().numpy()
+    sc = vals.double().numpy()
     for i in range(n_q):
         B = (int(q_pos[i]) + 1) // cr
         ref, n = oracle.select(sc[i, :B], top_k)
