@@ -513,10 +513,10 @@ struct SplitPlan {
 // Few (query, KV head) items -> split each list so that the CTAs fill one wave (one CTA per
 // SM: each streams a long run of tiles, so its fixed start-up cost is amortised); many items
 // -> one CTA per item.
-SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max) {
+SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max, int per_sm = 2) {
     const int64_t items = (int64_t)n_q * h_kv;
     const int64_t tiles = (n_kv_max + kT - 1) / kT;
-    const int64_t target = (int64_t)device_sm_count();
+    const int64_t target = (int64_t)per_sm * device_sm_count();
     int64_t ns = target / items;
     if (ns > tiles) ns = tiles;
     if (ns < 1) ns = 1;
@@ -533,18 +533,34 @@ bool shape_supported(int dkq, int dv) {
            (dkq == 64 && dv == 64);
 }
 
+// Shared memory of one bf16 CTA: the K/V stages plus Q, the S partials, P (hi, lo), the
+// softmax statistics, the token ids and the block list of its split.
 template <int DKQ, int DV, bool VK>
-int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st) {
+size_t bf16_smem(int stages, int blk_list) {
     constexpr int KROW = DKQ * 2, VROW = VK ? KROW : DV * 2;
     constexpr int STAGE = kT * KROW + (VK ? 0 : kT * VROW);
-    const size_t fixed = 16 * KROW + 4 * 16 * (kT + 8) * 4 + 2 * 16 * (kT + 8) * 2 + 48 * 4 +
-                        kMaxBlkList * 4 + 4 * kT * 4 + 256;
-    int stages = (int)((227 * 1024 - fixed) / STAGE);
-    if (stages > 4) stages = 4;
-    if (stages < 2) return SFA_ERR_UNSUPPORTED;
+    return (size_t)stages * STAGE + 16 * KROW + 4 * 16 * (kT + 8) * 4 + 2 * 16 * (kT + 8) * 2 +
+           48 * 4 + (size_t)stages * kT * 4 + (size_t)blk_list * 4 + 16;
+}
+
+// Two CTAs per SM when two stages fit in half the shared memory (more warps to hide the
+// latency of each tile's dependent steps), else one CTA with up to four stages.
+template <int DKQ, int DV, bool VK>
+int bf16_per_sm(int blk_list) {
+    return bf16_smem<DKQ, DV, VK>(2, blk_list) <= 113 * 1024 ? 2 : 1;
+}
+
+template <int DKQ, int DV, bool VK>
+int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
+    int stages = 2;
+    if (bf16_per_sm<DKQ, DV, VK>(blk_list) == 1) {
+        stages = 4;
+        while (stages > 2 && bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) --stages;
+    }
+    if (bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
     AttnParams q = p;
     q.stages = stages;
-    const size_t smem = fixed + (size_t)stages * STAGE;
+    const size_t smem = bf16_smem<DKQ, DV, VK>(stages, blk_list);
     static bool attr = false;
     if (!attr) {
         if (!allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
@@ -574,7 +590,16 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
-    const SplitPlan sp = plan_split(n_q, h_kv, n_kv_max);
+    // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
+    int per_sm = 1;
+    if (dtype == SFA_BF16) {
+        const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
+        if (dkq == 576) per_sm = bf16_per_sm<576, 512, true>(bl_max);
+        else if (dkq == 512) per_sm = V ? bf16_per_sm<512, 512, false>(bl_max) : bf16_per_sm<512, 512, true>(bl_max);
+        else if (dkq == 128) per_sm = V ? bf16_per_sm<128, 128, false>(bl_max) : bf16_per_sm<128, 128, true>(bl_max);
+        else per_sm = V ? bf16_per_sm<64, 64, false>(bl_max) : bf16_per_sm<64, 64, true>(bl_max);
+    }
+    const SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm);
     const size_t need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max);
     if (need > 0 && (!ws || ws_bytes < need)) return SFA_ERR_WORKSPACE;
 
@@ -597,13 +622,14 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         p.part_ml = p.part_o + n_rows * dv;
     }
     if (!dense && (int64_t)sp.split_tokens / cr + 2 > kMaxBlkList) return SFA_ERR_UNSUPPORTED;
+    const int bl = dense ? 0 : sp.split_tokens / cr + 2;   // block-list entries a split needs
     const dim3 grid(sp.n_split, h_kv, n_q);
     int rc;
     if (dtype == SFA_BF16) {
-        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true>(p, grid, st);
-        else if (dkq == 512) rc = V ? launch_bf16<512, 512, false>(p, grid, st) : launch_bf16<512, 512, true>(p, grid, st);
-        else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st) : launch_bf16<128, 128, true>(p, grid, st);
-        else rc = V ? launch_bf16<64, 64, false>(p, grid, st) : launch_bf16<64, 64, true>(p, grid, st);
+        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true>(p, grid, st, bl);
+        else if (dkq == 512) rc = V ? launch_bf16<512, 512, false>(p, grid, st, bl) : launch_bf16<512, 512, true>(p, grid, st, bl);
+        else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
+        else rc = V ? launch_bf16<64, 64, false>(p, grid, st, bl) : launch_bf16<64, 64, true>(p, grid, st, bl);
     } else {
         if (dkq == 576) attend_f32_kernel<576, 512><<<grid, kThreads, 0, st>>>(p);
         else if (dkq == 512) attend_f32_kernel<512, 512><<<grid, kThreads, 0, st>>>(p);
@@ -624,7 +650,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
 
 extern "C" size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max) {
     if (n_q <= 0 || h_q <= 0 || h_kv <= 0 || dv <= 0 || n_kv_max <= 0) return 0;
-    const sfa::SplitPlan sp = sfa::plan_split(n_q, h_kv, n_kv_max);
+    const sfa::SplitPlan sp = sfa::plan_split(n_q, h_kv, n_kv_max, 2);  // the largest plan
     if (sp.n_split <= 1) return 0;
     return (size_t)n_q * h_q * sp.n_split * ((size_t)dv + 2) * sizeof(float);
 }
