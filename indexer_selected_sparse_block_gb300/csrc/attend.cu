@@ -387,6 +387,412 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// tcgen05 kernel for the MLA / 512-wide heads (DKQ 576 or 512, DV 512).  One CTA = one query x
+// one KV head x one split of its list, 12 warps:
+//   warps 8-11  producers, two groups of two warps taking alternate tiles: 16-byte cp.async
+//               gathers of TT selected token rows into the 128-byte-swizzled K-major layout
+//               (one 64-wide slab of the head dim per TT x 128 B block); each group waits for
+//               its own copies, fences them for the tensor cores and publishes the tile, so
+//               the next tile's gather is already in flight; Q once at the start;
+//   warp 6      tensor-memory owner and single-thread MMA issuer:
+//                 S^T[TT tokens x 16 heads]  = K_tile (A, K-major) x Q^T (B, K-major)
+//                 O^T[512 dv x 16 heads]    += V^T (A, MN-major: the same K tile when V is
+//                                              the first 512 dims of K) x P^T (B, K-major),
+//               P carried as bf16 hi + lo (two MMAs), M = 128 (rows past TT of the S MMA are
+//               not used);
+//   warps 4-5   softmax (TMEM lanes 0..63 = tokens): S from tensor memory through shared
+//               memory, per-head running max / sum, P^T hi/lo into shared memory;
+//   warps 0-3   correction (TMEM lanes 0..127 = value dims): O kept in registers,
+//               O = O * alpha + P V per tile, normalised (or written as a split partial).
+// S and O tensor-memory buffers and the P buffers are double-buffered, so the MMAs of tile
+// t + 1 overlap the softmax and correction of tile t.  Every wait is bounded.
+namespace tc {
+constexpr int kThreads = 384;
+constexpr int kProdWarp0 = 8, kProdThreads = 128, kGroupThreads = 64;
+constexpr int kSoftWarp0 = 4, kSoftThreads = 64;
+constexpr int kMmaWarp = 6;
+constexpr int kStages = 2;
+constexpr int kTmemCols = 256;  // S: 2 x 16, O: 2 x 64
+constexpr int kSPitch = 17;     // floats per token row of the S staging area
+}  // namespace tc
+
+template <int DKQ, int DV, bool V_IS_K, int TT>
+struct TcLayout {
+    static constexpr int kSlabK = DKQ / 64;                   // 64-wide slabs of K
+    static constexpr int kSlabV = V_IS_K ? 0 : DV / 64;       // separate V slabs
+    static constexpr int kSlabBytes = TT * 128;               // TT rows x 128 B
+    static constexpr int kStageBytes = (kSlabK + kSlabV) * kSlabBytes;
+    static constexpr int kPad = 128 * 128 - kSlabBytes;       // the M=128 S MMA reads 128 rows
+    static constexpr int kQBytes = kSlabK * 16 * 128;         // B operand: 16 rows per slab
+    static constexpr int kPBytes = 16 * 128;                  // one P^T half (16 x 64 tokens)
+    // offsets from the 1024-aligned base
+    static constexpr int kOffStages = 0;
+    static constexpr int kOffQ = tc::kStages * kStageBytes + kPad;
+    static constexpr int kOffP = kOffQ + kQBytes;                         // [2 buf][hi, lo]
+    static constexpr int kOffS = kOffP + 4 * kPBytes;                     // TT x kSPitch f32
+    static constexpr int kOffAlpha = kOffS + TT * tc::kSPitch * 4;        // [2][16]
+    static constexpr int kOffStat = kOffAlpha + 2 * 16 * 4;               // m[16], l[16]
+    static constexpr int kOffBar = kOffStat + 32 * 4;                     // mbarriers
+    static constexpr int kNumBars = 2 * tc::kStages + 2 * 6 + 4;
+    static constexpr int kOffTok = kOffBar + kNumBars * 8 + 16;           // [stages][TT]
+    static constexpr int kOffBlk = kOffTok + tc::kStages * TT * 4;
+    static constexpr size_t bytes(int blk_list) { return 1024 + kOffBlk + (size_t)blk_list * 4 + 16; }
+};
+
+template <int DKQ, int DV, bool V_IS_K, int TT>
+__global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnParams p) {
+    using Lay = TcLayout<DKQ, DV, V_IS_K, TT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sStage = smem + Lay::kOffStages;
+    uint8_t *sQ = smem + Lay::kOffQ;
+    uint8_t *sP = smem + Lay::kOffP;
+    float *sS = reinterpret_cast<float *>(smem + Lay::kOffS);
+    float *sAlpha = reinterpret_cast<float *>(smem + Lay::kOffAlpha);
+    float *sStat = reinterpret_cast<float *>(smem + Lay::kOffStat);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
+    uint64_t *full = bars, *empty = bars + tc::kStages;
+    uint64_t *s_full = bars + 2 * tc::kStages, *s_empty = s_full + 2;
+    uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
+    uint64_t *o_full = p_empty + 2, *o_empty = o_full + 2;
+    uint64_t *q_ready = o_empty + 2, *stats_ready = q_ready + 1, *drain = q_ready + 2;
+    uint64_t *soft_bar = q_ready + 3;   // the softmax threads' own (bounded) barrier
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *sTok = reinterpret_cast<int *>(smem + Lay::kOffTok);
+    int *sBlk = reinterpret_cast<int *>(smem + Lay::kOffBlk);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
+    const ListInfo L = list_info(p, i, split == 0 && g == 0 && tid == 0);
+    const int j0 = split * p.split_tokens;
+    const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
+    const int G = p.G;
+
+    if (j0 >= j1) {  // nothing to attend in this split
+        for (int e = tid; e < G * DV; e += tc::kThreads) {
+            const int row = e / DV, d = e % DV;
+            const int h = g * G + row;
+            if (p.n_split == 1) {
+                p.O[((int64_t)i * p.h_q + h) * DV + d] = 0.f;
+                if (d == 0 && p.lse) p.lse[(int64_t)i * p.h_q + h] = -INFINITY;
+            } else {
+                const int64_t base = (((int64_t)i * p.h_kv + g) * p.n_split + split) * G + row;
+                p.part_o[base * DV + d] = 0.f;
+                if (d == 0) {
+                    p.part_ml[base * 2] = -INFINITY;
+                    p.part_ml[base * 2 + 1] = 0.f;
+                }
+            }
+        }
+        return;
+    }
+    const int n_tiles = (j1 - j0 + TT - 1) / TT;
+    const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+
+    // ------------------------------------------------------------------ set-up
+    if (tid == 0) {
+        for (int s = 0; s < tc::kStages; ++s) {
+            mbar_init(&full[s], tc::kGroupThreads);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_empty[b], 2);      // the two softmax warps
+            mbar_init(&p_full[b], 2);
+            mbar_init(&p_empty[b], 1 + 4);  // the PV commit + the four correction warps
+            mbar_init(&o_full[b], 1);
+            mbar_init(&o_empty[b], 4);
+        }
+        mbar_init(q_ready, tc::kProdThreads);
+        mbar_init(stats_ready, 2);
+        mbar_init(drain, 1);
+        mbar_init(soft_bar, tc::kSoftThreads);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == tc::kMmaWarp) {
+        tmem_alloc(tmem_slot, tc::kTmemCols);
+        tmem_relinquish();
+    }
+    const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 32;  // S: cols [0, 32), O: cols [32, 160)
+
+    auto fail = [&]() {
+        set_status(p.status, SFA_DEV_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp >= tc::kProdWarp0) {
+        // ------------------------------------------------------------ producers
+        const int pt = tid - tc::kProdWarp0 * 32;   // 0..127
+        constexpr int KCH = DKQ / 8, VCH = DV / 8;
+        const __nv_bfloat16 *Kseq = reinterpret_cast<const __nv_bfloat16 *>(p.K) +
+                                    (int64_t)L.seq * p.k_seq_stride + (int64_t)g * DKQ;
+        const __nv_bfloat16 *Vseq = V_IS_K ? Kseq
+                                           : reinterpret_cast<const __nv_bfloat16 *>(p.V) +
+                                                 (int64_t)L.seq * p.v_seq_stride + (int64_t)g * DV;
+        {   // Q^T operand: 16 rows (heads; rows >= G zero) x DKQ, one slab per 64 dims
+            const __nv_bfloat16 *Qg = reinterpret_cast<const __nv_bfloat16 *>(p.Q) +
+                                      ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ;
+            const uint32_t qs = smem_u32(sQ);
+            for (int e = pt; e < 16 * KCH; e += tc::kProdThreads) {
+                const int r = e / KCH, c = e % KCH;
+                const bool live = r < G;
+                cp_async16(qs + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                           live ? Qg + (int64_t)r * DKQ + c * 8 : Qg, live ? 16u : 0u);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(q_ready);
+        }
+        // group pg takes tiles t = pg, pg + 2, ... (stage t % 2 == pg)
+        const int pg = pt / tc::kGroupThreads, gt = pt % tc::kGroupThreads;
+        constexpr int PER_ROW = tc::kGroupThreads / TT;      // threads per token row
+        const int r = gt % TT, part = gt / TT;
+        for (int t = pg; t < n_tiles; t += 2) {
+            const int st = t % tc::kStages;
+            if (*abort_flag) break;
+            if (!mbar_wait(&empty[st], ((t / tc::kStages) & 1) ^ 1, deadline)) { fail(); break; }
+            const uint32_t dk = smem_u32(sStage + (size_t)st * Lay::kStageBytes);
+            const int tok = token_at(p, L, j0 + t * TT + r, j1, sBlk, jb0);
+            if (part == 0) sTok[st * TT + r] = tok;
+            const uint32_t nbytes = tok >= 0 ? 16u : 0u;
+            const __nv_bfloat16 *srcK = tok >= 0 ? Kseq + (int64_t)tok * p.k_tok_stride : Kseq;
+            for (int c = part; c < KCH; c += PER_ROW)
+                cp_async16(dk + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                           srcK + c * 8, nbytes);
+            if constexpr (!V_IS_K) {
+                const __nv_bfloat16 *srcV = tok >= 0 ? Vseq + (int64_t)tok * p.v_tok_stride : Vseq;
+                const uint32_t dv0 = dk + Lay::kSlabK * Lay::kSlabBytes;
+                for (int c = part; c < VCH; c += PER_ROW)
+                    cp_async16(dv0 + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                               srcV + c * 8, nbytes);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full[st]);
+        }
+    } else if (warp == tc::kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(128, 16);
+            const uint32_t idPV = idesc_bf16_f32(128, 16) | (1u << 15);   // A (V^T) MN-major
+            const uint32_t st0 = smem_u32(sStage), q0 = smem_u32(sQ), p0 = smem_u32(sP);
+            bool ok = mbar_wait(q_ready, 0, deadline);
+            auto issue_pv = [&](int u) -> bool {
+                const int st = u % tc::kStages, b = u & 1;
+                if (!mbar_wait(&p_full[b], (u >> 1) & 1, deadline)) return false;
+                if (!mbar_wait(&o_empty[b], ((u >> 1) & 1) ^ 1, deadline)) return false;
+                tc_fence_after();
+                const uint32_t vbase = st0 + st * Lay::kStageBytes + (V_IS_K ? 0 : Lay::kSlabK * Lay::kSlabBytes);
+                const uint32_t ph = p0 + (b * 2) * Lay::kPBytes, pl = ph + Lay::kPBytes;
+#pragma unroll
+                for (int mt = 0; mt < DV / 128; ++mt) {
+                    const uint32_t d = tO + b * 64 + mt * 16;
+#pragma unroll
+                    for (int kk = 0; kk < TT / 16; ++kk) {
+                        const uint64_t a = sw128_desc(vbase + 2 * mt * Lay::kSlabBytes + kk * 2048,
+                                                      Lay::kSlabBytes, 1024);
+                        tc_mma_bf16(d, a, sw128_desc(ph + kk * 32, 16, 1024), idPV, kk > 0 ? 1u : 0u);
+                        tc_mma_bf16(d, a, sw128_desc(pl + kk * 32, 16, 1024), idPV, 1u);
+                    }
+                }
+                tc_commit(&o_full[b]);
+                tc_commit(&empty[st]);
+                tc_commit(&p_empty[b]);
+                return true;
+            };
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                if (*abort_flag) { ok = false; break; }
+                const int st = t % tc::kStages, b = t & 1;
+                if (!mbar_wait(&full[st], (t / tc::kStages) & 1, deadline) ||
+                    !mbar_wait(&s_empty[b], ((t >> 1) & 1) ^ 1, deadline)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t kbase = st0 + st * Lay::kStageBytes;
+#pragma unroll 1
+                for (int s = 0; s < Lay::kSlabK; ++s) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(tS + b * 16,
+                                    sw128_desc(kbase + s * Lay::kSlabBytes + kk * 32, 16, 1024),
+                                    sw128_desc(q0 + s * 2048 + kk * 32, 16, 1024), idS,
+                                    (s > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&s_full[b]);
+                if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+            }
+            if (ok && !issue_pv(n_tiles - 1)) ok = false;
+            if (!ok) fail();
+        }
+    } else if (warp >= tc::kSoftWarp0 && warp < tc::kSoftWarp0 + 2) {
+        // ------------------------------------------------------------ softmax (64 threads)
+        const int sid = tid - tc::kSoftWarp0 * 32;        // 0..63: TMEM lane / token row
+        const int h = sid >> 2, q = sid & 3;              // head-major phase: head, quarter
+        constexpr int TPQ = TT / 4;                       // tokens per quarter
+        float m_run = -INFINITY, l_run = 0.f;             // of head h (the 4 threads agree)
+        uint32_t soft_phase = 0;
+        auto soft_sync = [&]() -> bool {   // all 64 softmax threads, bounded
+            mbar_arrive(soft_bar);
+            const bool done = mbar_wait(soft_bar, soft_phase, deadline);
+            soft_phase ^= 1;
+            return done;
+        };
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % tc::kStages, b = t & 1;
+            if (*abort_flag) break;
+            if (!mbar_wait(&s_full[b], (t >> 1) & 1, deadline) ||
+                !mbar_wait(&full[st], (t / tc::kStages) & 1, deadline)) { fail(); break; }
+            tc_fence_after();
+            uint32_t r[16];
+            tmem_ld16(tS + b * 16 + ((uint32_t)((warp & 3) * 32) << 16), r);
+            tmem_ld_wait();
+            if (sid < TT) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) sS[sid * tc::kSPitch + c] = __uint_as_float(r[c]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[b]);
+            if (!soft_sync()) { fail(); break; }
+            // head h, tokens [q*TPQ, (q+1)*TPQ)
+            float sv[TPQ], mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < TPQ; ++e) {
+                const int tk = q * TPQ + e;
+                const float v = sS[tk * tc::kSPitch + h] * p.scale_log2;
+                sv[e] = sTok[st * TT + tk] >= 0 ? v : -INFINITY;
+                mx = fmaxf(mx, sv[e]);
+            }
+            if (!soft_sync()) { fail(); break; }    // the S staging area may be refilled now
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+            float rs = 0.f;
+            uint32_t hi[TPQ / 2], lo[TPQ / 2];
+#pragma unroll
+            for (int e = 0; e < TPQ; e += 2) {
+                const float p0 = m_new == -INFINITY ? 0.f : exp2f(sv[e] - m_new);
+                const float p1 = m_new == -INFINITY ? 0.f : exp2f(sv[e + 1] - m_new);
+                rs += p0 + p1;
+                const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
+                hi[e / 2] = pack_bf16(h0, h1);
+                lo[e / 2] = pack_bf16(p0 - h0, p1 - h1);
+            }
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
+            l_run = l_run * alpha + rs;
+            m_run = m_new;
+            // P^T rows (head h) of this buffer: wait until the PV two tiles back is done
+            if (!mbar_wait(&p_empty[b], ((t >> 1) & 1) ^ 1, deadline)) { fail(); break; }
+            uint8_t *ph = sP + (b * 2) * Lay::kPBytes, *pl = ph + Lay::kPBytes;
+#pragma unroll
+            for (int cc = 0; cc < TPQ / 8; ++cc) {      // 16-byte chunks of 8 tokens
+                const int chunk = (q * TPQ) / 8 + cc;
+                const int off = h * 128 + ((chunk ^ (h & 7)) << 4);
+                *reinterpret_cast<uint4 *>(ph + off) =
+                    make_uint4(hi[cc * 4], hi[cc * 4 + 1], hi[cc * 4 + 2], hi[cc * 4 + 3]);
+                *reinterpret_cast<uint4 *>(pl + off) =
+                    make_uint4(lo[cc * 4], lo[cc * 4 + 1], lo[cc * 4 + 2], lo[cc * 4 + 3]);
+            }
+            if (q == 0) sAlpha[b * 16 + h] = alpha;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[b]);
+        }
+        if (q == 0) {
+            sStat[h] = m_run;
+            sStat[16 + h] = l_run;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stats_ready);
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ correction (128 thr)
+        float o[DV / 128][16];
+#pragma unroll
+        for (int mt = 0; mt < DV / 128; ++mt)
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[mt][c] = 0.f;
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int b = t & 1;
+            if (*abort_flag) { ok = false; break; }
+            if (!mbar_wait(&o_full[b], (t >> 1) & 1, deadline) ||
+                !mbar_wait(&p_full[b], (t >> 1) & 1, deadline)) { fail(); ok = false; break; }
+            tc_fence_after();
+            float al[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) al[c] = sAlpha[b * 16 + c];
+#pragma unroll
+            for (int mt = 0; mt < DV / 128; ++mt) {
+                uint32_t r[16];
+                tmem_ld16(tO + b * 64 + mt * 16 + lane_addr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) o[mt][c] = fmaf(o[mt][c], al[c], __uint_as_float(r[c]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&o_empty[b]);
+                mbar_arrive(&p_empty[b]);
+            }
+        }
+        if (ok && mbar_wait(stats_ready, 0, deadline)) {
+            const int dv_base = warp * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                if (c >= G) break;
+                const int h = g * G + c;
+                const float m = sStat[c], l = sStat[16 + c];
+                if (p.n_split == 1) {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    float *dst = p.O + ((int64_t)i * p.h_q + h) * DV + dv_base;
+#pragma unroll
+                    for (int mt = 0; mt < DV / 128; ++mt) dst[mt * 128] = o[mt][c] * inv;
+                    if (p.lse && dv_base == 0)
+                        p.lse[(int64_t)i * p.h_q + h] = l > 0.f ? (m + log2f(l)) / kLog2e : -INFINITY;
+                } else {
+                    const int64_t base = (((int64_t)i * p.h_kv + g) * p.n_split + split) * G + c;
+                    float *dst = p.part_o + base * DV + dv_base;
+#pragma unroll
+                    for (int mt = 0; mt < DV / 128; ++mt) dst[mt * 128] = o[mt][c];
+                    if (dv_base == 0) {
+                        p.part_ml[base * 2] = m;
+                        p.part_ml[base * 2 + 1] = l;
+                    }
+                }
+            }
+        } else if (ok) {
+            fail();
+        }
+    }
+
+    // ------------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == tc::kMmaWarp) {
+        if (*abort_flag && lane == 0) {   // all issued MMAs must finish before TMEM goes
+            tc_commit(drain);
+            mbar_wait(drain, 0, global_timer_ns() + kWaitLimitNs);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, tc::kTmemCols);
+    }
+}
+
 // fp32 inputs: plain SIMT online softmax, one head per 8 threads (accuracy path).
 template <int DKQ, int DV>
 __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p) {
@@ -513,16 +919,16 @@ struct SplitPlan {
 // Few (query, KV head) items -> split each list so that the CTAs fill one wave (one CTA per
 // SM: each streams a long run of tiles, so its fixed start-up cost is amortised); many items
 // -> one CTA per item.
-SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max, int per_sm = 2) {
+SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max, int per_sm = 2, int tile = kT) {
     const int64_t items = (int64_t)n_q * h_kv;
-    const int64_t tiles = (n_kv_max + kT - 1) / kT;
+    const int64_t tiles = (n_kv_max + tile - 1) / tile;
     const int64_t target = (int64_t)per_sm * device_sm_count();
     int64_t ns = target / items;
     if (ns > tiles) ns = tiles;
     if (ns < 1) ns = 1;
     const int64_t per = (tiles + ns - 1) / ns;
     SplitPlan sp;
-    sp.split_tokens = (int)(per * kT);
+    sp.split_tokens = (int)(per * tile);
     sp.n_split = (int)((tiles + per - 1) / per);
     if (sp.n_split < 1) sp.n_split = 1;
     return sp;
@@ -571,6 +977,20 @@ int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     return SFA_OK;
 }
 
+template <int DKQ, int DV, bool VK, int TT>
+int launch_tc(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
+    const size_t smem = TcLayout<DKQ, DV, VK, TT>::bytes(blk_list);
+    if (smem > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    static bool attr = false;
+    if (!attr) {
+        if (!allow_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK, TT>)) return SFA_ERR_CUDA;
+        attr = true;
+    }
+    attend_tc_kernel<DKQ, DV, VK, TT><<<grid, tc::kThreads, smem, st>>>(p);
+    SFA_CHECK_LAUNCH();
+    return SFA_OK;
+}
+
 int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
                int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv, float scale,
                const int32_t *q_seq, const int32_t *q_pos, const int32_t *blk_idx,
@@ -590,16 +1010,20 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
+    // The 512-wide heads take the tcgen05 kernel (one CTA per SM; 64-token tiles, or 32 when
+    // V is separate); the narrow test shapes and fp32 inputs take the warp-level kernels.
+    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512);
+    const int tc_tile = V ? 32 : 64;
     // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
     int per_sm = 1;
-    if (dtype == SFA_BF16) {
+    if (dtype == SFA_BF16 && !use_tc) {
         const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
         if (dkq == 576) per_sm = bf16_per_sm<576, 512, true>(bl_max);
         else if (dkq == 512) per_sm = V ? bf16_per_sm<512, 512, false>(bl_max) : bf16_per_sm<512, 512, true>(bl_max);
         else if (dkq == 128) per_sm = V ? bf16_per_sm<128, 128, false>(bl_max) : bf16_per_sm<128, 128, true>(bl_max);
         else per_sm = V ? bf16_per_sm<64, 64, false>(bl_max) : bf16_per_sm<64, 64, true>(bl_max);
     }
-    const SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm);
+    const SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, use_tc ? tc_tile : kT);
     const size_t need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max);
     if (need > 0 && (!ws || ws_bytes < need)) return SFA_ERR_WORKSPACE;
 
@@ -625,10 +1049,11 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     const int bl = dense ? 0 : sp.split_tokens / cr + 2;   // block-list entries a split needs
     const dim3 grid(sp.n_split, h_kv, n_q);
     int rc;
-    if (dtype == SFA_BF16) {
-        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true>(p, grid, st, bl);
-        else if (dkq == 512) rc = V ? launch_bf16<512, 512, false>(p, grid, st, bl) : launch_bf16<512, 512, true>(p, grid, st, bl);
-        else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
+    if (use_tc) {
+        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_tc<576, 512, true, 64>(p, grid, st, bl);
+        else rc = V ? launch_tc<512, 512, false, 32>(p, grid, st, bl) : launch_tc<512, 512, true, 64>(p, grid, st, bl);
+    } else if (dtype == SFA_BF16) {
+        if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
         else rc = V ? launch_bf16<64, 64, false>(p, grid, st, bl) : launch_bf16<64, 64, true>(p, grid, st, bl);
     } else {
         if (dkq == 576) attend_f32_kernel<576, 512><<<grid, kThreads, 0, st>>>(p);
