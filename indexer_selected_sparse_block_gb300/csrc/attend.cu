@@ -23,6 +23,8 @@
 // partial (O, m, l) are merged by combine_kernel.  fp32 inputs take a plain SIMT kernel with
 // the same split/merge structure (accuracy reference path).
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -389,76 +391,162 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
 
 // ---------------------------------------------------------------------------------------
 // tcgen05 kernel for the MLA / 512-wide heads (DKQ 576 or 512, DV 512).  One CTA = one query x
-// one KV head x one split of its list, 12 warps:
-//   warps 8-11  producers, two groups of two warps taking alternate tiles: 16-byte cp.async
-//               gathers of TT selected token rows into the 128-byte-swizzled K-major layout
-//               (one 64-wide slab of the head dim per TT x 128 B block); each group waits for
-//               its own copies, fences them for the tensor cores and publishes the tile, so
-//               the next tile's gather is already in flight; Q once at the start;
-//   warp 6      tensor-memory owner and single-thread MMA issuer:
-//                 S^T[TT tokens x 16 heads]  = K_tile (A, K-major) x Q^T (B, K-major)
-//                 O^T[512 dv x 16 heads]    += V^T (A, MN-major: the same K tile when V is
-//                                              the first 512 dims of K) x P^T (B, K-major),
-//               P carried as bf16 hi + lo (two MMAs), M = 128 (rows past TT of the S MMA are
-//               not used);
-//   warps 4-5   softmax (TMEM lanes 0..63 = tokens): S from tensor memory through shared
-//               memory, per-head running max / sum, P^T hi/lo into shared memory;
-//   warps 0-3   correction (TMEM lanes 0..127 = value dims): O kept in registers,
-//               O = O * alpha + P V per tile, normalised (or written as a split partial).
-// S and O tensor-memory buffers and the P buffers are double-buffered, so the MMAs of tile
-// t + 1 overlap the softmax and correction of tile t.  Every wait is bounded.
+// one KV head x one split of its list; the list is cut into 32-token tiles that stream
+// through a ring of NR stages (NR = 4, or 2 when V is separate and the stages are twice as
+// large).  Within each 64-wide slab of the head dim the ring's rows are contiguous (tile t
+// sits at rows 32 * (t % NR) ...), so one M = 128 MMA over the ring scores every tile in it
+// at once.  Warp roles (9 warps):
+//   warps 5-8   producers (one per SM sub-partition): Q once (cp.async), then 8 rows of
+//               every tile each, as 4-row groups: a group of 4 consecutive tokens (a kept
+//               block of cr = 4, half of one of cr = 8, the tail, the dense case) is one TMA
+//               box per 64-wide slab, landing 128-byte-swizzled in the K-major layout with
+//               its bytes counted on the stage's barrier; any other group (the ragged end of
+//               the list, a dropped block) is copied row by row with zero-filling cp.async,
+//               waited for and fenced into the async proxy by the producer itself;
+//   warp 4      tensor-memory owner and single-thread MMA issuer.  It groups the landed,
+//               not yet scored tiles into a batch (two at least, unless the list ends;
+//               the whole ring at most) and issues
+//                 S^T[128 ring rows x 16 heads] = ring (A, K-major) x Q^T (B, K-major),
+//               then, once the batch's P is ready, for each 128-wide slice of DV
+//                 O^T[128 dv x 32] = V^T (A, MN-major; the K rows when V is the first 512
+//                                    dims of K) x [P_hi | P_lo]^T (B, K-major, N = 32),
+//               P carried as bf16 hi + lo in one MMA and the halves summed on read-out;
+//               the stages of a batch are released when its PV MMAs complete;
+//   warps 0-3   softmax and correction.  Warp s reads the S rows of ring stage s (TMEM lanes
+//               32s ..); per-head max and sum are reduced across the batch through shared
+//               memory and P^T hi/lo is written at the tokens' ring positions.  The same
+//               warps own the value dims 32s .. of every 128-wide slice of O (TMEM lanes of
+//               the PV result) and keep O in registers: after the softmax of batch b they
+//               fold in batch b - 1 (O = O * alpha + P_hi V + P_lo V) while the tensor cores
+//               run the PV of batch b; O is normalised at the end (or written as a split
+//               partial).
+// S, P and O are double-buffered per batch, so the MMAs of batch b + 1 overlap the softmax
+// and correction of batch b.  Staging the ring through TMA (the async proxy) keeps generic
+// copies out of flight, so the proxy fence that publishes P stays cheap.  Every wait is
+// bounded.
 namespace tc {
-constexpr int kThreads = 384;
-constexpr int kProdWarp0 = 8, kProdThreads = 128, kGroupThreads = 64;
-constexpr int kSoftWarp0 = 4, kSoftThreads = 64;
-constexpr int kMmaWarp = 6;
-constexpr int kStages = 2;
-constexpr int kTmemCols = 256;  // S: 2 x 16, O: 2 x 64
-constexpr int kSPitch = 17;     // floats per token row of the S staging area
+constexpr int kThreads = 288;
+constexpr int kMmaWarp = 4, kProdWarp0 = 5;
+constexpr int kProdThreads = 128;
+constexpr int kTT = 32;          // tokens per tile (ring stage)
+constexpr int kBatchMin = 2;     // tiles an S / PV batch waits for (at most the whole ring)
+constexpr int kTmemCols = 512;   // S: 2 x 16, O: 2 x (4 x 32); one CTA per SM
 }  // namespace tc
 
-template <int DKQ, int DV, bool V_IS_K, int TT>
+template <int DKQ, int DV, bool V_IS_K>
 struct TcLayout {
+    static constexpr int kNR = V_IS_K ? 4 : 2;                // ring stages
+    static constexpr int kRingRows = kNR * tc::kTT;
     static constexpr int kSlabK = DKQ / 64;                   // 64-wide slabs of K
     static constexpr int kSlabV = V_IS_K ? 0 : DV / 64;       // separate V slabs
-    static constexpr int kSlabBytes = TT * 128;               // TT rows x 128 B
-    static constexpr int kStageBytes = (kSlabK + kSlabV) * kSlabBytes;
-    static constexpr int kPad = 128 * 128 - kSlabBytes;       // the M=128 S MMA reads 128 rows
+    static constexpr int kSlabBytes = kRingRows * 128;        // ring rows x 128 B
+    static constexpr int kRingBytes = (kSlabK + kSlabV) * kSlabBytes;
     static constexpr int kQBytes = kSlabK * 16 * 128;         // B operand: 16 rows per slab
-    static constexpr int kPBytes = 16 * 128;                  // one P^T half (16 x 64 tokens)
-    // offsets from the 1024-aligned base
-    static constexpr int kOffStages = 0;
-    static constexpr int kOffQ = tc::kStages * kStageBytes + kPad;
-    static constexpr int kOffP = kOffQ + kQBytes;                         // [2 buf][hi, lo]
-    static constexpr int kOffS = kOffP + 4 * kPBytes;                     // TT x kSPitch f32
-    static constexpr int kOffAlpha = kOffS + TT * tc::kSPitch * 4;        // [2][16]
-    static constexpr int kOffStat = kOffAlpha + 2 * 16 * 4;               // m[16], l[16]
-    static constexpr int kOffBar = kOffStat + 32 * 4;                     // mbarriers
-    static constexpr int kNumBars = 2 * tc::kStages + 2 * 6 + 4;
-    static constexpr int kOffTok = kOffBar + kNumBars * 8 + 16;           // [stages][TT]
-    static constexpr int kOffBlk = kOffTok + tc::kStages * TT * 4;
+    static constexpr int kPRegion = 32 * 128;                 // 32 rows (hi, lo) x 64 tokens
+    static constexpr int kPBuf = ((kRingRows + 63) / 64) * kPRegion;
+    // the S MMA reads 128 rows from each slab start; past the ring they fall in Q and P
+    static_assert(kQBytes + 2 * kPBuf >= (128 - kRingRows) * 128, "over-read stays in the CTA");
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffQ = kRingBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;                         // [2][kPBuf]
+    static constexpr int kOffRed = kOffP + 2 * kPBuf;                     // max, sum [4][16]
+    static constexpr int kOffAlpha = kOffRed + 2 * 4 * 16 * 4;            // [2][16]
+    static constexpr int kOffL = kOffAlpha + 2 * 16 * 4;                  // running sums [16]
+    static constexpr int kOffM = kOffL + 16 * 4;                          // running maxima [2][16]
+    static constexpr int kOffBat = kOffM + 2 * 16 * 4;                    // [2] x (t0, n)
+    static constexpr int kOffBar = kOffBat + 16;                          // mbarriers
+    static constexpr int kNumBars = 2 * kNR + 2 * 7 + 3;
+    static constexpr int kOffTok = kOffBar + kNumBars * 8 + 16;           // [ring rows]
+    static constexpr int kOffBlk = kOffTok + kRingRows * 4;
     static constexpr size_t bytes(int blk_list) { return 1024 + kOffBlk + (size_t)blk_list * 4 + 16; }
 };
 
-template <int DKQ, int DV, bool V_IS_K, int TT>
-__global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnParams p) {
-    using Lay = TcLayout<DKQ, DV, V_IS_K, TT>;
+// Reduces v[0..15] (one value per head) over the 32 lanes with op: afterwards lanes 2h and
+// 2h + 1 hold the reduction of head h.  16 shuffles (a transposing butterfly).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+    auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+    float a8[8], a4[4], a2[2];
+    const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float keep = u16 ? v[i + 8] : v[i], send = u16 ? v[i] : v[i + 8];
+        a8[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float keep = u8 ? a8[i + 4] : a8[i], send = u8 ? a8[i] : a8[i + 4];
+        a4[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float keep = u4 ? a4[i + 2] : a4[i], send = u4 ? a4[i] : a4[i + 2];
+        a2[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+    }
+    const float keep = u2 ? a2[1] : a2[0], send = u2 ? a2[0] : a2[1];
+    const float a1 = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+    return op(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, 1));
+}
+
+// O = O * alpha + (P_hi V + P_lo V) of batch bb, whose PV result sits in O buffer bb & 1
+// (32 columns per 128-wide slice of DV: the hi half, then the lo half).
+template <int DV>
+__device__ __forceinline__ bool tc_fold(float (&o)[DV / 128][16], const float *al, int bb,
+                                        uint64_t *o_full, uint64_t *o_empty, uint32_t tO,
+                                        uint32_t lane_addr, int lane, uint64_t deadline) {
+    const int x = bb & 1;
+    if (!mbar_wait(&o_full[x], (bb >> 1) & 1, deadline)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const float a = al[c];
+#pragma unroll
+        for (int mt = 0; mt < DV / 128; ++mt) o[mt][c] *= a;
+    }
+#pragma unroll
+    for (int mt = 0; mt < DV / 128; ++mt) {
+        uint32_t r[16];
+        tmem_ld16(tO + x * 128 + mt * 32 + lane_addr, r);          // P_hi V
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[mt][c] += __uint_as_float(r[c]);
+        tmem_ld16(tO + x * 128 + mt * 32 + 16 + lane_addr, r);     // P_lo V
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[mt][c] += __uint_as_float(r[c]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&o_empty[x]);
+    return true;
+}
+
+template <int DKQ, int DV, bool V_IS_K>
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    attend_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+    using Lay = TcLayout<DKQ, DV, V_IS_K>;
+    constexpr int NR = Lay::kNR, TT = tc::kTT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
-    uint8_t *sStage = smem + Lay::kOffStages;
+    // 1024-aligned base, derived by pointer arithmetic so accesses stay shared-space ones
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sRing = smem + Lay::kOffRing;
     uint8_t *sQ = smem + Lay::kOffQ;
     uint8_t *sP = smem + Lay::kOffP;
-    float *sS = reinterpret_cast<float *>(smem + Lay::kOffS);
-    float *sAlpha = reinterpret_cast<float *>(smem + Lay::kOffAlpha);
-    float *sStat = reinterpret_cast<float *>(smem + Lay::kOffStat);
+    float *sMax = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [4 warps][16 heads]
+    float *sSum = sMax + 64;
+    float *sAlpha = reinterpret_cast<float *>(smem + Lay::kOffAlpha);  // per batch buffer
+    float *sL = reinterpret_cast<float *>(smem + Lay::kOffL);          // running sums per head
+    float *sM = reinterpret_cast<float *>(smem + Lay::kOffM);          // running maxima; after
+                                                                       // batch b in [b & 1]
+    int *sBat = reinterpret_cast<int *>(smem + Lay::kOffBat);        // [2] x (first tile, n)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
-    uint64_t *full = bars, *empty = bars + tc::kStages;
-    uint64_t *s_full = bars + 2 * tc::kStages, *s_empty = s_full + 2;
+    uint64_t *full = bars, *empty = bars + NR;
+    uint64_t *bat_ready = bars + 2 * NR, *s_full = bat_ready + 2, *s_empty = s_full + 2;
     uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
     uint64_t *o_full = p_empty + 2, *o_empty = o_full + 2;
-    uint64_t *q_ready = o_empty + 2, *stats_ready = q_ready + 1, *drain = q_ready + 2;
-    uint64_t *soft_bar = q_ready + 3;   // the softmax threads' own (bounded) barrier
+    uint64_t *q_ready = o_empty + 2, *drain = q_ready + 1;
+    uint64_t *soft_bar = q_ready + 2;   // the softmax threads' own (bounded) barrier
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *sTok = reinterpret_cast<int *>(smem + Lay::kOffTok);
@@ -493,23 +581,27 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnPa
     const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
 
     // ------------------------------------------------------------------ set-up
+    if (tid == tc::kProdWarp0 * 32) {
+        prefetch_tensormap(&kmap);
+        if constexpr (!V_IS_K) prefetch_tensormap(&vmap);
+    }
     if (tid == 0) {
-        for (int s = 0; s < tc::kStages; ++s) {
-            mbar_init(&full[s], tc::kGroupThreads);
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&full[s], tc::kProdThreads / 32);   // one expect-tx arrival per warp
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&bat_ready[b], 1);
             mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 2);      // the two softmax warps
-            mbar_init(&p_full[b], 2);
-            mbar_init(&p_empty[b], 1 + 4);  // the PV commit + the four correction warps
+            mbar_init(&s_empty[b], 4);      // the four softmax warps
+            mbar_init(&p_full[b], 4);
+            mbar_init(&p_empty[b], 1);      // the PV commit
             mbar_init(&o_full[b], 1);
             mbar_init(&o_empty[b], 4);
         }
-        mbar_init(q_ready, tc::kProdThreads);
-        mbar_init(stats_ready, 2);
+        mbar_init(q_ready, 128);   // the softmax warps load Q
         mbar_init(drain, 1);
-        mbar_init(soft_bar, tc::kSoftThreads);
+        mbar_init(soft_bar, 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -522,7 +614,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnPa
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 32;  // S: cols [0, 32), O: cols [32, 160)
+    const uint32_t tS = tmem, tO = tmem + 32;  // S: cols [0, 32), O: cols [32, 288)
 
     auto fail = [&]() {
         set_status(p.status, SFA_DEV_TIMEOUT);
@@ -531,18 +623,178 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnPa
 
     if (warp >= tc::kProdWarp0) {
         // ------------------------------------------------------------ producers
-        const int pt = tid - tc::kProdWarp0 * 32;   // 0..127
         constexpr int KCH = DKQ / 8, VCH = DV / 8;
         const __nv_bfloat16 *Kseq = reinterpret_cast<const __nv_bfloat16 *>(p.K) +
                                     (int64_t)L.seq * p.k_seq_stride + (int64_t)g * DKQ;
         const __nv_bfloat16 *Vseq = V_IS_K ? Kseq
                                            : reinterpret_cast<const __nv_bfloat16 *>(p.V) +
                                                  (int64_t)L.seq * p.v_seq_stride + (int64_t)g * DV;
+        // warp pw owns tile rows 8pw .. 8pw + 7: two 4-row groups
+        const int pw = warp - tc::kProdWarp0;
+        constexpr int NSL = Lay::kSlabK + Lay::kSlabV;
+        static_assert(2 * NSL <= 32, "one box per lane");
+        static_assert((4 * KCH) % 32 == 0 && (4 * VCH) % 32 == 0, "uniform row-copy loops");
+        const int64_t zseq = (int64_t)L.seq * p.n_tok_cap;   // TMA row of the sequence's token 0
+        const uint32_t ring = smem_u32(sRing);
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % NR;
+            if (*abort_flag) break;
+            if (!mbar_wait(&empty[st], ((t / NR) & 1) ^ 1, deadline)) { fail(); break; }
+            const int row0 = st * TT + pw * 8;                  // ring row of this warp's row 0
+            int tok_l = -1;
+            if (lane < 8) {
+                tok_l = token_at(p, L, j0 + t * TT + pw * 8 + lane, j1, sBlk, jb0);
+                sTok[row0 + lane] = tok_l;
+            }
+            int tk[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) tk[k] = __shfl_sync(0xFFFFFFFFu, tok_l, k);
+            bool box[2];
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi)
+                box[gi] = tk[4 * gi] >= 0 && tk[4 * gi + 1] == tk[4 * gi] + 1 &&
+                          tk[4 * gi + 2] == tk[4 * gi] + 2 && tk[4 * gi + 3] == tk[4 * gi] + 3;
+            if (!box[0] || !box[1]) {
+                // row-by-row copies (zero rows for masked positions), landed and fenced here
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    if (box[gi]) continue;
+#pragma unroll 1
+                    for (int e = lane; e < 4 * KCH; e += 32) {
+                        const int k = e / KCH, c = e - k * KCH, r = row0 + 4 * gi + k;
+                        const int tok = tk[4 * gi + k];
+                        cp_async16(ring + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                                   tok >= 0 ? Kseq + (int64_t)tok * p.k_tok_stride + c * 8 : Kseq,
+                                   tok >= 0 ? 16u : 0u);
+                    }
+                    if constexpr (!V_IS_K) {
+                        const uint32_t v0 = ring + Lay::kSlabK * Lay::kSlabBytes;
+#pragma unroll 1
+                        for (int e = lane; e < 4 * VCH; e += 32) {
+                            const int k = e / VCH, c = e - k * VCH, r = row0 + 4 * gi + k;
+                            const int tok = tk[4 * gi + k];
+                            cp_async16(v0 + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                                       tok >= 0 ? Vseq + (int64_t)tok * p.v_tok_stride + c * 8 : Vseq,
+                                       tok >= 0 ? 16u : 0u);
+                        }
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[st], (uint32_t)((box[0] ? 1 : 0) + (box[1] ? 1 : 0)) * NSL * 512u);
+            __syncwarp();
+            if (lane < 2 * NSL) {   // lane -> (group, slab): one 4-row x 128-byte box each
+                const int gi = lane / NSL, sl = lane - gi * NSL;
+                if (box[gi]) {
+                    const bool is_v = !V_IS_K && sl >= Lay::kSlabK;
+                    tma_load_3d(sRing + sl * Lay::kSlabBytes + (row0 + 4 * gi) * 128,
+                                is_v ? &vmap : &kmap, (is_v ? sl - Lay::kSlabK : sl) * 64, g,
+                                (int32_t)(zseq + tk[4 * gi]), &full[st]);
+                }
+            }
+        }
+    } else if (warp == tc::kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(128, 16);
+            const uint32_t idPV = idesc_bf16_f32(128, 32) | (1u << 15);   // A (V^T) MN-major
+            const uint32_t ring = smem_u32(sRing), q0 = smem_u32(sQ), p0 = smem_u32(sP);
+            const uint64_t aS = sw128_desc(ring, 16, 1024);
+            const uint64_t bq = sw128_desc(q0, 16, 1024);
+            const uint32_t vbase = ring + (V_IS_K ? 0 : Lay::kSlabK * Lay::kSlabBytes);
+            // V^T (MN-major): 64-dim atoms one slab apart, 8-token groups 1024 B apart
+            const uint64_t av0 = sw128_desc(vbase, Lay::kSlabBytes, 1024);
+            const uint64_t bp0 = sw128_desc(p0, 16, 1024);
+            static_assert((NR & (NR - 1)) == 0, "ring size is a power of two");
+            bool ok = mbar_wait(q_ready, 0, deadline);
+            int t_next = 0, nb = 0, np = 0;      // next tile to score, batches formed, PV'd
+            int bt0[2] = {0, 0}, btn[2] = {0, 0};
+            // PV of the oldest batch whose P is ready (it releases stages); also called
+            // between the chunks of an S issue so that PV never waits behind a whole S
+            auto try_pv = [&]() -> bool {
+                if (np >= nb) return false;
+                const int x = np & 1;
+                if (!mbar_try_wait(smem_u32(&p_full[x]), (np >> 1) & 1) ||
+                    !mbar_try_wait(smem_u32(&o_empty[x]), ((np >> 1) & 1) ^ 1))
+                    return false;
+                tc_fence_after();
+                // u outer, the slices of DV inner: the first tile starts each slice
+#pragma unroll 1
+                for (int u = 0; u < btn[x]; ++u) {
+                    const int st = (bt0[x] + u) & (NR - 1);
+                    const uint64_t a_u = av0 + (uint64_t)((st * TT * 128) >> 4);
+                    const uint64_t b_u = bp0 + (uint64_t)((x * Lay::kPBuf + (st >> 1) * Lay::kPRegion +
+                                                           (st & 1) * 64) >> 4);
+#pragma unroll
+                    for (int mt = 0; mt < DV / 128; ++mt) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+                            tc_mma_bf16(tO + x * 128 + mt * 32,
+                                        a_u + (uint64_t)((2 * mt * Lay::kSlabBytes + hf * 2048) >> 4),
+                                        b_u + (uint64_t)(hf * 2), idPV, (u > 0 || hf > 0) ? 1u : 0u);
+                    }
+                }
+                tc_commit(&o_full[x]);
+                tc_commit(&p_empty[x]);
+                for (int u = 0; u < btn[x]; ++u) tc_commit(&empty[(bt0[x] + u) & (NR - 1)]);
+                ++np;
+                return true;
+            };
+            uint32_t spin = 0;
+            while (ok && (t_next < n_tiles || np < nb)) {
+                if (*abort_flag) { ok = false; break; }
+                bool progressed = try_pv();
+                // S for the landed, unscored tiles (a batch), when an S buffer is free
+                if (t_next < n_tiles && nb - np < 2) {
+                    const int x = nb & 1;
+                    // at least kBatchMin landed tiles (fewer only at the end), then every
+                    // further landed one up to the whole ring: S costs the same for all of them
+                    const int n_min = min(tc::kBatchMin, n_tiles - t_next);
+                    bool ready = mbar_try_wait(smem_u32(&s_empty[x]), ((nb >> 1) & 1) ^ 1);
+                    for (int u = 0; ready && u < n_min; ++u)
+                        ready = mbar_try_wait(smem_u32(&full[(t_next + u) % NR]), ((t_next + u) / NR) & 1);
+                    if (ready) {
+                        int n = n_min;
+                        while (n < NR && t_next + n < n_tiles &&
+                               mbar_try_wait(smem_u32(&full[(t_next + n) % NR]), ((t_next + n) / NR) & 1))
+                            ++n;
+                        bt0[x] = t_next;
+                        btn[x] = n;
+                        sBat[2 * x] = t_next;
+                        sBat[2 * x + 1] = n;
+                        mbar_arrive(&bat_ready[x]);
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int sl = 0; sl < Lay::kSlabK; ++sl) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma_bf16(tS + x * 16, aS + (uint64_t)((sl * Lay::kSlabBytes + kk * 32) >> 4),
+                                            bq + (uint64_t)((sl * 2048 + kk * 32) >> 4), idS,
+                                            (sl > 0 || kk > 0) ? 1u : 0u);
+                            if (sl % 3 == 2 && sl + 1 < Lay::kSlabK) try_pv();   // PV cuts in
+                        }
+                        tc_commit(&s_full[x]);
+                        t_next += n;
+                        ++nb;
+                        progressed = true;
+                    }
+                }
+                if (!progressed && (++spin & 63u) == 0 && global_timer_ns() > deadline) ok = false;
+            }
+            if (!ok) fail();
+        }
+    } else {
+        // ------------------------------------------------- softmax + correction (4 warps)
         {   // Q^T operand: 16 rows (heads; rows >= G zero) x DKQ, one slab per 64 dims
+            constexpr int KCH = DKQ / 8;
             const __nv_bfloat16 *Qg = reinterpret_cast<const __nv_bfloat16 *>(p.Q) +
                                       ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ;
             const uint32_t qs = smem_u32(sQ);
-            for (int e = pt; e < 16 * KCH; e += tc::kProdThreads) {
+            for (int e = tid; e < 16 * KCH; e += 128) {
                 const int r = e / KCH, c = e % KCH;
                 const bool live = r < G;
                 cp_async16(qs + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4),
@@ -553,209 +805,128 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnPa
             fence_proxy_async_smem();
             mbar_arrive(q_ready);
         }
-        // group pg takes tiles t = pg, pg + 2, ... (stage t % 2 == pg)
-        const int pg = pt / tc::kGroupThreads, gt = pt % tc::kGroupThreads;
-        constexpr int PER_ROW = tc::kGroupThreads / TT;      // threads per token row
-        const int r = gt % TT, part = gt / TT;
-        for (int t = pg; t < n_tiles; t += 2) {
-            const int st = t % tc::kStages;
-            if (*abort_flag) break;
-            if (!mbar_wait(&empty[st], ((t / tc::kStages) & 1) ^ 1, deadline)) { fail(); break; }
-            const uint32_t dk = smem_u32(sStage + (size_t)st * Lay::kStageBytes);
-            const int tok = token_at(p, L, j0 + t * TT + r, j1, sBlk, jb0);
-            if (part == 0) sTok[st * TT + r] = tok;
-            const uint32_t nbytes = tok >= 0 ? 16u : 0u;
-            const __nv_bfloat16 *srcK = tok >= 0 ? Kseq + (int64_t)tok * p.k_tok_stride : Kseq;
-            for (int c = part; c < KCH; c += PER_ROW)
-                cp_async16(dk + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
-                           srcK + c * 8, nbytes);
-            if constexpr (!V_IS_K) {
-                const __nv_bfloat16 *srcV = tok >= 0 ? Vseq + (int64_t)tok * p.v_tok_stride : Vseq;
-                const uint32_t dv0 = dk + Lay::kSlabK * Lay::kSlabBytes;
-                for (int c = part; c < VCH; c += PER_ROW)
-                    cp_async16(dv0 + (c >> 3) * Lay::kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4),
-                               srcV + c * 8, nbytes);
-            }
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(&full[st]);
+        const int sq = warp;                       // ring stage / TMEM lane quarter
+        const int rrow = sq * TT + lane;           // ring row = TMEM lane of this thread
+        const uint32_t lane_addr = (uint32_t)(sq * 32) << 16;
+        // the running maxima and sums live in sM / sL; lanes 0-15 of warp 0 update them
+        float o[DV / 128][16];
+        if (tid < 16) {
+            sL[tid] = 0.f;
+            sM[16 + tid] = -INFINITY;   // "after batch -1"
         }
-    } else if (warp == tc::kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idS = idesc_bf16_f32(128, 16);
-            const uint32_t idPV = idesc_bf16_f32(128, 16) | (1u << 15);   // A (V^T) MN-major
-            const uint32_t st0 = smem_u32(sStage), q0 = smem_u32(sQ), p0 = smem_u32(sP);
-            bool ok = mbar_wait(q_ready, 0, deadline);
-            auto issue_pv = [&](int u) -> bool {
-                const int st = u % tc::kStages, b = u & 1;
-                if (!mbar_wait(&p_full[b], (u >> 1) & 1, deadline)) return false;
-                if (!mbar_wait(&o_empty[b], ((u >> 1) & 1) ^ 1, deadline)) return false;
-                tc_fence_after();
-                const uint32_t vbase = st0 + st * Lay::kStageBytes + (V_IS_K ? 0 : Lay::kSlabK * Lay::kSlabBytes);
-                const uint32_t ph = p0 + (b * 2) * Lay::kPBytes, pl = ph + Lay::kPBytes;
 #pragma unroll
-                for (int mt = 0; mt < DV / 128; ++mt) {
-                    const uint32_t d = tO + b * 64 + mt * 16;
+        for (int mt = 0; mt < DV / 128; ++mt)
 #pragma unroll
-                    for (int kk = 0; kk < TT / 16; ++kk) {
-                        const uint64_t a = sw128_desc(vbase + 2 * mt * Lay::kSlabBytes + kk * 2048,
-                                                      Lay::kSlabBytes, 1024);
-                        tc_mma_bf16(d, a, sw128_desc(ph + kk * 32, 16, 1024), idPV, kk > 0 ? 1u : 0u);
-                        tc_mma_bf16(d, a, sw128_desc(pl + kk * 32, 16, 1024), idPV, 1u);
-                    }
-                }
-                tc_commit(&o_full[b]);
-                tc_commit(&empty[st]);
-                tc_commit(&p_empty[b]);
-                return true;
-            };
-            for (int t = 0; t < n_tiles && ok; ++t) {
-                if (*abort_flag) { ok = false; break; }
-                const int st = t % tc::kStages, b = t & 1;
-                if (!mbar_wait(&full[st], (t / tc::kStages) & 1, deadline) ||
-                    !mbar_wait(&s_empty[b], ((t >> 1) & 1) ^ 1, deadline)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t kbase = st0 + st * Lay::kStageBytes;
-#pragma unroll 1
-                for (int s = 0; s < Lay::kSlabK; ++s) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(tS + b * 16,
-                                    sw128_desc(kbase + s * Lay::kSlabBytes + kk * 32, 16, 1024),
-                                    sw128_desc(q0 + s * 2048 + kk * 32, 16, 1024), idS,
-                                    (s > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&s_full[b]);
-                if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
-            }
-            if (ok && !issue_pv(n_tiles - 1)) ok = false;
-            if (!ok) fail();
-        }
-    } else if (warp >= tc::kSoftWarp0 && warp < tc::kSoftWarp0 + 2) {
-        // ------------------------------------------------------------ softmax (64 threads)
-        const int sid = tid - tc::kSoftWarp0 * 32;        // 0..63: TMEM lane / token row
-        const int h = sid >> 2, q = sid & 3;              // head-major phase: head, quarter
-        constexpr int TPQ = TT / 4;                       // tokens per quarter
-        float m_run = -INFINITY, l_run = 0.f;             // of head h (the 4 threads agree)
+            for (int c = 0; c < 16; ++c) o[mt][c] = 0.f;
         uint32_t soft_phase = 0;
-        auto soft_sync = [&]() -> bool {   // all 64 softmax threads, bounded
+        auto soft_sync = [&]() -> bool {   // the 128 threads of warps 0-3, bounded
             mbar_arrive(soft_bar);
             const bool done = mbar_wait(soft_bar, soft_phase, deadline);
             soft_phase ^= 1;
             return done;
         };
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % tc::kStages, b = t & 1;
-            if (*abort_flag) break;
-            if (!mbar_wait(&s_full[b], (t >> 1) & 1, deadline) ||
-                !mbar_wait(&full[st], (t / tc::kStages) & 1, deadline)) { fail(); break; }
+        bool ok = true;
+        int done_tiles = 0, b = 0;
+        for (; done_tiles < n_tiles; ++b) {
+            const int x = b & 1;
+            const uint32_t par = (b >> 1) & 1;
+            if (*abort_flag) { ok = false; break; }
+            if (!mbar_wait(&bat_ready[x], par, deadline)) { ok = false; break; }
+            const int t0 = sBat[2 * x], n = sBat[2 * x + 1];
+            const int u = ((sq - t0 % NR) + NR) % NR;      // this stage's place in the batch
+            const bool part = sq < NR && u < n;
+            const int tq = t0 + u;
+            if (!mbar_wait(&s_full[x], par, deadline) ||
+                (part && !mbar_wait(&full[sq], (tq / NR) & 1, deadline))) { ok = false; break; }
             tc_fence_after();
-            uint32_t r[16];
-            tmem_ld16(tS + b * 16 + ((uint32_t)((warp & 3) * 32) << 16), r);
-            tmem_ld_wait();
-            if (sid < TT) {
+            float s[16];
+            if (part) {
+                uint32_t r[16];
+                tmem_ld16(tS + x * 16 + lane_addr, r);
+                tmem_ld_wait();
+                const bool valid = sTok[rrow] >= 0;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) sS[sid * tc::kSPitch + c] = __uint_as_float(r[c]);
+                for (int h = 0; h < 16; ++h) s[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
+            } else {
+#pragma unroll
+                for (int h = 0; h < 16; ++h) s[h] = -INFINITY;
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[b]);
-            if (!soft_sync()) { fail(); break; }
-            // head h, tokens [q*TPQ, (q+1)*TPQ)
-            float sv[TPQ], mx = -INFINITY;
+            if (lane == 0) mbar_arrive(&s_empty[x]);
+            {
+                float v[16];
 #pragma unroll
-            for (int e = 0; e < TPQ; ++e) {
-                const int tk = q * TPQ + e;
-                const float v = sS[tk * tc::kSPitch + h] * p.scale_log2;
-                sv[e] = sTok[st * TT + tk] >= 0 ? v : -INFINITY;
-                mx = fmaxf(mx, sv[e]);
+                for (int h = 0; h < 16; ++h) v[h] = s[h];
+                const float mx = warp_reduce16<true>(v, lane);
+                if ((lane & 1) == 0) sMax[sq * 16 + (lane >> 1)] = mx;
             }
-            if (!soft_sync()) { fail(); break; }    // the S staging area may be refilled now
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-            float rs = 0.f;
-            uint32_t hi[TPQ / 2], lo[TPQ / 2];
+            if (!soft_sync()) { ok = false; break; }
+            // P^T (ring row rrow) into buffer x once the PV two batches back is done with it
+            if (!mbar_wait(&p_empty[x], par ^ 1, deadline)) { ok = false; break; }
+            // new running max mn; l and (through sAlpha, at the fold) O are rescaled by alpha
+            uint8_t *pb = sP + x * Lay::kPBuf + (rrow >> 6) * Lay::kPRegion;
+            const int col = rrow & 63;
+            const float *mold = sM + (x ^ 1) * 16;
+            // every shared load first (the P stores below could alias them for the compiler)
 #pragma unroll
-            for (int e = 0; e < TPQ; e += 2) {
-                const float p0 = m_new == -INFINITY ? 0.f : exp2f(sv[e] - m_new);
-                const float p1 = m_new == -INFINITY ? 0.f : exp2f(sv[e + 1] - m_new);
-                rs += p0 + p1;
-                const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
-                hi[e / 2] = pack_bf16(h0, h1);
-                lo[e / 2] = pack_bf16(p0 - h0, p1 - h1);
+            for (int h = 0; h < 16; ++h) {
+                const float4 m4 = make_float4(sMax[h], sMax[16 + h], sMax[32 + h], sMax[48 + h]);
+                const float mn = fmaxf(mold[h], fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)));
+                s[h] = (!part || mn == -INFINITY) ? -INFINITY : s[h] - mn;   // exponent of p
             }
-            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
-            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
-            l_run = l_run * alpha + rs;
-            m_run = m_new;
-            // P^T rows (head h) of this buffer: wait until the PV two tiles back is done
-            if (!mbar_wait(&p_empty[b], ((t >> 1) & 1) ^ 1, deadline)) { fail(); break; }
-            uint8_t *ph = sP + (b * 2) * Lay::kPBytes, *pl = ph + Lay::kPBytes;
 #pragma unroll
-            for (int cc = 0; cc < TPQ / 8; ++cc) {      // 16-byte chunks of 8 tokens
-                const int chunk = (q * TPQ) / 8 + cc;
-                const int off = h * 128 + ((chunk ^ (h & 7)) << 4);
-                *reinterpret_cast<uint4 *>(ph + off) =
-                    make_uint4(hi[cc * 4], hi[cc * 4 + 1], hi[cc * 4 + 2], hi[cc * 4 + 3]);
-                *reinterpret_cast<uint4 *>(pl + off) =
-                    make_uint4(lo[cc * 4], lo[cc * 4 + 1], lo[cc * 4 + 2], lo[cc * 4 + 3]);
+            for (int h = 0; h < 16; ++h) {
+                const float pe = exp2f(s[h]);
+                s[h] = pe;
+                if (part) {
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pe);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(pe - __bfloat162float(hi));
+                    const int off = ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2;
+                    *reinterpret_cast<__nv_bfloat16 *>(pb + h * 128 + off) = hi;
+                    *reinterpret_cast<__nv_bfloat16 *>(pb + (16 + h) * 128 + off) = lo;
+                }
             }
-            if (q == 0) sAlpha[b * 16 + h] = alpha;
+            {
+                const float rs = warp_reduce16<false>(s, lane);
+                if ((lane & 1) == 0) sSum[sq * 16 + (lane >> 1)] = rs;
+            }
+            if (warp == 0 && lane < 16) {   // running max / alpha / rescaled sum of head lane
+                const int h = lane;
+                const float mx = fmaxf(fmaxf(sMax[h], sMax[16 + h]), fmaxf(sMax[32 + h], sMax[48 + h]));
+                const float mo = mold[h], mn = fmaxf(mo, mx);
+                const float alpha = mn == -INFINITY ? 1.f : exp2f(mo - mn);
+                sAlpha[x * 16 + h] = alpha;
+                sL[h] *= alpha;
+                sM[x * 16 + h] = mn;
+            }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
-        }
-        if (q == 0) {
-            sStat[h] = m_run;
-            sStat[16 + h] = l_run;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(stats_ready);
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ correction (128 thr)
-        float o[DV / 128][16];
-#pragma unroll
-        for (int mt = 0; mt < DV / 128; ++mt)
-#pragma unroll
-            for (int c = 0; c < 16; ++c) o[mt][c] = 0.f;
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        bool ok = true;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int b = t & 1;
-            if (*abort_flag) { ok = false; break; }
-            if (!mbar_wait(&o_full[b], (t >> 1) & 1, deadline) ||
-                !mbar_wait(&p_full[b], (t >> 1) & 1, deadline)) { fail(); ok = false; break; }
-            tc_fence_after();
-            float al[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) al[c] = sAlpha[b * 16 + c];
-#pragma unroll
-            for (int mt = 0; mt < DV / 128; ++mt) {
-                uint32_t r[16];
-                tmem_ld16(tO + b * 64 + mt * 16 + lane_addr, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) o[mt][c] = fmaf(o[mt][c], al[c], __uint_as_float(r[c]));
+            if (lane == 0) mbar_arrive(&p_full[x]);
+            // while the PV of this batch runs: fold the previous batch into O
+            if (b > 0 && !tc_fold<DV>(o, sAlpha + ((b - 1) & 1) * 16, b - 1, o_full, o_empty, tO,
+                                      lane_addr, lane, deadline)) {
+                ok = false;
+                break;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&o_empty[b]);
-                mbar_arrive(&p_empty[b]);
-            }
+            if (!soft_sync()) { ok = false; break; }
+            if (warp == 0 && lane < 16)
+                sL[lane] += (sSum[lane] + sSum[16 + lane]) + (sSum[32 + lane] + sSum[48 + lane]);
+            done_tiles = t0 + n;
         }
-        if (ok && mbar_wait(stats_ready, 0, deadline)) {
-            const int dv_base = warp * 32 + lane;
+        if (ok && b > 0 &&
+            !tc_fold<DV>(o, sAlpha + ((b - 1) & 1) * 16, b - 1, o_full, o_empty, tO, lane_addr, lane, deadline))
+            ok = false;
+        if (ok && !soft_sync()) ok = false;   // thread 0's last update of sL is visible
+        if (!ok) {
+            fail();
+        } else {
+            const int dv_base = sq * 32 + lane;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 if (c >= G) break;
                 const int h = g * G + c;
-                const float m = sStat[c], l = sStat[16 + c];
+                const float m = sM[((b - 1) & 1) * 16 + c], l = sL[c];
                 if (p.n_split == 1) {
                     const float inv = l > 0.f ? 1.f / l : 0.f;
                     float *dst = p.O + ((int64_t)i * p.h_q + h) * DV + dv_base;
@@ -774,8 +945,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1) attend_tc_kernel(const AttnPa
                     }
                 }
             }
-        } else if (ok) {
-            fail();
         }
     }
 
@@ -934,6 +1103,12 @@ SplitPlan plan_split(int n_q, int h_kv, int64_t n_kv_max, int per_sm = 2, int ti
     return sp;
 }
 
+// SFA_ATTEND_KERNEL=tcgen05 in the environment (read at each call) picks the tcgen05 kernel.
+bool want_tcgen05() {
+    const char *e = getenv("SFA_ATTEND_KERNEL");
+    return e && strcmp(e, "tcgen05") == 0;
+}
+
 bool shape_supported(int dkq, int dv) {
     return (dkq == 576 && dv == 512) || (dkq == 512 && dv == 512) || (dkq == 128 && dv == 128) ||
            (dkq == 64 && dv == 64);
@@ -977,16 +1152,35 @@ int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     return SFA_OK;
 }
 
-template <int DKQ, int DV, bool VK, int TT>
+// Tensor map of a bf16 cache [n_seq][n_tok_cap][h_kv][d] as 3-D {d, h_kv, n_seq * n_tok_cap}
+// with 4-row x 64-element boxes in the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *map, const void *base, int d, int h_kv, int64_t rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)h_kv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)h_kv * d * 2};
+    const cuuint32_t box[3] = {64, 1, 4}, es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DKQ, int DV, bool VK>
 int launch_tc(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
-    const size_t smem = TcLayout<DKQ, DV, VK, TT>::bytes(blk_list);
+    const size_t smem = TcLayout<DKQ, DV, VK>::bytes(blk_list);
     if (smem > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)p.n_seq * p.n_tok_cap;
+    if (rows > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map(&kmap, p.K, DKQ, p.h_kv, rows)) return SFA_ERR_CUDA;
+    if (VK) vmap = kmap;
+    else if (!encode_cache_map(&vmap, p.V, DV, p.h_kv, rows)) return SFA_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
-        if (!allow_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK, TT>)) return SFA_ERR_CUDA;
+        if (!allow_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    attend_tc_kernel<DKQ, DV, VK, TT><<<grid, tc::kThreads, smem, st>>>(p);
+    attend_tc_kernel<DKQ, DV, VK><<<grid, tc::kThreads, smem, st>>>(kmap, vmap, p);
     SFA_CHECK_LAUNCH();
     return SFA_OK;
 }
@@ -1010,10 +1204,12 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
-    // The 512-wide heads take the tcgen05 kernel (one CTA per SM; 64-token tiles, or 32 when
-    // V is separate); the narrow test shapes and fp32 inputs take the warp-level kernels.
-    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512);
-    const int tc_tile = V ? 32 : 64;
+    // bf16 inputs take the warp-level mma.sync kernel, which is the faster one on the decode
+    // and prefill shapes measured; SFA_ATTEND_KERNEL=tcgen05 selects the tcgen05 kernel for the
+    // 512-wide heads instead (same results within the same tolerances).  fp32 inputs take the
+    // SIMT kernel.
+    const int tc_tile = tc::kTT;
+    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && want_tcgen05();
     // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
     int per_sm = 1;
     if (dtype == SFA_BF16 && !use_tc) {
@@ -1050,10 +1246,12 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     const dim3 grid(sp.n_split, h_kv, n_q);
     int rc;
     if (use_tc) {
-        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_tc<576, 512, true, 64>(p, grid, st, bl);
-        else rc = V ? launch_tc<512, 512, false, 32>(p, grid, st, bl) : launch_tc<512, 512, true, 64>(p, grid, st, bl);
+        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_tc<576, 512, true>(p, grid, st, bl);
+        else rc = V ? launch_tc<512, 512, false>(p, grid, st, bl) : launch_tc<512, 512, true>(p, grid, st, bl);
     } else if (dtype == SFA_BF16) {
-        if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
+        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true>(p, grid, st, bl);
+        else if (dkq == 512) rc = V ? launch_bf16<512, 512, false>(p, grid, st, bl) : launch_bf16<512, 512, true>(p, grid, st, bl);
+        else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
         else rc = V ? launch_bf16<64, 64, false>(p, grid, st, bl) : launch_bf16<64, 64, true>(p, grid, st, bl);
     } else {
         if (dkq == 576) attend_f32_kernel<576, 512><<<grid, kThreads, 0, st>>>(p);
