@@ -4,7 +4,9 @@ A step is one pass of the whole method over one batch of queries: pool the index
 that this step's tokens complete, score every visible block, keep the top-k blocks plus the
 tail, and attend over the kept cells (sfa_pool_index_keys -> sfa_index_scores ->
 sfa_topk_blocks -> sfa_gather_attend).  Inputs are seeded synthetic tensors resident in HBM;
-L2 is flushed (a 512 MB write) before every timed step, outside the timed events.
+L2 is flushed before every timed step, outside the timed events: 512 MB are written, then a
+separate 256 MB buffer is read, so that no dirty line of the flush is written back inside the
+timed step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -15,6 +17,7 @@ workload on its own GPU (weak scaling, no collective on the data path); rank 0 p
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -35,7 +38,7 @@ METRIC = "sparse-attn tokens/s (decode, pp2048) at depth; gathered-KV HBM GB/s v
 DEFAULT_WORKLOAD = "decode_32x131072"
 SECOND_WORKLOAD = "pp2048_131072"
 L2_FLUSH_BYTES = 512 << 20
-HOLD_CYCLES = 2_000_000        # ~1 ms GPU spin that covers the host's enqueue of one step
+HOLD_CYCLES = 400_000          # ~0.2 ms GPU spin that covers the host's enqueue of one step
 CSRC = os.path.join(ROOT, "indexer_selected_sparse_block_gb300", "csrc")
 
 
@@ -92,7 +95,9 @@ def algorithmic(w, attended):
 
 # ------------------------------------------------------------------------------- clocks
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 10 ms while the steps run; summary() keeps the samples taken
+    between mark_start() and mark_end() (warm-up and timed steps: the GPU under load)."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -104,11 +109,19 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                 "-i", str(self.index), "-lms", "10"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+        time.sleep(0.3)   # let the sampler start before the load does
+        self.t0 = self.t1 = None
         return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def __exit__(self, *a):
         self.lines = []
@@ -126,14 +139,21 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in getattr(self, "lines", []):
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            if ts is not None and self.t0 is not None and self.t1 is not None and \
+                    not (self.t0 <= ts <= self.t1):
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx = max(mx, float(f[3]))
             except ValueError:
                 continue
-            for name, v in zip(names, f[5:9]):
+            for name, v in zip(names, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
@@ -203,20 +223,29 @@ class Workbench:
             ev["attend"][1].record()
 
 
-def measure(wb, steps, warmup, flush, per_stage=True):
+def flush_l2(flush):
+    """Evicts L2: writes the 512 MB flush buffer, then reads a clean 256 MB one, so that the
+    flush leaves clean lines only (nothing of it is written back inside a timed step)."""
+    flush[0].zero_()
+    flush[1].sum()
+
+
+def measure(wb, steps, warmup, flush, per_stage=True, clk=None):
     """Device time of `steps` steps (L2 flushed before each), plus per-stage averages.
 
     Before each timed step the stream is held by a short GPU spin (outside the timed events)
     so that the host has enqueued the whole step before the first timed event runs: the
     events then see GPU execution only, not host launch latency."""
+    if clk is not None:
+        clk.mark_start()
     for _ in range(warmup):
-        flush.zero_()
+        flush_l2(flush)
         wb.run_step()
     torch.cuda.synchronize()
     stages = ["pool", "scores", "topk", "attend"]
     step_ms, stage_ms = [], {s: [] for s in stages}
     for _ in range(steps):
-        flush.zero_()
+        flush_l2(flush)
         torch.cuda._sleep(HOLD_CYCLES)
         ev = {s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for s in stages} if per_stage else {}
@@ -229,9 +258,32 @@ def measure(wb, steps, warmup, flush, per_stage=True):
         for s, (a, b) in ev.items():
             try:
                 stage_ms[s].append(a.elapsed_time(b))
-            except RuntimeError:
+            except (RuntimeError, ValueError):   # a stage this workload does not run
                 pass
+    if clk is not None:
+        clk.mark_end()
     return step_ms, {s: (sum(v) / len(v) if v else 0.0) for s, v in stage_ms.items()}
+
+
+def read_floor(nbytes, flush, dev, reps=10):
+    """Device time of a plain contiguous read of nbytes (a torch sum over a bf16 buffer, L2
+    flushed first): the shortest time any kernel needs to stream that many bytes once on this
+    GPU, launch, ramp-up and tail included.  A reference for the gathered-KV attention of the
+    same size, not part of the method."""
+    buf = torch.ones(max(nbytes // 2, 1), dtype=torch.bfloat16, device=dev)
+    best = None
+    for _ in range(reps + 3):
+        flush_l2(flush)
+        torch.cuda._sleep(HOLD_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        buf.sum(dtype=torch.float32)
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b)
+        best = t if best is None else min(best, t)
+    del buf
+    return best
 
 
 def measure_e2e(wb, steps, warmup):
@@ -377,14 +429,15 @@ def main():
         dist.barrier()
         __graft_entry__.build()
     hbm_peak, tf_peak, peak_kind = peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
+             torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
     wb = Workbench(w, dev)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        step_ms, stage_ms = measure(wb, args.steps, args.warmup, flush)
+        step_ms, stage_ms = measure(wb, args.steps, args.warmup, flush, clk=clk)
         total_ms = sum(step_ms)
         if dist is not None:
             t = torch.tensor([total_ms], device=dev)
@@ -424,11 +477,13 @@ def main():
         if "flops" in k:
             k["TFLOPs"] = k["flops"] / (ms * 1e9)
             k["tensor_frac"] = k["TFLOPs"] / tf_peak
+            k["bound"] = "tensor" if k["tensor_frac"] > k.get("hbm_frac", 0.0) else "hbm"
         kernels[name] = k
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     dk = kernels[dom]
     src = {"scores": "scores.cu", "attend": "attend.cu", "topk": "topk.cu", "pool": "pool.cu"}[dom]
-    if dk.get("bound") == "tensor":
+    # the kernel's bound is the resource it uses the larger fraction of
+    if dk.get("tensor_frac", 0.0) > dk.get("hbm_frac", 0.0):
         roof = {"bound": "tensor", "achieved": dk["TFLOPs"], "peak": tf_peak, "unit": "TFLOP/s",
                 "frac": dk["TFLOPs"] / tf_peak}
     else:
@@ -441,6 +496,13 @@ def main():
     roof["source"] = src
 
     e2e_ms, h2d, d2h = measure_e2e(wb, max(3, args.steps // 2), 3)
+    floor = None
+    if "attend" in kernels and w.kind == "decode":
+        fb = kernels["attend"]["bytes"]
+        fms = read_floor(fb, flush, dev)
+        floor = {"bytes": fb, "ms": fms, "GBps": fb / (fms * 1e6), "hbm_frac": fb / (fms * 1e6) / hbm_peak,
+                 "attend_over_floor": kernels["attend"]["ms"] / fms,
+                 "what": "plain contiguous read of the gathered-KV byte count (torch sum), L2 flushed"}
     launches = wb.launches_per_step() * args.steps
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -451,9 +513,11 @@ def main():
                        "queries_per_step": w.n_q, "depth": w.depth, "h_q": w.h_q,
                        "h_kv": w.h_kv, "dkq": w.dkq, "dv": w.dv, "v_is_k": w.v_is_k,
                        "h_idx": w.h_idx, "d_idx": w.d_idx, "compress_ratio": w.compress_ratio,
-                       "indexer_top_k": w.indexer_top_k, "l2": "flushed (512 MB write) "
-                       "before every timed step, outside the timed events"},
+                       "indexer_top_k": w.indexer_top_k, "l2": "flushed before every timed "
+                       "step outside the timed events (512 MB written, then 256 MB of another "
+                       "buffer read)"},
             "gathered_kv_GBps": kernels.get("attend", {}).get("GBps"),
+            "gathered_kv_read_floor": floor,
             "gathered_kv_hbm_frac": kernels.get("attend", {}).get("hbm_frac"),
             "roofline": roof, "kernels": kernels,
             "e2e": {"value": n_q_total / (e2e_ms / 1000.0), "unit": "tokens/s",

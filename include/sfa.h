@@ -102,7 +102,7 @@ int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_
  *           <= score_stride).
  * The q.kbar contraction runs on tcgen05 tensor cores (bf16 x (hi, lo) into an fp32 TMEM
  * accumulator); the ReLU, weights and head sum run in the TMEM read-back.
- * Limits: d_idx in {64, 128}; h_idx in [1, 32]; h_idx * 16 <= 256.
+ * Limits: d_idx in {64, 128}; h_idx in {4, 8, 16}; n_seq * blk_cap < 2^31.
  */
 int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
                      const int32_t *q_pos, int n_q, int q_group, int h_idx, int d_idx,
@@ -145,8 +145,10 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
  *   workspace: sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, top_k*cr + cr - 1) bytes
  *           (split-KV partial results; may be NULL when that size is 0).
  * Query head h reads KV head h / (h_q / h_kv).  p_i < n_tok_cap is required.
- * Limits (bf16): dkq in {64, 128, 512, 576}, dv in {64, 128, 512}, dv <= dkq, h_q/h_kv <= 16.
- *        (fp32): dkq, dv <= 576 and multiples of 4, h_q/h_kv <= 16.
+ * Limits (bf16): (dkq, dv) in {(576, 512), (512, 512), (128, 128), (64, 64)}, h_q/h_kv <= 16;
+ *        dv > dkq needs a separate V.  SFA_ATTEND_KERNEL=tcgen05 in the environment selects the
+ *        tcgen05 kernel for dkq 576 / 512 (default: the mma.sync kernel; same results).
+ *        (fp32): the same (dkq, dv) pairs and h_q/h_kv <= 16.
  */
 size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max);
 int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
