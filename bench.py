@@ -69,7 +69,7 @@ def recorded_traffic(kernel, workload):
 
 
 # ------------------------------------------------------------------ algorithmic work per step
-def algorithmic(w, attended):
+def algorithmic(w, attended, bounded=False):
     """Bytes / FLOPs each stage must move / do for one step of workload w (one rank).
 
     attended[i] = |A_i|, the number of cells query i attends (kept blocks * cr + tail).
@@ -80,13 +80,14 @@ def algorithmic(w, attended):
     cr = w.compress_ratio
     nb = [(w.depth + j + 1) // cr for j in range(w.n_q_per_seq)] * w.n_seq
     kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
+    per_blk = (2 if bounded else 4) * w.d_idx   # bounded selection: the hi halves only
     if w.kind == "decode":
-        kbar_bytes = sum(b * 4 * w.d_idx for b in nb)
+        kbar_bytes = sum(b * per_blk for b in nb)
     else:
-        kbar_bytes = w.n_seq * max(nb) * 4 * w.d_idx
+        kbar_bytes = w.n_seq * max(nb) * per_blk
     return {
         "kbar_bytes": kbar_bytes,
-        "score_bytes": sum(b * 4 for b in nb),
+        "score_bytes": sum(b * (8 if bounded else 4) for b in nb),   # + the bounds
         "score_flops": sum(b * 2 * w.h_idx * w.d_idx for b in nb),
         "gathered_kv_bytes": sum(a * kv_row for a in attended),
         "attend_flops": sum(a * 2 * w.h_q * (w.dkq + w.dv) for a in attended),
@@ -166,7 +167,7 @@ class ClockSampler:
 class Workbench:
     """Inputs, buffers and one step of the method for workload w on the current device."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, bounded=None):
         self.w, self.dev = w, dev
         self.case = sfa.make_case(w, device=dev)
         self.n_blk_max = w.n_tok // w.compress_ratio
@@ -174,7 +175,7 @@ class Workbench:
                                 h_kv=w.h_kv, dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                                 compress_ratio=w.compress_ratio,
                                 indexer_top_k=w.indexer_top_k, n_blk_max=self.n_blk_max,
-                                q_group=w.n_q_per_seq, device=dev)
+                                q_group=w.n_q_per_seq, bounded=bounded, device=dev)
         # the cache state before the step: every block completed by earlier tokens is pooled
         self.first_new_blk = w.depth // w.compress_ratio
         self.step.pool(self.case["X"], 0, self.first_new_blk)
@@ -187,7 +188,10 @@ class Workbench:
         n = 1 if self.new_blocks[1] > self.new_blocks[0] else 0
         if not st.dense:
             n += 1  # scores
-            n += 1 + (B.sfa_topk_workspace_bytes(w.n_q, self.n_blk_max, w.indexer_top_k) > 0)
+            if st.bounded:
+                n += 2  # refine + the final selection
+            else:
+                n += 1 + (B.sfa_topk_workspace_bytes(w.n_q, self.n_blk_max, w.indexer_top_k) > 0)
             n_kv = w.indexer_top_k * w.compress_ratio + w.compress_ratio - 1
         else:
             n_kv = st.n_kv_dense
@@ -205,15 +209,11 @@ class Workbench:
         if not st.dense:
             if "scores" in ev:
                 ev["scores"][0].record()
-            B.sfa_index_scores(c["q_idx"], c["w"], c["q_seq"], c["q_pos"], st.Kbar,
-                               w.compress_ratio, st.n_blk_max, st.scores, q_group=st.q_group,
-                               dev_status=st.status)
+            st.score(c["q_idx"], c["w"], c["q_seq"], c["q_pos"])
             if "scores" in ev:
                 ev["scores"][1].record()
                 ev["topk"][0].record()
-            B.sfa_topk_blocks(st.scores, c["q_pos"], w.compress_ratio, w.indexer_top_k,
-                              st.n_blk_max, st.blk_idx, st.n_sel, workspace=st.topk_ws,
-                              dev_status=st.status)
+            st.topk(c["q_idx"], c["w"], c["q_seq"], c["q_pos"])
             if "topk" in ev:
                 ev["topk"][1].record()
         if "attend" in ev:
@@ -399,6 +399,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-second", action="store_true", help="skip the pp2048 companion line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--exact", action="store_true",
+                    help="decode: exact scores + select instead of the bounded selection")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller runs for ncu captures)")
     args = ap.parse_args()
@@ -432,7 +434,7 @@ def main():
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
              torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
-    wb = Workbench(w, dev)
+    wb = Workbench(w, dev, bounded=False if args.exact else None)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -453,7 +455,7 @@ def main():
     tail = [(int(p) + 1) % w.compress_ratio for p in wb.case["q_pos"].cpu()]
     attended = [int(n) * w.compress_ratio + t for n, t in zip(n_sel, tail)] if not wb.step.dense \
         else [int(p) + 1 for p in wb.case["q_pos"].cpu()]
-    alg = algorithmic(w, attended)
+    alg = algorithmic(w, attended, wb.step.bounded)
     kernels = {}
     for name, ms in stage_ms.items():
         if ms <= 0 or (name == "pool" and wb.new_blocks[1] <= wb.new_blocks[0]):
@@ -513,7 +515,9 @@ def main():
                        "queries_per_step": w.n_q, "depth": w.depth, "h_q": w.h_q,
                        "h_kv": w.h_kv, "dkq": w.dkq, "dv": w.dv, "v_is_k": w.v_is_k,
                        "h_idx": w.h_idx, "d_idx": w.d_idx, "compress_ratio": w.compress_ratio,
-                       "indexer_top_k": w.indexer_top_k, "l2": "flushed before every timed "
+                       "indexer_top_k": w.indexer_top_k,
+                       "selection": "bounded" if wb.step.bounded else "exact",
+                       "l2": "flushed before every timed "
                        "step outside the timed events (512 MB written, then 256 MB of another "
                        "buffer read)"},
             "gathered_kv_GBps": kernels.get("attend", {}).get("GBps"),
@@ -524,6 +528,12 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches, "clocks": clk.summary(), "device_status": status}
+    if wb.step.bounded:   # candidates per query the bounds could not rule out
+        nb = max(wb.n_blk_max, 1)
+        cn = wb.step.refine_ws.view(torch.int32)[2 * w.n_q * nb: 2 * w.n_q * nb + w.n_q].cpu()
+        cn = [int(x) for x in cn if int(x) >= 0]
+        line["bounded_selection"] = {"candidates_per_query_mean": (sum(cn) / len(cn)) if cn else 0,
+                                     "candidates_per_query_max": max(cn) if cn else 0}
     del wb
     torch.cuda.empty_cache()
 
@@ -535,7 +545,7 @@ def main():
         n_sel2 = wb2.step.n_sel.cpu()
         att2 = [int(n) * w2.compress_ratio + (int(p) + 1) % w2.compress_ratio
                 for n, p in zip(n_sel2, wb2.case["q_pos"].cpu())]
-        a2 = algorithmic(w2, att2)
+        a2 = algorithmic(w2, att2, wb2.step.bounded)
         line["pp2048"] = {
             "workload": w2.name, "value": w2.n_q / (ms2 / 1000.0), "unit": "tokens/s",
             "ms_per_step": ms2, "stage_ms": st2,

@@ -133,6 +133,50 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
                     int32_t *dev_status, sfa_stream_t stream);
 
 /*
+ * sfa_index_scores_bounded / sfa_topk_blocks_refine -- the same kept sets as
+ * sfa_index_scores + sfa_topk_blocks from half the pooled-key bytes (a library addition: the
+ * pages score and select in one pass each).
+ *
+ * sfa_index_scores_bounded: arguments as sfa_index_scores; it reads only the hi halves of
+ * the pooled keys and writes lower and upper bounds of the hi + lo score s_ib:
+ *   lower, upper [n_q][score_stride] fp32: lower = a - e <= s_ib <= a + e = upper, with
+ *           a_ib = sum_j w_ij * max(0, qidx_ij . hi_b) and
+ *           e_ib = 1.02 * 2^-9 * (sum_j |w_ij| |qidx_ij|_2) * |hi_b|_2 (the lo half is the bf16
+ *           rounding remainder, |lo| <= 2^-9/(1 - 2^-9) |hi| elementwise; ReLU is 1-Lipschitz;
+ *           Cauchy-Schwarz per head; the 2% covers the fp32 rounding of both scores).
+ * Both arrays share score_stride; entries at b >= B_i are left untouched.
+ *
+ * sfa_topk_blocks_refine: per query, L = a lower bound of the k-th largest lower bound (the
+ * k-th largest maximum of the lower bounds of groups of four consecutive blocks, rounded down
+ * to its histogram bin); every block with upper >= L is a candidate (every block of the top k
+ * by s is one, and so is every block whose s ties the k-th); the candidates are rescored from
+ * hi + lo (bf16 products, fp32 sums) and the top indexer_top_k of them by (score desc, block
+ * asc) are written as sfa_topk_blocks writes them.  One kernel launch; each query's row is
+ * split over a cluster of four CTAs.
+ *   lower, upper: as written by sfa_index_scores_bounded for the same queries and Kbar
+ *   q_idx, w, q_seq, q_pos, Kbar, kbar_seq_stride, n_seq: as given to it; Kbar 16-byte
+ *           aligned with kbar_seq_stride a multiple of 8, q_idx 4-byte aligned
+ *   blk_idx, n_sel: as sfa_topk_blocks
+ *   workspace: sfa_topk_refine_workspace_bytes(n_q, n_blk_max) bytes of device memory (used
+ *           for candidate lists longer than 4096)
+ * Limits: n_blk_max <= 36864; 1 <= top_k <= 2048; d_idx in {64, 128}; 1 <= h_idx <= 16.
+ * Errors as the other entry points (host checks before any launch, SFA_DEV_* flags).
+ */
+int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
+                             const int32_t *q_pos, int n_q, int q_group, int h_idx, int d_idx,
+                             int compress_ratio, const void *Kbar, int64_t kbar_seq_stride,
+                             int n_seq, int64_t n_blk_max, float *lower, float *upper,
+                             int64_t score_stride, int32_t *dev_status, sfa_stream_t stream);
+size_t sfa_topk_refine_workspace_bytes(int n_q, int64_t n_blk_max);
+int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score_stride,
+                           const void *q_idx, const float *w, const int32_t *q_seq,
+                           const int32_t *q_pos, int n_q, int h_idx, int d_idx,
+                           const void *Kbar, int64_t kbar_seq_stride, int n_seq,
+                           int compress_ratio, int top_k, int64_t n_blk_max, int32_t *blk_idx,
+                           int32_t *n_sel, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_status, sfa_stream_t stream);
+
+/*
  * sfa_gather_attend -- softmax attention of each query over the cells of its kept blocks plus
  * its tail (PR #27970: flash attention whose K/V tile loads are gathered through a per-query
  * index list; V may be a view of the first DV dims of K; no ALiBi, no softcap).

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libsfa.so")
 SFA_OK, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA, SFA_ERR_WORKSPACE = range(5)
 SFA_BF16, SFA_F32 = 0, 1
 SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT = 1, 2, 4, 8
+SFA_REFINE_MAX_BLOCKS = 36864   # longest row sfa_topk_blocks_refine takes (one selection piece)
 
 _lib = None
 _vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -29,7 +30,13 @@ SIGNATURES = {
     "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp]),
     "sfa_index_scores": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _i64,
                                 _int, _i64, _vp, _i64, _vp, _vp]),
+    "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
+                                        _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
     "sfa_topk_workspace_bytes": (_sz, [_int, _i64, _int]),
+    "sfa_topk_refine_workspace_bytes": (_sz, [_int, _i64]),
+    "sfa_topk_blocks_refine": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int, _vp,
+                                      _i64, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp,
+                                      _vp]),
     "sfa_topk_blocks": (_int, [_vp, _i64, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp,
                                _vp]),
     "sfa_attend_workspace_bytes": (_sz, [_int, _int, _int, _int, _i64]),
@@ -122,6 +129,42 @@ def sfa_index_scores(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_ma
                                 n_blk_max, _p(scores), scores.stride(0), _p(dev_status),
                                 _stream(stream))
     _check("sfa_index_scores", rc)
+
+
+def sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_max: int,
+                             lower, upper, q_group: int = 1, dev_status=None, stream=None):
+    """lower[i][b] <= s_ib <= upper[i][b] for the hi + lo score s_ib, from the hi halves of the
+    pooled keys only."""
+    n_q, h_idx, d_idx = q_idx.shape
+    if lower.stride(0) != upper.stride(0):
+        raise ValueError("lower and upper must share a row stride")
+    rc = lib().sfa_index_scores_bounded(_p(q_idx), _p(w), _p(q_seq), _p(q_pos), n_q, q_group,
+                                        h_idx, d_idx, compress_ratio, _p(Kbar), Kbar.stride(0),
+                                        Kbar.shape[0], n_blk_max, _p(lower), _p(upper),
+                                        lower.stride(0), _p(dev_status), _stream(stream))
+    _check("sfa_index_scores_bounded", rc)
+
+
+def sfa_topk_refine_workspace_bytes(n_q: int, n_blk_max: int) -> int:
+    return int(lib().sfa_topk_refine_workspace_bytes(n_q, n_blk_max))
+
+
+def sfa_topk_blocks_refine(lower, upper, q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int,
+                           top_k: int, n_blk_max: int, blk_idx, n_sel, workspace=None,
+                           dev_status=None, stream=None):
+    """The top_k best blocks by the hi + lo score, from its lower and upper bounds: only the
+    blocks the bounds cannot rule out are rescored."""
+    n_q, h_idx, d_idx = q_idx.shape
+    need = sfa_topk_refine_workspace_bytes(n_q, n_blk_max)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_pos.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().sfa_topk_blocks_refine(_p(lower), _p(upper), lower.stride(0), _p(q_idx), _p(w),
+                                      _p(q_seq), _p(q_pos), n_q, h_idx, d_idx, _p(Kbar),
+                                      Kbar.stride(0), Kbar.shape[0], compress_ratio, top_k,
+                                      n_blk_max, _p(blk_idx), _p(n_sel), _p(workspace),
+                                      ws_bytes, _p(dev_status), _stream(stream))
+    _check("sfa_topk_blocks_refine", rc)
 
 
 def sfa_topk_workspace_bytes(n_q: int, n_blk_max: int, top_k: int) -> int:

@@ -29,13 +29,21 @@ namespace {
 constexpr int kBM = 128;               // blocks per tile (MMA M)
 constexpr int kThreads = 192;          // 6 warps
 constexpr int kSlabBytes = kBM * 128;  // one pipeline stage
+// The bounded mode's error bound per score: |s - a| <= kLoRel * C_q * |hi_b|_2 (+ kAbs), where
+// the lo half of a pooled key is the rounding remainder of bf16(m): |lo_e| <= 2^-9 |m_e| <=
+// 2^-9 / (1 - 2^-9) |hi_e| (plus 2^-134 below the normal range), ReLU is 1-Lipschitz and the
+// head sum is weighted by w (Cauchy-Schwarz per head).  The factor 1.02 covers the fp32
+// rounding of the approximate dot product (128 terms: < 2^-16 relative) and of the bound.
+constexpr float kLoRel = 1.953125e-3f * 1.02f;
+constexpr float kAbs = 1e-30f;
 
 struct ScoreParams {
     const __nv_bfloat16 *q_idx;
     const float *w;
     const int32_t *q_seq;
     const int32_t *q_pos;
-    float *scores;
+    float *scores;       // exact mode: the scores; bounded mode: their lower bounds
+    float *bounds;       // bounded mode: the upper bounds (else null)
     int32_t *status;
     int64_t score_stride;
     int64_t blk_cap;
@@ -46,27 +54,32 @@ struct ScoreParams {
 template <int KP>
 struct Layout {
     static constexpr int kSlabs = KP / 64;
-    static constexpr int kABytes = kBM * KP * 2;  // one tile = kSlabs stages
 };
 
-template <int KP, int H>
+// HI = false: K' = 2 d_idx over [hi | lo] against [q | q] (the exact score).  HI = true (the
+// bounded mode): K' = d_idx over hi only against q; the score from hi, less and plus its error
+// bound (from the norm of the hi row), gives the lower and upper bounds of the exact score
+// (see sfa_index_scores_bounded).
+template <int KP, int H, bool HI>
 __global__ void __launch_bounds__(kThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap kbar_map, const ScoreParams p) {
-    using L = Layout<KP>;
+    using L = Layout<HI ? KP / 2 : KP>;   // KP: the stored row (2 d_idx); L: the slabs read
     constexpr int D = KP / 2;
+    constexpr int KB = HI ? D : KP;       // K' of the MMA chain and of the B operand
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int S = p.stages, N = p.N;
     uint8_t *sA = smem;                                    // S x kSlabBytes
-    uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x KP bf16, swizzled
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KP * 2);
+    uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x KB bf16, swizzled
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KB * 2);
     uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S,
              *acc_empty = bars + 2 * S + 2, *drain = bars + 2 * S + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_nblk = reinterpret_cast<int *>(tmem_slot + 2);  // [q_tile] visible blocks, -1 skip
     float *s_w = reinterpret_cast<float *>(s_nblk + 256);  // [q_tile * H]
+    float *s_cq = s_w + p.q_tile * H;                       // [q_tile] sum_j |w_j| |q_j|_2
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = blockIdx.y * p.q_tile;
@@ -78,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], HI ? 1 + 4 : 1);   // bounded mode: + the four norm readers
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -111,9 +124,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qq = e / H;
         s_w[e] = qq < nq_tile ? p.w[(int64_t)(q0 + qq) * H + (e % H)] : 0.f;
     }
-    // B operand: row n = (query qq, head j), K' = [q | q]; 16-byte chunks, 128-byte swizzle.
-    for (int e = threadIdx.x; e < N * (KP / 8); e += kThreads) {
-        const int n = e / (KP / 8), c = e % (KP / 8);
+    if (HI) {   // C_q = sum_j |w_j| |q_j|_2, one warp per query
+        for (int qq = warp; qq < p.q_tile; qq += kThreads / 32) {
+            float c = 0.f;
+            if (qq < nq_tile) {
+                for (int j = 0; j < H; ++j) {
+                    const __nv_bfloat16 *qv = p.q_idx + ((int64_t)(q0 + qq) * H + j) * D;
+                    float ss = 0.f;
+                    for (int e = lane; e < D; e += 32) {
+                        const float v = __bfloat162float(qv[e]);
+                        ss = fmaf(v, v, ss);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+                    c = fmaf(fabsf(p.w[(int64_t)(q0 + qq) * H + j]), sqrtf(ss), c);
+                }
+            }
+            if (lane == 0) s_cq[qq] = c;
+        }
+    }
+    // B operand: row n = (query qq, head j), K' = [q | q] (or q); 16-byte chunks, 128-byte
+    // swizzle.
+    for (int e = threadIdx.x; e < N * (KB / 8); e += kThreads) {
+        const int n = e / (KB / 8), c = e % (KB / 8);
         const int qq = n / H, j = n % H;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (qq < nq_tile && n < p.q_tile * H) {
@@ -212,6 +245,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < my_tiles; ++it) {
             const int acc = it & 1;
             if (*abort_flag) break;
+            float nrm2 = 0.f;   // bounded mode: |hi_b|^2 of this thread's block row
+            if constexpr (HI) {
+                const int r = quarter * 32 + lane;
+                bool ok = true;
+                for (int sl = 0; sl < L::kSlabs; ++sl) {
+                    const int ld = it * L::kSlabs + sl, st = ld % S;
+                    if (!mbar_wait(&full[st], (ld / S) & 1, deadline)) { ok = false; break; }
+                    const uint8_t *row = sA + (size_t)st * kSlabBytes + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float x0 = __uint_as_float(w4[q] << 16);
+                            const float x1 = __uint_as_float(w4[q] & 0xFFFF0000u);
+                            nrm2 = fmaf(x0, x0, nrm2);
+                            nrm2 = fmaf(x1, x1, nrm2);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the slab
+                }
+                if (!ok) {
+                    set_status(p.status, SFA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
             if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, deadline)) {
                 set_status(p.status, SFA_DEV_TIMEOUT);
                 *abort_flag = 1;
@@ -219,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
+            const float hn = HI ? sqrtf(nrm2) : 0.f;
             for (int c0 = 0; c0 < ncols; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tmem_base + lane_addr + (uint32_t)(acc * N + c0), r);
@@ -231,7 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < H; ++j)
                         s = fmaf(s_w[qq * H + j], fmaxf(__uint_as_float(r[g * H + j]), 0.f), s);
-                    if (b < s_nblk[qq]) p.scores[(int64_t)(q0 + qq) * p.score_stride + b] = s;
+                    if (b < s_nblk[qq]) {
+                        const int64_t o = (int64_t)(q0 + qq) * p.score_stride + b;
+                        if (HI) {
+                            const float e = fmaf(kLoRel * s_cq[qq], hn, kAbs);
+                            p.scores[o] = s - e;   // the hi + lo score lies in [s - e, s + e]
+                            p.bounds[o] = s + e;
+                        } else {
+                            p.scores[o] = s;
+                        }
+                    }
                 }
             }
             tc_fence_before();
@@ -256,24 +328,24 @@ int pow2_at_least(int v) {
     return r;
 }
 
-template <int KP, int H>
+template <int KP, int H, bool HI>
 int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
            cudaStream_t stream) {
-    const size_t b_bytes = (size_t)p.N * KP * 2;
+    const size_t b_bytes = (size_t)p.N * (HI ? KP / 2 : KP) * 2;
     // Narrow B tiles (decode) are HBM-bound streams: two CTAs per SM keep more slabs in
     // flight; wide ones (prefill) are tensor-bound: one CTA per SM with a deep pipeline.
     const int per_sm = p.N <= 32 ? 2 : 1;
     const size_t budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
-    const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * H * 4;
+    const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     if (budget < b_bytes + misc + kSlabBytes) return SFA_ERR_UNSUPPORTED;
     int stages = (int)((budget - b_bytes - misc) / kSlabBytes);
     if (stages > 16) stages = 16;
     p.stages = stages;
     const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes + 8 * (2 * stages + 5) + 8 +
-                        256 * 4 + (size_t)p.q_tile * H * 4;
+                        256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     static bool attr_set = false;
     if (!attr_set) {
-        if (!allow_max_dynamic_smem(index_score_kernel<KP, H>)) return SFA_ERR_CUDA;
+        if (!allow_max_dynamic_smem(index_score_kernel<KP, H, HI>)) return SFA_ERR_CUDA;
         attr_set = true;
     }
     // One wave: the block tiles of each query tile are split over as many CTAs as the
@@ -284,7 +356,7 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
     if (cta_per_qtile < 1) cta_per_qtile = 1;
     p.tiles_per_cta = (n_blk_tiles + cta_per_qtile - 1) / cta_per_qtile;
     const int grid_x = (n_blk_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
-    index_score_kernel<KP, H><<<dim3(grid_x, n_qtiles), kThreads, smem, stream>>>(map, p);
+    index_score_kernel<KP, H, HI><<<dim3(grid_x, n_qtiles), kThreads, smem, stream>>>(map, p);
     SFA_CHECK_LAUNCH();
     return SFA_OK;
 }
@@ -292,13 +364,14 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
 }  // namespace
 }  // namespace sfa
 
-extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
-                                const int32_t *q_pos, int n_q, int q_group, int h_idx,
-                                int d_idx, int compress_ratio, const void *Kbar,
-                                int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max,
-                                float *scores, int64_t score_stride, int32_t *dev_status,
-                                sfa_stream_t stream) {
-    using namespace sfa;
+namespace sfa {
+namespace {
+
+int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const int32_t *q_pos,
+               int n_q, int q_group, int h_idx, int d_idx, int compress_ratio, const void *Kbar,
+               int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max, float *scores,
+               float *bounds, int64_t score_stride, int32_t *dev_status, cudaStream_t st) {
+    const bool hi = bounds != nullptr;
     if (!q_idx || !w || !q_seq || !q_pos || !Kbar || !scores) return SFA_ERR_INVALID_ARG;
     if (n_q < 0 || q_group < 1 || n_seq < 1 || compress_ratio < 1 || n_blk_max < 0)
         return SFA_ERR_INVALID_ARG;
@@ -316,7 +389,7 @@ extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t
 
     // Queries per tile: the largest power of two that divides q_group and fits N <= 256 (and
     // the B tile fits next to the pooled-key stages).
-    const int n_cap = (KP == 256) ? 128 : 256;
+    const int n_cap = (KP == 256 && !hi) ? 128 : 256;
     int q_tile = 1;
     while (q_tile * 2 * h_idx <= n_cap && q_group % (q_tile * 2) == 0) q_tile *= 2;
     ScoreParams p{};
@@ -325,6 +398,7 @@ extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t
     p.q_seq = q_seq;
     p.q_pos = q_pos;
     p.scores = scores;
+    p.bounds = bounds;
     p.status = dev_status;
     p.score_stride = score_stride;
     p.blk_cap = blk_cap;
@@ -349,11 +423,40 @@ extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t
     const int n_qtiles = (n_q + q_tile - 1) / q_tile;
     if (n_qtiles > 65535) return SFA_ERR_UNSUPPORTED;
     const int n_blk_tiles = (int)((n_blk_max + kBM - 1) / kBM);
-    const cudaStream_t st = (cudaStream_t)stream;
-    if (d_idx == 64 && h_idx == 4) return launch<128, 4>(map, p, n_qtiles, n_blk_tiles, st);
-    if (d_idx == 64 && h_idx == 8) return launch<128, 8>(map, p, n_qtiles, n_blk_tiles, st);
-    if (d_idx == 64 && h_idx == 16) return launch<128, 16>(map, p, n_qtiles, n_blk_tiles, st);
-    if (d_idx == 128 && h_idx == 4) return launch<256, 4>(map, p, n_qtiles, n_blk_tiles, st);
-    if (d_idx == 128 && h_idx == 8) return launch<256, 8>(map, p, n_qtiles, n_blk_tiles, st);
-    return launch<256, 16>(map, p, n_qtiles, n_blk_tiles, st);
+#define SFA_SCORES_LAUNCH(KP_, H_)                                                            \
+    return hi ? launch<KP_, H_, true>(map, p, n_qtiles, n_blk_tiles, st)                      \
+              : launch<KP_, H_, false>(map, p, n_qtiles, n_blk_tiles, st)
+    if (d_idx == 64 && h_idx == 4) SFA_SCORES_LAUNCH(128, 4);
+    if (d_idx == 64 && h_idx == 8) SFA_SCORES_LAUNCH(128, 8);
+    if (d_idx == 64 && h_idx == 16) SFA_SCORES_LAUNCH(128, 16);
+    if (d_idx == 128 && h_idx == 4) SFA_SCORES_LAUNCH(256, 4);
+    if (d_idx == 128 && h_idx == 8) SFA_SCORES_LAUNCH(256, 8);
+    SFA_SCORES_LAUNCH(256, 16);
+#undef SFA_SCORES_LAUNCH
+}
+
+}  // namespace
+}  // namespace sfa
+
+extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t *q_seq,
+                                const int32_t *q_pos, int n_q, int q_group, int h_idx,
+                                int d_idx, int compress_ratio, const void *Kbar,
+                                int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max,
+                                float *scores, int64_t score_stride, int32_t *dev_status,
+                                sfa_stream_t stream) {
+    return sfa::run_scores(q_idx, w, q_seq, q_pos, n_q, q_group, h_idx, d_idx, compress_ratio,
+                           Kbar, kbar_seq_stride, n_seq, n_blk_max, scores, nullptr,
+                           score_stride, dev_status, (cudaStream_t)stream);
+}
+
+extern "C" int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
+                                        const int32_t *q_pos, int n_q, int q_group, int h_idx,
+                                        int d_idx, int compress_ratio, const void *Kbar,
+                                        int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max,
+                                        float *lower, float *upper, int64_t score_stride,
+                                        int32_t *dev_status, sfa_stream_t stream) {
+    if (!upper || !sfa::aligned16(upper)) return SFA_ERR_INVALID_ARG;
+    return sfa::run_scores(q_idx, w, q_seq, q_pos, n_q, q_group, h_idx, d_idx, compress_ratio,
+                           Kbar, kbar_seq_stride, n_seq, n_blk_max, lower, upper, score_stride,
+                           dev_status, (cudaStream_t)stream);
 }

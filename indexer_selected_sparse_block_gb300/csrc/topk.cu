@@ -8,19 +8,24 @@
 // llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM" are padded the same way).
 //
 // Exact and deterministic without sorting.  A 1024-thread CTA takes a piece of at most 36864
-// elements and holds it in registers, R consecutive elements per thread, read with 16-byte
-// loads; each score becomes its order-preserving 32-bit key.  The k-th largest of the 1024
-// per-thread maxima is at most the k-th largest key T (the maxima are a subset), so the floor
-// of its 12-bit histogram bin bounds T from below: only the keys at or above it (k and a few
+// elements: coalesced 16-byte loads stage it in shared memory, and each thread then holds R
+// consecutive elements in registers as order-preserving 32-bit keys.  The k-th largest of the
+// 1024 per-thread maxima is at most the k-th largest key T (the maxima are a subset), so the
+// floor of its histogram bin bounds T from below; the bins are 12-bit windows sized to the
+// range the maxima span, so the bound is tight.  Only the keys at or above it (k and a few
 // per cent more on score rows) are compacted, in index order, into shared memory, where a
-// radix select (bits 31..20, 19..8, 7..0) finds T and the keys equal to T are ranked lower
-// index first.  Kept candidates set their bit in their owner thread's mask; a scan of the
-// per-thread kept counts gives each thread its output offset, so the kept ids come out
-// ascending with no sort.  Pieces with too many candidates, or many equal keys at the cut,
-// run the same digits over the registers and rank the equal keys by a block-wide scan.
+// radix select whose 12-bit digit windows are again sized to the candidates' range finds T
+// (one pass for most rows, at most three).  A single block scan over the candidate list, of
+// the counts above T and equal to T packed in one word, then gives every kept candidate its
+// output slot, the keys equal to T ranked lower index first, so the kept ids come out
+// ascending with no sort.  Pieces with too many candidates (many equal keys, or a budget above
+// the thread count) run fixed 12/12/8-bit digits over the registers and rank the keys equal
+// to T by a block-wide scan.
 // A row longer than one piece is cut into chunks: each chunk keeps its own top k as (score
 // bits, id) candidates in chunk order (the global top k lies in their union, the order being
 // total), and the next level selects among them the same way, until one piece holds the row.
+#include <cooperative_groups.h>
+
 #include "sfa_common.cuh"
 
 namespace sfa {
@@ -32,9 +37,10 @@ constexpr int kPerSm = 1;                 // resident CTAs per SM
 constexpr int kBins = 4096;               // 12-bit digits
 constexpr int kMaxR = 36;                 // elements per thread
 constexpr int kChunk = kMaxR * kThreads;  // 36864: the largest piece
-constexpr int kMaxCand = 4096;            // candidates resolved from a compacted list
-constexpr int kMaxEqRank = 256;           // keys equal to T that are ranked pairwise
+constexpr int kMaxCand = 4 * kThreads;    // candidates resolved from a compacted list
 constexpr int kMaxLevels = 8;
+constexpr int kAllEq = 0x7FFFFFFF;        // Cut::take_eq: every key equal to T is kept
+static_assert(kWarps == 32, "one warp reduces the per-warp values");
 
 // Order-preserving image of a score: larger score -> larger key; -0 == +0; NaN lowest.
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -52,11 +58,20 @@ __device__ __forceinline__ uint32_t key_bits(uint32_t key) {
 struct __align__(16) Smem {
     int hist[kBins];
     uint32_t cand_key[kMaxCand];   // the candidate keys, in index order
-    int cand_idx[kMaxCand];
-    unsigned long long kept[kThreads];   // candidates kept, one bit per element of a thread
+    int cand_idx[kMaxCand];        // their element index within the piece
     int wsum[kWarps + 1];
+    uint32_t wred[3][kWarps];      // per-warp extrema
     int cut_bin, cut_above, cut_cnt;
+    uint32_t kmin;
 };
+// The piece is staged right after Smem: R * kThreads words, 16-byte aligned (so is Smem's size).
+template <int R>
+constexpr size_t smem_bytes() {
+    return sizeof(Smem) + (size_t)R * kThreads * 4;
+}
+__device__ __forceinline__ uint32_t *staged(Smem &sh) {
+    return reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(&sh) + sizeof(Smem));
+}
 
 // Exclusive scan of one value per thread (thread order); *total gets the sum.
 __device__ __forceinline__ int block_scan_excl(int v, Smem &sh, int *total) {
@@ -118,6 +133,262 @@ __device__ __forceinline__ void clear_hist(Smem &sh, int nbins) {
     __syncthreads();
 }
 
+// Words [0, n) of src into dst (shared memory, 16-byte aligned), n <= R * kThreads: coalesced
+// 16-byte loads over the aligned body, single words at its two ends.
+template <int R>
+__device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t *dst) {
+    const int tid = threadIdx.x;
+    int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u)) & 15u) >> 2);
+    head = head < n ? head : n;
+    const int nvec = (n - head) >> 2;
+    const int tail0 = head + 4 * nvec;
+    const uint4 *v = reinterpret_cast<const uint4 *>(src + head);
+    uint4 x[R / 4];
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+        const int q = tid + m * kThreads;
+        x[m] = q < nvec ? __ldg(v + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid < head) dst[tid] = __ldg(src + tid);
+    if (tid < n - tail0) dst[tail0 + tid] = __ldg(src + tail0 + tid);
+    if (head == 0) {
+#pragma unroll
+        for (int m = 0; m < R / 4; ++m) {
+            const int q = tid + m * kThreads;
+            if (q < nvec) reinterpret_cast<uint4 *>(dst)[q] = x[m];
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < R / 4; ++m) {
+            const int q = tid + m * kThreads;
+            if (q < nvec) {
+                uint32_t *d = dst + head + 4 * q;
+                d[0] = x[m].x;
+                d[1] = x[m].y;
+                d[2] = x[m].z;
+                d[3] = x[m].w;
+            }
+        }
+    }
+}
+
+// Key of -inf: keys below it are NaN images only (order_key maps every NaN to 0).
+constexpr uint32_t kNegInfKey = 0x007FFFFFu;
+
+// This thread's R staged scores from e0 (a NaN past the nv valid ones: no comparison keeps
+// it and fmaxf skips it).
+template <int R>
+__device__ __forceinline__ void load_vals(const uint32_t *stg, int e0, int nv, float (&v)[R]) {
+    const float past = __uint_as_float(0x7FFFFFFFu);
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+        const uint4 w = reinterpret_cast<const uint4 *>(stg + e0)[m];
+        v[4 * m] = 4 * m < nv ? __uint_as_float(w.x) : past;
+        v[4 * m + 1] = 4 * m + 1 < nv ? __uint_as_float(w.y) : past;
+        v[4 * m + 2] = 4 * m + 2 < nv ? __uint_as_float(w.z) : past;
+        v[4 * m + 3] = 4 * m + 3 < nv ? __uint_as_float(w.w) : past;
+    }
+}
+
+// Block-wide maximum of a and minima of b and c (one value of each per thread).
+__device__ __forceinline__ void block_extrema(uint32_t a, uint32_t b, uint32_t c, Smem &sh,
+                                              uint32_t &amax, uint32_t &bmin, uint32_t &cmin) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    a = __reduce_max_sync(0xFFFFFFFFu, a);
+    b = __reduce_min_sync(0xFFFFFFFFu, b);
+    c = __reduce_min_sync(0xFFFFFFFFu, c);
+    if (lane == 0) {
+        sh.wred[0][warp] = a;
+        sh.wred[1][warp] = b;
+        sh.wred[2][warp] = c;
+    }
+    __syncthreads();
+    amax = __reduce_max_sync(0xFFFFFFFFu, sh.wred[0][lane]);
+    bmin = __reduce_min_sync(0xFFFFFFFFu, sh.wred[1][lane]);
+    cmin = __reduce_min_sync(0xFFFFFFFFu, sh.wred[2][lane]);
+}
+
+// The smallest s with (span >> s) < kBins: 12-bit bins over a range of span + 1 keys.
+__device__ __forceinline__ int bin_shift(uint32_t span) {
+    const int bits = 32 - __clz((int)span);
+    return bits > 12 ? bits - 12 : 0;
+}
+
+// The cut at the k-th largest key T: the keys above T are kept, and of the keys equal to T the
+// first take_eq in index order (kAllEq: all of them).  nc candidates sit in sh.cand_* in index
+// order; nc < 0: they were too many, nothing was compacted.
+struct Cut {
+    uint32_t T;
+    int take_eq;
+    int nc;
+};
+
+// The cut at the k-th largest of the nc keys in sh.cand_key (1 <= k <= nc), all within
+// [lo, kmax]: a radix select whose 12-bit digit windows are sized to the range still open,
+// from [lo, kmax] down to single keys (at most three passes).  sh.hist is zero on entry and on
+// return; the returned nc is left for the caller.
+__device__ Cut cut_candidates(Smem &sh, int nc, int k, uint32_t lo, uint32_t kmax) {
+    const int tid = threadIdx.x;
+    Cut cut;
+    cut.nc = nc;
+    uint32_t base = lo;
+    uint64_t top = (uint64_t)kmax + 1;
+    int s = bin_shift(kmax - lo);
+    int rem = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        for (int q = tid; q < nc; q += kThreads) {
+            const uint32_t kq = sh.cand_key[q];
+            if (kq >= base && (uint64_t)kq < top) atomicAdd(&sh.hist[(kq - base) >> s], 1);
+        }
+        __syncthreads();
+        find_cut(sh, kBins, rem);
+        const int bin = sh.cut_bin, above = sh.cut_above, c = sh.cut_cnt;
+        clear_hist(sh, kBins);
+        rem -= above;
+        base += (uint32_t)bin << s;
+        if (c == rem || s == 0) {   // the whole cut bin is kept / the cut bin is one key
+            cut.T = base;
+            cut.take_eq = c == rem ? kAllEq : rem;
+            return cut;
+        }
+        top = (uint64_t)base + ((uint64_t)1 << s);
+        s = s > 12 ? s - 12 : 0;
+    }
+    cut.T = base;   // not reached: s is 0 by the third pass
+    cut.take_eq = rem;
+    return cut;
+}
+
+// The cut over the block's n staged scores (this thread's nv from element e0; 1 <= k < n),
+// from the compacted candidates.  sh.hist is zero on entry and on return.
+template <int R>
+__device__ Cut select_cut(const uint32_t *stg, int e0, int nv, int n, int k, Smem &sh) {
+    uint32_t mx;
+    {
+        float v[R];
+        load_vals<R>(stg, e0, nv, v);
+        float mxf = v[0];
+#pragma unroll
+        for (int j = 1; j < R; ++j) mxf = fmaxf(mxf, v[j]);
+        mx = nv > 0 ? order_key(mxf) : 0u;   // all-NaN: 0, like their keys
+    }
+    uint32_t kmax, mxmin, unused;
+    block_extrema(mx, nv > 0 ? mx : 0xFFFFFFFFu, 0xFFFFFFFFu, sh, kmax, mxmin, unused);
+    // ---- a lower bound of T: the floor of the bin of the k-th largest per-thread maximum (the
+    // maxima are a subset of the keys, so their k-th largest is <= T), bins sized to their range
+    uint32_t lo = 0;
+    if (k <= (n + R - 1) / R) {   // at least k threads hold elements, so k maxima exist
+        const int s = bin_shift(kmax - mxmin);
+        if (nv > 0) atomicAdd(&sh.hist[(mx - mxmin) >> s], 1);
+        __syncthreads();
+        find_cut(sh, kBins, k);
+        lo = mxmin + ((uint32_t)sh.cut_bin << s);
+        clear_hist(sh, kBins);
+    }
+    // ---- candidates: the keys >= lo (at least k), compacted in index order.  Above the key of
+    // -inf, lo is a float's key and the test is a float comparison (NaNs fail it, as their key
+    // 0 fails key >= lo); below, it runs on keys.
+    uint64_t cm = 0;
+    float v[R];   // read again: not held across the barriers above
+    load_vals<R>(stg, e0, nv, v);
+    if (lo >= kNegInfKey) {
+        const float lof = __uint_as_float(key_bits(lo));
+#pragma unroll
+        for (int j = 0; j < R; ++j) cm |= (uint64_t)(v[j] >= lof) << j;
+    } else {
+#pragma unroll
+        for (int j = 0; j < R; ++j) cm |= (uint64_t)(j < nv && order_key(v[j]) >= lo) << j;
+    }
+    int nc;
+    int pos = block_scan_excl(__popcll(cm), sh, &nc);
+    Cut cut;
+    cut.T = 0;
+    cut.take_eq = 0;
+    cut.nc = nc <= kMaxCand ? nc : -1;
+    if (cut.nc < 0) return cut;
+    for (uint64_t m = cm; m; m &= m - 1) {
+        const int j = __ffsll((long long)m) - 1;
+        sh.cand_key[pos] = order_key(__uint_as_float(stg[e0 + j]));
+        sh.cand_idx[pos] = e0 + j;
+        ++pos;
+    }
+    __syncthreads();
+    const Cut c = cut_candidates(sh, nc, k, lo, kmax);
+    cut.T = c.T;
+    cut.take_eq = c.take_eq;
+    return cut;
+}
+
+// Calls f(slot, key, idx) for every kept candidate, slot = its place among the kept ones in
+// index order: one block scan of the counts above T and equal to T (packed in one word; each
+// thread takes four consecutive candidates).
+template <class F>
+__device__ __forceinline__ void for_each_kept(const Cut &cut, Smem &sh, F f) {
+    const int q0 = threadIdx.x * 4;
+    uint32_t kk[4];
+    int ngt = 0, neq = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const bool ok = q0 + u < cut.nc;
+        kk[u] = ok ? sh.cand_key[q0 + u] : 0u;
+        ngt += (ok && kk[u] > cut.T) ? 1 : 0;
+        neq += (ok && kk[u] == cut.T) ? 1 : 0;
+    }
+    int tot;
+    const int ex = block_scan_excl(ngt | (neq << 16), sh, &tot);   // fields stay below 2^13
+    int gt = ex & 0xFFFF, eq = ex >> 16;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (q0 + u < cut.nc) {
+            if (kk[u] > cut.T) {
+                f(gt + (eq < cut.take_eq ? eq : cut.take_eq), kk[u], sh.cand_idx[q0 + u]);
+                ++gt;
+            } else if (kk[u] == cut.T) {
+                if (eq < cut.take_eq) f(gt + eq, kk[u], sh.cand_idx[q0 + u]);
+                ++eq;
+            }
+        }
+    }
+}
+
+// The key of this thread's staged element j (0 past the nv valid ones).
+__device__ __forceinline__ uint32_t staged_key(const uint32_t *stg, int e0, int nv, int j) {
+    return j < nv ? order_key(__uint_as_float(stg[e0 + j])) : 0u;
+}
+
+// The cut over the staged piece when the candidates do not fit: fixed digits (bits 31..20,
+// 19..8, 7..0) down to the exact key T; take_eq of the cnt_eq keys equal to T are kept.
+// sh.hist is zero on entry and on return.
+struct RegCut {
+    uint32_t T;
+    int take_eq, cnt_eq;
+};
+template <int R>
+__device__ RegCut cut_staged(const uint32_t *stg, int e0, int nv, int k, Smem &sh) {
+    uint32_t prefix = 0;
+    int rem = k, cnt = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+        const int fixed = pass == 1 ? 20 : 8;   // the bits above this digit, fixed by now
+        const uint32_t mask = pass == 2 ? 0xFFu : 0xFFFu;
+#pragma unroll 4
+        for (int j = 0; j < nv; ++j) {
+            const uint32_t kj = staged_key(stg, e0, nv, j);
+            if (pass == 0 || (kj >> fixed) == (prefix >> fixed))
+                atomicAdd(&sh.hist[(kj >> shift) & mask], 1);
+        }
+        __syncthreads();
+        find_cut(sh, (int)mask + 1, rem);
+        prefix |= (uint32_t)sh.cut_bin << shift;
+        rem -= sh.cut_above;
+        cnt = sh.cut_cnt;
+        clear_hist(sh, (int)mask + 1);
+    }
+    return RegCut{prefix, rem, cnt};
+}
+
 struct TopkParams {
     const float *scores;            // level 0 input
     const int32_t *q_pos;
@@ -163,9 +434,11 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
     static_assert(R % 4 == 0 && R <= 64, "16-byte loads, one kept bit per element");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem &sh = *reinterpret_cast<Smem *>(smem_raw);
+    uint32_t *stg = staged(sh);
     const int tid = threadIdx.x;
     const int k = p.top_k;
     const int n_items = n_q * n_chunks;
+    clear_hist(sh, kBins);   // kept zero between items from here on
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int i = item / n_chunks, c = item % n_chunks;
         int64_t len = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
@@ -195,197 +468,553 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
             continue;
         }
         // ---- this thread's R consecutive elements, as keys (0 past the piece: never kept)
+        stage_piece<R>(src, n, stg);
+        __syncthreads();
         const int e0 = tid * R;
         const int nv = n - e0 < 0 ? 0 : (n - e0 < R ? n - e0 : R);
-        uint32_t key[R];
-        const uint32_t *mine = src + e0;
-        if (nv == R && (reinterpret_cast<uintptr_t>(mine) & 15u) == 0) {
-#pragma unroll
-            for (int m = 0; m < R / 4; ++m) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(mine) + m);
-                key[4 * m] = order_key(__uint_as_float(v.x));
-                key[4 * m + 1] = order_key(__uint_as_float(v.y));
-                key[4 * m + 2] = order_key(__uint_as_float(v.z));
-                key[4 * m + 3] = order_key(__uint_as_float(v.w));
+        const Cut cut = select_cut<R>(stg, e0, nv, n, k, sh);
+        if (cut.nc >= 0) {
+            // ---- ascending write-out from the candidate list
+            if (p.final_stage) {
+                int32_t *out = p.blk_idx + (int64_t)i * k;
+                for_each_kept(cut, sh, [&](int slot, uint32_t, int idx) {
+                    if (slot < k) out[slot] = p.level == 0 ? idx : in_id[idx];
+                });
+            } else {
+                uint32_t *ob = p.out_bits + (int64_t)i * p.out_stride + (int64_t)c * k;
+                int32_t *oi = p.out_id + (int64_t)i * p.out_stride + (int64_t)c * k;
+                for_each_kept(cut, sh, [&](int slot, uint32_t kq, int idx) {
+                    if (slot < k) {
+                        ob[slot] = key_bits(kq);
+                        oi[slot] = p.level == 0 ? (int)(b0 + idx) : in_id[b0 + idx];
+                    }
+                });
             }
         } else {
-#pragma unroll
-            for (int j = 0; j < R; ++j) key[j] = j < nv ? order_key(__uint_as_float(__ldg(mine + j))) : 0u;
-        }
-        // ---- a lower bound of T: the floor of the cut bin of the k-th largest per-thread
-        // maximum (the maxima are a subset of the keys, so their k-th largest is <= T)
-        uint32_t lo = 0;
-        if (k <= (n + R - 1) / R) {   // at least k threads hold elements, so k maxima exist
-            uint32_t mx = 0;
-#pragma unroll
-            for (int j = 0; j < R; ++j) mx = key[j] > mx ? key[j] : mx;   // 0 past the piece
-            clear_hist(sh, kBins);
-            if (nv > 0) atomicAdd(&sh.hist[mx >> 20], 1);
-            __syncthreads();
-            find_cut(sh, kBins, k);
-            lo = (uint32_t)sh.cut_bin << 20;
-        }
-        // ---- candidates: the keys >= lo (at least k), compacted in index order
-        uint64_t candm = 0;
-        {
-            const uint64_t valid = nv ? ~0ull >> (64 - nv) : 0ull;
-#pragma unroll
-            for (int j = 0; j < R; ++j) candm |= (uint64_t)(key[j] >= lo) << j;
-            candm &= valid;
-        }
-        int nc;
-        int cpos = block_scan_excl(__popcll(candm), sh, &nc);
-        uint64_t keep = 0;
-        bool fallback = nc > kMaxCand;
-        if (!fallback) {
-            sh.kept[tid] = 0ull;
-            for (uint64_t m = candm; m; m &= m - 1) {
-                const int j = __ffsll((long long)m) - 1;
-                uint32_t kj = 0;
-#pragma unroll
-                for (int jj = 0; jj < R; ++jj) kj = jj == j ? key[jj] : kj;   // register pick
-                sh.cand_key[cpos] = kj;
-                sh.cand_idx[cpos] = e0 + j;
-                ++cpos;
-            }
-            // ---- exact radix select over the candidates: T and the keys equal to it to take
-            __syncthreads();
-            clear_hist(sh, kBins);
-            for (int q = tid; q < nc; q += kThreads) atomicAdd(&sh.hist[sh.cand_key[q] >> 20], 1);
-            __syncthreads();
-            find_cut(sh, kBins, k);
-            const uint32_t binA = (uint32_t)sh.cut_bin;
-            int rem = k - sh.cut_above;
-            uint32_t T = binA << 20;      // keys >= T are kept (all unless take_eq < cnt_eq)
-            int take_eq = 0, cnt_eq = 0;  // keys == T to keep (lowest ids first) / present
-            if (sh.cut_cnt != rem) {
-                __syncthreads();
-                clear_hist(sh, kBins);
-                for (int q = tid; q < nc; q += kThreads)
-                    if ((sh.cand_key[q] >> 20) == binA) atomicAdd(&sh.hist[(sh.cand_key[q] >> 8) & 0xFFFu], 1);
-                __syncthreads();
-                find_cut(sh, kBins, rem);
-                const uint32_t pre24 = (binA << 12) | (uint32_t)sh.cut_bin;
-                rem -= sh.cut_above;
-                T = pre24 << 8;
-                if (sh.cut_cnt != rem) {
-                    __syncthreads();
-                    clear_hist(sh, 256);
-                    for (int q = tid; q < nc; q += kThreads)
-                        if ((sh.cand_key[q] >> 8) == pre24) atomicAdd(&sh.hist[sh.cand_key[q] & 0xFFu], 1);
-                    __syncthreads();
-                    find_cut(sh, 256, rem);
-                    T = (pre24 << 8) | (uint32_t)sh.cut_bin;
-                    take_eq = rem - sh.cut_above;
-                    cnt_eq = sh.cut_cnt;
-                }
-            }
-            const bool rank_eq = take_eq < cnt_eq;
-            if (rank_eq && cnt_eq > kMaxEqRank) {
-                fallback = true;   // many equal keys at the cut: ranked by a block scan below
-            } else {
-                for (int q = tid; q < nc; q += kThreads) {
-                    const uint32_t kq = sh.cand_key[q];
-                    bool kp = kq >= T;
-                    if (kq == T && rank_eq) {   // lower index (= list position) first
-                        int r = 0;
-                        for (int u = 0; u < q; ++u) r += sh.cand_key[u] == T;
-                        kp = r < take_eq;
-                    }
-                    if (kp) {
-                        const int iq = sh.cand_idx[q];
-                        atomicOr(&sh.kept[iq / R], 1ull << (iq % R));
-                    }
-                }
-                __syncthreads();
-                keep = sh.kept[tid];
-            }
-        }
-        if (fallback) {
-            // ---- general path: the three digits and the ranking over the registers
-            keep = 0;
-            __syncthreads();
-            clear_hist(sh, kBins);
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-                if (j < nv) atomicAdd(&sh.hist[key[j] >> 20], 1);
-            __syncthreads();
-            find_cut(sh, kBins, k);
-            const uint32_t binA = (uint32_t)sh.cut_bin;
-            int rem = k - sh.cut_above;
-            uint32_t T = binA << 20;
-            int take_eq = 0, cnt_eq = 0;
-            if (sh.cut_cnt != rem) {
-                __syncthreads();
-                clear_hist(sh, kBins);
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-                    if (j < nv && (key[j] >> 20) == binA) atomicAdd(&sh.hist[(key[j] >> 8) & 0xFFFu], 1);
-                __syncthreads();
-                find_cut(sh, kBins, rem);
-                const uint32_t pre24 = (binA << 12) | (uint32_t)sh.cut_bin;
-                rem -= sh.cut_above;
-                T = pre24 << 8;
-                if (sh.cut_cnt != rem) {
-                    __syncthreads();
-                    clear_hist(sh, 256);
-#pragma unroll
-                    for (int j = 0; j < R; ++j)
-                        if (j < nv && (key[j] >> 8) == pre24) atomicAdd(&sh.hist[key[j] & 0xFFu], 1);
-                    __syncthreads();
-                    find_cut(sh, 256, rem);
-                    T = (pre24 << 8) | (uint32_t)sh.cut_bin;
-                    take_eq = rem - sh.cut_above;
-                    cnt_eq = sh.cut_cnt;
-                }
-            }
-            const bool rank_eq = take_eq < cnt_eq;
+            // ---- general path: the three digits over the staged piece, and the ranking of the
+            // keys equal to T by a block scan
+            const RegCut rc = cut_staged<R>(stg, e0, nv, k, sh);
+            const bool rank_eq = rc.take_eq < rc.cnt_eq;
             int eq_rank = 0, tot_eq;
             if (rank_eq) {   // rank of this thread's keys equal to T among all of them
                 int c_eq = 0;
-#pragma unroll
-                for (int j = 0; j < R; ++j) c_eq += (j < nv && key[j] == T) ? 1 : 0;
+                for (int j = 0; j < nv; ++j) c_eq += staged_key(stg, e0, nv, j) == rc.T ? 1 : 0;
                 eq_rank = block_scan_excl(c_eq, sh, &tot_eq);
             }
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                bool kp = false;
-                if (j < nv) {
-                    if (key[j] > T) {
-                        kp = true;
-                    } else if (key[j] == T) {
-                        kp = !rank_eq || eq_rank < take_eq;
-                        ++eq_rank;
-                    }
+            uint64_t keep = 0;
+            for (int j = 0; j < nv; ++j) {
+                const uint32_t kj = staged_key(stg, e0, nv, j);
+                bool kp = kj > rc.T;
+                if (kj == rc.T) {
+                    kp = !rank_eq || eq_rank < rc.take_eq;
+                    ++eq_rank;
                 }
                 if (kp) keep |= 1ull << j;
             }
-        }
-        // ---- output offsets, ascending write-out
-        int tot;
-        int pos = block_scan_excl(__popcll(keep), sh, &tot);
-        if (p.final_stage) {
-            int32_t *out = p.blk_idx + (int64_t)i * k;
-            for (uint64_t m = keep; m; m &= m - 1) {
-                const int j = __ffsll((long long)m) - 1;
-                out[pos++] = p.level == 0 ? e0 + j : in_id[e0 + j];
-            }
-            if (tid == 0) p.n_sel[i] = k;
-        } else {
-            uint32_t *ob = p.out_bits + (int64_t)i * p.out_stride + (int64_t)c * k;
-            int32_t *oi = p.out_id + (int64_t)i * p.out_stride + (int64_t)c * k;
-            for (uint64_t m = keep; m; m &= m - 1) {
-                const int j = __ffsll((long long)m) - 1;
-                uint32_t kj = 0;
-#pragma unroll
-                for (int jj = 0; jj < R; ++jj) kj = jj == j ? key[jj] : kj;   // register pick
-                ob[pos] = key_bits(kj);
-                oi[pos] = p.level == 0 ? (int)(b0 + e0 + j) : in_id[b0 + e0 + j];
-                ++pos;
+            int tot;
+            int pos = block_scan_excl(__popcll(keep), sh, &tot);
+            if (p.final_stage) {
+                int32_t *out = p.blk_idx + (int64_t)i * k;
+                for (uint64_t m = keep; m && pos < k; m &= m - 1) {
+                    const int j = __ffsll((long long)m) - 1;
+                    out[pos++] = p.level == 0 ? e0 + j : in_id[e0 + j];
+                }
+            } else {
+                uint32_t *ob = p.out_bits + (int64_t)i * p.out_stride + (int64_t)c * k;
+                int32_t *oi = p.out_id + (int64_t)i * p.out_stride + (int64_t)c * k;
+                for (uint64_t m = keep; m && pos < k; m &= m - 1) {
+                    const int j = __ffsll((long long)m) - 1;
+                    ob[pos] = key_bits(staged_key(stg, e0, nv, j));
+                    oi[pos] = p.level == 0 ? (int)(b0 + e0 + j) : in_id[b0 + e0 + j];
+                    ++pos;
+                }
             }
         }
+        if (tid == 0 && p.final_stage) p.n_sel[i] = k;
         __syncthreads();   // shared memory is reused by the next item
     }
+}
+
+namespace cg = cooperative_groups;
+
+// Loads group g of a row (elements 4g .. 4g+3, those below B; NaN past B).
+__device__ __forceinline__ float4 load_group(const float *row, int g, int B, bool vec) {
+    const float nan = __uint_as_float(0x7FFFFFFFu);
+    const int e = 4 * g;
+    if (vec && e + 3 < B) return __ldg(reinterpret_cast<const float4 *>(row) + g);
+    float4 v;
+    v.x = e < B ? __ldg(row + e) : nan;
+    v.y = e + 1 < B ? __ldg(row + e + 1) : nan;
+    v.z = e + 2 < B ? __ldg(row + e + 2) : nan;
+    v.w = e + 3 < B ? __ldg(row + e + 3) : nan;
+    return v;
+}
+
+// The top k of a list of n > k exact-score bits in global memory whose ids are ascending, by
+// fixed digits (bits 31..20, 19..8, 7..0) over the keys and packed scans over chunks of 4096
+// for the kept ids in order.  The path for candidate lists too long for shared memory.
+// sh.hist is zero on entry and on return.
+__device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int n, int k,
+                                   int32_t *out, Smem &sh) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0;
+    int rem = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+        const int fixed = pass == 1 ? 20 : 8;
+        const uint32_t mask = pass == 2 ? 0xFFu : 0xFFFu;
+        for (int q = tid; q < n; q += kThreads) {
+            const uint32_t kq = order_key(__uint_as_float(bits[q]));
+            if (pass == 0 || (kq >> fixed) == (prefix >> fixed))
+                atomicAdd(&sh.hist[(kq >> shift) & mask], 1);
+        }
+        __syncthreads();
+        find_cut(sh, (int)mask + 1, rem);
+        prefix |= (uint32_t)sh.cut_bin << shift;
+        rem -= sh.cut_above;
+        clear_hist(sh, (int)mask + 1);
+    }
+    const uint32_t T = prefix;
+    const int take_eq = rem;
+    int G = 0, E = 0;   // keys above T / equal to T in the chunks before
+#pragma unroll 1
+    for (int c0 = 0; c0 < n; c0 += kMaxCand) {
+        const int q0 = c0 + 4 * tid;
+        uint32_t kk[4];
+        int ngt = 0, neq = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool ok = q0 + u < n;
+            kk[u] = ok ? order_key(__uint_as_float(bits[q0 + u])) : 0u;
+            ngt += (ok && kk[u] > T) ? 1 : 0;
+            neq += (ok && kk[u] == T) ? 1 : 0;
+        }
+        int tot;
+        const int ex = block_scan_excl(ngt | (neq << 16), sh, &tot);
+        int gt = G + (ex & 0xFFFF), eq = E + (ex >> 16);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (q0 + u < n) {
+                if (kk[u] > T) {
+                    const int slot = gt + (eq < take_eq ? eq : take_eq);
+                    if (slot < k) out[slot] = ids[q0 + u];
+                    ++gt;
+                } else if (kk[u] == T) {
+                    if (eq < take_eq && gt + eq < k) out[gt + eq] = ids[q0 + u];
+                    ++eq;
+                }
+            }
+        }
+        G += tot & 0xFFFF;
+        E += tot >> 16;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// The bounded selection (sfa_topk_blocks_refine), one 4-CTA cluster per row.  With lower and
+// upper bounds lo_b <= s_b <= up_b of the exact (hi + lo) score s_b, each CTA takes a quarter
+// of the row's blocks:
+//   1. the maxima of groups of four lower bounds, their range (cluster-wide extrema) and a
+//      histogram of them in the leader CTA's shared memory; the floor of the bin of the k-th
+//      largest group maximum is L, a lower bound of the k-th largest lower bound (each group
+//      maximum bounds a distinct block from below);
+//   2. the candidates up_b >= L of the quarter, in ascending order; every block of the exact
+//      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k);
+//   3. their exact scores from the hi + lo pooled keys (fp32 on the CUDA cores), written as
+//      keys with the block ids into the leader's candidate list at the quarter's offset;
+//   4. the leader selects the top k of the list.
+// Lists longer than 4096 go through global memory (select_global_list).
+constexpr int kCl = 4;                                       // CTAs per row
+constexpr int kClRounds = (kChunk / kCl) / (4 * kThreads);   // 3 rounds of groups of four
+
+struct RefineParams {
+    const float *lower, *upper;
+    int64_t stride;
+    const __nv_bfloat16 *q_idx;   // [n_q][H][D]
+    const float *w;               // [n_q][H]
+    const int32_t *q_seq, *q_pos;
+    const __nv_bfloat16 *kbar;    // [n_seq][blk_cap][2 D]
+    int64_t kbar_seq_stride;
+    int64_t n_blk_max;
+    uint32_t *cand_bits;          // [n_q][n_blk_max] exact-score bits (long lists)
+    int32_t *cand_id, *cand_n;    // [n_q][n_blk_max], [n_q] (-1: within the budget)
+    int32_t *blk_idx, *n_sel;
+    int32_t *status;
+    int n_seq, cr, H, D, top_k;
+};
+
+// The query's index heads as mma.sync B fragments (m16n8k16, bf16): entry ((nt * kPq + pq) * 2
+// + h) * 32 + lane holds the pair of registers for heads 8 nt .. 8 nt + 7 and the k-step (pair
+// pq, half h) of the column order the A loads use (see rescore_tile).
+constexpr int kPq = 4;   // q dims / 32 (D <= 128)
+struct BoundedSmem {
+    Smem sh;                        // the leader's candidate list serves the cluster
+    float up[kChunk / kCl];         // this quarter's upper bounds (cp.async)
+    uint2 qf[2 * kPq * 2 * 32];
+    float w[16];
+    int woff[kClRounds * kWarps];   // per (round, warp): this CTA's candidates before it
+    uint32_t ext_max[kCl], ext_min[kCl];   // leader slots, per rank
+    int cnt[kCl];
+    uint32_t lo;
+};
+
+// Exact scores of 16 candidates on the tensor cores: S[16 x heads] = [hi | lo] rows x [q ; q],
+// K = 2D, fp32 accumulation, then sum_j w_j ReLU(S_j) per row.  Lane (g, t) loads 16 bytes of
+// rows g and g + 8 at element 32 pp + 8 t of each 32-element piece pp of the 2D-wide row: the
+// first four elements are its A columns (2t, 2t+1, 2t+8, 2t+9) of k-step (pp, 0), the last
+// four those of (pp, 1).  The B table pairs the same columns with q (dims mod D), so each
+// k-step sums over 16 distinct columns and the pieces cover all 2D.  Returns the score of row
+// g (lanes with t == 0) and of row g + 8 through s0, s1.
+template <int D>
+__device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv_bfloat16 *r1,
+                                             const BoundedSmem &bs, int H, float &s0, float &s1) {
+    constexpr int kPieces = 2 * D / 32;   // 8 or 4
+    constexpr int kG = kPieces < 4 ? kPieces : 4;   // pieces in flight
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    const int nt_n = (H + 7) / 8;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int p0 = 0; p0 < kPieces; p0 += kG) {
+        uint4 a0[kG], a1[kG];
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+            a0[u] = __ldg(reinterpret_cast<const uint4 *>(r0 + 32 * (p0 + u) + 8 * t));
+            a1[u] = __ldg(reinterpret_cast<const uint4 *>(r1 + 32 * (p0 + u) + 8 * t));
+        }
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+            const int pq = (p0 + u) % (D / 32);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t a[4] = {h ? a0[u].z : a0[u].x, h ? a1[u].z : a1[u].x,
+                                       h ? a0[u].w : a0[u].y, h ? a1[u].w : a1[u].y};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    if (nt < nt_n) {
+                        const uint2 b = bs.qf[((nt * kPq + pq) * 2 + h) * 32 + lane];
+                        mma_bf16_16816(acc[nt], a, b.x, b.y);
+                    }
+                }
+            }
+        }
+    }
+    float p0s = 0.f, p1s = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int h0 = 8 * nt + 2 * t;
+        const float w0 = h0 < H ? bs.w[h0] : 0.f, w1 = h0 + 1 < H ? bs.w[h0 + 1] : 0.f;
+        p0s = fmaf(w0, fmaxf(acc[nt][0], 0.f), p0s);
+        p0s = fmaf(w1, fmaxf(acc[nt][1], 0.f), p0s);
+        p1s = fmaf(w0, fmaxf(acc[nt][2], 0.f), p1s);
+        p1s = fmaf(w1, fmaxf(acc[nt][3], 0.f), p1s);
+    }
+    p0s += __shfl_xor_sync(0xFFFFFFFFu, p0s, 1);
+    p0s += __shfl_xor_sync(0xFFFFFFFFu, p0s, 2);
+    p1s += __shfl_xor_sync(0xFFFFFFFFu, p1s, 1);
+    p1s += __shfl_xor_sync(0xFFFFFFFFu, p1s, 2);
+    s0 = p0s;
+    s1 = p1s;
+}
+
+template <int D>
+__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
+    bounded_select_kernel(const RefineParams p, int n_q) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    BoundedSmem &bs = *reinterpret_cast<BoundedSmem *>(smem_raw);
+    Smem &sh = bs.sh;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    BoundedSmem &lead = *cluster.map_shared_rank(&bs, 0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = p.top_k, H = p.H;
+    const int n_cl = gridDim.x / kCl;
+    clear_hist(sh, kBins);   // kept zero between rows from here on
+    cluster.sync();          // every CTA of the cluster is running before any remote access
+    for (int i = blockIdx.x / kCl; i < n_q; i += n_cl) {
+        const int seq = p.q_seq[i];
+        int B = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
+                               (rank == 0 && tid == 0) ? p.status : nullptr);
+        if (seq < 0 || seq >= p.n_seq) {
+            if (rank == 0 && tid == 0) set_status(p.status, SFA_DEV_BAD_QUERY);
+            B = 0;
+        }
+        if (B <= k) {   // every block fits the budget (the same for the whole cluster)
+            if (rank == 0) {
+                int32_t *out = p.blk_idx + (int64_t)i * k;
+                for (int j = tid; j < k; j += kThreads) out[j] = j < B ? j : -1;
+                if (tid == 0) {
+                    p.n_sel[i] = B;
+                    p.cand_n[i] = -1;
+                }
+            }
+            continue;
+        }
+        // this CTA's groups of four: [g0, g1)
+        const int ng = (B + 3) / 4;
+        const int per = (ng + kCl - 1) / kCl;
+        const int g0 = rank * per < ng ? rank * per : ng;
+        const int g1 = g0 + per < ng ? g0 + per : ng;
+        const float *lp = p.lower + (int64_t)i * p.stride;
+        const float *up = p.upper + (int64_t)i * p.stride;
+        {   // this quarter's upper bounds into shared memory, in flight while L is found
+            const bool vec = (reinterpret_cast<uintptr_t>(up) & 15u) == 0;
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m) {
+                const int lg = tid + kThreads * m, g = g0 + lg;
+                if (g < g1) {
+                    if (vec && 4 * g + 3 < B) {
+                        cp_async16(smem_u32(&bs.up[4 * lg]), up + 4 * g, 16);
+                    } else {
+                        const float4 v = load_group(up, g, B, false);
+                        bs.up[4 * lg] = v.x;
+                        bs.up[4 * lg + 1] = v.y;
+                        bs.up[4 * lg + 2] = v.z;
+                        bs.up[4 * lg + 3] = v.w;
+                    }
+                }
+            }
+            cp_async_commit();
+        }
+        if (tid < 2 * kPq * 2 * 32) {   // the B fragment table of this query
+            const int ln = tid & 31, h = (tid >> 5) & 1, pq = (tid >> 6) % kPq, nt = tid / (64 * kPq);
+            const int n = 8 * nt + (ln >> 2), d0 = 32 * pq + 8 * (ln & 3) + 4 * h;
+            uint2 b = make_uint2(0u, 0u);
+            if (n < H && d0 < D) {
+                const uint32_t *qr = reinterpret_cast<const uint32_t *>(p.q_idx + ((int64_t)i * H + n) * D + d0);
+                b = make_uint2(qr[0], qr[1]);
+            }
+            bs.qf[tid] = b;
+        }
+        if (tid < H) bs.w[tid] = p.w[(int64_t)i * H + tid];
+        // ---- 1. group maxima of the lower bounds -> L
+        uint32_t gm[kClRounds];
+        uint32_t mx = 0, mn = 0xFFFFFFFFu;
+        {
+            const bool vec = (reinterpret_cast<uintptr_t>(lp) & 15u) == 0;
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m) {
+                const int g = g0 + tid + kThreads * m;
+                gm[m] = 0;
+                if (g < g1) {
+                    const float4 v = load_group(lp, g, B, vec);
+                    gm[m] = order_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                    mx = gm[m] > mx ? gm[m] : mx;
+                    mn = gm[m] < mn ? gm[m] : mn;
+                }
+            }
+        }
+        {
+            uint32_t bmax, bmin, unused;
+            block_extrema(mx, mn, 0xFFFFFFFFu, sh, bmax, bmin, unused);
+            if (tid == 0) {
+                lead.ext_max[rank] = bmax;
+                lead.ext_min[rank] = bmin;
+            }
+        }
+        cluster.sync();   // (a) the extrema of every quarter are in the leader
+        uint32_t gmax = 0, gmin = 0xFFFFFFFFu;
+#pragma unroll
+        for (int r = 0; r < kCl; ++r) {
+            const uint32_t a = lead.ext_max[r], b = lead.ext_min[r];
+            gmax = a > gmax ? a : gmax;
+            gmin = b < gmin ? b : gmin;
+        }
+        const bool have_k = k <= ng;   // k group maxima exist
+        const int sft = bin_shift(gmax - gmin);
+        if (have_k) {
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m)
+                if (g0 + tid + kThreads * m < g1) atomicAdd(&sh.hist[(gm[m] - gmin) >> sft], 1);
+        }
+        cluster.sync();   // (b) every quarter's histogram is complete
+        if (rank == 0) {
+            uint32_t lo = 0;
+            if (have_k) {   // the leader adds the other quarters' histograms to its own
+                static_assert(kBins == 4 * kThreads, "one int4 of bins per thread");
+                int4 a = reinterpret_cast<const int4 *>(sh.hist)[tid];
+#pragma unroll
+                for (int r = 1; r < kCl; ++r) {
+                    const int4 v = reinterpret_cast<const int4 *>(cluster.map_shared_rank(sh.hist, r))[tid];
+                    a.x += v.x;
+                    a.y += v.y;
+                    a.z += v.z;
+                    a.w += v.w;
+                }
+                reinterpret_cast<int4 *>(sh.hist)[tid] = a;
+                __syncthreads();
+                find_cut(sh, kBins, k);
+                lo = gmin + ((uint32_t)sh.cut_bin << sft);
+                clear_hist(sh, kBins);
+            }
+            if (tid == 0) bs.lo = lo;
+        }
+        cluster.sync();   // (c) L is known; the leader has read every histogram
+        if (rank != 0 && have_k) clear_hist(sh, kBins);
+        const uint32_t lo = lead.lo;
+        // ---- 2. candidates up_b >= L (as keys: >= lo); bit 4m + r for element 4g + r
+        uint32_t cm = 0;
+        cp_async_wait<0>();
+        __syncthreads();   // the quarter's upper bounds have landed
+        {
+            const bool fcmp = lo >= kNegInfKey;   // lo is a float's key: compare floats
+            const float L = __uint_as_float(key_bits(lo));
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m) {
+                const int lg = tid + kThreads * m, g = g0 + lg;
+                if (g < g1) {
+                    const float4 v = *reinterpret_cast<const float4 *>(&bs.up[4 * lg]);
+                    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const bool c = 4 * g + r < B && (fcmp ? f[r] >= L : order_key(f[r]) >= lo);
+                        cm |= (uint32_t)c << (4 * m + r);
+                    }
+                }
+            }
+        }
+        // ascending order within the quarter = (round, warp, lane, r)
+        int incl[kClRounds];
+#pragma unroll
+        for (int m = 0; m < kClRounds; ++m) {
+            const int c = __popc((cm >> (4 * m)) & 0xFu);
+            int x = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            incl[m] = x - c;
+            if (lane == 31) bs.woff[m * kWarps + warp] = x;
+        }
+        __syncthreads();
+        if (warp == 0) {   // scan of the kClRounds * 32 totals: kClRounds per lane
+            int loc[kClRounds], sum = 0;
+#pragma unroll
+            for (int e = 0; e < kClRounds; ++e) {
+                loc[e] = bs.woff[lane * kClRounds + e];
+                sum += loc[e];
+            }
+            int x = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            int run = x - sum;
+#pragma unroll
+            for (int e = 0; e < kClRounds; ++e) {
+                bs.woff[lane * kClRounds + e] = run;
+                run += loc[e];
+            }
+            if (lane == 31) lead.cnt[rank] = x;
+        }
+        cluster.sync();   // (d) every quarter's count is in the leader
+        int off = 0, total = 0;
+#pragma unroll
+        for (int r = 0; r < kCl; ++r) {
+            const int c = lead.cnt[r];
+            off += r < rank ? c : 0;
+            total += c;
+        }
+        const int mine = lead.cnt[rank];
+        const bool in_smem = total <= kMaxCand;   // the same in every CTA
+        int32_t *gid = p.cand_id + (int64_t)i * p.n_blk_max;
+        uint32_t *gbits = p.cand_bits + (int64_t)i * p.n_blk_max;
+        // this quarter's list: local shared memory, or the row's global list at its offset
+#pragma unroll
+        for (int m = 0; m < kClRounds; ++m) {
+            int pos = bs.woff[m * kWarps + warp] + incl[m];
+            const int g = g0 + tid + kThreads * m;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if ((cm >> (4 * m + r)) & 1u) {
+                    if (in_smem)
+                        sh.cand_idx[pos] = 4 * g + r;
+                    else
+                        gid[off + pos] = 4 * g + r;
+                    ++pos;
+                }
+        }
+        __syncthreads();
+        // ---- 3. exact scores of this quarter's candidates: a warp takes 16 at a time
+        {
+            const int32_t *lid = in_smem ? sh.cand_idx : gid + off;
+            const __nv_bfloat16 *kseq = p.kbar + (int64_t)seq * p.kbar_seq_stride;
+            const int g = lane >> 2;
+            for (int c0 = warp * 16; c0 < mine; c0 += kWarps * 16) {
+                const int ra = c0 + g, rb = c0 + g + 8;
+                const int ba = lid[ra < mine ? ra : c0], bb = lid[rb < mine ? rb : c0];
+                float sa, sb;
+                rescore_tile<D>(kseq + (int64_t)ba * 2 * D, kseq + (int64_t)bb * 2 * D, bs, H, sa, sb);
+                if ((lane & 3) == 0) {
+                    if (ra < mine) {
+                        if (in_smem) {
+                            lead.sh.cand_key[off + ra] = order_key(sa);
+                            lead.sh.cand_idx[off + ra] = ba;
+                        } else {
+                            gbits[off + ra] = __float_as_uint(sa);
+                        }
+                    }
+                    if (rb < mine) {
+                        if (in_smem) {
+                            lead.sh.cand_key[off + rb] = order_key(sb);
+                            lead.sh.cand_idx[off + rb] = bb;
+                        } else {
+                            gbits[off + rb] = __float_as_uint(sb);
+                        }
+                    }
+                }
+            }
+        }
+        if (!in_smem) __threadfence();   // the global list is complete before the leader reads it
+        cluster.sync();   // (e) the list is complete
+        // ---- 4. the leader selects the top k of the list
+        if (rank == 0) {
+            int32_t *out = p.blk_idx + (int64_t)i * k;
+            if (in_smem) {
+                uint32_t kx = 0, kn = 0xFFFFFFFFu;
+                for (int q = tid; q < total; q += kThreads) {
+                    const uint32_t kq = sh.cand_key[q];
+                    kx = kq > kx ? kq : kx;
+                    kn = kq < kn ? kq : kn;
+                }
+                uint32_t kmax, kmin, unused;
+                block_extrema(kx, kn, 0xFFFFFFFFu, sh, kmax, kmin, unused);
+                const Cut cut = cut_candidates(sh, total, k, kmin, kmax);
+                for_each_kept(cut, sh, [&](int slot, uint32_t, int idx) {
+                    if (slot < k) out[slot] = idx;
+                });
+            } else {
+                select_global_list(gbits, gid, total, k, out, sh);
+            }
+            if (tid == 0) {
+                p.n_sel[i] = k;
+                p.cand_n[i] = total;
+            }
+            __syncthreads();
+        }
+    }
+    cluster.sync();   // no CTA leaves while another may still address its shared memory
+}
+
+template <int D>
+int launch_bounded_d(const RefineParams &p, int n_q, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        if (!allow_max_dynamic_smem(bounded_select_kernel<D>)) return SFA_ERR_CUDA;
+        attr = true;
+    }
+    int clusters = device_sm_count() / kCl;
+    if (clusters < 1) return SFA_ERR_CUDA;
+    if (n_q < clusters) clusters = n_q;
+    bounded_select_kernel<D><<<clusters * kCl, kThreads, sizeof(BoundedSmem), st>>>(p, n_q);
+    SFA_CHECK_LAUNCH();
+    return SFA_OK;
+}
+
+int launch_bounded(const RefineParams &p, int n_q, cudaStream_t st) {
+    return p.D == 64 ? launch_bounded_d<64>(p, n_q, st) : launch_bounded_d<128>(p, n_q, st);
 }
 
 // The levels for rows of up to n_blk_max scores: lengths per row at each level (n[0] =
@@ -421,7 +1050,7 @@ int launch_stage(const TopkParams &p, int n_q, int n_chunks, cudaStream_t st) {
         if (!allow_max_dynamic_smem(topk_stage_kernel<R>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    topk_stage_kernel<R><<<grid, kThreads, sizeof(Smem), st>>>(p, n_q, n_chunks);
+    topk_stage_kernel<R><<<grid, kThreads, smem_bytes<R>(), st>>>(p, n_q, n_chunks);
     SFA_CHECK_LAUNCH();
     return SFA_OK;
 }
@@ -506,4 +1135,63 @@ extern "C" int sfa_topk_blocks(const float *scores, int64_t score_stride, const 
         if (rc != SFA_OK) return rc;
     }
     return SFA_OK;
+}
+
+extern "C" size_t sfa_topk_refine_workspace_bytes(int n_q, int64_t n_blk_max) {
+    if (n_q <= 0 || n_blk_max <= 0) return 0;
+    // candidate score bits and ids [n_q][n_blk_max], counts [n_q]
+    return (size_t)n_q * (size_t)n_blk_max * 8 + (size_t)n_q * 4 + 256;
+}
+
+extern "C" int sfa_topk_blocks_refine(const float *lower, const float *upper,
+                                      int64_t score_stride, const void *q_idx, const float *w,
+                                      const int32_t *q_seq, const int32_t *q_pos, int n_q,
+                                      int h_idx, int d_idx, const void *Kbar,
+                                      int64_t kbar_seq_stride, int n_seq, int compress_ratio,
+                                      int top_k, int64_t n_blk_max, int32_t *blk_idx,
+                                      int32_t *n_sel, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, sfa_stream_t stream) {
+    using namespace sfa;
+    if (!q_pos || !q_seq || !blk_idx || !n_sel || !q_idx || !w || !Kbar || n_q < 0 ||
+        compress_ratio < 1 || n_blk_max < 0 || n_seq < 1)
+        return SFA_ERR_INVALID_ARG;
+    if (top_k < 1 || top_k > 2048) return SFA_ERR_UNSUPPORTED;
+    if (d_idx != 64 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
+    if (h_idx < 1 || h_idx > 16) return SFA_ERR_UNSUPPORTED;
+    if (n_blk_max > kChunk) return SFA_ERR_UNSUPPORTED;   // one piece per row
+    if (n_blk_max > 0 && (!lower || !upper || score_stride < n_blk_max))
+        return SFA_ERR_INVALID_ARG;
+    if (kbar_seq_stride < n_blk_max * 2 * d_idx) return SFA_ERR_INVALID_ARG;
+    // 16-byte loads of pooled-key rows, 4-byte loads of index-query pairs
+    if (!aligned16(Kbar) || kbar_seq_stride % 8 != 0 || (reinterpret_cast<uintptr_t>(q_idx) & 3u))
+        return SFA_ERR_INVALID_ARG;
+    if (n_q == 0) return SFA_OK;
+    const int64_t nb = n_blk_max > 0 ? n_blk_max : 1;
+    const size_t need = sfa_topk_refine_workspace_bytes(n_q, nb);
+    if (!workspace || workspace_bytes < need) return SFA_ERR_WORKSPACE;
+    const cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    RefineParams r{};
+    r.lower = lower;
+    r.upper = upper;
+    r.stride = score_stride;
+    r.q_idx = reinterpret_cast<const __nv_bfloat16 *>(q_idx);
+    r.w = w;
+    r.q_seq = q_seq;
+    r.q_pos = q_pos;
+    r.kbar = reinterpret_cast<const __nv_bfloat16 *>(Kbar);
+    r.kbar_seq_stride = kbar_seq_stride;
+    r.n_blk_max = nb;
+    r.cand_bits = reinterpret_cast<uint32_t *>(ws);
+    r.cand_id = reinterpret_cast<int32_t *>(ws + (size_t)n_q * nb * 4);
+    r.cand_n = reinterpret_cast<int32_t *>(ws + (size_t)n_q * nb * 8);
+    r.status = dev_status;
+    r.blk_idx = blk_idx;
+    r.n_sel = n_sel;
+    r.n_seq = n_seq;
+    r.cr = compress_ratio;
+    r.H = h_idx;
+    r.D = d_idx;
+    r.top_k = top_k;
+    return launch_bounded(r, n_q, st);
 }

@@ -5,6 +5,10 @@ kept block lists, workspaces, outputs) and runs the stages as the C entry points
 
   sfa_pool_index_keys -> sfa_index_scores -> sfa_topk_blocks -> sfa_gather_attend
 
+(decode-like steps -- few queries per sequence, rows of at most 36864 blocks -- take
+sfa_index_scores_bounded -> sfa_topk_blocks_refine for the middle two: the same kept sets from
+half the pooled-key bytes plus the rescoring of the few blocks the bounds cannot rule out)
+
 or, when every query is below the budget (B_i <= indexer_top_k for all i), the dense case
 ``sfa_dense_attend``: every block then fits the budget, so the method is exactly dense
 attention (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
@@ -19,7 +23,7 @@ from . import _binding as B
 class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
-                 n_blk_max: int, q_group: int = 1, device="cuda"):
+                 n_blk_max: int, q_group: int = 1, bounded=None, device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -29,7 +33,21 @@ class SfaStep:
         self.Kbar = torch.zeros(B.kbar_shape(n_seq, self.blk_cap, d_idx), dtype=torch.bfloat16,
                                 device=dev)
         self.dense = n_blk_max <= indexer_top_k
+        # The bounded selection (hi-only scores + exact rescoring of the blocks the bounds
+        # cannot rule out) halves the pooled-key bytes of decode-like steps, where each query
+        # streams its sequence's pooled keys; prefill tiles share those reads and take the
+        # exact scores directly.  Rows must fit one selection piece (36864 blocks).
+        if bounded is None:
+            bounded = q_group <= 4 and n_blk_max <= B.SFA_REFINE_MAX_BLOCKS
+        self.bounded = bool(bounded) and not self.dense
+        if self.bounded and n_blk_max > B.SFA_REFINE_MAX_BLOCKS:
+            raise ValueError(f"bounded selection takes rows of at most "
+                             f"{B.SFA_REFINE_MAX_BLOCKS} blocks, got n_blk_max={n_blk_max}")
         self.scores = torch.empty((n_q, max(n_blk_max, 1)), dtype=torch.float32, device=dev)
+        # bounded: scores holds the lower bounds and upper the upper bounds
+        self.upper = (torch.empty_like(self.scores) if self.bounded else None)
+        nr = B.sfa_topk_refine_workspace_bytes(n_q, max(n_blk_max, 1)) if self.bounded else 0
+        self.refine_ws = torch.empty(max(nr, 16), dtype=torch.uint8, device=dev)
         self.blk_idx = torch.empty((n_q, indexer_top_k), dtype=torch.int32, device=dev)
         self.n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
         nt = B.sfa_topk_workspace_bytes(n_q, max(n_blk_max, 1), indexer_top_k)
@@ -47,13 +65,31 @@ class SfaStep:
         if blk_end > blk_begin:
             B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, stream=stream)
 
+    def score(self, q_idx, w, q_seq, q_pos, stream=None):
+        if self.bounded:
+            B.sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, self.Kbar, self.cr,
+                                       self.n_blk_max, self.scores, self.upper,
+                                       q_group=self.q_group, dev_status=self.status,
+                                       stream=stream)
+        else:
+            B.sfa_index_scores(q_idx, w, q_seq, q_pos, self.Kbar, self.cr, self.n_blk_max,
+                               self.scores, q_group=self.q_group, dev_status=self.status,
+                               stream=stream)
+
+    def topk(self, q_idx, w, q_seq, q_pos, stream=None):
+        if self.bounded:
+            B.sfa_topk_blocks_refine(self.scores, self.upper, q_idx, w, q_seq, q_pos, self.Kbar,
+                                     self.cr, self.top_k, self.n_blk_max, self.blk_idx,
+                                     self.n_sel, workspace=self.refine_ws,
+                                     dev_status=self.status, stream=stream)
+        else:
+            B.sfa_topk_blocks(self.scores, q_pos, self.cr, self.top_k, self.n_blk_max,
+                              self.blk_idx, self.n_sel, workspace=self.topk_ws,
+                              dev_status=self.status, stream=stream)
+
     def select(self, q_idx, w, q_seq, q_pos, stream=None):
-        B.sfa_index_scores(q_idx, w, q_seq, q_pos, self.Kbar, self.cr, self.n_blk_max,
-                           self.scores, q_group=self.q_group, dev_status=self.status,
-                           stream=stream)
-        B.sfa_topk_blocks(self.scores, q_pos, self.cr, self.top_k, self.n_blk_max, self.blk_idx,
-                          self.n_sel, workspace=self.topk_ws, dev_status=self.status,
-                          stream=stream)
+        self.score(q_idx, w, q_seq, q_pos, stream=stream)
+        self.topk(q_idx, w, q_seq, q_pos, stream=stream)
 
     def attend(self, Q, K, V, q_seq, q_pos, scale: float, stream=None):
         if self.dense:

@@ -1,0 +1,165 @@
+"""The bounded selection (sfa_index_scores_bounded -> sfa_topk_blocks_refine): the bounds hold
+against the hi + lo scores, and the refined kept sets follow the oracle's agreement rule
+(the same bar as sfa_index_scores -> sfa_topk_blocks)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import check_selection, np32
+from test_gpu_pipeline import _check_sampled, _run
+
+pytestmark = pytest.mark.gpu
+
+sfa = pytest.importorskip("indexer_selected_sparse_block_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _case(dev, seed, n_seq, n_tok, d_idx, h_idx, cr, q_pos, constant_keys=False):
+    g = torch.Generator().manual_seed(seed)
+    if constant_keys:   # every pooled key equal: every score ties
+        X = torch.ones((n_seq, n_tok, d_idx)).to(torch.bfloat16).to(dev)
+    else:
+        X = torch.randn((n_seq, n_tok, d_idx), generator=g).to(torch.bfloat16).to(dev)
+    n_q = len(q_pos)
+    qi = torch.randn((n_q, h_idx, d_idx), generator=g).to(torch.bfloat16).to(dev)
+    w = torch.rand((n_q, h_idx), generator=g).to(dev)
+    q_seq = torch.arange(n_q, dtype=torch.int32) % n_seq
+    q_pos = torch.tensor(q_pos, dtype=torch.int32)
+    blk_cap = n_tok // cr
+    Kbar = torch.zeros(sfa.kbar_shape(n_seq, blk_cap, d_idx), dtype=torch.bfloat16, device=dev)
+    sfa.sfa_pool_index_keys(X, cr, 0, blk_cap, Kbar)
+    return X, qi, w, q_seq.to(dev), q_pos.to(dev), Kbar
+
+
+@pytest.mark.parametrize("d_idx,h_idx", [(128, 8), (64, 4), (128, 16)])
+def test_bounds_hold(dev, d_idx, h_idx):
+    cr, n_seq, n_tok = 4, 3, 6000
+    X, qi, w, q_seq, q_pos, Kbar = _case(dev, d_idx + h_idx, n_seq, n_tok, d_idx, h_idx, cr,
+                                         [5999, 4003, 1299])
+    n_blk_max = 1500
+    exact = torch.full((3, n_blk_max), float("nan"), device=dev)
+    lower = torch.full_like(exact, float("nan"))
+    upper = torch.full_like(exact, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, exact, dev_status=status)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    e, lo, up = np32(exact), np32(lower), np32(upper)
+    for i, p in enumerate([5999, 4003, 1299]):
+        B = (p + 1) // cr
+        assert np.all(lo[i, :B] <= e[i, :B]) and np.all(e[i, :B] <= up[i, :B]), i
+        assert np.all(np.isnan(lo[i, B:])) and np.all(np.isnan(up[i, B:]))
+        # tight enough to be useful: a few per cent of the typical score
+        half = 0.5 * (up[i, :B] - lo[i, :B])
+        assert np.median(half) < 0.1 * np.median(np.abs(e[i, :B]) + 1e-30)
+
+
+@pytest.mark.parametrize("top_k", [1, 64, 512, 2048])
+def test_refine_follows_agreement_rule(dev, top_k):
+    cr, d_idx, h_idx = 4, 128, 8
+    pos = [11999, 9000, 2047, 700, 3, 8191]
+    X, qi, w, q_seq, q_pos, Kbar = _case(dev, top_k, 2, 12000, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), 3000
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.full((n_q, top_k), -7, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kbar, cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Xh, qh, wh = np32(X), np32(qi), np32(w)
+    got, gn = np32(blk), np32(n_sel)
+    n_exact = 0
+    for i, p in enumerate(pos):
+        s = i % 2
+        B = (p + 1) // cr
+        sc = oracle.index_scores(qh[i], wh[i], oracle.pool(Xh[s], B, cr))
+        ok, exact = check_selection(got[i], int(gn[i]), sc, top_k)
+        assert ok, (i, p)
+        n_exact += exact
+        assert np.all(np.diff(got[i, :gn[i]]) > 0)        # ascending
+        assert np.all(got[i, gn[i]:] == -1)                # padded
+    assert n_exact >= len(pos) - 1
+
+
+@pytest.mark.parametrize("n_tok", [4000, 24000])
+def test_refine_all_tied(dev, n_tok):
+    """Every pooled key equal, so every score ties: every block is a candidate and the
+    lowest block indices win.  At 6000 blocks the candidate list is longer than the 4096
+    resolved in shared memory and takes the global-memory path."""
+    cr, d_idx, h_idx, top_k = 4, 64, 4, 100
+    pos = [n_tok - 1, n_tok // 2 + 1]
+    X, qi, w, q_seq, q_pos, Kbar = _case(dev, 3, 2, n_tok, d_idx, h_idx, cr, pos,
+                                         constant_keys=True)
+    n_q, n_blk_max = 2, n_tok // cr
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kbar, cr, top_k, n_blk_max,
+                               blk, n_sel)
+    torch.cuda.synchronize()
+    got = np32(blk)
+    assert np.array_equal(np32(n_sel), [top_k, top_k])
+    for i in range(n_q):
+        assert np.array_equal(got[i], np.arange(top_k))
+
+
+def test_refine_below_budget_and_bad_query(dev):
+    cr, d_idx, h_idx, top_k = 4, 64, 4, 50
+    pos = [150, 2, 3999]
+    X, qi, w, q_seq, q_pos, Kbar = _case(dev, 9, 1, 4000, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = 3, 1000
+    q_pos_bad = q_pos.clone()
+    q_pos_bad[2] = -1                                     # a query outside the cache
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos_bad, Kbar, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos_bad, Kbar, cr, top_k,
+                               n_blk_max, blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) & sfa.SFA_DEV_BAD_QUERY
+    got, gn = np32(blk), np32(n_sel)
+    assert gn[0] == 37 and np.array_equal(got[0, :37], np.arange(37)) and np.all(got[0, 37:] == -1)
+    assert gn[1] == 0 and np.all(got[1] == -1)
+    assert gn[2] == 0 and np.all(got[2] == -1)
+
+
+@pytest.mark.parametrize("name,queries", [("decode_32x131072", [0, 7, 31]),
+                                          ("decode_1x4096", [0])])
+def test_bounded_step_full_size_sampled(dev, name, queries):
+    """The whole step with the bounded selection (SfaStep(bounded=True)) at full size:
+    sampled queries follow the oracle's agreement rule and attend within tolerance."""
+    w = sfa.WORKLOADS[name]
+    case, step = _run(w, dev, bounded=True)
+    assert step.bounded
+    _check_sampled(w, case, step, queries)
+
+
+def test_bounded_step_rejects_long_rows(dev):
+    w = sfa.WORKLOADS["decode_4x1048576"]
+    with pytest.raises(ValueError):
+        sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
+                    dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
+                    compress_ratio=w.compress_ratio, indexer_top_k=w.indexer_top_k,
+                    n_blk_max=w.n_tok // w.compress_ratio, q_group=1, bounded=True, device=dev)

@@ -27,18 +27,18 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _step_for(w, dev, top_k=None):
+def _step_for(w, dev, top_k=None, bounded=None):
     n_blk_max = w.n_tok // w.compress_ratio
     return sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
                        dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                        compress_ratio=w.compress_ratio,
                        indexer_top_k=top_k or w.indexer_top_k, n_blk_max=n_blk_max,
-                       q_group=w.n_q_per_seq, device=dev)
+                       q_group=w.n_q_per_seq, bounded=bounded, device=dev)
 
 
-def _run(w, dev, top_k=None):
+def _run(w, dev, top_k=None, bounded=None):
     case = sfa.make_case(w, device=dev)
-    step = _step_for(w, dev, top_k)
+    step = _step_for(w, dev, top_k, bounded)
     step.pool(case["X"], 0, step.n_blk_max)
     step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
              case["q_seq"], case["q_pos"], w.scale)
@@ -93,9 +93,10 @@ def _check_sampled(w, case, step, queries):
     return n_exact
 
 
-def test_decode_1x4096_all(dev):
-    w = sfa.WORKLOADS["decode_1x4096"]
-    case, step = _run(w, dev)
+@pytest.mark.parametrize("bounded", [None, False])
+def test_decode_1x4096_all(dev, bounded):
+    w = sfa.WORKLOADS["decode_1x4096"].with_(n_seq=6)
+    case, step = _run(w, dev, bounded=bounded)
     assert _check_sampled(w, case, step, range(w.n_q)) >= 0
 
 
@@ -152,9 +153,13 @@ def test_prefill_512x1000_below_budget_is_dense(dev):
     assert row_rel_err(np32(O), de["O"]).max() < TOL_BF16
 
 
-def test_decode_32x131072_sampled(dev):
+@pytest.mark.parametrize("bounded", [None, False])
+def test_decode_32x131072_sampled(dev, bounded):
+    """The step as configured by default (the bounded selection for this shape) and with the
+    exact scores and select forced."""
     w = sfa.WORKLOADS["decode_32x131072"]
-    case, step = _run(w, dev)
+    case, step = _run(w, dev, bounded=bounded)
+    assert step.bounded == (bounded is None)
     _check_sampled(w, case, step, [0, 7, 19, 31])
 
 
