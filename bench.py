@@ -80,7 +80,8 @@ def algorithmic(w, attended, bounded=False):
     cr = w.compress_ratio
     nb = [(w.depth + j + 1) // cr for j in range(w.n_q_per_seq)] * w.n_seq
     kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
-    per_blk = (2 if bounded else 4) * w.d_idx   # bounded selection: the hi halves only
+    # bounded selection: the hi halves and the 4-byte bound factor of each block only
+    per_blk = (2 * w.d_idx + 4) if bounded else 4 * w.d_idx
     if w.kind == "decode":
         kbar_bytes = sum(b * per_blk for b in nb)
     else:
@@ -189,7 +190,7 @@ class Workbench:
         if not st.dense:
             n += 1  # scores
             if st.bounded:
-                n += 2  # refine + the final selection
+                n += 1  # the cluster selection kernel
             else:
                 n += 1 + (B.sfa_topk_workspace_bytes(w.n_q, self.n_blk_max, w.indexer_top_k) > 0)
             n_kv = w.indexer_top_k * w.compress_ratio + w.compress_ratio - 1

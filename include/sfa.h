@@ -76,12 +76,17 @@ enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
  *            row b  = (hi[0..d_idx), lo[0..d_idx))
  *          so that hi + lo carries m to about 2^-17 relative while the tensor cores read it
  *          as plain bf16.
+ *   Kbar_r [n_seq][kr_seq_stride] fp32, or NULL: the error-bound factor of each pooled row
+ *          for sfa_index_scores_bounded, from the stored halves,
+ *            r_b = (|lo|_2 + 2^-14 |hi|_2) * (1 + 2^-16)   (fp32 norms)
  * Writes rows [blk_begin, blk_end) of every sequence; reads tokens [blk_begin*cr, blk_end*cr).
- * Limits: 1 <= cr <= 64, d_idx in {32, 64, 96, 128}, 0 <= blk_begin <= blk_end.
+ * Limits: 1 <= cr <= 64, d_idx in {32, 64, 96, 128} (Kbar_r: not 96), 0 <= blk_begin <=
+ * blk_end; kr_seq_stride >= blk_end when Kbar_r is given.
  */
 int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq, int d_idx,
                         int compress_ratio, int64_t blk_begin, int64_t blk_end, void *Kbar,
-                        int64_t kbar_seq_stride, sfa_stream_t stream);
+                        int64_t kbar_seq_stride, float *Kbar_r, int64_t kr_seq_stride,
+                        sfa_stream_t stream);
 
 /*
  * sfa_index_scores -- the indexer score of every complete block visible to each query: each
@@ -137,13 +142,15 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
  * sfa_index_scores + sfa_topk_blocks from half the pooled-key bytes (a library addition: the
  * pages score and select in one pass each).
  *
- * sfa_index_scores_bounded: arguments as sfa_index_scores; it reads only the hi halves of
- * the pooled keys and writes lower and upper bounds of the hi + lo score s_ib:
+ * sfa_index_scores_bounded: arguments as sfa_index_scores plus Kbar_r, kr_seq_stride (the
+ * bound factors written by sfa_pool_index_keys with the same Kbar); it reads only the hi
+ * halves of the pooled keys and writes lower and upper bounds of the hi + lo score s_ib:
  *   lower, upper [n_q][score_stride] fp32: lower = a - e <= s_ib <= a + e = upper, with
  *           a_ib = sum_j w_ij * max(0, qidx_ij . hi_b) and
- *           e_ib = 1.02 * 2^-9 * (sum_j |w_ij| |qidx_ij|_2) * |hi_b|_2 (the lo half is the bf16
- *           rounding remainder, |lo| <= 2^-9/(1 - 2^-9) |hi| elementwise; ReLU is 1-Lipschitz;
- *           Cauchy-Schwarz per head; the 2% covers the fp32 rounding of both scores).
+ *           e_ib = (1 + 2^-10) * (sum_j |w_ij| |qidx_ij|_2) * r_b.  The exact difference is at
+ *           most (sum_j |w_ij| |qidx_ij|_2) |lo_b|_2 (ReLU is 1-Lipschitz; Cauchy-Schwarz per
+ *           head); r_b's second term covers the fp32 rounding of both scores (< 2^-15 of
+ *           sum_j |w_ij| |qidx_ij|_2 |hi_b|_2).
  * Both arrays share score_stride; entries at b >= B_i are left untouched.
  *
  * sfa_topk_blocks_refine: per query, L = a lower bound of the k-th largest lower bound (the
@@ -165,8 +172,9 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
 int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
                              const int32_t *q_pos, int n_q, int q_group, int h_idx, int d_idx,
                              int compress_ratio, const void *Kbar, int64_t kbar_seq_stride,
-                             int n_seq, int64_t n_blk_max, float *lower, float *upper,
-                             int64_t score_stride, int32_t *dev_status, sfa_stream_t stream);
+                             const float *Kbar_r, int64_t kr_seq_stride, int n_seq,
+                             int64_t n_blk_max, float *lower, float *upper, int64_t score_stride,
+                             int32_t *dev_status, sfa_stream_t stream);
 size_t sfa_topk_refine_workspace_bytes(int n_q, int64_t n_blk_max);
 int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score_stride,
                            const void *q_idx, const float *w, const int32_t *q_seq,

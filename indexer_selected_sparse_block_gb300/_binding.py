@@ -27,11 +27,12 @@ _vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, cty
 
 # name -> (restype, argtypes); mirrors include/sfa.h
 SIGNATURES = {
-    "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp]),
+    "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp,
+                                   _i64, _vp]),
     "sfa_index_scores": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _i64,
                                 _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
-                                        _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
+                                        _i64, _vp, _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
     "sfa_topk_workspace_bytes": (_sz, [_int, _i64, _int]),
     "sfa_topk_refine_workspace_bytes": (_sz, [_int, _i64]),
     "sfa_topk_blocks_refine": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int, _vp,
@@ -111,11 +112,14 @@ def kbar_shape(n_seq: int, blk_cap: int, d_idx: int):
     return (n_seq, blk_cap, 2 * d_idx)
 
 
-def sfa_pool_index_keys(X, compress_ratio: int, blk_begin: int, blk_end: int, Kbar, stream=None):
-    """X [n_seq][n_tok_cap][d_idx] (bf16/f32) -> rows [blk_begin, blk_end) of Kbar."""
+def sfa_pool_index_keys(X, compress_ratio: int, blk_begin: int, blk_end: int, Kbar,
+                        Kbar_r=None, stream=None):
+    """X [n_seq][n_tok_cap][d_idx] (bf16/f32) -> rows [blk_begin, blk_end) of Kbar, and of the
+    bound factors Kbar_r [n_seq][blk_cap] fp32 when given."""
     n_seq, _, d_idx = X.shape
     rc = lib().sfa_pool_index_keys(_p(X), _dtype_code(X), X.stride(0), n_seq, d_idx,
                                    compress_ratio, blk_begin, blk_end, _p(Kbar), Kbar.stride(0),
+                                   _p(Kbar_r), Kbar_r.stride(0) if Kbar_r is not None else 0,
                                    _stream(stream))
     _check("sfa_pool_index_keys", rc)
 
@@ -131,17 +135,19 @@ def sfa_index_scores(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_ma
     _check("sfa_index_scores", rc)
 
 
-def sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_max: int,
-                             lower, upper, q_group: int = 1, dev_status=None, stream=None):
+def sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, Kbar, Kbar_r, compress_ratio: int,
+                             n_blk_max: int, lower, upper, q_group: int = 1, dev_status=None,
+                             stream=None):
     """lower[i][b] <= s_ib <= upper[i][b] for the hi + lo score s_ib, from the hi halves of the
-    pooled keys only."""
+    pooled keys and their bound factors Kbar_r only."""
     n_q, h_idx, d_idx = q_idx.shape
     if lower.stride(0) != upper.stride(0):
         raise ValueError("lower and upper must share a row stride")
     rc = lib().sfa_index_scores_bounded(_p(q_idx), _p(w), _p(q_seq), _p(q_pos), n_q, q_group,
                                         h_idx, d_idx, compress_ratio, _p(Kbar), Kbar.stride(0),
-                                        Kbar.shape[0], n_blk_max, _p(lower), _p(upper),
-                                        lower.stride(0), _p(dev_status), _stream(stream))
+                                        _p(Kbar_r), Kbar_r.stride(0), Kbar.shape[0], n_blk_max,
+                                        _p(lower), _p(upper), lower.stride(0), _p(dev_status),
+                                        _stream(stream))
     _check("sfa_index_scores_bounded", rc)
 
 

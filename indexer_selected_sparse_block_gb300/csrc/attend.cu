@@ -141,6 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     const bool lead = split == 0 && g == 0;
+    pdl_wait();   // global memory from here on
+    pdl_trigger();
     const ListInfo L = list_info(p, i, lead && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -554,6 +556,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
+    pdl_wait();   // global memory from here on
+    pdl_trigger();
     const ListInfo L = list_info(p, i, split == 0 && g == 0 && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -970,6 +974,8 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
     const int tid = threadIdx.x;
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     const int row = tid >> 3, part = tid & 7;
+    pdl_wait();   // global memory from here on
+    pdl_trigger();
     const ListInfo L = list_info(p, i, split == 0 && g == 0 && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -1034,6 +1040,8 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
 // consecutive value dims and sums the weighted partials with 16-byte loads.
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p, int dv) {
     extern __shared__ float s_w[];  // [n_split] weights, then 1/L and M
+    pdl_wait();   // the partials of the attention kernel
+    pdl_trigger();
     const int i = blockIdx.x / p.h_q, h = blockIdx.x % p.h_q;
     const int g = h / p.G, row = h % p.G;
     const int64_t base0 = ((int64_t)i * p.h_kv + g) * p.n_split * p.G + row;
@@ -1147,8 +1155,11 @@ int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
         if (!allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    attend_bf16_kernel<DKQ, DV, VK><<<grid, kThreads, smem, st>>>(q);
-    SFA_CHECK_LAUNCH();
+    if (launch_pdl(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads), smem, st, q) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
     return SFA_OK;
 }
 
@@ -1180,8 +1191,11 @@ int launch_tc(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
         if (!allow_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    attend_tc_kernel<DKQ, DV, VK><<<grid, tc::kThreads, smem, st>>>(kmap, vmap, p);
-    SFA_CHECK_LAUNCH();
+    if (launch_pdl(attend_tc_kernel<DKQ, DV, VK>, grid, dim3(tc::kThreads), smem, st, kmap, vmap,
+                   p) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
     return SFA_OK;
 }
 
@@ -1254,16 +1268,21 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
         else rc = V ? launch_bf16<64, 64, false>(p, grid, st, bl) : launch_bf16<64, 64, true>(p, grid, st, bl);
     } else {
-        if (dkq == 576) attend_f32_kernel<576, 512><<<grid, kThreads, 0, st>>>(p);
-        else if (dkq == 512) attend_f32_kernel<512, 512><<<grid, kThreads, 0, st>>>(p);
-        else if (dkq == 128) attend_f32_kernel<128, 128><<<grid, kThreads, 0, st>>>(p);
-        else attend_f32_kernel<64, 64><<<grid, kThreads, 0, st>>>(p);
-        rc = cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+        const cudaError_t e =
+            dkq == 576   ? launch_pdl(attend_f32_kernel<576, 512>, grid, dim3(kThreads), 0, st, p)
+            : dkq == 512 ? launch_pdl(attend_f32_kernel<512, 512>, grid, dim3(kThreads), 0, st, p)
+            : dkq == 128 ? launch_pdl(attend_f32_kernel<128, 128>, grid, dim3(kThreads), 0, st, p)
+                         : launch_pdl(attend_f32_kernel<64, 64>, grid, dim3(kThreads), 0, st, p);
+        if (e != cudaSuccess) cudaGetLastError();
+        rc = e == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
     }
     if (rc != SFA_OK) return rc;
     if (sp.n_split > 1) {
-        combine_kernel<<<n_q * h_q, 128, (sp.n_split + 2) * sizeof(float), st>>>(p, dv);
-        SFA_CHECK_LAUNCH();
+        if (launch_pdl(combine_kernel, dim3(n_q * h_q), dim3(128), (sp.n_split + 2) * sizeof(float),
+                       st, p, dv) != cudaSuccess) {
+            cudaGetLastError();
+            return SFA_ERR_CUDA;
+        }
     }
     return SFA_OK;
 }

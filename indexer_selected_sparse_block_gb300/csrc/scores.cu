@@ -29,12 +29,13 @@ namespace {
 constexpr int kBM = 128;               // blocks per tile (MMA M)
 constexpr int kThreads = 192;          // 6 warps
 constexpr int kSlabBytes = kBM * 128;  // one pipeline stage
-// The bounded mode's error bound per score: |s - a| <= kLoRel * C_q * |hi_b|_2 (+ kAbs), where
-// the lo half of a pooled key is the rounding remainder of bf16(m): |lo_e| <= 2^-9 |m_e| <=
-// 2^-9 / (1 - 2^-9) |hi_e| (plus 2^-134 below the normal range), ReLU is 1-Lipschitz and the
-// head sum is weighted by w (Cauchy-Schwarz per head).  The factor 1.02 covers the fp32
-// rounding of the approximate dot product (128 terms: < 2^-16 relative) and of the bound.
-constexpr float kLoRel = 1.953125e-3f * 1.02f;
+// The bounded mode's error bound per score: |s - a| <= e = kMargin * C_q * r_b (+ kAbs), with
+// C_q = sum_j |w_j| |q_j|_2 and r_b = |lo_b|_2 + 2^-14 |hi_b|_2 from the pooling pass.  The
+// exact difference of the two scores is at most C_q |lo_b|_2 (ReLU is 1-Lipschitz, the head
+// sum is weighted by w, Cauchy-Schwarz per head); the fp32 rounding of the two MMA chains and
+// of the head sums is below 2^-15 C_q |hi_b|_2, which the second term of r_b covers twice;
+// kMargin covers the rounding of C_q and of e itself.
+constexpr float kMargin = 1.0f + 9.765625e-4f;
 constexpr float kAbs = 1e-30f;
 
 struct ScoreParams {
@@ -44,6 +45,8 @@ struct ScoreParams {
     const int32_t *q_pos;
     float *scores;       // exact mode: the scores; bounded mode: their lower bounds
     float *bounds;       // bounded mode: the upper bounds (else null)
+    const float *kbar_r; // bounded mode: the per-block bound factors r_b
+    int64_t kr_seq_stride;
     int32_t *status;
     int64_t score_stride;
     int64_t blk_cap;
@@ -84,14 +87,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = blockIdx.y * p.q_tile;
     const int nq_tile = min(p.q_tile, p.n_q - q0);
-    const int seq0 = p.q_seq[q0];
-    const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
 
     // ---------------------------------------------------------------- set-up (all warps)
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], HI ? 1 + 4 : 1);   // bounded mode: + the four norm readers
+            mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -106,6 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
     }
+    pdl_wait();   // global memory from here on
+    pdl_trigger();
+    const int seq0 = p.q_seq[q0];
+    const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
     for (int qq = threadIdx.x; qq < p.q_tile; qq += kThreads) {
         int nb = -1;
         if (qq < nq_tile) {
@@ -245,43 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < my_tiles; ++it) {
             const int acc = it & 1;
             if (*abort_flag) break;
-            float nrm2 = 0.f;   // bounded mode: |hi_b|^2 of this thread's block row
-            if constexpr (HI) {
-                const int r = quarter * 32 + lane;
-                bool ok = true;
-                for (int sl = 0; sl < L::kSlabs; ++sl) {
-                    const int ld = it * L::kSlabs + sl, st = ld % S;
-                    if (!mbar_wait(&full[st], (ld / S) & 1, deadline)) { ok = false; break; }
-                    const uint8_t *row = sA + (size_t)st * kSlabBytes + r * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
-                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float x0 = __uint_as_float(w4[q] << 16);
-                            const float x1 = __uint_as_float(w4[q] & 0xFFFF0000u);
-                            nrm2 = fmaf(x0, x0, nrm2);
-                            nrm2 = fmaf(x1, x1, nrm2);
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);   // this warp is done with the slab
-                }
-                if (!ok) {
-                    set_status(p.status, SFA_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-            }
+            const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
+            // bounded mode: this block's bound factor, loaded before the accumulator wait
+            const float rb = (HI && b < p.n_blk_max) ? __ldg(p.kbar_r + (int64_t)seq0 * p.kr_seq_stride + b) : 0.f;
             if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, deadline)) {
                 set_status(p.status, SFA_DEV_TIMEOUT);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
-            const float hn = HI ? sqrtf(nrm2) : 0.f;
             for (int c0 = 0; c0 < ncols; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tmem_base + lane_addr + (uint32_t)(acc * N + c0), r);
@@ -297,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (b < s_nblk[qq]) {
                         const int64_t o = (int64_t)(q0 + qq) * p.score_stride + b;
                         if (HI) {
-                            const float e = fmaf(kLoRel * s_cq[qq], hn, kAbs);
+                            const float e = fmaf(kMargin * s_cq[qq], rb, kAbs);
                             p.scores[o] = s - e;   // the hi + lo score lies in [s - e, s + e]
                             p.bounds[o] = s + e;
                         } else {
@@ -356,8 +333,11 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
     if (cta_per_qtile < 1) cta_per_qtile = 1;
     p.tiles_per_cta = (n_blk_tiles + cta_per_qtile - 1) / cta_per_qtile;
     const int grid_x = (n_blk_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
-    index_score_kernel<KP, H, HI><<<dim3(grid_x, n_qtiles), kThreads, smem, stream>>>(map, p);
-    SFA_CHECK_LAUNCH();
+    if (launch_pdl(index_score_kernel<KP, H, HI>, dim3(grid_x, n_qtiles), dim3(kThreads), smem,
+                   stream, map, p) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
     return SFA_OK;
 }
 
@@ -369,9 +349,11 @@ namespace {
 
 int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const int32_t *q_pos,
                int n_q, int q_group, int h_idx, int d_idx, int compress_ratio, const void *Kbar,
-               int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max, float *scores,
-               float *bounds, int64_t score_stride, int32_t *dev_status, cudaStream_t st) {
+               int64_t kbar_seq_stride, const float *kbar_r, int64_t kr_seq_stride, int n_seq,
+               int64_t n_blk_max, float *scores, float *bounds, int64_t score_stride,
+               int32_t *dev_status, cudaStream_t st) {
     const bool hi = bounds != nullptr;
+    if (hi && (!kbar_r || kr_seq_stride < n_blk_max)) return SFA_ERR_INVALID_ARG;
     if (!q_idx || !w || !q_seq || !q_pos || !Kbar || !scores) return SFA_ERR_INVALID_ARG;
     if (n_q < 0 || q_group < 1 || n_seq < 1 || compress_ratio < 1 || n_blk_max < 0)
         return SFA_ERR_INVALID_ARG;
@@ -399,6 +381,8 @@ int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const in
     p.q_pos = q_pos;
     p.scores = scores;
     p.bounds = bounds;
+    p.kbar_r = kbar_r;
+    p.kr_seq_stride = kr_seq_stride;
     p.status = dev_status;
     p.score_stride = score_stride;
     p.blk_cap = blk_cap;
@@ -445,18 +429,19 @@ extern "C" int sfa_index_scores(const void *q_idx, const float *w, const int32_t
                                 float *scores, int64_t score_stride, int32_t *dev_status,
                                 sfa_stream_t stream) {
     return sfa::run_scores(q_idx, w, q_seq, q_pos, n_q, q_group, h_idx, d_idx, compress_ratio,
-                           Kbar, kbar_seq_stride, n_seq, n_blk_max, scores, nullptr,
+                           Kbar, kbar_seq_stride, nullptr, 0, n_seq, n_blk_max, scores, nullptr,
                            score_stride, dev_status, (cudaStream_t)stream);
 }
 
 extern "C" int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
                                         const int32_t *q_pos, int n_q, int q_group, int h_idx,
                                         int d_idx, int compress_ratio, const void *Kbar,
-                                        int64_t kbar_seq_stride, int n_seq, int64_t n_blk_max,
+                                        int64_t kbar_seq_stride, const float *Kbar_r,
+                                        int64_t kr_seq_stride, int n_seq, int64_t n_blk_max,
                                         float *lower, float *upper, int64_t score_stride,
                                         int32_t *dev_status, sfa_stream_t stream) {
     if (!upper || !sfa::aligned16(upper)) return SFA_ERR_INVALID_ARG;
     return sfa::run_scores(q_idx, w, q_seq, q_pos, n_q, q_group, h_idx, d_idx, compress_ratio,
-                           Kbar, kbar_seq_stride, n_seq, n_blk_max, lower, upper, score_stride,
-                           dev_status, (cudaStream_t)stream);
+                           Kbar, kbar_seq_stride, Kbar_r, kr_seq_stride, n_seq, n_blk_max, lower,
+                           upper, score_stride, dev_status, (cudaStream_t)stream);
 }

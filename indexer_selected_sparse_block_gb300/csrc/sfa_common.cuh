@@ -28,6 +28,26 @@ namespace sfa {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launches `kernel` with programmatic dependent launch allowed: its CTAs may start while the
+// kernel before it in the stream finishes.  Every kernel launched this way calls pdl_wait()
+// before its first global-memory access, which returns once that kernel has completed and
+// its writes are visible (at once when the stream held no kernel before it).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 int device_sm_count();  // cached per device (api.cu)
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time libcuda; api.cu).
@@ -61,6 +81,14 @@ constexpr uint64_t kWaitLimitNs = 1500000000ull;
 // ----------------------------------------------------------------------------- device side
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
+}
+
+// Programmatic dependent launch, device side: pdl_wait() blocks until the previous kernel in
+// the stream has completed (its writes visible); pdl_trigger() lets the next kernel start
+// launching once every CTA of this one has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

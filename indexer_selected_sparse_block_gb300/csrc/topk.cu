@@ -439,6 +439,8 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
     const int k = p.top_k;
     const int n_items = n_q * n_chunks;
     clear_hist(sh, kBins);   // kept zero between items from here on
+    pdl_wait();              // global memory from here on
+    pdl_trigger();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int i = item / n_chunks, c = item % n_chunks;
         int64_t len = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
@@ -730,6 +732,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     const int k = p.top_k, H = p.H;
     const int n_cl = gridDim.x / kCl;
     clear_hist(sh, kBins);   // kept zero between rows from here on
+    pdl_wait();              // global memory from here on
+    pdl_trigger();
     cluster.sync();          // every CTA of the cluster is running before any remote access
     for (int i = blockIdx.x / kCl; i < n_q; i += n_cl) {
         const int seq = p.q_seq[i];
@@ -1008,8 +1012,11 @@ int launch_bounded_d(const RefineParams &p, int n_q, cudaStream_t st) {
     int clusters = device_sm_count() / kCl;
     if (clusters < 1) return SFA_ERR_CUDA;
     if (n_q < clusters) clusters = n_q;
-    bounded_select_kernel<D><<<clusters * kCl, kThreads, sizeof(BoundedSmem), st>>>(p, n_q);
-    SFA_CHECK_LAUNCH();
+    if (launch_pdl(bounded_select_kernel<D>, dim3(clusters * kCl), dim3(kThreads),
+                   sizeof(BoundedSmem), st, p, n_q) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
     return SFA_OK;
 }
 
@@ -1050,8 +1057,11 @@ int launch_stage(const TopkParams &p, int n_q, int n_chunks, cudaStream_t st) {
         if (!allow_max_dynamic_smem(topk_stage_kernel<R>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    topk_stage_kernel<R><<<grid, kThreads, smem_bytes<R>(), st>>>(p, n_q, n_chunks);
-    SFA_CHECK_LAUNCH();
+    if (launch_pdl(topk_stage_kernel<R>, dim3(grid), dim3(kThreads), smem_bytes<R>(), st, p, n_q,
+                   n_chunks) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
     return SFA_OK;
 }
 

@@ -43,6 +43,9 @@ class SfaStep:
         if self.bounded and n_blk_max > B.SFA_REFINE_MAX_BLOCKS:
             raise ValueError(f"bounded selection takes rows of at most "
                              f"{B.SFA_REFINE_MAX_BLOCKS} blocks, got n_blk_max={n_blk_max}")
+        # bounded: the pooling pass also writes each pooled row's bound factor
+        self.Kbar_r = (torch.zeros((n_seq, max(self.blk_cap, 1)), dtype=torch.float32, device=dev)
+                       if self.bounded else None)
         self.scores = torch.empty((n_q, max(n_blk_max, 1)), dtype=torch.float32, device=dev)
         # bounded: scores holds the lower bounds and upper the upper bounds
         self.upper = (torch.empty_like(self.scores) if self.bounded else None)
@@ -63,11 +66,12 @@ class SfaStep:
 
     def pool(self, X, blk_begin: int, blk_end: int, stream=None):
         if blk_end > blk_begin:
-            B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, stream=stream)
+            B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, self.Kbar_r,
+                                  stream=stream)
 
     def score(self, q_idx, w, q_seq, q_pos, stream=None):
         if self.bounded:
-            B.sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, self.Kbar, self.cr,
+            B.sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, self.Kbar, self.Kbar_r, self.cr,
                                        self.n_blk_max, self.scores, self.upper,
                                        q_group=self.q_group, dev_status=self.status,
                                        stream=stream)

@@ -44,14 +44,16 @@ ODD = ctypes.c_void_p(0x10008)      # not 16-byte aligned
 
 def test_pool_rejects_bad_arguments(L):
     f = L.sfa_pool_index_keys
-    assert f(None, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1
-    assert f(FAKE, 2, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1          # dtype
-    assert f(FAKE, 0, 1024, 1, 48, 4, 0, 4, FAKE, 1024, None) == 2          # d_idx
-    assert f(FAKE, 0, 1024, 1, 64, 0, 0, 4, FAKE, 1024, None) == 1          # cr
-    assert f(FAKE, 0, 1024, 1, 64, 4, 5, 4, FAKE, 1024, None) == 1          # begin > end
-    assert f(ODD, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1           # alignment
-    assert f(FAKE, 0, 100, 1, 64, 4, 0, 4, FAKE, 1024, None) == 1           # X too short
-    assert f(FAKE, 0, 1024, 1, 64, 4, 0, 0, FAKE, 1024, None) == 0          # empty: no work
+    assert f(None, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None, 0, None) == 1
+    assert f(FAKE, 2, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None, 0, None) == 1          # dtype
+    assert f(FAKE, 0, 1024, 1, 48, 4, 0, 4, FAKE, 1024, None, 0, None) == 2          # d_idx
+    assert f(FAKE, 0, 1024, 1, 64, 0, 0, 4, FAKE, 1024, None, 0, None) == 1          # cr
+    assert f(FAKE, 0, 1024, 1, 64, 4, 5, 4, FAKE, 1024, None, 0, None) == 1          # begin > end
+    assert f(ODD, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, None, 0, None) == 1           # alignment
+    assert f(FAKE, 0, 100, 1, 64, 4, 0, 4, FAKE, 1024, None, 0, None) == 1           # X too short
+    assert f(FAKE, 0, 1024, 1, 64, 4, 0, 4, FAKE, 1024, FAKE, 3, None) == 1          # Kbar_r short
+    assert f(FAKE, 0, 1536, 1, 96, 4, 0, 4, FAKE, 1024, FAKE, 4, None) == 2          # r for 96
+    assert f(FAKE, 0, 1024, 1, 64, 4, 0, 0, FAKE, 1024, None, 0, None) == 0          # empty: no work
 
 
 def test_scores_reject_bad_arguments(L):
@@ -67,6 +69,32 @@ def test_scores_reject_bad_arguments(L):
     assert f(*bad) == 1                                                    # q_group
     bad = list(ok); bad[10] = 250
     assert f(*bad) == 1                                                    # stride % 2*d_idx
+
+
+def test_bounded_entry_points_reject_bad_arguments(L):
+    f = L.sfa_index_scores_bounded
+    #     q_idx w     q_seq q_pos n_q grp h  d    cr Kbar  stride     Kbar_r kr   n_seq nbm
+    ok = [FAKE, FAKE, FAKE, FAKE, 4, 1, 8, 128, 4, FAKE, 256 * 100, FAKE, 100, 1, 100,
+          FAKE, FAKE, 100, None, None]
+    bad = list(ok); bad[11] = None
+    assert f(*bad) == 1                                                    # no bound factors
+    bad = list(ok); bad[12] = 99
+    assert f(*bad) == 1                                                    # factor rows short
+    bad = list(ok); bad[16] = None
+    assert f(*bad) == 1                                                    # no upper array
+    g = L.sfa_topk_blocks_refine
+    #     lower upper stride q_idx w  q_seq q_pos n_q h  d   Kbar  kstride    n_seq cr top_k nbm
+    ok = [FAKE, FAKE, 100, FAKE, FAKE, FAKE, FAKE, 4, 8, 128, FAKE, 256 * 100, 1, 4, 16, 100,
+          FAKE, FAKE, FAKE, 1 << 20, None, None]
+    bad = list(ok); bad[15] = 40000
+    assert g(*bad) == 2                                                    # rows > 36864
+    bad = list(ok); bad[14] = 0
+    assert g(*bad) == 2                                                    # top_k
+    bad = list(ok); bad[10] = ODD
+    assert g(*bad) == 1                                                    # Kbar alignment
+    bad = list(ok); bad[18] = None
+    assert g(*bad) == 4                                                    # workspace
+    assert L.sfa_topk_refine_workspace_bytes(4, 100) > 4 * 100 * 8
 
 
 def test_topk_rejects_bad_arguments(L):

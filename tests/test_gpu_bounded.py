@@ -36,22 +36,46 @@ def _case(dev, seed, n_seq, n_tok, d_idx, h_idx, cr, q_pos, constant_keys=False)
     q_pos = torch.tensor(q_pos, dtype=torch.int32)
     blk_cap = n_tok // cr
     Kbar = torch.zeros(sfa.kbar_shape(n_seq, blk_cap, d_idx), dtype=torch.bfloat16, device=dev)
-    sfa.sfa_pool_index_keys(X, cr, 0, blk_cap, Kbar)
-    return X, qi, w, q_seq.to(dev), q_pos.to(dev), Kbar
+    Kr = torch.zeros((n_seq, blk_cap), dtype=torch.float32, device=dev)
+    sfa.sfa_pool_index_keys(X, cr, 0, blk_cap, Kbar, Kr)
+    return X, qi, w, q_seq.to(dev), q_pos.to(dev), (Kbar, Kr)
+
+
+@pytest.mark.parametrize("d_idx", [128, 64, 32])
+def test_pool_bound_factors(dev, d_idx):
+    """r_b from the pooling pass bounds (|lo_b|_2 + 2^-14 |hi_b|_2) of the stored halves from
+    above, within the fp32 margin, for bf16 and fp32 raw keys."""
+    for dtype in (torch.bfloat16, torch.float32):
+        g = torch.Generator().manual_seed(d_idx)
+        cr, n_seq, n_tok = 3, 2, 3000
+        X = (torch.randn((n_seq, n_tok, d_idx), generator=g) * 5).to(dtype).to(dev)
+        blk_cap = n_tok // cr
+        Kbar = torch.zeros(sfa.kbar_shape(n_seq, blk_cap, d_idx), dtype=torch.bfloat16, device=dev)
+        Kr = torch.full((n_seq, blk_cap), -1.0, device=dev)
+        sfa.sfa_pool_index_keys(X, cr, 7, blk_cap - 5, Kbar, Kr)
+        torch.cuda.synchronize()
+        kb = Kbar.float().cpu().double().numpy()
+        r = np32(Kr).astype(np.float64)
+        hi, lo = kb[..., :d_idx], kb[..., d_idx:]
+        ref = np.sqrt((lo ** 2).sum(-1)) + 2.0 ** -14 * np.sqrt((hi ** 2).sum(-1))
+        inside = slice(7, blk_cap - 5)
+        assert np.all(r[:, inside] >= ref[:, inside])
+        assert np.all(r[:, inside] <= ref[:, inside] * (1 + 2.0 ** -14) + 1e-30)
+        assert np.all(r[:, :7] == -1.0) and np.all(r[:, blk_cap - 5:] == -1.0)   # untouched
 
 
 @pytest.mark.parametrize("d_idx,h_idx", [(128, 8), (64, 4), (128, 16)])
 def test_bounds_hold(dev, d_idx, h_idx):
     cr, n_seq, n_tok = 4, 3, 6000
-    X, qi, w, q_seq, q_pos, Kbar = _case(dev, d_idx + h_idx, n_seq, n_tok, d_idx, h_idx, cr,
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, d_idx + h_idx, n_seq, n_tok, d_idx, h_idx, cr,
                                          [5999, 4003, 1299])
     n_blk_max = 1500
     exact = torch.full((3, n_blk_max), float("nan"), device=dev)
     lower = torch.full_like(exact, float("nan"))
     upper = torch.full_like(exact, float("nan"))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, exact, dev_status=status)
-    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper,
+    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kb[0], cr, n_blk_max, exact, dev_status=status)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
                                  dev_status=status)
     torch.cuda.synchronize()
     assert sfa.sfa_read_device_status(status) == 0
@@ -69,16 +93,16 @@ def test_bounds_hold(dev, d_idx, h_idx):
 def test_refine_follows_agreement_rule(dev, top_k):
     cr, d_idx, h_idx = 4, 128, 8
     pos = [11999, 9000, 2047, 700, 3, 8191]
-    X, qi, w, q_seq, q_pos, Kbar = _case(dev, top_k, 2, 12000, d_idx, h_idx, cr, pos)
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, top_k, 2, 12000, d_idx, h_idx, cr, pos)
     n_q, n_blk_max = len(pos), 3000
     lower = torch.empty((n_q, n_blk_max), device=dev)
     upper = torch.empty_like(lower)
     blk = torch.full((n_q, top_k), -7, dtype=torch.int32, device=dev)
     n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper,
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
                                  dev_status=status)
-    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kbar, cr, top_k, n_blk_max,
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
                                blk, n_sel, dev_status=status)
     torch.cuda.synchronize()
     assert sfa.sfa_read_device_status(status) == 0
@@ -104,15 +128,15 @@ def test_refine_all_tied(dev, n_tok):
     resolved in shared memory and takes the global-memory path."""
     cr, d_idx, h_idx, top_k = 4, 64, 4, 100
     pos = [n_tok - 1, n_tok // 2 + 1]
-    X, qi, w, q_seq, q_pos, Kbar = _case(dev, 3, 2, n_tok, d_idx, h_idx, cr, pos,
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 3, 2, n_tok, d_idx, h_idx, cr, pos,
                                          constant_keys=True)
     n_q, n_blk_max = 2, n_tok // cr
     lower = torch.empty((n_q, n_blk_max), device=dev)
     upper = torch.empty_like(lower)
     blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
     n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
-    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, Kbar, cr, n_blk_max, lower, upper)
-    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kbar, cr, top_k, n_blk_max,
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
                                blk, n_sel)
     torch.cuda.synchronize()
     got = np32(blk)
@@ -124,7 +148,7 @@ def test_refine_all_tied(dev, n_tok):
 def test_refine_below_budget_and_bad_query(dev):
     cr, d_idx, h_idx, top_k = 4, 64, 4, 50
     pos = [150, 2, 3999]
-    X, qi, w, q_seq, q_pos, Kbar = _case(dev, 9, 1, 4000, d_idx, h_idx, cr, pos)
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 9, 1, 4000, d_idx, h_idx, cr, pos)
     n_q, n_blk_max = 3, 1000
     q_pos_bad = q_pos.clone()
     q_pos_bad[2] = -1                                     # a query outside the cache
@@ -133,9 +157,9 @@ def test_refine_below_budget_and_bad_query(dev):
     blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
     n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos_bad, Kbar, cr, n_blk_max, lower, upper,
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos_bad, *Kb, cr, n_blk_max, lower, upper,
                                  dev_status=status)
-    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos_bad, Kbar, cr, top_k,
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos_bad, Kb[0], cr, top_k,
                                n_blk_max, blk, n_sel, dev_status=status)
     torch.cuda.synchronize()
     assert sfa.sfa_read_device_status(status) & sfa.SFA_DEV_BAD_QUERY
