@@ -196,7 +196,8 @@ class Workbench:
             n_kv = w.indexer_top_k * w.compress_ratio + w.compress_ratio - 1
         else:
             n_kv = st.n_kv_dense
-        n += 1 + (B.sfa_attend_workspace_bytes(w.n_q, w.h_q, w.h_kv, w.dv, n_kv) > 0)
+        n += B.sfa_attend_plan(B.SFA_BF16, w.n_q, w.h_kv, w.dkq, not w.v_is_k, n_kv,
+                               w.compress_ratio, st.dense)[1]
         return n
 
     def run_step(self, events=None):
@@ -440,7 +441,11 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        step_ms, stage_ms = measure(wb, args.steps, args.warmup, flush, clk=clk)
+        # the timed steps run back to back with no event between their kernels (an event
+        # there would hold each kernel until the one before it has fully drained); the
+        # per-stage split comes from a separate, shorter pass with events between stages
+        step_ms, _ = measure(wb, args.steps, args.warmup, flush, per_stage=False, clk=clk)
+        _, stage_ms = measure(wb, max(3, args.steps // 2), 3, flush, per_stage=True)
         total_ms = sum(step_ms)
         if dist is not None:
             t = torch.tensor([total_ms], device=dev)
@@ -541,7 +546,8 @@ def main():
     if not args.no_second and rank == 0 and world == 1:
         w2 = sfa.WORKLOADS[SECOND_WORKLOAD]
         wb2 = Workbench(w2, dev)
-        s2, st2 = measure(wb2, max(3, args.steps // 4), 3, flush)
+        s2, _ = measure(wb2, max(3, args.steps // 4), 3, flush, per_stage=False)
+        _, st2 = measure(wb2, 3, 3, flush, per_stage=True)
         ms2 = sum(s2) / len(s2)
         n_sel2 = wb2.step.n_sel.cpu()
         att2 = [int(n) * w2.compress_ratio + (int(p) + 1) % w2.compress_ratio

@@ -201,8 +201,19 @@ int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score
  *        dv > dkq needs a separate V.  SFA_ATTEND_KERNEL=tcgen05 in the environment selects the
  *        tcgen05 kernel for dkq 576 / 512 (default: the mma.sync kernel; same results).
  *        (fp32): the same (dkq, dv) pairs and h_q/h_kv <= 16.
+ * Few (query, KV head) lists are split over several CTAs (flash-decoding); with the bf16
+ * kernel, 2 to 8 splits merge inside a thread-block cluster, else a second kernel merges them.
  */
 size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max);
+/*
+ * sfa_attend_plan -- the launch plan the attention entry points take on the current device
+ * for these sizes: *n_split CTAs per (query, KV head) list and *kernels launched per call
+ * (1, or 2 when a merge kernel follows).  n_kv_max as in sfa_attend_workspace_bytes (the
+ * dense entry point: n_tok_cap, dense = 1); has_v: a separate V is given.  Host only, no
+ * launch.  SFA_ERR_INVALID_ARG / SFA_ERR_UNSUPPORTED as the entry points.
+ */
+int sfa_attend_plan(int dtype, int n_q, int h_kv, int dkq, int has_v, int64_t n_kv_max,
+                    int compress_ratio, int dense, int *n_split, int *kernels);
 int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
                       int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv,
                       float scale, const int32_t *q_seq, const int32_t *q_pos,

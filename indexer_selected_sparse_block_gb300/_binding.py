@@ -34,6 +34,7 @@ SIGNATURES = {
     "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
                                         _i64, _vp, _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
     "sfa_topk_workspace_bytes": (_sz, [_int, _i64, _int]),
+    "sfa_attend_plan": (_int, [_int, _int, _int, _int, _int, _i64, _int, _int, _vp, _vp]),
     "sfa_topk_refine_workspace_bytes": (_sz, [_int, _i64]),
     "sfa_topk_blocks_refine": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _int, _int, _vp,
                                       _i64, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp,
@@ -193,6 +194,17 @@ def sfa_topk_blocks(scores, q_pos, compress_ratio: int, top_k: int, n_blk_max: i
 
 def sfa_attend_workspace_bytes(n_q: int, h_q: int, h_kv: int, dv: int, n_kv_max: int) -> int:
     return int(lib().sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max))
+
+
+def sfa_attend_plan(dtype_code: int, n_q: int, h_kv: int, dkq: int, has_v: bool, n_kv_max: int,
+                    compress_ratio: int, dense: bool = False):
+    """(n_split, kernels): CTAs per (query, KV head) list and kernels one attention call
+    launches on the current device."""
+    ns, nk = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().sfa_attend_plan(dtype_code, n_q, h_kv, dkq, int(has_v), n_kv_max, compress_ratio,
+                               int(dense), ctypes.byref(ns), ctypes.byref(nk))
+    _check("sfa_attend_plan", rc)
+    return ns.value, nk.value
 
 
 def _attn_dims(Q, K, V, O):

@@ -28,10 +28,14 @@
 
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "sfa_common.cuh"
 
 namespace sfa {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kT = 32;          // tokens per tile
 constexpr int kThreads = 128;   // 4 warps
@@ -45,6 +49,7 @@ struct AttnParams {
     int32_t *status;
     int64_t k_tok_stride, k_seq_stride, v_tok_stride, v_seq_stride, n_tok_cap;
     int n_seq, n_q, h_q, h_kv, G, top_k, cr, dense, n_split, split_tokens, stages;
+    int cluster_merge;   // 1: the n_split CTAs of an item form one cluster and merge in place
     float scale_log2;
 };
 
@@ -116,6 +121,53 @@ __device__ __forceinline__ int token_at(const AttnParams &p, const ListInfo &L, 
 
 __device__ __forceinline__ uint32_t swz(int c, int r) { return (uint32_t)((c & ~7) | ((c ^ r) & 7)); }
 
+// The merge of the splits of one (query, KV head) inside their cluster (flash-decoding without
+// a second kernel): each CTA holds its unnormalised O rows sPart[G][DV] and their (m, l) in
+// sM, sL (base-2 maxima and sums); CTA r of the n_split writes the value dims [r DV/ns,
+// (r+1) DV/ns) of every row as sum_c w_c O_c / sum_c w_c l_c with w_c = 2^(m_c - M), reading
+// the other CTAs' shared memory.  sW (n_split * 16 + 32 floats) is this CTA's scratch.
+template <int DV>
+__device__ void cluster_merge(const AttnParams &p, float *sPart, float *sL, float *sM, float *sW,
+                              int i, int g) {
+    cg::cluster_group cl = cg::this_cluster();
+    const int tid = threadIdx.x, G = p.G, ns = p.n_split;
+    cl.sync();   // every CTA's partial rows and statistics are in its shared memory
+    const int r = (int)cl.block_rank();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int c = 0; c < ns; ++c) M = fmaxf(M, cl.map_shared_rank(sM, c)[tid]);
+        float Lsum = 0.f;
+        for (int c = 0; c < ns; ++c) {
+            const float m = cl.map_shared_rank(sM, c)[tid];
+            const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+            sW[c * 16 + tid] = w;
+            Lsum += w * cl.map_shared_rank(sL, c)[tid];
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        for (int c = 0; c < ns; ++c) sW[c * 16 + tid] *= inv;
+        if (r == 0 && p.lse)
+            p.lse[(int64_t)i * p.h_q + g * G + tid] = Lsum > 0.f ? (M + log2f(Lsum)) / kLog2e : -INFINITY;
+    }
+    __syncthreads();
+    const int dq = DV / ns / 4;   // float4 per row in this CTA's slice
+    const int d0 = r * (DV / ns);
+    for (int e = tid; e < G * dq; e += kThreads) {
+        const int row = e / dq, d = d0 + 4 * (e % dq);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < ns; ++c) {
+            const float w = sW[c * 16 + row];
+            if (w == 0.f) continue;   // an empty split: its rows are not written
+            const float4 v = *reinterpret_cast<const float4 *>(cl.map_shared_rank(sPart, c) + row * DV + d);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(p.O + ((int64_t)i * p.h_q + g * G + row) * DV + d) = acc;
+    }
+    cl.sync();   // no CTA leaves while another may still read its shared memory
+}
+
 template <int DKQ, int DV, bool V_IS_K>
 __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnParams p) {
     constexpr int KROW = DKQ * 2;                 // bytes of a K row in shared memory
@@ -149,6 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     const int G = p.G;
 
     if (j0 >= j1) {  // nothing to attend in this split
+        if (p.cluster_merge) {   // it still takes its part in the cluster's merge
+            if (tid < 16) {
+                sL[tid] = 0.f;
+                sM[tid] = -INFINITY;
+            }
+            cluster_merge<DV>(p, reinterpret_cast<float *>(sStage), sL, sM,
+                              reinterpret_cast<float *>(sStage) + 16 * DV, i, g);
+            return;
+        }
         for (int e = tid; e < G * DV; e += kThreads) {
             const int row = e / DV, d = e % DV;
             const int h = g * G + row;
@@ -361,6 +422,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     }
     __syncthreads();
     const int dv0 = warp * (DV / 4);
+    if (p.cluster_merge) {   // the unnormalised rows into this CTA's (now idle) stage memory
+        float *sPart = reinterpret_cast<float *>(sStage);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int row = gq + half * 8;
+            if (row >= G) continue;
+#pragma unroll
+            for (int n = 0; n < NTV; ++n)
+                *reinterpret_cast<float2 *>(sPart + row * DV + dv0 + n * 8 + 2 * tq) =
+                    make_float2(o[n][2 * half], o[n][2 * half + 1]);
+        }
+        cluster_merge<DV>(p, sPart, sL, sM, sPart + 16 * DV, i, g);
+        return;
+    }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int row = gq + half * 8;
@@ -1139,6 +1214,47 @@ int bf16_per_sm(int blk_list) {
     return bf16_smem<DKQ, DV, VK>(2, blk_list) <= 113 * 1024 ? 2 : 1;
 }
 
+// Whether clusters of ns CTAs of the bf16 kernel (its shared memory for blk_list entries) can
+// be resident at all; asked once per (shape, ns, list size).
+template <int DKQ, int DV, bool VK>
+bool bf16_clusters_fit(int ns, int blk_list) {
+    static std::mutex mu;
+    static int cache[9][4] = {};   // [ns][slot]: 0 unknown, 1 yes, 2 no (last four list sizes)
+    static int keys[9][4] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int k = 0; k < 4; ++k)
+        if (cache[ns][k] && keys[ns][k] == blk_list) return cache[ns][k] == 1;
+    int stages = 2;
+    if (bf16_per_sm<DKQ, DV, VK>(blk_list) == 1) {
+        stages = 4;
+        while (stages > 2 && bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) --stages;
+    }
+    const size_t smem = bf16_smem<DKQ, DV, VK>(stages, blk_list);
+    bool ok = allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>);
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ns, 1, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)ns;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, attend_bf16_kernel<DKQ, DV, VK>, &cfg) ==
+                 cudaSuccess && n > 0;
+        cudaGetLastError();
+    }
+    int slot = 0;
+    while (slot < 3 && cache[ns][slot]) ++slot;
+    cache[ns][slot] = ok ? 1 : 2;
+    keys[ns][slot] = blk_list;
+    return ok;
+}
+
 template <int DKQ, int DV, bool VK>
 int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     int stages = 2;
@@ -1155,8 +1271,12 @@ int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
         if (!allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
         attr = true;
     }
-    if (launch_pdl(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads), smem, st, q) !=
-        cudaSuccess) {
+    const cudaError_t e =
+        q.cluster_merge ? launch_pdl_cluster(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads),
+                                             smem, st, q.n_split, q)
+                        : launch_pdl(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads), smem,
+                                     st, q);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
     }
@@ -1199,6 +1319,60 @@ int launch_tc(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     return SFA_OK;
 }
 
+// The launch plan of one attention call: the kernel, the split of each list over CTAs and
+// whether the splits merge inside a cluster (else through combine_kernel).
+struct AttendPlan {
+    SplitPlan sp;
+    int cluster_ns;   // > 1: clusters of this many CTAs merge their splits in place
+    bool use_tc;
+};
+
+AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, int64_t n_kv_max,
+                            int cr, int dense) {
+    // bf16 inputs take the warp-level mma.sync kernel, which is the faster one on the decode
+    // and prefill shapes measured; SFA_ATTEND_KERNEL=tcgen05 selects the tcgen05 kernel for the
+    // 512-wide heads instead (same results within the same tolerances).  fp32 inputs take the
+    // SIMT kernel.
+    const int tc_tile = tc::kTT;
+    AttendPlan ap{};
+    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && want_tcgen05();
+    ap.use_tc = use_tc;
+    // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
+    int per_sm = 1;
+    if (dtype == SFA_BF16 && !use_tc) {
+        const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
+        if (dkq == 576) per_sm = bf16_per_sm<576, 512, true>(bl_max);
+        else if (dkq == 512) per_sm = has_v ? bf16_per_sm<512, 512, false>(bl_max) : bf16_per_sm<512, 512, true>(bl_max);
+        else if (dkq == 128) per_sm = has_v ? bf16_per_sm<128, 128, false>(bl_max) : bf16_per_sm<128, 128, true>(bl_max);
+        else per_sm = has_v ? bf16_per_sm<64, 64, false>(bl_max) : bf16_per_sm<64, 64, true>(bl_max);
+    }
+    SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, use_tc ? tc_tile : kT);
+    // bf16 decode-like plans of a few splits merge them inside a cluster (2, 4 or 8 CTAs)
+    // instead of through a second kernel
+    int cluster_ns = 0;
+    if (dtype == SFA_BF16 && !use_tc && sp.n_split >= 2 && sp.n_split <= 12) {
+        const int ns = sp.n_split >= 6 ? 8 : (sp.n_split >= 3 ? 4 : 2);
+        const int64_t tiles = (n_kv_max + kT - 1) / kT;
+        const int64_t per = (tiles + ns - 1) / ns;
+        const int bl = dense ? 0 : (int)(per * kT / cr + 2);
+        bool fit = (int64_t)((tiles + per - 1) / per) == ns && bl <= kMaxBlkList;
+        if (fit) {
+            if (dkq == 576) fit = bf16_clusters_fit<576, 512, true>(ns, bl);
+            else if (dkq == 512) fit = has_v ? bf16_clusters_fit<512, 512, false>(ns, bl) : bf16_clusters_fit<512, 512, true>(ns, bl);
+            else if (dkq == 128) fit = has_v ? bf16_clusters_fit<128, 128, false>(ns, bl) : bf16_clusters_fit<128, 128, true>(ns, bl);
+            else fit = has_v ? bf16_clusters_fit<64, 64, false>(ns, bl) : bf16_clusters_fit<64, 64, true>(ns, bl);
+        }
+        if (fit) {
+            cluster_ns = ns;
+            sp.n_split = ns;
+            sp.split_tokens = (int)(per * kT);
+        }
+    }
+    ap.sp = sp;
+    ap.cluster_ns = cluster_ns;
+    return ap;
+}
+
 int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq,
                int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv, float scale,
                const int32_t *q_seq, const int32_t *q_pos, const int32_t *blk_idx,
@@ -1218,22 +1392,10 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
-    // bf16 inputs take the warp-level mma.sync kernel, which is the faster one on the decode
-    // and prefill shapes measured; SFA_ATTEND_KERNEL=tcgen05 selects the tcgen05 kernel for the
-    // 512-wide heads instead (same results within the same tolerances).  fp32 inputs take the
-    // SIMT kernel.
-    const int tc_tile = tc::kTT;
-    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && want_tcgen05();
-    // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
-    int per_sm = 1;
-    if (dtype == SFA_BF16 && !use_tc) {
-        const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
-        if (dkq == 576) per_sm = bf16_per_sm<576, 512, true>(bl_max);
-        else if (dkq == 512) per_sm = V ? bf16_per_sm<512, 512, false>(bl_max) : bf16_per_sm<512, 512, true>(bl_max);
-        else if (dkq == 128) per_sm = V ? bf16_per_sm<128, 128, false>(bl_max) : bf16_per_sm<128, 128, true>(bl_max);
-        else per_sm = V ? bf16_per_sm<64, 64, false>(bl_max) : bf16_per_sm<64, 64, true>(bl_max);
-    }
-    const SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, use_tc ? tc_tile : kT);
+    const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, V != nullptr, n_kv_max, cr, dense);
+    const bool use_tc = ap.use_tc;
+    SplitPlan sp = ap.sp;
+    const int cluster_ns = ap.cluster_ns;
     const size_t need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max);
     if (need > 0 && (!ws || ws_bytes < need)) return SFA_ERR_WORKSPACE;
 
@@ -1249,6 +1411,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.n_seq = n_seq; p.n_q = n_q; p.h_q = h_q; p.h_kv = h_kv; p.G = h_q / h_kv;
     p.top_k = top_k; p.cr = cr; p.dense = dense;
     p.n_split = sp.n_split; p.split_tokens = sp.split_tokens;
+    p.cluster_merge = cluster_ns > 1;
     p.scale_log2 = scale * kLog2e;
     if (sp.n_split > 1) {
         const size_t n_rows = (size_t)n_q * h_q * sp.n_split;
@@ -1277,7 +1440,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         rc = e == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
     }
     if (rc != SFA_OK) return rc;
-    if (sp.n_split > 1) {
+    if (sp.n_split > 1 && !p.cluster_merge) {
         if (launch_pdl(combine_kernel, dim3(n_q * h_q), dim3(128), (sp.n_split + 2) * sizeof(float),
                        st, p, dv) != cudaSuccess) {
             cudaGetLastError();
@@ -1289,6 +1452,21 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
 
 }  // namespace
 }  // namespace sfa
+
+extern "C" int sfa_attend_plan(int dtype, int n_q, int h_kv, int dkq, int has_v,
+                               int64_t n_kv_max, int compress_ratio, int dense, int *n_split,
+                               int *kernels) {
+    using namespace sfa;
+    if (!n_split || !kernels || n_q < 1 || h_kv < 1 || n_kv_max < 1 || compress_ratio < 1)
+        return SFA_ERR_INVALID_ARG;
+    if (dtype != SFA_BF16 && dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
+    if (dkq != 576 && dkq != 512 && dkq != 128 && dkq != 64) return SFA_ERR_UNSUPPORTED;
+    const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, has_v != 0, n_kv_max,
+                                           compress_ratio, dense);
+    *n_split = ap.sp.n_split;
+    *kernels = ap.sp.n_split > 1 && ap.cluster_ns <= 1 ? 2 : 1;
+    return SFA_OK;
+}
 
 extern "C" size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max) {
     if (n_q <= 0 || h_q <= 0 || h_kv <= 0 || dv <= 0 || n_kv_max <= 0) return 0;

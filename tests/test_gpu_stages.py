@@ -227,6 +227,40 @@ def test_gather_attend_matches_oracle(dev, dkq, dv, v_is_k, h_q, h_kv, mode, dty
         assert np.abs(Ln[i] - rlse).max() < (2e-3 if dtype == torch.bfloat16 else 1e-5)
 
 
+@pytest.mark.parametrize("n_q", [32, 76, 128])
+def test_gather_attend_cluster_merge(dev, n_q):
+    """Decode batches whose lists the bf16 kernel splits over 8, 4 or 2 CTAs merged inside a
+    cluster (no second kernel): full 512-block lists, shorter ones and tail-only ones (whose
+    later splits are empty) all match the oracle, with their log-sum-exp."""
+    dkq, dv, h_q, h_kv, cr, top_k = 576, 512, 16, 1, 4, 512
+    n_seq, n_tok = 4, 2600
+    rng = np.random.default_rng(n_q)
+    q_seq = (np.arange(n_q) % n_seq).astype(np.int32)
+    kinds = np.arange(n_q) % 4
+    q_pos = np.where(kinds == 0, 2599, np.where(kinds == 1, 2100,
+                     np.where(kinds == 2, rng.integers(300, 1800, n_q), rng.integers(0, 4, n_q))))
+    q_pos = q_pos.astype(np.int32)
+    Q, K, V = _attend_case(dev, dkq, dv, True, h_q, h_kv, n_seq, n_tok, q_seq, q_pos,
+                           torch.bfloat16, 17 + n_q)
+    sel, n_sel = _random_selection(q_pos, cr, top_k, n_q)
+    scale = 1.0 / math.sqrt(dkq)
+    O = torch.full((n_q, h_q, dv), float("nan"), device=dev)
+    lse = torch.full((n_q, h_q), float("nan"), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_gather_attend(Q, K, V, torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_pos).to(dev),
+                          torch.from_numpy(sel).to(dev), torch.from_numpy(n_sel).to(dev), top_k,
+                          cr, scale, O, lse=lse, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Kn, Qn, On, Ln = np32(K), np32(Q), np32(O), np32(lse)
+    for i in range(n_q):
+        s, p = q_seq[i], int(q_pos[i])
+        msk = oracle.mask(p, cr, sel[i], int(n_sel[i]))
+        ref, rlse = oracle.attend(Qn[i], Kn[s], None, msk, scale, h_kv, dv=dv)
+        assert row_rel_err(On[i], ref).max() < TOL_BF16, i
+        assert np.abs(Ln[i] - rlse).max() < 2e-3, i
+
+
 @pytest.mark.parametrize("dkq,dv,v_is_k,h_q,h_kv", ATTN_SHAPES[:2])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_dense_attend_matches_oracle(dev, dkq, dv, v_is_k, h_q, h_kv, dtype):
