@@ -17,9 +17,9 @@
 //               (16 KB, 128-byte swizzle); a tile is 2 (d_idx 64) or 4 (d_idx 128) slabs
 //   warp 1      tensor-memory owner and single-thread MMA issuer (M = 128, N = q_tile*H pad 16)
 //   warps 2..5  epilogue: tcgen05.ld (lane = block), ReLU . w, head sum, coalesced stores
-// Up to four accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs
-// of the tiles after it; the producer fills the pipeline before the rest of the set-up.  Every
-// wait is bounded (SFA_DEV_TIMEOUT) and tensor memory is always released.
+// Two accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs of
+// tile t + 1; for narrow tiles the producer fills the pipeline before the rest of the set-up.
+// Every wait is bounded (SFA_DEV_TIMEOUT) and tensor memory is always released.
 #include <mutex>
 
 #include "sfa_common.cuh"
@@ -30,7 +30,6 @@ namespace {
 constexpr int kBM = 128;               // blocks per tile (MMA M)
 constexpr int kThreads = 192;          // 6 warps
 constexpr int kSlabBytes = kBM * 128;  // one pipeline stage
-constexpr int kMaxAcc = 4;             // accumulator buffers in tensor memory (at most)
 // The bounded mode's error bound per score: |s - a| <= e = kMargin * C_q * r_b (+ kAbs), with
 // C_q = sum_j |w_j| |q_j|_2 and r_b = |lo_b|_2 + 2^-14 |hi_b|_2 from the pooling pass.  The
 // exact difference of the two scores is at most C_q |lo_b|_2 (ReLU is 1-Lipschitz, the head
@@ -53,7 +52,7 @@ struct ScoreParams {
     int64_t score_stride;
     int64_t blk_cap;
     int64_t n_blk_max;
-    int n_q, q_tile, n_seq, cr, N, stages, tiles_per_cta, tmem_cols, n_acc;
+    int n_q, q_tile, n_seq, cr, N, stages, tiles_per_cta, tmem_cols;
 };
 
 template <int KP>
@@ -79,9 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x KB bf16, swizzled
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KB * 2);
     uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S,
-             *acc_empty = bars + 2 * S + kMaxAcc, *drain = bars + 2 * S + 2 * kMaxAcc;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 2 * kMaxAcc + 1);
-    const int NA = p.n_acc;   // accumulator buffers: the MMAs run up to NA tiles ahead
+             *acc_empty = bars + 2 * S + 2, *drain = bars + 2 * S + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_nblk = reinterpret_cast<int *>(tmem_slot + 2);  // [q_tile] visible blocks, -1 skip
     float *s_w = reinterpret_cast<float *>(s_nblk + 256);  // [q_tile * H]
@@ -97,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < NA; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
@@ -114,10 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();
     const int seq0 = p.q_seq[q0];
     const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
-    // The producer fills the pipeline before the rest of the set-up: its tile range needs only
-    // the visible block counts of the tile's queries (the same rule as s_nblk below).
+    // For narrow tiles the producer fills the pipeline before the rest of the set-up: its tile
+    // range needs only the visible block counts of the tile's queries (the rule of s_nblk).
     int primed = 0;
-    if (warp == 0) {
+    if (warp == 0 && N <= 32) {   // narrow (decode) tiles stream; wide ones measured no gain
         int nbw = 0;
         for (int qq = lane; qq < nq_tile; qq += 32) {
             const int s = p.q_seq[q0 + qq], pos = p.q_pos[q0 + qq];
@@ -233,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0, ld = 0;
             bool ok = true;
             for (int it = 0; it < my_tiles && ok && !*abort_flag; ++it) {
-                const int acc = it % NA;
-                if (!mbar_wait(&acc_empty[acc], ((it / NA) & 1) ^ 1, deadline)) {
+                const int acc = it & 1;
+                if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, deadline)) {
                     ok = false;
                     break;
                 }
@@ -266,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(drain, 0, deadline + kWaitLimitNs);
             } else if (issued > 0) {  // tensor memory may only be released once the MMAs are done
                 const int last = issued - 1;
-                mbar_wait(&acc_full[last % NA], (last / NA) & 1, deadline + kWaitLimitNs);
+                mbar_wait(&acc_full[last & 1], (last >> 1) & 1, deadline + kWaitLimitNs);
             }
         }
     } else {
@@ -275,12 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int ncols = nq_tile * H;
         for (int it = 0; it < my_tiles; ++it) {
-            const int acc = it % NA;
+            const int acc = it & 1;
             if (*abort_flag) break;
             const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
             // bounded mode: this block's bound factor, loaded before the accumulator wait
             const float rb = (HI && b < p.n_blk_max) ? __ldg(p.kbar_r + (int64_t)seq0 * p.kr_seq_stride + b) : 0.f;
-            if (!mbar_wait(&acc_full[acc], (it / NA) & 1, deadline)) {
+            if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, deadline)) {
                 set_status(p.status, SFA_DEV_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -340,15 +338,13 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
     // flight; wide ones (prefill) are tensor-bound: one CTA per SM with a deep pipeline.
     const int per_sm = p.N <= 32 ? 2 : 1;
     const size_t budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
-    const size_t misc = 1024 + 8 * (2 * 16 + 2 * kMaxAcc + 1) + 8 + 256 * 4 +
-                        (size_t)p.q_tile * (H + 1) * 4;
+    const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     if (budget < b_bytes + misc + kSlabBytes) return SFA_ERR_UNSUPPORTED;
     int stages = (int)((budget - b_bytes - misc) / kSlabBytes);
     if (stages > 16) stages = 16;
     p.stages = stages;
-    const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes +
-                        8 * (2 * stages + 2 * kMaxAcc + 1) + 8 + 256 * 4 +
-                        (size_t)p.q_tile * (H + 1) * 4;
+    const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes + 8 * (2 * stages + 5) + 8 +
+                        256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     static bool attr_set = false;
     if (!attr_set) {
         if (!allow_max_dynamic_smem(index_score_kernel<KP, H, HI>)) return SFA_ERR_CUDA;
@@ -421,10 +417,7 @@ int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const in
     p.n_seq = n_seq;
     p.cr = compress_ratio;
     p.N = ((q_tile * h_idx + 15) / 16) * 16;
-    // Narrow (decode) tiles: four accumulators keep the MMAs ahead of the epilogue; wide
-    // (prefill) tiles measured faster with two.
-    p.n_acc = p.N <= 32 ? kMaxAcc : 2;
-    p.tmem_cols = pow2_at_least(p.n_acc * p.N);
+    p.tmem_cols = pow2_at_least(2 * p.N);
 
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)KP, (cuuint64_t)(n_seq * blk_cap)};
