@@ -405,6 +405,8 @@ def main():
                     help="decode: exact scores + select instead of the bounded selection")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller runs for ncu captures)")
+    ap.add_argument("--depth", type=int, default=0,
+                    help="override the cache depth (smaller runs for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -414,6 +416,8 @@ def main():
     w = sfa.WORKLOADS[args.workload]
     if args.seqs:
         w = w.with_(n_seq=args.seqs, name=f"{w.name}[seqs={args.seqs}]")
+    if args.depth:
+        w = w.with_(depth=args.depth, name=f"{w.name}[depth={args.depth}]")
     if args.impl == "reference":
         if world > 1:
             import torch.distributed as dist
