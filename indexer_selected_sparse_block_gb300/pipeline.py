@@ -105,6 +105,23 @@ class SfaStep:
                                 self.cr, scale, self.O, lse=self.lse, workspace=self.attn_ws,
                                 dev_status=self.status, stream=stream)
 
+    @staticmethod
+    def graphed(fn, warmup: int = 2):
+        """fn() captured into a CUDA graph, after `warmup` runs on a side stream.  The entry
+        points launch on the current stream and never synchronise or allocate, so a step of
+        them -- with the caller's input copies and output read-back -- replays as one graph
+        launch (torch.cuda.CUDAGraph.replay()), free of per-call host overhead."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
     def run(self, X, K, V, Q, q_idx, w, q_seq, q_pos, scale: float, new_blocks=(0, 0),
             stream=None):
         """One step: pool the blocks completed by this step's tokens, score, select, attend."""

@@ -188,3 +188,35 @@ def test_stream_isolation(dev):
     torch.cuda.synchronize()
     same = [bool(torch.equal(O1[i], step.O[i])) for i in range(4)]
     assert same == [True, True, False, True]
+
+
+def test_graphed_step_matches_eager(dev):
+    """A step captured by SfaStep.graphed (host input copies, the library's launches, the
+    output read-back) replays to the eager step's results bit for bit, and a replay after the
+    pinned host inputs change computes on the new inputs."""
+    w = sfa.WORKLOADS["decode_32x131072"].with_(depth=8000, seed=5)   # bounded, cluster attend
+    case, step = _run(w, dev)
+    host_q = case["Q"].cpu().pin_memory()
+    host_qi = case["q_idx"].cpu().pin_memory()
+    out = torch.empty(step.O.shape, dtype=torch.float32).pin_memory()
+
+    def one():
+        case["Q"].copy_(host_q, non_blocking=True)
+        case["q_idx"].copy_(host_qi, non_blocking=True)
+        step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
+                 case["q_seq"], case["q_pos"], w.scale)
+        out.copy_(step.O, non_blocking=True)
+
+    graph = sfa.SfaStep.graphed(one)
+    for rnd in range(2):
+        if rnd:   # new inputs in the pinned buffers: the graph's copies pick them up
+            g = torch.Generator().manual_seed(99)
+            host_q.copy_(torch.randn(host_q.shape, generator=g).to(host_q.dtype))
+            host_qi.copy_(torch.randn(host_qi.shape, generator=g).to(host_qi.dtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        one()   # the same step, eager
+        torch.cuda.synchronize()
+        assert torch.equal(got, out), rnd
+        assert sfa.sfa_read_device_status(step.status) == 0
