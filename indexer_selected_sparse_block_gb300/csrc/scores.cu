@@ -334,10 +334,12 @@ template <int KP, int H, bool HI>
 int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
            cudaStream_t stream) {
     const size_t b_bytes = (size_t)p.N * (HI ? KP / 2 : KP) * 2;
-    // Narrow B tiles (decode) are HBM-bound streams: two CTAs per SM keep more slabs in
-    // flight; wide ones (prefill) are tensor-bound: one CTA per SM with a deep pipeline.
-    const int per_sm = p.N <= 32 ? 2 : 1;
-    const size_t budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
+    // Narrow B tiles (decode) are HBM-bound streams: four CTAs per SM, three stages each,
+    // overlap four producer -> MMA -> epilogue chains (measured 6% faster than two CTAs of six
+    // stages, 10% faster than one of thirteen); wide ones (prefill) are tensor-bound: one CTA
+    // per SM with a deep pipeline.
+    const int per_sm = p.N <= 32 ? 4 : 1;
+    const size_t budget = per_sm == 4 ? 55 * 1024 : 220 * 1024;
     const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     if (budget < b_bytes + misc + kSlabBytes) return SFA_ERR_UNSUPPORTED;
     int stages = (int)((budget - b_bytes - misc) / kSlabBytes);
