@@ -628,7 +628,9 @@ __device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int
 //   4. the leader selects the top k of the list.
 // Lists longer than 4096 go through global memory (select_global_list).
 constexpr int kCl = 4;                                       // CTAs per row
-constexpr int kClRounds = (kChunk / kCl) / (4 * kThreads);   // 3 rounds of groups of four
+constexpr int kClRounds = (kChunk / kCl + 4 * kThreads - 1) / (4 * kThreads);   // 3 rounds
+static_assert(kClRounds * 4 * kThreads >= kChunk / kCl, "a quarter of the longest row fits the rounds");
+static_assert(4 * kClRounds <= 32, "one candidate bit per element in a 32-bit mask");
 
 struct RefineParams {
     const float *lower, *upper;

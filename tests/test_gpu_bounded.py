@@ -187,3 +187,37 @@ def test_bounded_step_rejects_long_rows(dev):
                     dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                     compress_ratio=w.compress_ratio, indexer_top_k=w.indexer_top_k,
                     n_blk_max=w.n_tok // w.compress_ratio, q_group=1, bounded=True, device=dev)
+
+
+def test_refine_longest_rows(dev):
+    """Rows of up to the 36864-block limit: each CTA of the cluster takes three rounds of
+    groups, and blocks past 32768 are candidates like any other."""
+    cr, d_idx, h_idx, top_k = 4, 128, 8, 512
+    pos = [147455, 144003, 131075, 40000]   # B = 36864, 36001, 32769, 10000
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 777, 1, 147456, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), 36864
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Xh, qh, wh = np32(X), np32(qi), np32(w)
+    got, gn = np32(blk), np32(n_sel)
+    n_exact = 0
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        sc = oracle.index_scores(qh[i], wh[i], oracle.pool(Xh[0], B, cr))
+        ok, exact = check_selection(got[i], int(gn[i]), sc, top_k)
+        assert ok, (i, p)
+        n_exact += exact
+        # the selection reaches past block 32768 when the best blocks are there
+        top = np.argsort(-sc, kind="stable")[:top_k]
+        if exact and (top >= 32768).any():
+            assert (got[i] >= 32768).any()
+    assert n_exact >= len(pos) - 1
