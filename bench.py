@@ -383,6 +383,20 @@ def time_oracle(w, sample, n_q, n_threads, min_seconds=3.0, max_reps=50):
     return n_q * reps / el, out["threads"], el
 
 
+def job_throughput(local_ms_total, local_units, steps, dist=None, device="cpu"):
+    """Whole-job throughput of weak-scaled replicas.  The job takes as long as its slowest
+    rank (the timed totals reduce to their maximum) and processes the units of every rank
+    (they sum).  Returns (units per second, milliseconds per step).  `dist` is
+    torch.distributed when several ranks run (NCCL wants `device` on the GPU, gloo the CPU)."""
+    ms = torch.tensor([float(local_ms_total)], dtype=torch.float64, device=device)
+    units = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+        dist.all_reduce(units, op=dist.ReduceOp.SUM)
+    ms_per_step = float(ms.item()) / steps
+    return float(units.item()) / (ms_per_step / 1000.0), ms_per_step
+
+
 def run_reference(args, w, rank, world):
     """--impl reference: the CPU oracle on the host cores, on bounded samples of w."""
     if rank != 0:
@@ -473,16 +487,10 @@ def main():
         # per-stage split comes from a separate, shorter pass with events between stages
         step_ms, _ = measure(wb, args.steps, args.warmup, flush, per_stage=False, clk=clk)
         _, stage_ms = measure(wb, max(3, args.steps // 2), 3, flush, per_stage=True)
-        total_ms = sum(step_ms)
-        if dist is not None:
-            t = torch.tensor([total_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
+        value, ms_per_step = job_throughput(sum(step_ms), w.n_q, args.steps, dist, dev)
     torch.cuda.synchronize()
     status = B.sfa_read_device_status(wb.step.status)
-    ms_per_step = total_ms / args.steps
     n_q_total = w.n_q * world
-    value = n_q_total / (ms_per_step / 1000.0)
 
     n_sel = wb.step.n_sel.cpu()
     tail = [(int(p) + 1) % w.compress_ratio for p in wb.case["q_pos"].cpu()]
