@@ -65,7 +65,8 @@ class Workload:
 # The synthetic workloads: three decode shapes (1 sequence at depth 4096; 32 sequences at
 # depth 131072; 4 sequences of two KV heads at depth 1048576) and two prefill shapes
 # (512 tokens at depth 8192, also at depth 1000 where every block fits the budget; 2048
-# tokens at depth 131072, the pp2048@d131072 shape).
+# tokens at depth 131072, the pp2048@d131072 shape); and token-level selection
+# (compress_ratio 1) at 32 sequences of depth 32768.
 WORKLOADS = {
     "decode_1x4096": Workload("decode_1x4096", "decode", 1, 1, 4096, 16, 1, 576, 512, True,
                               4, 64, 4, 256, seed=1000),
@@ -79,6 +80,10 @@ WORKLOADS = {
                               True, 8, 128, 4, 512, seed=1003),
     "decode_4x1048576": Workload("decode_4x1048576", "decode", 4, 1, 1048576, 16, 2, 512, 512,
                                  False, 8, 128, 8, 256, seed=1004),
+    # token-level selection (compress_ratio 1: every token its own block, a budget of 2048
+    # tokens), at 32 sequences of depth 32768
+    "decode_cr1_32x32768": Workload("decode_cr1_32x32768", "decode", 32, 1, 32768, 16, 1, 576,
+                                    512, True, 16, 128, 1, 2048, seed=1005),
 }
 
 _ROLE = {"K": 1, "V": 2, "X": 3, "Q": 4, "QI": 5, "W": 6}

@@ -169,6 +169,16 @@ def test_pp2048_131072_sampled(dev):
     _check_sampled(w, case, step, [0, 1, 511, 1024, 1500, 2046, 2047])
 
 
+def test_decode_cr1_32x32768_sampled(dev):
+    """Token-level selection: compress_ratio 1 and a budget of 2048 single-token blocks
+    (pooling is the identity, no tail, the top-k takes its register path since k exceeds the
+    CTA's threads; decode takes the bounded selection)."""
+    w = sfa.WORKLOADS["decode_cr1_32x32768"]
+    case, step = _run(w, dev)
+    assert step.bounded
+    _check_sampled(w, case, step, [0, 17, 31])
+
+
 def test_decode_4x1048576_sampled(dev):
     w = sfa.WORKLOADS["decode_4x1048576"]
     case, step = _run(w, dev)
