@@ -51,6 +51,8 @@ def load(path: str | None = None):
         return _lib
     lib = ctypes.CDLL(path or build())
     lib.sfa_oracle_pool.argtypes = [_f32p, _i64, _int, _int, _f64p]
+    lib.sfa_oracle_key_transform.argtypes = [_f64p, _i64, _int, _int, _int, _f32p, _f32p,
+                                             ctypes.c_double, _int, ctypes.c_double, _int, _i64]
     lib.sfa_oracle_index_scores.argtypes = [_f32p, _f32p, _int, _int, _f64p, _i64, _f64p]
     lib.sfa_oracle_select.argtypes = [_f64p, _i64, _int, _i32p]
     lib.sfa_oracle_select.restype = _int
@@ -76,6 +78,21 @@ def pool(X, n_blk: int, cr: int, lib=None) -> np.ndarray:
     assert n_blk * cr <= X.shape[0]
     out = np.zeros((n_blk, X.shape[1]), np.float64)
     lib.sfa_oracle_pool(X, n_blk, X.shape[1], cr, out)
+    return out
+
+
+def key_transform(kbar, cr: int, *, norm: int = 0, gamma=None, beta=None, eps: float = 1e-6,
+                  n_rot: int = 0, rope_base: float = 10000.0, rope_neox: bool = True,
+                  pos_offset: int = 0, lib=None) -> np.ndarray:
+    """The pooled keys kbar[n_blk][d_idx] after the norm (0 none, 1 RMS, 2 layer) and the
+    rotation of their first n_rot dims at positions b*cr + pos_offset (a new array)."""
+    lib = lib or load()
+    out = np.array(kbar, dtype=np.float64, order="C", copy=True)
+    d = out.shape[1]
+    g = _f32(np.ones(d) if gamma is None else gamma)
+    bt = _f32(np.zeros(d) if beta is None else beta)
+    lib.sfa_oracle_key_transform(out, out.shape[0], d, cr, norm, g, bt, eps, n_rot, rope_base,
+                                 int(rope_neox), pos_offset)
     return out
 
 

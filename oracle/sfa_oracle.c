@@ -48,6 +48,49 @@ void sfa_oracle_pool(const float *X, int64_t n_blk, int d_idx, int cr, double *k
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Step 1b -- the norm and the rotation of the pooled keys [QSA, indexer key cache paragraph:
+ * the cache holds raw keys because pooling precedes the norm and the rotation; the indexer
+ * ropes with the main attention's rotary width].  In place on kbar[n_blk][d_idx]; the pages
+ * name neither the norm nor the rotary pairing nor a block's position, so each is a choice
+ * (the readings are listed in the design notes):
+ *   norm_kind 0: none;  1: RMS norm   y_d = x_d / sqrt(mean_e x_e^2 + eps) * gamma_d;
+ *              2: layer norm         y_d = (x_d - mu) / sqrt(mean_e (x_e - mu)^2 + eps) * gamma_d + beta_d
+ *   rotation of the first n_rot dims at position p = b * cr + pos_offset, pair j
+ *   (0 <= j < n_rot/2) turned by theta_j = p * rope_base^(-2j / n_rot):
+ *     rope_neox 1: the pair (j, j + n_rot/2);  0: the pair (2j, 2j + 1)
+ *     (x_a, x_b) -> (x_a cos theta - x_b sin theta, x_a sin theta + x_b cos theta)        */
+void sfa_oracle_key_transform(double *kbar, int64_t n_blk, int d_idx, int cr, int norm_kind,
+                              const float *gamma, const float *beta, double eps, int n_rot,
+                              double rope_base, int rope_neox, int64_t pos_offset)
+{
+    for (int64_t b = 0; b < n_blk; ++b) {
+        double *x = kbar + b * d_idx;
+        if (norm_kind == 1) {
+            double ss = 0.0;
+            for (int d = 0; d < d_idx; ++d) ss += x[d] * x[d];
+            const double r = sqrt(ss / d_idx + eps);
+            for (int d = 0; d < d_idx; ++d) x[d] = x[d] / r * (double)gamma[d];
+        } else if (norm_kind == 2) {
+            double mu = 0.0;
+            for (int d = 0; d < d_idx; ++d) mu += x[d];
+            mu /= d_idx;
+            double var = 0.0;
+            for (int d = 0; d < d_idx; ++d) var += (x[d] - mu) * (x[d] - mu);
+            const double r = sqrt(var / d_idx + eps);
+            for (int d = 0; d < d_idx; ++d) x[d] = (x[d] - mu) / r * (double)gamma[d] + (double)beta[d];
+        }
+        const double p = (double)(b * cr + pos_offset);
+        for (int j = 0; j < n_rot / 2; ++j) {
+            const double theta = p * pow(rope_base, -2.0 * j / n_rot);
+            const int ia = rope_neox ? j : 2 * j, ib = rope_neox ? j + n_rot / 2 : 2 * j + 1;
+            const double xa = x[ia], xb = x[ib];
+            x[ia] = xa * cos(theta) - xb * sin(theta);
+            x[ib] = xa * sin(theta) + xb * cos(theta);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Step 2 -- indexer score of every complete block [QSA, ReLU paragraph].
  *   s_b = sum_j w_j * max(0, q_j . kbar_b)
  * q_idx is [h_idx][d_idx] for one query token, w is [h_idx].                              */

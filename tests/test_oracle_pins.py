@@ -305,8 +305,72 @@ def pin_pipeline(lib):
         assert same == (c["q_seq"][i] == 0)
 
 
+# ------------------------------------------------------------------------ key transform
+def pin_key_transform(lib):
+    kt = lambda k, cr, **kw: oracle.key_transform(k, cr, lib=lib, **kw)  # noqa: E731
+    rng = _rng(31)
+    K = rng.standard_normal((6, 16))
+    # nothing to do: the identity
+    assert np.array_equal(kt(K, 4), K)
+    # a rotation at position 0 (block 0, no offset) is the identity
+    for neox in (True, False):
+        assert np.allclose(kt(K[:1], 4, n_rot=16, rope_neox=neox), K[:1], rtol=0, atol=1e-15)
+    # rotations preserve every row's length
+    R = kt(K, 3, n_rot=16, pos_offset=11)
+    np.testing.assert_allclose(np.linalg.norm(R, axis=1), np.linalg.norm(K, axis=1), rtol=1e-13)
+    # dot products of rotated vectors depend only on their position difference
+    q, k = rng.standard_normal(16), rng.standard_normal(16)
+    rows = np.zeros((13, 16))
+    rows[5], rows[2], rows[12], rows[9] = q, k, q, k
+    for neox in (True, False):
+        Rr = kt(rows, 1, n_rot=16, rope_base=50.0, rope_neox=neox)
+        assert abs(Rr[5] @ Rr[2] - Rr[12] @ Rr[9]) < 1e-12
+        same = np.zeros((4, 16))
+        same[3] = q
+        a = kt(same, 1, n_rot=16, rope_neox=neox)[3]
+        same[3] = k
+        b = kt(same, 1, n_rot=16, rope_neox=neox)[3]
+        assert abs(a @ b - q @ k) < 1e-12
+    # closed forms: block 1 at cr = 4 sits at position 4; pair 0 turns by 4 rad, pair 1 of
+    # n_rot = 4 by 4 / sqrt(base) rad
+    base = 100.0
+    e = np.zeros((2, 4))
+    e[1, 0] = 1.0                                   # dim 0: pair 0 in both pairings
+    r = kt(e, 4, n_rot=4, rope_base=base, rope_neox=True)[1]
+    np.testing.assert_allclose(r, [math.cos(4), 0, math.sin(4), 0], atol=1e-15)   # (0, 2)
+    r = kt(e, 4, n_rot=4, rope_base=base, rope_neox=False)[1]
+    np.testing.assert_allclose(r, [math.cos(4), math.sin(4), 0, 0], atol=1e-15)   # (0, 1)
+    e = np.zeros((2, 4))
+    e[1, 1] = 1.0                                   # dim 1: NeoX pair 1 (1, 3); adjacent pair 0
+    t1 = 4 / math.sqrt(base)
+    np.testing.assert_allclose(kt(e, 4, n_rot=4, rope_base=base, rope_neox=True)[1],
+                               [0, math.cos(t1), 0, math.sin(t1)], atol=1e-15)
+    np.testing.assert_allclose(kt(e, 4, n_rot=4, rope_base=base, rope_neox=False)[1],
+                               [-math.sin(4), math.cos(4), 0, 0], atol=1e-15)
+    # the norms: statistics of the result (eps = 0, unit gain)
+    y = kt(K, 4, norm=1, eps=0.0)
+    np.testing.assert_allclose((y ** 2).mean(1), 1.0, rtol=1e-13)
+    y = kt(K, 4, norm=2, eps=0.0)
+    np.testing.assert_allclose(y.mean(1), 0.0, atol=1e-13)
+    np.testing.assert_allclose((y ** 2).mean(1), 1.0, rtol=1e-13)
+    # a constant row: RMS norm gives gamma * sign, layer norm gives beta
+    g = rng.uniform(0.5, 2, 16).astype(np.float32)
+    bt = rng.standard_normal(16).astype(np.float32)
+    c = np.full((1, 16), -3.0)
+    np.testing.assert_allclose(kt(c, 1, norm=1, gamma=g, eps=0.0)[0], -g.astype(np.float64),
+                               rtol=1e-14)
+    np.testing.assert_allclose(kt(c, 1, norm=2, gamma=g, beta=bt, eps=1e-6)[0],
+                               bt.astype(np.float64), rtol=0, atol=0)
+    # the norm comes before the rotation (with a non-uniform gain the two do not commute)
+    both = kt(K, 2, norm=1, gamma=g, n_rot=16, pos_offset=3)
+    step = kt(kt(K, 2, norm=1, gamma=g), 2, n_rot=16, pos_offset=3)
+    np.testing.assert_allclose(both, step, rtol=1e-14)
+    rot_first = kt(kt(K, 2, n_rot=16, pos_offset=3), 2, norm=1, gamma=g)
+    assert not np.allclose(both, rot_first, rtol=1e-6)
+
+
 PINS = [pin_pool_closed_forms, pin_scores, pin_select, pin_token_expanded, pin_mask,
-        pin_attend, pin_pipeline]
+        pin_attend, pin_pipeline, pin_key_transform]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -333,6 +397,14 @@ MUTANTS = {
                              "const double e = exp(m - logit[t]);"),
     "v_from_wrong_offset": ("K + r * k_row_stride + (int64_t)g * dkq;\n            const double e",
                             "K + r * k_row_stride + (int64_t)g * dkq + 1;\n            const double e"),
+    "rope_sin_sign": ("x[ia] = xa * cos(theta) - xb * sin(theta);",
+                      "x[ia] = xa * cos(theta) + xb * sin(theta);"),
+    "rope_neox_partner": ("ib = rope_neox ? j + n_rot / 2 : 2 * j + 1;",
+                          "ib = rope_neox ? j + 1 : 2 * j + 1;"),
+    "rms_without_root": ("const double r = sqrt(ss / d_idx + eps);",
+                         "const double r = ss / d_idx + eps;"),
+    "position_ignores_cr": ("const double p = (double)(b * cr + pos_offset);",
+                            "const double p = (double)(b + pos_offset);"),
 }
 
 
