@@ -89,6 +89,30 @@ int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_
                         sfa_stream_t stream);
 
 /*
+ * sfa_pool_index_keys_transformed -- sfa_pool_index_keys with the norm and the rotation the
+ * model applies to the pooled index key before scoring (QSA commit: the index-key cache holds
+ * raw keys because pooling precedes the norm and the rotation; the indexer ropes with the main
+ * attention's rotary width).  The pages name neither the norm nor the rotary pairing nor the
+ * position of a pooled block, so the caller chooses:
+ *   norm 0: none; 1: RMS norm, y = m / sqrt(mean(m^2) + eps) * gamma;
+ *        2: layer norm, y = (m - mean(m)) / sqrt(var(m) + eps) * gamma + beta
+ *        (over the d_idx dims of the pooled row m; gamma, beta: [d_idx] fp32 device arrays)
+ *   n_rot dims (even, <= d_idx; 0: no rotation) turned pairwise at position
+ *        p_b = b * compress_ratio + pos_offset, pair j by p_b * rope_base^(-2j / n_rot);
+ *        rope_neox 1: pairs (j, j + n_rot/2) (n_rot a multiple of 16); 0: pairs (2j, 2j + 1)
+ * The transformed key is what is split into hi + lo and what Kbar_r bounds.  Norm statistics
+ * are fp32; angles, sines and cosines double.
+ * Limits: those of sfa_pool_index_keys; d_idx in {32, 64, 128} when a transform is given.
+ */
+int sfa_pool_index_keys_transformed(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq,
+                                    int d_idx, int compress_ratio, int64_t blk_begin,
+                                    int64_t blk_end, int norm, const float *gamma,
+                                    const float *beta, float eps, int n_rot, float rope_base,
+                                    int rope_neox, int64_t pos_offset, void *Kbar,
+                                    int64_t kbar_seq_stride, float *Kbar_r, int64_t kr_seq_stride,
+                                    sfa_stream_t stream);
+
+/*
  * sfa_index_scores -- the indexer score of every complete block visible to each query: each
  * index head's dot product passes through a ReLU before the weighted sum over heads (QSA
  * commit, index comparison paragraph); a query is scored only against the blocks of its own

@@ -10,6 +10,7 @@ from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BA
                        sfa_attend_plan, sfa_attend_workspace_bytes, sfa_dense_attend,
                        sfa_gather_attend,
                        sfa_index_scores, sfa_index_scores_bounded, sfa_pool_index_keys,
+                       sfa_pool_index_keys_transformed,
                        sfa_read_device_status, sfa_topk_blocks, sfa_topk_blocks_refine,
                        sfa_topk_refine_workspace_bytes, sfa_topk_workspace_bytes)
 from .inputs import WORKLOADS, Workload, make_case

@@ -29,6 +29,9 @@ _vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, cty
 SIGNATURES = {
     "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp,
                                    _i64, _vp]),
+    "sfa_pool_index_keys_transformed": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64,
+                                               _int, _vp, _vp, _f32, _int, _f32, _int, _i64,
+                                               _vp, _i64, _vp, _i64, _vp]),
     "sfa_index_scores": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _i64,
                                 _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
@@ -123,6 +126,21 @@ def sfa_pool_index_keys(X, compress_ratio: int, blk_begin: int, blk_end: int, Kb
                                    _p(Kbar_r), Kbar_r.stride(0) if Kbar_r is not None else 0,
                                    _stream(stream))
     _check("sfa_pool_index_keys", rc)
+
+
+def sfa_pool_index_keys_transformed(X, compress_ratio: int, blk_begin: int, blk_end: int, Kbar,
+                                    Kbar_r=None, *, norm: int = 0, gamma=None, beta=None,
+                                    eps: float = 1e-6, n_rot: int = 0, rope_base: float = 10000.0,
+                                    rope_neox: bool = True, pos_offset: int = 0, stream=None):
+    """sfa_pool_index_keys with the pooled key normalised (norm 0 none, 1 RMS, 2 layer; gamma,
+    beta [d_idx] fp32 on the device) and its first n_rot dims rotated at b*cr + pos_offset."""
+    n_seq, _, d_idx = X.shape
+    rc = lib().sfa_pool_index_keys_transformed(
+        _p(X), _dtype_code(X), X.stride(0), n_seq, d_idx, compress_ratio, blk_begin, blk_end,
+        norm, _p(gamma), _p(beta), eps, n_rot, rope_base, int(rope_neox), pos_offset, _p(Kbar),
+        Kbar.stride(0), _p(Kbar_r), Kbar_r.stride(0) if Kbar_r is not None else 0,
+        _stream(stream))
+    _check("sfa_pool_index_keys_transformed", rc)
 
 
 def sfa_index_scores(q_idx, w, q_seq, q_pos, Kbar, compress_ratio: int, n_blk_max: int, scores,

@@ -11,6 +11,14 @@
 //   r_b = (|lo_b|_2 + 2^-14 |hi_b|_2) * (1 + 2^-16)
 // from the stored bf16 halves (the chunks of a row are consecutive lanes: a shuffle sum); the
 // factor (1 + 2^-16) covers the fp32 rounding of the two norms (128 squares: < 2^-17).
+// Optionally the pooled key is normalised and rotated before it is split (the indexer key
+// cache holds raw keys because pooling precedes the norm and the rotation; the indexer ropes
+// with the main attention's rotary width -- llama.cpp commit "model: add Qwen3.8-Flash-Next
+// (qwen4exp)", indexer key cache paragraph): RMS or layer norm over the row (statistics by a
+// shuffle sum over the row's lanes, fp32), then the first n_rot dims turned pairwise at the
+// block's position b*cr + pos_offset, NeoX pairs (j, j + n_rot/2) through a shuffle with the
+// partner lane, or adjacent pairs (2j, 2j + 1) within a thread.  Angles and their sines and
+// cosines are computed in double: at positions near 1e6 an fp32 angle is off by ~0.06 rad.
 // Bytes per block: cr * d_idx * sizeof(X) read + 4 * d_idx (+ 4) written.
 #include "sfa_common.cuh"
 
@@ -41,13 +49,29 @@ struct Vec8<float> {
     }
 };
 
+struct KeyTransform {
+    int norm;                    // 0 none, 1 RMS, 2 layer
+    const float *gamma, *beta;   // [d_idx] gain, [d_idx] bias (layer norm)
+    float eps;
+    int n_rot;                   // rotated dims (0: none)
+    double log2_base;            // log2 of the rotary base
+    int neox;                    // 1: pairs (j, j + n_rot/2); 0: (2j, 2j + 1)
+    int64_t pos_offset;          // block b sits at position b * cr + pos_offset
+};
+
+// Sum over the `chunks` lanes that hold one row (aligned groups; chunks divides 32).
+__device__ __forceinline__ float row_sum(float v, int chunks) {
+    for (int o = 1; o < chunks; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
 // grid: (ceil(rows * chunks / 256), n_seq); one thread per (pooled row, 8-element chunk).
 template <typename T>
 __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int64_t x_seq_stride,
                                                    int d_idx, int cr, int64_t blk_begin,
                                                    int64_t n_rows, __nv_bfloat16 *__restrict__ Kbar,
                                                    int64_t kbar_seq_stride, float *__restrict__ Kr,
-                                                   int64_t kr_seq_stride) {
+                                                   int64_t kr_seq_stride, const KeyTransform tf) {
     pdl_wait();
     pdl_trigger();
     const int chunks = d_idx >> 3;
@@ -56,7 +80,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
     const int64_t b = blk_begin + (valid ? gid / chunks : 0);
     const int c = (int)(gid % chunks);
     const int64_t seq = blockIdx.y;
-    float lo2 = 0.f, hi2 = 0.f;
+    float mv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // this chunk of the pooled row
     if (valid) {
         const T *src = X + seq * x_seq_stride + b * cr * d_idx + c * 8;
         float sum[8];
@@ -68,10 +92,69 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
             for (int i = 0; i < 8; ++i) sum[i] += v[i];
         }
         const float rcr = (float)cr;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mv[i] = __fdiv_rn(sum[i], rcr);
+    }
+    if (tf.norm) {   // uniform: every lane takes part in the row sums
+        float mu = 0.f;
+        if (tf.norm == 2) {
+            float s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s1 += mv[i];
+            mu = __fdiv_rn(row_sum(s1, chunks), (float)d_idx);
+        }
+        float s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s2 = fmaf(mv[i] - mu, mv[i] - mu, s2);
+        const float r = __fsqrt_rn(__fdiv_rn(row_sum(s2, chunks), (float)d_idx) + tf.eps);
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = c * 8 + i;
+                const float y = __fdiv_rn(mv[i] - mu, r) * __ldg(tf.gamma + d);
+                mv[i] = tf.norm == 2 ? y + __ldg(tf.beta + d) : y;
+            }
+        }
+    }
+    if (tf.n_rot) {
+        const double pos = (double)(b * cr + tf.pos_offset);
+        const int d0 = c * 8;
+        if (tf.neox) {   // pairs (j, j + half): whole chunks, the partner half/8 lanes away
+            const int half = tf.n_rot / 2;
+            const int lane = threadIdx.x & 31;
+            const int src_lane = d0 < half ? lane + half / 8 : (d0 < tf.n_rot ? lane - half / 8 : lane);
+            float pv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pv[i] = __shfl_sync(0xFFFFFFFFu, mv[i], src_lane);
+            if (valid && d0 < tf.n_rot) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d = d0 + i, j = d < half ? d : d - half;
+                    double sn, cs;
+                    sincos(pos * exp2(-2.0 * j / tf.n_rot * tf.log2_base), &sn, &cs);
+                    const float fc = (float)cs, fs = (float)sn;
+                    mv[i] = d < half ? fmaf(mv[i], fc, -pv[i] * fs)    // x_j cos - x_{j+half} sin
+                                     : fmaf(pv[i], fs, mv[i] * fc);   // x_j sin + x_{j+half} cos
+                }
+            }
+        } else if (valid && d0 < tf.n_rot) {   // pairs (2j, 2j + 1) inside the chunk
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const int j = (d0 + i) / 2;
+                double sn, cs;
+                sincos(pos * exp2(-2.0 * j / tf.n_rot * tf.log2_base), &sn, &cs);
+                const float fc = (float)cs, fs = (float)sn, a = mv[i], bb = mv[i + 1];
+                mv[i] = fmaf(a, fc, -bb * fs);
+                mv[i + 1] = fmaf(a, fs, bb * fc);
+            }
+        }
+    }
+    float lo2 = 0.f, hi2 = 0.f;
+    if (valid) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float m0 = __fdiv_rn(sum[2 * i], rcr), m1 = __fdiv_rn(sum[2 * i + 1], rcr);
+            const float m0 = mv[2 * i], m1 = mv[2 * i + 1];
             const __nv_bfloat16 h0 = __float2bfloat16_rn(m0), h1 = __float2bfloat16_rn(m1);
             const __nv_bfloat16 l0 = __float2bfloat16_rn(m0 - __bfloat162float(h0));
             const __nv_bfloat16 l1 = __float2bfloat16_rn(m1 - __bfloat162float(h1));
@@ -100,11 +183,13 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
 }  // namespace
 }  // namespace sfa
 
-extern "C" int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq,
-                                   int d_idx, int compress_ratio, int64_t blk_begin,
-                                   int64_t blk_end, void *Kbar, int64_t kbar_seq_stride,
-                                   float *Kbar_r, int64_t kr_seq_stride, sfa_stream_t stream) {
-    using namespace sfa;
+namespace sfa {
+namespace {
+
+int run_pool(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq, int d_idx,
+             int compress_ratio, int64_t blk_begin, int64_t blk_end, void *Kbar,
+             int64_t kbar_seq_stride, float *Kbar_r, int64_t kr_seq_stride,
+             const KeyTransform &tf, cudaStream_t st) {
     if (!X || !Kbar || n_seq < 1 || compress_ratio < 1 || compress_ratio > 64) return SFA_ERR_INVALID_ARG;
     if (x_dtype != SFA_BF16 && x_dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
     if (d_idx != 32 && d_idx != 64 && d_idx != 96 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
@@ -112,7 +197,8 @@ extern "C" int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_str
     if (!aligned16(X) || !aligned16(Kbar)) return SFA_ERR_INVALID_ARG;
     if (x_seq_stride < blk_end * compress_ratio * d_idx) return SFA_ERR_INVALID_ARG;
     if (kbar_seq_stride < blk_end * 2 * d_idx || kbar_seq_stride % 8 != 0) return SFA_ERR_INVALID_ARG;
-    if (Kbar_r && d_idx == 96) return SFA_ERR_UNSUPPORTED;   // a row's chunks must tile a warp
+    // the row statistics, the NeoX partner and the bound factors work on whole-warp lane groups
+    if ((Kbar_r || tf.norm || tf.n_rot) && d_idx == 96) return SFA_ERR_UNSUPPORTED;
     if (Kbar_r && kr_seq_stride < blk_end) return SFA_ERR_INVALID_ARG;
     const size_t esz = x_dtype == SFA_BF16 ? 2 : 4;
     if ((x_seq_stride * esz) % 16 != 0) return SFA_ERR_INVALID_ARG;
@@ -123,20 +209,61 @@ extern "C" int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_str
     if (nblk > 0x7FFFFFFF || n_seq > 65535) return SFA_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)nblk, (unsigned)n_seq);
     auto *out = reinterpret_cast<__nv_bfloat16 *>(Kbar);
-    const cudaStream_t st = (cudaStream_t)stream;
     const cudaError_t e =
         x_dtype == SFA_BF16
             ? launch_pdl(pool_kernel<__nv_bfloat16>, grid, dim3(256), 0, st,
                          reinterpret_cast<const __nv_bfloat16 *>(X), x_seq_stride, d_idx,
                          compress_ratio, blk_begin, n_rows, out, kbar_seq_stride, Kbar_r,
-                         kr_seq_stride)
+                         kr_seq_stride, tf)
             : launch_pdl(pool_kernel<float>, grid, dim3(256), 0, st,
                          reinterpret_cast<const float *>(X), x_seq_stride, d_idx,
                          compress_ratio, blk_begin, n_rows, out, kbar_seq_stride, Kbar_r,
-                         kr_seq_stride);
+                         kr_seq_stride, tf);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
     }
     return SFA_OK;
+}
+
+}  // namespace
+}  // namespace sfa
+
+extern "C" int sfa_pool_index_keys(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq,
+                                   int d_idx, int compress_ratio, int64_t blk_begin,
+                                   int64_t blk_end, void *Kbar, int64_t kbar_seq_stride,
+                                   float *Kbar_r, int64_t kr_seq_stride, sfa_stream_t stream) {
+    const sfa::KeyTransform none{};
+    return sfa::run_pool(X, x_dtype, x_seq_stride, n_seq, d_idx, compress_ratio, blk_begin,
+                         blk_end, Kbar, kbar_seq_stride, Kbar_r, kr_seq_stride, none,
+                         (cudaStream_t)stream);
+}
+
+extern "C" int sfa_pool_index_keys_transformed(const void *X, int x_dtype, int64_t x_seq_stride,
+                                               int n_seq, int d_idx, int compress_ratio,
+                                               int64_t blk_begin, int64_t blk_end, int norm,
+                                               const float *gamma, const float *beta, float eps,
+                                               int n_rot, float rope_base, int rope_neox,
+                                               int64_t pos_offset, void *Kbar,
+                                               int64_t kbar_seq_stride, float *Kbar_r,
+                                               int64_t kr_seq_stride, sfa_stream_t stream) {
+    using namespace sfa;
+    if (norm < 0 || norm > 2) return SFA_ERR_INVALID_ARG;
+    if (norm >= 1 && !gamma) return SFA_ERR_INVALID_ARG;
+    if (norm == 2 && !beta) return SFA_ERR_INVALID_ARG;
+    if (norm && !(eps >= 0.f && isfinite(eps))) return SFA_ERR_INVALID_ARG;
+    if (n_rot < 0 || n_rot % 2 != 0 || n_rot > d_idx) return SFA_ERR_INVALID_ARG;
+    if (n_rot && rope_neox && n_rot % 16 != 0) return SFA_ERR_UNSUPPORTED;   // whole-chunk pairs
+    if (n_rot && !(rope_base > 0.f && isfinite(rope_base))) return SFA_ERR_INVALID_ARG;
+    KeyTransform tf{};
+    tf.norm = norm;
+    tf.gamma = gamma;
+    tf.beta = beta;
+    tf.eps = eps;
+    tf.n_rot = n_rot;
+    tf.log2_base = n_rot ? log2((double)rope_base) : 0.0;
+    tf.neox = rope_neox ? 1 : 0;
+    tf.pos_offset = pos_offset;
+    return run_pool(X, x_dtype, x_seq_stride, n_seq, d_idx, compress_ratio, blk_begin, blk_end,
+                    Kbar, kbar_seq_stride, Kbar_r, kr_seq_stride, tf, (cudaStream_t)stream);
 }

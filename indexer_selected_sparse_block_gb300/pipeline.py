@@ -23,7 +23,8 @@ from . import _binding as B
 class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
-                 n_blk_max: int, q_group: int = 1, bounded=None, device="cuda"):
+                 n_blk_max: int, q_group: int = 1, bounded=None, key_transform=None,
+                 device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -33,6 +34,9 @@ class SfaStep:
         self.Kbar = torch.zeros(B.kbar_shape(n_seq, self.blk_cap, d_idx), dtype=torch.bfloat16,
                                 device=dev)
         self.dense = n_blk_max <= indexer_top_k
+        # the norm and rotation of pooled index keys (keyword arguments of
+        # sfa_pool_index_keys_transformed), or None: raw pooled keys
+        self.key_transform = dict(key_transform) if key_transform else None
         # The bounded selection (hi-only scores + exact rescoring of the blocks the bounds
         # cannot rule out) halves the pooled-key bytes of decode-like steps, where each query
         # streams its sequence's pooled keys; prefill tiles share those reads and take the
@@ -66,8 +70,12 @@ class SfaStep:
 
     def pool(self, X, blk_begin: int, blk_end: int, stream=None):
         if blk_end > blk_begin:
-            B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, self.Kbar_r,
-                                  stream=stream)
+            if self.key_transform:
+                B.sfa_pool_index_keys_transformed(X, self.cr, blk_begin, blk_end, self.Kbar,
+                                                  self.Kbar_r, stream=stream, **self.key_transform)
+            else:
+                B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, self.Kbar_r,
+                                      stream=stream)
 
     def score(self, q_idx, w, q_seq, q_pos, stream=None):
         if self.bounded:

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import TOL_BF16, TOL_F32, np32, row_rel_err
+from gpu_util import TOL_BF16, TOL_F32, check_selection, np32, row_rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -309,3 +309,77 @@ def test_attend_flags_bad_block_lists(dev):
         msk = oracle.mask(99, cr, np.array(valid, np.int32), len(valid))
         ref, _ = oracle.attend(Qn[i], Kn[0], None, msk, 0.125, h_kv, dv=dv)
         assert row_rel_err(On[i], ref).max() < TOL_BF16
+
+
+# ---------------------------------------------------------------------- key transform
+@pytest.mark.parametrize("norm", [0, 1, 2])
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("d_idx,n_rot", [(128, 64), (64, 64), (32, 16)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_pool_transform_matches_oracle(dev, norm, neox, d_idx, n_rot, dtype):
+    """Pooled keys normalised and rotated on the GPU (hi + lo) match the fp64 oracle, at block
+    positions past 1e5 where only double-precision angles keep the rotation exact enough."""
+    g = torch.Generator().manual_seed(norm * 10 + d_idx + int(neox))
+    cr, n_seq, n_tok, b0 = 4, 2, 4 * 30000, 29500
+    blk_cap = n_tok // cr
+    X = (torch.randn((n_seq, n_tok, d_idx), generator=g) * 3 + 0.5).to(dtype).to(dev)
+    gamma = (torch.rand(d_idx, generator=g) + 0.5).to(dev)
+    beta = torch.randn(d_idx, generator=g).to(dev)
+    Kbar = torch.zeros(sfa.kbar_shape(n_seq, blk_cap, d_idx), dtype=torch.bfloat16, device=dev)
+    Kr = torch.zeros((n_seq, blk_cap), device=dev)
+    tf = dict(norm=norm, gamma=gamma if norm else None, beta=beta if norm == 2 else None,
+              eps=1e-5, n_rot=n_rot, rope_base=10000.0, rope_neox=neox, pos_offset=3)
+    sfa.sfa_pool_index_keys_transformed(X, cr, b0, blk_cap, Kbar, Kr, **tf)
+    torch.cuda.synchronize()
+    kb = Kbar.float().cpu().double().numpy()
+    got = kb[..., :d_idx] + kb[..., d_idx:]
+    Xh = np32(X)
+    for s in range(n_seq):
+        pooled = oracle.pool(Xh[s], blk_cap, cr)
+        ref = oracle.key_transform(pooled, cr, norm=norm, gamma=np32(gamma), beta=np32(beta),
+                                   eps=1e-5, n_rot=n_rot, rope_base=10000.0, rope_neox=neox,
+                                   pos_offset=3)[b0:]
+        err = np.abs(got[s, b0:] - ref).max(axis=1) / np.abs(ref).max(axis=1)
+        assert err.max() < 2e-5, (s, err.max())
+        assert np.all(got[s, :b0] == 0)                       # rows outside the range untouched
+        hi, lo = kb[s, b0:, :d_idx], kb[s, b0:, d_idx:]
+        bound = np.sqrt((lo ** 2).sum(1)) + 2.0 ** -14 * np.sqrt((hi ** 2).sum(1))
+        assert np.all(np32(Kr)[s, b0:] >= bound)
+
+
+def test_step_with_key_transform_matches_oracle(dev):
+    """A decode step whose pooled index keys are RMS-normalised and rotated: its selections
+    follow the agreement rule against the oracle's selection on the transformed keys, and
+    its outputs match the oracle attending the same cells."""
+    w = sfa.WORKLOADS["decode_32x131072"].with_(n_seq=4, depth=40000, seed=21)
+    case = sfa.make_case(w, device=dev)
+    g = torch.Generator().manual_seed(4)
+    gamma = (torch.rand(w.d_idx, generator=g) + 0.5).to(dev)
+    tf = dict(norm=1, gamma=gamma, eps=1e-6, n_rot=64, rope_base=10000.0, rope_neox=True,
+              pos_offset=0)
+    n_blk_max = w.n_tok // w.compress_ratio
+    step = sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
+                       dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
+                       compress_ratio=w.compress_ratio, indexer_top_k=w.indexer_top_k,
+                       n_blk_max=n_blk_max, key_transform=tf, device=dev)
+    step.pool(case["X"], 0, n_blk_max)
+    step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
+             case["q_seq"], case["q_pos"], w.scale)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(step.status) == 0
+    c = {k: np32(v) for k, v in case.items() if v is not None}
+    got_sel, got_n, O = np32(step.blk_idx), np32(step.n_sel), np32(step.O)
+    cr, n_exact = w.compress_ratio, 0
+    for i in range(w.n_q):
+        s, p = int(c["q_seq"][i]), int(c["q_pos"][i])
+        B = (p + 1) // cr
+        kbar = oracle.key_transform(oracle.pool(c["X"][s], B, cr), cr, norm=1, gamma=np32(gamma),
+                                    eps=1e-6, n_rot=64, rope_base=10000.0, rope_neox=True)
+        sc = oracle.index_scores(c["q_idx"][i], c["w"][i], kbar)
+        ok, exact = check_selection(got_sel[i], int(got_n[i]), sc, w.indexer_top_k)
+        assert ok, i
+        n_exact += exact
+        msk = oracle.mask(p, cr, got_sel[i], int(got_n[i]))
+        ref, _ = oracle.attend(c["Q"][i], c["K"][s], None, msk, w.scale, w.h_kv, dv=w.dv)
+        assert row_rel_err(O[i], ref).max() < TOL_BF16, i
+    assert n_exact >= w.n_q - 1
