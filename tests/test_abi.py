@@ -56,6 +56,34 @@ def test_pool_rejects_bad_arguments(L):
     assert f(FAKE, 0, 1024, 1, 64, 4, 0, 0, FAKE, 1024, None, 0, None) == 0          # empty: no work
 
 
+def test_pool_transform_rejects_bad_arguments(L):
+    f = L.sfa_pool_index_keys_transformed
+    F = ctypes.c_float
+    #     X     dt  stride n_seq d   cr b0 b1 norm gamma beta eps      n_rot base      neox off
+    ok = [FAKE, 0, 1024, 1, 64, 4, 0, 4, 1, FAKE, None, F(1e-6), 32, F(1e4), 1, 0,
+          FAKE, 1024, None, 0, None]
+    bad = list(ok); bad[8] = 3
+    assert f(*bad) == 1                                                    # norm kind
+    bad = list(ok); bad[9] = None
+    assert f(*bad) == 1                                                    # RMS norm, no gain
+    bad = list(ok); bad[8] = 2
+    assert f(*bad) == 1                                                    # layer norm, no bias
+    bad = list(ok); bad[11] = F(float("nan"))
+    assert f(*bad) == 1                                                    # eps
+    bad = list(ok); bad[12] = 33
+    assert f(*bad) == 1                                                    # odd n_rot
+    bad = list(ok); bad[12] = 128
+    assert f(*bad) == 1                                                    # n_rot > d_idx
+    bad = list(ok); bad[12] = 24
+    assert f(*bad) == 2                                                    # NeoX needs n_rot % 16
+    bad = list(ok); bad[13] = F(-1.0)
+    assert f(*bad) == 1                                                    # rotary base
+    bad = list(ok); bad[4], bad[2] = 96, 1536
+    assert f(*bad) == 2                                                    # 96-wide keys
+    bad = list(ok); bad[7] = 0
+    assert f(*bad) == 0                                                    # empty range: no work
+
+
 def test_scores_reject_bad_arguments(L):
     f = L.sfa_index_scores
     ok = [FAKE, FAKE, FAKE, FAKE, 4, 1, 8, 128, 4, FAKE, 256 * 100, 1, 100, FAKE, 100, None, None]
