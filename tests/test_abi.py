@@ -158,3 +158,13 @@ def test_attend_rejects_bad_arguments(L):
     g = L.sfa_dense_attend
     assert g(FAKE, FAKE, None, 0, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04), FAKE, FAKE,
              0, FAKE, None, None, 0, None, None) == 1                      # n_kv_max 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: with libsfa.so absent, the first entry-point call raises."""
+    import indexer_selected_sparse_block_gb300 as sfa
+    from indexer_selected_sparse_block_gb300 import _binding as B
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libsfa.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        sfa.sfa_attend_workspace_bytes(1, 16, 1, 512, 2051)
