@@ -51,6 +51,8 @@ def load(path: str | None = None):
         return _lib
     lib = ctypes.CDLL(path or build())
     lib.sfa_oracle_pool.argtypes = [_f32p, _i64, _int, _int, _f64p]
+    lib.sfa_oracle_pool_cells.argtypes = [_f32p, _i64, _i32p, _i64, _int, _int, _f64p]
+    lib.sfa_oracle_pool_cells.restype = _int
     lib.sfa_oracle_key_transform.argtypes = [_f64p, _i64, _int, _int, _int, _f32p, _f32p,
                                              ctypes.c_double, _int, ctypes.c_double, _int, _i64]
     lib.sfa_oracle_index_scores.argtypes = [_f32p, _f32p, _int, _int, _f64p, _i64, _f64p]
@@ -78,6 +80,19 @@ def pool(X, n_blk: int, cr: int, lib=None) -> np.ndarray:
     assert n_blk * cr <= X.shape[0]
     out = np.zeros((n_blk, X.shape[1]), np.float64)
     lib.sfa_oracle_pool(X, n_blk, X.shape[1], cr, out)
+    return out
+
+
+def pool_cells(X, cell_of, n_blk: int, cr: int, lib=None) -> np.ndarray:
+    """Block means in the paged layout: X[n_cells][d_idx] is the flat cell array and
+    cell_of[t] the cell of position t of one sequence -> [n_blk][d_idx] f64."""
+    lib = lib or load()
+    X = _f32(X)
+    cell_of = np.ascontiguousarray(cell_of, dtype=np.int32)
+    assert n_blk * cr <= cell_of.shape[0]
+    out = np.zeros((n_blk, X.shape[1]), np.float64)
+    if lib.sfa_oracle_pool_cells(X, X.shape[0], cell_of, n_blk, X.shape[1], cr, out) != 0:
+        raise ValueError("a cell map entry lies outside the cell array")
     return out
 
 

@@ -48,6 +48,30 @@ void sfa_oracle_pool(const float *X, int64_t n_blk, int d_idx, int cr, double *k
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Step 1, paged cell layout [QSA paragraph that computes every layout-dependent input on the
+ * host and cuts blocks on positions, so nothing assumes a contiguous cache; "support a
+ * non-unified KV cache in QSA": a cell means a different token in each stream, so the maps
+ * are kept per stream].  Position t's raw key is row cell_of[t] of the flat cell array
+ * X[n_cells][d_idx] (cell_of is one stream's map); blocks are still cuts of the positions:
+ *   kbar_b[d] = (1/cr) * sum_{t = b*cr}^{b*cr + cr - 1} X[cell_of[t]][d]
+ * Returns 0, or -1 when a map entry read lies outside [0, n_cells).                       */
+int sfa_oracle_pool_cells(const float *X, int64_t n_cells, const int32_t *cell_of,
+                          int64_t n_blk, int d_idx, int cr, double *kbar)
+{
+    for (int64_t t = 0; t < n_blk * cr; ++t)
+        if (cell_of[t] < 0 || cell_of[t] >= n_cells) return -1;
+    for (int64_t b = 0; b < n_blk; ++b) {
+        for (int d = 0; d < d_idx; ++d) {
+            double sum = 0.0;
+            for (int t = 0; t < cr; ++t)
+                sum += (double)X[(int64_t)cell_of[b * cr + t] * d_idx + d];
+            kbar[b * d_idx + d] = sum / (double)cr;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Step 1b -- the norm and the rotation of the pooled keys [QSA, indexer key cache paragraph:
  * the cache holds raw keys because pooling precedes the norm and the rotation; the indexer
  * ropes with the main attention's rotary width].  In place on kbar[n_blk][d_idx]; the pages

@@ -55,6 +55,33 @@ def pin_pool_closed_forms(lib):
     np.testing.assert_allclose(oracle.pool(X, 64, 4, lib=lib), want, rtol=0, atol=1e-15)
 
 
+def pin_pool_cells(lib):
+    # Worked example of the paged layout: four cells, position t held in cell [2, 0, 3, 1][t],
+    # cr 2.  Block 0 covers positions 0 and 1 (cells 2 and 0): (4 + 1)/2, (40 + 10)/2; block 1
+    # covers positions 2 and 3 (cells 3 and 1): (8 + 2)/2, (80 + 20)/2.  Reading the map the
+    # wrong way round (cell -> position) or ignoring it gives other values.
+    X = np.array([[1, 10], [2, 20], [4, 40], [8, 80]], np.float32)
+    assert np.array_equal(oracle.pool_cells(X, [2, 0, 3, 1], 2, 2, lib=lib),
+                          [[2.5, 25.0], [5.0, 50.0]])
+    # the identity map is the per-sequence layout
+    Y = _bf16(_rng(40).standard_normal((130, 16)))
+    assert np.array_equal(oracle.pool_cells(Y, np.arange(130), 32, 4, lib=lib),
+                          oracle.pool(Y, 32, 4, lib=lib))
+    # a shuffled page table (10 of 14 pages of 16 cells, the rest unused), against numpy's
+    # block means of the gathered rows
+    r = _rng(41)
+    page = 16
+    pages = r.permutation(14)[:10]
+    cell_of = (pages[:, None] * page + np.arange(page)[None, :]).reshape(-1)
+    cells = _bf16(r.standard_normal((14 * page, 8)))
+    want = cells[cell_of].astype(np.float64)[:160].reshape(40, 4, 8).mean(axis=1)
+    np.testing.assert_allclose(oracle.pool_cells(cells, cell_of, 40, 4, lib=lib), want,
+                               rtol=0, atol=1e-15)
+    # an entry outside the cell array is an error, not a read
+    with pytest.raises(ValueError):
+        oracle.pool_cells(X, [2, 0, 4, 1], 2, 2, lib=lib)
+
+
 # -------------------------------------------------------------------------------- score
 def pin_scores(lib):
     g = _golden("qsa_tiny_relu.json")
@@ -369,7 +396,7 @@ def pin_key_transform(lib):
     assert not np.allclose(both, rot_first, rtol=1e-6)
 
 
-PINS = [pin_pool_closed_forms, pin_scores, pin_select, pin_token_expanded, pin_mask,
+PINS = [pin_pool_closed_forms, pin_pool_cells, pin_scores, pin_select, pin_token_expanded, pin_mask,
         pin_attend, pin_pipeline, pin_key_transform]
 
 
@@ -384,9 +411,12 @@ MUTANTS = {
     "ties_to_higher_block": ("return (a->b < b->b) ? -1 : (a->b > b->b);",
                              "return (a->b > b->b) ? -1 : (a->b < b->b);"),
     "tail_dropped": ("for (int64_t t = n_blk * cr; t < n_vis; ++t) mask[t] = 1;", ""),
-    "sum_not_mean": ("kbar[b * d_idx + d] = sum / (double)cr;", "kbar[b * d_idx + d] = sum;"),
+    "sum_not_mean": ("(int64_t)d_idx + d];\n            kbar[b * d_idx + d] = sum / (double)cr;",
+                     "(int64_t)d_idx + d];\n            kbar[b * d_idx + d] = sum;"),
     "pool_window_shifted": ("X[(b * cr + t) * (int64_t)d_idx + d]",
                             "X[(b * cr + t + 1) * (int64_t)d_idx + d]"),
+    "cell_map_ignored": ("sum += (double)X[(int64_t)cell_of[b * cr + t] * d_idx + d];",
+                         "sum += (double)X[(b * cr + t) * (int64_t)d_idx + d];"),
     "scale_dropped": ("logit[t] = scale * dot;", "logit[t] = dot;"),
     "wrong_kv_head": ("const int g = h / group;", "const int g = h % h_kv;"),
     "weight_outside_relu": ("s += (double)w[j] * relu;", "s += relu;"),
