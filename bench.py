@@ -37,6 +37,9 @@ from indexer_selected_sparse_block_gb300 import _binding as B  # noqa: E402
 METRIC = "sparse-attn tokens/s (decode, pp2048) at depth; gathered-KV HBM GB/s vs peak"
 DEFAULT_WORKLOAD = "decode_32x131072"
 SECOND_WORKLOAD = "pp2048_131072"
+PAGE_CELLS = 64
+PAGED_LAYOUT = (f"paged: {PAGE_CELLS}-cell pages dealt from a seeded shuffled page table, "
+                "one spare page per sequence")
 L2_FLUSH_BYTES = 512 << 20
 HOLD_CYCLES = 400_000          # ~0.2 ms GPU spin that covers the host's enqueue of one step
 CSRC = os.path.join(ROOT, "indexer_selected_sparse_block_gb300", "csrc")
@@ -168,15 +171,29 @@ class ClockSampler:
 class Workbench:
     """Inputs, buffers and one step of the method for workload w on the current device."""
 
-    def __init__(self, w, dev, bounded=None):
-        self.w, self.dev = w, dev
+    def __init__(self, w, dev, bounded=None, paged=False):
+        self.w, self.dev, self.paged = w, dev, paged
         self.case = sfa.make_case(w, device=dev)
         self.n_blk_max = w.n_tok // w.compress_ratio
+        self.cell_of = None
+        if paged:
+            # a paged cache: the same rows in 64-cell pages dealt from a seeded shuffled page
+            # table (one spare page per sequence); the per-sequence copies stay as the host
+            # source of the end-to-end step's new rows
+            self.cell_of, n_cells = sfa.make_cell_map(w.n_seq, w.n_tok, page=PAGE_CELLS,
+                                                      spare_pages=w.n_seq, seed=w.seed,
+                                                      device=dev)
+            self.seq_rows = {}
+            for n in ("X", "K", "V"):
+                if self.case[n] is not None:
+                    self.seq_rows[n] = self.case[n]
+                    self.case[n] = sfa.to_cells(self.case[n], self.cell_of, n_cells)
         self.step = sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q,
                                 h_kv=w.h_kv, dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                                 compress_ratio=w.compress_ratio,
                                 indexer_top_k=w.indexer_top_k, n_blk_max=self.n_blk_max,
-                                q_group=w.n_q_per_seq, bounded=bounded, device=dev)
+                                q_group=w.n_q_per_seq, bounded=bounded, cell_of=self.cell_of,
+                                device=dev)
         # the cache state before the step: every block completed by earlier tokens is pooled
         self.first_new_blk = w.depth // w.compress_ratio
         self.step.pool(self.case["X"], 0, self.first_new_blk)
@@ -295,9 +312,12 @@ def measure_e2e(wb, steps, warmup):
     are then placed into the caches by device copies."""
     c, w = wb.case, wb.w
     sl = slice(w.depth, w.n_tok)   # the step's new cache rows (positions depth .. n_tok - 1)
-    new_rows = {"K": c["K"][:, sl], "X": c["X"][:, sl]}
+    rows = wb.seq_rows if wb.paged else c
+    new_rows = {"K": rows["K"][:, sl], "X": rows["X"][:, sl]}
     if c["V"] is not None:
-        new_rows["V"] = c["V"][:, sl]
+        new_rows["V"] = rows["V"][:, sl]
+    # paged: the new rows go to their cells (the page table is known before the step)
+    new_cells = wb.cell_of[:, sl].reshape(-1).long() if wb.paged else None
     names = ["Q", "q_idx", "w", "q_seq", "q_pos"]
     parts = {n: c[n] for n in names}
     parts.update({f"{n}_new": t for n, t in new_rows.items()})
@@ -321,7 +341,11 @@ def measure_e2e(wb, steps, warmup):
     def one():
         dev_arena.copy_(host_arena, non_blocking=True)
         for n, dst in new_rows.items():
-            dst.copy_(dv[f"{n}_new"])
+            if new_cells is None:
+                dst.copy_(dv[f"{n}_new"])
+            else:
+                src = dv[f"{n}_new"]
+                c[n].index_copy_(0, new_cells, src.reshape((-1,) + tuple(c[n].shape[1:])))
         wb.run_step()
         out.copy_(wb.step.O, non_blocking=True)
 
@@ -442,6 +466,9 @@ def main():
                     help="decode: exact scores + select instead of the bounded selection")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller runs for ncu captures)")
+    ap.add_argument("--paged", action="store_true",
+                    help="time the paged cache layout (shuffled 64-cell pages) as the main line")
+    ap.add_argument("--no-paged", action="store_true", help="skip the paged companion line")
     ap.add_argument("--depth", type=int, default=0,
                     help="override the cache depth (smaller runs for ncu captures)")
     args = ap.parse_args()
@@ -477,7 +504,7 @@ def main():
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
              torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
-    wb = Workbench(w, dev, bounded=False if args.exact else None)
+    wb = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -558,6 +585,7 @@ def main():
                        "h_idx": w.h_idx, "d_idx": w.d_idx, "compress_ratio": w.compress_ratio,
                        "indexer_top_k": w.indexer_top_k,
                        "selection": "bounded" if wb.step.bounded else "exact",
+                       "cache_layout": PAGED_LAYOUT if wb.paged else "contiguous per sequence",
                        "l2": "flushed before every timed "
                        "step outside the timed events (512 MB written, then 256 MB of another "
                        "buffer read)"},
@@ -576,8 +604,23 @@ def main():
         cn = [int(x) for x in cn if int(x) >= 0]
         line["bounded_selection"] = {"candidates_per_query_mean": (sum(cn) / len(cn)) if cn else 0,
                                      "candidates_per_query_max": max(cn) if cn else 0}
+    wb_sel = (wb.step.n_sel.clone(), wb.step.O.clone())
     del wb
     torch.cuda.empty_cache()
+
+    if not args.no_paged and not args.paged and rank == 0 and world == 1:
+        # the same workload on a paged cache: the pool and the attention read through the map
+        wbp = Workbench(w, dev, bounded=False if args.exact else None, paged=True)
+        sp, _ = measure(wbp, max(3, args.steps // 2), 3, flush, per_stage=False)
+        _, stp = measure(wbp, 3, 3, flush, per_stage=True)
+        msp = sum(sp) / len(sp)
+        same = bool(torch.equal(wbp.step.n_sel, wb_sel[0]) and torch.equal(wbp.step.O, wb_sel[1]))
+        line["paged"] = {"cache_layout": PAGED_LAYOUT, "value": w.n_q / (msp / 1000.0),
+                         "unit": "tokens/s", "ms_per_step": msp, "stage_ms": stp,
+                         "same_output_as_contiguous": same,
+                         "device_status": B.sfa_read_device_status(wbp.step.status)}
+        del wbp
+        torch.cuda.empty_cache()
 
     if not args.no_second and rank == 0 and world == 1:
         w2 = sfa.WORKLOADS[SECOND_WORKLOAD]

@@ -61,6 +61,8 @@ enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
                                  spans sequences (that query is skipped)                  */
 #define SFA_DEV_TIMEOUT 0x8   /* a bounded wait inside a kernel ran out; the kernel
                                  released its resources and returned early                */
+#define SFA_DEV_BAD_CELL 0x10 /* a paged cell map entry outside [0, n_cells): that position
+                                 reads as a zero row (pool) or is left out (attention)    */
 
 /*
  * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, taken
@@ -257,6 +259,50 @@ int sfa_dense_attend(const void *Q, const void *K, const void *V, int dtype, int
                      float scale, const int32_t *q_seq, const int32_t *q_pos, int64_t n_kv_max,
                      float *O, float *lse, void *workspace, size_t workspace_bytes,
                      int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * Paged (non-contiguous) cell layout.  The cache holds each stream's tokens in cells of a flat
+ * array in any order; blocks are still cuts of the position line, so the block of position t
+ * is t / cr wherever its cell sits, and a map from positions to cells, kept per stream because
+ * a cell index means a different token in each stream, is all the kernels need (qwen4exp
+ * commits in llama.cpp: the QSA paragraph that computes every layout-dependent input on the
+ * host and cuts blocks on positions, and "support a non-unified KV cache in QSA", where the
+ * cell maps gain a stream dimension).  The scores and the selection work on pooled blocks and
+ * are unchanged; the pool and the attention read their rows through the map:
+ *
+ *   cell_of [n_seq][n_pos_cap] int32 (device): cell_of[s][t] = the cell that holds position t
+ *           of sequence s.  Only the positions a call reads are looked at (t < blk_end*cr for
+ *           the pool, t <= p_i for the attention), so unused entries may hold anything.
+ *   X       [n_cells][d_idx] raw index keys (pool);  K [n_cells][h_kv][dkq], V [n_cells][h_kv][dv]
+ *           or NULL (attention), each row one cell.
+ *
+ * Results equal those of the per-sequence calls on the gathered layout X'[s][t] = X[cell_of[s][t]]
+ * (K', V' the same) bit for bit under the default kernel choice: the same kernels read the
+ * same values in the same order.  An entry outside [0, n_cells) sets SFA_DEV_BAD_CELL
+ * (dev_status is nullable for the pool too).  The
+ * attention calls never take the tcgen05 kernel (its producers copy runs of four consecutive
+ * rows as one TMA box), whatever SFA_ATTEND_KERNEL says; sfa_attend_plan describes them
+ * otherwise.  n_pos_cap plays the role of n_tok_cap (p_i < n_pos_cap); n_cells < 2^31.
+ * Arguments otherwise as sfa_pool_index_keys, sfa_gather_attend and sfa_dense_attend.
+ */
+int sfa_pool_index_keys_paged(const void *X, int x_dtype, int64_t n_cells, const int32_t *cell_of,
+                              int64_t n_pos_cap, int n_seq, int d_idx, int compress_ratio,
+                              int64_t blk_begin, int64_t blk_end, void *Kbar,
+                              int64_t kbar_seq_stride, float *Kbar_r, int64_t kr_seq_stride,
+                              int32_t *dev_status, sfa_stream_t stream);
+int sfa_gather_attend_paged(const void *Q, const void *K, const void *V, int dtype,
+                            int64_t n_cells, const int32_t *cell_of, int n_seq, int64_t n_pos_cap,
+                            int n_q, int h_q, int h_kv, int dkq, int dv, float scale,
+                            const int32_t *q_seq, const int32_t *q_pos, const int32_t *blk_idx,
+                            const int32_t *n_sel, int top_k, int compress_ratio, float *O,
+                            float *lse, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, sfa_stream_t stream);
+int sfa_dense_attend_paged(const void *Q, const void *K, const void *V, int dtype,
+                           int64_t n_cells, const int32_t *cell_of, int n_seq, int64_t n_pos_cap,
+                           int n_q, int h_q, int h_kv, int dkq, int dv, float scale,
+                           const int32_t *q_seq, const int32_t *q_pos, int64_t n_kv_max, float *O,
+                           float *lse, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_status, sfa_stream_t stream);
 
 /*
  * sfa_gather_attend_noalloc -- sfa_gather_attend for callers that cannot allocate device

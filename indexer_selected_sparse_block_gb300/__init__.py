@@ -4,16 +4,16 @@ The product is libsfa.so (C ABI in include/sfa.h, CUDA kernels for sm_103a in cs
 package is its Python binding (argument marshalling only), the step runner that chains the
 entry points, and the seeded synthetic input generators.
 """
-from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY,
-                       SFA_DEV_TIMEOUT, SFA_ERR_CUDA, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED,
-                       SFA_ERR_WORKSPACE, SFA_F32, SFA_OK, SfaError, kbar_shape, lib,
-                       sfa_attend_plan, sfa_attend_workspace_bytes, sfa_dense_attend,
-                       sfa_gather_attend,
-                       sfa_index_scores, sfa_index_scores_bounded, sfa_pool_index_keys,
-                       sfa_pool_index_keys_transformed,
-                       sfa_read_device_status, sfa_topk_blocks, sfa_topk_blocks_refine,
+from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_CELL, SFA_DEV_BAD_NSEL,
+                       SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT, SFA_ERR_CUDA, SFA_ERR_INVALID_ARG,
+                       SFA_ERR_UNSUPPORTED, SFA_ERR_WORKSPACE, SFA_F32, SFA_OK, SfaError,
+                       kbar_shape, lib, sfa_attend_plan, sfa_attend_workspace_bytes,
+                       sfa_dense_attend, sfa_dense_attend_paged, sfa_gather_attend,
+                       sfa_gather_attend_paged, sfa_index_scores, sfa_index_scores_bounded,
+                       sfa_pool_index_keys, sfa_pool_index_keys_paged,
+                       sfa_pool_index_keys_transformed, sfa_read_device_status, sfa_topk_blocks, sfa_topk_blocks_refine,
                        sfa_topk_refine_workspace_bytes, sfa_topk_workspace_bytes)
-from .inputs import WORKLOADS, Workload, make_case
+from .inputs import WORKLOADS, Workload, make_case, make_cell_map, to_cells
 from .pipeline import SfaStep
 
 __all__ = [n for n in dir() if not n.startswith("_")]

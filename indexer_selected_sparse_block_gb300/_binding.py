@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libsfa.so")
 SFA_OK, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA, SFA_ERR_WORKSPACE = range(5)
 SFA_BF16, SFA_F32 = 0, 1
 SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT = 1, 2, 4, 8
+SFA_DEV_BAD_CELL = 16
 SFA_REFINE_MAX_BLOCKS = 36864   # longest row sfa_topk_blocks_refine takes (one selection piece)
 
 _lib = None
@@ -32,6 +33,8 @@ SIGNATURES = {
     "sfa_pool_index_keys_transformed": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64,
                                                _int, _vp, _vp, _f32, _int, _f32, _int, _i64,
                                                _vp, _i64, _vp, _i64, _vp]),
+    "sfa_pool_index_keys_paged": (_int, [_vp, _int, _i64, _vp, _i64, _int, _int, _int, _i64,
+                                         _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
     "sfa_index_scores": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp, _i64,
                                 _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
@@ -53,6 +56,12 @@ SIGNATURES = {
     "sfa_gather_attend_noalloc": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int,
                                          _int, _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _vp,
                                          _vp, _vp, _vp]),
+    "sfa_gather_attend_paged": (_int, [_vp, _vp, _vp, _int, _i64, _vp, _int, _i64, _int, _int,
+                                       _int, _int, _int, _f32, _vp, _vp, _vp, _vp, _int, _int,
+                                       _vp, _vp, _vp, _sz, _vp, _vp]),
+    "sfa_dense_attend_paged": (_int, [_vp, _vp, _vp, _int, _i64, _vp, _int, _i64, _int, _int,
+                                      _int, _int, _int, _f32, _vp, _vp, _i64, _vp, _vp, _vp, _sz,
+                                      _vp, _vp]),
     "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
     "sfa_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -280,6 +289,72 @@ def sfa_dense_attend(Q, K, V, q_seq, q_pos, n_kv_max: int, scale: float, O, lse=
                                 _p(O), _p(lse), _p(workspace), ws_bytes, _p(dev_status),
                                 _stream(stream))
     _check("sfa_dense_attend", rc)
+
+
+def _paged_dims(cell_of, n_cells_of):
+    if cell_of.dtype != torch.int32 or cell_of.dim() != 2 or not cell_of.is_contiguous():
+        raise ValueError("cell_of must be a contiguous [n_seq][n_pos_cap] int32 tensor")
+    return cell_of.shape[0], cell_of.shape[1], n_cells_of
+
+
+def sfa_pool_index_keys_paged(X, cell_of, compress_ratio: int, blk_begin: int, blk_end: int, Kbar,
+                              Kbar_r=None, dev_status=None, stream=None):
+    """Paged layout: X [n_cells][d_idx] raw index keys, one cell per row; position t of
+    sequence s is in cell cell_of[s][t].  Writes rows [blk_begin, blk_end) of Kbar (and Kbar_r)
+    as sfa_pool_index_keys does for the gathered layout."""
+    n_cells, d_idx = X.shape
+    n_seq, n_pos_cap, _ = _paged_dims(cell_of, n_cells)
+    rc = lib().sfa_pool_index_keys_paged(_p(X), _dtype_code(X), n_cells, _p(cell_of), n_pos_cap,
+                                         n_seq, d_idx, compress_ratio, blk_begin, blk_end,
+                                         _p(Kbar), Kbar.stride(0), _p(Kbar_r),
+                                         Kbar_r.stride(0) if Kbar_r is not None else 0,
+                                         _p(dev_status), _stream(stream))
+    _check("sfa_pool_index_keys_paged", rc)
+
+
+def _paged_attn_dims(Q, K, V, O, cell_of):
+    n_q, h_q, dkq = Q.shape
+    n_cells, h_kv, _ = K.shape
+    if V is not None and (K.dtype != V.dtype or V.shape[0] != n_cells):
+        raise ValueError("V must share K's dtype and cell count")
+    if Q.dtype != K.dtype:
+        raise ValueError("Q and K must share a dtype")
+    n_seq, n_pos_cap, _ = _paged_dims(cell_of, n_cells)
+    return n_q, h_q, dkq, n_cells, n_seq, n_pos_cap, h_kv, O.shape[-1]
+
+
+def sfa_gather_attend_paged(Q, K, V, cell_of, q_seq, q_pos, blk_idx, n_sel, top_k: int,
+                            compress_ratio: int, scale: float, O, lse=None, workspace=None,
+                            dev_status=None, stream=None):
+    """sfa_gather_attend on the paged layout: K [n_cells][h_kv][dkq], V [n_cells][h_kv][dv] or
+    None, position t of sequence s in cell cell_of[s][t]."""
+    n_q, h_q, dkq, n_cells, n_seq, n_pos_cap, h_kv, dv = _paged_attn_dims(Q, K, V, O, cell_of)
+    n_kv_max = top_k * compress_ratio + compress_ratio - 1
+    need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_gather_attend_paged(_p(Q), _p(K), _p(V), _dtype_code(K), n_cells, _p(cell_of),
+                                       n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, float(scale),
+                                       _p(q_seq), _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
+                                       compress_ratio, _p(O), _p(lse), _p(workspace), ws_bytes,
+                                       _p(dev_status), _stream(stream))
+    _check("sfa_gather_attend_paged", rc)
+
+
+def sfa_dense_attend_paged(Q, K, V, cell_of, q_seq, q_pos, n_kv_max: int, scale: float, O,
+                           lse=None, workspace=None, dev_status=None, stream=None):
+    """sfa_dense_attend on the paged layout (see sfa_gather_attend_paged)."""
+    n_q, h_q, dkq, n_cells, n_seq, n_pos_cap, h_kv, dv = _paged_attn_dims(Q, K, V, O, cell_of)
+    need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_dense_attend_paged(_p(Q), _p(K), _p(V), _dtype_code(K), n_cells, _p(cell_of),
+                                      n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, float(scale),
+                                      _p(q_seq), _p(q_pos), n_kv_max, _p(O), _p(lse),
+                                      _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
+    _check("sfa_dense_attend_paged", rc)
 
 
 def sfa_read_device_status(dev_status, stream=None) -> int:

@@ -48,10 +48,27 @@ struct AttnParams {
     float *O, *lse, *part_o, *part_ml;
     int32_t *status;
     int64_t k_tok_stride, k_seq_stride, v_tok_stride, v_seq_stride, n_tok_cap;
+    const int32_t *cell_of;   // paged layout: [n_seq][n_tok_cap] cell of each position, or null
+    int64_t n_cells;          // rows of the paged K (and V) arrays
     int n_seq, n_q, h_q, h_kv, G, top_k, cr, dense, n_split, split_tokens, stages;
     int cluster_merge;   // 1: the n_split CTAs of an item form one cluster and merge in place
     float scale_log2;
 };
+
+// Row of position tok of sequence seq in the K (and V) arrays, in units of k_tok_stride
+// (v_tok_stride) from the sequence's base: the position itself in the per-sequence layout, the
+// cell the map gives in the paged one (where the sequence bases are all zero).  Padding
+// (tok < 0) and a cell outside [0, n_cells) give -1: the position is left out of the softmax,
+// and a bad cell raises SFA_DEV_BAD_CELL.
+__device__ __forceinline__ int64_t kv_row(const AttnParams &p, int seq, int tok) {
+    if (tok < 0 || !p.cell_of) return tok;
+    const int32_t c = __ldg(p.cell_of + (int64_t)seq * p.n_tok_cap + tok);
+    if (c < 0 || (int64_t)c >= p.n_cells) {
+        set_status(p.status, SFA_DEV_BAD_CELL);
+        return -1;
+    }
+    return c;
+}
 
 // Per-CTA view of the attended list of one query.
 struct ListInfo {
@@ -257,14 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
         uint8_t *dstK = sStage + (size_t)st * STAGE_BYTES;
         const int r = tid >> 2, sub = tid & 3;
         const int tok = token_at(p, L, j0 + t * kT + r, j1, sBlk, jb0);
-        if (sub == 0) sTok[st * kT + r] = tok;
-        const __nv_bfloat16 *srcK = tok >= 0 ? Kseq + (int64_t)tok * p.k_tok_stride : Kseq;
-        const uint32_t nbytes = tok >= 0 ? 16u : 0u;
+        const int64_t row = kv_row(p, L.seq, tok);
+        if (sub == 0) sTok[st * kT + r] = row >= 0 ? tok : -1;
+        const __nv_bfloat16 *srcK = row >= 0 ? Kseq + row * p.k_tok_stride : Kseq;
+        const uint32_t nbytes = row >= 0 ? 16u : 0u;
         const uint32_t rowK = smem_u32(dstK) + r * KROW;
 #pragma unroll 6
         for (int c = sub; c < KCH; c += 4) cp_async16(rowK + swz(c, r) * 16, srcK + c * 8, nbytes);
         if constexpr (!V_IS_K) {
-            const __nv_bfloat16 *srcV = tok >= 0 ? Vseq + (int64_t)tok * p.v_tok_stride : Vseq;
+            const __nv_bfloat16 *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
             const uint32_t rowV = smem_u32(dstK + kT * KROW) + r * VROW;
 #pragma unroll 4
             for (int c = sub; c < VCH; c += 4)
@@ -1071,9 +1089,9 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
                             : Kseq;
     const int64_t vstride = p.V ? p.v_tok_stride : p.k_tok_stride;
     for (int j = j0; j < j1; ++j) {
-        const int tok = token_at(p, L, j, j1, sBlk, jb0);
-        if (tok < 0) continue;
-        const float *kr = Kseq + (int64_t)tok * p.k_tok_stride;
+        const int64_t row = kv_row(p, L.seq, token_at(p, L, j, j1, sBlk, jb0));
+        if (row < 0) continue;
+        const float *kr = Kseq + row * p.k_tok_stride;
         float s = 0.f;
 #pragma unroll
         for (int e = 0; e < QE; ++e) s = fmaf(q[e], kr[part + 8 * e], s);
@@ -1086,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
         const float pe = exp2f(s - m_new);
         l_run = l_run * corr + pe;
         m_run = m_new;
-        const float *vr = Vseq + (int64_t)tok * vstride;
+        const float *vr = Vseq + row * vstride;
 #pragma unroll
         for (int e = 0; e < OE; ++e) o[e] = fmaf(pe, vr[part + 8 * e], o[e] * corr);
     }
@@ -1328,14 +1346,15 @@ struct AttendPlan {
 };
 
 AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, int64_t n_kv_max,
-                            int cr, int dense) {
+                            int cr, int dense, bool paged = false) {
     // bf16 inputs take the warp-level mma.sync kernel, which is the faster one on the decode
     // and prefill shapes measured; SFA_ATTEND_KERNEL=tcgen05 selects the tcgen05 kernel for the
     // 512-wide heads instead (same results within the same tolerances).  fp32 inputs take the
-    // SIMT kernel.
+    // SIMT kernel.  The paged layout always takes the mma.sync kernel: the tcgen05 kernel's
+    // producers copy runs of four consecutive rows as one TMA box.
     const int tc_tile = tc::kTT;
     AttendPlan ap{};
-    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && want_tcgen05();
+    const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && !paged && want_tcgen05();
     ap.use_tc = use_tc;
     // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
     int per_sm = 1;
@@ -1377,7 +1396,8 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
                int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv, float scale,
                const int32_t *q_seq, const int32_t *q_pos, const int32_t *blk_idx,
                const int32_t *n_sel, int top_k, int cr, int dense, int64_t n_kv_max, float *O,
-               float *lse, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t st) {
+               float *lse, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t st,
+               const int32_t *cell_of = nullptr, int64_t n_cells = 0) {
     if (!Q || !K || !q_seq || !q_pos || !O) return SFA_ERR_INVALID_ARG;
     if (dtype != SFA_BF16 && dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
     if (n_seq < 1 || n_tok_cap < 1 || n_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0)
@@ -1386,13 +1406,15 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     if (!dense && (!blk_idx || !n_sel || cr < 1 || top_k < 1)) return SFA_ERR_INVALID_ARG;
     if (!dense && top_k > 2048) return SFA_ERR_UNSUPPORTED;
     if (n_kv_max < 1) return SFA_ERR_INVALID_ARG;
+    if (cell_of && (n_cells < 1 || n_cells > 0x7FFFFFFF)) return SFA_ERR_INVALID_ARG;
     if (dv > dkq && !V) return SFA_ERR_INVALID_ARG;
     if (!shape_supported(dkq, dv) || h_q / h_kv > 16) return SFA_ERR_UNSUPPORTED;
     if (!aligned16(Q) || !aligned16(K) || (V && !aligned16(V)) || !aligned16(O))
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
-    const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, V != nullptr, n_kv_max, cr, dense);
+    const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, V != nullptr, n_kv_max, cr, dense,
+                                           cell_of != nullptr);
     const bool use_tc = ap.use_tc;
     SplitPlan sp = ap.sp;
     const int cluster_ns = ap.cluster_ns;
@@ -1408,6 +1430,11 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.v_tok_stride = V ? (int64_t)h_kv * dv : p.k_tok_stride;
     p.v_seq_stride = V ? n_tok_cap * p.v_tok_stride : p.k_seq_stride;
     p.n_tok_cap = n_tok_cap;
+    if (cell_of) {   // rows come from the map: every sequence starts at row 0 of the cell arrays
+        p.k_seq_stride = p.v_seq_stride = 0;
+        p.cell_of = cell_of;
+        p.n_cells = n_cells;
+    }
     p.n_seq = n_seq; p.n_q = n_q; p.h_q = h_q; p.h_kv = h_kv; p.G = h_q / h_kv;
     p.top_k = top_k; p.cr = cr; p.dense = dense;
     p.n_split = sp.n_split; p.split_tokens = sp.split_tokens;
@@ -1498,6 +1525,36 @@ extern "C" int sfa_dense_attend(const void *Q, const void *K, const void *V, int
     return sfa::run_attend(Q, K, V, dtype, n_seq, n_tok_cap, n_q, h_q, h_kv, dkq, dv, scale,
                            q_seq, q_pos, nullptr, nullptr, 0, 1, 1, n_kv_max, O, lse, workspace,
                            workspace_bytes, dev_status, (cudaStream_t)stream);
+}
+
+extern "C" int sfa_gather_attend_paged(const void *Q, const void *K, const void *V, int dtype,
+                                       int64_t n_cells, const int32_t *cell_of, int n_seq,
+                                       int64_t n_pos_cap, int n_q, int h_q, int h_kv, int dkq,
+                                       int dv, float scale, const int32_t *q_seq,
+                                       const int32_t *q_pos, const int32_t *blk_idx,
+                                       const int32_t *n_sel, int top_k, int compress_ratio,
+                                       float *O, float *lse, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       sfa_stream_t stream) {
+    if (!cell_of || compress_ratio < 1 || top_k < 1) return SFA_ERR_INVALID_ARG;
+    const int64_t n_kv_max = (int64_t)top_k * compress_ratio + compress_ratio - 1;
+    return sfa::run_attend(Q, K, V, dtype, n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, scale,
+                           q_seq, q_pos, blk_idx, n_sel, top_k, compress_ratio, 0, n_kv_max, O,
+                           lse, workspace, workspace_bytes, dev_status, (cudaStream_t)stream,
+                           cell_of, n_cells);
+}
+
+extern "C" int sfa_dense_attend_paged(const void *Q, const void *K, const void *V, int dtype,
+                                      int64_t n_cells, const int32_t *cell_of, int n_seq,
+                                      int64_t n_pos_cap, int n_q, int h_q, int h_kv, int dkq,
+                                      int dv, float scale, const int32_t *q_seq,
+                                      const int32_t *q_pos, int64_t n_kv_max, float *O,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, sfa_stream_t stream) {
+    if (!cell_of) return SFA_ERR_INVALID_ARG;
+    return sfa::run_attend(Q, K, V, dtype, n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, scale,
+                           q_seq, q_pos, nullptr, nullptr, 0, 1, 1, n_kv_max, O, lse, workspace,
+                           workspace_bytes, dev_status, (cudaStream_t)stream, cell_of, n_cells);
 }
 
 // ---------------------------------------------------------------------------------------

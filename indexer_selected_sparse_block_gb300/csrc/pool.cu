@@ -59,6 +59,15 @@ struct KeyTransform {
     int64_t pos_offset;          // block b sits at position b * cr + pos_offset
 };
 
+// Paged layout: the raw key of position t of sequence s sits in row cell_of[s * stride + t] of
+// a flat [n_cells][d_idx] array; blocks are still cut on positions.  cell_of null: per-sequence
+// layout.  A cell outside [0, n_cells) reads as a zero row and raises SFA_DEV_BAD_CELL.
+struct CellMap {
+    const int32_t *cell_of;
+    int64_t stride, n_cells;
+    int32_t *status;
+};
+
 // Sum over the `chunks` lanes that hold one row (aligned groups; chunks divides 32).
 __device__ __forceinline__ float row_sum(float v, int chunks) {
     for (int o = 1; o < chunks; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -71,7 +80,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
                                                    int d_idx, int cr, int64_t blk_begin,
                                                    int64_t n_rows, __nv_bfloat16 *__restrict__ Kbar,
                                                    int64_t kbar_seq_stride, float *__restrict__ Kr,
-                                                   int64_t kr_seq_stride, const KeyTransform tf) {
+                                                   int64_t kr_seq_stride, const KeyTransform tf,
+                                                   const CellMap cm) {
     pdl_wait();
     pdl_trigger();
     const int chunks = d_idx >> 3;
@@ -83,11 +93,25 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
     float mv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // this chunk of the pooled row
     if (valid) {
         const T *src = X + seq * x_seq_stride + b * cr * d_idx + c * 8;
+        auto load_row = [&](int t, float (&v)[8]) {   // chunk c of the raw key of token b*cr + t
+            if (!cm.cell_of) {
+                Vec8<T>::load(src + (int64_t)t * d_idx, v);
+                return;
+            }
+            const int32_t cell = __ldg(cm.cell_of + seq * cm.stride + b * cr + t);
+            if (cell >= 0 && (int64_t)cell < cm.n_cells) {
+                Vec8<T>::load(X + (int64_t)cell * d_idx + c * 8, v);
+                return;
+            }
+            set_status(cm.status, SFA_DEV_BAD_CELL);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        };
         float sum[8];
-        Vec8<T>::load(src, sum);
+        load_row(0, sum);
         for (int t = 1; t < cr; ++t) {
             float v[8];
-            Vec8<T>::load(src + (int64_t)t * d_idx, v);
+            load_row(t, v);
 #pragma unroll
             for (int i = 0; i < 8; ++i) sum[i] += v[i];
         }
@@ -189,13 +213,17 @@ namespace {
 int run_pool(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq, int d_idx,
              int compress_ratio, int64_t blk_begin, int64_t blk_end, void *Kbar,
              int64_t kbar_seq_stride, float *Kbar_r, int64_t kr_seq_stride,
-             const KeyTransform &tf, cudaStream_t st) {
+             const KeyTransform &tf, cudaStream_t st, const CellMap &cm = CellMap{}) {
     if (!X || !Kbar || n_seq < 1 || compress_ratio < 1 || compress_ratio > 64) return SFA_ERR_INVALID_ARG;
     if (x_dtype != SFA_BF16 && x_dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
     if (d_idx != 32 && d_idx != 64 && d_idx != 96 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
     if (blk_begin < 0 || blk_end < blk_begin) return SFA_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(Kbar)) return SFA_ERR_INVALID_ARG;
-    if (x_seq_stride < blk_end * compress_ratio * d_idx) return SFA_ERR_INVALID_ARG;
+    if (cm.cell_of) {   // x_seq_stride is unused: the map gives every row
+        if (cm.n_cells < 1 || cm.stride < blk_end * compress_ratio) return SFA_ERR_INVALID_ARG;
+    } else if (x_seq_stride < blk_end * compress_ratio * d_idx) {
+        return SFA_ERR_INVALID_ARG;
+    }
     if (kbar_seq_stride < blk_end * 2 * d_idx || kbar_seq_stride % 8 != 0) return SFA_ERR_INVALID_ARG;
     // the row statistics, the NeoX partner and the bound factors work on whole-warp lane groups
     if ((Kbar_r || tf.norm || tf.n_rot) && d_idx == 96) return SFA_ERR_UNSUPPORTED;
@@ -214,11 +242,11 @@ int run_pool(const void *X, int x_dtype, int64_t x_seq_stride, int n_seq, int d_
             ? launch_pdl(pool_kernel<__nv_bfloat16>, grid, dim3(256), 0, st,
                          reinterpret_cast<const __nv_bfloat16 *>(X), x_seq_stride, d_idx,
                          compress_ratio, blk_begin, n_rows, out, kbar_seq_stride, Kbar_r,
-                         kr_seq_stride, tf)
+                         kr_seq_stride, tf, cm)
             : launch_pdl(pool_kernel<float>, grid, dim3(256), 0, st,
                          reinterpret_cast<const float *>(X), x_seq_stride, d_idx,
                          compress_ratio, blk_begin, n_rows, out, kbar_seq_stride, Kbar_r,
-                         kr_seq_stride, tf);
+                         kr_seq_stride, tf, cm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
@@ -266,4 +294,17 @@ extern "C" int sfa_pool_index_keys_transformed(const void *X, int x_dtype, int64
     tf.pos_offset = pos_offset;
     return run_pool(X, x_dtype, x_seq_stride, n_seq, d_idx, compress_ratio, blk_begin, blk_end,
                     Kbar, kbar_seq_stride, Kbar_r, kr_seq_stride, tf, (cudaStream_t)stream);
+}
+
+extern "C" int sfa_pool_index_keys_paged(const void *X, int x_dtype, int64_t n_cells,
+                                         const int32_t *cell_of, int64_t n_pos_cap, int n_seq,
+                                         int d_idx, int compress_ratio, int64_t blk_begin,
+                                         int64_t blk_end, void *Kbar, int64_t kbar_seq_stride,
+                                         float *Kbar_r, int64_t kr_seq_stride,
+                                         int32_t *dev_status, sfa_stream_t stream) {
+    if (!cell_of) return SFA_ERR_INVALID_ARG;
+    const sfa::KeyTransform none{};
+    const sfa::CellMap cm{cell_of, n_pos_cap, n_cells, dev_status};
+    return sfa::run_pool(X, x_dtype, 0, n_seq, d_idx, compress_ratio, blk_begin, blk_end, Kbar,
+                         kbar_seq_stride, Kbar_r, kr_seq_stride, none, (cudaStream_t)stream, cm);
 }

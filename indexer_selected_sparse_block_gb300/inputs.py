@@ -24,7 +24,8 @@ import math
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_case", "draw_normal_bf16", "draw_uniform"]
+__all__ = ["Workload", "WORKLOADS", "make_case", "draw_normal_bf16", "draw_uniform",
+           "make_cell_map", "to_cells"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -150,3 +151,27 @@ def make_case(w: Workload, device="cpu", dtype=torch.bfloat16, n_tok_cap: int | 
     q_pos = (w.depth + torch.arange(w.n_q_per_seq, dtype=torch.int32, device=dev)).repeat(w.n_seq)
     return {"X": X, "K": K, "V": V, "Q": Q, "q_idx": q_idx, "w": wts, "q_seq": q_seq,
             "q_pos": q_pos}
+
+
+def make_cell_map(n_seq: int, n_pos: int, page: int = 64, spare_pages: int = 0, seed: int = 0,
+                  device="cpu"):
+    """A paged cache layout: each sequence's positions fill pages of ``page`` consecutive
+    cells, dealt from a seeded random permutation of n_seq * ceil(n_pos / page) + spare_pages
+    pages (the spare pages stay unused).  Returns (cell_of [n_seq][n_pos] int32, n_cells)."""
+    pps = -(-n_pos // page)
+    n_pages = n_seq * pps + spare_pages
+    g = torch.Generator()
+    g.manual_seed(seed)
+    perm = torch.randperm(n_pages, generator=g)[: n_seq * pps].view(n_seq, pps)
+    t = torch.arange(n_pos)
+    cell_of = perm[:, t // page] * page + t % page
+    return cell_of.to(torch.int32).to(device), n_pages * page
+
+
+def to_cells(x, cell_of, n_cells: int):
+    """The flat cell array of the per-sequence tensor x [n_seq][n_pos][...]: row cell_of[s][t]
+    holds x[s][t]; unused cells are zero."""
+    tail = tuple(x.shape[2:])
+    cells = torch.zeros((n_cells,) + tail, dtype=x.dtype, device=x.device)
+    cells.index_copy_(0, cell_of.reshape(-1).to(x.device).long(), x.reshape((-1,) + tail))
+    return cells

@@ -12,6 +12,10 @@ half the pooled-key bytes plus the rescoring of the few blocks the bounds cannot
 or, when every query is below the budget (B_i <= indexer_top_k for all i), the dense case
 ``sfa_dense_attend``: every block then fits the budget, so the method is exactly dense
 attention (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+
+With a position -> cell map (``cell_of``), the caches are flat cell arrays in any order (a
+paged serving cache) and the pool and the attention take their ``_paged`` entry points; the
+scores and the selection work on pooled blocks, which are cut on positions either way.
 """
 from __future__ import annotations
 
@@ -24,7 +28,7 @@ class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
                  n_blk_max: int, q_group: int = 1, bounded=None, key_transform=None,
-                 device="cuda"):
+                 cell_of=None, device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -37,6 +41,14 @@ class SfaStep:
         # the norm and rotation of pooled index keys (keyword arguments of
         # sfa_pool_index_keys_transformed), or None: raw pooled keys
         self.key_transform = dict(key_transform) if key_transform else None
+        # paged caches: cell_of [n_seq][n_tok_cap] int32 on the device gives the cell of each
+        # position; X, K and V are then [n_cells][...] arrays
+        self.cell_of = cell_of
+        if cell_of is not None:
+            if tuple(cell_of.shape) != (n_seq, n_tok_cap) or cell_of.dtype != torch.int32:
+                raise ValueError("cell_of must be an int32 [n_seq][n_tok_cap] tensor")
+            if self.key_transform:
+                raise ValueError("the paged pool takes raw pooled keys (no key transform)")
         # The bounded selection (hi-only scores + exact rescoring of the blocks the bounds
         # cannot rule out) halves the pooled-key bytes of decode-like steps, where each query
         # streams its sequence's pooled keys; prefill tiles share those reads and take the
@@ -70,7 +82,11 @@ class SfaStep:
 
     def pool(self, X, blk_begin: int, blk_end: int, stream=None):
         if blk_end > blk_begin:
-            if self.key_transform:
+            if self.cell_of is not None:
+                B.sfa_pool_index_keys_paged(X, self.cell_of, self.cr, blk_begin, blk_end,
+                                            self.Kbar, self.Kbar_r, dev_status=self.status,
+                                            stream=stream)
+            elif self.key_transform:
                 B.sfa_pool_index_keys_transformed(X, self.cr, blk_begin, blk_end, self.Kbar,
                                                   self.Kbar_r, stream=stream, **self.key_transform)
             else:
@@ -104,7 +120,17 @@ class SfaStep:
         self.topk(q_idx, w, q_seq, q_pos, stream=stream)
 
     def attend(self, Q, K, V, q_seq, q_pos, scale: float, stream=None):
-        if self.dense:
+        if self.cell_of is not None:
+            if self.dense:
+                B.sfa_dense_attend_paged(Q, K, V, self.cell_of, q_seq, q_pos, self.n_kv_dense,
+                                         scale, self.O, lse=self.lse, workspace=self.attn_ws,
+                                         dev_status=self.status, stream=stream)
+            else:
+                B.sfa_gather_attend_paged(Q, K, V, self.cell_of, q_seq, q_pos, self.blk_idx,
+                                          self.n_sel, self.top_k, self.cr, scale, self.O,
+                                          lse=self.lse, workspace=self.attn_ws,
+                                          dev_status=self.status, stream=stream)
+        elif self.dense:
             B.sfa_dense_attend(Q, K, V, q_seq, q_pos, self.n_kv_dense, scale, self.O,
                                lse=self.lse, workspace=self.attn_ws, dev_status=self.status,
                                stream=stream)

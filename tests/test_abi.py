@@ -160,6 +160,39 @@ def test_attend_rejects_bad_arguments(L):
              0, FAKE, None, None, 0, None, None) == 1                      # n_kv_max 0
 
 
+def test_paged_entry_points_reject_bad_arguments(L):
+    f = L.sfa_pool_index_keys_paged
+    #       X     dt  n_cells cell_of cap   seq d_idx cr b0 b1 Kbar  stride Kr    kr  status
+    base = [FAKE, 0, 5000, FAKE, 4096, 2, 64, 4, 0, 1024, FAKE, 131072, None, 0, None, None]
+    assert f(*base[:3], None, *base[4:]) == 1                                     # no map
+    a = list(base); a[2] = 0
+    assert f(*a) == 1                                                             # no cells
+    a = list(base); a[4] = 4095
+    assert f(*a) == 1                                                             # map too short
+    a = list(base); a[6] = 48
+    assert f(*a) == 2                                                             # d_idx
+    a = list(base); a[0] = ODD
+    assert f(*a) == 1                                                             # alignment
+    a = list(base); a[9] = 0
+    assert f(*a) == 0                                                             # empty: no work
+    g = L.sfa_gather_attend_paged
+    base = [FAKE, FAKE, None, 0, 5000, FAKE, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04),
+            FAKE, FAKE, FAKE, FAKE, 256, 4, FAKE, None, None, 0, None, None]
+    a = list(base); a[5] = None
+    assert g(*a) == 1                                                             # no map
+    a = list(base); a[4] = 0
+    assert g(*a) == 1                                                             # no cells
+    a = list(base); a[4] = 1 << 31
+    assert g(*a) == 1                                                             # cells >= 2^31
+    a = list(base); a[11], a[12] = 320, 256
+    assert g(*a) == 2                                                             # head dim
+    h = L.sfa_dense_attend_paged
+    assert h(FAKE, FAKE, None, 0, 5000, None, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04),
+             FAKE, FAKE, 4096, FAKE, None, None, 0, None, None) == 1               # no map
+    assert h(FAKE, FAKE, None, 0, 0, FAKE, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04),
+             FAKE, FAKE, 4096, FAKE, None, None, 0, None, None) == 1               # no cells
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No CPU fallback: with libsfa.so absent, the first entry-point call raises."""
     import indexer_selected_sparse_block_gb300 as sfa
