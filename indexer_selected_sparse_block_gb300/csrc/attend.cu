@@ -60,14 +60,16 @@ struct AttnParams {
 // cell the map gives in the paged one (where the sequence bases are all zero).  Padding
 // (tok < 0) and a cell outside [0, n_cells) give -1: the position is left out of the softmax,
 // and a bad cell raises SFA_DEV_BAD_CELL.
-__device__ __forceinline__ int64_t kv_row(const AttnParams &p, int seq, int tok) {
-    if (tok < 0 || !p.cell_of) return tok;
-    const int32_t c = __ldg(p.cell_of + (int64_t)seq * p.n_tok_cap + tok);
+__device__ __forceinline__ int64_t checked_cell(const AttnParams &p, int32_t c) {
     if (c < 0 || (int64_t)c >= p.n_cells) {
         set_status(p.status, SFA_DEV_BAD_CELL);
         return -1;
     }
     return c;
+}
+__device__ __forceinline__ int64_t kv_row(const AttnParams &p, int seq, int tok) {
+    if (tok < 0 || !p.cell_of) return tok;
+    return checked_cell(p, __ldg(p.cell_of + (int64_t)seq * p.n_tok_cap + tok));
 }
 
 // Per-CTA view of the attended list of one query.
@@ -269,12 +271,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
                                              (int64_t)L.seq * p.v_seq_stride + (int64_t)g * DV;
     const int n_tiles = (j1 - j0 + kT - 1) / kT;
 
+    // The token (and, paged, the map entry) of this thread's row is looked up one tile ahead
+    // of the copy that uses it: tiles are issued in order, so the lookup for tile t + 1 is
+    // made while tile t is issued, and its latency overlaps a tile of compute.
+    int nx_tok = -1;
+    int32_t nx_cell = 0;
+    auto lookup = [&](int t) {
+        nx_tok = t < n_tiles ? token_at(p, L, j0 + t * kT + (tid >> 2), j1, sBlk, jb0) : -1;
+        if (p.cell_of && nx_tok >= 0)
+            nx_cell = __ldg(p.cell_of + (int64_t)L.seq * p.n_tok_cap + nx_tok);
+    };
+    lookup(0);
+
     auto issue_tile = [&](int t) {
         const int st = t % p.stages;
         uint8_t *dstK = sStage + (size_t)st * STAGE_BYTES;
         const int r = tid >> 2, sub = tid & 3;
-        const int tok = token_at(p, L, j0 + t * kT + r, j1, sBlk, jb0);
-        const int64_t row = kv_row(p, L.seq, tok);
+        const int tok = nx_tok;
+        const int64_t row = p.cell_of && tok >= 0 ? checked_cell(p, nx_cell) : tok;
+        lookup(t + 1);
         if (sub == 0) sTok[st * kT + r] = row >= 0 ? tok : -1;
         const __nv_bfloat16 *srcK = row >= 0 ? Kseq + row * p.k_tok_stride : Kseq;
         const uint32_t nbytes = row >= 0 ? 16u : 0u;
