@@ -30,6 +30,8 @@ _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
 _u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _int = ctypes.c_int
@@ -53,6 +55,10 @@ def load(path: str | None = None):
     lib.sfa_oracle_pool.argtypes = [_f32p, _i64, _int, _int, _f64p]
     lib.sfa_oracle_pool_cells.argtypes = [_f32p, _i64, _i32p, _i64, _int, _int, _f64p]
     lib.sfa_oracle_pool_cells.restype = _int
+    lib.sfa_oracle_quantize_q8_0.argtypes = [_f32p, _i64, _int, _i8p, _u16p]
+    lib.sfa_oracle_quantize_q8_0.restype = _int
+    lib.sfa_oracle_dequantize_q8_0.argtypes = [_i8p, _u16p, _i64, _int, _f32p]
+    lib.sfa_oracle_fp16_bits.argtypes = [_f32p, _i64, _u16p]
     lib.sfa_oracle_key_transform.argtypes = [_f64p, _i64, _int, _int, _int, _f32p, _f32p,
                                              ctypes.c_double, _int, ctypes.c_double, _int, _i64]
     lib.sfa_oracle_index_scores.argtypes = [_f32p, _f32p, _int, _int, _f64p, _i64, _f64p]
@@ -93,6 +99,42 @@ def pool_cells(X, cell_of, n_blk: int, cr: int, lib=None) -> np.ndarray:
     out = np.zeros((n_blk, X.shape[1]), np.float64)
     if lib.sfa_oracle_pool_cells(X, X.shape[0], cell_of, n_blk, X.shape[1], cr, out) != 0:
         raise ValueError("a cell map entry lies outside the cell array")
+    return out
+
+
+def quantize_q8_0(x, lib=None):
+    """q8_0 blocks of the rows of x[..., d] (d a multiple of 32): (codes int8 [..., d],
+    binary16 scale bits uint16 [..., d/32])."""
+    lib = lib or load()
+    x = _f32(x)
+    d = x.shape[-1]
+    assert d % 32 == 0
+    rows = x.reshape(-1, d)
+    q = np.zeros(rows.shape, np.int8)
+    s = np.zeros((rows.shape[0], d // 32), np.uint16)
+    if lib.sfa_oracle_quantize_q8_0(rows, rows.shape[0], d, q, s) != 0:
+        raise ValueError("a q8_0 scale overflows binary16")
+    return q.reshape(x.shape), s.reshape(x.shape[:-1] + (d // 32,))
+
+
+def dequantize_q8_0(q, scale, lib=None) -> np.ndarray:
+    """The values q8_0 codes stand for (float32 [..., d], exact)."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    d = q.shape[-1]
+    scale = np.ascontiguousarray(scale, dtype=np.uint16)
+    out = np.zeros(q.shape, np.float32)
+    lib.sfa_oracle_dequantize_q8_0(q.reshape(-1, d), scale.reshape(-1, d // 32),
+                                   q.size // d if d else 0, d, out.reshape(-1, d))
+    return out
+
+
+def fp16_bits(x, lib=None) -> np.ndarray:
+    """binary16 bits of each element of x (round to nearest, ties to even)."""
+    lib = lib or load()
+    x = _f32(x).reshape(-1)
+    out = np.zeros(x.shape, np.uint16)
+    lib.sfa_oracle_fp16_bits(x, x.shape[0], out)
     return out
 
 

@@ -115,6 +115,91 @@ void sfa_oracle_key_transform(double *kbar, int64_t n_blk, int d_idx, int cr, in
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* KV cache quantization, q8_0 [qwen4exp commit: the QSA attention path takes a quantized KV
+ * cache; the pages do not spell the format out, and q8_0 is the 8-bit block format of the
+ * llama.cpp caches they describe].  Each row of d elements (d a multiple of 32) is cut into
+ * blocks of 32 consecutive elements.  Per block:
+ *   amax = max_j |x_j|,  delta = amax / 127                        (binary32 division)
+ *   q_j  = x_j / delta rounded half away from zero, or 0 when delta = 0   (binary32)
+ *   the stored scale s = delta rounded to binary16 (nearest, ties to even)
+ * and the value a quantized element stands for is s * q_j.  The codes are taken with the
+ * unrounded delta; only the stored scale is binary16.                                     */
+
+/* binary16 bits of a finite or infinite float, rounded to nearest with ties to even (IEEE
+ * 754): subnormals in units of 2^-24, normals with a 10-bit fraction, overflow to infinity. */
+static uint16_t fp16_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);   /* NaN */
+    const double a = fabs((double)f);
+    if (a < 6.103515625e-05) {                       /* below 2^-14: subnormal or zero */
+        const double units = nearbyint(a * 16777216.0);   /* a / 2^-24, exact, then RNE */
+        return (uint16_t)(sign | (uint16_t)units);        /* 1024 units is 2^-14: 0x0400 */
+    }
+    int e;
+    const double m = frexp(a, &e);                   /* a = m * 2^e, 0.5 <= m < 1 */
+    double frac = nearbyint(ldexp(m, 11));           /* 1024 .. 2048 after rounding */
+    int E = e - 1 + 15;                              /* biased binary16 exponent */
+    if (frac == 2048.0) {
+        frac = 1024.0;
+        E += 1;
+    }
+    if (E >= 31) return (uint16_t)(sign | 0x7C00u);  /* infinity */
+    return (uint16_t)(sign | (uint16_t)(E << 10) | (uint16_t)((int)frac - 1024));
+}
+
+/* The value of binary16 bits (IEEE 754). */
+static float fp16_value(uint16_t h)
+{
+    const int E = (h >> 10) & 0x1F, M = h & 0x3FF;
+    double v;
+    if (E == 0) v = ldexp((double)M, -24);
+    else if (E == 31) v = M ? NAN : INFINITY;
+    else v = ldexp((double)(M | 0x400), E - 25);
+    return (float)((h & 0x8000u) ? -v : v);
+}
+
+/* x[n_rows][d] -> codes q[n_rows][d] and scale bits[n_rows][d/32].  Returns -1 when a scale
+ * overflows binary16 (amax above ~8.3e6), else 0.                                          */
+int sfa_oracle_quantize_q8_0(const float *x, int64_t n_rows, int d, int8_t *q, uint16_t *scale)
+{
+    int rc = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        for (int b = 0; b < d / 32; ++b) {
+            const float *xb = x + i * d + b * 32;
+            int8_t *qb = q + i * d + b * 32;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j)
+                if (fabsf(xb[j]) > amax) amax = fabsf(xb[j]);
+            const float delta = amax / 127.0f;
+            for (int j = 0; j < 32; ++j)
+                qb[j] = delta == 0.0f ? 0 : (int8_t)roundf(xb[j] / delta);
+            const uint16_t sb = fp16_bits(delta);
+            scale[i * (d / 32) + b] = sb;
+            if ((sb & 0x7FFFu) == 0x7C00u) rc = -1;
+        }
+    }
+    return rc;
+}
+
+/* The values the codes stand for: out[i][j] = s(i, j / 32) * q[i][j] (exact in binary32).  */
+void sfa_oracle_dequantize_q8_0(const int8_t *q, const uint16_t *scale, int64_t n_rows, int d,
+                                float *out)
+{
+    for (int64_t i = 0; i < n_rows; ++i)
+        for (int j = 0; j < d; ++j)
+            out[i * d + j] = fp16_value(scale[i * (d / 32) + j / 32]) * (float)q[i * d + j];
+}
+
+/* binary16 bits of each float (exposed so the conversion can be checked on its own).       */
+void sfa_oracle_fp16_bits(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = fp16_bits(x[i]);
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Step 2 -- indexer score of every complete block [QSA, ReLU paragraph].
  *   s_b = sum_j w_j * max(0, q_j . kbar_b)
  * q_idx is [h_idx][d_idx] for one query token, w is [h_idx].                              */

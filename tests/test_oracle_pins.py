@@ -82,6 +82,57 @@ def pin_pool_cells(lib):
         oracle.pool_cells(X, [2, 0, 4, 1], 2, 2, lib=lib)
 
 
+# ----------------------------------------------------------------------- q8_0 KV blocks
+def pin_q8_0(lib):
+    # Worked example: amax 127 gives delta = 1 exactly; codes round half away from zero.
+    x = np.zeros((1, 64), np.float32)
+    x[0, :7] = [127, 0.5, -0.5, 1.5, -2.5, 2.49, -126.5]
+    q, s = oracle.quantize_q8_0(x, lib=lib)
+    assert q[0, :7].tolist() == [127, 1, -1, 2, -3, 2, -127] and not q[0, 7:].any()
+    assert s.tolist() == [[0x3C00, 0x0000]]                # 1.0; the all-zero block has scale 0
+    assert oracle.dequantize_q8_0(q, s, lib=lib)[0, :7].tolist() == [127, 1, -1, 2, -3, 2, -127]
+    # Codes are taken with the unrounded delta.  amax = 127 (1 + 2^-12) gives delta = 1 + 2^-12,
+    # stored as binary16 1.0; x = 2.5 + 2^-11 is 2.4999 deltas (code 2), but 2.5005 stored scales.
+    y = np.zeros((1, 32), np.float32)
+    y[0, 0], y[0, 1] = 127 * (1 + 2.0 ** -12), 2.5 + 2.0 ** -11
+    q, s = oracle.quantize_q8_0(y, lib=lib)
+    assert q[0, :2].tolist() == [127, 2] and s[0, 0] == 0x3C00
+    # Scales that fall exactly between two binary16 values round to the even one.
+    for delta, bits in [(1 + 2.0 ** -11, 0x3C00), (1 + 3 * 2.0 ** -11, 0x3C02),
+                        (2.0 ** -24 * 1.5, 0x0002), (2.0 ** -24 * 2.5, 0x0002)]:
+        z = np.zeros((1, 32), np.float32)
+        z[0, 0] = 127 * delta
+        assert np.float32(z[0, 0]) / np.float32(127) == np.float32(delta)
+        assert oracle.quantize_q8_0(z, lib=lib)[1][0, 0] == bits, delta
+    # Values on the code grid come back exactly: x = k * 2^-3, one |k| = 127 per block.
+    k = _rng(50).integers(-127, 128, (20, 96))
+    k[:, ::32] = 127 * np.sign(k[:, ::32] + 0.5).astype(np.int64)
+    g = (k * 0.125).astype(np.float32)
+    q, s = oracle.quantize_q8_0(g, lib=lib)
+    assert np.array_equal(q, k) and np.all(s == 0x3000)      # 2^-3
+    assert np.array_equal(oracle.dequantize_q8_0(q, s, lib=lib), g)
+    # binary16 rounding of the scale against numpy's conversion, over many binades
+    r = _rng(51)
+    v = (r.standard_normal(50000) * 10.0 ** r.integers(-10, 6, 50000)).astype(np.float32)
+    with np.errstate(over="ignore"):                          # large values go to infinity
+        want = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.fp16_bits(v, lib=lib), want)
+    # Error bound on random rows: |s q - x| <= delta / 2 (rounding of the code, plus the binary32
+    # division) + 127 |s - delta| (the binary16 scale).
+    X = (r.standard_normal((300, 128)) * 10.0 ** r.integers(-6, 5, (300, 1))).astype(np.float32)
+    q, s = oracle.quantize_q8_0(X, lib=lib)
+    assert np.abs(q.astype(np.int64)).max() <= 127
+    xb = X.astype(np.float64).reshape(300, 4, 32)
+    delta = (np.float32(1) * np.abs(X).reshape(300, 4, 32).max(-1) / np.float32(127)).astype(np.float64)
+    sv = s.view(np.float16).astype(np.float64)
+    err = np.abs(oracle.dequantize_q8_0(q, s, lib=lib).astype(np.float64).reshape(300, 4, 32) - xb)
+    bound = delta * 0.5 * (1 + 2.0 ** -20) + 127 * np.abs(sv - delta)
+    assert np.all(err <= bound[..., None])
+    # a scale that overflows binary16 is an error
+    with pytest.raises(ValueError):
+        oracle.quantize_q8_0(np.full((1, 32), 1e7, np.float32), lib=lib)
+
+
 # -------------------------------------------------------------------------------- score
 def pin_scores(lib):
     g = _golden("qsa_tiny_relu.json")
@@ -396,7 +447,7 @@ def pin_key_transform(lib):
     assert not np.allclose(both, rot_first, rtol=1e-6)
 
 
-PINS = [pin_pool_closed_forms, pin_pool_cells, pin_scores, pin_select, pin_token_expanded, pin_mask,
+PINS = [pin_pool_closed_forms, pin_pool_cells, pin_q8_0, pin_scores, pin_select, pin_token_expanded, pin_mask,
         pin_attend, pin_pipeline, pin_key_transform]
 
 
@@ -417,6 +468,12 @@ MUTANTS = {
                             "X[(b * cr + t + 1) * (int64_t)d_idx + d]"),
     "cell_map_ignored": ("sum += (double)X[(int64_t)cell_of[b * cr + t] * d_idx + d];",
                          "sum += (double)X[(b * cr + t) * (int64_t)d_idx + d];"),
+    "q8_truncated_codes": ("qb[j] = delta == 0.0f ? 0 : (int8_t)roundf(xb[j] / delta);",
+                           "qb[j] = delta == 0.0f ? 0 : (int8_t)truncf(xb[j] / delta);"),
+    "q8_codes_from_stored_scale": ("qb[j] = delta == 0.0f ? 0 : (int8_t)roundf(xb[j] / delta);",
+                                   "qb[j] = delta == 0.0f ? 0 : (int8_t)roundf(xb[j] / fp16_value(fp16_bits(delta)));"),
+    "q8_amax_over_128": ("const float delta = amax / 127.0f;", "const float delta = amax / 128.0f;"),
+    "fp16_ties_away": ("double frac = nearbyint(ldexp(m, 11));", "double frac = round(ldexp(m, 11));"),
     "scale_dropped": ("logit[t] = scale * dot;", "logit[t] = dot;"),
     "wrong_kv_head": ("const int g = h / group;", "const int g = h % h_kv;"),
     "weight_outside_relu": ("s += (double)w[j] * relu;", "s += relu;"),
