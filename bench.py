@@ -38,6 +38,8 @@ METRIC = "sparse-attn tokens/s (decode, pp2048) at depth; gathered-KV HBM GB/s v
 DEFAULT_WORKLOAD = "decode_32x131072"
 SECOND_WORKLOAD = "pp2048_131072"
 PAGE_CELLS = 64
+Q8_CACHE = ("q8_0 rows (blocks of 32 int8 codes with a binary16 scale; 624 B per 576-wide row), "
+            "attention on binary16 tensor-core operands")
 PAGED_LAYOUT = (f"paged: {PAGE_CELLS}-cell pages dealt from a seeded shuffled page table, "
                 "one spare page per sequence")
 L2_FLUSH_BYTES = 512 << 20
@@ -72,7 +74,7 @@ def recorded_traffic(kernel, workload):
 
 
 # ------------------------------------------------------------------ algorithmic work per step
-def algorithmic(w, attended, bounded=False):
+def algorithmic(w, attended, bounded=False, kv="bf16"):
     """Bytes / FLOPs each stage must move / do for one step of workload w (one rank).
 
     attended[i] = |A_i|, the number of cells query i attends (kept blocks * cr + tail).
@@ -82,7 +84,10 @@ def algorithmic(w, attended, bounded=False):
     """
     cr = w.compress_ratio
     nb = [(w.depth + j + 1) // cr for j in range(w.n_q_per_seq)] * w.n_seq
-    kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
+    if kv == "q8_0":   # q8_0 cache rows: codes, binary16 scales, padding
+        kv_row = w.h_kv * (B.sfa_q8_0_row_bytes(w.dkq) + (0 if w.v_is_k else B.sfa_q8_0_row_bytes(w.dv)))
+    else:
+        kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
     # bounded selection: the hi halves and the 4-byte bound factor of each block only
     per_blk = (2 * w.d_idx + 4) if bounded else 4 * w.d_idx
     if w.kind == "decode":
@@ -171,22 +176,30 @@ class ClockSampler:
 class Workbench:
     """Inputs, buffers and one step of the method for workload w on the current device."""
 
-    def __init__(self, w, dev, bounded=None, paged=False):
-        self.w, self.dev, self.paged = w, dev, paged
+    def __init__(self, w, dev, bounded=None, paged=False, kv="bf16"):
+        self.w, self.dev, self.paged, self.kv = w, dev, paged, kv
         self.case = sfa.make_case(w, device=dev)
         self.n_blk_max = w.n_tok // w.compress_ratio
+        # the drawn bf16 rows, per sequence: the host source of the end-to-end step's new rows
+        self.seq_rows = {n: self.case[n] for n in ("X", "K", "V") if self.case[n] is not None}
+        if kv == "q8_0":   # K and V as q8_0 cache rows (the index keys X stay bf16)
+            for n in ("K", "V"):
+                t = self.case[n]
+                if t is not None:
+                    rb = B.sfa_q8_0_row_bytes(t.shape[-1])
+                    y = torch.empty(t.shape[:-1] + (rb,), dtype=torch.uint8, device=dev)
+                    B.sfa_quantize_kv_q8_0(t.view(t.shape[0], -1, t.shape[-1]),
+                                           y.view(t.shape[0], -1, rb))
+                    self.case[n] = y
         self.cell_of = None
         if paged:
             # a paged cache: the same rows in 64-cell pages dealt from a seeded shuffled page
-            # table (one spare page per sequence); the per-sequence copies stay as the host
-            # source of the end-to-end step's new rows
+            # table (one spare page per sequence)
             self.cell_of, n_cells = sfa.make_cell_map(w.n_seq, w.n_tok, page=PAGE_CELLS,
                                                       spare_pages=w.n_seq, seed=w.seed,
                                                       device=dev)
-            self.seq_rows = {}
             for n in ("X", "K", "V"):
                 if self.case[n] is not None:
-                    self.seq_rows[n] = self.case[n]
                     self.case[n] = sfa.to_cells(self.case[n], self.cell_of, n_cells)
         self.step = sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q,
                                 h_kv=w.h_kv, dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
@@ -213,8 +226,9 @@ class Workbench:
             n_kv = w.indexer_top_k * w.compress_ratio + w.compress_ratio - 1
         else:
             n_kv = st.n_kv_dense
-        n += B.sfa_attend_plan(B.SFA_BF16, w.n_q, w.h_kv, w.dkq, not w.v_is_k, n_kv,
-                               w.compress_ratio, st.dense)[1]
+        dt = B.SFA_Q8_0 if self.kv == "q8_0" else B.SFA_BF16
+        n += B.sfa_attend_plan(dt, w.n_q, w.h_kv, w.dkq, not w.v_is_k, n_kv, w.compress_ratio,
+                               st.dense)[1]
         return n
 
     def run_step(self, events=None):
@@ -312,12 +326,17 @@ def measure_e2e(wb, steps, warmup):
     are then placed into the caches by device copies."""
     c, w = wb.case, wb.w
     sl = slice(w.depth, w.n_tok)   # the step's new cache rows (positions depth .. n_tok - 1)
-    rows = wb.seq_rows if wb.paged else c
-    new_rows = {"K": rows["K"][:, sl], "X": rows["X"][:, sl]}
-    if c["V"] is not None:
-        new_rows["V"] = rows["V"][:, sl]
+    new_rows = {n: t[:, sl] for n, t in wb.seq_rows.items()}   # bf16, from the host
     # paged: the new rows go to their cells (the page table is known before the step)
     new_cells = wb.cell_of[:, sl].reshape(-1).long() if wb.paged else None
+    # q8_0 caches: the new K / V rows are quantized on the device into a staging slice first
+    staging = {}
+    if wb.kv == "q8_0":
+        for n in ("K", "V"):
+            if n in new_rows:
+                t = new_rows[n]
+                rb = B.sfa_q8_0_row_bytes(t.shape[-1])
+                staging[n] = torch.empty(t.shape[:-1] + (rb,), dtype=torch.uint8, device=t.device)
     names = ["Q", "q_idx", "w", "q_seq", "q_pos"]
     parts = {n: c[n] for n in names}
     parts.update({f"{n}_new": t for n, t in new_rows.items()})
@@ -340,11 +359,16 @@ def measure_e2e(wb, steps, warmup):
 
     def one():
         dev_arena.copy_(host_arena, non_blocking=True)
-        for n, dst in new_rows.items():
+        for n in new_rows:
+            src = dv[f"{n}_new"]
+            if n in staging:
+                stg = staging[n]
+                B.sfa_quantize_kv_q8_0(src.view(src.shape[0], -1, src.shape[-1]),
+                                       stg.view(stg.shape[0], -1, stg.shape[-1]))
+                src = stg
             if new_cells is None:
-                dst.copy_(dv[f"{n}_new"])
+                c[n][:, sl].copy_(src)
             else:
-                src = dv[f"{n}_new"]
                 c[n].index_copy_(0, new_cells, src.reshape((-1,) + tuple(c[n].shape[1:])))
         wb.run_step()
         out.copy_(wb.step.O, non_blocking=True)
@@ -469,6 +493,9 @@ def main():
     ap.add_argument("--paged", action="store_true",
                     help="time the paged cache layout (shuffled 64-cell pages) as the main line")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged companion line")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0"],
+                    help="KV cache type of the main line (q8_0: quantized rows)")
+    ap.add_argument("--no-q8", action="store_true", help="skip the q8_0-cache companion line")
     ap.add_argument("--depth", type=int, default=0,
                     help="override the cache depth (smaller runs for ncu captures)")
     args = ap.parse_args()
@@ -504,7 +531,7 @@ def main():
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
              torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
-    wb = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged)
+    wb = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged, kv=args.kv)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -523,7 +550,7 @@ def main():
     tail = [(int(p) + 1) % w.compress_ratio for p in wb.case["q_pos"].cpu()]
     attended = [int(n) * w.compress_ratio + t for n, t in zip(n_sel, tail)] if not wb.step.dense \
         else [int(p) + 1 for p in wb.case["q_pos"].cpu()]
-    alg = algorithmic(w, attended, wb.step.bounded)
+    alg = algorithmic(w, attended, wb.step.bounded, kv=args.kv)
     kernels = {}
     for name, ms in stage_ms.items():
         if ms <= 0 or (name == "pool" and wb.new_blocks[1] <= wb.new_blocks[0]):
@@ -577,7 +604,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.kv == "bf16" else "f16 (q8_0 KV)",
             "data": "synthetic (seeded N(0,1) K/Q/index keys, U(0,1) head weights)",
             "config": {"workload": w.name, "kind": w.kind, "n_seq": w.n_seq,
                        "queries_per_step": w.n_q, "depth": w.depth, "h_q": w.h_q,
@@ -586,6 +614,7 @@ def main():
                        "indexer_top_k": w.indexer_top_k,
                        "selection": "bounded" if wb.step.bounded else "exact",
                        "cache_layout": PAGED_LAYOUT if wb.paged else "contiguous per sequence",
+                       "kv_cache": Q8_CACHE if args.kv == "q8_0" else "bf16",
                        "l2": "flushed before every timed "
                        "step outside the timed events (512 MB written, then 256 MB of another "
                        "buffer read)"},
@@ -604,13 +633,13 @@ def main():
         cn = [int(x) for x in cn if int(x) >= 0]
         line["bounded_selection"] = {"candidates_per_query_mean": (sum(cn) / len(cn)) if cn else 0,
                                      "candidates_per_query_max": max(cn) if cn else 0}
-    wb_sel = (wb.step.n_sel.clone(), wb.step.O.clone())
+    wb_sel = (wb.step.n_sel.clone(), wb.step.O.clone(), wb.step.blk_idx.clone())
     del wb
     torch.cuda.empty_cache()
 
     if not args.no_paged and not args.paged and rank == 0 and world == 1:
         # the same workload on a paged cache: the pool and the attention read through the map
-        wbp = Workbench(w, dev, bounded=False if args.exact else None, paged=True)
+        wbp = Workbench(w, dev, bounded=False if args.exact else None, paged=True, kv=args.kv)
         sp, _ = measure(wbp, max(3, args.steps // 2), 3, flush, per_stage=False)
         _, stp = measure(wbp, 3, 3, flush, per_stage=True)
         msp = sum(sp) / len(sp)
@@ -620,6 +649,27 @@ def main():
                          "same_output_as_contiguous": same,
                          "device_status": B.sfa_read_device_status(wbp.step.status)}
         del wbp
+        torch.cuda.empty_cache()
+
+    if not args.no_q8 and args.kv == "bf16" and rank == 0 and world == 1:
+        # the same workload on q8_0 K/V caches: the attention gathers the quantized rows
+        wbq = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged, kv="q8_0")
+        sq, _ = measure(wbq, max(3, args.steps // 2), 3, flush, per_stage=False)
+        _, stq = measure(wbq, 3, 3, flush, per_stage=True)
+        msq = sum(sq) / len(sq)
+        aq = algorithmic(w, attended, wbq.step.bounded, kv="q8_0")
+        same = bool(torch.equal(wbq.step.n_sel, wb_sel[0]) and torch.equal(wbq.step.blk_idx, wb_sel[2]))
+        ref = wb_sel[1]
+        dev_rel = ((wbq.step.O - ref).abs().amax(-1) / ref.abs().amax(-1).clamp_min(1e-30)).max()
+        att_ms = stq.get("attend", 0.0)
+        line["kv_q8_0"] = {"kv_cache": Q8_CACHE, "value": w.n_q / (msq / 1000.0),
+                           "unit": "tokens/s", "ms_per_step": msq, "stage_ms": stq,
+                           "gathered_kv_bytes": aq["gathered_kv_bytes"],
+                           "gathered_kv_GBps": aq["gathered_kv_bytes"] / (att_ms * 1e6) if att_ms else None,
+                           "same_selection_as_bf16": same,
+                           "max_rel_diff_vs_bf16_cache": float(dev_rel),
+                           "device_status": B.sfa_read_device_status(wbq.step.status)}
+        del wbq
         torch.cuda.empty_cache()
 
     if not args.no_second and rank == 0 and world == 1:

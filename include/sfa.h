@@ -52,7 +52,9 @@ enum sfa_status {
     SFA_ERR_WORKSPACE = 4    /* the workspace is NULL or smaller than the size query says  */
 };
 
-enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
+/* SFA_Q8_0: K and V are q8_0 cache rows (sfa_quantize_kv_q8_0) and Q is bf16; the attention
+ * then runs its tensor-core products on binary16 operands.                                 */
+enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1, SFA_Q8_0 = 2 };
 
 /* bits of the device status word */
 #define SFA_DEV_BAD_BLOCK 0x1 /* a selected block id outside [0, B_i) or not ascending      */
@@ -63,6 +65,9 @@ enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1 };
                                  released its resources and returned early                */
 #define SFA_DEV_BAD_CELL 0x10 /* a paged cell map entry outside [0, n_cells): that position
                                  reads as a zero row (pool) or is left out (attention)    */
+#define SFA_DEV_FP16_RANGE 0x20 /* quantized-cache path: a value beyond binary16's range (a
+                                 q8_0 scale, a query element or a dequantized K/V value);
+                                 the results that involve it are not finite              */
 
 /*
  * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, taken
@@ -303,6 +308,39 @@ int sfa_dense_attend_paged(const void *Q, const void *K, const void *V, int dtyp
                            const int32_t *q_seq, const int32_t *q_pos, int64_t n_kv_max, float *O,
                            float *lse, void *workspace, size_t workspace_bytes,
                            int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * Quantized KV cache (q8_0).  The qwen4exp commits let the QSA attention path read a quantized
+ * KV cache; q8_0 is the 8-bit block format of the llama.cpp caches they describe.  Each row of
+ * d elements (one token and KV head of K, or of V) is cut into blocks of 32; per block
+ *   delta = max |x| / 127 (binary32), code_j = x_j / delta rounded half away from zero
+ *   (binary32; 0 when delta = 0), scale = delta rounded to binary16 (ties to even),
+ * and the element stands for scale * code_j.  A cache row holds the d int8 codes, then the
+ * d/32 binary16 scales, then zero bytes up to sfa_q8_0_row_bytes(d) (a multiple of 16):
+ * 624 bytes for d = 576, 544 for 512, 144 for 128, 80 for 64.  With V = NULL the values are the
+ * first dv elements of K: the first dv codes and dv/32 scales of the K row.
+ *
+ * sfa_quantize_kv_q8_0 writes such rows: for o < n_outer and i < n_inner, the d elements at
+ * X + o*x_outer_stride + i*d (elements of x_dtype) go to the row at
+ * Y + o*y_outer_stride + i*sfa_q8_0_row_bytes(d) (bytes), so a slice of new tokens of every
+ * sequence is one call.  d in {64, 128, 512, 576}.  A scale beyond binary16 sets
+ * SFA_DEV_FP16_RANGE (inputs must be finite).  The codes and scales equal the rule above bit for
+ * bit.
+ *
+ * The attention entry points (gathered, dense, paged) take dtype = SFA_Q8_0: K is
+ * [n_seq][n_tok_cap][h_kv][row_bytes(dkq)] (or [n_cells][h_kv][row_bytes(dkq)] paged) and V the
+ * same with dv, or NULL; Q is bf16.  The kernel gathers the quantized rows (about half the
+ * bytes of bf16 rows), dequantizes each tile in shared memory to binary16, converts Q to
+ * binary16, and runs S = Q K^T and O = P V on binary16 tensor-core operands with fp32
+ * accumulation (P as binary16 hi + lo halves).  The dequantized values have up to 19
+ * significant bits, so binary16 (11) keeps the outputs within the 2e-3 bf16 tolerance where
+ * bf16 (8) would not.  A query element or a dequantized value beyond binary16's range sets
+ * SFA_DEV_FP16_RANGE.  Limits: those of the bf16 kernel.
+ */
+size_t sfa_q8_0_row_bytes(int d);
+int sfa_quantize_kv_q8_0(const void *X, int x_dtype, int64_t n_outer, int64_t n_inner, int d,
+                         int64_t x_outer_stride, void *Y, int64_t y_outer_stride,
+                         int32_t *dev_status, sfa_stream_t stream);
 
 /*
  * sfa_gather_attend_noalloc -- sfa_gather_attend for callers that cannot allocate device

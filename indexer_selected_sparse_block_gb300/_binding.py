@@ -17,9 +17,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsfa.so")
 
 SFA_OK, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA, SFA_ERR_WORKSPACE = range(5)
-SFA_BF16, SFA_F32 = 0, 1
+SFA_BF16, SFA_F32, SFA_Q8_0 = 0, 1, 2
 SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT = 1, 2, 4, 8
-SFA_DEV_BAD_CELL = 16
+SFA_DEV_BAD_CELL, SFA_DEV_FP16_RANGE = 16, 32
 SFA_REFINE_MAX_BLOCKS = 36864   # longest row sfa_topk_blocks_refine takes (one selection piece)
 
 _lib = None
@@ -62,6 +62,8 @@ SIGNATURES = {
     "sfa_dense_attend_paged": (_int, [_vp, _vp, _vp, _int, _i64, _vp, _int, _i64, _int, _int,
                                       _int, _int, _int, _f32, _vp, _vp, _i64, _vp, _vp, _vp, _sz,
                                       _vp, _vp]),
+    "sfa_q8_0_row_bytes": (_sz, [_int]),
+    "sfa_quantize_kv_q8_0": (_int, [_vp, _int, _i64, _i64, _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
     "sfa_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -117,6 +119,8 @@ def _dtype_code(t) -> int:
         return SFA_BF16
     if t.dtype == torch.float32:
         return SFA_F32
+    if t.dtype == torch.uint8:   # q8_0 cache rows
+        return SFA_Q8_0
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
@@ -234,14 +238,21 @@ def sfa_attend_plan(dtype_code: int, n_q: int, h_kv: int, dkq: int, has_v: bool,
     return ns.value, nk.value
 
 
+def _check_qkv(Q, K, V):
+    if V is not None and K.dtype != V.dtype:
+        raise ValueError("K and V must share a dtype")
+    if K.dtype == torch.uint8:   # q8_0 cache rows: Q stays bf16
+        if Q.dtype != torch.bfloat16:
+            raise ValueError("a q8_0 cache takes a bf16 Q")
+    elif Q.dtype != K.dtype:
+        raise ValueError("Q and K must share a dtype")
+
+
 def _attn_dims(Q, K, V, O):
     n_q, h_q, dkq = Q.shape
     n_seq, n_tok_cap, h_kv, _ = K.shape
     dv = O.shape[-1]
-    if V is not None and K.dtype != V.dtype:
-        raise ValueError("K and V must share a dtype")
-    if Q.dtype != K.dtype:
-        raise ValueError("Q and K must share a dtype")
+    _check_qkv(Q, K, V)
     return n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv
 
 
@@ -315,10 +326,9 @@ def sfa_pool_index_keys_paged(X, cell_of, compress_ratio: int, blk_begin: int, b
 def _paged_attn_dims(Q, K, V, O, cell_of):
     n_q, h_q, dkq = Q.shape
     n_cells, h_kv, _ = K.shape
-    if V is not None and (K.dtype != V.dtype or V.shape[0] != n_cells):
-        raise ValueError("V must share K's dtype and cell count")
-    if Q.dtype != K.dtype:
-        raise ValueError("Q and K must share a dtype")
+    if V is not None and V.shape[0] != n_cells:
+        raise ValueError("V must have K's cell count")
+    _check_qkv(Q, K, V)
     n_seq, n_pos_cap, _ = _paged_dims(cell_of, n_cells)
     return n_q, h_q, dkq, n_cells, n_seq, n_pos_cap, h_kv, O.shape[-1]
 
@@ -355,6 +365,26 @@ def sfa_dense_attend_paged(Q, K, V, cell_of, q_seq, q_pos, n_kv_max: int, scale:
                                       _p(q_seq), _p(q_pos), n_kv_max, _p(O), _p(lse),
                                       _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_dense_attend_paged", rc)
+
+
+def sfa_q8_0_row_bytes(d: int) -> int:
+    """Bytes of one q8_0 cache row of d elements (codes, binary16 scales, padding to 16)."""
+    return int(lib().sfa_q8_0_row_bytes(d))
+
+
+def sfa_quantize_kv_q8_0(X, Y, dev_status=None, stream=None):
+    """q8_0 rows of X [n_outer][n_inner][d] (bf16/f32) into Y [n_outer][n_inner][row_bytes(d)]
+    uint8; within an outer index the rows of both are contiguous (a cache slice of new tokens of
+    every sequence viewed as [n_seq][tokens * h_kv][d])."""
+    n_outer, n_inner, d = X.shape
+    rb = sfa_q8_0_row_bytes(d)
+    if Y.dtype != torch.uint8 or tuple(Y.shape) != (n_outer, n_inner, rb):
+        raise ValueError(f"Y must be uint8 [{n_outer}][{n_inner}][{rb}]")
+    if (X.stride(2), Y.stride(2)) != (1, 1) or (n_inner > 1 and (X.stride(1), Y.stride(1)) != (d, rb)):
+        raise ValueError("rows must be contiguous within an outer index")
+    rc = lib().sfa_quantize_kv_q8_0(_p(X), _dtype_code(X), n_outer, n_inner, d, X.stride(0), _p(Y),
+                                    Y.stride(0), _p(dev_status), _stream(stream))
+    _check("sfa_quantize_kv_q8_0", rc)
 
 
 def sfa_read_device_status(dev_status, stream=None) -> int:

@@ -27,6 +27,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -187,20 +188,77 @@ __device__ void cluster_merge(const AttnParams &p, float *sPart, float *sL, floa
     cl.sync();   // no CTA leaves while another may still read its shared memory
 }
 
-template <int DKQ, int DV, bool V_IS_K>
-__global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnParams p) {
+// m16n8k16 MMA, packing and rounding of the 16-bit operand type: bf16, or binary16 (F16).
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (F16) mma_f16_16816(d, a, b0, b1);
+    else mma_bf16_16816(d, a, b0, b1);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+    if constexpr (F16) return pack_f16(lo, hi);
+    else return pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float round16(float x) {
+    if constexpr (F16) return __half2float(__float2half_rn(x));
+    else return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Dequantizes kT q8_0 rows of D elements (pitch SROW bytes: D codes, then D/32 binary16 scales)
+// into binary16 rows of the swizzled tile layout (pitch 2*D bytes): element j of a row is
+// scale(j / 32) * code_j, exact in fp32, then rounded to binary16.  Zero-filled rows (padding)
+// give zeros.  Returns false when a value exceeds binary16's range.
+template <int D, int SROW>
+__device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, int tid) {
+    constexpr int C8 = D / 8;   // 8-element chunks per row
+    bool ok = true;
+    for (int e = tid; e < kT * C8; e += kThreads) {
+        const int r = e / C8, c = e - r * C8;
+        const uint8_t *row = src + r * SROW;
+        const uint2 w = *reinterpret_cast<const uint2 *>(row + c * 8);
+        const float sc = __half2float(*reinterpret_cast<const __half *>(row + D + (c >> 2) * 2));
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[k] = sc * (float)(int8_t)(w.x >> (8 * k));
+            v[4 + k] = sc * (float)(int8_t)(w.y >> (8 * k));
+        }
+        if (fabsf(sc) * 127.f >= 65520.f) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ok &= fabsf(v[k]) < 65520.f;
+        }
+        *reinterpret_cast<uint4 *>(dst + r * (2 * D) + swz(c, r) * 16) =
+            make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
+                       pack_f16(v[6], v[7]));
+    }
+    return ok;
+}
+
+// Gathered attention on warp-level MMAs: the body of attend_bf16_kernel (bf16 K/V) and of
+// attend_q8_kernel (Q8: q8_0 K/V rows, gathered as such, dequantized per tile in shared memory
+// to binary16, with Q converted to binary16 and every tensor-core product on binary16).
+template <int DKQ, int DV, bool V_IS_K, bool Q8>
+__device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     constexpr int KROW = DKQ * 2;                 // bytes of a K row in shared memory
     constexpr int VROW = V_IS_K ? KROW : DV * 2;  // bytes of a V row
     constexpr int KCH = DKQ / 8, VCH = DV / 8;    // 16-byte chunks per row
     constexpr int KS = DKQ / 64;                  // k16 steps of S per warp
     constexpr int NTV = DV / 32;                  // n8 tiles of O per warp
     constexpr int SP_PITCH = kT + 8;              // fp32 S-partial row pitch
-    constexpr int P_PITCH = kT + 8;               // bf16 P row pitch
-    constexpr int STAGE_BYTES = kT * KROW + (V_IS_K ? 0 : kT * VROW);
+    constexpr int P_PITCH = kT + 8;               // 16-bit P row pitch
+    constexpr int QKROW = q8_row_bytes(DKQ), QVROW = q8_row_bytes(DV);   // q8_0 rows (Q8)
+    constexpr int STAGE_BYTES = Q8 ? kT * QKROW + (V_IS_K ? 0 : kT * QVROW)
+                                   : kT * KROW + (V_IS_K ? 0 : kT * VROW);
+    constexpr int DEQ_BYTES = Q8 ? kT * KROW + (V_IS_K ? 0 : kT * VROW) : 0;
+    using KElem = std::conditional_t<Q8, uint8_t, __nv_bfloat16>;   // element of a cache row
+    constexpr int KG = Q8 ? QKROW : DKQ, VG = Q8 ? QVROW : DV;       // its elements per row
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sStage = smem;                                              // stages x STAGE_BYTES
-    uint8_t *sQ = sStage + (size_t)p.stages * STAGE_BYTES;               // 16 x KROW
+    uint8_t *sDeq = sStage + (size_t)p.stages * STAGE_BYTES;             // Q8: DEQ_BYTES
+    uint8_t *sQ = sDeq + DEQ_BYTES;                                      // 16 x KROW
     float *sSP = reinterpret_cast<float *>(sQ + 16 * KROW);              // 4 x 16 x SP_PITCH
     __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(sSP + 4 * 16 * SP_PITCH);  // hi, lo
     float *sAlpha = reinterpret_cast<float *>(sP + 2 * 16 * P_PITCH);    // 16
@@ -264,11 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
     __syncthreads();
 
-    const __nv_bfloat16 *Kseq = reinterpret_cast<const __nv_bfloat16 *>(p.K) +
-                                (int64_t)L.seq * p.k_seq_stride + (int64_t)g * DKQ;
-    const __nv_bfloat16 *Vseq = V_IS_K ? Kseq
-                                       : reinterpret_cast<const __nv_bfloat16 *>(p.V) +
-                                             (int64_t)L.seq * p.v_seq_stride + (int64_t)g * DV;
+    const KElem *Kseq = reinterpret_cast<const KElem *>(p.K) + (int64_t)L.seq * p.k_seq_stride +
+                        (int64_t)g * KG;
+    const KElem *Vseq = V_IS_K ? Kseq
+                               : reinterpret_cast<const KElem *>(p.V) +
+                                     (int64_t)L.seq * p.v_seq_stride + (int64_t)g * VG;
     const int n_tiles = (j1 - j0 + kT - 1) / kT;
 
     // The token (and, paged, the map entry) of this thread's row is looked up one tile ahead
@@ -291,17 +349,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
         const int64_t row = p.cell_of && tok >= 0 ? checked_cell(p, nx_cell) : tok;
         lookup(t + 1);
         if (sub == 0) sTok[st * kT + r] = row >= 0 ? tok : -1;
-        const __nv_bfloat16 *srcK = row >= 0 ? Kseq + row * p.k_tok_stride : Kseq;
+        const KElem *srcK = row >= 0 ? Kseq + row * p.k_tok_stride : Kseq;
         const uint32_t nbytes = row >= 0 ? 16u : 0u;
-        const uint32_t rowK = smem_u32(dstK) + r * KROW;
-#pragma unroll 6
-        for (int c = sub; c < KCH; c += 4) cp_async16(rowK + swz(c, r) * 16, srcK + c * 8, nbytes);
-        if constexpr (!V_IS_K) {
-            const __nv_bfloat16 *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
-            const uint32_t rowV = smem_u32(dstK + kT * KROW) + r * VROW;
+        if constexpr (Q8) {   // the quantized rows as they are (the tile is dequantized later)
+            const uint32_t rowK = smem_u32(dstK) + r * QKROW;
 #pragma unroll 4
-            for (int c = sub; c < VCH; c += 4)
-                cp_async16(rowV + swz(c, r) * 16, srcV + c * 8, nbytes);
+            for (int c = sub; c < QKROW / 16; c += 4) cp_async16(rowK + c * 16, srcK + c * 16, nbytes);
+            if constexpr (!V_IS_K) {
+                const KElem *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
+                const uint32_t rowV = smem_u32(dstK + kT * QKROW) + r * QVROW;
+#pragma unroll 4
+                for (int c = sub; c < QVROW / 16; c += 4)
+                    cp_async16(rowV + c * 16, srcV + c * 16, nbytes);
+            }
+        } else {
+            const uint32_t rowK = smem_u32(dstK) + r * KROW;
+#pragma unroll 6
+            for (int c = sub; c < KCH; c += 4) cp_async16(rowK + swz(c, r) * 16, srcK + c * 8, nbytes);
+            if constexpr (!V_IS_K) {
+                const KElem *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
+                const uint32_t rowV = smem_u32(dstK + kT * KROW) + r * VROW;
+#pragma unroll 4
+                for (int c = sub; c < VCH; c += 4)
+                    cp_async16(rowV + swz(c, r) * 16, srcV + c * 8, nbytes);
+            }
         }
     };
 
@@ -315,6 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
     else if (p.stages == 3) cp_async_wait<2>();
     else cp_async_wait<3>();
     __syncthreads();
+    if constexpr (Q8) {   // Q to binary16 in place: this path's tensor-core operand type
+        bool ok = true;
+        for (int e = tid; e < 16 * KCH; e += kThreads) {
+            const int r = e / KCH, c = e % KCH;
+            uint4 *q4 = reinterpret_cast<uint4 *>(sQ + r * KROW + swz(c, r) * 16);
+            const uint4 u = *q4;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+                ok &= fabsf(lo) < 65520.f && fabsf(hi) < 65520.f;
+                h[k] = pack_f16(lo, hi);
+            }
+            *q4 = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+        __syncthreads();
+    }
 
     // Q fragments of this warp's head-dim slice (A operand, kept in registers)
     uint32_t qa[KS][4];
@@ -344,7 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
         cp_async_commit();
 
         const int st = t % p.stages;
-        const uint32_t kbase = smem_u32(sStage + (size_t)st * STAGE_BYTES);
+        if constexpr (Q8) {   // tile t from its q8_0 rows into the binary16 tile
+            const uint8_t *stg = sStage + (size_t)st * STAGE_BYTES;
+            bool ok = dequant_tile<DKQ, QKROW>(stg, sDeq, tid);
+            if constexpr (!V_IS_K) ok &= dequant_tile<DV, QVROW>(stg + kT * QKROW, sDeq + kT * KROW, tid);
+            if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+            __syncthreads();
+        }
+        const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
         const uint32_t vbase = V_IS_K ? kbase : kbase + kT * KROW;
 
         // ---- S partial over this warp's head-dim slice
@@ -361,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
                 const int c = kg * 2 + (mi & 1);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + n * KROW + swz(c, n) * 16, b0, b1, b2, b3);
-                mma_bf16_16816(acc[2 * np], qa[ks], b0, b1);
-                mma_bf16_16816(acc[2 * np + 1], qa[ks], b2, b3);
+                mma16816<Q8>(acc[2 * np], qa[ks], b0, b1);
+                mma16816<Q8>(acc[2 * np + 1], qa[ks], b2, b3);
             }
         }
         float *sp = sSP + warp * 16 * SP_PITCH;
@@ -397,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
-                ph[e] = __bfloat162float(__float2bfloat16_rn(pe));
+                ph[e] = round16<Q8>(pe);
                 pl[e] = pe - ph[e];
                 rs += pe;
             }
@@ -407,9 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
             l_run = l_run * alpha + rs;
             m_run = m_new;
             *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
-                make_uint2(pack_bf16(ph[0], ph[1]), pack_bf16(ph[2], ph[3]));
+                make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
             *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
-                make_uint2(pack_bf16(pl[0], pl[1]), pack_bf16(pl[2], pl[3]));
+                make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
             if ((tid & 7) == 0) sAlpha[row] = alpha;
         }
         __syncthreads();
@@ -438,10 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
                     const int c = (warp * (DV / 4)) / 8 + np * 2 + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(vbase + k * VROW + swz(c, k) * 16, b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * np], pa, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
-                    mma_bf16_16816(o[2 * np], pb, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pb, b2, b3);
+                    mma16816<Q8>(o[2 * np], pa, b0, b1);
+                    mma16816<Q8>(o[2 * np + 1], pa, b2, b3);
+                    mma16816<Q8>(o[2 * np], pb, b0, b1);
+                    mma16816<Q8>(o[2 * np + 1], pb, b2, b3);
                 }
             }
         }
@@ -497,6 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
             }
         }
     }
+}
+
+template <int DKQ, int DV, bool V_IS_K>
+__global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnParams p) {
+    attend_mma_body<DKQ, DV, V_IS_K, false>(p);
+}
+template <int DKQ, int DV, bool V_IS_K>
+__global__ void __launch_bounds__(kThreads, 1) attend_q8_kernel(const AttnParams p) {
+    attend_mma_body<DKQ, DV, V_IS_K, true>(p);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1230,26 +1336,36 @@ bool shape_supported(int dkq, int dv) {
            (dkq == 64 && dv == 64);
 }
 
-// Shared memory of one bf16 CTA: the K/V stages plus Q, the S partials, P (hi, lo), the
-// softmax statistics, the token ids and the block list of its split.
-template <int DKQ, int DV, bool VK>
+// The warp-level MMA attention kernel of a shape: bf16 K/V, or q8_0 K/V rows (Q8).
+template <int DKQ, int DV, bool VK, bool Q8>
+constexpr auto mma_kernel() {
+    if constexpr (Q8) return attend_q8_kernel<DKQ, DV, VK>;
+    else return attend_bf16_kernel<DKQ, DV, VK>;
+}
+
+// Shared memory of one CTA of that kernel: the K/V stages (Q8: quantized rows, plus one
+// binary16 tile), Q, the S partials, P (hi, lo), the softmax statistics, the token ids and the
+// block list of its split.  The layout is the kernel's (attend_mma_body).
+template <int DKQ, int DV, bool VK, bool Q8 = false>
 size_t bf16_smem(int stages, int blk_list) {
     constexpr int KROW = DKQ * 2, VROW = VK ? KROW : DV * 2;
-    constexpr int STAGE = kT * KROW + (VK ? 0 : kT * VROW);
-    return (size_t)stages * STAGE + 16 * KROW + 4 * 16 * (kT + 8) * 4 + 2 * 16 * (kT + 8) * 2 +
-           48 * 4 + (size_t)stages * kT * 4 + (size_t)blk_list * 4 + 16;
+    constexpr int QK = q8_row_bytes(DKQ), QV = q8_row_bytes(DV);
+    constexpr int STAGE = Q8 ? kT * QK + (VK ? 0 : kT * QV) : kT * KROW + (VK ? 0 : kT * VROW);
+    constexpr int DEQ = Q8 ? kT * KROW + (VK ? 0 : kT * VROW) : 0;
+    return (size_t)stages * STAGE + DEQ + 16 * KROW + 4 * 16 * (kT + 8) * 4 +
+           2 * 16 * (kT + 8) * 2 + 48 * 4 + (size_t)stages * kT * 4 + (size_t)blk_list * 4 + 16;
 }
 
 // Two CTAs per SM when two stages fit in half the shared memory (more warps to hide the
 // latency of each tile's dependent steps), else one CTA with up to four stages.
-template <int DKQ, int DV, bool VK>
+template <int DKQ, int DV, bool VK, bool Q8 = false>
 int bf16_per_sm(int blk_list) {
-    return bf16_smem<DKQ, DV, VK>(2, blk_list) <= 113 * 1024 ? 2 : 1;
+    return bf16_smem<DKQ, DV, VK, Q8>(2, blk_list) <= 113 * 1024 ? 2 : 1;
 }
 
-// Whether clusters of ns CTAs of the bf16 kernel (its shared memory for blk_list entries) can
-// be resident at all; asked once per (shape, ns, list size).
-template <int DKQ, int DV, bool VK>
+// Whether clusters of ns CTAs of the kernel (its shared memory for blk_list entries) can be
+// resident at all; asked once per (shape, ns, list size).
+template <int DKQ, int DV, bool VK, bool Q8 = false>
 bool bf16_clusters_fit(int ns, int blk_list) {
     static std::mutex mu;
     static int cache[9][4] = {};   // [ns][slot]: 0 unknown, 1 yes, 2 no (last four list sizes)
@@ -1258,12 +1374,12 @@ bool bf16_clusters_fit(int ns, int blk_list) {
     for (int k = 0; k < 4; ++k)
         if (cache[ns][k] && keys[ns][k] == blk_list) return cache[ns][k] == 1;
     int stages = 2;
-    if (bf16_per_sm<DKQ, DV, VK>(blk_list) == 1) {
+    if (bf16_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
         stages = 4;
-        while (stages > 2 && bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) --stages;
+        while (stages > 2 && bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
     }
-    const size_t smem = bf16_smem<DKQ, DV, VK>(stages, blk_list);
-    bool ok = allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>);
+    const size_t smem = bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list);
+    bool ok = allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>());
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(ns, 1, 1);
@@ -1277,7 +1393,7 @@ bool bf16_clusters_fit(int ns, int blk_list) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        ok = cudaOccupancyMaxActiveClusters(&n, attend_bf16_kernel<DKQ, DV, VK>, &cfg) ==
+        ok = cudaOccupancyMaxActiveClusters(&n, mma_kernel<DKQ, DV, VK, Q8>(), &cfg) ==
                  cudaSuccess && n > 0;
         cudaGetLastError();
     }
@@ -1288,26 +1404,26 @@ bool bf16_clusters_fit(int ns, int blk_list) {
     return ok;
 }
 
-template <int DKQ, int DV, bool VK>
+template <int DKQ, int DV, bool VK, bool Q8 = false>
 int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     int stages = 2;
-    if (bf16_per_sm<DKQ, DV, VK>(blk_list) == 1) {
+    if (bf16_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
         stages = 4;
-        while (stages > 2 && bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) --stages;
+        while (stages > 2 && bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
     }
-    if (bf16_smem<DKQ, DV, VK>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    if (bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
     AttnParams q = p;
     q.stages = stages;
-    const size_t smem = bf16_smem<DKQ, DV, VK>(stages, blk_list);
+    const size_t smem = bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list);
     static bool attr = false;
     if (!attr) {
-        if (!allow_max_dynamic_smem(attend_bf16_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
+        if (!allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>())) return SFA_ERR_CUDA;
         attr = true;
     }
     const cudaError_t e =
-        q.cluster_merge ? launch_pdl_cluster(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads),
+        q.cluster_merge ? launch_pdl_cluster(mma_kernel<DKQ, DV, VK, Q8>(), grid, dim3(kThreads),
                                              smem, st, q.n_split, q)
-                        : launch_pdl(attend_bf16_kernel<DKQ, DV, VK>, grid, dim3(kThreads), smem,
+                        : launch_pdl(mma_kernel<DKQ, DV, VK, Q8>(), grid, dim3(kThreads), smem,
                                      st, q);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1360,42 +1476,62 @@ struct AttendPlan {
     bool use_tc;
 };
 
+// The per-shape dispatch of the warp-level MMA kernel's helpers (dkq in {576, 512, 128, 64};
+// 576 only with V = K).
+template <bool Q8>
+int mma_per_sm(int dkq, bool has_v, int bl) {
+    if (dkq == 576) return bf16_per_sm<576, 512, true, Q8>(bl);
+    if (dkq == 512) return has_v ? bf16_per_sm<512, 512, false, Q8>(bl) : bf16_per_sm<512, 512, true, Q8>(bl);
+    if (dkq == 128) return has_v ? bf16_per_sm<128, 128, false, Q8>(bl) : bf16_per_sm<128, 128, true, Q8>(bl);
+    return has_v ? bf16_per_sm<64, 64, false, Q8>(bl) : bf16_per_sm<64, 64, true, Q8>(bl);
+}
+template <bool Q8>
+bool mma_clusters_fit(int dkq, bool has_v, int ns, int bl) {
+    if (dkq == 576) return bf16_clusters_fit<576, 512, true, Q8>(ns, bl);
+    if (dkq == 512) return has_v ? bf16_clusters_fit<512, 512, false, Q8>(ns, bl) : bf16_clusters_fit<512, 512, true, Q8>(ns, bl);
+    if (dkq == 128) return has_v ? bf16_clusters_fit<128, 128, false, Q8>(ns, bl) : bf16_clusters_fit<128, 128, true, Q8>(ns, bl);
+    return has_v ? bf16_clusters_fit<64, 64, false, Q8>(ns, bl) : bf16_clusters_fit<64, 64, true, Q8>(ns, bl);
+}
+template <bool Q8>
+int mma_launch(int dkq, bool has_v, const AttnParams &p, dim3 grid, cudaStream_t st, int bl) {
+    if (dkq == 576) return has_v ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true, Q8>(p, grid, st, bl);
+    if (dkq == 512) return has_v ? launch_bf16<512, 512, false, Q8>(p, grid, st, bl) : launch_bf16<512, 512, true, Q8>(p, grid, st, bl);
+    if (dkq == 128) return has_v ? launch_bf16<128, 128, false, Q8>(p, grid, st, bl) : launch_bf16<128, 128, true, Q8>(p, grid, st, bl);
+    return has_v ? launch_bf16<64, 64, false, Q8>(p, grid, st, bl) : launch_bf16<64, 64, true, Q8>(p, grid, st, bl);
+}
+
 AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, int64_t n_kv_max,
                             int cr, int dense, bool paged = false) {
     // bf16 inputs take the warp-level mma.sync kernel, which is the faster one on the decode
     // and prefill shapes measured; SFA_ATTEND_KERNEL=tcgen05 selects the tcgen05 kernel for the
     // 512-wide heads instead (same results within the same tolerances).  fp32 inputs take the
     // SIMT kernel.  The paged layout always takes the mma.sync kernel: the tcgen05 kernel's
-    // producers copy runs of four consecutive rows as one TMA box.
+    // producers copy runs of four consecutive rows as one TMA box.  q8_0 caches take the
+    // mma.sync kernel's quantized-cache variant.
     const int tc_tile = tc::kTT;
     AttendPlan ap{};
     const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && !paged && want_tcgen05();
     ap.use_tc = use_tc;
+    const bool q8 = dtype == SFA_Q8_0;
+    const bool mma = (dtype == SFA_BF16 && !use_tc) || q8;
     // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
     int per_sm = 1;
-    if (dtype == SFA_BF16 && !use_tc) {
+    if (mma) {
         const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
-        if (dkq == 576) per_sm = bf16_per_sm<576, 512, true>(bl_max);
-        else if (dkq == 512) per_sm = has_v ? bf16_per_sm<512, 512, false>(bl_max) : bf16_per_sm<512, 512, true>(bl_max);
-        else if (dkq == 128) per_sm = has_v ? bf16_per_sm<128, 128, false>(bl_max) : bf16_per_sm<128, 128, true>(bl_max);
-        else per_sm = has_v ? bf16_per_sm<64, 64, false>(bl_max) : bf16_per_sm<64, 64, true>(bl_max);
+        per_sm = q8 ? mma_per_sm<true>(dkq, has_v, bl_max) : mma_per_sm<false>(dkq, has_v, bl_max);
     }
     SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, use_tc ? tc_tile : kT);
     // bf16 decode-like plans of a few splits merge them inside a cluster (2, 4 or 8 CTAs)
     // instead of through a second kernel
     int cluster_ns = 0;
-    if (dtype == SFA_BF16 && !use_tc && sp.n_split >= 2 && sp.n_split <= 12) {
+    if (mma && sp.n_split >= 2 && sp.n_split <= 12) {
         const int ns = sp.n_split >= 6 ? 8 : (sp.n_split >= 3 ? 4 : 2);
         const int64_t tiles = (n_kv_max + kT - 1) / kT;
         const int64_t per = (tiles + ns - 1) / ns;
         const int bl = dense ? 0 : (int)(per * kT / cr + 2);
         bool fit = (int64_t)((tiles + per - 1) / per) == ns && bl <= kMaxBlkList;
-        if (fit) {
-            if (dkq == 576) fit = bf16_clusters_fit<576, 512, true>(ns, bl);
-            else if (dkq == 512) fit = has_v ? bf16_clusters_fit<512, 512, false>(ns, bl) : bf16_clusters_fit<512, 512, true>(ns, bl);
-            else if (dkq == 128) fit = has_v ? bf16_clusters_fit<128, 128, false>(ns, bl) : bf16_clusters_fit<128, 128, true>(ns, bl);
-            else fit = has_v ? bf16_clusters_fit<64, 64, false>(ns, bl) : bf16_clusters_fit<64, 64, true>(ns, bl);
-        }
+        if (fit) fit = q8 ? mma_clusters_fit<true>(dkq, has_v, ns, bl)
+                          : mma_clusters_fit<false>(dkq, has_v, ns, bl);
         if (fit) {
             cluster_ns = ns;
             sp.n_split = ns;
@@ -1414,7 +1550,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
                float *lse, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t st,
                const int32_t *cell_of = nullptr, int64_t n_cells = 0) {
     if (!Q || !K || !q_seq || !q_pos || !O) return SFA_ERR_INVALID_ARG;
-    if (dtype != SFA_BF16 && dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
+    if (dtype != SFA_BF16 && dtype != SFA_F32 && dtype != SFA_Q8_0) return SFA_ERR_INVALID_ARG;
     if (n_seq < 1 || n_tok_cap < 1 || n_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0)
         return SFA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return SFA_ERR_INVALID_ARG;
@@ -1440,9 +1576,12 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.Q = Q; p.K = K; p.V = V;
     p.q_seq = q_seq; p.q_pos = q_pos; p.blk_idx = blk_idx; p.n_sel = n_sel;
     p.O = O; p.lse = lse; p.status = status;
-    p.k_tok_stride = (int64_t)h_kv * dkq;
+    // strides in elements of the cache's type: bf16 / fp32 values, or bytes of q8_0 rows
+    const int64_t krow = dtype == SFA_Q8_0 ? q8_row_bytes(dkq) : dkq;
+    const int64_t vrow = dtype == SFA_Q8_0 ? q8_row_bytes(dv) : dv;
+    p.k_tok_stride = (int64_t)h_kv * krow;
     p.k_seq_stride = n_tok_cap * p.k_tok_stride;
-    p.v_tok_stride = V ? (int64_t)h_kv * dv : p.k_tok_stride;
+    p.v_tok_stride = V ? (int64_t)h_kv * vrow : p.k_tok_stride;
     p.v_seq_stride = V ? n_tok_cap * p.v_tok_stride : p.k_seq_stride;
     p.n_tok_cap = n_tok_cap;
     if (cell_of) {   // rows come from the map: every sequence starts at row 0 of the cell arrays
@@ -1468,10 +1607,9 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_tc<576, 512, true>(p, grid, st, bl);
         else rc = V ? launch_tc<512, 512, false>(p, grid, st, bl) : launch_tc<512, 512, true>(p, grid, st, bl);
     } else if (dtype == SFA_BF16) {
-        if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true>(p, grid, st, bl);
-        else if (dkq == 512) rc = V ? launch_bf16<512, 512, false>(p, grid, st, bl) : launch_bf16<512, 512, true>(p, grid, st, bl);
-        else if (dkq == 128) rc = V ? launch_bf16<128, 128, false>(p, grid, st, bl) : launch_bf16<128, 128, true>(p, grid, st, bl);
-        else rc = V ? launch_bf16<64, 64, false>(p, grid, st, bl) : launch_bf16<64, 64, true>(p, grid, st, bl);
+        rc = mma_launch<false>(dkq, V != nullptr, p, grid, st, bl);
+    } else if (dtype == SFA_Q8_0) {
+        rc = mma_launch<true>(dkq, V != nullptr, p, grid, st, bl);
     } else {
         const cudaError_t e =
             dkq == 576   ? launch_pdl(attend_f32_kernel<576, 512>, grid, dim3(kThreads), 0, st, p)
@@ -1501,7 +1639,7 @@ extern "C" int sfa_attend_plan(int dtype, int n_q, int h_kv, int dkq, int has_v,
     using namespace sfa;
     if (!n_split || !kernels || n_q < 1 || h_kv < 1 || n_kv_max < 1 || compress_ratio < 1)
         return SFA_ERR_INVALID_ARG;
-    if (dtype != SFA_BF16 && dtype != SFA_F32) return SFA_ERR_INVALID_ARG;
+    if (dtype != SFA_BF16 && dtype != SFA_F32 && dtype != SFA_Q8_0) return SFA_ERR_INVALID_ARG;
     if (dkq != 576 && dkq != 512 && dkq != 128 && dkq != 64) return SFA_ERR_UNSUPPORTED;
     const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, has_v != 0, n_kv_max,
                                            compress_ratio, dense);

@@ -15,7 +15,9 @@ attention (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA para
 
 With a position -> cell map (``cell_of``), the caches are flat cell arrays in any order (a
 paged serving cache) and the pool and the attention take their ``_paged`` entry points; the
-scores and the selection work on pooled blocks, which are cut on positions either way.
+scores and the selection work on pooled blocks, which are cut on positions either way.  K and
+V may be q8_0 cache rows (uint8 tensors written by ``sfa_quantize_kv_q8_0``): the attention
+entry points then take them as ``SFA_Q8_0``; the index keys stay bf16.
 """
 from __future__ import annotations
 

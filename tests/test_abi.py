@@ -193,6 +193,31 @@ def test_paged_entry_points_reject_bad_arguments(L):
              FAKE, FAKE, 4096, FAKE, None, None, 0, None, None) == 1               # no cells
 
 
+def test_q8_0_entry_points(L):
+    assert [L.sfa_q8_0_row_bytes(d) for d in (64, 128, 512, 576, 100, 0)] == [80, 144, 544, 624, 0, 0]
+    f = L.sfa_quantize_kv_q8_0
+    #       X     dt n_out n_in  d    x_outer Y     y_outer status stream
+    base = [FAKE, 0, 2, 100, 576, 57600, FAKE, 62400, None, None]
+    assert f(None, *base[1:]) == 1                                                # no X
+    a = list(base); a[1] = 2
+    assert f(*a) == 1                                                             # x dtype
+    a = list(base); a[4] = 96
+    assert f(*a) == 2                                                             # d
+    a = list(base); a[2] = -1
+    assert f(*a) == 1                                                             # n_outer
+    a = list(base); a[6] = ODD
+    assert f(*a) == 1                                                             # Y alignment
+    a = list(base); a[7] = 62400 - 16
+    assert f(*a) == 1                                                             # Y groups overlap
+    a = list(base); a[5] = 57599
+    assert f(*a) == 1                                                             # X groups overlap
+    a = list(base); a[3] = 0
+    assert f(*a) == 0                                                             # empty: no work
+    g = L.sfa_gather_attend
+    assert g(FAKE, FAKE, None, 3, 1, 4096, 1, 16, 1, 576, 512, ctypes.c_float(0.04), FAKE, FAKE,
+             FAKE, FAKE, 256, 4, FAKE, None, None, 0, None, None) == 1     # dtype 3
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No CPU fallback: with libsfa.so absent, the first entry-point call raises."""
     import indexer_selected_sparse_block_gb300 as sfa
