@@ -94,12 +94,13 @@ def lib(path: str | None = None):
     return L
 
 
-def _p(t):
+def _p(t, strided=False):
+    """Device pointer of t; strided=True when the caller passes t's strides to the library."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("libsfa takes CUDA tensors only")
-    if not t.is_contiguous():
+    if not strided and not t.is_contiguous():
         raise ValueError("libsfa takes contiguous tensors only")
     return ctypes.c_void_p(t.data_ptr())
 
@@ -382,8 +383,9 @@ def sfa_quantize_kv_q8_0(X, Y, dev_status=None, stream=None):
         raise ValueError(f"Y must be uint8 [{n_outer}][{n_inner}][{rb}]")
     if (X.stride(2), Y.stride(2)) != (1, 1) or (n_inner > 1 and (X.stride(1), Y.stride(1)) != (d, rb)):
         raise ValueError("rows must be contiguous within an outer index")
-    rc = lib().sfa_quantize_kv_q8_0(_p(X), _dtype_code(X), n_outer, n_inner, d, X.stride(0), _p(Y),
-                                    Y.stride(0), _p(dev_status), _stream(stream))
+    rc = lib().sfa_quantize_kv_q8_0(_p(X, strided=True), _dtype_code(X), n_outer, n_inner, d,
+                                    X.stride(0), _p(Y, strided=True), Y.stride(0), _p(dev_status),
+                                    _stream(stream))
     _check("sfa_quantize_kv_q8_0", rc)
 
 
