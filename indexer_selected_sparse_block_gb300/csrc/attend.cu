@@ -1347,7 +1347,7 @@ constexpr auto mma_kernel() {
 // binary16 tile), Q, the S partials, P (hi, lo), the softmax statistics, the token ids and the
 // block list of its split.  The layout is the kernel's (attend_mma_body).
 template <int DKQ, int DV, bool VK, bool Q8 = false>
-size_t bf16_smem(int stages, int blk_list) {
+size_t mma_smem(int stages, int blk_list) {
     constexpr int KROW = DKQ * 2, VROW = VK ? KROW : DV * 2;
     constexpr int QK = q8_row_bytes(DKQ), QV = q8_row_bytes(DV);
     constexpr int STAGE = Q8 ? kT * QK + (VK ? 0 : kT * QV) : kT * KROW + (VK ? 0 : kT * VROW);
@@ -1359,14 +1359,14 @@ size_t bf16_smem(int stages, int blk_list) {
 // Two CTAs per SM when two stages fit in half the shared memory (more warps to hide the
 // latency of each tile's dependent steps), else one CTA with up to four stages.
 template <int DKQ, int DV, bool VK, bool Q8 = false>
-int bf16_per_sm(int blk_list) {
-    return bf16_smem<DKQ, DV, VK, Q8>(2, blk_list) <= 113 * 1024 ? 2 : 1;
+int mma_cta_per_sm(int blk_list) {
+    return mma_smem<DKQ, DV, VK, Q8>(2, blk_list) <= 113 * 1024 ? 2 : 1;
 }
 
 // Whether clusters of ns CTAs of the kernel (its shared memory for blk_list entries) can be
 // resident at all; asked once per (shape, ns, list size).
 template <int DKQ, int DV, bool VK, bool Q8 = false>
-bool bf16_clusters_fit(int ns, int blk_list) {
+bool mma_clusters_fit_shape(int ns, int blk_list) {
     static std::mutex mu;
     static int cache[9][4] = {};   // [ns][slot]: 0 unknown, 1 yes, 2 no (last four list sizes)
     static int keys[9][4] = {};
@@ -1374,11 +1374,11 @@ bool bf16_clusters_fit(int ns, int blk_list) {
     for (int k = 0; k < 4; ++k)
         if (cache[ns][k] && keys[ns][k] == blk_list) return cache[ns][k] == 1;
     int stages = 2;
-    if (bf16_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
+    if (mma_cta_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
         stages = 4;
-        while (stages > 2 && bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
+        while (stages > 2 && mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
     }
-    const size_t smem = bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list);
+    const size_t smem = mma_smem<DKQ, DV, VK, Q8>(stages, blk_list);
     bool ok = allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>());
     if (ok) {
         cudaLaunchConfig_t cfg = {};
@@ -1405,16 +1405,16 @@ bool bf16_clusters_fit(int ns, int blk_list) {
 }
 
 template <int DKQ, int DV, bool VK, bool Q8 = false>
-int launch_bf16(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
+int launch_mma_shape(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     int stages = 2;
-    if (bf16_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
+    if (mma_cta_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
         stages = 4;
-        while (stages > 2 && bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
+        while (stages > 2 && mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
     }
-    if (bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    if (mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
     AttnParams q = p;
     q.stages = stages;
-    const size_t smem = bf16_smem<DKQ, DV, VK, Q8>(stages, blk_list);
+    const size_t smem = mma_smem<DKQ, DV, VK, Q8>(stages, blk_list);
     static bool attr = false;
     if (!attr) {
         if (!allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>())) return SFA_ERR_CUDA;
@@ -1480,24 +1480,24 @@ struct AttendPlan {
 // 576 only with V = K).
 template <bool Q8>
 int mma_per_sm(int dkq, bool has_v, int bl) {
-    if (dkq == 576) return bf16_per_sm<576, 512, true, Q8>(bl);
-    if (dkq == 512) return has_v ? bf16_per_sm<512, 512, false, Q8>(bl) : bf16_per_sm<512, 512, true, Q8>(bl);
-    if (dkq == 128) return has_v ? bf16_per_sm<128, 128, false, Q8>(bl) : bf16_per_sm<128, 128, true, Q8>(bl);
-    return has_v ? bf16_per_sm<64, 64, false, Q8>(bl) : bf16_per_sm<64, 64, true, Q8>(bl);
+    if (dkq == 576) return mma_cta_per_sm<576, 512, true, Q8>(bl);
+    if (dkq == 512) return has_v ? mma_cta_per_sm<512, 512, false, Q8>(bl) : mma_cta_per_sm<512, 512, true, Q8>(bl);
+    if (dkq == 128) return has_v ? mma_cta_per_sm<128, 128, false, Q8>(bl) : mma_cta_per_sm<128, 128, true, Q8>(bl);
+    return has_v ? mma_cta_per_sm<64, 64, false, Q8>(bl) : mma_cta_per_sm<64, 64, true, Q8>(bl);
 }
 template <bool Q8>
 bool mma_clusters_fit(int dkq, bool has_v, int ns, int bl) {
-    if (dkq == 576) return bf16_clusters_fit<576, 512, true, Q8>(ns, bl);
-    if (dkq == 512) return has_v ? bf16_clusters_fit<512, 512, false, Q8>(ns, bl) : bf16_clusters_fit<512, 512, true, Q8>(ns, bl);
-    if (dkq == 128) return has_v ? bf16_clusters_fit<128, 128, false, Q8>(ns, bl) : bf16_clusters_fit<128, 128, true, Q8>(ns, bl);
-    return has_v ? bf16_clusters_fit<64, 64, false, Q8>(ns, bl) : bf16_clusters_fit<64, 64, true, Q8>(ns, bl);
+    if (dkq == 576) return mma_clusters_fit_shape<576, 512, true, Q8>(ns, bl);
+    if (dkq == 512) return has_v ? mma_clusters_fit_shape<512, 512, false, Q8>(ns, bl) : mma_clusters_fit_shape<512, 512, true, Q8>(ns, bl);
+    if (dkq == 128) return has_v ? mma_clusters_fit_shape<128, 128, false, Q8>(ns, bl) : mma_clusters_fit_shape<128, 128, true, Q8>(ns, bl);
+    return has_v ? mma_clusters_fit_shape<64, 64, false, Q8>(ns, bl) : mma_clusters_fit_shape<64, 64, true, Q8>(ns, bl);
 }
 template <bool Q8>
 int mma_launch(int dkq, bool has_v, const AttnParams &p, dim3 grid, cudaStream_t st, int bl) {
-    if (dkq == 576) return has_v ? SFA_ERR_UNSUPPORTED : launch_bf16<576, 512, true, Q8>(p, grid, st, bl);
-    if (dkq == 512) return has_v ? launch_bf16<512, 512, false, Q8>(p, grid, st, bl) : launch_bf16<512, 512, true, Q8>(p, grid, st, bl);
-    if (dkq == 128) return has_v ? launch_bf16<128, 128, false, Q8>(p, grid, st, bl) : launch_bf16<128, 128, true, Q8>(p, grid, st, bl);
-    return has_v ? launch_bf16<64, 64, false, Q8>(p, grid, st, bl) : launch_bf16<64, 64, true, Q8>(p, grid, st, bl);
+    if (dkq == 576) return has_v ? SFA_ERR_UNSUPPORTED : launch_mma_shape<576, 512, true, Q8>(p, grid, st, bl);
+    if (dkq == 512) return has_v ? launch_mma_shape<512, 512, false, Q8>(p, grid, st, bl) : launch_mma_shape<512, 512, true, Q8>(p, grid, st, bl);
+    if (dkq == 128) return has_v ? launch_mma_shape<128, 128, false, Q8>(p, grid, st, bl) : launch_mma_shape<128, 128, true, Q8>(p, grid, st, bl);
+    return has_v ? launch_mma_shape<64, 64, false, Q8>(p, grid, st, bl) : launch_mma_shape<64, 64, true, Q8>(p, grid, st, bl);
 }
 
 AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, int64_t n_kv_max,
