@@ -1,0 +1,41 @@
+"""The bench's algorithmic work per step (CPU): closed forms of the bytes each stage must move,
+for the bf16 and the q8_0 caches."""
+import importlib
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    import __graft_entry__
+    __graft_entry__.build()
+    sys.path.insert(0, ROOT)
+    return importlib.import_module("bench")
+
+
+def test_gathered_bytes_per_cell():
+    b = _bench()
+    import indexer_selected_sparse_block_gb300 as sfa
+    w = sfa.WORKLOADS["decode_32x131072"]          # 576-wide K, V = K, one KV head
+    att = [512 * 4 + 1] * w.n_q                      # 512 kept blocks of 4 cells + a 1-cell tail
+    assert b.algorithmic(w, att)["gathered_kv_bytes"] == 32 * 2049 * 1152
+    assert b.algorithmic(w, att, kv="q8_0")["gathered_kv_bytes"] == 32 * 2049 * 624
+    v = sfa.WORKLOADS["decode_4x1048576"]           # 512-wide K and separate V, two KV heads
+    att = [256 * 8 + 1] * v.n_q
+    assert b.algorithmic(v, att)["gathered_kv_bytes"] == 4 * 2049 * 2 * (512 + 512) * 2
+    assert b.algorithmic(v, att, kv="q8_0")["gathered_kv_bytes"] == 4 * 2049 * 2 * (544 + 544)
+    # the attention's flops do not depend on the cache type
+    assert b.algorithmic(v, att)["attend_flops"] == b.algorithmic(v, att, kv="q8_0")["attend_flops"]
+
+
+def test_pooled_key_bytes():
+    b = _bench()
+    import indexer_selected_sparse_block_gb300 as sfa
+    w = sfa.WORKLOADS["decode_32x131072"]
+    a = b.algorithmic(w, [1] * w.n_q, bounded=True)
+    nb = (w.depth + 1) // w.compress_ratio
+    assert a["kbar_bytes"] == w.n_q * nb * (2 * w.d_idx + 4)     # hi halves + bound factor
+    assert a["score_bytes"] == w.n_q * nb * 8                     # lower + upper bounds
+    e = b.algorithmic(w, [1] * w.n_q, bounded=False)
+    assert e["kbar_bytes"] == w.n_q * nb * 4 * w.d_idx             # hi + lo halves
