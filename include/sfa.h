@@ -24,7 +24,8 @@
  *    enqueued.  A CUDA launch error returns SFA_ERR_CUDA.
  *  - All data pointers are caller-owned DEVICE pointers; work is enqueued on `stream` (a
  *    cudaStream_t; NULL is the legacy default stream).  The library keeps no state between
- *    calls except a per-device cache of the SM count and of the driver's tensor-map encoder.
+ *    calls except a per-device cache of the SM count and of the CUDA driver's tensor-map
+ *    encoder.
  *  - Strides are in elements of the buffer's own type.  Buffers must be 16-byte aligned.
  *  - `dev_status` (nullable) is a device int32 the kernels OR bits into (SFA_DEV_*) when they
  *    meet data they cannot use (a block id outside [0, B_i), a non-ascending list, n_sel out

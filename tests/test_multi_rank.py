@@ -55,7 +55,7 @@ def test_job_throughput_single_rank():
 
 
 def test_reference_arm_under_torchrun_two_ranks():
-    """`bench.py --impl reference` launched as the driver launches N > 1: rank 0 alone runs the
+    """`bench.py --impl reference` launched under torchrun with 2 ranks: rank 0 alone runs the
     oracle and prints one JSON line; rank 1 exits 0 without work or output."""
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
