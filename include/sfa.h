@@ -241,7 +241,9 @@ size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_
  * sfa_attend_plan -- the launch plan the attention entry points take on the current device
  * for these sizes: *n_split CTAs per (query, KV head) list and *kernels launched per call
  * (1, or 2 when a merge kernel follows).  n_kv_max as in sfa_attend_workspace_bytes (the
- * dense entry point: n_tok_cap, dense = 1); has_v: a separate V is given.  Host only, no
+ * dense entry point: n_tok_cap, dense = 1); has_v: a separate V is given; dtype as the entry
+ * points (SFA_BF16, SFA_F32 or SFA_Q8_0).  It describes the per-sequence layout; the paged
+ * calls take the same plan, except that they never take the tcgen05 kernel.  Host only, no
  * launch.  SFA_ERR_INVALID_ARG / SFA_ERR_UNSUPPORTED as the entry points.
  */
 int sfa_attend_plan(int dtype, int n_q, int h_kv, int dkq, int has_v, int64_t n_kv_max,
