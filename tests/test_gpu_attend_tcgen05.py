@@ -1,6 +1,6 @@
 """Parity of the tcgen05 attention kernel (selected with SFA_ATTEND_KERNEL=tcgen05) against the
 oracle: the stage-level gathered and dense cases of the 512-wide heads, and the full-size
-decode and prefill workloads on sampled queries.  The default path (the warp-level kernel) is
+decode and prefill workloads on every query.  The default path (the warp-level kernel) is
 covered by test_gpu_stages / test_gpu_pipeline."""
 import math
 
@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from gpu_util import TOL_BF16, np32, row_rel_err
-from test_gpu_pipeline import _check_sampled, _run
+from test_gpu_pipeline import _check_queries, _run
 from test_gpu_stages import _attend_case, _random_selection
 
 pytestmark = pytest.mark.gpu
@@ -101,10 +101,8 @@ def test_tcgen05_matches_default_kernel(dev, monkeypatch):
     assert row_rel_err(np32(step.O), O_default).max() < TOL_BF16
 
 
-@pytest.mark.parametrize("name,queries", [("decode_32x131072", [0, 13, 31]),
-                                          ("pp2048_131072", [0, 1023, 2047]),
-                                          ("decode_4x1048576", [0, 3])])
-def test_tcgen05_full_size_sampled(dev, tcgen05, name, queries):
+@pytest.mark.parametrize("name", ["decode_32x131072", "pp2048_131072", "decode_4x1048576"])
+def test_tcgen05_full_size_all(dev, tcgen05, name):
     w = sfa.WORKLOADS[name]
     case, step = _run(w, dev)
-    _check_sampled(w, case, step, queries)
+    _check_queries(w, case, step)

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from gpu_util import check_selection, np32
-from test_gpu_pipeline import _check_sampled, _run
+from test_gpu_pipeline import _check_queries, _run
 
 pytestmark = pytest.mark.gpu
 
@@ -169,15 +169,14 @@ def test_refine_below_budget_and_bad_query(dev):
     assert gn[2] == 0 and np.all(got[2] == -1)
 
 
-@pytest.mark.parametrize("name,queries", [("decode_32x131072", [0, 7, 31]),
-                                          ("decode_1x4096", [0])])
-def test_bounded_step_full_size_sampled(dev, name, queries):
-    """The whole step with the bounded selection (SfaStep(bounded=True)) at full size:
-    sampled queries follow the oracle's agreement rule and attend within tolerance."""
+@pytest.mark.parametrize("name", ["decode_32x131072", "decode_1x4096"])
+def test_bounded_step_full_size_all(dev, name):
+    """The whole step with the bounded selection (SfaStep(bounded=True)) at full size: every
+    query follows the oracle's agreement rule and attends within tolerance."""
     w = sfa.WORKLOADS[name]
     case, step = _run(w, dev, bounded=True)
     assert step.bounded
-    _check_sampled(w, case, step, queries)
+    _check_queries(w, case, step)
 
 
 def test_bounded_step_rejects_long_rows(dev):
