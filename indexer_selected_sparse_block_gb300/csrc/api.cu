@@ -1,5 +1,7 @@
 // api.cu -- status strings, the device status read-back, and the per-device SM count cache.
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "sfa_common.cuh"
 
@@ -20,6 +22,31 @@ int device_sm_count() {
     return cache[dev];
 }
 
+namespace {
+std::mutex g_smem_mu;
+std::set<std::pair<int, const void *>> g_smem_raised;   // (device, kernel)
+}  // namespace
+
+bool smem_limit_raised(const void *kernel) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    return g_smem_raised.count({dev, kernel}) != 0;
+}
+
+void mark_smem_limit_raised(const void *kernel) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    g_smem_raised.insert({dev, kernel});
+}
+
 EncodeTiledFn encode_tiled() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
@@ -32,6 +59,23 @@ EncodeTiledFn encode_tiled() {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
+}
+
+void *current_context() {
+    typedef CUresult (*GetCtxFn)(CUcontext *);
+    static GetCtxFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCtxFn>(ptr);
+    });
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return reinterpret_cast<void *>(ctx);
 }
 
 }  // namespace sfa

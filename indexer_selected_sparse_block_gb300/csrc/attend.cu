@@ -1,143 +1,41 @@
 // attend.cu -- gathered flash attention over the kept cells (sfa_gather_attend) and its
-// below-budget dense twin (sfa_dense_attend).
+// below-budget dense twin (sfa_dense_attend): the warp-level kernel (the default for bf16 and
+// q8_0 caches), the tcgen05 kernel (opt-in), the fp32 SIMT kernel, combine_kernel, the launch
+// plans and the C entry points.  The attended list of a query and the shared parameters are in
+// attend_common.cuh; the warp-specialised bulk-copy kernel (opt-in) is in attend_ws.cu.
 //
-// llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM" gathers the K/V tiles of the
-// flash-attention loop through a per-query index list, with V a view of the first 512 dims
-// of K for the MLA-shaped heads (576/512) and separate V for 512/512; no ALiBi, no softcap.
-// Here the list is built on the fly from the kept block ids: list position j maps to token
-//   j < n_sel*cr : blk[j / cr]*cr + j % cr       (kept blocks, ascending)
-//   otherwise     : B*cr + (j - n_sel*cr)          (the tail, always attended)
-// and the dense case is the identity j -> j over 0..p.
-//
-// bf16 kernel (one CTA = one query x one KV head x one split of its list, 4 warps):
-//   * cp.async 16-byte gathers of 32 selected token rows per stage (each kept block is cr
-//     contiguous rows), XOR-swizzled rows so that ldmatrix is conflict-free, 2-4 stages;
+// bf16 kernel (one CTA = one query x one KV head x one split of its list, 4 warps, two CTAs
+// per SM):
+//   * Q's A fragments go straight from global memory into registers;
+//   * cp.async 16-byte gathers of the selected token rows, 32 rows per stage (each kept block
+//     is cr contiguous rows), XOR-swizzled rows so that ldmatrix is conflict-free;
 //   * S = Q K^T on tensor cores (mma.sync m16n8k16, M = the 16 query heads of the KV head),
 //     the head dim split over the 4 warps and the partial sums reduced through shared memory;
-//   * online softmax (base 2) over the 32 tokens; P is carried as two bf16 halves
+//   * online softmax (base 2) over the tile; P is carried as two bf16 halves
 //     (hi = bf16(p), lo = bf16(p - hi)), so P V is accurate to ~2^-17 instead of the 2^-9 of
 //     a single bf16 rounding (which alone uses up a 2e-3 output tolerance);
 //   * O += P_hi V + P_lo V on tensor cores, the 512 value dims split over the 4 warps; V = K
 //     reuses the K tile in shared memory.
-// Decode has few queries, so each list is split over several CTAs (flash-decoding) and the
-// partial (O, m, l) are merged by combine_kernel.  fp32 inputs take a plain SIMT kernel with
-// the same split/merge structure (accuracy reference path).
+// Decode has few queries, so each list is split over several CTAs (flash-decoding); the
+// partial (O, m, l) merge inside a thread-block cluster or through combine_kernel.  fp32 inputs
+// take a plain SIMT kernel with the same split/merge structure (accuracy reference path).
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <type_traits>
 
 #include <cooperative_groups.h>
 
-#include "sfa_common.cuh"
+#include "attend_common.cuh"
 
 namespace sfa {
 namespace {
 
 namespace cg = cooperative_groups;
-
-constexpr int kT = 32;          // tokens per tile
-constexpr int kThreads = 128;   // 4 warps
-constexpr int kMaxBlkList = 2056;
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct AttnParams {
-    const void *Q, *K, *V;
-    const int32_t *q_seq, *q_pos, *blk_idx, *n_sel;
-    float *O, *lse, *part_o, *part_ml;
-    int32_t *status;
-    int64_t k_tok_stride, k_seq_stride, v_tok_stride, v_seq_stride, n_tok_cap;
-    const int32_t *cell_of;   // paged layout: [n_seq][n_tok_cap] cell of each position, or null
-    int64_t n_cells;          // rows of the paged K (and V) arrays
-    int n_seq, n_q, h_q, h_kv, G, top_k, cr, dense, n_split, split_tokens, stages;
-    int cluster_merge;   // 1: the n_split CTAs of an item form one cluster and merge in place
-    float scale_log2;
-};
-
-// Row of position tok of sequence seq in the K (and V) arrays, in units of k_tok_stride
-// (v_tok_stride) from the sequence's base: the position itself in the per-sequence layout, the
-// cell the map gives in the paged one (where the sequence bases are all zero).  Padding
-// (tok < 0) and a cell outside [0, n_cells) give -1: the position is left out of the softmax,
-// and a bad cell raises SFA_DEV_BAD_CELL.
-__device__ __forceinline__ int64_t checked_cell(const AttnParams &p, int32_t c) {
-    if (c < 0 || (int64_t)c >= p.n_cells) {
-        set_status(p.status, SFA_DEV_BAD_CELL);
-        return -1;
-    }
-    return c;
-}
-__device__ __forceinline__ int64_t kv_row(const AttnParams &p, int seq, int tok) {
-    if (tok < 0 || !p.cell_of) return tok;
-    return checked_cell(p, __ldg(p.cell_of + (int64_t)seq * p.n_tok_cap + tok));
-}
-
-// Per-CTA view of the attended list of one query.
-struct ListInfo {
-    int ok;        // 0: the query is outside the caches (skipped)
-    int seq, pos;
-    int len;       // list length
-    int n_blk_tok; // n_sel * cr: positions [0, n_blk_tok) come from kept blocks
-    int tail0;     // first tail token (B * cr)
-};
-
-__device__ __forceinline__ ListInfo list_info(const AttnParams &p, int i, bool flag) {
-    ListInfo L{};
-    L.seq = p.q_seq[i];
-    L.pos = p.q_pos[i];
-    L.ok = L.seq >= 0 && L.seq < p.n_seq && L.pos >= 0 && (int64_t)L.pos < p.n_tok_cap;
-    if (!L.ok) {
-        if (flag) set_status(p.status, SFA_DEV_BAD_QUERY);
-        return L;
-    }
-    if (p.dense) {
-        L.len = L.pos + 1;
-        L.n_blk_tok = 0;
-        L.tail0 = 0;
-        return L;
-    }
-    const int B = (L.pos + 1) / p.cr;
-    int ns = p.n_sel[i];
-    const int ns_max = min(p.top_k, B);
-    if (ns < 0 || ns > ns_max) {
-        if (flag) set_status(p.status, SFA_DEV_BAD_NSEL);
-        ns = ns < 0 ? 0 : ns_max;
-    }
-    L.n_blk_tok = ns * p.cr;
-    L.tail0 = B * p.cr;
-    L.len = L.n_blk_tok + (L.pos + 1 - L.tail0);
-    return L;
-}
-
-// Loads the validated block ids that list positions [j0, j1) need into s_blk (from jb0).
-__device__ __forceinline__ int load_block_list(const AttnParams &p, int i, const ListInfo &L,
-                                               int j0, int j1, int *s_blk, bool flag) {
-    if (p.dense || L.n_blk_tok == 0 || j0 >= L.n_blk_tok) return 0;
-    const int jb0 = j0 / p.cr;
-    const int jb1 = (min(j1, L.n_blk_tok) + p.cr - 1) / p.cr;
-    const int B = (L.pos + 1) / p.cr;
-    const int32_t *row = p.blk_idx + (int64_t)i * p.top_k;
-    for (int jb = jb0 + threadIdx.x; jb < jb1; jb += blockDim.x) {
-        const int b = row[jb];
-        const bool ok = b >= 0 && b < B && (jb == 0 || b > row[jb - 1]);
-        if (!ok && flag) set_status(p.status, SFA_DEV_BAD_BLOCK);
-        s_blk[jb - jb0] = ok ? b : -1;
-    }
-    return jb0;
-}
-
-__device__ __forceinline__ int token_at(const AttnParams &p, const ListInfo &L, int j, int j1,
-                                        const int *s_blk, int jb0) {
-    if (j >= j1) return -1;
-    if (p.dense) return j;
-    if (j < L.n_blk_tok) {
-        const int jb = j / p.cr;
-        const int b = s_blk[jb - jb0];
-        return b < 0 ? -1 : b * p.cr + (j - jb * p.cr);
-    }
-    return L.tail0 + (j - L.n_blk_tok);
-}
 
 __device__ __forceinline__ uint32_t swz(int c, int r) { return (uint32_t)((c & ~7) | ((c ^ r) & 7)); }
 
@@ -206,15 +104,15 @@ __device__ __forceinline__ float round16(float x) {
     else return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// Dequantizes kT q8_0 rows of D elements (pitch SROW bytes: D codes, then D/32 binary16 scales)
+// Dequantizes TT q8_0 rows of D elements (pitch SROW bytes: D codes, then D/32 binary16 scales)
 // into binary16 rows of the swizzled tile layout (pitch 2*D bytes): element j of a row is
 // scale(j / 32) * code_j, exact in fp32, then rounded to binary16.  Zero-filled rows (padding)
 // give zeros.  Returns false when a value exceeds binary16's range.
-template <int D, int SROW>
+template <int D, int SROW, int TT>
 __device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, int tid) {
     constexpr int C8 = D / 8;   // 8-element chunks per row
     bool ok = true;
-    for (int e = tid; e < kT * C8; e += kThreads) {
+    for (int e = tid; e < TT * C8; e += kThreads) {
         const int r = e / C8, c = e - r * C8;
         const uint8_t *row = src + r * SROW;
         const uint2 w = *reinterpret_cast<const uint2 *>(row + c * 8);
@@ -236,46 +134,90 @@ __device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, i
     return ok;
 }
 
+// Waits until at most n of this thread's cp.async groups are pending (n in 0 .. 4).
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        default: cp_async_wait<4>(); break;
+    }
+}
+
+// Shared memory of one CTA of the warp-level kernel with TT-token tiles: the K/V stages (Q8:
+// quantized rows, plus one binary16 tile), the S partials, P (hi, lo), the softmax statistics,
+// the token ids and the block list of its split.  The layout is attend_mma_body's.
+template <int DKQ, int DV, bool VK, bool Q8, int TT>
+__host__ __device__ constexpr size_t mma_smem_bytes(int stages, int blk_list) {
+    return (size_t)stages * (Q8 ? TT * q8_row_bytes(DKQ) + (VK ? 0 : TT * q8_row_bytes(DV))
+                                : TT * DKQ * 2 + (VK ? 0 : TT * DV * 2)) +
+           (Q8 ? TT * DKQ * 2 + (VK ? 0 : TT * DV * 2) : 0) + 4 * 16 * (TT + 8) * 4 +
+           2 * 16 * (TT + 8) * 2 + 48 * 4 + (size_t)stages * TT * 4 + (size_t)blk_list * 4 + 16;
+}
+
 // Gathered attention on warp-level MMAs: the body of attend_bf16_kernel (bf16 K/V) and of
 // attend_q8_kernel (Q8: q8_0 K/V rows, gathered as such, dequantized per tile in shared memory
 // to binary16, with Q converted to binary16 and every tensor-core product on binary16).
-template <int DKQ, int DV, bool V_IS_K, bool Q8>
+// Tiles of TT tokens (16 or 32) stream through a ring of p.stages stages: tile t + stages - 1
+// is issued while tile t is scored, so stages - 1 tiles are in flight behind the one in use.
+// Q never passes through shared memory: each warp loads its A fragments straight from global
+// memory into registers.
+template <int DKQ, int DV, bool V_IS_K, bool Q8, int TT>
 __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     constexpr int KROW = DKQ * 2;                 // bytes of a K row in shared memory
     constexpr int VROW = V_IS_K ? KROW : DV * 2;  // bytes of a V row
     constexpr int KCH = DKQ / 8, VCH = DV / 8;    // 16-byte chunks per row
     constexpr int KS = DKQ / 64;                  // k16 steps of S per warp
     constexpr int NTV = DV / 32;                  // n8 tiles of O per warp
-    constexpr int SP_PITCH = kT + 8;              // fp32 S-partial row pitch
-    constexpr int P_PITCH = kT + 8;               // 16-bit P row pitch
+    constexpr int SP_PITCH = TT + 8;              // fp32 S-partial row pitch
+    constexpr int P_PITCH = TT + 8;               // 16-bit P row pitch
+    constexpr int TPR = kThreads / TT;            // copying threads per tile row
+    constexpr int SPT = TT / 8;                   // softmax columns per thread
+    static_assert(TT == 16 || TT == 32, "tile sizes");
     constexpr int QKROW = q8_row_bytes(DKQ), QVROW = q8_row_bytes(DV);   // q8_0 rows (Q8)
-    constexpr int STAGE_BYTES = Q8 ? kT * QKROW + (V_IS_K ? 0 : kT * QVROW)
-                                   : kT * KROW + (V_IS_K ? 0 : kT * VROW);
-    constexpr int DEQ_BYTES = Q8 ? kT * KROW + (V_IS_K ? 0 : kT * VROW) : 0;
+    constexpr int STAGE_BYTES = Q8 ? TT * QKROW + (V_IS_K ? 0 : TT * QVROW)
+                                   : TT * KROW + (V_IS_K ? 0 : TT * VROW);
+    constexpr int DEQ_BYTES = Q8 ? TT * KROW + (V_IS_K ? 0 : TT * VROW) : 0;
     using KElem = std::conditional_t<Q8, uint8_t, __nv_bfloat16>;   // element of a cache row
     constexpr int KG = Q8 ? QKROW : DKQ, VG = Q8 ? QVROW : DV;       // its elements per row
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sStage = smem;                                              // stages x STAGE_BYTES
     uint8_t *sDeq = sStage + (size_t)p.stages * STAGE_BYTES;             // Q8: DEQ_BYTES
-    uint8_t *sQ = sDeq + DEQ_BYTES;                                      // 16 x KROW
-    float *sSP = reinterpret_cast<float *>(sQ + 16 * KROW);              // 4 x 16 x SP_PITCH
+    float *sSP = reinterpret_cast<float *>(sDeq + DEQ_BYTES);            // 4 x 16 x SP_PITCH
     __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(sSP + 4 * 16 * SP_PITCH);  // hi, lo
     float *sAlpha = reinterpret_cast<float *>(sP + 2 * 16 * P_PITCH);    // 16
     float *sL = sAlpha + 16;                                             // 16
     float *sM = sL + 16;                                                 // 16
-    int *sTok = reinterpret_cast<int *>(sM + 16);                        // stages x kT
-    int *sBlk = sTok + p.stages * kT;                                    // block list
+    int *sTok = reinterpret_cast<int *>(sM + 16);                        // stages x TT
+    int *sBlk = sTok + p.stages * TT;                                    // block list
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     const bool lead = split == 0 && g == 0;
+    const int G = p.G;
     pdl_wait();   // global memory from here on
     pdl_trigger();
+    // Q fragments of this warp's head-dim slice (A operand, rows >= G zero), loaded first so
+    // that their latency overlaps the list look-ups
+    uint32_t qa[KS][4];
+    {
+        const uint32_t *Qw = reinterpret_cast<const uint32_t *>(
+            reinterpret_cast<const __nv_bfloat16 *>(p.Q) + ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int col = (warp * KS + ks) * 8 + tq;   // 32-bit word of columns 2 tq, 2 tq + 1
+            qa[ks][0] = gq < G ? __ldg(Qw + gq * (DKQ / 2) + col) : 0u;
+            qa[ks][1] = gq + 8 < G ? __ldg(Qw + (gq + 8) * (DKQ / 2) + col) : 0u;
+            qa[ks][2] = gq < G ? __ldg(Qw + gq * (DKQ / 2) + col + 4) : 0u;
+            qa[ks][3] = gq + 8 < G ? __ldg(Qw + (gq + 8) * (DKQ / 2) + col + 4) : 0u;
+        }
+    }
     const ListInfo L = list_info(p, i, lead && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
-    const int G = p.G;
 
     if (j0 >= j1) {  // nothing to attend in this split
         if (p.cluster_merge) {   // it still takes its part in the cluster's merge
@@ -304,22 +246,20 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         }
         return;
     }
-    // Q rows of this KV head (rows >= G zero-filled), swizzled like the K tile: copied
-    // asynchronously as the oldest cp.async group, so the copy overlaps the block-list reads
-    // and the first K/V tiles.
-    {
-        const __nv_bfloat16 *Qg = reinterpret_cast<const __nv_bfloat16 *>(p.Q) +
-                                  ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ;
-        const uint32_t qs = smem_u32(sQ);
-        for (int e = tid; e < 16 * KCH; e += kThreads) {
-            const int r = e / KCH, c = e % KCH;
-            const bool live = r < G;
-            cp_async16(qs + r * KROW + swz(c, r) * 16, live ? Qg + (int64_t)r * DKQ + c * 8 : Qg,
-                       live ? 16u : 0u);
-        }
-        cp_async_commit();
-    }
     const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
+    if constexpr (Q8) {   // Q to binary16 in registers: this path's tensor-core operand type
+        bool ok = true;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t w = qa[ks][e];
+                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+                ok &= fabsf(lo) < 65520.f && fabsf(hi) < 65520.f;
+                qa[ks][e] = pack_f16(lo, hi);
+            }
+        if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+    }
     __syncthreads();
 
     const KElem *Kseq = reinterpret_cast<const KElem *>(p.K) + (int64_t)L.seq * p.k_seq_stride +
@@ -327,7 +267,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     const KElem *Vseq = V_IS_K ? Kseq
                                : reinterpret_cast<const KElem *>(p.V) +
                                      (int64_t)L.seq * p.v_seq_stride + (int64_t)g * VG;
-    const int n_tiles = (j1 - j0 + kT - 1) / kT;
+    const int n_tiles = (j1 - j0 + TT - 1) / TT;
 
     // The token (and, paged, the map entry) of this thread's row is looked up one tile ahead
     // of the copy that uses it: tiles are issued in order, so the lookup for tile t + 1 is
@@ -335,7 +275,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     int nx_tok = -1;
     int32_t nx_cell = 0;
     auto lookup = [&](int t) {
-        nx_tok = t < n_tiles ? token_at(p, L, j0 + t * kT + (tid >> 2), j1, sBlk, jb0) : -1;
+        nx_tok = t < n_tiles ? token_at(p, L, j0 + t * TT + tid / TPR, j1, sBlk, jb0) : -1;
         if (p.cell_of && nx_tok >= 0)
             nx_cell = __ldg(p.cell_of + (int64_t)L.seq * p.n_tok_cap + nx_tok);
     };
@@ -344,78 +284,42 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     auto issue_tile = [&](int t) {
         const int st = t % p.stages;
         uint8_t *dstK = sStage + (size_t)st * STAGE_BYTES;
-        const int r = tid >> 2, sub = tid & 3;
+        const int r = tid / TPR, sub = tid % TPR;
         const int tok = nx_tok;
         const int64_t row = p.cell_of && tok >= 0 ? checked_cell(p, nx_cell) : tok;
         lookup(t + 1);
-        if (sub == 0) sTok[st * kT + r] = row >= 0 ? tok : -1;
+        if (sub == 0) sTok[st * TT + r] = row >= 0 ? tok : -1;
         const KElem *srcK = row >= 0 ? Kseq + row * p.k_tok_stride : Kseq;
         const uint32_t nbytes = row >= 0 ? 16u : 0u;
         if constexpr (Q8) {   // the quantized rows as they are (the tile is dequantized later)
             const uint32_t rowK = smem_u32(dstK) + r * QKROW;
 #pragma unroll 4
-            for (int c = sub; c < QKROW / 16; c += 4) cp_async16(rowK + c * 16, srcK + c * 16, nbytes);
+            for (int c = sub; c < QKROW / 16; c += TPR) cp_async16(rowK + c * 16, srcK + c * 16, nbytes);
             if constexpr (!V_IS_K) {
                 const KElem *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
-                const uint32_t rowV = smem_u32(dstK + kT * QKROW) + r * QVROW;
+                const uint32_t rowV = smem_u32(dstK + TT * QKROW) + r * QVROW;
 #pragma unroll 4
-                for (int c = sub; c < QVROW / 16; c += 4)
+                for (int c = sub; c < QVROW / 16; c += TPR)
                     cp_async16(rowV + c * 16, srcV + c * 16, nbytes);
             }
         } else {
             const uint32_t rowK = smem_u32(dstK) + r * KROW;
 #pragma unroll 6
-            for (int c = sub; c < KCH; c += 4) cp_async16(rowK + swz(c, r) * 16, srcK + c * 8, nbytes);
+            for (int c = sub; c < KCH; c += TPR) cp_async16(rowK + swz(c, r) * 16, srcK + c * 8, nbytes);
             if constexpr (!V_IS_K) {
                 const KElem *srcV = row >= 0 ? Vseq + row * p.v_tok_stride : Vseq;
-                const uint32_t rowV = smem_u32(dstK + kT * KROW) + r * VROW;
+                const uint32_t rowV = smem_u32(dstK + TT * KROW) + r * VROW;
 #pragma unroll 4
-                for (int c = sub; c < VCH; c += 4)
+                for (int c = sub; c < VCH; c += TPR)
                     cp_async16(rowV + swz(c, r) * 16, srcV + c * 8, nbytes);
             }
         }
     };
 
-    // prologue: stages-1 tiles in flight (behind the Q group)
+    // prologue: stages-1 tiles in flight
     for (int t = 0; t < p.stages - 1; ++t) {
         if (t < n_tiles) issue_tile(t);
         cp_async_commit();
-    }
-    // Q has landed once at most stages-1 younger groups are pending
-    if (p.stages == 2) cp_async_wait<1>();
-    else if (p.stages == 3) cp_async_wait<2>();
-    else cp_async_wait<3>();
-    __syncthreads();
-    if constexpr (Q8) {   // Q to binary16 in place: this path's tensor-core operand type
-        bool ok = true;
-        for (int e = tid; e < 16 * KCH; e += kThreads) {
-            const int r = e / KCH, c = e % KCH;
-            uint4 *q4 = reinterpret_cast<uint4 *>(sQ + r * KROW + swz(c, r) * 16);
-            const uint4 u = *q4;
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            uint32_t h[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-                ok &= fabsf(lo) < 65520.f && fabsf(hi) < 65520.f;
-                h[k] = pack_f16(lo, hi);
-            }
-            *q4 = make_uint4(h[0], h[1], h[2], h[3]);
-        }
-        if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
-        __syncthreads();
-    }
-
-    // Q fragments of this warp's head-dim slice (A operand, kept in registers)
-    uint32_t qa[KS][4];
-    {
-        const uint32_t q_base = smem_u32(sQ);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int kg = warp * KS + ks;
-            const int r = lane & 15, c = kg * 2 + (lane >> 4);
-            ldsm_x4(q_base + r * KROW + swz(c, r) * 16, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-        }
     }
 
     float o[NTV][4];
@@ -423,12 +327,9 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     for (int n = 0; n < NTV; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;   // of row (tid >> 3), kept by its 8 threads
 
-    const int gq = lane >> 2, tq = lane & 3;
     for (int t = 0; t < n_tiles; ++t) {
         // tile t has landed once at most stages-2 younger groups are pending
-        if (p.stages == 2) cp_async_wait<0>();
-        else if (p.stages == 3) cp_async_wait<1>();
-        else cp_async_wait<2>();
+        cp_async_wait_n(p.stages - 2);
         __syncthreads();
         if (t + p.stages - 1 < n_tiles) issue_tile(t + p.stages - 1);
         cp_async_commit();
@@ -436,20 +337,20 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         const int st = t % p.stages;
         if constexpr (Q8) {   // tile t from its q8_0 rows into the binary16 tile
             const uint8_t *stg = sStage + (size_t)st * STAGE_BYTES;
-            bool ok = dequant_tile<DKQ, QKROW>(stg, sDeq, tid);
-            if constexpr (!V_IS_K) ok &= dequant_tile<DV, QVROW>(stg + kT * QKROW, sDeq + kT * KROW, tid);
+            bool ok = dequant_tile<DKQ, QKROW, TT>(stg, sDeq, tid);
+            if constexpr (!V_IS_K) ok &= dequant_tile<DV, QVROW, TT>(stg + TT * QKROW, sDeq + TT * KROW, tid);
             if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
             __syncthreads();
         }
         const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
-        const uint32_t vbase = V_IS_K ? kbase : kbase + kT * KROW;
+        const uint32_t vbase = V_IS_K ? kbase : kbase + TT * KROW;
 
         // ---- S partial over this warp's head-dim slice
-        float acc[kT / 8][4];
+        float acc[TT / 8][4];
 #pragma unroll
-        for (int n = 0; n < kT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        for (int n = 0; n < TT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
-        for (int np = 0; np < kT / 16; ++np) {
+        for (int np = 0; np < TT / 16; ++np) {
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int kg = warp * KS + ks;
@@ -464,25 +365,33 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         }
         float *sp = sSP + warp * 16 * SP_PITCH;
 #pragma unroll
-        for (int n = 0; n < kT / 8; ++n) {
+        for (int n = 0; n < TT / 8; ++n) {
             *reinterpret_cast<float2 *>(sp + gq * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][0], acc[n][1]);
             *reinterpret_cast<float2 *>(sp + (gq + 8) * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][2], acc[n][3]);
         }
         __syncthreads();
 
-        // ---- online softmax: thread -> row tid/8, columns 4*(tid%8) .. +3
+        // ---- online softmax: thread -> row tid/8, columns SPT*(tid%8) .. +SPT-1
         {
-            const int row = tid >> 3, c0 = (tid & 7) * 4;
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            const int row = tid >> 3, c0 = (tid & 7) * SPT;
+            float s[SPT];
+#pragma unroll
+            for (int e = 0; e < SPT; ++e) s[e] = 0.f;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const float4 v = *reinterpret_cast<const float4 *>(sSP + (w * 16 + row) * SP_PITCH + c0);
-                s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
+                const float *src = sSP + (w * 16 + row) * SP_PITCH + c0;
+                if constexpr (SPT == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    s[0] += v.x; s[1] += v.y;
+                }
             }
             float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                s[e] = sTok[st * kT + c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
+            for (int e = 0; e < SPT; ++e) {
+                s[e] = sTok[st * TT + c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, s[e]);
             }
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -490,9 +399,9 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
             const float m_new = fmaxf(m_run, mx);
             const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-            float ph[4], pl[4], rs = 0.f;
+            float ph[SPT], pl[SPT], rs = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < SPT; ++e) {
                 const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
                 ph[e] = round16<Q8>(pe);
                 pl[e] = pe - ph[e];
@@ -503,10 +412,15 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
             l_run = l_run * alpha + rs;
             m_run = m_new;
-            *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
-                make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
-            *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
-                make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
+            if constexpr (SPT == 4) {
+                *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
+                    make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
+                *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
+                    make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
+            } else {
+                *reinterpret_cast<uint32_t *>(sP + row * P_PITCH + c0) = pack16<Q8>(ph[0], ph[1]);
+                *reinterpret_cast<uint32_t *>(sP + (16 + row) * P_PITCH + c0) = pack16<Q8>(pl[0], pl[1]);
+            }
             if ((tid & 7) == 0) sAlpha[row] = alpha;
         }
         __syncthreads();
@@ -514,13 +428,15 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         // ---- O = O * alpha + P V over this warp's value-dim slice
         {
             const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
+            if (__any_sync(0xFFFFFFFFu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-            for (int n = 0; n < NTV; ++n) {
-                o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
+                for (int n = 0; n < NTV; ++n) {
+                    o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
+                }
             }
             const uint32_t pbase = smem_u32(sP);
 #pragma unroll
-            for (int ks = 0; ks < kT / 16; ++ks) {
+            for (int ks = 0; ks < TT / 16; ++ks) {
                 uint32_t pa[4], pb[4];
                 {
                     const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
@@ -596,13 +512,13 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     }
 }
 
-template <int DKQ, int DV, bool V_IS_K>
+template <int DKQ, int DV, bool V_IS_K, int TT>
 __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnParams p) {
-    attend_mma_body<DKQ, DV, V_IS_K, false>(p);
+    attend_mma_body<DKQ, DV, V_IS_K, false, TT>(p);
 }
-template <int DKQ, int DV, bool V_IS_K>
+template <int DKQ, int DV, bool V_IS_K, int TT>
 __global__ void __launch_bounds__(kThreads, 1) attend_q8_kernel(const AttnParams p) {
-    attend_mma_body<DKQ, DV, V_IS_K, true>(p);
+    attend_mma_body<DKQ, DV, V_IS_K, true, TT>(p);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1330,61 +1246,75 @@ bool want_tcgen05() {
     const char *e = getenv("SFA_ATTEND_KERNEL");
     return e && strcmp(e, "tcgen05") == 0;
 }
+// SFA_ATTEND_KERNEL=ws picks the warp-specialised bulk-copy kernel (attend_ws.cu) for bf16.
+bool want_ws() {
+    const char *e = getenv("SFA_ATTEND_KERNEL");
+    return e && strcmp(e, "ws") == 0;
+}
 
 bool shape_supported(int dkq, int dv) {
     return (dkq == 576 && dv == 512) || (dkq == 512 && dv == 512) || (dkq == 128 && dv == 128) ||
            (dkq == 64 && dv == 64);
 }
 
+// SFA_ATTEND_TT=16 in the environment (read at each call) makes the warp-level kernel stream
+// 16-token tiles through up to six stages instead of 32-token tiles through two (measured on
+// GB300: no faster in decode, slower in prefill, where the extra barriers per byte cost more
+// than the deeper prefetch gains).
+int mma_tile() {
+    const char *e = getenv("SFA_ATTEND_TT");
+    return e && strcmp(e, "16") == 0 ? 16 : 32;
+}
+
 // The warp-level MMA attention kernel of a shape: bf16 K/V, or q8_0 K/V rows (Q8).
-template <int DKQ, int DV, bool VK, bool Q8>
+template <int DKQ, int DV, bool VK, bool Q8, int TT>
 constexpr auto mma_kernel() {
-    if constexpr (Q8) return attend_q8_kernel<DKQ, DV, VK>;
-    else return attend_bf16_kernel<DKQ, DV, VK>;
+    if constexpr (Q8) return attend_q8_kernel<DKQ, DV, VK, TT>;
+    else return attend_bf16_kernel<DKQ, DV, VK, TT>;
 }
 
-// Shared memory of one CTA of that kernel: the K/V stages (Q8: quantized rows, plus one
-// binary16 tile), Q, the S partials, P (hi, lo), the softmax statistics, the token ids and the
-// block list of its split.  The layout is the kernel's (attend_mma_body).
-template <int DKQ, int DV, bool VK, bool Q8 = false>
-size_t mma_smem(int stages, int blk_list) {
-    constexpr int KROW = DKQ * 2, VROW = VK ? KROW : DV * 2;
-    constexpr int QK = q8_row_bytes(DKQ), QV = q8_row_bytes(DV);
-    constexpr int STAGE = Q8 ? kT * QK + (VK ? 0 : kT * QV) : kT * KROW + (VK ? 0 : kT * VROW);
-    constexpr int DEQ = Q8 ? kT * KROW + (VK ? 0 : kT * VROW) : 0;
-    return (size_t)stages * STAGE + DEQ + 16 * KROW + 4 * 16 * (kT + 8) * 4 +
-           2 * 16 * (kT + 8) * 2 + 48 * 4 + (size_t)stages * kT * 4 + (size_t)blk_list * 4 + 16;
-}
-
-// Two CTAs per SM when two stages fit in half the shared memory (more warps to hide the
-// latency of each tile's dependent steps), else one CTA with up to four stages.
-template <int DKQ, int DV, bool VK, bool Q8 = false>
-int mma_cta_per_sm(int blk_list) {
-    return mma_smem<DKQ, DV, VK, Q8>(2, blk_list) <= 113 * 1024 ? 2 : 1;
+// The ring of a CTA of that kernel for a block list of blk_list entries: two CTAs per SM when
+// two stages fit in half the shared memory (more warps to hide the latency of each tile's
+// dependent steps), else one; and as many stages (2 .. 6) as then fit.
+struct MmaRing {
+    int per_sm, stages;
+    size_t smem;
+};
+template <int DKQ, int DV, bool VK, bool Q8, int TT>
+MmaRing mma_ring(int blk_list) {
+    MmaRing r;
+    r.per_sm = mma_smem_bytes<DKQ, DV, VK, Q8, TT>(2, blk_list) <= 113 * 1024 ? 2 : 1;
+    const size_t cap = r.per_sm == 2 ? 113 * 1024 : 227 * 1024;
+    r.stages = 2;
+    while (r.stages < 6 && mma_smem_bytes<DKQ, DV, VK, Q8, TT>(r.stages + 1, blk_list) <= cap)
+        ++r.stages;
+    r.smem = mma_smem_bytes<DKQ, DV, VK, Q8, TT>(r.stages, blk_list);
+    return r;
 }
 
 // Whether clusters of ns CTAs of the kernel (its shared memory for blk_list entries) can be
-// resident at all; asked once per (shape, ns, list size).
-template <int DKQ, int DV, bool VK, bool Q8 = false>
+// resident at all; asked once per (device, kernel, ns, list size).
+template <int DKQ, int DV, bool VK, bool Q8, int TT>
 bool mma_clusters_fit_shape(int ns, int blk_list) {
     static std::mutex mu;
-    static int cache[9][4] = {};   // [ns][slot]: 0 unknown, 1 yes, 2 no (last four list sizes)
-    static int keys[9][4] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    for (int k = 0; k < 4; ++k)
-        if (cache[ns][k] && keys[ns][k] == blk_list) return cache[ns][k] == 1;
-    int stages = 2;
-    if (mma_cta_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
-        stages = 4;
-        while (stages > 2 && mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
+    static std::map<std::tuple<int, int, int>, bool> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
     }
-    const size_t smem = mma_smem<DKQ, DV, VK, Q8>(stages, blk_list);
-    bool ok = allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>());
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto f = cache.find({dev, ns, blk_list});
+        if (f != cache.end()) return f->second;
+    }
+    const MmaRing ring = mma_ring<DKQ, DV, VK, Q8, TT>(blk_list);
+    bool ok = ensure_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8, TT>());
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(ns, 1, 1);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
+        cfg.dynamicSmemBytes = ring.smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)ns;
@@ -1393,38 +1323,27 @@ bool mma_clusters_fit_shape(int ns, int blk_list) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        ok = cudaOccupancyMaxActiveClusters(&n, mma_kernel<DKQ, DV, VK, Q8>(), &cfg) ==
+        ok = cudaOccupancyMaxActiveClusters(&n, mma_kernel<DKQ, DV, VK, Q8, TT>(), &cfg) ==
                  cudaSuccess && n > 0;
         cudaGetLastError();
     }
-    int slot = 0;
-    while (slot < 3 && cache[ns][slot]) ++slot;
-    cache[ns][slot] = ok ? 1 : 2;
-    keys[ns][slot] = blk_list;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[{dev, ns, blk_list}] = ok;
     return ok;
 }
 
-template <int DKQ, int DV, bool VK, bool Q8 = false>
+template <int DKQ, int DV, bool VK, bool Q8, int TT>
 int launch_mma_shape(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
-    int stages = 2;
-    if (mma_cta_per_sm<DKQ, DV, VK, Q8>(blk_list) == 1) {
-        stages = 4;
-        while (stages > 2 && mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) --stages;
-    }
-    if (mma_smem<DKQ, DV, VK, Q8>(stages, blk_list) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    const MmaRing ring = mma_ring<DKQ, DV, VK, Q8, TT>(blk_list);
+    if (ring.smem > 227 * 1024) return SFA_ERR_UNSUPPORTED;
     AttnParams q = p;
-    q.stages = stages;
-    const size_t smem = mma_smem<DKQ, DV, VK, Q8>(stages, blk_list);
-    static bool attr = false;
-    if (!attr) {
-        if (!allow_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8>())) return SFA_ERR_CUDA;
-        attr = true;
-    }
+    q.stages = ring.stages;
+    if (!ensure_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8, TT>())) return SFA_ERR_CUDA;
     const cudaError_t e =
-        q.cluster_merge ? launch_pdl_cluster(mma_kernel<DKQ, DV, VK, Q8>(), grid, dim3(kThreads),
-                                             smem, st, q.n_split, q)
-                        : launch_pdl(mma_kernel<DKQ, DV, VK, Q8>(), grid, dim3(kThreads), smem,
-                                     st, q);
+        q.cluster_merge ? launch_pdl_cluster(mma_kernel<DKQ, DV, VK, Q8, TT>(), grid,
+                                             dim3(kThreads), ring.smem, st, q.n_split, q)
+                        : launch_pdl(mma_kernel<DKQ, DV, VK, Q8, TT>(), grid, dim3(kThreads),
+                                     ring.smem, st, q);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
@@ -1455,11 +1374,7 @@ int launch_tc(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_list) {
     if (!encode_cache_map(&kmap, p.K, DKQ, p.h_kv, rows)) return SFA_ERR_CUDA;
     if (VK) vmap = kmap;
     else if (!encode_cache_map(&vmap, p.V, DV, p.h_kv, rows)) return SFA_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-        if (!allow_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
-        attr = true;
-    }
+    if (!ensure_max_dynamic_smem(attend_tc_kernel<DKQ, DV, VK>)) return SFA_ERR_CUDA;
     if (launch_pdl(attend_tc_kernel<DKQ, DV, VK>, grid, dim3(tc::kThreads), smem, st, kmap, vmap,
                    p) != cudaSuccess) {
         cudaGetLastError();
@@ -1474,30 +1389,45 @@ struct AttendPlan {
     SplitPlan sp;
     int cluster_ns;   // > 1: clusters of this many CTAs merge their splits in place
     bool use_tc;
+    bool use_ws;      // the warp-specialised bulk-copy kernel (attend_ws.cu)
+    WsPlan wp;
+    int tt;           // tokens per tile of the warp-level kernel
 };
 
 // The per-shape dispatch of the warp-level MMA kernel's helpers (dkq in {576, 512, 128, 64};
-// 576 only with V = K).
-template <bool Q8>
-int mma_per_sm(int dkq, bool has_v, int bl) {
-    if (dkq == 576) return mma_cta_per_sm<576, 512, true, Q8>(bl);
-    if (dkq == 512) return has_v ? mma_cta_per_sm<512, 512, false, Q8>(bl) : mma_cta_per_sm<512, 512, true, Q8>(bl);
-    if (dkq == 128) return has_v ? mma_cta_per_sm<128, 128, false, Q8>(bl) : mma_cta_per_sm<128, 128, true, Q8>(bl);
-    return has_v ? mma_cta_per_sm<64, 64, false, Q8>(bl) : mma_cta_per_sm<64, 64, true, Q8>(bl);
+// 576 only with V = K), for tiles of TT tokens.
+template <bool Q8, int TT>
+int mma_per_sm_tt(int dkq, bool has_v, int bl) {
+    if (dkq == 576) return mma_ring<576, 512, true, Q8, TT>(bl).per_sm;
+    if (dkq == 512) return has_v ? mma_ring<512, 512, false, Q8, TT>(bl).per_sm : mma_ring<512, 512, true, Q8, TT>(bl).per_sm;
+    if (dkq == 128) return has_v ? mma_ring<128, 128, false, Q8, TT>(bl).per_sm : mma_ring<128, 128, true, Q8, TT>(bl).per_sm;
+    return has_v ? mma_ring<64, 64, false, Q8, TT>(bl).per_sm : mma_ring<64, 64, true, Q8, TT>(bl).per_sm;
 }
 template <bool Q8>
-bool mma_clusters_fit(int dkq, bool has_v, int ns, int bl) {
-    if (dkq == 576) return mma_clusters_fit_shape<576, 512, true, Q8>(ns, bl);
-    if (dkq == 512) return has_v ? mma_clusters_fit_shape<512, 512, false, Q8>(ns, bl) : mma_clusters_fit_shape<512, 512, true, Q8>(ns, bl);
-    if (dkq == 128) return has_v ? mma_clusters_fit_shape<128, 128, false, Q8>(ns, bl) : mma_clusters_fit_shape<128, 128, true, Q8>(ns, bl);
-    return has_v ? mma_clusters_fit_shape<64, 64, false, Q8>(ns, bl) : mma_clusters_fit_shape<64, 64, true, Q8>(ns, bl);
+int mma_per_sm(int dkq, bool has_v, int bl, int tt) {
+    return tt == 32 ? mma_per_sm_tt<Q8, 32>(dkq, has_v, bl) : mma_per_sm_tt<Q8, 16>(dkq, has_v, bl);
+}
+template <bool Q8, int TT>
+bool mma_clusters_fit_tt(int dkq, bool has_v, int ns, int bl) {
+    if (dkq == 576) return mma_clusters_fit_shape<576, 512, true, Q8, TT>(ns, bl);
+    if (dkq == 512) return has_v ? mma_clusters_fit_shape<512, 512, false, Q8, TT>(ns, bl) : mma_clusters_fit_shape<512, 512, true, Q8, TT>(ns, bl);
+    if (dkq == 128) return has_v ? mma_clusters_fit_shape<128, 128, false, Q8, TT>(ns, bl) : mma_clusters_fit_shape<128, 128, true, Q8, TT>(ns, bl);
+    return has_v ? mma_clusters_fit_shape<64, 64, false, Q8, TT>(ns, bl) : mma_clusters_fit_shape<64, 64, true, Q8, TT>(ns, bl);
 }
 template <bool Q8>
-int mma_launch(int dkq, bool has_v, const AttnParams &p, dim3 grid, cudaStream_t st, int bl) {
-    if (dkq == 576) return has_v ? SFA_ERR_UNSUPPORTED : launch_mma_shape<576, 512, true, Q8>(p, grid, st, bl);
-    if (dkq == 512) return has_v ? launch_mma_shape<512, 512, false, Q8>(p, grid, st, bl) : launch_mma_shape<512, 512, true, Q8>(p, grid, st, bl);
-    if (dkq == 128) return has_v ? launch_mma_shape<128, 128, false, Q8>(p, grid, st, bl) : launch_mma_shape<128, 128, true, Q8>(p, grid, st, bl);
-    return has_v ? launch_mma_shape<64, 64, false, Q8>(p, grid, st, bl) : launch_mma_shape<64, 64, true, Q8>(p, grid, st, bl);
+bool mma_clusters_fit(int dkq, bool has_v, int ns, int bl, int tt) {
+    return tt == 32 ? mma_clusters_fit_tt<Q8, 32>(dkq, has_v, ns, bl) : mma_clusters_fit_tt<Q8, 16>(dkq, has_v, ns, bl);
+}
+template <bool Q8, int TT>
+int mma_launch_tt(int dkq, bool has_v, const AttnParams &p, dim3 grid, cudaStream_t st, int bl) {
+    if (dkq == 576) return has_v ? SFA_ERR_UNSUPPORTED : launch_mma_shape<576, 512, true, Q8, TT>(p, grid, st, bl);
+    if (dkq == 512) return has_v ? launch_mma_shape<512, 512, false, Q8, TT>(p, grid, st, bl) : launch_mma_shape<512, 512, true, Q8, TT>(p, grid, st, bl);
+    if (dkq == 128) return has_v ? launch_mma_shape<128, 128, false, Q8, TT>(p, grid, st, bl) : launch_mma_shape<128, 128, true, Q8, TT>(p, grid, st, bl);
+    return has_v ? launch_mma_shape<64, 64, false, Q8, TT>(p, grid, st, bl) : launch_mma_shape<64, 64, true, Q8, TT>(p, grid, st, bl);
+}
+template <bool Q8>
+int mma_launch(int dkq, bool has_v, const AttnParams &p, dim3 grid, cudaStream_t st, int bl, int tt) {
+    return tt == 32 ? mma_launch_tt<Q8, 32>(dkq, has_v, p, grid, st, bl) : mma_launch_tt<Q8, 16>(dkq, has_v, p, grid, st, bl);
 }
 
 AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, int64_t n_kv_max,
@@ -1512,30 +1442,41 @@ AttendPlan make_attend_plan(int dtype, int n_q, int h_kv, int dkq, bool has_v, i
     AttendPlan ap{};
     const bool use_tc = dtype == SFA_BF16 && (dkq == 576 || dkq == 512) && !paged && want_tcgen05();
     ap.use_tc = use_tc;
+    if (dtype == SFA_BF16 && !use_tc && want_ws() &&
+        ws_make_plan(n_q, h_kv, dkq, dkq == 576 ? 512 : dkq, has_v, n_kv_max, cr, dense, &ap.wp)) {
+        ap.use_ws = true;
+        ap.sp.n_split = ap.wp.n_split;
+        ap.sp.split_tokens = ap.wp.split_tokens;
+        ap.cluster_ns = ap.wp.cluster;
+        return ap;
+    }
     const bool q8 = dtype == SFA_Q8_0;
     const bool mma = (dtype == SFA_BF16 && !use_tc) || q8;
+    const int tt = mma ? mma_tile() : (use_tc ? tc_tile : kT);
+    ap.tt = tt;
     // resident CTAs per SM of the kernel this shape takes (the split plan fills them once)
     int per_sm = 1;
     if (mma) {
         const int bl_max = dense ? 0 : (int)(n_kv_max / cr + 2);
-        per_sm = q8 ? mma_per_sm<true>(dkq, has_v, bl_max) : mma_per_sm<false>(dkq, has_v, bl_max);
+        per_sm = q8 ? mma_per_sm<true>(dkq, has_v, bl_max, tt)
+                    : mma_per_sm<false>(dkq, has_v, bl_max, tt);
     }
-    SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, use_tc ? tc_tile : kT);
+    SplitPlan sp = plan_split(n_q, h_kv, n_kv_max, per_sm, tt);
     // bf16 decode-like plans of a few splits merge them inside a cluster (2, 4 or 8 CTAs)
     // instead of through a second kernel
     int cluster_ns = 0;
     if (mma && sp.n_split >= 2 && sp.n_split <= 12) {
         const int ns = sp.n_split >= 6 ? 8 : (sp.n_split >= 3 ? 4 : 2);
-        const int64_t tiles = (n_kv_max + kT - 1) / kT;
+        const int64_t tiles = (n_kv_max + tt - 1) / tt;
         const int64_t per = (tiles + ns - 1) / ns;
-        const int bl = dense ? 0 : (int)(per * kT / cr + 2);
+        const int bl = dense ? 0 : (int)(per * tt / cr + 2);
         bool fit = (int64_t)((tiles + per - 1) / per) == ns && bl <= kMaxBlkList;
-        if (fit) fit = q8 ? mma_clusters_fit<true>(dkq, has_v, ns, bl)
-                          : mma_clusters_fit<false>(dkq, has_v, ns, bl);
+        if (fit) fit = q8 ? mma_clusters_fit<true>(dkq, has_v, ns, bl, tt)
+                          : mma_clusters_fit<false>(dkq, has_v, ns, bl, tt);
         if (fit) {
             cluster_ns = ns;
             sp.n_split = ns;
-            sp.split_tokens = (int)(per * kT);
+            sp.split_tokens = (int)(per * tt);
         }
     }
     ap.sp = sp;
@@ -1593,6 +1534,8 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.top_k = top_k; p.cr = cr; p.dense = dense;
     p.n_split = sp.n_split; p.split_tokens = sp.split_tokens;
     p.cluster_merge = cluster_ns > 1;
+    p.n_items = n_q * h_kv * sp.n_split;
+    p.n_kv_max = n_kv_max;
     p.scale_log2 = scale * kLog2e;
     if (sp.n_split > 1) {
         const size_t n_rows = (size_t)n_q * h_q * sp.n_split;
@@ -1603,13 +1546,15 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     const int bl = dense ? 0 : sp.split_tokens / cr + 2;   // block-list entries a split needs
     const dim3 grid(sp.n_split, h_kv, n_q);
     int rc;
-    if (use_tc) {
+    if (ap.use_ws) {
+        rc = ws_launch(p, ap.wp, dkq, dv, V != nullptr, st);
+    } else if (use_tc) {
         if (dkq == 576) rc = V ? SFA_ERR_UNSUPPORTED : launch_tc<576, 512, true>(p, grid, st, bl);
         else rc = V ? launch_tc<512, 512, false>(p, grid, st, bl) : launch_tc<512, 512, true>(p, grid, st, bl);
     } else if (dtype == SFA_BF16) {
-        rc = mma_launch<false>(dkq, V != nullptr, p, grid, st, bl);
+        rc = mma_launch<false>(dkq, V != nullptr, p, grid, st, bl, ap.tt);
     } else if (dtype == SFA_Q8_0) {
-        rc = mma_launch<true>(dkq, V != nullptr, p, grid, st, bl);
+        rc = mma_launch<true>(dkq, V != nullptr, p, grid, st, bl, ap.tt);
     } else {
         const cudaError_t e =
             dkq == 576   ? launch_pdl(attend_f32_kernel<576, 512>, grid, dim3(kThreads), 0, st, p)
@@ -1650,9 +1595,16 @@ extern "C" int sfa_attend_plan(int dtype, int n_q, int h_kv, int dkq, int has_v,
 
 extern "C" size_t sfa_attend_workspace_bytes(int n_q, int h_q, int h_kv, int dv, int64_t n_kv_max) {
     if (n_q <= 0 || h_q <= 0 || h_kv <= 0 || dv <= 0 || n_kv_max <= 0) return 0;
-    const sfa::SplitPlan sp = sfa::plan_split(n_q, h_kv, n_kv_max, 2);  // the largest plan
-    if (sp.n_split <= 1) return 0;
-    return (size_t)n_q * h_q * sp.n_split * ((size_t)dv + 2) * sizeof(float);
+    // the largest split count any kernel's plan takes: the warp-level kernel's (two CTAs per
+    // SM, 16-row tiles; 32-row tiles and the tcgen05 kernel split less) and the
+    // warp-specialised kernel's (one CTA per SM, pieces of at least 64 rows)
+    const sfa::SplitPlan sp = sfa::plan_split(n_q, h_kv, n_kv_max, 2, 16);
+    int64_t ns_ws = sfa::device_sm_count() / ((int64_t)n_q * h_kv);
+    const int64_t ws_cap = ((n_kv_max + 15) / 16 + 3) / 4;
+    if (ns_ws > ws_cap) ns_ws = ws_cap;
+    const int ns = sp.n_split > ns_ws ? sp.n_split : (int)ns_ws;
+    if (ns <= 1) return 0;
+    return (size_t)n_q * h_q * ns * ((size_t)dv + 2) * sizeof(float);
 }
 
 extern "C" int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype,
@@ -1718,25 +1670,35 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SFA_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {nullptr};
+struct NoallocSlot {
+    void *ctx;    // the context the address was looked up in
+    void *ptr;    // device address of g_noalloc_scratch in that context
+};
+NoallocSlot g_noalloc_slot[64] = {};
 
-// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+// Device address of g_noalloc_scratch on the current device (nullptr on failure).  The address
+// is looked up once per device and context: a new context on the device (after
+// cudaDeviceReset, or another context made current) looks it up again.
 void *noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return nullptr;
     }
+    void *ctx = sfa::current_context();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocSlot &s = g_noalloc_slot[dev];
+    if (!s.ptr || s.ctx != ctx || !ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             cudaGetLastError();
+            s.ptr = nullptr;
             return nullptr;
         }
-        g_noalloc_ptr[dev] = p;
+        s.ptr = p;
+        s.ctx = ctx;
     }
-    return g_noalloc_ptr[dev];
+    return s.ptr;
 }
 }  // namespace
 

@@ -347,11 +347,7 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
     p.stages = stages;
     const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes + 8 * (2 * stages + 5) + 8 +
                         256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (!allow_max_dynamic_smem(index_score_kernel<KP, H, HI>)) return SFA_ERR_CUDA;
-        attr_set = true;
-    }
+    if (!ensure_max_dynamic_smem(index_score_kernel<KP, H, HI>)) return SFA_ERR_CUDA;
     // One wave: the block tiles of each query tile are split over as many CTAs as the
     // resident slots allow.
     const int slots = per_sm * device_sm_count();

@@ -79,6 +79,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled();
 
+// The calling thread's current CUDA context (cuCtxGetCurrent through the runtime), or null.
+void *current_context();
+
 // Opts `fn` into the largest dynamic shared memory its static usage leaves (227 KB per CTA on
 // sm_103a in total).  Clears the runtime's last error on failure.
 template <typename F>
@@ -94,6 +97,21 @@ inline bool allow_max_dynamic_smem(F *fn) {
         cudaGetLastError();
         return false;
     }
+    return true;
+}
+
+// Whether `kernel`'s dynamic shared-memory limit has been raised on the current device, and
+// recording that it has (api.cu; one record per device and kernel, thread-safe).
+bool smem_limit_raised(const void *kernel);
+void mark_smem_limit_raised(const void *kernel);
+
+// allow_max_dynamic_smem once per device and kernel.
+template <typename F>
+inline bool ensure_max_dynamic_smem(F *fn) {
+    const void *key = reinterpret_cast<const void *>(fn);
+    if (smem_limit_raised(key)) return true;
+    if (!allow_max_dynamic_smem(fn)) return false;
+    mark_smem_limit_raised(key);
     return true;
 }
 

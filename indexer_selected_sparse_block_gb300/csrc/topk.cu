@@ -1006,11 +1006,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int D>
 int launch_bounded_d(const RefineParams &p, int n_q, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        if (!allow_max_dynamic_smem(bounded_select_kernel<D>)) return SFA_ERR_CUDA;
-        attr = true;
-    }
+    if (!ensure_max_dynamic_smem(bounded_select_kernel<D>)) return SFA_ERR_CUDA;
     int clusters = device_sm_count() / kCl;
     if (clusters < 1) return SFA_ERR_CUDA;
     if (n_q < clusters) clusters = n_q;
@@ -1054,11 +1050,7 @@ int launch_stage(const TopkParams &p, int n_q, int n_chunks, cudaStream_t st) {
     int grid = kPerSm * device_sm_count();
     if (grid < 1) return SFA_ERR_CUDA;
     if (items < grid) grid = (int)items;
-    static bool attr = false;   // the shared memory is above the default 48 KB
-    if (!attr) {
-        if (!allow_max_dynamic_smem(topk_stage_kernel<R>)) return SFA_ERR_CUDA;
-        attr = true;
-    }
+    if (!ensure_max_dynamic_smem(topk_stage_kernel<R>)) return SFA_ERR_CUDA;
     if (launch_pdl(topk_stage_kernel<R>, dim3(grid), dim3(kThreads), smem_bytes<R>(), st, p, n_q,
                    n_chunks) != cudaSuccess) {
         cudaGetLastError();

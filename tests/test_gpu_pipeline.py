@@ -184,11 +184,14 @@ def test_decode_32x131072_all(dev, bounded):
 
 
 def test_pp2048_131072_all(dev):
-    """All 2048 queries of the pp2048 workload at depth 131072 against the oracle."""
+    """All 2048 queries of the pp2048 workload at depth 131072 against the oracle.  With
+    33 280 blocks per row the k-th and (k+1)-th scores are close: about two queries in three
+    have an oracle gap above 1e-4 at the cut (the exact-set rule); the rest are checked by the
+    agreement rule and against the oracle attending the GPU's own set."""
     w = sfa.WORKLOADS["pp2048_131072"]
     case, step = _run(w, dev)
     n_exact = _check_queries(w, case, step)
-    assert n_exact > 0.9 * w.n_q
+    assert n_exact > 0.5 * w.n_q
 
 
 def test_decode_cr1_32x32768_all(dev):

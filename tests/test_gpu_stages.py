@@ -383,3 +383,31 @@ def test_step_with_key_transform_matches_oracle(dev):
         ref, _ = oracle.attend(c["Q"][i], c["K"][s], None, msk, w.scale, w.h_kv, dv=w.dv)
         assert row_rel_err(O[i], ref).max() < TOL_BF16, i
     assert n_exact >= w.n_q - 1
+
+
+@pytest.mark.parametrize("kernel", ["default", "mma"])
+def test_dense_query_past_the_bound_is_flagged(dev, monkeypatch, kernel):
+    """A dense query whose q_pos + 1 exceeds the n_kv_max the call was given: SFA_DEV_BAD_QUERY
+    is raised, and the query attends its first n_kv_max keys (the other queries are exact)."""
+    if kernel == "mma":
+        monkeypatch.setenv("SFA_ATTEND_KERNEL", "mma")
+    dkq, dv, h_q, h_kv = 576, 512, 16, 1
+    n_seq, n_tok = 2, 700
+    q_seq = np.array([0, 1], np.int32)
+    q_pos = np.array([699, 200], np.int32)      # query 0 sees 700 keys, the bound is 500
+    n_kv_max = 500
+    Q, K, V = _attend_case(dev, dkq, dv, True, h_q, h_kv, n_seq, n_tok, q_seq, q_pos,
+                           torch.bfloat16, 77)
+    O = torch.empty((2, h_q, dv), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_dense_attend(Q, K, V, torch.from_numpy(q_seq).to(dev),
+                         torch.from_numpy(q_pos).to(dev), n_kv_max, 1.0 / math.sqrt(dkq), O,
+                         dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) & sfa.SFA_DEV_BAD_QUERY
+    Kn, Qn, On = np32(K), np32(Q), np32(O)
+    for i, keys in ((0, n_kv_max), (1, 201)):
+        msk = np.zeros(int(q_pos[i]) + 1, np.uint8)
+        msk[:keys] = 1
+        ref, _ = oracle.attend(Qn[i], Kn[q_seq[i]], None, msk, 1.0 / math.sqrt(dkq), h_kv, dv=dv)
+        assert row_rel_err(On[i], ref).max() < TOL_BF16, i

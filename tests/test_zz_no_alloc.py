@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_util import TOL_BF16, np32, row_rel_err
 
 pytestmark = pytest.mark.gpu
@@ -75,10 +76,36 @@ def _call_workspace(L, c, O, lse, status):
                                _ptr(lse), _ptr(ws), need, _ptr(status), stream)
 
 
+def _plan(L, c):
+    """(splits per list, kernels per call) of the attention call of case c."""
+    n_seq, n_tok, n_q, h_q, h_kv, dkq, dv = c["dims"]
+    ns, nk = ctypes.c_int(0), ctypes.c_int(0)
+    n_kv = c["top_k"] * c["cr"] + c["cr"] - 1
+    assert L.sfa_attend_plan(0, n_q, h_kv, dkq, 0, ctypes.c_int64(n_kv), c["cr"], 0,
+                             ctypes.byref(ns), ctypes.byref(nk)) == 0
+    return ns.value, nk.value
+
+
+def _oracle_outputs(c):
+    """The oracle's attention of every query of case c over its kept blocks and tail."""
+    n_seq, n_tok, n_q, h_q, h_kv, dkq, dv = c["dims"]
+    K, Q = np32(c["K"]), np32(c["Q"])
+    sel, n_sel, q_pos = np32(c["sel"]), np32(c["n_sel"]), np32(c["q_pos"])
+    out = []
+    for i in range(n_q):
+        msk = oracle.mask(int(q_pos[i]), c["cr"], sel[i], int(n_sel[i]))
+        out.append(oracle.attend(Q[i], K[i], None, msk, c["scale"], h_kv, dv=dv))
+    return np.stack([o for o, _ in out]), np.stack([l for _, l in out])
+
+
 def test_noalloc_matches_workspace_entry_point_twice(L):
     dev = torch.device("cuda:0")
     for seed in (11, 12):   # two calls in a row, different data, one shared scratch array
         c = _case(seed, dev)
+        # the plan splits each list over several CTAs and merges them through the scratch
+        # (a second kernel), so the shared array is really written and read
+        n_split, kernels = _plan(L, c)
+        assert n_split > 1 and kernels == 2, (n_split, kernels)
         n_q, h_q, dv = c["dims"][2], c["dims"][3], c["dims"][6]
         O1 = torch.empty((n_q, h_q, dv), device=dev)
         O2 = torch.full((n_q, h_q, dv), float("nan"), device=dev)
@@ -91,6 +118,9 @@ def test_noalloc_matches_workspace_entry_point_twice(L):
         assert int(st.item()) == 0
         assert row_rel_err(np32(O2), np32(O1)).max() < TOL_BF16
         assert np.abs(np32(l2) - np32(l1)).max() < 2e-3
+        ref_o, ref_l = _oracle_outputs(c)
+        assert row_rel_err(np32(O2), ref_o).max() < TOL_BF16
+        assert np.abs(np32(l2) - ref_l).max() < 2e-3
 
 
 def test_noalloc_scratch_bound(L):
