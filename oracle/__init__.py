@@ -65,6 +65,7 @@ def load(path: str | None = None):
     lib.sfa_oracle_select.argtypes = [_f64p, _i64, _int, _i32p]
     lib.sfa_oracle_select.restype = _int
     lib.sfa_oracle_mask.argtypes = [_i64, _int, _vp, _int, _int, _u8p]
+    lib.sfa_oracle_mask_window.argtypes = [_i64, _int, _vp, _int, _i64, _u8p]
     lib.sfa_oracle_attend.argtypes = [_f32p, _int, _int, _int, _int, ctypes.c_double, _f32p,
                                       _i64, _vp, _i64, _vp, _u8p, _i64, _f64p, _vp]
     lib.sfa_oracle_run.argtypes = [_f32p, _f32p, _f32p, _f32p, _f32p, _vp, _i32p, _i32p,
@@ -173,13 +174,18 @@ def select(score, top_k: int, lib=None):
     return sel, int(n)
 
 
-def mask(p: int, cr: int, sel=None, n_sel: int = 0, dense: bool = False, lib=None):
-    """Attended-set mask over positions 0..p (uint8[p+1])."""
+def mask(p: int, cr: int, sel=None, n_sel: int = 0, dense: bool = False, window: int = 0,
+         lib=None):
+    """Attended-set mask over positions 0..p (uint8[p+1]); window > 0: the set joined with
+    the `window` most recent positions (the dense-window + sparse variant)."""
     lib = lib or load()
     out = np.zeros(p + 1, np.uint8)
     sel_arr = None if sel is None else np.ascontiguousarray(sel, dtype=np.int32)
-    lib.sfa_oracle_mask(p, cr, None if sel_arr is None else sel_arr.ctypes.data, n_sel,
-                        1 if dense else 0, out)
+    ptr = None if sel_arr is None else sel_arr.ctypes.data
+    if window > 0 and not dense:
+        lib.sfa_oracle_mask_window(p, cr, ptr, n_sel, window, out)
+    else:
+        lib.sfa_oracle_mask(p, cr, ptr, n_sel, 1 if dense else 0, out)
     return out
 
 

@@ -280,6 +280,22 @@ void sfa_oracle_mask(int64_t p, int cr, const int32_t *sel, int n_sel, int dense
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Step 4, windowed -- the attended set when a contiguous run of the most recent keys is
+ * attended densely beside the selected blocks [PR #27970 review discussion: dense attention
+ * over the continuous block of keys, sparse attention over the selected keys, the two
+ * results combined].  Reading: the run is the window of the `window` most recent positions
+ * p - window + 1 .. p (clipped at 0); the attended set is its union with the kept blocks and
+ * the tail.  window = 0 gives the plain set above; window >= p + 1 gives every position.    */
+void sfa_oracle_mask_window(int64_t p, int cr, const int32_t *sel, int n_sel, int64_t window,
+                            uint8_t *mask)
+{
+    sfa_oracle_mask(p, cr, sel, n_sel, 0, mask);
+    int64_t first = p - window + 1;
+    if (first < 0) first = 0;
+    for (int64_t t = first; t <= p; ++t) mask[t] = 1;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Step 5 -- exact softmax attention over the masked tokens [SFA].
  * For head h (KV head g = h / (h_q / h_kv)):
  *   l_t = scale * q_h . K[t][g],   O_h = sum_t exp(l_t - m) V[t][g] / sum_t exp(l_t - m),

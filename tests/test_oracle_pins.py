@@ -242,6 +242,55 @@ def pin_mask(lib):
     assert np.all(oracle.mask(9, 4, dense=True, lib=lib) == 1)
 
 
+def pin_mask_window(lib):
+    """The windowed attended set (dense window + kept blocks + tail): hand-derived sets; no
+    window is the plain set; a window reaching position 0 is every position; the set only
+    grows with the window; and the window suffix with the kept tokens before it is a disjoint
+    cover of the set, over which attention splits exactly into two log-sum-exp-combined
+    parts (the decomposition the dense + sparse variant computes)."""
+    for c in _golden("qsa_window.json")["cases"]:
+        sel = np.array(c["sel"], np.int32)
+        m = oracle.mask(c["p"], c["compress_ratio"], sel, len(sel), window=c["window"], lib=lib)
+        assert list(np.nonzero(m)[0]) == c["attended"], c["derivation"][0]
+    r = _rng(17)
+    for trial in range(30):
+        cr = int(r.choice([1, 2, 3, 4, 8]))
+        p = int(r.integers(0, 160))
+        B = (p + 1) // cr
+        k = int(r.integers(1, 20))
+        sel, n = oracle.select(r.standard_normal(B), k, lib=lib)
+        plain = oracle.mask(p, cr, sel, n, lib=lib)
+        assert np.array_equal(oracle.mask(p, cr, sel, n, window=0, lib=lib), plain)
+        assert np.all(oracle.mask(p, cr, sel, n, window=p + 1 + int(r.integers(0, 5)), lib=lib) == 1)
+        prev = plain
+        for W in sorted(r.integers(1, p + 2, 4)):
+            cur = oracle.mask(p, cr, sel, n, window=int(W), lib=lib)
+            assert np.all(cur >= prev) and cur.sum() >= prev.sum()
+            prev = cur
+    # attention over the set == the two parts combined by their log-sum-exp
+    r = _rng(19)
+    h_q, h_kv, dkq, dv, cr, p, W = 4, 2, 32, 16, 4, 70, 13
+    K = r.standard_normal((p + 1, h_kv, dkq)).astype(np.float32)
+    V = r.standard_normal((p + 1, h_kv, dv)).astype(np.float32)
+    q = r.standard_normal((h_q, dkq)).astype(np.float32)
+    sel, n = oracle.select(r.standard_normal((p + 1) // cr), 5, lib=lib)
+    full = oracle.mask(p, cr, sel, n, window=W, lib=lib)
+    s0 = min(((p + 1) // cr) * cr, p - W + 1)
+    suffix = np.zeros(p + 1, np.uint8)
+    suffix[s0:] = 1
+    before = oracle.mask(p, cr, sel, n, lib=lib).copy()
+    before[s0:] = 0
+    assert np.array_equal(suffix | before, full) and not np.any(suffix & before)
+    O, lse = oracle.attend(q, K, V, full, 0.2, h_kv, lib=lib)
+    Oa, la = oracle.attend(q, K, V, suffix, 0.2, h_kv, lib=lib)
+    Ob, lb = oracle.attend(q, K, V, before, 0.2, h_kv, lib=lib)
+    M = np.maximum(la, lb)
+    wa, wb = np.exp(la - M), np.exp(lb - M)
+    np.testing.assert_allclose(O, (wa[:, None] * Oa + wb[:, None] * Ob) / (wa + wb)[:, None],
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, M + np.log(wa + wb), rtol=1e-13)
+
+
 # ------------------------------------------------------------------------------- attend
 def _sdpa_fp64(q, K, V, msk, scale, group):
     """torch's scaled_dot_product_attention in fp64 over the masked tokens."""
@@ -448,7 +497,7 @@ def pin_key_transform(lib):
 
 
 PINS = [pin_pool_closed_forms, pin_pool_cells, pin_q8_0, pin_scores, pin_select, pin_token_expanded, pin_mask,
-        pin_attend, pin_pipeline, pin_key_transform]
+        pin_mask_window, pin_attend, pin_pipeline, pin_key_transform]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -492,6 +541,8 @@ MUTANTS = {
                          "const double r = ss / d_idx + eps;"),
     "position_ignores_cr": ("const double p = (double)(b * cr + pos_offset);",
                             "const double p = (double)(b + pos_offset);"),
+    "window_one_too_long": ("int64_t first = p - window + 1;", "int64_t first = p - window;"),
+    "window_ignored": ("for (int64_t t = first; t <= p; ++t) mask[t] = 1;", ""),
 }
 
 
