@@ -40,6 +40,7 @@ SECOND_WORKLOAD = "pp2048_131072"
 PAGE_CELLS = 64
 Q8_CACHE = ("q8_0 rows (blocks of 32 int8 codes with a binary16 scale; 624 B per 576-wide row), "
             "attention on binary16 tensor-core operands")
+WINDOW = 128   # positions of the dense window in the dense-window + sparse companion line
 PAGED_LAYOUT = (f"paged: {PAGE_CELLS}-cell pages dealt from a seeded shuffled page table, "
                 "one spare page per sequence")
 L2_FLUSH_BYTES = 512 << 20
@@ -176,7 +177,8 @@ class ClockSampler:
 class Workbench:
     """Inputs, buffers and one step of the method for workload w on the current device."""
 
-    def __init__(self, w, dev, bounded=None, paged=False, kv="bf16"):
+    def __init__(self, w, dev, bounded=None, paged=False, kv="bf16", window=0,
+                 window_mode="single"):
         self.w, self.dev, self.paged, self.kv = w, dev, paged, kv
         self.case = sfa.make_case(w, device=dev)
         self.n_blk_max = w.n_tok // w.compress_ratio
@@ -206,7 +208,7 @@ class Workbench:
                                 compress_ratio=w.compress_ratio,
                                 indexer_top_k=w.indexer_top_k, n_blk_max=self.n_blk_max,
                                 q_group=w.n_q_per_seq, bounded=bounded, cell_of=self.cell_of,
-                                device=dev)
+                                window=window, window_mode=window_mode, device=dev)
         # the cache state before the step: every block completed by earlier tokens is pooled
         self.first_new_blk = w.depth // w.compress_ratio
         self.step.pool(self.case["X"], 0, self.first_new_blk)
@@ -496,6 +498,8 @@ def main():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0"],
                     help="KV cache type of the main line (q8_0: quantized rows)")
     ap.add_argument("--no-q8", action="store_true", help="skip the q8_0-cache companion line")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the dense-window + sparse companion line (decode workloads)")
     ap.add_argument("--depth", type=int, default=0,
                     help="override the cache depth (smaller runs for ncu captures)")
     args = ap.parse_args()
@@ -671,6 +675,47 @@ def main():
                            "device_status": B.sfa_read_device_status(wbq.step.status)}
         del wbq
         torch.cuda.empty_cache()
+
+    if not args.no_window and args.kv == "bf16" and not args.paged and w.kind == "decode" \
+            and rank == 0 and world == 1:
+        # the dense window of the WINDOW most recent positions beside the kept blocks, in one
+        # pass and as the two parts combined by their log-sum-exp
+        res, outs = {}, {}
+        for mode in ("single", "split"):
+            wbw = Workbench(w, dev, bounded=False if args.exact else None, window=WINDOW,
+                            window_mode=mode)
+            sw, _ = measure(wbw, max(3, args.steps // 2), 3, flush, per_stage=False)
+            _, stw = measure(wbw, 3, 3, flush, per_stage=True)
+            msw = sum(sw) / len(sw)
+            res[mode] = {"value": w.n_q / (msw / 1000.0), "unit": "tokens/s", "ms_per_step": msw,
+                         "stage_ms": stw,
+                         "device_status": B.sfa_read_device_status(wbw.step.status)}
+            outs[mode] = wbw.step.O.clone()
+            if mode == "single":   # the attended cells: kept tokens before the suffix + suffix
+                sel = wbw.step.blk_idx.cpu()
+                ns = wbw.step.n_sel.cpu()
+                cells = 0
+                for i, p in enumerate(wbw.case["q_pos"].cpu().tolist()):
+                    s0 = min(((p + 1) // w.compress_ratio) * w.compress_ratio,
+                             max(0, p - WINDOW + 1))
+                    kept = sel[i, : int(ns[i])].long() * w.compress_ratio
+                    kept_cells = int(((s0 - kept).clamp(0, w.compress_ratio)).sum())
+                    cells += kept_cells + (p + 1 - s0)
+                row_b = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
+                res["gathered_kv_bytes"] = cells * row_b
+            del wbw
+            torch.cuda.empty_cache()
+        a, b = outs["single"], outs["split"]
+        res["max_rel_diff_single_vs_split"] = float(
+            ((a - b).abs().amax(-1) / a.abs().amax(-1).clamp_min(1e-30)).max())
+        for mode in ("single", "split"):
+            att = res[mode]["stage_ms"].get("attend", 0.0)
+            res[mode]["gathered_kv_GBps"] = res["gathered_kv_bytes"] / (att * 1e6) if att else None
+        line["window"] = {"window": WINDOW,
+                          "what": "attention over the kept blocks, the tail and the WINDOW most "
+                                  "recent positions: one pass (single) vs the kept part and the "
+                                  "window part apart + sfa_combine_attention (split)", **res}
+        del outs
 
     if not args.no_second and rank == 0 and world == 1:
         w2 = sfa.WORKLOADS[SECOND_WORKLOAD]

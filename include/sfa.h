@@ -61,14 +61,17 @@ enum sfa_dtype { SFA_BF16 = 0, SFA_F32 = 1, SFA_Q8_0 = 2 };
 #define SFA_DEV_BAD_BLOCK 0x1 /* a selected block id outside [0, B_i) or not ascending      */
 #define SFA_DEV_BAD_NSEL 0x2  /* n_sel[i] < 0 or > top_k (clamped)                         */
 #define SFA_DEV_BAD_QUERY 0x4 /* q_seq/q_pos outside the caches, or a query group that
-                                 spans sequences (that query is skipped)                  */
+                                 spans sequences (that query is skipped), or a dense query
+                                 with q_pos + 1 > n_kv_max (its first n_kv_max keys only) */
 #define SFA_DEV_TIMEOUT 0x8   /* a bounded wait inside a kernel ran out; the kernel
                                  released its resources and returned early                */
 #define SFA_DEV_BAD_CELL 0x10 /* a paged cell map entry outside [0, n_cells): that position
                                  reads as a zero row (pool) or is left out (attention)    */
-#define SFA_DEV_FP16_RANGE 0x20 /* quantized-cache path: a value beyond binary16's range (a
-                                 q8_0 scale, a query element or a dequantized K/V value);
-                                 the results that involve it are not finite              */
+#define SFA_DEV_FP16_RANGE 0x20 /* a binary16 operand path: a value beyond binary16's range
+                                 (a q8_0 scale, a query element or a dequantized K/V value;
+                                 with SFA_ATTEND_KERNEL=ws, a bf16 V element at or above
+                                 65520 in magnitude); the results involving it are not
+                                 finite                                                  */
 
 /*
  * sfa_pool_index_keys -- one mean-pooled index key per block of compress_ratio tokens, taken
@@ -198,7 +201,9 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
  *   blk_idx, n_sel: as sfa_topk_blocks
  *   workspace: sfa_topk_refine_workspace_bytes(n_q, n_blk_max) bytes of device memory (used
  *           for candidate lists longer than 4096)
- * Limits: n_blk_max <= 36864; 1 <= top_k <= 2048; d_idx in {64, 128}; 1 <= h_idx <= 16.
+ * Limits: n_blk_max <= 131072 (each CTA of a row's cluster takes 3 rounds of 4096 blocks
+ * up to 36864 blocks per row, 8 beyond); 1 <= top_k <= 2048; d_idx in {64, 128};
+ * 1 <= h_idx <= 16.
  * Errors as the other entry points (host checks before any launch, SFA_DEV_* flags).
  */
 int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
@@ -230,8 +235,11 @@ int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score
  *           (split-KV partial results; may be NULL when that size is 0).
  * Query head h reads KV head h / (h_q / h_kv).  p_i < n_tok_cap is required.
  * Limits (bf16): (dkq, dv) in {(576, 512), (512, 512), (128, 128), (64, 64)}, h_q/h_kv <= 16;
- *        dv > dkq needs a separate V.  SFA_ATTEND_KERNEL=tcgen05 in the environment selects the
- *        tcgen05 kernel for dkq 576 / 512 (default: the mma.sync kernel; same results).
+ *        dv > dkq needs a separate V.  Kernel choice (read from the environment at each call):
+ *        default, the warp-level mma.sync kernel with 32-token tiles (SFA_ATTEND_TT=16: 16-token
+ *        tiles, deeper prefetch); SFA_ATTEND_KERNEL=tcgen05, the tcgen05 kernel for dkq 576 /
+ *        512; SFA_ATTEND_KERNEL=ws, the warp-specialised bulk-copy kernel (P V on binary16
+ *        operands, SFA_ATTEND_PV=bf16x2 for bf16 hi + lo).  All meet the same tolerances.
  *        (fp32): the same (dkq, dv) pairs and h_q/h_kv <= 16.
  * Few (query, KV head) lists are split over several CTAs (flash-decoding); with the bf16
  * kernel, 2 to 8 splits merge inside a thread-block cluster, else a second kernel merges them.
@@ -254,6 +262,48 @@ int sfa_gather_attend(const void *Q, const void *K, const void *V, int dtype, in
                       const int32_t *blk_idx, const int32_t *n_sel, int top_k,
                       int compress_ratio, float *O, float *lse, void *workspace,
                       size_t workspace_bytes, int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_gather_attend_window -- attention over the kept blocks, the tail AND a dense window of
+ * the `window` most recent positions p_i - window + 1 .. p_i (clipped at 0): the dense +
+ * sparse variant of PR #27970's review discussion (dense attention over the continuous block
+ * of keys, sparse attention over the selected keys, the results combined).  Let s0 be the
+ * first position of the suffix attended in full: min(B_i*cr, p_i - window + 1) (B_i*cr when
+ * window = 0).  `part` chooses what one call attends:
+ *   SFA_PART_ALL       the whole set in one pass: the kept tokens before s0, then s0 .. p_i;
+ *   SFA_PART_SELECTED  only the kept tokens before s0 (no tail, no window);
+ *   SFA_PART_WINDOW    only the suffix s0 .. p_i;
+ * the two parts are disjoint and cover the set, so sfa_combine_attention of their (O, lse)
+ * gives SFA_PART_ALL's result.  window = 0 with SFA_PART_ALL is sfa_gather_attend.  A part
+ * with nothing to attend gives O = 0 and lse = -inf.
+ *   workspace: sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv,
+ *               sfa_window_kv_max(top_k, compress_ratio, window, part)) bytes.
+ * Arguments otherwise, limits and kernels as sfa_gather_attend; window >= 0.
+ */
+enum sfa_part { SFA_PART_ALL = 0, SFA_PART_SELECTED = 1, SFA_PART_WINDOW = 2 };
+int64_t sfa_window_kv_max(int top_k, int compress_ratio, int64_t window, int part);
+int sfa_gather_attend_window(const void *Q, const void *K, const void *V, int dtype, int n_seq,
+                             int64_t n_tok_cap, int n_q, int h_q, int h_kv, int dkq, int dv,
+                             float scale, const int32_t *q_seq, const int32_t *q_pos,
+                             const int32_t *blk_idx, const int32_t *n_sel, int top_k,
+                             int compress_ratio, int64_t window, int part, float *O,
+                             float *lse, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_combine_attention -- merges two attentions of the same queries over disjoint key sets
+ * into the attention over their union, by their log-sum-exp (the "combining the result" step
+ * of the dense + sparse variant; exact: softmax over a disjoint union):
+ *   O[r] = (e^lse_a[r] O_a[r] + e^lse_b[r] O_b[r]) / (e^lse_a[r] + e^lse_b[r]),
+ *   lse[r] = log(e^lse_a[r] + e^lse_b[r]),
+ * for the n_rows rows of dv fp32 values (rows = query x head).  A part with lse = -inf
+ * contributes nothing; both -inf gives O = 0, lse = -inf.  O may be O_a or O_b and lse may be
+ * lse_a or lse_b (in place); every pointer is device memory, 16-byte aligned; dv a multiple
+ * of 4.  One kernel launch.  SFA_ERR_INVALID_ARG for bad arguments.
+ */
+int sfa_combine_attention(const float *O_a, const float *lse_a, const float *O_b,
+                          const float *lse_b, int64_t n_rows, int dv, float *O, float *lse,
+                          sfa_stream_t stream);
 
 /*
  * sfa_dense_attend -- causal attention of each query over all of its sequence's tokens

@@ -20,7 +20,8 @@ SFA_OK, SFA_ERR_INVALID_ARG, SFA_ERR_UNSUPPORTED, SFA_ERR_CUDA, SFA_ERR_WORKSPAC
 SFA_BF16, SFA_F32, SFA_Q8_0 = 0, 1, 2
 SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_NSEL, SFA_DEV_BAD_QUERY, SFA_DEV_TIMEOUT = 1, 2, 4, 8
 SFA_DEV_BAD_CELL, SFA_DEV_FP16_RANGE = 16, 32
-SFA_REFINE_MAX_BLOCKS = 36864   # longest row sfa_topk_blocks_refine takes (one selection piece)
+SFA_PART_ALL, SFA_PART_SELECTED, SFA_PART_WINDOW = 0, 1, 2
+SFA_REFINE_MAX_BLOCKS = 131072  # longest row sfa_topk_blocks_refine takes
 
 _lib = None
 _vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
@@ -53,6 +54,11 @@ SIGNATURES = {
                                  _vp]),
     "sfa_dense_attend": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int, _int, _int,
                                 _f32, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "sfa_window_kv_max": (_i64, [_int, _int, _i64, _int]),
+    "sfa_gather_attend_window": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int, _int,
+                                        _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _i64, _int,
+                                        _vp, _vp, _vp, _sz, _vp, _vp]),
+    "sfa_combine_attention": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _vp, _vp, _vp]),
     "sfa_gather_attend_noalloc": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int,
                                          _int, _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _vp,
                                          _vp, _vp, _vp]),
@@ -271,6 +277,46 @@ def sfa_gather_attend(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int, compres
                                  _p(n_sel), top_k, compress_ratio, _p(O), _p(lse), _p(workspace),
                                  ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_gather_attend", rc)
+
+
+def sfa_window_kv_max(top_k: int, compress_ratio: int, window: int, part: int = 0) -> int:
+    return int(lib().sfa_window_kv_max(top_k, compress_ratio, window, part))
+
+
+def sfa_gather_attend_window(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,
+                             compress_ratio: int, window: int, scale: float, O, lse=None,
+                             part: int = SFA_PART_ALL, workspace=None, dev_status=None,
+                             stream=None):
+    """Attention over the kept blocks, the tail and a dense window of the `window` most recent
+    positions (part: the whole set, its kept part before the window, or the window suffix)."""
+    n_q, h_q, dkq, n_seq, n_tok_cap, h_kv, dv = _attn_dims(Q, K, V, O)
+    n_kv_max = sfa_window_kv_max(top_k, compress_ratio, window, part)
+    need = sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv_max)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sfa_gather_attend_window(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap,
+                                        n_q, h_q, h_kv, dkq, dv, float(scale), _p(q_seq),
+                                        _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
+                                        compress_ratio, int(window), int(part), _p(O), _p(lse),
+                                        _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
+    _check("sfa_gather_attend_window", rc)
+
+
+def sfa_combine_attention(O_a, lse_a, O_b, lse_b, O, lse, stream=None):
+    """O, lse = the attention over the union of two disjoint key sets, from each set's (O, lse)
+    ([rows][dv] and [rows] fp32; O / lse may be either input)."""
+    dv = O.shape[-1]
+    n_rows = O.numel() // dv
+    for t in (O_a, O_b, O):
+        if t.numel() != n_rows * dv or not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError("O_a, O_b, O must be contiguous fp32 tensors of one shape")
+    for t in (lse_a, lse_b, lse):
+        if t.numel() != n_rows or not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError("lse_a, lse_b, lse must be contiguous fp32 tensors of O's rows")
+    rc = lib().sfa_combine_attention(_p(O_a), _p(lse_a), _p(O_b), _p(lse_b), n_rows, dv, _p(O),
+                                     _p(lse), _stream(stream))
+    _check("sfa_combine_attention", rc)
 
 
 def sfa_gather_attend_noalloc(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,

@@ -6,7 +6,6 @@
 //
 // bf16 kernel (one CTA = one query x one KV head x one split of its list, 4 warps, two CTAs
 // per SM):
-//   * Q's A fragments go straight from global memory into registers;
 //   * cp.async 16-byte gathers of the selected token rows, 32 rows per stage (each kept block
 //     is cr contiguous rows), XOR-swizzled rows so that ldmatrix is conflict-free;
 //   * S = Q K^T on tensor cores (mma.sync m16n8k16, M = the 16 query heads of the KV head),
@@ -134,25 +133,26 @@ __device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, i
     return ok;
 }
 
-// Waits until at most n of this thread's cp.async groups are pending (n in 0 .. 4).
+// Waits until at most n of this thread's cp.async groups are pending (n in 0 .. 5).
 __device__ __forceinline__ void cp_async_wait_n(int n) {
     switch (n) {
         case 0: cp_async_wait<0>(); break;
         case 1: cp_async_wait<1>(); break;
         case 2: cp_async_wait<2>(); break;
         case 3: cp_async_wait<3>(); break;
-        default: cp_async_wait<4>(); break;
+        case 4: cp_async_wait<4>(); break;
+        default: cp_async_wait<5>(); break;
     }
 }
 
 // Shared memory of one CTA of the warp-level kernel with TT-token tiles: the K/V stages (Q8:
-// quantized rows, plus one binary16 tile), the S partials, P (hi, lo), the softmax statistics,
-// the token ids and the block list of its split.  The layout is attend_mma_body's.
+// quantized rows, plus one binary16 tile), Q, the S partials, P (hi, lo), the softmax
+// statistics, the token ids and the block list of its split.  The layout is attend_mma_body's.
 template <int DKQ, int DV, bool VK, bool Q8, int TT>
 __host__ __device__ constexpr size_t mma_smem_bytes(int stages, int blk_list) {
     return (size_t)stages * (Q8 ? TT * q8_row_bytes(DKQ) + (VK ? 0 : TT * q8_row_bytes(DV))
                                 : TT * DKQ * 2 + (VK ? 0 : TT * DV * 2)) +
-           (Q8 ? TT * DKQ * 2 + (VK ? 0 : TT * DV * 2) : 0) + 4 * 16 * (TT + 8) * 4 +
+           (Q8 ? TT * DKQ * 2 + (VK ? 0 : TT * DV * 2) : 0) + 16 * DKQ * 2 + 4 * 16 * (TT + 8) * 4 +
            2 * 16 * (TT + 8) * 2 + 48 * 4 + (size_t)stages * TT * 4 + (size_t)blk_list * 4 + 16;
 }
 
@@ -161,8 +161,6 @@ __host__ __device__ constexpr size_t mma_smem_bytes(int stages, int blk_list) {
 // to binary16, with Q converted to binary16 and every tensor-core product on binary16).
 // Tiles of TT tokens (16 or 32) stream through a ring of p.stages stages: tile t + stages - 1
 // is issued while tile t is scored, so stages - 1 tiles are in flight behind the one in use.
-// Q never passes through shared memory: each warp loads its A fragments straight from global
-// memory into registers.
 template <int DKQ, int DV, bool V_IS_K, bool Q8, int TT>
 __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     constexpr int KROW = DKQ * 2;                 // bytes of a K row in shared memory
@@ -185,7 +183,8 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *sStage = smem;                                              // stages x STAGE_BYTES
     uint8_t *sDeq = sStage + (size_t)p.stages * STAGE_BYTES;             // Q8: DEQ_BYTES
-    float *sSP = reinterpret_cast<float *>(sDeq + DEQ_BYTES);            // 4 x 16 x SP_PITCH
+    uint8_t *sQ = sDeq + DEQ_BYTES;                                      // 16 x KROW
+    float *sSP = reinterpret_cast<float *>(sQ + 16 * KROW);              // 4 x 16 x SP_PITCH
     __nv_bfloat16 *sP = reinterpret_cast<__nv_bfloat16 *>(sSP + 4 * 16 * SP_PITCH);  // hi, lo
     float *sAlpha = reinterpret_cast<float *>(sP + 2 * 16 * P_PITCH);    // 16
     float *sL = sAlpha + 16;                                             // 16
@@ -200,21 +199,6 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     const int G = p.G;
     pdl_wait();   // global memory from here on
     pdl_trigger();
-    // Q fragments of this warp's head-dim slice (A operand, rows >= G zero), loaded first so
-    // that their latency overlaps the list look-ups
-    uint32_t qa[KS][4];
-    {
-        const uint32_t *Qw = reinterpret_cast<const uint32_t *>(
-            reinterpret_cast<const __nv_bfloat16 *>(p.Q) + ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int col = (warp * KS + ks) * 8 + tq;   // 32-bit word of columns 2 tq, 2 tq + 1
-            qa[ks][0] = gq < G ? __ldg(Qw + gq * (DKQ / 2) + col) : 0u;
-            qa[ks][1] = gq + 8 < G ? __ldg(Qw + (gq + 8) * (DKQ / 2) + col) : 0u;
-            qa[ks][2] = gq < G ? __ldg(Qw + gq * (DKQ / 2) + col + 4) : 0u;
-            qa[ks][3] = gq + 8 < G ? __ldg(Qw + (gq + 8) * (DKQ / 2) + col + 4) : 0u;
-        }
-    }
     const ListInfo L = list_info(p, i, lead && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -246,20 +230,22 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         }
         return;
     }
-    const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
-    if constexpr (Q8) {   // Q to binary16 in registers: this path's tensor-core operand type
-        bool ok = true;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t w = qa[ks][e];
-                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
-                ok &= fabsf(lo) < 65520.f && fabsf(hi) < 65520.f;
-                qa[ks][e] = pack_f16(lo, hi);
-            }
-        if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+    // Q rows of this KV head (rows >= G zero-filled), swizzled like the K tile: copied
+    // asynchronously as the oldest cp.async group, so the copy overlaps the block-list reads
+    // and the first K/V tiles.
+    {
+        const __nv_bfloat16 *Qg = reinterpret_cast<const __nv_bfloat16 *>(p.Q) +
+                                  ((int64_t)i * p.h_q + (int64_t)g * G) * DKQ;
+        const uint32_t qs = smem_u32(sQ);
+        for (int e = tid; e < 16 * KCH; e += kThreads) {
+            const int r = e / KCH, c = e % KCH;
+            const bool live = r < G;
+            cp_async16(qs + r * KROW + swz(c, r) * 16, live ? Qg + (int64_t)r * DKQ + c * 8 : Qg,
+                       live ? 16u : 0u);
+        }
+        cp_async_commit();
     }
+    const int jb0 = load_block_list(p, i, L, j0, j1, sBlk, g == 0);
     __syncthreads();
 
     const KElem *Kseq = reinterpret_cast<const KElem *>(p.K) + (int64_t)L.seq * p.k_seq_stride +
@@ -316,10 +302,43 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         }
     };
 
-    // prologue: stages-1 tiles in flight
+    // prologue: stages-1 tiles in flight (behind the Q group)
     for (int t = 0; t < p.stages - 1; ++t) {
         if (t < n_tiles) issue_tile(t);
         cp_async_commit();
+    }
+    // Q has landed once at most stages-1 younger groups are pending
+    cp_async_wait_n(p.stages - 1);
+    __syncthreads();
+    if constexpr (Q8) {   // Q to binary16 in place: this path's tensor-core operand type
+        bool ok = true;
+        for (int e = tid; e < 16 * KCH; e += kThreads) {
+            const int r = e / KCH, c = e % KCH;
+            uint4 *q4 = reinterpret_cast<uint4 *>(sQ + r * KROW + swz(c, r) * 16);
+            const uint4 u = *q4;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+                ok &= fabsf(lo) < 65520.f && fabsf(hi) < 65520.f;
+                h[k] = pack_f16(lo, hi);
+            }
+            *q4 = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+        __syncthreads();
+    }
+    // Q fragments of this warp's head-dim slice (A operand, kept in registers)
+    uint32_t qa[KS][4];
+    {
+        const uint32_t q_base = smem_u32(sQ);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int kg = warp * KS + ks;
+            const int r = lane & 15, c = kg * 2 + (lane >> 4);
+            ldsm_x4(q_base + r * KROW + swz(c, r) * 16, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+        }
     }
 
     float o[NTV][4];
@@ -428,11 +447,9 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         // ---- O = O * alpha + P V over this warp's value-dim slice
         {
             const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
-            if (__any_sync(0xFFFFFFFFu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-                for (int n = 0; n < NTV; ++n) {
-                    o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
-                }
+            for (int n = 0; n < NTV; ++n) {
+                o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
             }
             const uint32_t pbase = smem_u32(sP);
 #pragma unroll
@@ -1218,6 +1235,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p, int dv
     }
 }
 
+// The attention over the union of two disjoint key sets from the attentions over each: one
+// warp per (query, head) row; lane 0 reads both log-sum-exps, the lanes scale and add the
+// row's values, and lane 0 writes the new log-sum-exp after the whole row is read (so that
+// O and lse may overwrite either input).
+__global__ void __launch_bounds__(128) combine2_kernel(const float4 *Oa, const float *la,
+                                                      const float4 *Ob, const float *lb,
+                                                      int64_t n_rows, int dv4, float4 *O,
+                                                      float *lse) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (r >= n_rows) return;
+    float a = -INFINITY, b = -INFINITY;
+    if (lane == 0) {
+        a = la[r];
+        b = lb[r];
+    }
+    a = __shfl_sync(0xFFFFFFFFu, a, 0);
+    b = __shfl_sync(0xFFFFFFFFu, b, 0);
+    const float M = fmaxf(a, b);
+    const float wa = M == -INFINITY ? 0.f : expf(a - M);
+    const float wb = M == -INFINITY ? 0.f : expf(b - M);
+    const float inv = wa + wb > 0.f ? 1.f / (wa + wb) : 0.f;
+    for (int d = lane; d < dv4; d += 32) {
+        const float4 x = Oa[r * dv4 + d], y = Ob[r * dv4 + d];
+        O[r * dv4 + d] = make_float4((wa * x.x + wb * y.x) * inv, (wa * x.y + wb * y.y) * inv,
+                                     (wa * x.z + wb * y.z) * inv, (wa * x.w + wb * y.w) * inv);
+    }
+    __syncwarp();
+    if (lane == 0) lse[r] = M == -INFINITY ? -INFINITY : M + logf(wa + wb);
+}
+
 // ------------------------------------------------------------------------------ host side
 struct SplitPlan {
     int n_split, split_tokens;
@@ -1489,7 +1539,8 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
                const int32_t *q_seq, const int32_t *q_pos, const int32_t *blk_idx,
                const int32_t *n_sel, int top_k, int cr, int dense, int64_t n_kv_max, float *O,
                float *lse, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t st,
-               const int32_t *cell_of = nullptr, int64_t n_cells = 0) {
+               const int32_t *cell_of = nullptr, int64_t n_cells = 0, int64_t window = 0,
+               int part = SFA_PART_ALL) {
     if (!Q || !K || !q_seq || !q_pos || !O) return SFA_ERR_INVALID_ARG;
     if (dtype != SFA_BF16 && dtype != SFA_F32 && dtype != SFA_Q8_0) return SFA_ERR_INVALID_ARG;
     if (n_seq < 1 || n_tok_cap < 1 || n_q < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0)
@@ -1536,6 +1587,8 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.cluster_merge = cluster_ns > 1;
     p.n_items = n_q * h_kv * sp.n_split;
     p.n_kv_max = n_kv_max;
+    p.window = window;
+    p.part = part;
     p.scale_log2 = scale * kLog2e;
     if (sp.n_split > 1) {
         const size_t n_rows = (size_t)n_q * h_q * sp.n_split;
@@ -1619,6 +1672,53 @@ extern "C" int sfa_gather_attend(const void *Q, const void *K, const void *V, in
     return sfa::run_attend(Q, K, V, dtype, n_seq, n_tok_cap, n_q, h_q, h_kv, dkq, dv, scale,
                            q_seq, q_pos, blk_idx, n_sel, top_k, compress_ratio, 0, n_kv_max, O,
                            lse, workspace, workspace_bytes, dev_status, (cudaStream_t)stream);
+}
+
+extern "C" int64_t sfa_window_kv_max(int top_k, int compress_ratio, int64_t window, int part) {
+    if (top_k < 1 || compress_ratio < 1 || window < 0) return 0;
+    const int64_t kept = (int64_t)top_k * compress_ratio;
+    // the suffix s0 .. p holds at most max(window, cr - 1) positions
+    const int64_t suffix = window > compress_ratio - 1 ? window : compress_ratio - 1;
+    if (part == SFA_PART_SELECTED) return kept;
+    if (part == SFA_PART_WINDOW) return suffix > 0 ? suffix : 1;
+    return kept + suffix;
+}
+
+extern "C" int sfa_gather_attend_window(const void *Q, const void *K, const void *V, int dtype,
+                                        int n_seq, int64_t n_tok_cap, int n_q, int h_q, int h_kv,
+                                        int dkq, int dv, float scale, const int32_t *q_seq,
+                                        const int32_t *q_pos, const int32_t *blk_idx,
+                                        const int32_t *n_sel, int top_k, int compress_ratio,
+                                        int64_t window, int part, float *O, float *lse,
+                                        void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_status, sfa_stream_t stream) {
+    if (compress_ratio < 1 || top_k < 1 || window < 0) return SFA_ERR_INVALID_ARG;
+    if (part != SFA_PART_ALL && part != SFA_PART_SELECTED && part != SFA_PART_WINDOW)
+        return SFA_ERR_INVALID_ARG;
+    const int64_t n_kv_max = sfa_window_kv_max(top_k, compress_ratio, window, part);
+    return sfa::run_attend(Q, K, V, dtype, n_seq, n_tok_cap, n_q, h_q, h_kv, dkq, dv, scale,
+                           q_seq, q_pos, blk_idx, n_sel, top_k, compress_ratio, 0, n_kv_max, O,
+                           lse, workspace, workspace_bytes, dev_status, (cudaStream_t)stream,
+                           nullptr, 0, window, part);
+}
+
+extern "C" int sfa_combine_attention(const float *O_a, const float *lse_a, const float *O_b,
+                                     const float *lse_b, int64_t n_rows, int dv, float *O,
+                                     float *lse, sfa_stream_t stream) {
+    using namespace sfa;
+    if (!O_a || !lse_a || !O_b || !lse_b || !O || !lse || n_rows < 0 || dv < 4 || dv % 4)
+        return SFA_ERR_INVALID_ARG;
+    if (!aligned16(O_a) || !aligned16(O_b) || !aligned16(O)) return SFA_ERR_INVALID_ARG;
+    if (n_rows == 0) return SFA_OK;
+    if ((n_rows + 3) / 4 > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
+    if (launch_pdl(combine2_kernel, dim3((unsigned)((n_rows + 3) / 4)), dim3(128), 0,
+                   (cudaStream_t)stream, reinterpret_cast<const float4 *>(O_a), lse_a,
+                   reinterpret_cast<const float4 *>(O_b), lse_b, n_rows, dv / 4,
+                   reinterpret_cast<float4 *>(O), lse) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    return SFA_OK;
 }
 
 extern "C" int sfa_dense_attend(const void *Q, const void *K, const void *V, int dtype,

@@ -31,6 +31,8 @@ struct AttnParams {
     int cluster_merge;   // 1: the n_split CTAs of an item form one cluster and merge in place
     int n_items;         // n_q * h_kv * n_split work items (query, KV head, split)
     int64_t n_kv_max;    // the caller's bound on every list's length
+    int64_t window;      // > 0: the window positions p - window + 1 .. p are attended too
+    int part;            // SFA_PART_*: the whole list, its kept part, or its window part
     float scale_log2;
 };
 
@@ -57,7 +59,9 @@ struct ListInfo {
     int seq, pos;
     int len;       // list length
     int n_blk_tok; // n_sel * cr: positions [0, n_blk_tok) come from kept blocks
-    int tail0;     // first tail token (B * cr)
+    int tail0;     // first token of the suffix attended in full: the tail (B * cr), or the
+                   // window's first position when a window reaches further back; kept
+                   // tokens from here on are left out of the kept part (padding)
 };
 
 __device__ __forceinline__ ListInfo list_info(const AttnParams &p, int i, bool flag) {
@@ -88,9 +92,15 @@ __device__ __forceinline__ ListInfo list_info(const AttnParams &p, int i, bool f
         if (flag) set_status(p.status, SFA_DEV_BAD_NSEL);
         ns = ns < 0 ? 0 : ns_max;
     }
-    L.n_blk_tok = ns * p.cr;
-    L.tail0 = B * p.cr;
-    L.len = L.n_blk_tok + (L.pos + 1 - L.tail0);
+    // the suffix attended in full: the tail, or the window when it starts earlier
+    int64_t s0 = (int64_t)B * p.cr;
+    if (p.window > 0) {
+        const int64_t w0 = (int64_t)L.pos - p.window + 1;
+        s0 = min(s0, w0 < 0 ? (int64_t)0 : w0);
+    }
+    L.tail0 = (int)s0;
+    L.n_blk_tok = p.part == SFA_PART_WINDOW ? 0 : ns * p.cr;
+    L.len = L.n_blk_tok + (p.part == SFA_PART_SELECTED ? 0 : L.pos + 1 - L.tail0);
     return L;
 }
 
@@ -124,7 +134,8 @@ __device__ __forceinline__ int token_at(const AttnParams &p, const ListInfo &L, 
     if (j < L.n_blk_tok) {
         const int jb = j / p.cr;
         const int b = s_blk[jb - jb0];
-        return b < 0 ? -1 : b * p.cr + (j - jb * p.cr);
+        const int t = b * p.cr + (j - jb * p.cr);
+        return b < 0 || t >= L.tail0 ? -1 : t;   // kept tokens inside the suffix: padding
     }
     return L.tail0 + (j - L.n_blk_tok);
 }

@@ -468,14 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- O = O * alpha + P V over this warp's value dims
             {
                 const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
-                if (__any_sync(0xFFFFFFFFu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-                    for (int n = 0; n < NTV; ++n) {
-                        o[n][0] *= a0;
-                        o[n][1] *= a0;
-                        o[n][2] *= a1;
-                        o[n][3] *= a1;
-                    }
+                for (int n = 0; n < NTV; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
                 }
 #pragma unroll
                 for (int ks = 0; ks < kTT / 16; ++ks) {

@@ -628,9 +628,13 @@ __device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int
 //   4. the leader selects the top k of the list.
 // Lists longer than 4096 go through global memory (select_global_list).
 constexpr int kCl = 4;                                       // CTAs per row
-constexpr int kClRounds = (kChunk / kCl + 4 * kThreads - 1) / (4 * kThreads);   // 3 rounds
-static_assert(kClRounds * 4 * kThreads >= kChunk / kCl, "a quarter of the longest row fits the rounds");
-static_assert(4 * kClRounds <= 32, "one candidate bit per element in a 32-bit mask");
+// Rounds of 4 * kThreads elements a CTA takes of its quarter of the row: 3 for rows of up to
+// one selection piece (36864 blocks), 8 for rows of up to 131072 blocks.
+constexpr int kClRoundsShort = (kChunk / kCl + 4 * kThreads - 1) / (4 * kThreads);   // 3
+constexpr int kClRoundsLong = 8;
+constexpr int64_t kRefineMaxLong = (int64_t)kCl * kClRoundsLong * 4 * kThreads;     // 131072
+static_assert(kClRoundsShort * 4 * kThreads >= kChunk / kCl, "a quarter of a piece fits the rounds");
+static_assert(4 * kClRoundsLong <= 32, "one candidate bit per element in a 32-bit mask");
 
 struct RefineParams {
     const float *lower, *upper;
@@ -652,12 +656,13 @@ struct RefineParams {
 // + h) * 32 + lane holds the pair of registers for heads 8 nt .. 8 nt + 7 and the k-step (pair
 // pq, half h) of the column order the A loads use (see rescore_tile).
 constexpr int kPq = 4;   // q dims / 32 (D <= 128)
+template <int R>
 struct BoundedSmem {
     Smem sh;                        // the leader's candidate list serves the cluster
-    float up[kChunk / kCl];         // this quarter's upper bounds (cp.async)
+    float up[R * 4 * kThreads];     // this quarter's upper bounds (cp.async)
     uint2 qf[2 * kPq * 2 * 32];
     float w[16];
-    int woff[kClRounds * kWarps];   // per (round, warp): this CTA's candidates before it
+    int woff[R * kWarps];           // per (round, warp): this CTA's candidates before it
     uint32_t ext_max[kCl], ext_min[kCl];   // leader slots, per rank
     int cnt[kCl];
     uint32_t lo;
@@ -670,9 +675,9 @@ struct BoundedSmem {
 // four those of (pp, 1).  The B table pairs the same columns with q (dims mod D), so each
 // k-step sums over 16 distinct columns and the pieces cover all 2D.  Returns the score of row
 // g (lanes with t == 0) and of row g + 8 through s0, s1.
-template <int D>
+template <int D, typename BS>
 __device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv_bfloat16 *r1,
-                                             const BoundedSmem &bs, int H, float &s0, float &s1) {
+                                             const BS &bs, int H, float &s0, float &s1) {
     constexpr int kPieces = 2 * D / 32;   // 8 or 4
     constexpr int kG = kPieces < 4 ? kPieces : 4;   // pieces in flight
     const int lane = threadIdx.x & 31, t = lane & 3;
@@ -721,15 +726,17 @@ __device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv
     s1 = p1s;
 }
 
-template <int D>
+template <int D, int R>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     bounded_select_kernel(const RefineParams p, int n_q) {
+    constexpr int kClRounds = R;
+    using BS = BoundedSmem<R>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    BoundedSmem &bs = *reinterpret_cast<BoundedSmem *>(smem_raw);
+    BS &bs = *reinterpret_cast<BS *>(smem_raw);
     Smem &sh = bs.sh;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    BoundedSmem &lead = *cluster.map_shared_rank(&bs, 0);
+    BS &lead = *cluster.map_shared_rank(&bs, 0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = p.top_k, H = p.H;
     const int n_cl = gridDim.x / kCl;
@@ -1004,22 +1011,28 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     cluster.sync();   // no CTA leaves while another may still address its shared memory
 }
 
-template <int D>
+template <int D, int R>
 int launch_bounded_d(const RefineParams &p, int n_q, cudaStream_t st) {
-    if (!ensure_max_dynamic_smem(bounded_select_kernel<D>)) return SFA_ERR_CUDA;
+    if (!ensure_max_dynamic_smem(bounded_select_kernel<D, R>)) return SFA_ERR_CUDA;
     int clusters = device_sm_count() / kCl;
     if (clusters < 1) return SFA_ERR_CUDA;
     if (n_q < clusters) clusters = n_q;
-    if (launch_pdl(bounded_select_kernel<D>, dim3(clusters * kCl), dim3(kThreads),
-                   sizeof(BoundedSmem), st, p, n_q) != cudaSuccess) {
+    if (launch_pdl(bounded_select_kernel<D, R>, dim3(clusters * kCl), dim3(kThreads),
+                   sizeof(BoundedSmem<R>), st, p, n_q) != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
     }
     return SFA_OK;
 }
 
+// Rows of up to one selection piece take 3 rounds per CTA; longer rows (up to 131072 blocks)
+// take 8, with a quarter's upper bounds (128 KB) in shared memory.
 int launch_bounded(const RefineParams &p, int n_q, cudaStream_t st) {
-    return p.D == 64 ? launch_bounded_d<64>(p, n_q, st) : launch_bounded_d<128>(p, n_q, st);
+    if (p.n_blk_max <= kChunk)
+        return p.D == 64 ? launch_bounded_d<64, kClRoundsShort>(p, n_q, st)
+                         : launch_bounded_d<128, kClRoundsShort>(p, n_q, st);
+    return p.D == 64 ? launch_bounded_d<64, kClRoundsLong>(p, n_q, st)
+                     : launch_bounded_d<128, kClRoundsLong>(p, n_q, st);
 }
 
 // The levels for rows of up to n_blk_max scores: lengths per row at each level (n[0] =
@@ -1162,7 +1175,7 @@ extern "C" int sfa_topk_blocks_refine(const float *lower, const float *upper,
     if (top_k < 1 || top_k > 2048) return SFA_ERR_UNSUPPORTED;
     if (d_idx != 64 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
     if (h_idx < 1 || h_idx > 16) return SFA_ERR_UNSUPPORTED;
-    if (n_blk_max > kChunk) return SFA_ERR_UNSUPPORTED;   // one piece per row
+    if (n_blk_max > kRefineMaxLong) return SFA_ERR_UNSUPPORTED;   // 8 rounds per quarter
     if (n_blk_max > 0 && (!lower || !upper || score_stride < n_blk_max))
         return SFA_ERR_INVALID_ARG;
     if (kbar_seq_stride < n_blk_max * 2 * d_idx) return SFA_ERR_INVALID_ARG;

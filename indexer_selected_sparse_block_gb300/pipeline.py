@@ -5,13 +5,18 @@ kept block lists, workspaces, outputs) and runs the stages as the C entry points
 
   sfa_pool_index_keys -> sfa_index_scores -> sfa_topk_blocks -> sfa_gather_attend
 
-(decode-like steps -- few queries per sequence, rows of at most 36864 blocks -- take
+(decode-like steps -- few queries per sequence, rows of at most 131072 blocks -- take
 sfa_index_scores_bounded -> sfa_topk_blocks_refine for the middle two: the same kept sets from
 half the pooled-key bytes plus the rescoring of the few blocks the bounds cannot rule out)
 
 or, when every query is below the budget (B_i <= indexer_top_k for all i), the dense case
 ``sfa_dense_attend``: every block then fits the budget, so the method is exactly dense
 attention (llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).
+
+With ``window > 0`` the attention also covers the ``window`` most recent positions densely
+(the dense + sparse + combine variant of PR #27970's review discussion): in one pass over the
+whole set, or (``window_mode="split"``) as the kept part and the window part attended apart and
+merged by ``sfa_combine_attention``.
 
 With a position -> cell map (``cell_of``), the caches are flat cell arrays in any order (a
 paged serving cache) and the pool and the attention take their ``_paged`` entry points; the
@@ -30,7 +35,7 @@ class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
                  n_blk_max: int, q_group: int = 1, bounded=None, key_transform=None,
-                 cell_of=None, device="cuda"):
+                 cell_of=None, window: int = 0, window_mode: str = "single", device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -54,7 +59,7 @@ class SfaStep:
         # The bounded selection (hi-only scores + exact rescoring of the blocks the bounds
         # cannot rule out) halves the pooled-key bytes of decode-like steps, where each query
         # streams its sequence's pooled keys; prefill tiles share those reads and take the
-        # exact scores directly.  Rows must fit one selection piece (36864 blocks).
+        # exact scores directly.  Rows of at most 131072 blocks.
         if bounded is None:
             bounded = q_group <= 4 and n_blk_max <= B.SFA_REFINE_MAX_BLOCKS
         self.bounded = bool(bounded) and not self.dense
@@ -73,13 +78,24 @@ class SfaStep:
         self.n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
         nt = B.sfa_topk_workspace_bytes(n_q, max(n_blk_max, 1), indexer_top_k)
         self.topk_ws = torch.empty(max(nt, 16), dtype=torch.uint8, device=dev)
+        # the dense window of recent keys beside the kept blocks (window > 0): one pass over
+        # the whole set ("single"), or the kept part and the window part attended apart and
+        # combined by their log-sum-exp ("split")
+        if window < 0 or window_mode not in ("single", "split"):
+            raise ValueError("window must be >= 0 and window_mode 'single' or 'split'")
+        if window and cell_of is not None:
+            raise ValueError("the windowed attention takes the per-sequence layout")
+        self.window, self.window_mode = int(window), window_mode
         self.n_kv_dense = n_tok_cap
         n_kv = (n_tok_cap if self.dense else
-                indexer_top_k * compress_ratio + compress_ratio - 1)
+                B.sfa_window_kv_max(indexer_top_k, compress_ratio, self.window, 0))
         na = B.sfa_attend_workspace_bytes(n_q, h_q, h_kv, dv, n_kv)
         self.attn_ws = torch.empty(max(na, 16), dtype=torch.uint8, device=dev)
         self.O = torch.empty((n_q, h_q, dv), dtype=torch.float32, device=dev)
         self.lse = torch.empty((n_q, h_q), dtype=torch.float32, device=dev)
+        if self.window and window_mode == "split" and not self.dense:
+            self.O_win = torch.empty_like(self.O)
+            self.lse_win = torch.empty_like(self.lse)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def pool(self, X, blk_begin: int, blk_end: int, stream=None):
@@ -136,6 +152,20 @@ class SfaStep:
             B.sfa_dense_attend(Q, K, V, q_seq, q_pos, self.n_kv_dense, scale, self.O,
                                lse=self.lse, workspace=self.attn_ws, dev_status=self.status,
                                stream=stream)
+        elif self.window and self.window_mode == "single":
+            B.sfa_gather_attend_window(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel,
+                                       self.top_k, self.cr, self.window, scale, self.O,
+                                       lse=self.lse, part=B.SFA_PART_ALL, workspace=self.attn_ws,
+                                       dev_status=self.status, stream=stream)
+        elif self.window:
+            for part, O, lse in ((B.SFA_PART_SELECTED, self.O, self.lse),
+                                 (B.SFA_PART_WINDOW, self.O_win, self.lse_win)):
+                B.sfa_gather_attend_window(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel,
+                                           self.top_k, self.cr, self.window, scale, O, lse=lse,
+                                           part=part, workspace=self.attn_ws,
+                                           dev_status=self.status, stream=stream)
+            B.sfa_combine_attention(self.O, self.lse, self.O_win, self.lse_win, self.O,
+                                    self.lse, stream=stream)
         else:
             B.sfa_gather_attend(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel, self.top_k,
                                 self.cr, scale, self.O, lse=self.lse, workspace=self.attn_ws,

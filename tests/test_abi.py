@@ -114,8 +114,8 @@ def test_bounded_entry_points_reject_bad_arguments(L):
     #     lower upper stride q_idx w  q_seq q_pos n_q h  d   Kbar  kstride    n_seq cr top_k nbm
     ok = [FAKE, FAKE, 100, FAKE, FAKE, FAKE, FAKE, 4, 8, 128, FAKE, 256 * 100, 1, 4, 16, 100,
           FAKE, FAKE, FAKE, 1 << 20, None, None]
-    bad = list(ok); bad[15] = 40000
-    assert g(*bad) == 2                                                    # rows > 36864
+    bad = list(ok); bad[15] = 131073
+    assert g(*bad) == 2                                                    # rows > 131072
     bad = list(ok); bad[14] = 0
     assert g(*bad) == 2                                                    # top_k
     bad = list(ok); bad[10] = ODD

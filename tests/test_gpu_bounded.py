@@ -179,13 +179,44 @@ def test_bounded_step_full_size_all(dev, name):
     _check_queries(w, case, step)
 
 
-def test_bounded_step_rejects_long_rows(dev):
+def test_bounded_step_rejects_rows_past_the_limit(dev):
     w = sfa.WORKLOADS["decode_4x1048576"]
     with pytest.raises(ValueError):
-        sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
+        sfa.SfaStep(n_seq=1, n_tok_cap=8 * 131073 + 8, n_q=1, h_q=w.h_q, h_kv=w.h_kv,
                     dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                     compress_ratio=w.compress_ratio, indexer_top_k=w.indexer_top_k,
-                    n_blk_max=w.n_tok // w.compress_ratio, q_group=1, bounded=True, device=dev)
+                    n_blk_max=131073, q_group=1, bounded=True, device=dev)
+
+
+@pytest.mark.parametrize("pos", [[1048575, 1000000, 600000, 296000]])
+def test_refine_long_rows(dev, pos):
+    """Rows past one selection piece (up to 131072 blocks at cr 8): each CTA of the row's
+    cluster takes eight rounds of 4096 blocks; selections follow the agreement rule."""
+    cr, d_idx, h_idx, top_k = 8, 128, 8, 256
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 778, 1, 1048576, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), 131072
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Xh, qh, wh = np32(X), np32(qi), np32(w)
+    got, gn = np32(blk), np32(n_sel)
+    kb = oracle.pool(Xh[0], (max(pos) + 1) // cr, cr)
+    n_exact = 0
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        sc = oracle.index_scores(qh[i], wh[i], kb[:B])
+        ok, exact = check_selection(got[i], int(gn[i]), sc, top_k)
+        assert ok, (i, p)
+        n_exact += exact
+    assert n_exact >= len(pos) - 1
 
 
 def test_refine_longest_rows(dev):

@@ -29,18 +29,18 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _step_for(w, dev, top_k=None, bounded=None):
+def _step_for(w, dev, top_k=None, bounded=None, **kw):
     n_blk_max = w.n_tok // w.compress_ratio
     return sfa.SfaStep(n_seq=w.n_seq, n_tok_cap=w.n_tok, n_q=w.n_q, h_q=w.h_q, h_kv=w.h_kv,
                        dkq=w.dkq, dv=w.dv, h_idx=w.h_idx, d_idx=w.d_idx,
                        compress_ratio=w.compress_ratio,
                        indexer_top_k=top_k or w.indexer_top_k, n_blk_max=n_blk_max,
-                       q_group=w.n_q_per_seq, bounded=bounded, device=dev)
+                       q_group=w.n_q_per_seq, bounded=bounded, device=dev, **kw)
 
 
-def _run(w, dev, top_k=None, bounded=None):
+def _run(w, dev, top_k=None, bounded=None, **kw):
     case = sfa.make_case(w, device=dev)
-    step = _step_for(w, dev, top_k, bounded)
+    step = _step_for(w, dev, top_k, bounded, **kw)
     step.pool(case["X"], 0, step.n_blk_max)
     step.run(case["X"], case["K"], case["V"], case["Q"], case["q_idx"], case["w"],
              case["q_seq"], case["q_pos"], w.scale)
@@ -49,7 +49,7 @@ def _run(w, dev, top_k=None, bounded=None):
     return case, step
 
 
-def _oracle_query(w, case, i, kb, got_sel, got_n, top_k):
+def _oracle_query(w, case, i, kb, got_sel, got_n, top_k, window=0):
     """The oracle for query i from its sequence's pooled keys kb (blocks 0 .. B_max - 1):
     scores, selection, attended-set mask and exact attention over the kept rows only.  The
     GPU's kept blocks are checked with the agreement rule; where the oracle's gap at the cut
@@ -64,7 +64,7 @@ def _oracle_query(w, case, i, kb, got_sel, got_n, top_k):
     sel, n = oracle.select(sc, top_k)
     if not exact and ok:      # attend the GPU's own set
         sel, n = np.asarray(got_sel, np.int32), int(got_n)
-    msk = oracle.mask(p, cr, sel, n)
+    msk = oracle.mask(p, cr, sel, n, window=window)
     toks = np.nonzero(msk)[0]
     rows = np.full(p + 1, -1, np.int64)
     rows[toks] = np.arange(len(toks))
@@ -76,7 +76,7 @@ def _oracle_query(w, case, i, kb, got_sel, got_n, top_k):
     return ok, exact, ref, lse
 
 
-def _check_queries(w, case, step, queries=None, tol=TOL_BF16):
+def _check_queries(w, case, step, queries=None, tol=TOL_BF16, window=0):
     """Checks every query of the step (or the given ones) against the oracle, element by
     element: kept blocks by the agreement rule, outputs and log-sum-exp within ``tol``.
 
@@ -106,7 +106,7 @@ def _check_queries(w, case, step, queries=None, tol=TOL_BF16):
         out = []
         for i in qs:
             ok, exact, ref, lse = _oracle_query(w, case, i, kb, got_sel[i], int(got_n[i]),
-                                                step.top_k)
+                                                step.top_k, window=window)
             out.append((i, ok, exact, float(row_rel_err(O[i], ref).max()),
                         float(np.abs(L[i] - lse).max())))
         return out
@@ -204,9 +204,13 @@ def test_decode_cr1_32x32768_all(dev):
     _check_queries(w, case, step)
 
 
-def test_decode_4x1048576_all(dev):
+@pytest.mark.parametrize("bounded", [None, False])
+def test_decode_4x1048576_all(dev, bounded):
+    """The 1M-token decode (rows of 131072 blocks at cr 8) with the bounded selection it takes
+    by default, and with the exact scores and select forced; all 4 queries."""
     w = sfa.WORKLOADS["decode_4x1048576"]
-    case, step = _run(w, dev)
+    case, step = _run(w, dev, bounded=bounded)
+    assert step.bounded == (bounded is None)
     _check_queries(w, case, step)
 
 
