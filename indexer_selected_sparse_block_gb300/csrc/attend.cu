@@ -107,28 +107,58 @@ __device__ __forceinline__ float round16(float x) {
 // into binary16 rows of the swizzled tile layout (pitch 2*D bytes): element j of a row is
 // scale(j / 32) * code_j, exact in fp32, then rounded to binary16.  Zero-filled rows (padding)
 // give zeros.  Returns false when a value exceeds binary16's range.
-template <int D, int SROW, int TT>
-__device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, int tid) {
-    constexpr int C8 = D / 8;   // 8-element chunks per row
+// Four int8 codes (one 32-bit word) -> two pairs of binary16 values, exactly: each biased code
+// c + 128 becomes the low byte of binary16 1024 + (c + 128) (a byte permute), and subtracting
+// 1152 leaves c.
+__device__ __forceinline__ void codes_to_f16(uint32_t w, __half2 &c01, __half2 &c23) {
+    const uint32_t b = w ^ 0x80808080u;
+    const uint32_t h01 = __byte_perm(b, 0x64646464u, 0x5140u);
+    const uint32_t h23 = __byte_perm(b, 0x64646464u, 0x7362u);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480u));   // 1152
+    c01 = __hsub2(*reinterpret_cast<const __half2 *>(&h01), bias);
+    c23 = __hsub2(*reinterpret_cast<const __half2 *>(&h23), bias);
+}
+
+// Chunks [c0, c0 + NC) of 8 elements of every row of the tile, by the threads first, first +
+// stride, ...
+template <int D, int SROW, int TT, int NC>
+__device__ __forceinline__ bool dequant_tile(const uint8_t *src, uint8_t *dst, int c0, int first,
+                                             int stride) {
     bool ok = true;
-    for (int e = tid; e < TT * C8; e += kThreads) {
-        const int r = e / C8, c = e - r * C8;
+    for (int e = first; e < TT * NC; e += stride) {
+        const int r = e / NC, c = c0 + (e - r * NC);
         const uint8_t *row = src + r * SROW;
         const uint2 w = *reinterpret_cast<const uint2 *>(row + c * 8);
-        const float sc = __half2float(*reinterpret_cast<const __half *>(row + D + (c >> 2) * 2));
-        float v[8];
+        const __half s = *reinterpret_cast<const __half *>(row + D + (c >> 2) * 2);
+        uint4 out;
+        if (fabsf(__half2float(s)) * 127.f < 65520.f) {
+            // scale * code is exact in binary32 (11 x 8 significant bits) and one binary16
+            // multiply rounds that exact product once, as the conversion of the binary32
+            // product does
+            const __half2 s2 = __half2half2(s);
+            __half2 c0, c1, c2, c3;
+            codes_to_f16(w.x, c0, c1);
+            codes_to_f16(w.y, c2, c3);
+            const __half2 v0 = __hmul2(c0, s2), v1 = __hmul2(c1, s2), v2 = __hmul2(c2, s2),
+                          v3 = __hmul2(c3, s2);
+            out = make_uint4(*reinterpret_cast<const uint32_t *>(&v0),
+                             *reinterpret_cast<const uint32_t *>(&v1),
+                             *reinterpret_cast<const uint32_t *>(&v2),
+                             *reinterpret_cast<const uint32_t *>(&v3));
+        } else {   // a scale that can overflow binary16: the binary32 path, with the range check
+            const float sc = __half2float(s);
+            float v[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            v[k] = sc * (float)(int8_t)(w.x >> (8 * k));
-            v[4 + k] = sc * (float)(int8_t)(w.y >> (8 * k));
-        }
-        if (fabsf(sc) * 127.f >= 65520.f) {
+            for (int k = 0; k < 4; ++k) {
+                v[k] = sc * (float)(int8_t)(w.x >> (8 * k));
+                v[4 + k] = sc * (float)(int8_t)(w.y >> (8 * k));
+            }
 #pragma unroll
             for (int k = 0; k < 8; ++k) ok &= fabsf(v[k]) < 65520.f;
+            out = make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
+                             pack_f16(v[6], v[7]));
         }
-        *reinterpret_cast<uint4 *>(dst + r * (2 * D) + swz(c, r) * 16) =
-            make_uint4(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]), pack_f16(v[4], v[5]),
-                       pack_f16(v[6], v[7]));
+        *reinterpret_cast<uint4 *>(dst + r * (2 * D) + swz(c, r) * 16) = out;
     }
     return ok;
 }
@@ -354,12 +384,18 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         cp_async_commit();
 
         const int st = t % p.stages;
-        if constexpr (Q8) {   // tile t from its q8_0 rows into the binary16 tile
+        if constexpr (Q8) {
+            // tile t from its q8_0 rows into the binary16 tile: each warp converts the K
+            // columns of its own head-dim slice (all it reads for S) and, with a separate V,
+            // the V columns of its value-dim slice; the block barrier after the S partials
+            // publishes the whole tile before any warp reads V columns of another's slice
             const uint8_t *stg = sStage + (size_t)st * STAGE_BYTES;
-            bool ok = dequant_tile<DKQ, QKROW, TT>(stg, sDeq, tid);
-            if constexpr (!V_IS_K) ok &= dequant_tile<DV, QVROW, TT>(stg + TT * QKROW, sDeq + TT * KROW, tid);
+            bool ok = dequant_tile<DKQ, QKROW, TT, DKQ / 32>(stg, sDeq, warp * (DKQ / 32), lane, 32);
+            if constexpr (!V_IS_K)
+                ok &= dequant_tile<DV, QVROW, TT, DV / 32>(stg + TT * QKROW, sDeq + TT * KROW,
+                                                            warp * (DV / 32), lane, 32);
             if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
-            __syncthreads();
+            __syncwarp();
         }
         const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
         const uint32_t vbase = V_IS_K ? kbase : kbase + TT * KROW;
