@@ -321,6 +321,30 @@ def read_floor(nbytes, flush, dev, reps=10):
     return best
 
 
+def gather_ceiling(wb, flush, reps=10):
+    """Device time of sfa_gather_kv_bandwidth on the step's own kept lists (L2 flushed before
+    each rep, as before the timed steps): the K/V rows the attention gathers, moved into shared
+    memory with nothing computed -- the attention's data-movement ceiling on these lists."""
+    w, st, c = wb.w, wb.step, wb.case
+    if w.dkq not in (576, 512) or wb.kv != "bf16" or wb.paged or st.dense:
+        return None
+    chk = torch.zeros(1, dtype=torch.int32, device=wb.dev)
+    ts = []
+    for r in range(reps + 2):
+        flush_l2(flush)
+        torch.cuda._sleep(HOLD_CYCLES)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.sfa_gather_kv_bandwidth(c["K"], c["V"], c["q_seq"], c["q_pos"], st.blk_idx, st.n_sel,
+                                  st.top_k, w.compress_ratio, w.dkq, w.dv, chk,
+                                  dev_status=st.status)
+        e1.record()
+        torch.cuda.synchronize()
+        if r >= 2:
+            ts.append(e0.elapsed_time(e1))
+    return sum(ts) / len(ts)
+
+
 def measure_e2e(wb, steps, warmup):
     """Same step through the public API with host inputs: each step copies this step's query
     inputs and new cache rows from pinned host memory, runs, and reads O back.  The inputs
@@ -604,6 +628,15 @@ def main():
         floor = {"bytes": fb, "ms": fms, "GBps": fb / (fms * 1e6), "hbm_frac": fb / (fms * 1e6) / hbm_peak,
                  "attend_over_floor": kernels["attend"]["ms"] / fms,
                  "what": "plain contiguous read of the gathered-KV byte count (torch sum), L2 flushed"}
+    gms = gather_ceiling(wb, flush) if "attend" in kernels else None
+    gather = None
+    if gms:
+        gb = kernels["attend"]["bytes"]
+        gather = {"ms": gms, "GBps": gb / (gms * 1e6), "hbm_frac": gb / (gms * 1e6) / hbm_peak,
+                  "attend_over_gather": kernels["attend"]["ms"] / gms,
+                  "what": "sfa_gather_kv_bandwidth on the step's kept lists: the attended K/V "
+                          "rows moved into shared memory (one bulk copy per 4-row run, four "
+                          "issuing warps per SM), nothing computed; L2 flushed"}
     launches = wb.launches_per_step() * args.steps
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -624,6 +657,7 @@ def main():
                        "buffer read)"},
             "gathered_kv_GBps": kernels.get("attend", {}).get("GBps"),
             "gathered_kv_read_floor": floor,
+            "gather_ceiling": gather,
             "gathered_kv_hbm_frac": kernels.get("attend", {}).get("hbm_frac"),
             "roofline": roof, "kernels": kernels,
             "e2e": {"value": n_q_total / (e2e_ms / 1000.0), "unit": "tokens/s",
@@ -727,7 +761,13 @@ def main():
         att2 = [int(n) * w2.compress_ratio + (int(p) + 1) % w2.compress_ratio
                 for n, p in zip(n_sel2, wb2.case["q_pos"].cpu())]
         a2 = algorithmic(w2, att2, wb2.step.bounded)
+        g2 = gather_ceiling(wb2, flush, reps=5)
         line["pp2048"] = {
+            "gather_ceiling": None if not g2 else {
+                "ms": g2, "GBps": a2["gathered_kv_bytes"] / (g2 * 1e6),
+                "attend_over_gather": st2["attend"] / g2,
+                "what": "sfa_gather_kv_bandwidth on the step's kept lists (mostly L2 -> shared "
+                        "memory; L2 flushed before each rep)"},
             "workload": w2.name, "value": w2.n_q / (ms2 / 1000.0), "unit": "tokens/s",
             "ms_per_step": ms2, "stage_ms": st2,
             "attend_TFLOPs": a2["attend_flops"] / (st2["attend"] * 1e9),

@@ -291,6 +291,23 @@ int sfa_gather_attend_window(const void *Q, const void *K, const void *V, int dt
                              int32_t *dev_status, sfa_stream_t stream);
 
 /*
+ * sfa_gather_kv_bandwidth -- a measurement, not part of the method: moves exactly the K (and
+ * V) rows that sfa_gather_attend attends for these lists (the kept blocks' rows and the tail's)
+ * into shared memory and computes nothing.  Each run of 4 consecutive rows (a kept block of
+ * cr >= 4, a run of the tail) is one bulk copy, issued by four warps per CTA, one CTA per SM;
+ * the first word of every row is summed into *checksum (device uint32, atomically added) so
+ * that no copy can be dropped.  Its time is the data-movement ceiling of the attention on the
+ * same lists: with the caches in HBM, that of the gather pattern out of HBM; with them in L2,
+ * that of the L2 -> shared-memory gather.  Arguments as sfa_gather_attend (bf16 K/V; (dkq, dv)
+ * in {(576, 512) with V = NULL, (512, 512)}).
+ */
+int sfa_gather_kv_bandwidth(const void *K, const void *V, int n_seq, int64_t n_tok_cap,
+                            int n_q, int h_kv, int dkq, int dv, const int32_t *q_seq,
+                            const int32_t *q_pos, const int32_t *blk_idx, const int32_t *n_sel,
+                            int top_k, int compress_ratio, uint32_t *checksum,
+                            int32_t *dev_status, sfa_stream_t stream);
+
+/*
  * sfa_combine_attention -- merges two attentions of the same queries over disjoint key sets
  * into the attention over their union, by their log-sum-exp (the "combining the result" step
  * of the dense + sparse variant; exact: softmax over a disjoint union):

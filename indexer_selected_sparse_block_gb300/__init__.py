@@ -9,7 +9,7 @@ from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_CELL, SFA_DEV_BA
                        sfa_q8_0_row_bytes, sfa_quantize_kv_q8_0, SFA_ERR_CUDA, SFA_ERR_INVALID_ARG,
                        SFA_ERR_UNSUPPORTED, SFA_ERR_WORKSPACE, SFA_F32, SFA_OK, SFA_PART_ALL,
                        SFA_PART_SELECTED, SFA_PART_WINDOW, SfaError, sfa_combine_attention,
-                       sfa_gather_attend_window, sfa_window_kv_max,
+                       sfa_gather_attend_window, sfa_gather_kv_bandwidth, sfa_window_kv_max,
                        kbar_shape, lib, sfa_attend_plan, sfa_attend_workspace_bytes,
                        sfa_dense_attend, sfa_dense_attend_paged, sfa_gather_attend,
                        sfa_gather_attend_paged, sfa_index_scores, sfa_index_scores_bounded,

@@ -59,6 +59,8 @@ SIGNATURES = {
                                         _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _i64, _int,
                                         _vp, _vp, _vp, _sz, _vp, _vp]),
     "sfa_combine_attention": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _vp, _vp, _vp]),
+    "sfa_gather_kv_bandwidth": (_int, [_vp, _vp, _int, _i64, _int, _int, _int, _int, _vp, _vp, _vp,
+                                       _vp, _int, _int, _vp, _vp, _vp]),
     "sfa_gather_attend_noalloc": (_int, [_vp, _vp, _vp, _int, _int, _i64, _int, _int, _int,
                                          _int, _int, _f32, _vp, _vp, _vp, _vp, _int, _int, _vp,
                                          _vp, _vp, _vp]),
@@ -317,6 +319,18 @@ def sfa_combine_attention(O_a, lse_a, O_b, lse_b, O, lse, stream=None):
     rc = lib().sfa_combine_attention(_p(O_a), _p(lse_a), _p(O_b), _p(lse_b), n_rows, dv, _p(O),
                                      _p(lse), _stream(stream))
     _check("sfa_combine_attention", rc)
+
+
+def sfa_gather_kv_bandwidth(K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int, compress_ratio: int,
+                            dkq: int, dv: int, checksum, dev_status=None, stream=None):
+    """A measurement: the K/V rows sfa_gather_attend would attend, moved into shared memory
+    and nothing else (its time is the attention's data-movement ceiling on these lists)."""
+    n_seq, n_tok_cap, h_kv = K.shape[0], K.shape[1], K.shape[2]
+    rc = lib().sfa_gather_kv_bandwidth(_p(K), _p(V), n_seq, n_tok_cap, q_seq.numel(), h_kv, dkq,
+                                       dv, _p(q_seq), _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
+                                       compress_ratio, _p(checksum), _p(dev_status),
+                                       _stream(stream))
+    _check("sfa_gather_kv_bandwidth", rc)
 
 
 def sfa_gather_attend_noalloc(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,

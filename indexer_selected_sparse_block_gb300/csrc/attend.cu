@@ -1738,6 +1738,44 @@ extern "C" int sfa_gather_attend_window(const void *Q, const void *K, const void
                            nullptr, 0, window, part);
 }
 
+extern "C" int sfa_gather_kv_bandwidth(const void *K, const void *V, int n_seq, int64_t n_tok_cap,
+                                       int n_q, int h_kv, int dkq, int dv,
+                                       const int32_t *q_seq, const int32_t *q_pos,
+                                       const int32_t *blk_idx, const int32_t *n_sel, int top_k,
+                                       int compress_ratio, uint32_t *checksum,
+                                       int32_t *dev_status, sfa_stream_t stream) {
+    using namespace sfa;
+    if (!K || !q_seq || !q_pos || !blk_idx || !n_sel || !checksum) return SFA_ERR_INVALID_ARG;
+    if (n_seq < 1 || n_tok_cap < 1 || n_q < 0 || h_kv < 1 || compress_ratio < 1 || top_k < 1)
+        return SFA_ERR_INVALID_ARG;
+    if (top_k > 2048) return SFA_ERR_UNSUPPORTED;
+    if (!((dkq == 576 && dv == 512 && !V) || (dkq == 512 && dv == 512)))
+        return SFA_ERR_UNSUPPORTED;
+    if (!aligned16(K) || (V && !aligned16(V))) return SFA_ERR_INVALID_ARG;
+    if (n_q == 0) return SFA_OK;
+    if (n_q > 65535 || h_kv > 65535) return SFA_ERR_UNSUPPORTED;
+    const int64_t n_kv_max = (int64_t)top_k * compress_ratio + compress_ratio - 1;
+    WsPlan wp{};
+    if (!ws_make_plan(n_q, h_kv, dkq, dv, V != nullptr, n_kv_max, compress_ratio, 0, &wp))
+        return SFA_ERR_UNSUPPORTED;
+    AttnParams p{};
+    p.K = K; p.V = V;
+    p.q_seq = q_seq; p.q_pos = q_pos; p.blk_idx = blk_idx; p.n_sel = n_sel;
+    p.status = dev_status;
+    p.k_tok_stride = (int64_t)h_kv * dkq;
+    p.k_seq_stride = n_tok_cap * p.k_tok_stride;
+    p.v_tok_stride = V ? (int64_t)h_kv * dv : p.k_tok_stride;
+    p.v_seq_stride = V ? n_tok_cap * p.v_tok_stride : p.k_seq_stride;
+    p.n_tok_cap = n_tok_cap;
+    p.n_seq = n_seq; p.n_q = n_q; p.h_q = h_kv; p.h_kv = h_kv; p.G = 1;
+    p.top_k = top_k; p.cr = compress_ratio; p.dense = 0;
+    p.n_split = wp.n_split; p.split_tokens = wp.split_tokens;
+    p.n_items = n_q * h_kv * wp.n_split;
+    p.n_kv_max = n_kv_max;
+    if (wp.split_tokens / compress_ratio + 2 > kMaxBlkList) return SFA_ERR_UNSUPPORTED;
+    return ws_gather_launch(p, wp, dkq, dv, V != nullptr, checksum, (cudaStream_t)stream);
+}
+
 extern "C" int sfa_combine_attention(const float *O_a, const float *lse_a, const float *O_b,
                                      const float *lse_b, int64_t n_rows, int dv, float *O,
                                      float *lse, sfa_stream_t stream) {

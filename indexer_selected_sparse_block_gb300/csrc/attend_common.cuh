@@ -153,5 +153,9 @@ bool ws_make_plan(int n_q, int h_kv, int dkq, int dv, bool has_v, int64_t n_kv_m
                   int dense, WsPlan *out);
 int ws_launch(const AttnParams &p, const WsPlan &plan, int dkq, int dv, bool has_v,
               cudaStream_t st);
+// The gather alone (the K/V rows of every attended list into shared memory, no arithmetic):
+// the data-movement ceiling of the attention on the same lists (attend_ws.cu).
+int ws_gather_launch(const AttnParams &p, const WsPlan &plan, int dkq, int dv, bool has_v,
+                     uint32_t *checksum, cudaStream_t st);
 
 }  // namespace sfa

@@ -581,6 +581,130 @@ __global__ void __launch_bounds__(kThreads, 1)
                           reinterpret_cast<float *>(sRing) + 16 * DV, cur.i, cur.g, tid);
 }
 
+// ---------------------------------------------------------------------------------------
+// gather_rows_kernel -- the data movement of the attention and nothing else: the K (and V)
+// rows of every query's attended list copied into a ring of shared-memory tiles of the layout
+// above, each run of 4 consecutive rows (a kept block of cr >= 4, a run of the tail) as one bulk
+// copy, issued by four producer warps (two slots of each tile each); a fifth warp waits for
+// every tile, reads the first word of each attended row and releases the stage.  The sum of
+// those words goes to *checksum, so that the copies cannot be dropped.  Its time is the data-movement ceiling of
+// the attention on the same lists.
+constexpr int kGatherThreads = 160;
+
+template <int DKQ, int DV, bool V_IS_K>
+__global__ void __launch_bounds__(kGatherThreads, 1)
+    gather_rows_kernel(const AttnParams p, const int ns, const int bl_cap, uint32_t *checksum) {
+    using Lay = Layout<DKQ, DV, V_IS_K>;
+    constexpr int KR = Lay::KR, VR = Lay::VR, KSLOT = Lay::KSLOT, VSLOT = Lay::VSLOT;
+    constexpr int STAGE = Lay::STAGE;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *sRing = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)ns * STAGE);
+    uint64_t *full = bars, *empty = bars + ns;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * ns);
+    int *sTok = const_cast<int *>(abort_flag) + 8;                   // [ns][kTT], MMA order
+    int *sBlk = sTok + ns * kTT;                                     // [bl_cap]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < ns; ++s) {
+            mbar_init(&full[s], 4);    // one expect-tx arrival per producer warp
+            mbar_init(&empty[s], 1);   // the reading warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+    const bool k_dense = p.k_tok_stride == DKQ, v_dense = p.v_tok_stride == DV;
+    const __nv_bfloat16 *Kb = reinterpret_cast<const __nv_bfloat16 *>(p.K);
+    const __nv_bfloat16 *Vb = reinterpret_cast<const __nv_bfloat16 *>(p.V);
+    uint32_t sum = 0;
+    int gt = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        const Item it = decompose(p, item);
+        const ListInfo L = list_info(p, it.i, false);
+        const int j0 = it.split * p.split_tokens;
+        const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
+        const int n_tiles = j0 < j1 ? (j1 - j0 + kTT - 1) / kTT : 0;
+        int jb0 = 0;
+        if (warp < 4) {
+            if (n_tiles > 0) jb0 = load_block_list(p, it.i, L, j0, j1, sBlk, false, tid, 128);
+            named_barrier(1, 128);   // the producers' block list
+            const __nv_bfloat16 *Kseq =
+                L.ok ? Kb + (int64_t)L.seq * p.k_seq_stride + (int64_t)it.g * DKQ : Kb;
+            const __nv_bfloat16 *Vseq =
+                V_IS_K ? Kseq
+                       : (L.ok ? Vb + (int64_t)L.seq * p.v_seq_stride + (int64_t)it.g * DV : Vb);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int g2 = gt + t, st = g2 % ns;
+                wait_or_abort(&empty[st], ((uint32_t)(g2 / ns) & 1u) ^ 1u, deadline, abort_flag,
+                              p.status);
+                const int slot = warp * 2 + lane;   // lanes 0, 1: slots 2 warp, 2 warp + 1
+                int n_valid = 0;
+                if (lane < 2) {
+                    int tok[kSlotRows];
+                    int64_t row[kSlotRows];
+                    bool run = !*abort_flag;
+#pragma unroll
+                    for (int r = 0; r < kSlotRows; ++r) {
+                        tok[r] = token_at(p, L, j0 + t * kTT + slot * kSlotRows + r, j1, sBlk, jb0);
+                        row[r] = tok[r];
+                        n_valid += row[r] >= 0;
+                        run &= row[r] >= 0 && row[r] == row[0] + r;
+                        sTok[st * kTT + r * kSlots + slot] = tok[r];
+                    }
+                    uint8_t *kdst = sRing + (size_t)st * STAGE + slot * KSLOT;
+                    uint8_t *vdst = sRing + (size_t)st * STAGE + Lay::KTILE + slot * VSLOT;
+                    if (run && k_dense && (V_IS_K || v_dense)) {
+                        bulk_load(kdst, Kseq + row[0] * p.k_tok_stride, kSlotRows * KR, &full[st]);
+                        if constexpr (!V_IS_K)
+                            bulk_load(vdst, Vseq + row[0] * p.v_tok_stride, kSlotRows * VR,
+                                      &full[st]);
+                    } else {
+                        n_valid = 0;
+#pragma unroll
+                        for (int r = 0; r < kSlotRows; ++r)
+                            if (row[r] >= 0 && !*abort_flag) {
+                                ++n_valid;
+                                bulk_load(kdst + r * KR, Kseq + row[r] * p.k_tok_stride, KR,
+                                          &full[st]);
+                                if constexpr (!V_IS_K)
+                                    bulk_load(vdst + r * VR, Vseq + row[r] * p.v_tok_stride, VR,
+                                              &full[st]);
+                            }
+                    }
+                    if (*abort_flag) n_valid = 0;
+                }
+                n_valid += __shfl_xor_sync(0xFFFFFFFFu, n_valid, 1);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[st],
+                                          (uint32_t)n_valid * (uint32_t)(KR + (V_IS_K ? 0 : VR)));
+            }
+            named_barrier(1, 128);   // every producer is done with the block list
+        } else {   // the reading warp
+            for (int t = 0; t < n_tiles; ++t) {
+                const int g2 = gt + t, st = g2 % ns;
+                wait_or_abort(&full[st], (uint32_t)(g2 / ns) & 1u, deadline, abort_flag, p.status);
+                if (sTok[st * kTT + lane] >= 0)
+                    sum += *reinterpret_cast<const uint32_t *>(sRing + (size_t)st * STAGE +
+                                                               tok_off(lane, KSLOT, KR));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+        }
+        gt += n_tiles;
+    }
+    // no copy is in flight when the CTA leaves: the reading warp waited for every fill
+    if (warp == 4) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane == 0 && checksum) atomicAdd(checksum, sum);
+    }
+}
+
 // ------------------------------------------------------------------------------ host side
 // SFA_ATTEND_PV=bf16x2 in the environment (read at each call) makes P V run on bf16 operands
 // with P as two bf16 halves instead of binary16 operands.
@@ -704,7 +828,42 @@ int launch_shape(const AttnParams &p, const WsPlan &plan, cudaStream_t st) {
     return SFA_OK;
 }
 
+template <int DKQ, int DV, bool VK>
+int launch_gather(const AttnParams &p, const WsPlan &plan, uint32_t *checksum,
+                  cudaStream_t st) {
+    using Lay = Layout<DKQ, DV, VK>;
+    const int bl = p.dense ? 0 : plan.split_tokens / p.cr + 2;
+    int ns = 6;
+    auto bytes = [&](int n) {
+        return (size_t)n * Lay::STAGE + (size_t)(2 * n) * 8 + 32 + (size_t)n * kTT * 4 +
+               (size_t)bl * 4 + 16;
+    };
+    while (ns > 2 && bytes(ns) > 227 * 1024) --ns;
+    if (bytes(ns) > 227 * 1024) return SFA_ERR_UNSUPPORTED;
+    auto fn = gather_rows_kernel<DKQ, DV, VK>;
+    if (!ensure_max_dynamic_smem(fn)) return SFA_ERR_CUDA;
+    AttnParams q = p;
+    q.cluster_merge = 0;
+    const int grid = q.n_items < device_sm_count() ? q.n_items : device_sm_count();
+    if (launch_pdl(fn, dim3(grid), dim3(kGatherThreads), bytes(ns), st, q, ns, bl, checksum) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    return SFA_OK;
+}
+
 }  // namespace ws
+
+int ws_gather_launch(const AttnParams &p, const WsPlan &plan, int dkq, int dv, bool has_v,
+                     uint32_t *checksum, cudaStream_t st) {
+    using namespace ws;
+    if (dkq == 576 && dv == 512 && !has_v) return launch_gather<576, 512, true>(p, plan, checksum, st);
+    if (dkq == 512 && dv == 512)
+        return has_v ? launch_gather<512, 512, false>(p, plan, checksum, st)
+                     : launch_gather<512, 512, true>(p, plan, checksum, st);
+    return SFA_ERR_UNSUPPORTED;
+}
 
 bool ws_make_plan(int n_q, int h_kv, int dkq, int dv, bool has_v, int64_t n_kv_max, int cr,
                   int dense, WsPlan *out) {

@@ -62,3 +62,30 @@ def test_ws_full_size_all(dev, ws, name):
     w = sfa.WORKLOADS[name]
     case, step = _run(w, dev)
     _check_queries(w, case, step)
+
+
+@pytest.mark.parametrize("name", ["decode_1x4096", "decode_4x1048576"])
+def test_gather_kv_bandwidth_moves_the_attended_rows(dev, name):
+    """The gather-only measurement kernel copies exactly the attended rows: the sum of the
+    first 32-bit word of every attended K row (V rows are copied beside them) equals the same
+    sum taken on the host over the kept blocks and the tail."""
+    w = sfa.WORKLOADS[name].with_(n_seq=3) if name == "decode_1x4096" else sfa.WORKLOADS[name]
+    case, step = _run(w, dev)
+    chk = torch.zeros(1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_gather_kv_bandwidth(case["K"], case["V"], case["q_seq"], case["q_pos"], step.blk_idx,
+                                step.n_sel, step.top_k, w.compress_ratio, w.dkq, w.dv, chk,
+                                dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    words = case["K"].view(torch.int32)[..., 0]            # [n_seq][n_tok][h_kv]: first word
+    total = 0
+    sel, ns = step.blk_idx.cpu().numpy(), step.n_sel.cpu().numpy()
+    for i in range(w.n_q):
+        s, p = int(case["q_seq"][i]), int(case["q_pos"][i])
+        cr = w.compress_ratio
+        toks = [b * cr + r for b in sel[i, : ns[i]] for r in range(cr)]
+        toks += list(range(((p + 1) // cr) * cr, p + 1))
+        rows = words[s].index_select(0, torch.tensor(toks, device=dev))
+        total += int(rows.to(torch.int64).sum().item())
+    assert (int(chk.item()) & 0xFFFFFFFF) == (total & 0xFFFFFFFF)
