@@ -614,25 +614,26 @@ __device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int
 }
 
 // ---------------------------------------------------------------------------------------
-// The bounded selection (sfa_topk_blocks_refine), one 4-CTA cluster per row.  With lower and
-// upper bounds lo_b <= s_b <= up_b of the exact (hi + lo) score s_b, each CTA takes a quarter
-// of the row's blocks:
+// The bounded selection (sfa_topk_blocks_refine), one cluster per row (4 CTAs, or 8 for rows
+// past one selection piece).  With lower and upper bounds lo_b <= s_b <= up_b of the exact
+// (hi + lo) score s_b, each CTA takes an equal share (a "quarter" below) of the row's blocks:
 //   1. the maxima of groups of four lower bounds, their range (cluster-wide extrema) and a
 //      histogram of them in the leader CTA's shared memory; the floor of the bin of the k-th
 //      largest group maximum is L, a lower bound of the k-th largest lower bound (each group
 //      maximum bounds a distinct block from below);
 //   2. the candidates up_b >= L of the quarter, in ascending order; every block of the exact
 //      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k);
-//   3. their exact scores from the hi + lo pooled keys (fp32 on the CUDA cores), written as
+//   3. their exact scores from the hi + lo pooled keys (mma.sync, fp32 sums), written as
 //      keys with the block ids into the leader's candidate list at the quarter's offset;
 //   4. the leader selects the top k of the list.
 // Lists longer than 4096 go through global memory (select_global_list).
-constexpr int kCl = 4;                                       // CTAs per row
-// Rounds of 4 * kThreads elements a CTA takes of its quarter of the row: 3 for rows of up to
-// one selection piece (36864 blocks), 8 for rows of up to 131072 blocks.
+// A row's cluster: 4 CTAs for rows of up to one selection piece (36864 blocks), each taking
+// 3 rounds of 4 * kThreads elements; 8 CTAs of 4 rounds each for rows of up to 131072 blocks.
+constexpr int kCl = 4;
 constexpr int kClRoundsShort = (kChunk / kCl + 4 * kThreads - 1) / (4 * kThreads);   // 3
-constexpr int kClRoundsLong = 8;
-constexpr int64_t kRefineMaxLong = (int64_t)kCl * kClRoundsLong * 4 * kThreads;     // 131072
+constexpr int kClLong = 8;
+constexpr int kClRoundsLong = 4;
+constexpr int64_t kRefineMaxLong = (int64_t)kClLong * kClRoundsLong * 4 * kThreads;   // 131072
 static_assert(kClRoundsShort * 4 * kThreads >= kChunk / kCl, "a quarter of a piece fits the rounds");
 static_assert(4 * kClRoundsLong <= 32, "one candidate bit per element in a 32-bit mask");
 
@@ -656,15 +657,15 @@ struct RefineParams {
 // + h) * 32 + lane holds the pair of registers for heads 8 nt .. 8 nt + 7 and the k-step (pair
 // pq, half h) of the column order the A loads use (see rescore_tile).
 constexpr int kPq = 4;   // q dims / 32 (D <= 128)
-template <int R>
+template <int R, int CL>
 struct BoundedSmem {
     Smem sh;                        // the leader's candidate list serves the cluster
     float up[R * 4 * kThreads];     // this quarter's upper bounds (cp.async)
     uint2 qf[2 * kPq * 2 * 32];
     float w[16];
     int woff[R * kWarps];           // per (round, warp): this CTA's candidates before it
-    uint32_t ext_max[kCl], ext_min[kCl];   // leader slots, per rank
-    int cnt[kCl];
+    uint32_t ext_max[CL], ext_min[CL];   // leader slots, per rank
+    int cnt[CL];
     uint32_t lo;
 };
 
@@ -726,11 +727,12 @@ __device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv
     s1 = p1s;
 }
 
-template <int D, int R>
-__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
+template <int D, int R, int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     bounded_select_kernel(const RefineParams p, int n_q) {
     constexpr int kClRounds = R;
-    using BS = BoundedSmem<R>;
+    constexpr int kCl = CL;
+    using BS = BoundedSmem<R, CL>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     BS &bs = *reinterpret_cast<BS *>(smem_raw);
     Smem &sh = bs.sh;
@@ -1011,28 +1013,29 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     cluster.sync();   // no CTA leaves while another may still address its shared memory
 }
 
-template <int D, int R>
+template <int D, int R, int CL>
 int launch_bounded_d(const RefineParams &p, int n_q, cudaStream_t st) {
-    if (!ensure_max_dynamic_smem(bounded_select_kernel<D, R>)) return SFA_ERR_CUDA;
-    int clusters = device_sm_count() / kCl;
+    if (!ensure_max_dynamic_smem(bounded_select_kernel<D, R, CL>)) return SFA_ERR_CUDA;
+    int clusters = device_sm_count() / CL;
     if (clusters < 1) return SFA_ERR_CUDA;
     if (n_q < clusters) clusters = n_q;
-    if (launch_pdl(bounded_select_kernel<D, R>, dim3(clusters * kCl), dim3(kThreads),
-                   sizeof(BoundedSmem<R>), st, p, n_q) != cudaSuccess) {
+    if (launch_pdl(bounded_select_kernel<D, R, CL>, dim3(clusters * CL), dim3(kThreads),
+                   sizeof(BoundedSmem<R, CL>), st, p, n_q) != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
     }
     return SFA_OK;
 }
 
-// Rows of up to one selection piece take 3 rounds per CTA; longer rows (up to 131072 blocks)
-// take 8, with a quarter's upper bounds (128 KB) in shared memory.
+// Rows of up to one selection piece take 4-CTA clusters of 3 rounds per CTA; longer rows (up
+// to 131072 blocks) take 8-CTA clusters of 4 rounds, an eighth of the row's upper bounds (64 KB)
+// in each CTA's shared memory.
 int launch_bounded(const RefineParams &p, int n_q, cudaStream_t st) {
     if (p.n_blk_max <= kChunk)
-        return p.D == 64 ? launch_bounded_d<64, kClRoundsShort>(p, n_q, st)
-                         : launch_bounded_d<128, kClRoundsShort>(p, n_q, st);
-    return p.D == 64 ? launch_bounded_d<64, kClRoundsLong>(p, n_q, st)
-                     : launch_bounded_d<128, kClRoundsLong>(p, n_q, st);
+        return p.D == 64 ? launch_bounded_d<64, kClRoundsShort, kCl>(p, n_q, st)
+                         : launch_bounded_d<128, kClRoundsShort, kCl>(p, n_q, st);
+    return p.D == 64 ? launch_bounded_d<64, kClRoundsLong, kClLong>(p, n_q, st)
+                     : launch_bounded_d<128, kClRoundsLong, kClLong>(p, n_q, st);
 }
 
 // The levels for rows of up to n_blk_max scores: lengths per row at each level (n[0] =
@@ -1175,7 +1178,7 @@ extern "C" int sfa_topk_blocks_refine(const float *lower, const float *upper,
     if (top_k < 1 || top_k > 2048) return SFA_ERR_UNSUPPORTED;
     if (d_idx != 64 && d_idx != 128) return SFA_ERR_UNSUPPORTED;
     if (h_idx < 1 || h_idx > 16) return SFA_ERR_UNSUPPORTED;
-    if (n_blk_max > kRefineMaxLong) return SFA_ERR_UNSUPPORTED;   // 8 rounds per quarter
+    if (n_blk_max > kRefineMaxLong) return SFA_ERR_UNSUPPORTED;   // 8 CTAs x 4 rounds
     if (n_blk_max > 0 && (!lower || !upper || score_stride < n_blk_max))
         return SFA_ERR_INVALID_ARG;
     if (kbar_seq_stride < n_blk_max * 2 * d_idx) return SFA_ERR_INVALID_ARG;
