@@ -228,7 +228,6 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     const bool lead = split == 0 && g == 0;
     const int G = p.G;
     pdl_wait();   // global memory from here on
-    pdl_trigger();
     const ListInfo L = list_info(p, i, lead && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -740,7 +739,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     pdl_wait();   // global memory from here on
-    pdl_trigger();
     const ListInfo L = list_info(p, i, split == 0 && g == 0 && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -1158,7 +1156,6 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
     const int split = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
     const int row = tid >> 3, part = tid & 7;
     pdl_wait();   // global memory from here on
-    pdl_trigger();
     const ListInfo L = list_info(p, i, split == 0 && g == 0 && tid == 0);
     const int j0 = split * p.split_tokens;
     const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
@@ -1224,7 +1221,6 @@ __global__ void __launch_bounds__(kThreads) attend_f32_kernel(const AttnParams p
 __global__ void __launch_bounds__(128) combine_kernel(const AttnParams p, int dv) {
     extern __shared__ float s_w[];  // [n_split] weights, then 1/L and M
     pdl_wait();   // the partials of the attention kernel
-    pdl_trigger();
     const int i = blockIdx.x / p.h_q, h = blockIdx.x % p.h_q;
     const int g = h / p.G, row = h % p.G;
     const int64_t base0 = ((int64_t)i * p.h_kv + g) * p.n_split * p.G + row;
@@ -1280,7 +1276,6 @@ __global__ void __launch_bounds__(128) combine2_kernel(const float4 *Oa, const f
                                                       int64_t n_rows, int dv4, float4 *O,
                                                       float *lse) {
     pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (r >= n_rows) return;

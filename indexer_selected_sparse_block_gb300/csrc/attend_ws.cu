@@ -235,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     pdl_wait();   // global memory from here on
-    pdl_trigger();
     const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
 
     if (warp == kProdWarp) {
@@ -615,7 +614,6 @@ __global__ void __launch_bounds__(kGatherThreads, 1)
     }
     __syncthreads();
     pdl_wait();
-    pdl_trigger();
     const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
     const bool k_dense = p.k_tok_stride == DKQ, v_dense = p.v_tok_stride == DV;
     const __nv_bfloat16 *Kb = reinterpret_cast<const __nv_bfloat16 *>(p.K);

@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ X, int6
                                                    int64_t kr_seq_stride, const KeyTransform tf,
                                                    const CellMap cm) {
     pdl_wait();
-    pdl_trigger();
     const int chunks = d_idx >> 3;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n_rows * chunks;

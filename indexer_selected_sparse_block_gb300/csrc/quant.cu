@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(256) quant_q8_kernel(const T *__restrict__ X, 
                                                        int64_t y_outer_stride, int64_t n_blocks,
                                                        int32_t *status) {
     pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (blk >= n_blocks) return;   // whole warps: blk is the same for all 32 lanes

@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     pdl_wait();   // global memory from here on
-    pdl_trigger();
     const int seq0 = p.q_seq[q0];
     const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
     // For narrow tiles the producer fills the pipeline before the rest of the set-up: its tile

@@ -124,11 +124,20 @@ __device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {
 }
 
 // Programmatic dependent launch, device side: pdl_wait() blocks until the previous kernel in
-// the stream has completed (its writes visible); pdl_trigger() lets the next kernel start
-// launching once every CTA of this one has called it or exited.
+// the stream has completed (its writes visible).  No kernel here signals its dependents early
+// (griddepcontrol.launch_dependents): the next kernel's launch is then prepared while this one
+// runs and its CTAs start as this one's leave.  Measured on GB300, early signals let the next
+// kernel's CTAs occupy SMs and wait there while this one still ran, and every step was slower
+// for it (decode_32x131072: 112 -> 98 us per step without them).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+// A split cluster barrier: every thread of every CTA of the cluster arrives (relaxed: no
+// memory ordering) and later waits; the wait returns once all have arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

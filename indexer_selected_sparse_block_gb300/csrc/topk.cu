@@ -403,9 +403,8 @@ struct TopkParams {
     int cr, top_k, level, final_stage;
 };
 
-__device__ __forceinline__ int visible_blocks(const int32_t *q_pos, int i, int cr,
-                                              int64_t n_blk_max, int32_t *status) {
-    const int pos = q_pos[i];
+__device__ __forceinline__ int visible_blocks_at(int pos, int cr, int64_t n_blk_max,
+                                                 int32_t *status) {
     if (pos < 0) {
         set_status(status, SFA_DEV_BAD_QUERY);
         return 0;
@@ -416,6 +415,10 @@ __device__ __forceinline__ int visible_blocks(const int32_t *q_pos, int i, int c
         return (int)n_blk_max;
     }
     return (int)b;
+}
+__device__ __forceinline__ int visible_blocks(const int32_t *q_pos, int i, int cr,
+                                              int64_t n_blk_max, int32_t *status) {
+    return visible_blocks_at(q_pos[i], cr, n_blk_max, status);
 }
 
 // Elements of a row at the next level after a chunk stage: every chunk but the last passes
@@ -440,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
     const int n_items = n_q * n_chunks;
     clear_hist(sh, kBins);   // kept zero between items from here on
     pdl_wait();              // global memory from here on
-    pdl_trigger();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int i = item / n_chunks, c = item % n_chunks;
         int64_t len = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
@@ -616,15 +618,16 @@ __device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int
 // ---------------------------------------------------------------------------------------
 // The bounded selection (sfa_topk_blocks_refine), one cluster per row (4 CTAs, or 8 for rows
 // past one selection piece).  With lower and upper bounds lo_b <= s_b <= up_b of the exact
-// (hi + lo) score s_b, each CTA takes an equal share (a "quarter" below) of the row's blocks:
-//   1. the maxima of groups of four lower bounds, their range (cluster-wide extrema) and a
-//      histogram of them in the leader CTA's shared memory; the floor of the bin of the k-th
-//      largest group maximum is L, a lower bound of the k-th largest lower bound (each group
-//      maximum bounds a distinct block from below);
-//   2. the candidates up_b >= L of the quarter, in ascending order; every block of the exact
-//      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k);
+// (hi + lo) score s_b, each CTA takes an equal share of the row's blocks:
+//   1. the maxima of groups of four lower bounds (each bounds a distinct block from below) and
+//      their histogram in the CTA's own shared memory; X_r is the floor of the bin of the CTA's
+//      k_r-th largest group maximum, with quotas k_r proportional to the shares' groups and
+//      summing to at least k; L = min_r X_r is a lower bound of the k-th largest score;
+//   2. the candidates up_b >= L of the share, in ascending order; every block of the exact
+//      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k); their pooled
+//      rows are prefetched into L2 while the list is ordered;
 //   3. their exact scores from the hi + lo pooled keys (mma.sync, fp32 sums), written as
-//      keys with the block ids into the leader's candidate list at the quarter's offset;
+//      keys with the block ids into the leader's candidate list at the share's offset;
 //   4. the leader selects the top k of the list.
 // Lists longer than 4096 go through global memory (select_global_list).
 // A row's cluster: 4 CTAs for rows of up to one selection piece (36864 blocks), each taking
@@ -660,27 +663,29 @@ constexpr int kPq = 4;   // q dims / 32 (D <= 128)
 template <int R, int CL>
 struct BoundedSmem {
     Smem sh;                        // the leader's candidate list serves the cluster
-    float up[R * 4 * kThreads];     // this quarter's upper bounds (cp.async)
+    float up[R * 4 * kThreads];     // this share's upper bounds (cp.async)
     uint2 qf[2 * kPq * 2 * 32];
     float w[16];
     int woff[R * kWarps];           // per (round, warp): this CTA's candidates before it
-    uint32_t ext_max[CL], ext_min[CL];   // leader slots, per rank
+    uint32_t cut_x[CL];             // leader slots, per rank: the share's cut X_r
     int cnt[CL];
-    uint32_t lo;
 };
 
-// Exact scores of 16 candidates on the tensor cores: S[16 x heads] = [hi | lo] rows x [q ; q],
-// K = 2D, fp32 accumulation, then sum_j w_j ReLU(S_j) per row.  Lane (g, t) loads 16 bytes of
-// rows g and g + 8 at element 32 pp + 8 t of each 32-element piece pp of the 2D-wide row: the
-// first four elements are its A columns (2t, 2t+1, 2t+8, 2t+9) of k-step (pp, 0), the last
-// four those of (pp, 1).  The B table pairs the same columns with q (dims mod D), so each
-// k-step sums over 16 distinct columns and the pieces cover all 2D.  Returns the score of row
-// g (lanes with t == 0) and of row g + 8 through s0, s1.
-template <int D, typename BS>
+// Exact scores of ROWS (16, or 8 with rows 8..15 of the MMA zero) candidates on the tensor
+// cores: S[16 x heads] = [hi | lo] rows x [q ; q], K = 2D, fp32 accumulation, then
+// sum_j w_j ReLU(S_j) per row.  Lane (g, t) loads 16 bytes of rows g and g + 8 at element
+// 32 pp + 8 t of each 32-element piece pp of the 2D-wide row: the first four elements are its A
+// columns (2t, 2t+1, 2t+8, 2t+9) of k-step (pp, 0), the last four those of (pp, 1).  The B table
+// pairs the same columns with q (dims mod D), so each k-step sums over 16 distinct columns and
+// the pieces cover all 2D.  With 8 rows every piece of a row is loaded at once (one memory round
+// trip); with 16, four pieces at a time.  Returns the score of row g (lanes with t == 0) and of
+// row g + 8 through s0, s1.
+template <int D, int ROWS, typename BS>
 __device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv_bfloat16 *r1,
                                              const BS &bs, int H, float &s0, float &s1) {
+    static_assert(ROWS == 8 || ROWS == 16, "tile rows");
     constexpr int kPieces = 2 * D / 32;   // 8 or 4
-    constexpr int kG = kPieces < 4 ? kPieces : 4;   // pieces in flight
+    constexpr int kG = ROWS == 8 ? kPieces : (kPieces < 4 ? kPieces : 4);   // pieces in flight
     const int lane = threadIdx.x & 31, t = lane & 3;
     const int nt_n = (H + 7) / 8;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -690,7 +695,10 @@ __device__ __forceinline__ void rescore_tile(const __nv_bfloat16 *r0, const __nv
 #pragma unroll
         for (int u = 0; u < kG; ++u) {
             a0[u] = __ldg(reinterpret_cast<const uint4 *>(r0 + 32 * (p0 + u) + 8 * t));
-            a1[u] = __ldg(reinterpret_cast<const uint4 *>(r1 + 32 * (p0 + u) + 8 * t));
+            if constexpr (ROWS == 16)
+                a1[u] = __ldg(reinterpret_cast<const uint4 *>(r1 + 32 * (p0 + u) + 8 * t));
+            else
+                a1[u] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kG; ++u) {
@@ -743,13 +751,65 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     const int k = p.top_k, H = p.H;
     const int n_cl = gridDim.x / kCl;
     clear_hist(sh, kBins);   // kept zero between rows from here on
+    // Every CTA of the cluster is running before any remote access: arrive here, wait just
+    // before the first one, so that the first row's loads overlap the barrier.
+    cluster_arrive_relaxed();
+    bool started = false;
     pdl_wait();              // global memory from here on
-    pdl_trigger();
-    cluster.sync();          // every CTA of the cluster is running before any remote access
+    // This CTA's groups of four blocks, [g0, g1): a share of the widest row (n_blk_max), fixed
+    // before any row's metadata is read, so that the bound loads of a row do not wait for its
+    // position.  Elements at or past the row's own length B are masked after the loads.
+    const int nbm = (int)p.n_blk_max;
+    const int ngm = (nbm + 3) / 4;
+    const int per = (ngm + kCl - 1) / kCl;
+    const int g0 = rank * per < ngm ? rank * per : ngm;
+    const int g1 = g0 + per < ngm ? g0 + per : ngm;
     for (int i = blockIdx.x / kCl; i < n_q; i += n_cl) {
+        // the row's metadata, its query's B-fragment table entry and head weight, and the
+        // share's bounds: every load of the row is issued before any of them is used
         const int seq = p.q_seq[i];
-        int B = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
-                               (rank == 0 && tid == 0) ? p.status : nullptr);
+        const int pos = p.q_pos[i];
+        uint2 qb = make_uint2(0u, 0u);
+        if (tid < 2 * kPq * 2 * 32) {   // the B fragment table of this query
+            const int ln = tid & 31, h = (tid >> 5) & 1, pq = (tid >> 6) % kPq, nt = tid / (64 * kPq);
+            const int n = 8 * nt + (ln >> 2), d0 = 32 * pq + 8 * (ln & 3) + 4 * h;
+            if (n < H && d0 < D) {
+                const uint32_t *qr = reinterpret_cast<const uint32_t *>(p.q_idx + ((int64_t)i * H + n) * D + d0);
+                qb = make_uint2(qr[0], qr[1]);
+            }
+        }
+        const float wv = tid < H ? p.w[(int64_t)i * H + tid] : 0.f;
+        const float *lp = p.lower + (int64_t)i * p.stride;
+        const float *up = p.upper + (int64_t)i * p.stride;
+        // lower bounds into registers, upper bounds into shared memory (cp.async), all within
+        // the n_blk_max columns of the row
+        float4 lv[kClRounds];
+        {
+            const bool lvec = (reinterpret_cast<uintptr_t>(lp) & 15u) == 0;
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m) {
+                const int g = g0 + tid + kThreads * m;
+                if (g < g1) lv[m] = load_group(lp, g, nbm, lvec);
+            }
+            const bool vec = (reinterpret_cast<uintptr_t>(up) & 15u) == 0;
+#pragma unroll
+            for (int m = 0; m < kClRounds; ++m) {
+                const int lg = tid + kThreads * m, g = g0 + lg;
+                if (g < g1) {
+                    if (vec && 4 * g + 3 < nbm) {
+                        cp_async16(smem_u32(&bs.up[4 * lg]), up + 4 * g, 16);
+                    } else {
+                        const float4 v = load_group(up, g, nbm, false);
+                        bs.up[4 * lg] = v.x;
+                        bs.up[4 * lg + 1] = v.y;
+                        bs.up[4 * lg + 2] = v.z;
+                        bs.up[4 * lg + 3] = v.w;
+                    }
+                }
+            }
+            cp_async_commit();
+        }
+        int B = visible_blocks_at(pos, p.cr, p.n_blk_max, (rank == 0 && tid == 0) ? p.status : nullptr);
         if (seq < 0 || seq >= p.n_seq) {
             if (rank == 0 && tid == 0) set_status(p.status, SFA_DEV_BAD_QUERY);
             B = 0;
@@ -763,121 +823,75 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                     p.cand_n[i] = -1;
                 }
             }
+            cp_async_wait<0>();   // no copy of this row lands in a later row's buffer
             continue;
         }
-        // this CTA's groups of four: [g0, g1)
-        const int ng = (B + 3) / 4;
-        const int per = (ng + kCl - 1) / kCl;
-        const int g0 = rank * per < ng ? rank * per : ng;
-        const int g1 = g0 + per < ng ? g0 + per : ng;
-        const float *lp = p.lower + (int64_t)i * p.stride;
-        const float *up = p.upper + (int64_t)i * p.stride;
-        {   // this quarter's upper bounds into shared memory, in flight while L is found
-            const bool vec = (reinterpret_cast<uintptr_t>(up) & 15u) == 0;
-#pragma unroll
-            for (int m = 0; m < kClRounds; ++m) {
-                const int lg = tid + kThreads * m, g = g0 + lg;
-                if (g < g1) {
-                    if (vec && 4 * g + 3 < B) {
-                        cp_async16(smem_u32(&bs.up[4 * lg]), up + 4 * g, 16);
-                    } else {
-                        const float4 v = load_group(up, g, B, false);
-                        bs.up[4 * lg] = v.x;
-                        bs.up[4 * lg + 1] = v.y;
-                        bs.up[4 * lg + 2] = v.z;
-                        bs.up[4 * lg + 3] = v.w;
-                    }
-                }
-            }
-            cp_async_commit();
-        }
-        if (tid < 2 * kPq * 2 * 32) {   // the B fragment table of this query
-            const int ln = tid & 31, h = (tid >> 5) & 1, pq = (tid >> 6) % kPq, nt = tid / (64 * kPq);
-            const int n = 8 * nt + (ln >> 2), d0 = 32 * pq + 8 * (ln & 3) + 4 * h;
-            uint2 b = make_uint2(0u, 0u);
-            if (n < H && d0 < D) {
-                const uint32_t *qr = reinterpret_cast<const uint32_t *>(p.q_idx + ((int64_t)i * H + n) * D + d0);
-                b = make_uint2(qr[0], qr[1]);
-            }
-            bs.qf[tid] = b;
-        }
-        if (tid < H) bs.w[tid] = p.w[(int64_t)i * H + tid];
-        // ---- 1. group maxima of the lower bounds -> L
+        if (tid < 2 * kPq * 2 * 32) bs.qf[tid] = qb;
+        if (tid < H) bs.w[tid] = wv;
+        // ---- 1. group maxima of the row's lower bounds -> this CTA's cut X_r -> L
+        const int ng = (B + 3) / 4;                       // groups of the row
+        const int gv = ng < g1 ? ng : g1;                 // this share's groups in the row: [g0, gv)
+        const int n_loc = gv > g0 ? gv - g0 : 0;
         uint32_t gm[kClRounds];
         uint32_t mx = 0, mn = 0xFFFFFFFFu;
-        {
-            const bool vec = (reinterpret_cast<uintptr_t>(lp) & 15u) == 0;
 #pragma unroll
-            for (int m = 0; m < kClRounds; ++m) {
-                const int g = g0 + tid + kThreads * m;
-                gm[m] = 0;
-                if (g < g1) {
-                    const float4 v = load_group(lp, g, B, vec);
-                    gm[m] = order_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-                    mx = gm[m] > mx ? gm[m] : mx;
-                    mn = gm[m] < mn ? gm[m] : mn;
-                }
+        for (int m = 0; m < kClRounds; ++m) {
+            const int g = g0 + tid + kThreads * m;
+            gm[m] = 0;
+            if (g < gv) {
+                const float nan = __uint_as_float(0x7FFFFFFFu);
+                const int e = 4 * g;
+                const float a = lv[m].x, b = e + 1 < B ? lv[m].y : nan;
+                const float c = e + 2 < B ? lv[m].z : nan, d = e + 3 < B ? lv[m].w : nan;
+                gm[m] = order_key(fmaxf(fmaxf(a, b), fmaxf(c, d)));
+                mx = gm[m] > mx ? gm[m] : mx;
+                mn = gm[m] < mn ? gm[m] : mn;
             }
         }
-        {
+        // This CTA's quota k_r = ceil(k n_loc / ng) (the quotas sum to at least k) and X_r, the
+        // floor of the bin of its k_r-th largest group maximum: at least k_r of its group maxima
+        // are >= X_r.  L = min_r X_r then has at least k group maxima >= L in the row, each the
+        // lower bound of a distinct block, so the k-th largest score is >= L.  A share with no
+        // group of the row takes no part (X_r = the largest key); k > ng: L = the lowest key.
+        uint32_t X = 0xFFFFFFFFu;
+        if (k > ng) {
+            X = 0;
+        } else if (n_loc > 0) {
+            const int k_r = (int)(((int64_t)k * n_loc + ng - 1) / ng);
             uint32_t bmax, bmin, unused;
             block_extrema(mx, mn, 0xFFFFFFFFu, sh, bmax, bmin, unused);
-            if (tid == 0) {
-                lead.ext_max[rank] = bmax;
-                lead.ext_min[rank] = bmin;
-            }
-        }
-        cluster.sync();   // (a) the extrema of every quarter are in the leader
-        uint32_t gmax = 0, gmin = 0xFFFFFFFFu;
-#pragma unroll
-        for (int r = 0; r < kCl; ++r) {
-            const uint32_t a = lead.ext_max[r], b = lead.ext_min[r];
-            gmax = a > gmax ? a : gmax;
-            gmin = b < gmin ? b : gmin;
-        }
-        const bool have_k = k <= ng;   // k group maxima exist
-        const int sft = bin_shift(gmax - gmin);
-        if (have_k) {
+            const int sft = bin_shift(bmax - bmin);
 #pragma unroll
             for (int m = 0; m < kClRounds; ++m)
-                if (g0 + tid + kThreads * m < g1) atomicAdd(&sh.hist[(gm[m] - gmin) >> sft], 1);
+                if (g0 + tid + kThreads * m < gv) atomicAdd(&sh.hist[(gm[m] - bmin) >> sft], 1);
+            __syncthreads();
+            find_cut(sh, kBins, k_r);
+            X = bmin + ((uint32_t)sh.cut_bin << sft);
+            clear_hist(sh, kBins);
         }
-        cluster.sync();   // (b) every quarter's histogram is complete
-        if (rank == 0) {
-            uint32_t lo = 0;
-            if (have_k) {   // the leader adds the other quarters' histograms to its own
-                static_assert(kBins == 4 * kThreads, "one int4 of bins per thread");
-                int4 a = reinterpret_cast<const int4 *>(sh.hist)[tid];
+        if (!started) {   // the first remote access of this CTA
+            cluster_wait();
+            started = true;
+        }
+        if (tid == 0) lead.cut_x[rank] = X;
+        cluster.sync();   // (a) every share's X_r is in the leader
+        uint32_t lo = 0xFFFFFFFFu;
 #pragma unroll
-                for (int r = 1; r < kCl; ++r) {
-                    const int4 v = reinterpret_cast<const int4 *>(cluster.map_shared_rank(sh.hist, r))[tid];
-                    a.x += v.x;
-                    a.y += v.y;
-                    a.z += v.z;
-                    a.w += v.w;
-                }
-                reinterpret_cast<int4 *>(sh.hist)[tid] = a;
-                __syncthreads();
-                find_cut(sh, kBins, k);
-                lo = gmin + ((uint32_t)sh.cut_bin << sft);
-                clear_hist(sh, kBins);
-            }
-            if (tid == 0) bs.lo = lo;
+        for (int r = 0; r < kCl; ++r) {
+            const uint32_t x = lead.cut_x[r];
+            lo = x < lo ? x : lo;
         }
-        cluster.sync();   // (c) L is known; the leader has read every histogram
-        if (rank != 0 && have_k) clear_hist(sh, kBins);
-        const uint32_t lo = lead.lo;
         // ---- 2. candidates up_b >= L (as keys: >= lo); bit 4m + r for element 4g + r
         uint32_t cm = 0;
         cp_async_wait<0>();
-        __syncthreads();   // the quarter's upper bounds have landed
+        __syncthreads();   // the share's upper bounds have landed
         {
             const bool fcmp = lo >= kNegInfKey;   // lo is a float's key: compare floats
             const float L = __uint_as_float(key_bits(lo));
 #pragma unroll
             for (int m = 0; m < kClRounds; ++m) {
                 const int lg = tid + kThreads * m, g = g0 + lg;
-                if (g < g1) {
+                if (g < gv) {
                     const float4 v = *reinterpret_cast<const float4 *>(&bs.up[4 * lg]);
                     const float f[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -888,7 +902,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // ascending order within the quarter = (round, warp, lane, r)
+        // ascending order within the share = (round, warp, lane, r)
         int incl[kClRounds];
 #pragma unroll
         for (int m = 0; m < kClRounds; ++m) {
@@ -924,7 +938,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (lane == 31) lead.cnt[rank] = x;
         }
-        cluster.sync();   // (d) every quarter's count is in the leader
+        cluster.sync();   // (d) every share's count is in the leader
         int off = 0, total = 0;
 #pragma unroll
         for (int r = 0; r < kCl; ++r) {
@@ -936,7 +950,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
         const bool in_smem = total <= kMaxCand;   // the same in every CTA
         int32_t *gid = p.cand_id + (int64_t)i * p.n_blk_max;
         uint32_t *gbits = p.cand_bits + (int64_t)i * p.n_blk_max;
-        // this quarter's list: local shared memory, or the row's global list at its offset
+        // this share's list: local shared memory, or the row's global list at its offset
 #pragma unroll
         for (int m = 0; m < kClRounds; ++m) {
             int pos = bs.woff[m * kWarps + warp] + incl[m];
@@ -952,32 +966,25 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                 }
         }
         __syncthreads();
-        // ---- 3. exact scores of this quarter's candidates: a warp takes 16 at a time
+        // ---- 3. exact scores of this share's candidates: a warp takes 8 at a time, every
+        // piece of their rows in flight at once
         {
+            constexpr int kTR = 8;
             const int32_t *lid = in_smem ? sh.cand_idx : gid + off;
             const __nv_bfloat16 *kseq = p.kbar + (int64_t)seq * p.kbar_seq_stride;
             const int g = lane >> 2;
-            for (int c0 = warp * 16; c0 < mine; c0 += kWarps * 16) {
-                const int ra = c0 + g, rb = c0 + g + 8;
-                const int ba = lid[ra < mine ? ra : c0], bb = lid[rb < mine ? rb : c0];
-                float sa, sb;
-                rescore_tile<D>(kseq + (int64_t)ba * 2 * D, kseq + (int64_t)bb * 2 * D, bs, H, sa, sb);
-                if ((lane & 3) == 0) {
-                    if (ra < mine) {
-                        if (in_smem) {
-                            lead.sh.cand_key[off + ra] = order_key(sa);
-                            lead.sh.cand_idx[off + ra] = ba;
-                        } else {
-                            gbits[off + ra] = __float_as_uint(sa);
-                        }
-                    }
-                    if (rb < mine) {
-                        if (in_smem) {
-                            lead.sh.cand_key[off + rb] = order_key(sb);
-                            lead.sh.cand_idx[off + rb] = bb;
-                        } else {
-                            gbits[off + rb] = __float_as_uint(sb);
-                        }
+            for (int c0 = warp * kTR; c0 < mine; c0 += kWarps * kTR) {
+                const int ra = c0 + g;
+                const int ba = lid[ra < mine ? ra : c0];
+                float sa, unused;
+                const __nv_bfloat16 *ka = kseq + (int64_t)ba * 2 * D;
+                rescore_tile<D, kTR>(ka, ka, bs, H, sa, unused);
+                if ((lane & 3) == 0 && ra < mine) {
+                    if (in_smem) {
+                        lead.sh.cand_key[off + ra] = order_key(sa);
+                        lead.sh.cand_idx[off + ra] = ba;
+                    } else {
+                        gbits[off + ra] = __float_as_uint(sa);
                     }
                 }
             }
@@ -1010,7 +1017,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
             __syncthreads();
         }
     }
-    cluster.sync();   // no CTA leaves while another may still address its shared memory
+    if (!started) cluster_wait();   // the arrival above is matched before the CTA exits
+    // The CTAs of a cluster leave together.  (Letting the other CTAs leave while the leader
+    // still selects -- which no remote access needs -- made the whole step slower: the next
+    // kernel's CTAs took their SMs early.)
+    cluster.sync();
 }
 
 template <int D, int R, int CL>

@@ -145,6 +145,45 @@ def test_refine_all_tied(dev, n_tok):
         assert np.array_equal(got[i], np.arange(top_k))
 
 
+def test_refine_many_rows_per_cluster(dev):
+    """More rows than clusters (each cluster loops over several rows), rows below the budget
+    (no cluster barrier for them) mixed with rows of every length up to the widest, so that
+    some shares of the widest row hold no group of a shorter one."""
+    cr, d_idx, h_idx, top_k = 4, 128, 8, 256
+    n_tok = 16000
+    rng = np.random.default_rng(5)
+    pos = [int(x) for x in rng.integers(0, n_tok, size=100)]
+    pos[:6] = [3, 1023, 1024, 1027, n_tok - 1, 2 * top_k * cr]   # at and around the budget
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 17, 3, n_tok, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), n_tok // cr
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.full((n_q, top_k), -7, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
+                                 dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Xh, qh, wh = np32(X), np32(qi), np32(w)
+    got, gn = np32(blk), np32(n_sel)
+    n_exact = 0
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        if B <= top_k:
+            assert gn[i] == B and np.array_equal(got[i, :B], np.arange(B))
+            assert np.all(got[i, B:] == -1)
+            continue
+        sc = oracle.index_scores(qh[i], wh[i], oracle.pool(Xh[i % 3], B, cr))
+        ok, exact = check_selection(got[i], int(gn[i]), sc, top_k)
+        assert ok, (i, p)
+        assert np.all(np.diff(got[i, :gn[i]]) > 0)        # ascending
+        n_exact += exact
+    assert n_exact >= 0.9 * sum((p + 1) // cr > top_k for p in pos)
+
+
 def test_refine_below_budget_and_bad_query(dev):
     cr, d_idx, h_idx, top_k = 4, 64, 4, 50
     pos = [150, 2, 3999]
