@@ -347,15 +347,19 @@ def gather_ceiling(wb, flush, reps=10):
 
 def measure_e2e(wb, steps, warmup):
     """Same step through the public API with host inputs: each step copies this step's query
-    inputs and new cache rows from pinned host memory, runs, and reads O back.  The inputs
-    travel in one copy (one pinned host arena mirrored by one device arena); the new cache rows
-    are then placed into the caches by device copies."""
+    inputs and new cache rows from pinned host memory, runs, and has O in host memory at its
+    end.  The query inputs travel in one copy (one pinned host arena mirrored by one device
+    arena).  The new cache rows go from the same host arena straight into their cache slots
+    (sfa_copy_cache_rows, one two-dimensional copy per cache); q8_0 caches quantize them on the
+    device first, and a paged cache places them into their cells.  The attention writes O
+    into pinned host memory directly (SfaStep.set_output)."""
     c, w = wb.case, wb.w
     sl = slice(w.depth, w.n_tok)   # the step's new cache rows (positions depth .. n_tok - 1)
     new_rows = {n: t[:, sl] for n, t in wb.seq_rows.items()}   # bf16, from the host
     # paged: the new rows go to their cells (the page table is known before the step)
     new_cells = wb.cell_of[:, sl].reshape(-1).long() if wb.paged else None
-    # q8_0 caches: the new K / V rows are quantized on the device into a staging slice first
+    # new rows through the device: q8_0 caches quantize them there; a paged cache scatters them
+    via_dev = wb.kv == "q8_0" or wb.paged
     staging = {}
     if wb.kv == "q8_0":
         for n in ("K", "V"):
@@ -370,22 +374,28 @@ def measure_e2e(wb, steps, warmup):
     for n, t in parts.items():
         offs[n] = total
         total += (t.numel() * t.element_size() + 255) // 256 * 256
+    n_dev = total if via_dev else offs[f"{next(iter(new_rows))}_new"]   # bytes the arena copies
     dev_arena = torch.empty(total, dtype=torch.uint8, device=c["Q"].device)
     host_arena = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dv, saved = {}, {n: c[n] for n in names}
+    dv, hv, saved = {}, {}, {n: c[n] for n in names}
     for n, t in parts.items():
         nbytes = t.numel() * t.element_size()
-        host_arena[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape).copy_(t.cpu())
+        hv[n] = host_arena[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+        hv[n].copy_(t.cpu())
         dv[n] = dev_arena[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
     for n in names:
         c[n] = dv[n]
     out = torch.empty(wb.step.O.shape, dtype=torch.float32).pin_memory()
+    dev_O = wb.step.set_output(out)   # the attention writes O into host memory
     h2d = total
     d2h = out.numel() * out.element_size()
 
     def one():
-        dev_arena.copy_(host_arena, non_blocking=True)
+        dev_arena[:n_dev].copy_(host_arena[:n_dev], non_blocking=True)
         for n in new_rows:
+            if not via_dev:   # host rows straight into the cache slots
+                B.sfa_copy_cache_rows(c[n][:, sl], hv[f"{n}_new"])
+                continue
             src = dv[f"{n}_new"]
             if n in staging:
                 stg = staging[n]
@@ -397,7 +407,6 @@ def measure_e2e(wb, steps, warmup):
             else:
                 c[n].index_copy_(0, new_cells, src.reshape((-1,) + tuple(c[n].shape[1:])))
         wb.run_step()
-        out.copy_(wb.step.O, non_blocking=True)
 
     for _ in range(warmup):
         one()
@@ -409,7 +418,7 @@ def measure_e2e(wb, steps, warmup):
     e1.record()
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / steps
-    # the same step captured once as a CUDA graph (copies, launches, read-back), replayed
+    # the same step captured once as a CUDA graph (copies, launches), replayed
     graph = sfa.SfaStep.graphed(one)
     for _ in range(warmup):
         graph.replay()
@@ -419,8 +428,13 @@ def measure_e2e(wb, steps, warmup):
         graph.replay()
     e1.record()
     torch.cuda.synchronize()
+    # the host copy of O is the device result: the same bits
+    wb.step.set_output(dev_O)
+    wb.run_step()
+    torch.cuda.synchronize()
+    same = bool(torch.equal(out, dev_O.cpu()))
     c.update(saved)
-    return e0.elapsed_time(e1) / steps, eager_ms, h2d, d2h
+    return e0.elapsed_time(e1) / steps, eager_ms, h2d, d2h, same
 
 
 def oracle_sample(w, dev_case, n_queries, n_threads):
@@ -620,7 +634,7 @@ def main():
     roof["traffic"] = recorded_traffic(dom, w.name)
     roof["source"] = src
 
-    e2e_ms, e2e_eager_ms, h2d, d2h = measure_e2e(wb, max(3, args.steps // 2), 3)
+    e2e_ms, e2e_eager_ms, h2d, d2h, e2e_same = measure_e2e(wb, max(3, args.steps // 2), 3)
     floor = None
     if "attend" in kernels and w.kind == "decode":
         fb = kernels["attend"]["bytes"]
@@ -663,7 +677,9 @@ def main():
             "e2e": {"value": n_q_total / (e2e_ms / 1000.0), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "launch": "one CUDA graph per step (SfaStep.graphed)",
-                    "eager_value": n_q_total / (e2e_eager_ms / 1000.0)},
+                    "eager_value": n_q_total / (e2e_eager_ms / 1000.0),
+                    "output": "O written by the attention into pinned host memory",
+                    "host_O_equals_device_O": e2e_same},
             "gpu_launches": launches, "clocks": clk.summary(), "device_status": status}
     if wb.step.bounded:   # candidates per query the bounds could not rule out
         nb = max(wb.n_blk_max, 1)

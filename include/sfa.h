@@ -22,10 +22,14 @@
  *  - Returns an sfa status (SFA_OK = 0).  Never aborts, never synchronises the stream, never
  *    allocates device memory.  Invalid arguments are rejected on the host before anything is
  *    enqueued.  A CUDA launch error returns SFA_ERR_CUDA.
- *  - All data pointers are caller-owned DEVICE pointers; work is enqueued on `stream` (a
- *    cudaStream_t; NULL is the legacy default stream).  The library keeps no state between
- *    calls except a per-device cache of the SM count and of the CUDA driver's tensor-map
- *    encoder.
+ *  - All data pointers are caller-owned DEVICE pointers, with two exceptions: the attention
+ *    outputs O and lse may also point to page-locked host memory that the device addresses
+ *    directly (cudaHostAlloc, or cudaHostRegister'd, with unified addressing) -- the kernels
+ *    then write the results over the host link and the caller reads them once the stream has
+ *    passed the call -- and sfa_copy_cache_rows takes either kind.  Work is enqueued on
+ *    `stream` (a cudaStream_t; NULL is the legacy default stream).  The library keeps no
+ *    state between calls except a per-device cache of the SM count and of the CUDA driver's
+ *    tensor-map encoder.
  *  - Strides are in elements of the buffer's own type.  Buffers must be 16-byte aligned.
  *  - `dev_status` (nullable) is a device int32 the kernels OR bits into (SFA_DEV_*) when they
  *    meet data they cannot use (a block id outside [0, B_i), a non-ascending list, n_sel out
@@ -445,6 +449,17 @@ int sfa_gather_attend_noalloc(const void *Q, const void *K, const void *V, int d
                               const int32_t *blk_idx, const int32_t *n_sel, int top_k,
                               int compress_ratio, float *O, float *lse, int32_t *dev_status,
                               sfa_stream_t stream);
+
+/*
+ * sfa_copy_cache_rows -- plumbing, not part of the method: places n_rows rows of row_bytes
+ * bytes, spaced src_pitch bytes apart at src, into rows spaced dst_pitch bytes apart at dst --
+ * typically a step's new cache rows (one per sequence) written into their slots of the K, V
+ * or index-key caches.  Either side may be device memory or page-locked host memory; the copy
+ * is one two-dimensional copy on `stream`.  row_bytes >= 1, pitches >= row_bytes, n_rows >= 0;
+ * SFA_ERR_INVALID_ARG otherwise, SFA_ERR_CUDA if the runtime refuses the copy.
+ */
+int sfa_copy_cache_rows(void *dst, int64_t dst_pitch, const void *src, int64_t src_pitch,
+                        int64_t row_bytes, int64_t n_rows, sfa_stream_t stream);
 
 /* Copies *dev_status to *host_out after the work already enqueued on `stream` (this call
  * synchronises the stream). */

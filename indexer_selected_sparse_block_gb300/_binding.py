@@ -72,6 +72,7 @@ SIGNATURES = {
                                       _vp, _vp]),
     "sfa_q8_0_row_bytes": (_sz, [_int]),
     "sfa_quantize_kv_q8_0": (_int, [_vp, _int, _i64, _i64, _int, _i64, _vp, _i64, _vp, _vp]),
+    "sfa_copy_cache_rows": (_int, [_vp, _i64, _vp, _i64, _i64, _i64, _vp]),
     "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
     "sfa_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -111,6 +112,18 @@ def _p(t, strided=False):
     if not strided and not t.is_contiguous():
         raise ValueError("libsfa takes contiguous tensors only")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _p_out(t):
+    """Pointer of an attention output: a CUDA tensor, or a page-locked host tensor that the
+    device writes directly."""
+    if t is not None and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError("an attention output on the host must be in page-locked memory")
+        if not t.is_contiguous():
+            raise ValueError("libsfa takes contiguous tensors only")
+        return ctypes.c_void_p(t.data_ptr())
+    return _p(t)
 
 
 def _stream(stream):
@@ -276,8 +289,8 @@ def sfa_gather_attend(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int, compres
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().sfa_gather_attend(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap, n_q, h_q,
                                  h_kv, dkq, dv, float(scale), _p(q_seq), _p(q_pos), _p(blk_idx),
-                                 _p(n_sel), top_k, compress_ratio, _p(O), _p(lse), _p(workspace),
-                                 ws_bytes, _p(dev_status), _stream(stream))
+                                 _p(n_sel), top_k, compress_ratio, _p_out(O), _p_out(lse),
+                                 _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_gather_attend", rc)
 
 
@@ -300,8 +313,9 @@ def sfa_gather_attend_window(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,
     rc = lib().sfa_gather_attend_window(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap,
                                         n_q, h_q, h_kv, dkq, dv, float(scale), _p(q_seq),
                                         _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
-                                        compress_ratio, int(window), int(part), _p(O), _p(lse),
-                                        _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
+                                        compress_ratio, int(window), int(part), _p_out(O),
+                                        _p_out(lse), _p(workspace), ws_bytes, _p(dev_status),
+                                        _stream(stream))
     _check("sfa_gather_attend_window", rc)
 
 
@@ -316,8 +330,8 @@ def sfa_combine_attention(O_a, lse_a, O_b, lse_b, O, lse, stream=None):
     for t in (lse_a, lse_b, lse):
         if t.numel() != n_rows or not t.is_contiguous() or t.dtype != torch.float32:
             raise ValueError("lse_a, lse_b, lse must be contiguous fp32 tensors of O's rows")
-    rc = lib().sfa_combine_attention(_p(O_a), _p(lse_a), _p(O_b), _p(lse_b), n_rows, dv, _p(O),
-                                     _p(lse), _stream(stream))
+    rc = lib().sfa_combine_attention(_p(O_a), _p(lse_a), _p(O_b), _p(lse_b), n_rows, dv, _p_out(O),
+                                     _p_out(lse), _stream(stream))
     _check("sfa_combine_attention", rc)
 
 
@@ -343,7 +357,7 @@ def sfa_gather_attend_noalloc(Q, K, V, q_seq, q_pos, blk_idx, n_sel, top_k: int,
     rc = lib().sfa_gather_attend_noalloc(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap,
                                          n_q, h_q, h_kv, dkq, dv, float(scale), _p(q_seq),
                                          _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
-                                         compress_ratio, _p(O), _p(lse), _p(dev_status),
+                                         compress_ratio, _p_out(O), _p_out(lse), _p(dev_status),
                                          _stream(stream))
     _check("sfa_gather_attend_noalloc", rc)
 
@@ -358,7 +372,7 @@ def sfa_dense_attend(Q, K, V, q_seq, q_pos, n_kv_max: int, scale: float, O, lse=
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().sfa_dense_attend(_p(Q), _p(K), _p(V), _dtype_code(K), n_seq, n_tok_cap, n_q, h_q,
                                 h_kv, dkq, dv, float(scale), _p(q_seq), _p(q_pos), n_kv_max,
-                                _p(O), _p(lse), _p(workspace), ws_bytes, _p(dev_status),
+                                _p_out(O), _p_out(lse), _p(workspace), ws_bytes, _p(dev_status),
                                 _stream(stream))
     _check("sfa_dense_attend", rc)
 
@@ -408,8 +422,8 @@ def sfa_gather_attend_paged(Q, K, V, cell_of, q_seq, q_pos, blk_idx, n_sel, top_
     rc = lib().sfa_gather_attend_paged(_p(Q), _p(K), _p(V), _dtype_code(K), n_cells, _p(cell_of),
                                        n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, float(scale),
                                        _p(q_seq), _p(q_pos), _p(blk_idx), _p(n_sel), top_k,
-                                       compress_ratio, _p(O), _p(lse), _p(workspace), ws_bytes,
-                                       _p(dev_status), _stream(stream))
+                                       compress_ratio, _p_out(O), _p_out(lse), _p(workspace),
+                                       ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_gather_attend_paged", rc)
 
 
@@ -423,7 +437,7 @@ def sfa_dense_attend_paged(Q, K, V, cell_of, q_seq, q_pos, n_kv_max: int, scale:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().sfa_dense_attend_paged(_p(Q), _p(K), _p(V), _dtype_code(K), n_cells, _p(cell_of),
                                       n_seq, n_pos_cap, n_q, h_q, h_kv, dkq, dv, float(scale),
-                                      _p(q_seq), _p(q_pos), n_kv_max, _p(O), _p(lse),
+                                      _p(q_seq), _p(q_pos), n_kv_max, _p_out(O), _p_out(lse),
                                       _p(workspace), ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_dense_attend_paged", rc)
 
@@ -447,6 +461,30 @@ def sfa_quantize_kv_q8_0(X, Y, dev_status=None, stream=None):
                                     X.stride(0), _p(Y, strided=True), Y.stride(0), _p(dev_status),
                                     _stream(stream))
     _check("sfa_quantize_kv_q8_0", rc)
+
+
+def sfa_copy_cache_rows(dst, src, stream=None) -> None:
+    """Copies the rows of src into the rows of dst (the same shape; dim 0 indexes the rows,
+    each row contiguous, rows at any stride): one two-dimensional copy, either side on the
+    device or in page-locked host memory.  Typically dst = cache[:, p] for a step's new
+    position p of every sequence."""
+    if tuple(dst.shape) != tuple(src.shape) or dst.dtype != src.dtype or dst.dim() < 1:
+        raise ValueError("dst and src must have the same shape and dtype")
+    for t in (dst, src):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("sfa_copy_cache_rows takes CUDA or page-locked host tensors")
+        if t.shape[0] > 0 and not t[0].is_contiguous():
+            raise ValueError("each row must be contiguous")
+    es = dst.element_size()
+    row = dst[0].numel() * es if dst.shape[0] > 0 else 0
+    n = dst.shape[0]
+    dp = dst.stride(0) * es if n > 1 else row
+    sp = src.stride(0) * es if n > 1 else row
+    if n == 0 or row == 0:
+        return
+    rc = lib().sfa_copy_cache_rows(ctypes.c_void_p(dst.data_ptr()), dp,
+                                   ctypes.c_void_p(src.data_ptr()), sp, row, n, _stream(stream))
+    _check("sfa_copy_cache_rows", rc)
 
 
 def sfa_read_device_status(dev_status, stream=None) -> int:

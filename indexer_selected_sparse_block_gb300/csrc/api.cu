@@ -91,6 +91,22 @@ extern "C" const char *sfa_status_string(int status) {
     }
 }
 
+extern "C" int sfa_copy_cache_rows(void *dst, int64_t dst_pitch, const void *src,
+                                   int64_t src_pitch, int64_t row_bytes, int64_t n_rows,
+                                   sfa_stream_t stream) {
+    if (n_rows < 0 || row_bytes < 1 || dst_pitch < row_bytes || src_pitch < row_bytes)
+        return SFA_ERR_INVALID_ARG;
+    if (n_rows == 0) return SFA_OK;
+    if (!dst || !src) return SFA_ERR_INVALID_ARG;
+    // one two-dimensional copy; the direction follows from the addresses (unified addressing)
+    if (cudaMemcpy2DAsync(dst, (size_t)dst_pitch, src, (size_t)src_pitch, (size_t)row_bytes,
+                          (size_t)n_rows, cudaMemcpyDefault, (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    return SFA_OK;
+}
+
 extern "C" int sfa_read_device_status(const int32_t *dev_status, int32_t *host_out,
                                       sfa_stream_t stream) {
     if (!dev_status || !host_out) return SFA_ERR_INVALID_ARG;

@@ -94,9 +94,21 @@ class SfaStep:
         self.O = torch.empty((n_q, h_q, dv), dtype=torch.float32, device=dev)
         self.lse = torch.empty((n_q, h_q), dtype=torch.float32, device=dev)
         if self.window and window_mode == "split" and not self.dense:
-            self.O_win = torch.empty_like(self.O)
-            self.lse_win = torch.empty_like(self.lse)
+            self.O_sel, self.O_win = torch.empty_like(self.O), torch.empty_like(self.O)
+            self.lse_sel, self.lse_win = torch.empty_like(self.lse), torch.empty_like(self.lse)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def set_output(self, O):
+        """Makes O the buffer the attention writes: a [n_q][h_q][dv] fp32 tensor on the device,
+        or in page-locked host memory, which the attention kernels then write directly (no
+        separate read-back).  The split window mode keeps its partial parts on the device and
+        only the merged result goes to O.  Returns the buffer it replaces."""
+        if tuple(O.shape) != tuple(self.O.shape) or O.dtype != torch.float32:
+            raise ValueError(f"O must be a float32 tensor of shape {tuple(self.O.shape)}")
+        if not O.is_contiguous() or not (O.is_cuda or O.is_pinned()):
+            raise ValueError("O must be contiguous, on the device or in page-locked host memory")
+        old, self.O = self.O, O
+        return old
 
     def pool(self, X, blk_begin: int, blk_end: int, stream=None):
         if blk_end > blk_begin:
@@ -158,13 +170,13 @@ class SfaStep:
                                        lse=self.lse, part=B.SFA_PART_ALL, workspace=self.attn_ws,
                                        dev_status=self.status, stream=stream)
         elif self.window:
-            for part, O, lse in ((B.SFA_PART_SELECTED, self.O, self.lse),
+            for part, O, lse in ((B.SFA_PART_SELECTED, self.O_sel, self.lse_sel),
                                  (B.SFA_PART_WINDOW, self.O_win, self.lse_win)):
                 B.sfa_gather_attend_window(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel,
                                            self.top_k, self.cr, self.window, scale, O, lse=lse,
                                            part=part, workspace=self.attn_ws,
                                            dev_status=self.status, stream=stream)
-            B.sfa_combine_attention(self.O, self.lse, self.O_win, self.lse_win, self.O,
+            B.sfa_combine_attention(self.O_sel, self.lse_sel, self.O_win, self.lse_win, self.O,
                                     self.lse, stream=stream)
         else:
             B.sfa_gather_attend(Q, K, V, q_seq, q_pos, self.blk_idx, self.n_sel, self.top_k,

@@ -218,6 +218,26 @@ def test_q8_0_entry_points(L):
              FAKE, FAKE, 256, 4, FAKE, None, None, 0, None, None) == 1     # dtype 3
 
 
+def test_copy_cache_rows_rejects_bad_arguments(L):
+    f = L.sfa_copy_cache_rows
+    #       dst   dpitch src   spitch row  n  stream
+    base = [FAKE, 2048, FAKE, 1152, 1152, 32, None]
+    a = list(base); a[4] = 0
+    assert f(*a) == 1                                                             # no row bytes
+    a = list(base); a[1] = 1024
+    assert f(*a) == 1                                                             # dst rows overlap
+    a = list(base); a[3] = 1000
+    assert f(*a) == 1                                                             # src rows overlap
+    a = list(base); a[5] = -1
+    assert f(*a) == 1                                                             # n_rows
+    a = list(base); a[0] = None
+    assert f(*a) == 1                                                             # no dst
+    a = list(base); a[2] = None
+    assert f(*a) == 1                                                             # no src
+    a = list(base); a[0] = None; a[5] = 0
+    assert f(*a) == 0                                                             # empty: no work
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No CPU fallback: with libsfa.so absent, the first entry-point call raises."""
     import indexer_selected_sparse_block_gb300 as sfa
