@@ -153,25 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qq = e / H;
         s_w[e] = qq < nq_tile ? p.w[(int64_t)(q0 + qq) * H + (e % H)] : 0.f;
     }
-    if (HI) {   // C_q = sum_j |w_j| |q_j|_2, one warp per query
-        for (int qq = warp; qq < p.q_tile; qq += kThreads / 32) {
-            float c = 0.f;
-            if (qq < nq_tile) {
-                for (int j = 0; j < H; ++j) {
-                    const __nv_bfloat16 *qv = p.q_idx + ((int64_t)(q0 + qq) * H + j) * D;
-                    float ss = 0.f;
-                    for (int e = lane; e < D; e += 32) {
-                        const float v = __bfloat162float(qv[e]);
-                        ss = fmaf(v, v, ss);
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-                    c = fmaf(fabsf(p.w[(int64_t)(q0 + qq) * H + j]), sqrtf(ss), c);
-                }
-            }
-            if (lane == 0) s_cq[qq] = c;
-        }
-    }
     // B operand: row n = (query qq, head j), K' = [q | q] (or q); 16-byte chunks, 128-byte
     // swizzle.
     for (int e = threadIdx.x; e < N * (KB / 8); e += kThreads) {
@@ -271,12 +252,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int ncols = nq_tile * H;
+        if (HI) {
+            // C_q = sum_j |w_j| |q_j|_2, from the query rows of the B operand in shared memory
+            // (the sum of squares of a row covers all its 16-byte chunks, so the swizzle does
+            // not matter): no global round trip before the epilogue's first tile.  (Computed
+            // from global memory in the set-up, it held every warp for 3.5 us per launch.)
+            constexpr int kCpr = KB / 8;        // 16-byte chunks per B row
+            constexpr int kHpp = 32 / kCpr;     // heads per warp pass
+            for (int qq = quarter; qq < nq_tile; qq += 4) {
+                float c = 0.f;
+#pragma unroll
+                for (int j0 = 0; j0 < H; j0 += kHpp) {
+                    const int j = j0 + lane / kCpr, cc = lane % kCpr;
+                    float ss = 0.f;
+                    if (j < H) {
+                        const int n = qq * H + j;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            sB + (size_t)(cc >> 3) * N * 128 + n * 128 +
+                            (((cc & 7) ^ (n & 7)) << 4));
+                        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float e0 = __uint_as_float(u[k] << 16);
+                            const float e1 = __uint_as_float(u[k] & 0xFFFF0000u);
+                            ss = fmaf(e0, e0, fmaf(e1, e1, ss));
+                        }
+                    }
+#pragma unroll
+                    for (int o = 1; o < kCpr; o <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+                    if (cc == 0 && j < H) c = fmaf(fabsf(s_w[qq * H + j]), sqrtf(ss), c);
+                }
+#pragma unroll
+                for (int o = kCpr; o < 32; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+                if (lane == 0) s_cq[qq] = c;
+            }
+            named_barrier(1, 128);   // the four epilogue warps
+        }
+        // bounded mode: this thread's block's bound factor, loaded one tile ahead so that its
+        // latency overlaps the tile before
+        const float *kr = HI ? p.kbar_r + (int64_t)seq0 * p.kr_seq_stride + quarter * 32 + lane
+                             : nullptr;
+        auto load_rb = [&](int it) {
+            const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
+            return (HI && it < my_tiles && b < p.n_blk_max)
+                       ? __ldg(kr + (int64_t)(t_begin + it) * kBM)
+                       : 0.f;
+        };
+        float rb_next = load_rb(0);
         for (int it = 0; it < my_tiles; ++it) {
             const int acc = it & 1;
             if (*abort_flag) break;
             const int64_t b = (int64_t)(t_begin + it) * kBM + quarter * 32 + lane;
-            // bounded mode: this block's bound factor, loaded before the accumulator wait
-            const float rb = (HI && b < p.n_blk_max) ? __ldg(p.kbar_r + (int64_t)seq0 * p.kr_seq_stride + b) : 0.f;
+            const float rb = rb_next;
+            rb_next = load_rb(it + 1);
             if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, deadline)) {
                 set_status(p.status, SFA_DEV_TIMEOUT);
                 *abort_flag = 1;
