@@ -75,13 +75,15 @@ def recorded_traffic(kernel, workload):
 
 
 # ------------------------------------------------------------------ algorithmic work per step
-def algorithmic(w, attended, bounded=False, kv="bf16"):
+def algorithmic(w, attended, bounded=None, kv="bf16"):
     """Bytes / FLOPs each stage must move / do for one step of workload w (one rank).
 
     attended[i] = |A_i|, the number of cells query i attends (kept blocks * cr + tail).
     Pooled keys are 4*d_idx bytes per block (bf16 hi + lo halves); a query tile of one
     sequence reads that sequence's pooled keys once, so decode reads them once per query and
-    a prefill ubatch once per sequence.
+    a prefill ubatch once per sequence.  bounded: the bound pass of the bounded selection --
+    "i8" reads d_idx bytes of codes and 8 of scale and bound factor per block, "hi" (or True)
+    2*d_idx bytes of hi halves and a 4-byte bound factor; None / False: the exact scores.
     """
     cr = w.compress_ratio
     nb = [(w.depth + j + 1) // cr for j in range(w.n_q_per_seq)] * w.n_seq
@@ -89,8 +91,12 @@ def algorithmic(w, attended, bounded=False, kv="bf16"):
         kv_row = w.h_kv * (B.sfa_q8_0_row_bytes(w.dkq) + (0 if w.v_is_k else B.sfa_q8_0_row_bytes(w.dv)))
     else:
         kv_row = w.h_kv * (w.dkq + (0 if w.v_is_k else w.dv)) * 2
-    # bounded selection: the hi halves and the 4-byte bound factor of each block only
-    per_blk = (2 * w.d_idx + 4) if bounded else 4 * w.d_idx
+    if bounded == "i8":   # codes + (scale, bound factor)
+        per_blk = w.d_idx + 8
+    elif bounded:         # hi halves + bound factor
+        per_blk = 2 * w.d_idx + 4
+    else:
+        per_blk = 4 * w.d_idx
     if w.kind == "decode":
         kbar_bytes = sum(b * per_blk for b in nb)
     else:
@@ -219,6 +225,8 @@ class Workbench:
     def launches_per_step(self):
         w, st = self.w, self.step
         n = 1 if self.new_blocks[1] > self.new_blocks[0] else 0
+        if n and st.bound_pass == "i8":
+            n += 1  # the 8-bit copy of the new pooled rows
         if not st.dense:
             n += 1  # scores
             if st.bounded:
@@ -592,7 +600,7 @@ def main():
     tail = [(int(p) + 1) % w.compress_ratio for p in wb.case["q_pos"].cpu()]
     attended = [int(n) * w.compress_ratio + t for n, t in zip(n_sel, tail)] if not wb.step.dense \
         else [int(p) + 1 for p in wb.case["q_pos"].cpu()]
-    alg = algorithmic(w, attended, wb.step.bounded, kv=args.kv)
+    alg = algorithmic(w, attended, wb.step.bound_pass, kv=args.kv)
     kernels = {}
     for name, ms in stage_ms.items():
         if ms <= 0 or (name == "pool" and wb.new_blocks[1] <= wb.new_blocks[0]):
@@ -663,7 +671,8 @@ def main():
                        "h_kv": w.h_kv, "dkq": w.dkq, "dv": w.dv, "v_is_k": w.v_is_k,
                        "h_idx": w.h_idx, "d_idx": w.d_idx, "compress_ratio": w.compress_ratio,
                        "indexer_top_k": w.indexer_top_k,
-                       "selection": "bounded" if wb.step.bounded else "exact",
+                       "selection": (f"bounded ({wb.step.bound_pass} bound pass)"
+                                     if wb.step.bounded else "exact"),
                        "cache_layout": PAGED_LAYOUT if wb.paged else "contiguous per sequence",
                        "kv_cache": Q8_CACHE if args.kv == "q8_0" else "bf16",
                        "l2": "flushed before every timed "
@@ -711,7 +720,7 @@ def main():
         sq, _ = measure(wbq, max(3, args.steps // 2), 3, flush, per_stage=False)
         _, stq = measure(wbq, 3, 3, flush, per_stage=True)
         msq = sum(sq) / len(sq)
-        aq = algorithmic(w, attended, wbq.step.bounded, kv="q8_0")
+        aq = algorithmic(w, attended, wbq.step.bound_pass, kv="q8_0")
         same = bool(torch.equal(wbq.step.n_sel, wb_sel[0]) and torch.equal(wbq.step.blk_idx, wb_sel[2]))
         ref = wb_sel[1]
         dev_rel = ((wbq.step.O - ref).abs().amax(-1) / ref.abs().amax(-1).clamp_min(1e-30)).max()
@@ -776,7 +785,7 @@ def main():
         n_sel2 = wb2.step.n_sel.cpu()
         att2 = [int(n) * w2.compress_ratio + (int(p) + 1) % w2.compress_ratio
                 for n, p in zip(n_sel2, wb2.case["q_pos"].cpu())]
-        a2 = algorithmic(w2, att2, wb2.step.bounded)
+        a2 = algorithmic(w2, att2, wb2.step.bound_pass)
         g2 = gather_ceiling(wb2, flush, reps=5)
         line["pp2048"] = {
             "gather_ceiling": None if not g2 else {

@@ -192,14 +192,18 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
  *           sum_j |w_ij| |qidx_ij|_2 |hi_b|_2).
  * Both arrays share score_stride; entries at b >= B_i are left untouched.
  *
- * sfa_topk_blocks_refine: per query, L = a lower bound of the k-th largest lower bound (the
- * k-th largest maximum of the lower bounds of groups of four consecutive blocks, rounded down
- * to its histogram bin); every block with upper >= L is a candidate (every block of the top k
- * by s is one, and so is every block whose s ties the k-th); the candidates are rescored from
- * hi + lo (bf16 products, fp32 sums) and the top indexer_top_k of them by (score desc, block
- * asc) are written as sfa_topk_blocks writes them.  One kernel launch; each query's row is
- * split over a cluster of four CTAs.
- *   lower, upper: as written by sfa_index_scores_bounded for the same queries and Kbar
+ * sfa_topk_blocks_refine: per query, L = a lower bound of the k-th largest lower bound: the
+ * row is split over the CTAs of a cluster; each CTA takes the maxima of the lower bounds of
+ * its groups of four consecutive blocks and a quota k_r of them (proportional to its share of
+ * the row's groups, the quotas summing to at least k), finds a floor X_r under its k_r
+ * largest (a histogram bin), and L = min_r X_r; every block
+ * with upper >= L is a candidate (every block of the top k by s is one, and so is every block
+ * whose s ties the k-th); the candidates are rescored from hi + lo (bf16 products, fp32 sums)
+ * and the top indexer_top_k of them by (score desc, block asc) are written as sfa_topk_blocks
+ * writes them.  One kernel launch; each query's row is split over a cluster of four CTAs
+ * (eight past 36864 blocks).
+ *   lower, upper: as written by sfa_index_scores_bounded (or sfa_index_scores_bounded_i8) for
+ *           the same queries and Kbar
  *   q_idx, w, q_seq, q_pos, Kbar, kbar_seq_stride, n_seq: as given to it; Kbar 16-byte
  *           aligned with kbar_seq_stride a multiple of 8, q_idx 4-byte aligned
  *   blk_idx, n_sel: as sfa_topk_blocks
@@ -224,6 +228,44 @@ int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score
                            int compress_ratio, int top_k, int64_t n_blk_max, int32_t *blk_idx,
                            int32_t *n_sel, void *workspace, size_t workspace_bytes,
                            int32_t *dev_status, sfa_stream_t stream);
+
+/*
+ * sfa_quantize_pooled_keys_i8 / sfa_index_scores_bounded_i8 -- the same lower and upper bounds
+ * from 8-bit copies of the pooled keys: the bound pass then reads d_idx bytes per block instead
+ * of the 2*d_idx bytes of the hi halves (the bounds are looser: about twice as many
+ * candidates reach the rescoring).
+ *
+ * sfa_quantize_pooled_keys_i8 writes, for rows [blk_begin, blk_end) of every sequence, from the
+ * pooled keys m = hi + lo of Kbar (as written by any sfa_pool_index_keys* call):
+ *   K8    [n_seq][k8_seq_stride / d_idx][d_idx] int8: c_bi = round(m_bi / sc_b), clamped to
+ *         [-127, 127], with sc_b = max_i |m_bi| / 127 (0 for a zero row: c = 0)
+ *   K8_sr [n_seq][sr_seq_stride] fp32, pairs per block: (sc_b, r_b),
+ *         r_b = (|m_b - sc_b c_b|_2 + 2^-14 sc_b |c_b|_2) (1 + 2^-16)   (fp32 norms)
+ * Call it for the rows each pool call wrote.  Limits: d_idx in {64, 128}; Kbar and K8 16-byte
+ * aligned, K8_sr 8-byte aligned; kbar_seq_stride >= blk_end*2*d_idx (a multiple of 8),
+ * k8_seq_stride >= blk_end*d_idx (a multiple of 16), sr_seq_stride >= 2*blk_end (even).
+ *
+ * sfa_index_scores_bounded_i8 writes lower and upper bounds of the hi + lo score s_ib:
+ *   lower = a - e <= s_ib <= a + e = upper,  a_ib = sc_b * sum_j w_ij * max(0, qidx_ij . c_b),
+ *   e_ib = (1 + 2^-10) * (sum_j |w_ij| |qidx_ij|_2) * r_b.  The exact difference is at most
+ *   (sum_j |w_ij| |qidx_ij|_2) |m_b - sc_b c_b|_2 (ReLU is 1-Lipschitz, sc_b >= 0,
+ *   Cauchy-Schwarz per head); r_b's second term covers the fp32 rounding of both scores.
+ *   K8, K8_sr: as written by sfa_quantize_pooled_keys_i8; the sequences' rows must be
+ *          contiguous (blk_cap = k8_seq_stride / d_idx rows per sequence, no gaps)
+ *   other arguments as sfa_index_scores_bounded (each query on its own: no query groups).
+ * Entries at b >= B_i are left untouched.  Limits: d_idx in {64, 128}, h_idx in {4, 8, 16};
+ * q_idx 16-byte aligned.  Errors as the other entry points.
+ */
+int sfa_quantize_pooled_keys_i8(const void *Kbar, int64_t kbar_seq_stride, int n_seq, int d_idx,
+                                int64_t blk_begin, int64_t blk_end, void *K8,
+                                int64_t k8_seq_stride, float *K8_sr, int64_t sr_seq_stride,
+                                sfa_stream_t stream);
+int sfa_index_scores_bounded_i8(const void *q_idx, const float *w, const int32_t *q_seq,
+                                const int32_t *q_pos, int n_q, int h_idx, int d_idx,
+                                int compress_ratio, const void *K8, int64_t k8_seq_stride,
+                                const float *K8_sr, int64_t sr_seq_stride, int n_seq,
+                                int64_t n_blk_max, float *lower, float *upper,
+                                int64_t score_stride, int32_t *dev_status, sfa_stream_t stream);
 
 /*
  * sfa_gather_attend -- softmax attention of each query over the cells of its kept blocks plus

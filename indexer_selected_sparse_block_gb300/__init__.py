@@ -13,7 +13,8 @@ from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_CELL, SFA_DEV_BA
                        sfa_copy_cache_rows, sfa_dense_attend, sfa_dense_attend_paged,
                        sfa_gather_attend, sfa_gather_attend_noalloc, sfa_gather_attend_paged,
                        sfa_gather_attend_window, sfa_gather_kv_bandwidth, sfa_index_scores,
-                       sfa_index_scores_bounded, sfa_pool_index_keys, sfa_pool_index_keys_paged,
+                       sfa_index_scores_bounded, sfa_index_scores_bounded_i8, k8_shapes,
+                       sfa_quantize_pooled_keys_i8, sfa_pool_index_keys, sfa_pool_index_keys_paged,
                        sfa_pool_index_keys_transformed, sfa_q8_0_row_bytes,
                        sfa_quantize_kv_q8_0, sfa_read_device_status, sfa_topk_blocks,
                        sfa_topk_blocks_refine, sfa_topk_refine_workspace_bytes,

@@ -40,6 +40,10 @@ SIGNATURES = {
                                 _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_index_scores_bounded": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _vp,
                                         _i64, _vp, _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "sfa_quantize_pooled_keys_i8": (_int, [_vp, _i64, _int, _int, _i64, _i64, _vp, _i64, _vp,
+                                           _i64, _vp]),
+    "sfa_index_scores_bounded_i8": (_int, [_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp, _i64,
+                                           _vp, _i64, _int, _i64, _vp, _vp, _i64, _vp, _vp]),
     "sfa_topk_workspace_bytes": (_sz, [_int, _i64, _int]),
     "sfa_attend_plan": (_int, [_int, _int, _int, _int, _int, _i64, _int, _int, _vp, _vp]),
     "sfa_topk_refine_workspace_bytes": (_sz, [_int, _i64]),
@@ -203,6 +207,39 @@ def sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, Kbar, Kbar_r, compress_rati
                                         _p(lower), _p(upper), lower.stride(0), _p(dev_status),
                                         _stream(stream))
     _check("sfa_index_scores_bounded", rc)
+
+
+def k8_shapes(n_seq: int, blk_cap: int, d_idx: int):
+    """Shapes of the 8-bit pooled-key copy: codes [n_seq][blk_cap][d_idx] int8 and
+    (scale, bound factor) pairs [n_seq][blk_cap][2] fp32."""
+    return (n_seq, blk_cap, d_idx), (n_seq, blk_cap, 2)
+
+
+def sfa_quantize_pooled_keys_i8(Kbar, blk_begin: int, blk_end: int, K8, K8_sr, stream=None):
+    """Rows [blk_begin, blk_end) of the 8-bit copy (K8 codes, K8_sr scale and bound factor) of
+    the pooled keys m = hi + lo in Kbar."""
+    n_seq, _, two_d = Kbar.shape
+    if K8.dtype != torch.int8 or K8_sr.dtype != torch.float32:
+        raise ValueError("K8 must be int8 and K8_sr float32")
+    rc = lib().sfa_quantize_pooled_keys_i8(_p(Kbar), Kbar.stride(0), n_seq, two_d // 2,
+                                           blk_begin, blk_end, _p(K8), K8.stride(0), _p(K8_sr),
+                                           K8_sr.stride(0), _stream(stream))
+    _check("sfa_quantize_pooled_keys_i8", rc)
+
+
+def sfa_index_scores_bounded_i8(q_idx, w, q_seq, q_pos, K8, K8_sr, compress_ratio: int,
+                                n_blk_max: int, lower, upper, dev_status=None, stream=None):
+    """lower[i][b] <= s_ib <= upper[i][b] for the hi + lo score s_ib, from the 8-bit copy of the
+    pooled keys (sfa_quantize_pooled_keys_i8)."""
+    n_q, h_idx, d_idx = q_idx.shape
+    if lower.stride(0) != upper.stride(0):
+        raise ValueError("lower and upper must share a row stride")
+    rc = lib().sfa_index_scores_bounded_i8(_p(q_idx), _p(w), _p(q_seq), _p(q_pos), n_q, h_idx,
+                                           d_idx, compress_ratio, _p(K8), K8.stride(0),
+                                           _p(K8_sr), K8_sr.stride(0), K8.shape[0], n_blk_max,
+                                           _p(lower), _p(upper), lower.stride(0),
+                                           _p(dev_status), _stream(stream))
+    _check("sfa_index_scores_bounded_i8", rc)
 
 
 def sfa_topk_refine_workspace_bytes(n_q: int, n_blk_max: int) -> int:

@@ -5,9 +5,12 @@ kept block lists, workspaces, outputs) and runs the stages as the C entry points
 
   sfa_pool_index_keys -> sfa_index_scores -> sfa_topk_blocks -> sfa_gather_attend
 
-(decode-like steps -- few queries per sequence, rows of at most 131072 blocks -- take
-sfa_index_scores_bounded -> sfa_topk_blocks_refine for the middle two: the same kept sets from
-half the pooled-key bytes plus the rescoring of the few blocks the bounds cannot rule out)
+(decode-like steps -- few queries per sequence, rows of at most 131072 blocks -- take a bound
+pass -> sfa_topk_blocks_refine for the middle two: the same kept sets from a quarter of the
+pooled-key bytes (sfa_index_scores_bounded_i8 on the 8-bit copy that
+sfa_quantize_pooled_keys_i8 writes after each pool call; bound_pass="hi":
+sfa_index_scores_bounded on the hi halves, half the bytes) plus the rescoring of the few blocks
+the bounds cannot rule out)
 
 or, when every query is below the budget (B_i <= indexer_top_k for all i), the dense case
 ``sfa_dense_attend``: every block then fits the budget, so the method is exactly dense
@@ -35,7 +38,8 @@ class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
                  n_blk_max: int, q_group: int = 1, bounded=None, key_transform=None,
-                 cell_of=None, window: int = 0, window_mode: str = "single", device="cuda"):
+                 cell_of=None, window: int = 0, window_mode: str = "single",
+                 bound_pass: str = "i8", device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -66,9 +70,19 @@ class SfaStep:
         if self.bounded and n_blk_max > B.SFA_REFINE_MAX_BLOCKS:
             raise ValueError(f"bounded selection takes rows of at most "
                              f"{B.SFA_REFINE_MAX_BLOCKS} blocks, got n_blk_max={n_blk_max}")
-        # bounded: the pooling pass also writes each pooled row's bound factor
-        self.Kbar_r = (torch.zeros((n_seq, max(self.blk_cap, 1)), dtype=torch.float32, device=dev)
-                       if self.bounded else None)
+        # bounded: the bound pass reads the 8-bit copy of the pooled keys ("i8": codes, a
+        # scale and a bound factor per row, written after each pool call) or the hi halves
+        # ("hi": the pooling pass also writes each pooled row's bound factor)
+        if bound_pass not in ("i8", "hi"):
+            raise ValueError("bound_pass must be 'i8' or 'hi'")
+        self.bound_pass = bound_pass if self.bounded else None
+        cap = max(self.blk_cap, 1)
+        self.Kbar_r = (torch.zeros((n_seq, cap), dtype=torch.float32, device=dev)
+                       if self.bound_pass == "hi" else None)
+        if self.bound_pass == "i8":
+            k8, sr = B.k8_shapes(n_seq, cap, d_idx)
+            self.K8 = torch.zeros(k8, dtype=torch.int8, device=dev)
+            self.K8_sr = torch.zeros(sr, dtype=torch.float32, device=dev)
         self.scores = torch.empty((n_q, max(n_blk_max, 1)), dtype=torch.float32, device=dev)
         # bounded: scores holds the lower bounds and upper the upper bounds
         self.upper = (torch.empty_like(self.scores) if self.bounded else None)
@@ -122,9 +136,16 @@ class SfaStep:
             else:
                 B.sfa_pool_index_keys(X, self.cr, blk_begin, blk_end, self.Kbar, self.Kbar_r,
                                       stream=stream)
+            if self.bound_pass == "i8":
+                B.sfa_quantize_pooled_keys_i8(self.Kbar, blk_begin, blk_end, self.K8, self.K8_sr,
+                                              stream=stream)
 
     def score(self, q_idx, w, q_seq, q_pos, stream=None):
-        if self.bounded:
+        if self.bound_pass == "i8":
+            B.sfa_index_scores_bounded_i8(q_idx, w, q_seq, q_pos, self.K8, self.K8_sr, self.cr,
+                                          self.n_blk_max, self.scores, self.upper,
+                                          dev_status=self.status, stream=stream)
+        elif self.bounded:
             B.sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, self.Kbar, self.Kbar_r, self.cr,
                                        self.n_blk_max, self.scores, self.upper,
                                        q_group=self.q_group, dev_status=self.status,

@@ -39,3 +39,6 @@ def test_pooled_key_bytes():
     assert a["score_bytes"] == w.n_q * nb * 8                     # lower + upper bounds
     e = b.algorithmic(w, [1] * w.n_q, bounded=False)
     assert e["kbar_bytes"] == w.n_q * nb * 4 * w.d_idx             # hi + lo halves
+    c = b.algorithmic(w, [1] * w.n_q, bounded="i8")
+    assert c["kbar_bytes"] == w.n_q * nb * (w.d_idx + 8)           # codes + scale, bound factor
+    assert c["score_bytes"] == a["score_bytes"]

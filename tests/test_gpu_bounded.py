@@ -290,3 +290,119 @@ def test_refine_longest_rows(dev):
         if exact and (top >= 32768).any():
             assert (got[i] >= 32768).any()
     assert n_exact >= len(pos) - 1
+
+
+# ------------------------------------------------------------------ the 8-bit bound pass
+def _k8(dev, Kbar, blk_cap, d_idx, b0, b1):
+    n_seq = Kbar.shape[0]
+    k8s, srs = sfa.k8_shapes(n_seq, blk_cap, d_idx)
+    K8 = torch.zeros(k8s, dtype=torch.int8, device=dev)
+    sr = torch.full(srs, -1.0, dtype=torch.float32, device=dev)
+    sfa.sfa_quantize_pooled_keys_i8(Kbar, b0, b1, K8, sr)
+    return K8, sr
+
+
+@pytest.mark.parametrize("d_idx", [128, 64])
+def test_quantize_pooled_keys_i8(dev, d_idx):
+    """Codes, scale and bound factor per row, checked against their definition in float64:
+    sc = max|m| / 127 (m = hi + lo), |m - sc c| <= sc / 2 elementwise, and the stored factor
+    covers |m - sc c|_2 + 2^-14 sc |c|_2 by at most a few ulps; rows outside the range are not
+    written, and a zero row gives zero codes, scale and factor."""
+    cr, n_seq, n_tok = 4, 2, 4000
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 31 + d_idx, n_seq, n_tok, d_idx, 4, cr, [3999, 17])
+    Kbar = Kb[0]
+    blk_cap = n_tok // cr
+    Kbar[1, 500].zero_()                                   # a zero row
+    b0, b1 = 3, blk_cap - 2
+    K8, sr = _k8(dev, Kbar, blk_cap, d_idx, b0, b1)
+    torch.cuda.synchronize()
+    kb = np32(Kbar).astype(np.float64)
+    m = kb[..., :d_idx] + kb[..., d_idx:]
+    c = K8.cpu().numpy().astype(np.float64)
+    s = np32(sr).astype(np.float64)
+    sc, r = s[..., 0], s[..., 1]
+    rows = slice(b0, b1)
+    mx = np.abs(m[:, rows]).max(-1)
+    assert np.allclose(sc[:, rows], mx / 127, rtol=2 ** -22, atol=0)
+    assert np.all(np.abs(c[:, rows]) <= 127)
+    res = m[:, rows] - sc[:, rows, None] * c[:, rows]
+    assert np.all(np.abs(res) <= 0.5 * sc[:, rows, None] * (1 + 2 ** -14) + 1e-38)
+    need = np.linalg.norm(res, axis=-1) + 2 ** -14 * sc[:, rows] * np.linalg.norm(c[:, rows], axis=-1)
+    assert np.all(r[:, rows] >= need)
+    assert np.all(r[:, rows] <= need * (1 + 2 ** -12) + 1e-38)
+    assert sc[1, 500] == 0 and r[1, 500] == 0 and np.all(c[1, 500] == 0)
+    assert np.all(c[:, :b0] == 0) and np.all(c[:, b1:] == 0)          # not written
+    assert np.all(s[:, :b0] == -1.0) and np.all(s[:, b1:] == -1.0)
+
+
+@pytest.mark.parametrize("d_idx,h_idx", [(128, 8), (64, 4), (128, 16), (64, 16)])
+def test_bounds_hold_i8(dev, d_idx, h_idx):
+    """The 8-bit bounds bracket the hi + lo scores the exact pass computes, for every visible
+    block of queries of several lengths (partial last tiles included)."""
+    cr, n_seq, n_tok = 4, 3, 6000
+    pos = [5999, 4003, 1299, 511, 5000]
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 7 * d_idx + h_idx, n_seq, n_tok, d_idx, h_idx, cr,
+                                         pos)
+    n_blk_max = 1500
+    K8, sr = _k8(dev, Kb[0], n_tok // cr, d_idx, 0, n_blk_max)
+    exact = torch.full((len(pos), n_blk_max), float("nan"), device=dev)
+    lower = torch.full_like(exact, float("nan"))
+    upper = torch.full_like(exact, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kb[0], cr, n_blk_max, exact, dev_status=status)
+    sfa.sfa_index_scores_bounded_i8(qi, w, q_seq, q_pos, K8, sr, cr, n_blk_max, lower, upper,
+                                    dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    e, lo, up = np32(exact), np32(lower), np32(upper)
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        assert np.all(lo[i, :B] <= e[i, :B]) and np.all(e[i, :B] <= up[i, :B]), i
+        assert np.all(np.isnan(lo[i, B:])) and np.all(np.isnan(up[i, B:]))
+        # useful, if looser than the hi-only bounds (a fifth of the typical score)
+        half = 0.5 * (up[i, :B] - lo[i, :B])
+        assert np.median(half) < 0.3 * np.median(np.abs(e[i, :B]) + 1e-30)
+
+
+@pytest.mark.parametrize("top_k", [64, 512, 2048])
+def test_refine_follows_agreement_rule_i8(dev, top_k):
+    cr, d_idx, h_idx = 4, 128, 8
+    pos = [11999, 9000, 2047, 700, 3, 8191]
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, top_k + 3, 2, 12000, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), 3000
+    K8, sr = _k8(dev, Kb[0], 3000, d_idx, 0, n_blk_max)
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.full((n_q, top_k), -7, dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded_i8(qi, w, q_seq, q_pos, K8, sr, cr, n_blk_max, lower, upper,
+                                    dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Xh, qh, wh = np32(X), np32(qi), np32(w)
+    got, gn = np32(blk), np32(n_sel)
+    n_exact = 0
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        sc = oracle.index_scores(qh[i], wh[i], oracle.pool(Xh[i % 2], B, cr))
+        ok, exact = check_selection(got[i], int(gn[i]), sc, top_k)
+        assert ok, (i, p)
+        assert np.all(np.diff(got[i, :gn[i]]) > 0)
+        assert np.all(got[i, gn[i]:] == -1)
+        n_exact += exact
+    assert n_exact >= len(pos) - 1
+
+
+@pytest.mark.parametrize("name,bound_pass", [("decode_32x131072", "hi"),
+                                             ("decode_4x1048576", "hi"),
+                                             ("decode_cr1_32x32768", "i8")])
+def test_bound_passes_full_size_all(dev, name, bound_pass):
+    """Every query of the full-size decode workloads through either bound pass (the i8 pass is
+    the default and the other full-size tests run it)."""
+    w = sfa.WORKLOADS[name]
+    case, step = _run(w, dev, bound_pass=bound_pass)
+    assert step.bound_pass == bound_pass
+    _check_queries(w, case, step)
