@@ -246,10 +246,13 @@ int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score
  * k8_seq_stride >= blk_end*d_idx (a multiple of 16), sr_seq_stride >= 2*blk_end (even).
  *
  * sfa_index_scores_bounded_i8 writes lower and upper bounds of the hi + lo score s_ib:
- *   lower = a - e <= s_ib <= a + e = upper,  a_ib = sc_b * sum_j w_ij * max(0, qidx_ij . c_b),
- *   e_ib = (1 + 2^-10) * (sum_j |w_ij| |qidx_ij|_2) * r_b.  The exact difference is at most
- *   (sum_j |w_ij| |qidx_ij|_2) |m_b - sc_b c_b|_2 (ReLU is 1-Lipschitz, sc_b >= 0,
- *   Cauchy-Schwarz per head); r_b's second term covers the fp32 rounding of both scores.
+ *   lower = a - e <= s_ib <= a + e = upper,  a_ib = sc_b * sum_j w_ij * max(0, q~_ij . c_b),
+ *   q~ = binary16(qidx) (clamped to +-65504),
+ *   e_ib = (1 + 2^-10) * (C_i r_b + D_i 127 sqrt(d_idx) sc_b),  C_i = sum_j |w_ij| |qidx_ij|_2,
+ *   D_i = sum_j |w_ij| |qidx_ij - q~_ij|_2.  The exact difference is at most
+ *   C_i |m_b - sc_b c_b|_2 + D_i sc_b |c_b|_2 (ReLU is 1-Lipschitz, sc_b >= 0, Cauchy-Schwarz
+ *   per head, |c_b|_2 <= 127 sqrt(d_idx)); r_b's second term covers the fp32 rounding of both
+ *   scores.
  *   K8, K8_sr: as written by sfa_quantize_pooled_keys_i8; the sequences' rows must be
  *          contiguous (blk_cap = k8_seq_stride / d_idx rows per sequence, no gaps)
  *   other arguments as sfa_index_scores_bounded (each query on its own: no query groups).

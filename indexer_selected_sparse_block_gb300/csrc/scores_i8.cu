@@ -9,22 +9,29 @@
 //   sc_b = max_i |m_bi| / 127,   c_bi = round(m_bi / sc_b) in [-127, 127],
 //   r_b  = (|m_b - sc_b c_b|_2 + 2^-14 sc_b |c_b|_2) (1 + 2^-16),
 // so that the pass reads d_idx bytes per block (the hi-only pass reads 2 d_idx):
-//   a_bj = q_ij . c_b          (bf16 x small integers on the tensor cores, fp32 sums)
+//   q~_ij = binary16(q_ij)     (clamped to +-65504)
+//   a_bj = q~_ij . c_b         (binary16 x small integers on the tensor cores: exact products,
+//                               fp32 sums)
 //   s~_b = sc_b sum_j w_ij max(0, a_bj)
-//   |s_ib - s~_b| <= C_i r_b,  C_i = sum_j |w_ij| |q_ij|_2
-// (ReLU is 1-Lipschitz and sc_b >= 0; Cauchy-Schwarz per head; the fp32 rounding of this
-// chain, of the scale product and of the exact hi + lo chain together stays below
+//   |s_ib - s~_b| <= C_i r_b + D_i 127 sqrt(d_idx) sc_b,
+//   C_i = sum_j |w_ij| |q_ij|_2,  D_i = sum_j |w_ij| |q_ij - q~_ij|_2
+// (ReLU is 1-Lipschitz and sc_b >= 0; per head |q.m - q~.sc c| <= |q|_2 |m - sc c|_2 +
+// |q - q~|_2 sc |c|_2 by Cauchy-Schwarz, with |c|_2 <= 127 sqrt(d_idx); the fp32 rounding of
+// this chain, of the scale products and of the exact hi + lo chain together stays below
 // 2^-15 C_i sc_b |c_b|_2, which the second term of r_b covers twice).  lower = s~ - e,
-// upper = s~ + e with e = (1 + 2^-10) C_i r_b + 1e-30 then bracket the exact score like the
-// hi-only bounds, and sfa_topk_blocks_refine takes them unchanged.  The codes are looser than
-// the hi halves (about twice as many blocks survive the bounds), and the pass reads half the
-// bytes.
+// upper = s~ + e with e = (1 + 2^-10) (C_i r_b + D_i 127 sqrt(d_idx) sc_b) + 1e-30 then bracket
+// the exact score like the hi-only bounds, and sfa_topk_blocks_refine takes them unchanged.
+// The codes are looser than the hi halves (about twice as many blocks survive the bounds),
+// and the pass reads half the bytes.
 //
-// The score kernel streams 128-row tiles of codes with 2-D TMA into a ring
-// of shared-memory stages filled by one producer warp; four warps each take 32 rows through
-// mma.sync m16n8k16 (codes widened to bf16 in registers, exactly), with the k order permuted
-// so that each thread's A elements of a k-step are four consecutive bytes and its B elements
-// four consecutive query elements.  Every wait is bounded (SFA_DEV_TIMEOUT).
+// The score kernel streams 128-row tiles of codes with 2-D TMA into a ring of shared-memory
+// stages filled by one producer warp; four warps each take 32 rows through mma.sync m16n8k16
+// (codes widened to binary16 in registers, exactly, with one byte permute and one paired
+// subtraction per pair), with the k order permuted so that each thread's A elements of a
+// k-step are four consecutive bytes and its B elements four consecutive query elements.
+// Widening to bf16 instead (fp32 arithmetic and a pack per pair) ran 20% slower: the pass is
+// bound by its instruction issue as much as by its bytes.  Every wait is bounded
+// (SFA_DEV_TIMEOUT).
 #include <mutex>
 
 #include "sfa_common.cuh"
@@ -124,13 +131,13 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t lin) {
     return lin;
 }
 
-// Two 8-bit codes (bytes e, e + 1 of u = w ^ 0x80808080) as a bf16 pair, exactly: a byte placed
-// under the exponent of 2^23 reads as 2^23 + (code + 128).
-__device__ __forceinline__ float code_at(uint32_t u, uint32_t e) {
-    return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | e)) - 8388736.0f;
-}
-__device__ __forceinline__ uint32_t codes_to_bf16x2(uint32_t u, uint32_t e) {
-    return pack_bf16(code_at(u, e), code_at(u, e + 1));
+// Two 8-bit codes (bytes e, e + 1 of u = w ^ 0x80808080, i.e. code + 128) as a binary16 pair,
+// exactly: a byte placed under the binary16 exponent of 1024 reads as 1024 + (code + 128), and
+// one paired subtraction of 1152 leaves the code.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t e) {
+    const uint32_t x = __byte_perm(u, 0x64646464u, e == 0 ? 0x5140u : 0x7362u);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&x), __float2half2_rn(1152.f));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 template <int D, int H>
@@ -197,41 +204,60 @@ __global__ void __launch_bounds__(kI8Threads)
 
     // ------------------------------------------------------------ compute warps
     const int g = lane >> 2, t = lane & 3;
-    // B fragments: head n = 8 nt + g; in k-step ks, b0 holds query elements BPT t + 4 ks + {0, 1}
-    // and b1 elements BPT t + 4 ks + {2, 3} -- the same bytes the A fragments take from a row
-    // (the k order of both operands permuted alike).  C_q from the same registers.
+    // B fragments: the query of head n = 8 nt + g in binary16 (q~ = fp16(q), clamped to
+    // +-65504); in k-step ks, b0 holds query elements BPT t + 4 ks + {0, 1} and b1 elements
+    // BPT t + 4 ks + {2, 3} -- the same bytes the A fragments take from a row (the k order of
+    // both operands permuted alike).  The codes widen to binary16 exactly with two
+    // instructions per pair (below), and binary16 x codes products are exact in the fp32 sums.
+    // Per query: C_q = sum_n |w_n| |q_n|_2 and Dq = sum_n |w_n| |q_n - q~_n|_2 (the rounding of
+    // q to binary16, below 2^-11 |q_n| in range).
     uint32_t bq[NT][KS][2];
     float wv[NT][2];
-    float cq = 0.f;
+    float cq = 0.f, dq = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int n = 8 * nt + g;
         const __nv_bfloat16 *qr = p.q_idx + ((int64_t)i * H + (n < H ? n : 0)) * D + BPT * t;
-        float ss = 0.f;
+        float ss = 0.f, d2 = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint2 v = make_uint2(0u, 0u);
             if (n < H) v = *reinterpret_cast<const uint2 *>(qr + 4 * ks);
-            bq[nt][ks][0] = v.x;
-            bq[nt][ks][1] = v.y;
             const uint32_t u[2] = {v.x, v.y};
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const float e0 = __uint_as_float(u[k] << 16);
                 const float e1 = __uint_as_float(u[k] & 0xFFFF0000u);
                 ss = fmaf(e0, e0, fmaf(e1, e1, ss));
+                const float h0 = fminf(fmaxf(e0, -65504.f), 65504.f);
+                const float h1 = fminf(fmaxf(e1, -65504.f), 65504.f);
+                const uint32_t hh = pack_f16(h0, h1);
+                const __half2 hv = *reinterpret_cast<const __half2 *>(&hh);
+                const float r0 = e0 - __low2float(hv), r1 = e1 - __high2float(hv);
+                d2 = fmaf(r0, r0, fmaf(r1, r1, d2));
+                bq[nt][ks][k] = hh;
             }
         }
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);   // over t: |q_n|^2 in the quad
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-        float c = (t == 0 && n < H) ? fabsf(p.w[(int64_t)i * H + n]) * sqrtf(ss) : 0.f;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        for (int o = 1; o < 4; o <<= 1) {   // over t: the whole head in the quad
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+            d2 += __shfl_xor_sync(0xFFFFFFFFu, d2, o);
+        }
+        const float wn = (t == 0 && n < H) ? fabsf(p.w[(int64_t)i * H + n]) : 0.f;
+        float c = wn * sqrtf(ss), d = wn * sqrtf(d2);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+            d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+        }
         cq += c;
+        dq += d;
         const int h0 = 8 * nt + 2 * t;   // this thread's accumulator columns
         wv[nt][0] = h0 < H ? p.w[(int64_t)i * H + h0] : 0.f;
         wv[nt][1] = h0 + 1 < H ? p.w[(int64_t)i * H + h0 + 1] : 0.f;
     }
+    // |q . m - q~ . sc c| <= |q|_2 |m - sc c|_2 + |q - q~|_2 sc |c|_2, sc |c|_2 <= 127 sqrt(D) sc
+    const float dq_row = dq * (D == 128 ? 1437.0f : 1016.0f);
 
     // (scale, bound factor) of this thread's four rows of a tile, loaded one tile ahead
     const float *srs = p.sr + (int64_t)(nb > 0 ? seq : 0) * p.sr_seq_stride;
@@ -281,11 +307,11 @@ __global__ void __launch_bounds__(kI8Threads)
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const uint32_t ua = wa[ks] ^ 0x80808080u, ub = wb[ks] ^ 0x80808080u;
-                const uint32_t a[4] = {codes_to_bf16x2(ua, 0), codes_to_bf16x2(ub, 0),
-                                       codes_to_bf16x2(ua, 2), codes_to_bf16x2(ub, 2)};
+                const uint32_t a[4] = {codes_to_f16x2(ua, 0), codes_to_f16x2(ub, 0),
+                                       codes_to_f16x2(ua, 2), codes_to_f16x2(ub, 2)};
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
-                    mma_bf16_16816(acc[nt], a, bq[nt][ks][0], bq[nt][ks][1]);
+                    mma_f16_16816(acc[nt], a, bq[nt][ks][0], bq[nt][ks][1]);
             }
             // sum_j w_j max(0, a_j) of rows ra (columns 0, 1) and ra + 8 (columns 2, 3)
             float pa = 0.f, pb = 0.f;
@@ -306,7 +332,7 @@ __global__ void __launch_bounds__(kI8Threads)
                 const float2 f = t ? src[mt][1] : src[mt][0];
                 if (b < nb) {
                     const float sv = f.x * (t ? pb : pa);
-                    const float e = fmaf(kMarginI8 * cq, f.y, kAbsI8);
+                    const float e = fmaf(kMarginI8, fmaf(cq, f.y, dq_row * f.x), kAbsI8);
                     lo_row[b] = sv - e;   // the hi + lo score lies in [sv - e, sv + e]
                     up_row[b] = sv + e;
                 }
