@@ -237,8 +237,9 @@ int sfa_topk_blocks_refine(const float *lower, const float *upper, int64_t score
  *
  * sfa_quantize_pooled_keys_i8 writes, for rows [blk_begin, blk_end) of every sequence, from the
  * pooled keys m = hi + lo of Kbar (as written by any sfa_pool_index_keys* call):
- *   K8    [n_seq][k8_seq_stride / d_idx][d_idx] int8: c_bi = round(m_bi / sc_b), clamped to
- *         [-127, 127], with sc_b = max_i |m_bi| / 127 (0 for a zero row: c = 0)
+ *   K8    [n_seq][k8_seq_stride / d_idx][d_idx] bytes: c_bi + 128 (offset binary), with
+ *         c_bi = round(m_bi / sc_b) clamped to [-127, 127] and sc_b = max_i |m_bi| / 127 (0 for
+ *         a zero row: c = 0)
  *   K8_sr [n_seq][sr_seq_stride] fp32, pairs per block: (sc_b, r_b),
  *         r_b = (|m_b - sc_b c_b|_2 + 2^-14 sc_b |c_b|_2) (1 + 2^-16)   (fp32 norms)
  * Call it for the rows each pool call wrote.  Limits: d_idx in {64, 128}; Kbar and K8 16-byte

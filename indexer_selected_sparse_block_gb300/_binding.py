@@ -210,8 +210,8 @@ def sfa_index_scores_bounded(q_idx, w, q_seq, q_pos, Kbar, Kbar_r, compress_rati
 
 
 def k8_shapes(n_seq: int, blk_cap: int, d_idx: int):
-    """Shapes of the 8-bit pooled-key copy: codes [n_seq][blk_cap][d_idx] int8 and
-    (scale, bound factor) pairs [n_seq][blk_cap][2] fp32."""
+    """Shapes of the 8-bit pooled-key copy: codes [n_seq][blk_cap][d_idx] (int8 storage of the
+    bytes c + 128) and (scale, bound factor) pairs [n_seq][blk_cap][2] fp32."""
     return (n_seq, blk_cap, d_idx), (n_seq, blk_cap, 2)
 
 

@@ -6,7 +6,7 @@
 // use; llama.cpp commit "model: add Qwen3.8-Flash-Next (qwen4exp)", QSA paragraphs).  Here
 // the interval comes from a third copy of the pooled key, 8-bit codes with one fp32 scale per
 // row,
-//   sc_b = max_i |m_bi| / 127,   c_bi = round(m_bi / sc_b) in [-127, 127],
+//   sc_b = max_i |m_bi| / 127,   c_bi = round(m_bi / sc_b) in [-127, 127]  (stored as c + 128),
 //   r_b  = (|m_b - sc_b c_b|_2 + 2^-14 sc_b |c_b|_2) (1 + 2^-16),
 // so that the pass reads d_idx bytes per block (the hi-only pass reads 2 d_idx):
 //   q~_ij = binary16(q_ij)     (clamped to +-65504)
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256)
         const float rr = fmaf(-sc, c, m[e]);   // the residual with one rounding
         res2 = fmaf(rr, rr, res2);
         c2 = fmaf(c, c, c2);
-        packed |= ((uint32_t)(int)c & 0xFFu) << (8 * e);
+        packed |= (uint32_t)((int)c + 128) << (8 * e);   // offset binary: c + 128
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -131,9 +131,9 @@ __device__ __forceinline__ uint32_t tile_off(uint32_t lin) {
     return lin;
 }
 
-// Two 8-bit codes (bytes e, e + 1 of u = w ^ 0x80808080, i.e. code + 128) as a binary16 pair,
-// exactly: a byte placed under the binary16 exponent of 1024 reads as 1024 + (code + 128), and
-// one paired subtraction of 1152 leaves the code.
+// Two 8-bit codes (bytes e, e + 1 of u, each code + 128) as a binary16 pair, exactly: a byte
+// placed under the binary16 exponent of 1024 reads as 1024 + (code + 128), and one paired
+// subtraction of 1152 leaves the code.
 __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t e) {
     const uint32_t x = __byte_perm(u, 0x64646464u, e == 0 ? 0x5140u : 0x7362u);
     const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&x), __float2half2_rn(1152.f));
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kI8Threads)
             for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const uint32_t ua = wa[ks] ^ 0x80808080u, ub = wb[ks] ^ 0x80808080u;
+                const uint32_t ua = wa[ks], ub = wb[ks];
                 const uint32_t a[4] = {codes_to_f16x2(ua, 0), codes_to_f16x2(ub, 0),
                                        codes_to_f16x2(ua, 2), codes_to_f16x2(ub, 2)};
 #pragma unroll

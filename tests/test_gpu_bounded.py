@@ -318,7 +318,7 @@ def test_quantize_pooled_keys_i8(dev, d_idx):
     torch.cuda.synchronize()
     kb = np32(Kbar).astype(np.float64)
     m = kb[..., :d_idx] + kb[..., d_idx:]
-    c = K8.cpu().numpy().astype(np.float64)
+    c = K8.cpu().numpy().view(np.uint8).astype(np.float64) - 128.0   # stored as c + 128
     s = np32(sr).astype(np.float64)
     sc, r = s[..., 0], s[..., 1]
     rows = slice(b0, b1)
@@ -331,7 +331,8 @@ def test_quantize_pooled_keys_i8(dev, d_idx):
     assert np.all(r[:, rows] >= need)
     assert np.all(r[:, rows] <= need * (1 + 2 ** -12) + 1e-38)
     assert sc[1, 500] == 0 and r[1, 500] == 0 and np.all(c[1, 500] == 0)
-    assert np.all(c[:, :b0] == 0) and np.all(c[:, b1:] == 0)          # not written
+    raw = K8.cpu().numpy()
+    assert np.all(raw[:, :b0] == 0) and np.all(raw[:, b1:] == 0)      # not written
     assert np.all(s[:, :b0] == -1.0) and np.all(s[:, b1:] == -1.0)
 
 
