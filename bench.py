@@ -62,14 +62,15 @@ def src_hash(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload):
-    """dram bytes per launch from a committed ncu summary, if taken on the current source."""
+def recorded_traffic(kernel, workload, source):
+    """dram bytes per launch from a committed ncu summary, if taken on the current source of
+    the kernel that runs (source: its file)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(f"{kernel}@{workload}")
     except Exception:
         return None
-    if not rec or rec.get("src_sha256_16") != src_hash(rec["source"]):
+    if not rec or rec.get("source") != source or rec.get("src_sha256_16") != src_hash(source):
         return None
     return rec["dram_bytes_per_launch"]
 
@@ -628,7 +629,8 @@ def main():
         kernels[name] = k
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     dk = kernels[dom]
-    src = {"scores": "scores.cu", "attend": "attend.cu", "topk": "topk.cu", "pool": "pool.cu"}[dom]
+    src = {"scores": "scores_i8.cu" if wb.step.bound_pass == "i8" else "scores.cu",
+           "attend": "attend.cu", "topk": "topk.cu", "pool": "pool.cu"}[dom]
     # the kernel's bound is the resource it uses the larger fraction of
     if dk.get("tensor_frac", 0.0) > dk.get("hbm_frac", 0.0):
         roof = {"bound": "tensor", "achieved": dk["TFLOPs"], "peak": tf_peak, "unit": "TFLOP/s",
@@ -639,7 +641,7 @@ def main():
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" \
         else "fallback"
-    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["traffic"] = recorded_traffic(dom, w.name, src)
     roof["source"] = src
 
     e2e_ms, e2e_eager_ms, h2d, d2h, e2e_same = measure_e2e(wb, max(3, args.steps // 2), 3)

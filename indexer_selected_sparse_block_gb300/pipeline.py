@@ -39,7 +39,7 @@ class SfaStep:
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
                  n_blk_max: int, q_group: int = 1, bounded=None, key_transform=None,
                  cell_of=None, window: int = 0, window_mode: str = "single",
-                 bound_pass: str = "i8", device="cuda"):
+                 bound_pass=None, device="cuda"):
         self.__dict__.update(n_seq=n_seq, n_tok_cap=n_tok_cap, n_q=n_q, h_q=h_q, h_kv=h_kv,
                              dkq=dkq, dv=dv, h_idx=h_idx, d_idx=d_idx, cr=compress_ratio,
                              top_k=indexer_top_k, n_blk_max=n_blk_max, q_group=q_group)
@@ -73,6 +73,12 @@ class SfaStep:
         # bounded: the bound pass reads the 8-bit copy of the pooled keys ("i8": codes, a
         # scale and a bound factor per row, written after each pool call) or the hi halves
         # ("hi": the pooling pass also writes each pooled row's bound factor)
+        # Default: the 8-bit pass up to a budget of 1024 blocks.  Its bounds leave about three
+        # times the budget as candidates, which the selection resolves in shared memory up to
+        # 4096; past that (token-level budgets of 2048) the hi-only pass, whose bounds leave
+        # fewer, measured faster.
+        if bound_pass is None:
+            bound_pass = "i8" if indexer_top_k <= 1024 else "hi"
         if bound_pass not in ("i8", "hi"):
             raise ValueError("bound_pass must be 'i8' or 'hi'")
         self.bound_pass = bound_pass if self.bounded else None
