@@ -50,18 +50,30 @@ __device__ void cluster_merge(const AttnParams &p, float *sPart, float *sL, floa
     const int tid = threadIdx.x, G = p.G, ns = p.n_split;
     cl.sync();   // every CTA's partial rows and statistics are in its shared memory
     const int r = (int)cl.block_rank();
+    // Every remote load of a step is issued before any is used (the split count is at most 8,
+    // unrolled with predicates): one round trip over distributed shared memory per step
+    // instead of one per split.
+    constexpr int kMaxNs = 8;
     if (tid < G) {
+        float mv[kMaxNs], lv[kMaxNs];
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c) {
+            mv[c] = c < ns ? cl.map_shared_rank(sM, c)[tid] : -INFINITY;
+            lv[c] = c < ns ? cl.map_shared_rank(sL, c)[tid] : 0.f;
+        }
         float M = -INFINITY;
-        for (int c = 0; c < ns; ++c) M = fmaxf(M, cl.map_shared_rank(sM, c)[tid]);
-        float Lsum = 0.f;
-        for (int c = 0; c < ns; ++c) {
-            const float m = cl.map_shared_rank(sM, c)[tid];
-            const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-            sW[c * 16 + tid] = w;
-            Lsum += w * cl.map_shared_rank(sL, c)[tid];
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c) M = fmaxf(M, mv[c]);
+        float Lsum = 0.f, wv[kMaxNs];
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c) {
+            wv[c] = mv[c] == -INFINITY ? 0.f : exp2f(mv[c] - M);
+            Lsum += wv[c] * lv[c];
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        for (int c = 0; c < ns; ++c) sW[c * 16 + tid] *= inv;
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c)
+            if (c < ns) sW[c * 16 + tid] = wv[c] * inv;
         if (r == 0 && p.lse)
             p.lse[(int64_t)i * p.h_q + g * G + tid] = Lsum > 0.f ? (M + log2f(Lsum)) / kLog2e : -INFINITY;
     }
@@ -70,15 +82,23 @@ __device__ void cluster_merge(const AttnParams &p, float *sPart, float *sL, floa
     const int d0 = r * (DV / ns);
     for (int e = tid; e < G * dq; e += kThreads) {
         const int row = e / dq, d = d0 + 4 * (e % dq);
+        float wc[kMaxNs];
+        float4 v[kMaxNs];
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c) {
+            wc[c] = c < ns ? sW[c * 16 + row] : 0.f;
+            // an empty split (weight 0) wrote no rows: not read
+            v[c] = wc[c] != 0.f
+                       ? *reinterpret_cast<const float4 *>(cl.map_shared_rank(sPart, c) + row * DV + d)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < ns; ++c) {
-            const float w = sW[c * 16 + row];
-            if (w == 0.f) continue;   // an empty split: its rows are not written
-            const float4 v = *reinterpret_cast<const float4 *>(cl.map_shared_rank(sPart, c) + row * DV + d);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+        for (int c = 0; c < kMaxNs; ++c) {
+            acc.x = fmaf(wc[c], v[c].x, acc.x);
+            acc.y = fmaf(wc[c], v[c].y, acc.y);
+            acc.z = fmaf(wc[c], v[c].z, acc.z);
+            acc.w = fmaf(wc[c], v[c].w, acc.w);
         }
         *reinterpret_cast<float4 *>(p.O + ((int64_t)i * p.h_q + g * G + row) * DV + d) = acc;
     }
