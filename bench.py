@@ -358,10 +358,10 @@ def measure_e2e(wb, steps, warmup):
     """Same step through the public API with host inputs: each step copies this step's query
     inputs and new cache rows from pinned host memory, runs, and has O in host memory at its
     end.  The query inputs travel in one copy (one pinned host arena mirrored by one device
-    arena).  The new cache rows go from the same host arena straight into their cache slots
-    (sfa_copy_cache_rows, one two-dimensional copy per cache); q8_0 caches quantize them on the
-    device first, and a paged cache places them into their cells.  The attention writes O
-    into pinned host memory directly (SfaStep.set_output)."""
+    arena), and the new cache rows go from the same host arena straight into their cache slots
+    (sfa_copy_cache_rows: a copy kernel reading the pinned host memory); q8_0 caches quantize
+    them on the device first, and a paged cache places them into their cells.  The attention
+    writes O into pinned host memory directly (SfaStep.set_output)."""
     c, w = wb.case, wb.w
     sl = slice(w.depth, w.n_tok)   # the step's new cache rows (positions depth .. n_tok - 1)
     new_rows = {n: t[:, sl] for n, t in wb.seq_rows.items()}   # bf16, from the host
@@ -400,7 +400,7 @@ def measure_e2e(wb, steps, warmup):
     d2h = out.numel() * out.element_size()
 
     def one():
-        dev_arena[:n_dev].copy_(host_arena[:n_dev], non_blocking=True)
+        B.sfa_copy_cache_rows(dev_arena[:n_dev].view(1, -1), host_arena[:n_dev].view(1, -1))
         for n in new_rows:
             if not via_dev:   # host rows straight into the cache slots
                 B.sfa_copy_cache_rows(c[n][:, sl], hv[f"{n}_new"])

@@ -500,9 +500,11 @@ int sfa_gather_attend_noalloc(const void *Q, const void *K, const void *V, int d
  * sfa_copy_cache_rows -- plumbing, not part of the method: places n_rows rows of row_bytes
  * bytes, spaced src_pitch bytes apart at src, into rows spaced dst_pitch bytes apart at dst --
  * typically a step's new cache rows (one per sequence) written into their slots of the K, V
- * or index-key caches.  Either side may be device memory or page-locked host memory; the copy
- * is one two-dimensional copy on `stream`.  row_bytes >= 1, pitches >= row_bytes, n_rows >= 0;
- * SFA_ERR_INVALID_ARG otherwise, SFA_ERR_CUDA if the runtime refuses the copy.
+ * or index-key caches, or a step's query inputs (one row).  Either side may be device memory
+ * or page-locked host memory that the device addresses (unified addressing); the copy is one
+ * kernel on `stream` (SM loads and stores, 16 bytes at a time when the addresses, pitches and
+ * row size are multiples of 16).  row_bytes >= 1, pitches >= row_bytes, n_rows >= 0;
+ * SFA_ERR_INVALID_ARG otherwise, SFA_ERR_CUDA if the launch fails.
  */
 int sfa_copy_cache_rows(void *dst, int64_t dst_pitch, const void *src, int64_t src_pitch,
                         int64_t row_bytes, int64_t n_rows, sfa_stream_t stream);

@@ -35,6 +35,27 @@ def test_copy_cache_rows_into_strided_slots(dev, src_on, n_new):
     assert torch.equal(cache[:, 17 + n_new:], before[:, 17 + n_new:])
 
 
+@pytest.mark.parametrize("src_on", ["host", "device"])
+def test_copy_cache_rows_odd_sizes(dev, src_on):
+    """Rows whose size and pitches are not multiples of 16 bytes (the byte-wise path), and one
+    long row (a step's query inputs as one copy)."""
+    g = torch.Generator().manual_seed(12)
+    cache = torch.randint(-100, 100, (4, 10, 15), generator=g, dtype=torch.int8).to(dev)
+    before = cache.clone()
+    rows = torch.randint(-100, 100, (4, 1, 15), generator=g, dtype=torch.int8)
+    src = rows.pin_memory() if src_on == "host" else rows.to(dev)
+    sfa.sfa_copy_cache_rows(cache[:, 7:8], src)
+    torch.cuda.synchronize()
+    assert torch.equal(cache[:, 7:8].cpu(), rows)
+    assert torch.equal(cache[:, :7], before[:, :7]) and torch.equal(cache[:, 8:], before[:, 8:])
+    big = torch.randint(0, 255, (1, 700000), generator=g, dtype=torch.uint8)
+    big_src = big.pin_memory() if src_on == "host" else big.to(dev)
+    dst = torch.zeros((1, 700000), dtype=torch.uint8, device=dev)
+    sfa.sfa_copy_cache_rows(dst, big_src)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), big)
+
+
 def test_copy_cache_rows_rejects_unpinned_and_mismatched(dev):
     cache = torch.zeros((4, 8, 16), dtype=torch.bfloat16, device=dev)
     with pytest.raises(ValueError):
