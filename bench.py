@@ -358,9 +358,9 @@ def measure_e2e(wb, steps, warmup):
     """Same step through the public API with host inputs: each step copies this step's query
     inputs and new cache rows from pinned host memory, runs, and has O in host memory at its
     end.  The query inputs travel in one copy (one pinned host arena mirrored by one device
-    arena), and the new cache rows go from the same host arena straight into their cache slots
-    (sfa_copy_cache_rows: a copy kernel reading the pinned host memory); q8_0 caches quantize
-    them on the device first, and a paged cache places them into their cells.  The attention
+    arena), and the new cache rows go from the same host arena straight into their cache slots,
+    all in one copy kernel reading the pinned host memory (sfa_copy_cache_rows_multi); q8_0
+    caches quantize them on the device first, and a paged cache places them into their cells.  The attention
     writes O into pinned host memory directly (SfaStep.set_output)."""
     c, w = wb.case, wb.w
     sl = slice(w.depth, w.n_tok)   # the step's new cache rows (positions depth .. n_tok - 1)
@@ -400,10 +400,12 @@ def measure_e2e(wb, steps, warmup):
     d2h = out.numel() * out.element_size()
 
     def one():
-        B.sfa_copy_cache_rows(dev_arena[:n_dev].view(1, -1), host_arena[:n_dev].view(1, -1))
+        copies = [(dev_arena[:n_dev].view(1, -1), host_arena[:n_dev].view(1, -1))]
+        if not via_dev:   # host rows straight into the cache slots, in the same launch
+            copies += [(c[n][:, sl], hv[f"{n}_new"]) for n in new_rows]
+        B.sfa_copy_cache_rows_multi(copies)
         for n in new_rows:
-            if not via_dev:   # host rows straight into the cache slots
-                B.sfa_copy_cache_rows(c[n][:, sl], hv[f"{n}_new"])
+            if not via_dev:
                 continue
             src = dv[f"{n}_new"]
             if n in staging:

@@ -508,6 +508,22 @@ int sfa_gather_attend_noalloc(const void *Q, const void *K, const void *V, int d
  */
 int sfa_copy_cache_rows(void *dst, int64_t dst_pitch, const void *src, int64_t src_pitch,
                         int64_t row_bytes, int64_t n_rows, sfa_stream_t stream);
+/*
+ * sfa_copy_cache_rows_multi -- n (<= SFA_MAX_ROW_COPIES) such copies in one kernel launch
+ * (a step's query inputs and the new rows of each cache at once).  Every entry is checked as
+ * sfa_copy_cache_rows checks its arguments before anything is launched; entries with n_rows = 0
+ * are skipped.  The copies must not overlap one another.
+ */
+#define SFA_MAX_ROW_COPIES 8
+typedef struct {
+    void *dst;
+    int64_t dst_pitch;
+    const void *src;
+    int64_t src_pitch;
+    int64_t row_bytes;
+    int64_t n_rows;
+} sfa_row_copy;
+int sfa_copy_cache_rows_multi(int n, const sfa_row_copy *copies, sfa_stream_t stream);
 
 /* Copies *dev_status to *host_out after the work already enqueued on `stream` (this call
  * synchronises the stream). */

@@ -10,7 +10,8 @@ from ._binding import (SFA_BF16, SFA_DEV_BAD_BLOCK, SFA_DEV_BAD_CELL, SFA_DEV_BA
                        SFA_OK, SFA_PART_ALL, SFA_PART_SELECTED, SFA_PART_WINDOW, SFA_Q8_0,
                        SFA_REFINE_MAX_BLOCKS, SfaError, kbar_shape, lib,
                        sfa_attend_plan, sfa_attend_workspace_bytes, sfa_combine_attention,
-                       sfa_copy_cache_rows, sfa_dense_attend, sfa_dense_attend_paged,
+                       sfa_copy_cache_rows, sfa_copy_cache_rows_multi, sfa_dense_attend,
+                       sfa_dense_attend_paged,
                        sfa_gather_attend, sfa_gather_attend_noalloc, sfa_gather_attend_paged,
                        sfa_gather_attend_window, sfa_gather_kv_bandwidth, sfa_index_scores,
                        sfa_index_scores_bounded, sfa_index_scores_bounded_i8, k8_shapes,

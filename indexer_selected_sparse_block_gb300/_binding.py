@@ -27,6 +27,15 @@ _lib = None
 _vp, _i64, _int, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                               ctypes.c_size_t)
 
+class _RowCopy(ctypes.Structure):
+    """sfa_row_copy of include/sfa.h."""
+    _fields_ = [("dst", ctypes.c_void_p), ("dst_pitch", ctypes.c_int64),
+                ("src", ctypes.c_void_p), ("src_pitch", ctypes.c_int64),
+                ("row_bytes", ctypes.c_int64), ("n_rows", ctypes.c_int64)]
+
+
+SFA_MAX_ROW_COPIES = 8
+
 # name -> (restype, argtypes); mirrors include/sfa.h
 SIGNATURES = {
     "sfa_pool_index_keys": (_int, [_vp, _int, _i64, _int, _int, _int, _i64, _i64, _vp, _i64, _vp,
@@ -77,6 +86,7 @@ SIGNATURES = {
     "sfa_q8_0_row_bytes": (_sz, [_int]),
     "sfa_quantize_kv_q8_0": (_int, [_vp, _int, _i64, _i64, _int, _i64, _vp, _i64, _vp, _vp]),
     "sfa_copy_cache_rows": (_int, [_vp, _i64, _vp, _i64, _i64, _i64, _vp]),
+    "sfa_copy_cache_rows_multi": (_int, [_int, _vp, _vp]),
     "sfa_read_device_status": (_int, [_vp, _vp, _vp]),
     "sfa_status_string": (ctypes.c_char_p, [_int]),
 }
@@ -498,6 +508,33 @@ def sfa_quantize_kv_q8_0(X, Y, dev_status=None, stream=None):
                                     X.stride(0), _p(Y, strided=True), Y.stride(0), _p(dev_status),
                                     _stream(stream))
     _check("sfa_quantize_kv_q8_0", rc)
+
+
+def _row_copy(dst, src):
+    if tuple(dst.shape) != tuple(src.shape) or dst.dtype != src.dtype or dst.dim() < 1:
+        raise ValueError("dst and src must have the same shape and dtype")
+    for t in (dst, src):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("sfa_copy_cache_rows takes CUDA or page-locked host tensors")
+        if t.shape[0] > 0 and not t[0].is_contiguous():
+            raise ValueError("each row must be contiguous")
+    es = dst.element_size()
+    n = dst.shape[0]
+    row = dst[0].numel() * es if n > 0 else 0
+    dp = dst.stride(0) * es if n > 1 else max(row, 1)
+    sp = src.stride(0) * es if n > 1 else max(row, 1)
+    return _RowCopy(dst.data_ptr(), dp, src.data_ptr(), sp, max(row, 1), n if row else 0)
+
+
+def sfa_copy_cache_rows_multi(pairs, stream=None) -> None:
+    """Several (dst, src) row copies as sfa_copy_cache_rows makes them, in one kernel launch."""
+    pairs = list(pairs)
+    if len(pairs) > SFA_MAX_ROW_COPIES:
+        raise ValueError(f"at most {SFA_MAX_ROW_COPIES} copies per call")
+    arr = (_RowCopy * max(len(pairs), 1))(*[_row_copy(d, s) for d, s in pairs])
+    rc = lib().sfa_copy_cache_rows_multi(len(pairs), ctypes.cast(arr, ctypes.c_void_p),
+                                         _stream(stream))
+    _check("sfa_copy_cache_rows_multi", rc)
 
 
 def sfa_copy_cache_rows(dst, src, stream=None) -> None:

@@ -117,8 +117,69 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Several such copies in one launch: copy blockIdx.y of the list.
+struct RowCopies {
+    sfa_row_copy c[SFA_MAX_ROW_COPIES];
+    int vec16[SFA_MAX_ROW_COPIES];
+};
+__global__ void __launch_bounds__(256) copy_rows_multi_kernel(const RowCopies rc) {
+    pdl_wait();
+    const sfa_row_copy &c = rc.c[blockIdx.y];
+    const int vec16 = rc.vec16[blockIdx.y];
+    uint8_t *dst = reinterpret_cast<uint8_t *>(c.dst);
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(c.src);
+    const int64_t per_row = vec16 ? c.row_bytes >> 4 : c.row_bytes;
+    const int64_t total = per_row * c.n_rows;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const int64_t r = e / per_row, k = e - r * per_row;
+        if (vec16)
+            *reinterpret_cast<uint4 *>(dst + r * c.dst_pitch + 16 * k) =
+                *reinterpret_cast<const uint4 *>(src + r * c.src_pitch + 16 * k);
+        else
+            dst[r * c.dst_pitch + k] = src[r * c.src_pitch + k];
+    }
+}
+
+bool copy_valid(const sfa_row_copy &c) {
+    return c.n_rows >= 0 && c.row_bytes >= 1 && c.dst_pitch >= c.row_bytes &&
+           c.src_pitch >= c.row_bytes && (c.n_rows == 0 || (c.dst && c.src));
+}
+bool copy_vec16(const sfa_row_copy &c) {
+    return aligned16(c.dst) && aligned16(c.src) && c.dst_pitch % 16 == 0 &&
+           c.src_pitch % 16 == 0 && c.row_bytes % 16 == 0;
+}
+
 }  // namespace
 }  // namespace sfa
+
+extern "C" int sfa_copy_cache_rows_multi(int n, const sfa_row_copy *copies, sfa_stream_t stream) {
+    using namespace sfa;
+    if (n < 0 || n > SFA_MAX_ROW_COPIES || (n > 0 && !copies)) return SFA_ERR_INVALID_ARG;
+    RowCopies rc{};
+    int64_t most = 0;
+    int m = 0;
+    for (int k = 0; k < n; ++k) {
+        if (!copy_valid(copies[k])) return SFA_ERR_INVALID_ARG;
+        if (copies[k].n_rows == 0) continue;
+        rc.c[m] = copies[k];
+        rc.vec16[m] = copy_vec16(copies[k]);
+        const int64_t t = (rc.vec16[m] ? copies[k].row_bytes / 16 : copies[k].row_bytes) *
+                          copies[k].n_rows;
+        most = t > most ? t : most;
+        ++m;
+    }
+    if (m == 0) return SFA_OK;
+    int64_t blocks = (most + 255) / 256;
+    const int64_t cap = 4 * (int64_t)device_sm_count();
+    if (blocks > cap) blocks = cap;
+    if (launch_pdl(copy_rows_multi_kernel, dim3((unsigned)blocks, (unsigned)m), dim3(256), 0,
+                   (cudaStream_t)stream, rc) != cudaSuccess) {
+        cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    return SFA_OK;
+}
 
 extern "C" int sfa_copy_cache_rows(void *dst, int64_t dst_pitch, const void *src,
                                    int64_t src_pitch, int64_t row_bytes, int64_t n_rows,

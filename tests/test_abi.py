@@ -238,6 +238,57 @@ def test_copy_cache_rows_rejects_bad_arguments(L):
     assert f(*a) == 0                                                             # empty: no work
 
 
+def test_i8_bound_pass_rejects_bad_arguments(L):
+    q = L.sfa_quantize_pooled_keys_i8
+    #     Kbar  kstride  n_seq d   b0 b1   K8    k8stride  sr    srstride stream
+    ok = [FAKE, 256 * 100, 2, 128, 0, 100, FAKE, 128 * 100, FAKE, 200, None]
+    bad = list(ok); bad[3] = 96
+    assert q(*bad) == 2                                                    # d_idx
+    bad = list(ok); bad[7] = 128 * 99
+    assert q(*bad) == 1                                                    # code rows short
+    bad = list(ok); bad[9] = 199
+    assert q(*bad) == 1                                                    # (scale, r) pairs short
+    bad = list(ok); bad[6] = ODD
+    assert q(*bad) == 1                                                    # K8 alignment
+    bad = list(ok); bad[4] = 5; bad[5] = 4
+    assert q(*bad) == 1                                                    # begin > end
+    bad = list(ok); bad[5] = 0
+    assert q(*bad) == 0                                                    # empty: no work
+    f = L.sfa_index_scores_bounded_i8
+    #     q_idx w     q_seq q_pos n_q h  d    cr K8    k8stride   sr    srstride n_seq nbm
+    ok = [FAKE, FAKE, FAKE, FAKE, 4, 8, 128, 4, FAKE, 128 * 100, FAKE, 200, 1, 100,
+          FAKE, FAKE, 100, None, None]
+    bad = list(ok); bad[5] = 5
+    assert f(*bad) == 2                                                    # h_idx
+    bad = list(ok); bad[6] = 32
+    assert f(*bad) == 2                                                    # d_idx
+    bad = list(ok); bad[13] = 101
+    assert f(*bad) == 1                                                    # n_blk_max > cap
+    bad = list(ok); bad[11] = 198
+    assert f(*bad) == 1                                                    # pairs short
+    bad = list(ok); bad[9] = 128 * 100 + 8
+    assert f(*bad) == 1                                                    # stride % d_idx
+    bad = list(ok); bad[15] = None
+    assert f(*bad) == 1                                                    # no upper array
+    bad = list(ok); bad[4] = 0
+    assert f(*bad) == 0                                                    # no queries: no work
+
+
+def test_copy_cache_rows_multi_rejects_bad_arguments(L):
+    from indexer_selected_sparse_block_gb300._binding import _RowCopy, SFA_MAX_ROW_COPIES
+    f = L.sfa_copy_cache_rows_multi
+    ok = _RowCopy(0x10000, 2048, 0x20000, 1152, 1152, 32)
+    bad = _RowCopy(0x10000, 1024, 0x20000, 1152, 1152, 32)       # dst rows overlap
+    arr = (_RowCopy * 2)(ok, bad)
+    assert f(2, ctypes.cast(arr, ctypes.c_void_p), None) == 1
+    assert f(1, None, None) == 1                                  # no list
+    assert f(-1, None, None) == 1
+    assert f(SFA_MAX_ROW_COPIES + 1, ctypes.cast(arr, ctypes.c_void_p), None) == 1
+    assert f(0, None, None) == 0                                  # nothing to copy
+    empty = (_RowCopy * 1)(_RowCopy(None, 16, None, 16, 16, 0))
+    assert f(1, ctypes.cast(empty, ctypes.c_void_p), None) == 0   # zero rows: skipped
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """No CPU fallback: with libsfa.so absent, the first entry-point call raises."""
     import indexer_selected_sparse_block_gb300 as sfa

@@ -56,6 +56,23 @@ def test_copy_cache_rows_odd_sizes(dev, src_on):
     assert torch.equal(dst.cpu(), big)
 
 
+def test_copy_cache_rows_multi(dev):
+    """Three copies in one launch -- one long row, strided bf16 rows, odd-sized int8 rows --
+    each lands where the single copy puts it."""
+    g = torch.Generator().manual_seed(13)
+    arena_h = torch.randint(0, 255, (1, 123456), generator=g, dtype=torch.uint8).pin_memory()
+    arena_d = torch.zeros((1, 123456), dtype=torch.uint8, device=dev)
+    K = torch.zeros((6, 30, 1, 576), dtype=torch.bfloat16, device=dev)
+    krows = torch.randn((6, 1, 1, 576), generator=g).to(torch.bfloat16).pin_memory()
+    X = torch.zeros((6, 30, 15), dtype=torch.int8, device=dev)
+    xrows = torch.randint(-9, 9, (6, 1, 15), generator=g, dtype=torch.int8).pin_memory()
+    sfa.sfa_copy_cache_rows_multi([(arena_d, arena_h), (K[:, 29:30], krows), (X[:, 4:5], xrows)])
+    torch.cuda.synchronize()
+    assert torch.equal(arena_d.cpu(), arena_h)
+    assert torch.equal(K[:, 29:30].cpu(), krows) and torch.count_nonzero(K[:, :29]) == 0
+    assert torch.equal(X[:, 4:5].cpu(), xrows) and torch.count_nonzero(X[:, 5:]) == 0
+
+
 def test_copy_cache_rows_rejects_unpinned_and_mismatched(dev):
     cache = torch.zeros((4, 8, 16), dtype=torch.bfloat16, device=dev)
     with pytest.raises(ValueError):
