@@ -966,25 +966,44 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                 }
         }
         __syncthreads();
-        // ---- 3. exact scores of this share's candidates: a warp takes 8 at a time, every
-        // piece of their rows in flight at once
+        // ---- 3. exact scores of the candidates, split evenly over the cluster's CTAs (global
+        // index q in [0, total), ordered by share; CTA r takes [total r / CL, total (r + 1) / CL)
+        // and reads the ids of other shares from their CTAs' shared memory): a warp takes 8 at a
+        // time, every piece of their rows in flight at once
         {
             constexpr int kTR = 8;
-            const int32_t *lid = in_smem ? sh.cand_idx : gid + off;
+            const int q0 = (int)((int64_t)total * rank / kCl);
+            const int q1 = (int)((int64_t)total * (rank + 1) / kCl);
+            const int nmine = q1 - q0;
+            int offs[kCl + 1];
+            offs[0] = 0;
+#pragma unroll
+            for (int r = 0; r < kCl; ++r) offs[r + 1] = offs[r] + lead.cnt[r];
             const __nv_bfloat16 *kseq = p.kbar + (int64_t)seq * p.kbar_seq_stride;
             const int g = lane >> 2;
-            for (int c0 = warp * kTR; c0 < mine; c0 += kWarps * kTR) {
-                const int ra = c0 + g;
-                const int ba = lid[ra < mine ? ra : c0];
+            for (int c0 = warp * kTR; c0 < nmine; c0 += kWarps * kTR) {
+                const bool live = c0 + g < nmine;
+                const int qa = q0 + c0 + (live ? g : 0);   // global index of this lane group's row
+                int ba;
+                if (in_smem) {
+                    int o = 0;   // the share holding qa
+#pragma unroll
+                    for (int r = 1; r < kCl; ++r) o += qa >= offs[r] ? 1 : 0;
+                    ba = cluster.map_shared_rank(sh.cand_idx, o)[qa - offs[o]];
+                } else {
+                    ba = gid[qa];
+                }
                 float sa, unused;
                 const __nv_bfloat16 *ka = kseq + (int64_t)ba * 2 * D;
                 rescore_tile<D, kTR>(ka, ka, bs, H, sa, unused);
-                if ((lane & 3) == 0 && ra < mine) {
+                if ((lane & 3) == 0 && live) {
                     if (in_smem) {
-                        lead.sh.cand_key[off + ra] = order_key(sa);
-                        lead.sh.cand_idx[off + ra] = ba;
+                        // rank 0's own list shares the leader's array with the result: the id
+                        // written at a position of it is the one already there
+                        lead.sh.cand_key[qa] = order_key(sa);
+                        lead.sh.cand_idx[qa] = ba;
                     } else {
-                        gbits[off + ra] = __float_as_uint(sa);
+                        gbits[qa] = __float_as_uint(sa);
                     }
                 }
             }
