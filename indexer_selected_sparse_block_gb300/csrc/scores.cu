@@ -419,9 +419,10 @@ int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const in
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return SFA_ERR_CUDA;
 
-    // Queries per tile: the largest power of two that divides q_group and fits N <= 256 (and
-    // the B tile fits next to the pooled-key stages).
-    const int n_cap = (KP == 256 && !hi) ? 128 : 256;
+    // Queries per tile: the largest power of two that divides q_group and fits N <= 256 (the
+    // B tile then takes 128 KB of the 220 KB budget at K' = 256, leaving five pooled-key
+    // stages; pp2048's scores ran 453 us with N capped at 128 there, 429 us at 256).
+    const int n_cap = 256;
     int q_tile = 1;
     while (q_tile * 2 * h_idx <= n_cap && q_group % (q_tile * 2) == 0) q_tile *= 2;
     ScoreParams p{};
