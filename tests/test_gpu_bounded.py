@@ -397,6 +397,33 @@ def test_refine_follows_agreement_rule_i8(dev, top_k):
     assert n_exact >= len(pos) - 1
 
 
+@pytest.mark.parametrize("n_tok", [4000, 24000])
+def test_refine_all_tied_i8(dev, n_tok):
+    """Every pooled key equal: the 8-bit bounds are equal too, every block is a candidate
+    (past 4096 of them, the global-memory list) and the lowest block indices win."""
+    cr, d_idx, h_idx, top_k = 4, 64, 4, 100
+    pos = [n_tok - 1, n_tok // 2 + 1]
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 5, 2, n_tok, d_idx, h_idx, cr, pos,
+                                         constant_keys=True)
+    n_q, n_blk_max = 2, n_tok // cr
+    K8, sr = _k8(dev, Kb[0], n_blk_max, d_idx, 0, n_blk_max)
+    lower = torch.empty((n_q, n_blk_max), device=dev)
+    upper = torch.empty_like(lower)
+    blk = torch.empty((n_q, top_k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(n_q, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores_bounded_i8(qi, w, q_seq, q_pos, K8, sr, cr, n_blk_max, lower, upper,
+                                    dev_status=status)
+    sfa.sfa_topk_blocks_refine(lower, upper, qi, w, q_seq, q_pos, Kb[0], cr, top_k, n_blk_max,
+                               blk, n_sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    assert np.array_equal(np32(n_sel), [top_k, top_k])
+    got = np32(blk)
+    for i in range(n_q):
+        assert np.array_equal(got[i], np.arange(top_k))
+
+
 @pytest.mark.parametrize("name,bound_pass", [("decode_32x131072", "hi"),
                                              ("decode_4x1048576", "hi"),
                                              ("decode_cr1_32x32768", "i8")])
