@@ -16,7 +16,8 @@
 //   warp 0      TMA producer: one pipeline stage = one 128-row x 128-byte slab of Kbar
 //               (16 KB, 128-byte swizzle); a tile is 2 (d_idx 64) or 4 (d_idx 128) slabs
 //   warp 1      tensor-memory owner and single-thread MMA issuer (M = 128, N = q_tile*H pad 16)
-//   warps 2..5  epilogue: tcgen05.ld (lane = block), ReLU . w, head sum, coalesced stores
+//   warps 2..5  epilogue (2..9 for wide tiles): tcgen05.ld (lane = block), ReLU . w, head
+//               sum, coalesced stores
 // Two accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs of
 // tile t + 1; for narrow tiles the producer fills the pipeline before the rest of the set-up.
 // Every wait is bounded (SFA_DEV_TIMEOUT) and tensor memory is always released.
@@ -28,7 +29,15 @@ namespace sfa {
 namespace {
 
 constexpr int kBM = 128;               // blocks per tile (MMA M)
-constexpr int kThreads = 192;          // 6 warps
+// Warps: the TMA producer, the MMA issuer and the epilogue warps -- four for narrow tiles
+// (decode, four CTAs per SM), twelve for wide ones (prefill, one CTA per SM: three epilogue
+// warps per scheduler hide each other's tensor-memory and arithmetic latency; pp2048's scores
+// took 430 us with four, 281 with eight, 248 with twelve and 262 with sixteen).
+template <bool WIDE>
+struct Warps {
+    static constexpr int kEpi = WIDE ? 12 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpi;
+};
 constexpr int kSlabBytes = kBM * 128;  // one pipeline stage
 // The bounded mode's error bound per score: |s - a| <= e = kMargin * C_q * r_b (+ kAbs), with
 // C_q = sum_j |w_j| |q_j|_2 and r_b = |lo_b|_2 + 2^-14 |hi_b|_2 from the pooling pass.  The
@@ -63,20 +72,24 @@ struct Layout {
 // HI = false: K' = 2 d_idx over [hi | lo] against [q | q] (the exact score).  HI = true (the
 // bounded mode): K' = d_idx over hi only against q; the score from hi, less and plus its error
 // bound (from the norm of the hi row), gives the lower and upper bounds of the exact score
-// (see sfa_index_scores_bounded).
-template <int KP, int H, bool HI>
-__global__ void __launch_bounds__(kThreads, 1)
+// (see sfa_index_scores_bounded).  WIDE: tiles of more than 32 columns (prefill), one CTA per
+// SM, whose epilogue reads 64 accumulator columns per wait; narrow tiles (decode) run four
+// CTAs per SM and read 16 at a time.
+template <int KP, int H, bool HI, bool WIDE>
+__global__ void __launch_bounds__(Warps<WIDE>::kThreads, WIDE ? 1 : 4)
     index_score_kernel(const __grid_constant__ CUtensorMap kbar_map, const ScoreParams p) {
     using L = Layout<HI ? KP / 2 : KP>;   // KP: the stored row (2 d_idx); L: the slabs read
+    constexpr int kThreads = Warps<WIDE>::kThreads, kEpi = Warps<WIDE>::kEpi;
     constexpr int D = KP / 2;
-    constexpr int KB = HI ? D : KP;       // K' of the MMA chain and of the B operand
+    // The B operand holds each query row once (d_idx wide): the exact mode's chain over
+    // [hi | lo] meets the same q rows for both halves, so its lo slabs reuse the hi slabs' B.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int S = p.stages, N = p.N;
     uint8_t *sA = smem;                                    // S x kSlabBytes
-    uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x KB bf16, swizzled
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * KB * 2);
+    uint8_t *sB = sA + (size_t)S * kSlabBytes;             // N x D bf16, swizzled
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)N * D * 2);
     uint64_t *full = bars, *empty = bars + S, *acc_full = bars + 2 * S,
              *acc_empty = bars + 2 * S + 2, *drain = bars + 2 * S + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
@@ -97,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&acc_empty[i], kEpi);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -153,17 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qq = e / H;
         s_w[e] = qq < nq_tile ? p.w[(int64_t)(q0 + qq) * H + (e % H)] : 0.f;
     }
-    // B operand: row n = (query qq, head j), K' = [q | q] (or q); 16-byte chunks, 128-byte
-    // swizzle.
-    for (int e = threadIdx.x; e < N * (KB / 8); e += kThreads) {
-        const int n = e / (KB / 8), c = e % (KB / 8);
+    // B operand: row n = (query qq, head j), its d_idx dims in slabs of 64; 16-byte chunks,
+    // 128-byte swizzle.
+    for (int e = threadIdx.x; e < N * (D / 8); e += kThreads) {
+        const int n = e / (D / 8), c = e % (D / 8);
         const int qq = n / H, j = n % H;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (qq < nq_tile && n < p.q_tile * H) {
-            const int src_c = c % (D / 8);
-            v = *reinterpret_cast<const uint4 *>(p.q_idx + ((int64_t)(q0 + qq) * H + j) * D +
-                                                 src_c * 8);
-        }
+        if (qq < nq_tile && n < p.q_tile * H)
+            v = *reinterpret_cast<const uint4 *>(p.q_idx + ((int64_t)(q0 + qq) * H + j) * D + c * 8);
         const int slab = c >> 3, cc = c & 7;
         *reinterpret_cast<uint4 *>(sB + (size_t)slab * N * 128 + n * 128 + ((cc ^ (n & 7)) << 4)) =
             v;
@@ -225,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_st = a0 + st * kSlabBytes;
-                    const uint32_t b_sl = b0 + sl * (N * 128);
+                    const uint32_t b_sl = b0 + (sl % (D / 64)) * (N * 128);   // hi and lo: the same q
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_bf16(d, sw128_kmajor_desc(a_st + kk * 32),
@@ -248,8 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (4 warps)
+        // ------------------------------------------------------------ epilogue warps
+        // Warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its quarter of the tile's
+        // blocks); the kEpi / 4 warps of a quarter take its column batches in turn.
+        const int ew = warp - 2;
         const int quarter = warp & 3;
+        constexpr int kParts = kEpi / 4;
+        const int part = ew >> 2;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int ncols = nq_tile * H;
         if (HI) {
@@ -257,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the sum of squares of a row covers all its 16-byte chunks, so the swizzle does
             // not matter): no global round trip before the epilogue's first tile.  (Computed
             // from global memory in the set-up, it held every warp for 3.5 us per launch.)
-            constexpr int kCpr = KB / 8;        // 16-byte chunks per B row
+            constexpr int kCpr = D / 8;         // 16-byte chunks per B row
             constexpr int kHpp = 32 / kCpr;     // heads per warp pass
-            for (int qq = quarter; qq < nq_tile; qq += 4) {
+            for (int qq = ew; qq < nq_tile; qq += kEpi) {
                 float c = 0.f;
 #pragma unroll
                 for (int j0 = 0; j0 < H; j0 += kHpp) {
@@ -286,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int o = kCpr; o < 32; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
                 if (lane == 0) s_cq[qq] = c;
             }
-            named_barrier(1, 128);   // the four epilogue warps
+            named_barrier(1, 32 * kEpi);   // the epilogue warps
         }
         // bounded mode: this thread's block's bound factor, loaded one tile ahead so that its
         // latency overlaps the tile before
@@ -311,26 +326,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            for (int c0 = 0; c0 < ncols; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tmem_base + lane_addr + (uint32_t)(acc * N + c0), r);
-                tmem_ld_wait();
+            // 16 columns per wait on tensor memory (batches of 32 or 64 measured slower).  The
+            // queries of a batch are summed with no branch between them (a query past the tile
+            // reads the last query's weights and stores nothing), so their head sums interleave.
+            constexpr int kCB = 16;
+            constexpr int kQB = kCB / H;   // queries per batch
+            static_assert(kCB % H == 0 && H % 4 == 0, "whole queries per column batch");
+            for (int c0 = part * kCB; c0 < ncols; c0 += kParts * kCB) {
+                uint32_t r[kCB / 16][16];
 #pragma unroll
-                for (int g = 0; g < 16 / H; ++g) {
-                    const int qq = (c0 / H) + g;
-                    if (qq >= nq_tile) break;
+                for (int u = 0; u < kCB / 16; ++u)
+                    if (c0 + 16 * u < ncols)
+                        tmem_ld16(tmem_base + lane_addr + (uint32_t)(acc * N + c0 + 16 * u), r[u]);
+                tmem_ld_wait();
+                float sq[kQB];
+#pragma unroll
+                for (int g = 0; g < kQB; ++g) {
+                    const int qq = min(c0 / H + g, nq_tile - 1);
+                    const float4 *w4 = reinterpret_cast<const float4 *>(s_w + qq * H);
                     float s = 0.f;
 #pragma unroll
-                    for (int j = 0; j < H; ++j)
-                        s = fmaf(s_w[qq * H + j], fmaxf(__uint_as_float(r[g * H + j]), 0.f), s);
-                    if (b < s_nblk[qq]) {
+                    for (int j4 = 0; j4 < H / 4; ++j4) {
+                        const float4 v = w4[j4];
+                        const float wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int col = g * H + 4 * j4 + k;
+                            s = fmaf(wv[k], fmaxf(__uint_as_float(r[col / 16][col % 16]), 0.f), s);
+                        }
+                    }
+                    sq[g] = s;
+                }
+#pragma unroll
+                for (int g = 0; g < kQB; ++g) {
+                    const int qq = c0 / H + g;
+                    if (qq < nq_tile && b < s_nblk[qq]) {
                         const int64_t o = (int64_t)(q0 + qq) * p.score_stride + b;
                         if (HI) {
                             const float e = fmaf(kMargin * s_cq[qq], rb, kAbs);
-                            p.scores[o] = s - e;   // the hi + lo score lies in [s - e, s + e]
-                            p.bounds[o] = s + e;
+                            p.scores[o] = sq[g] - e;   // the hi + lo score lies in [s - e, s + e]
+                            p.bounds[o] = sq[g] + e;
                         } else {
-                            p.scores[o] = s;
+                            p.scores[o] = sq[g];
                         }
                     }
                 }
@@ -357,24 +394,27 @@ int pow2_at_least(int v) {
     return r;
 }
 
-template <int KP, int H, bool HI>
-int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
-           cudaStream_t stream) {
-    const size_t b_bytes = (size_t)p.N * (HI ? KP / 2 : KP) * 2;
+template <int KP, int H, bool HI, bool WIDE>
+int launch_shape(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
+                 cudaStream_t stream) {
+    const size_t b_bytes = (size_t)p.N * (KP / 2) * 2;   // each query row once
     // Narrow B tiles (decode) are HBM-bound streams: four CTAs per SM, three stages each,
     // overlap four producer -> MMA -> epilogue chains (measured 6% faster than two CTAs of six
     // stages, 10% faster than one of thirteen); wide ones (prefill) are tensor-bound: one CTA
     // per SM with a deep pipeline.
-    const int per_sm = p.N <= 32 ? 4 : 1;
+    const int per_sm = WIDE ? 1 : 4;
     const size_t budget = per_sm == 4 ? 55 * 1024 : 220 * 1024;
     const size_t misc = 1024 + 8 * (2 * 16 + 5) + 8 + 256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
     if (budget < b_bytes + misc + kSlabBytes) return SFA_ERR_UNSUPPORTED;
     int stages = (int)((budget - b_bytes - misc) / kSlabBytes);
     if (stages > 16) stages = 16;
+    // Wide tiles: five stages (a tile and a slab) measured faster than nine (297 against
+    // 318 us on pp2048's scores); three starve the tensor cores.
+    if (WIDE && stages > 5) stages = 5;
     p.stages = stages;
     const size_t smem = 1024 + (size_t)stages * kSlabBytes + b_bytes + 8 * (2 * stages + 5) + 8 +
                         256 * 4 + (size_t)p.q_tile * (H + 1) * 4;
-    if (!ensure_max_dynamic_smem(index_score_kernel<KP, H, HI>)) return SFA_ERR_CUDA;
+    if (!ensure_max_dynamic_smem(index_score_kernel<KP, H, HI, WIDE>)) return SFA_ERR_CUDA;
     // One wave: the block tiles of each query tile are split over as many CTAs as the
     // resident slots allow.
     const int slots = per_sm * device_sm_count();
@@ -383,12 +423,18 @@ int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
     if (cta_per_qtile < 1) cta_per_qtile = 1;
     p.tiles_per_cta = (n_blk_tiles + cta_per_qtile - 1) / cta_per_qtile;
     const int grid_x = (n_blk_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
-    if (launch_pdl(index_score_kernel<KP, H, HI>, dim3(grid_x, n_qtiles), dim3(kThreads), smem,
-                   stream, map, p) != cudaSuccess) {
+    if (launch_pdl(index_score_kernel<KP, H, HI, WIDE>, dim3(grid_x, n_qtiles),
+                   dim3(Warps<WIDE>::kThreads), smem, stream, map, p) != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
     }
     return SFA_OK;
+}
+template <int KP, int H, bool HI>
+int launch(const CUtensorMap &map, ScoreParams p, int n_qtiles, int n_blk_tiles,
+           cudaStream_t stream) {
+    return p.N <= 32 ? launch_shape<KP, H, HI, false>(map, p, n_qtiles, n_blk_tiles, stream)
+                     : launch_shape<KP, H, HI, true>(map, p, n_qtiles, n_blk_tiles, stream);
 }
 
 }  // namespace
@@ -420,7 +466,7 @@ int run_scores(const void *q_idx, const float *w, const int32_t *q_seq, const in
     if (!enc) return SFA_ERR_CUDA;
 
     // Queries per tile: the largest power of two that divides q_group and fits N <= 256 (the
-    // B tile then takes 128 KB of the 220 KB budget at K' = 256, leaving five pooled-key
+    // B tile then takes 64 KB of the 220 KB budget at d_idx = 128, leaving nine pooled-key
     // stages; pp2048's scores ran 453 us with N capped at 128 there, 429 us at 256).
     const int n_cap = 256;
     int q_tile = 1;

@@ -63,14 +63,21 @@ def _oracle_scores(Xn, qi, w, q_seq, q_pos, cr):
 
 
 @pytest.mark.parametrize("d_idx,h_idx", [(64, 4), (128, 8), (64, 16), (128, 4)])
-@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("mode", ["decode", "prefill", "prefill_wide"])
 def test_scores_match_oracle(dev, d_idx, h_idx, mode):
+    """decode: one query per tile; prefill: 70 queries in tiles of 2 (narrow B tiles);
+    prefill_wide: 96 queries in tiles of 16 or 32 (B tiles of 128 or 256 columns, the
+    prefill workloads' shape), causal over a ragged last block tile."""
     g = torch.Generator().manual_seed(d_idx + h_idx)
     cr = 4
     if mode == "decode":
         n_seq, n_tok, n_q, q_group = 5, 1500, 5, 1
         q_seq = torch.arange(5, dtype=torch.int32)
         q_pos = torch.tensor([1499, 700, 3, 1023, 511], dtype=torch.int32)
+    elif mode == "prefill_wide":
+        n_seq, n_tok, n_q, q_group = 1, 2100, 96, 96
+        q_seq = torch.zeros(n_q, dtype=torch.int32)
+        q_pos = torch.arange(2100 - n_q, 2100, dtype=torch.int32)
     else:
         n_seq, n_tok, n_q, q_group = 1, 2100, 70, 70
         q_seq = torch.zeros(n_q, dtype=torch.int32)
