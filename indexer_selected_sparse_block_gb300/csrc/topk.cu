@@ -134,9 +134,12 @@ __device__ __forceinline__ void clear_hist(Smem &sh, int nbins) {
 }
 
 // Words [0, n) of src into dst (shared memory, 16-byte aligned), n <= R * kThreads: coalesced
-// 16-byte loads over the aligned body, single words at its two ends.
+// 16-byte loads over the aligned body, single words at its two ends.  Each word is loaded by
+// exactly one thread; *mxf is the largest (NaN-skipping) of the scores this thread loaded and
+// *n_mine their count, so that the per-thread maxima are maxima of disjoint groups.
 template <int R>
-__device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t *dst) {
+__device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t *dst,
+                                            float *mxf, int *n_mine) {
     const int tid = threadIdx.x;
     int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u)) & 15u) >> 2);
     head = head < n ? head : n;
@@ -149,8 +152,30 @@ __device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t
         const int q = tid + m * kThreads;
         x[m] = q < nvec ? __ldg(v + q) : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (tid < head) dst[tid] = __ldg(src + tid);
-    if (tid < n - tail0) dst[tail0 + tid] = __ldg(src + tail0 + tid);
+    float mx = __uint_as_float(0x7FFFFFFFu);   // NaN: fmaxf returns the other operand
+    int cnt = 0;
+    if (tid < head) {
+        const uint32_t w = __ldg(src + tid);
+        dst[tid] = w;
+        mx = fmaxf(mx, __uint_as_float(w));
+        ++cnt;
+    }
+    if (tid < n - tail0) {
+        const uint32_t w = __ldg(src + tail0 + tid);
+        dst[tail0 + tid] = w;
+        mx = fmaxf(mx, __uint_as_float(w));
+        ++cnt;
+    }
+#pragma unroll
+    for (int m = 0; m < R / 4; ++m) {
+        if (tid + m * kThreads < nvec) {
+            mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(x[m].x), __uint_as_float(x[m].y)),
+                                 fmaxf(__uint_as_float(x[m].z), __uint_as_float(x[m].w))));
+            cnt += 4;
+        }
+    }
+    *mxf = mx;
+    *n_mine = cnt;
     if (head == 0) {
 #pragma unroll
         for (int m = 0; m < R / 4; ++m) {
@@ -179,6 +204,17 @@ constexpr uint32_t kNegInfKey = 0x007FFFFFu;
 // it and fmaxf skips it).
 template <int R>
 __device__ __forceinline__ void load_vals(const uint32_t *stg, int e0, int nv, float (&v)[R]) {
+    if (nv >= R) {   // every thread but the last few: no bounds to apply
+#pragma unroll
+        for (int m = 0; m < R / 4; ++m) {
+            const uint4 w = reinterpret_cast<const uint4 *>(stg + e0)[m];
+            v[4 * m] = __uint_as_float(w.x);
+            v[4 * m + 1] = __uint_as_float(w.y);
+            v[4 * m + 2] = __uint_as_float(w.z);
+            v[4 * m + 3] = __uint_as_float(w.w);
+        }
+        return;
+    }
     const float past = __uint_as_float(0x7FFFFFFFu);
 #pragma unroll
     for (int m = 0; m < R / 4; ++m) {
@@ -261,26 +297,23 @@ __device__ Cut cut_candidates(Smem &sh, int nc, int k, uint32_t lo, uint32_t kma
 }
 
 // The cut over the block's n staged scores (this thread's nv from element e0; 1 <= k < n),
-// from the compacted candidates.  sh.hist is zero on entry and on return.
+// from the compacted candidates.  mxf / n_mine: the maximum and the count of the scores this
+// thread staged (groups that partition the piece); at least `groups` threads hold some.
+// sh.hist is zero on entry and on return.
 template <int R>
-__device__ Cut select_cut(const uint32_t *stg, int e0, int nv, int n, int k, Smem &sh) {
-    uint32_t mx;
-    {
-        float v[R];
-        load_vals<R>(stg, e0, nv, v);
-        float mxf = v[0];
-#pragma unroll
-        for (int j = 1; j < R; ++j) mxf = fmaxf(mxf, v[j]);
-        mx = nv > 0 ? order_key(mxf) : 0u;   // all-NaN: 0, like their keys
-    }
+__device__ Cut select_cut(const uint32_t *stg, int e0, int nv, int n, int k, float mxf,
+                          int n_mine, int groups, Smem &sh) {
+    const bool has = n_mine > 0;
+    const uint32_t mx = has ? order_key(mxf) : 0u;   // all-NaN: 0, like their keys
     uint32_t kmax, mxmin, unused;
-    block_extrema(mx, nv > 0 ? mx : 0xFFFFFFFFu, 0xFFFFFFFFu, sh, kmax, mxmin, unused);
-    // ---- a lower bound of T: the floor of the bin of the k-th largest per-thread maximum (the
-    // maxima are a subset of the keys, so their k-th largest is <= T), bins sized to their range
+    block_extrema(mx, has ? mx : 0xFFFFFFFFu, 0xFFFFFFFFu, sh, kmax, mxmin, unused);
+    // ---- a lower bound of T: the floor of the bin of the k-th largest group maximum (the
+    // maxima are keys of distinct elements, so their k-th largest is <= T), bins sized to their
+    // range
     uint32_t lo = 0;
-    if (k <= (n + R - 1) / R) {   // at least k threads hold elements, so k maxima exist
+    if (k <= groups) {   // at least k groups hold elements, so k maxima exist
         const int s = bin_shift(kmax - mxmin);
-        if (nv > 0) atomicAdd(&sh.hist[(mx - mxmin) >> s], 1);
+        if (has) atomicAdd(&sh.hist[(mx - mxmin) >> s], 1);
         __syncthreads();
         find_cut(sh, kBins, k);
         lo = mxmin + ((uint32_t)sh.cut_bin << s);
@@ -472,11 +505,16 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
             continue;
         }
         // ---- this thread's R consecutive elements, as keys (0 past the piece: never kept)
-        stage_piece<R>(src, n, stg);
+        float mxf;
+        int n_mine;
+        stage_piece<R>(src, n, stg, &mxf, &n_mine);
         __syncthreads();
         const int e0 = tid * R;
         const int nv = n - e0 < 0 ? 0 : (n - e0 < R ? n - e0 : R);
-        const Cut cut = select_cut<R>(stg, e0, nv, n, k, sh);
+        // threads holding at least one 16-byte vector of the piece (stage_piece's split)
+        const int head = min((int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u)) & 15u) >> 2), n);
+        const int groups = min(kThreads, (n - head) >> 2);
+        const Cut cut = select_cut<R>(stg, e0, nv, n, k, mxf, n_mine, groups, sh);
         if (cut.nc >= 0) {
             // ---- ascending write-out from the candidate list
             if (p.final_stage) {
