@@ -212,6 +212,11 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// Starts a copy of [src, src + bytes) from global memory into L2 (src 16-byte aligned, bytes a
+// multiple of 16); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

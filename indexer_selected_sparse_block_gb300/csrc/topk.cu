@@ -476,6 +476,17 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
     const int n_items = n_q * n_chunks;
     clear_hist(sh, kBins);   // kept zero between items from here on
     pdl_wait();              // global memory from here on
+    // The piece of item `it`: its first word and its length (no status is raised here).
+    auto piece_of = [&](int it, const uint32_t *&src, int &n) {
+        const int i = it / n_chunks, c = it % n_chunks;
+        int64_t len = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max, nullptr);
+        for (int l = 0; l < p.level; ++l) len = next_len(len, k);   // this row at this level
+        const int64_t b0 = (int64_t)c * kChunk;
+        n = (int)(p.final_stage ? len : (len - b0 < kChunk ? len - b0 : kChunk));
+        src = (p.level == 0
+                   ? reinterpret_cast<const uint32_t *>(p.scores + (int64_t)i * p.score_stride)
+                   : p.in_bits + (int64_t)i * p.in_stride) + b0;   // score bits either way
+    };
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int i = item / n_chunks, c = item % n_chunks;
         int64_t len = visible_blocks(p.q_pos, i, p.cr, p.n_blk_max,
@@ -488,6 +499,23 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
                                   : p.in_bits + (int64_t)i * p.in_stride;   // score bits either way
         const int32_t *in_id = p.level ? p.in_id + (int64_t)i * p.in_stride : nullptr;
         src += b0;
+        // The CTA's next piece starts towards L2 now, so that its staging reads L2 rather than
+        // DRAM (pp2048's top-k: 158 -> 149 us): the piece's 16-byte-aligned interior, 16 KB per
+        // bulk prefetch, issued by warp 0.
+        if (tid < 32 && item + (int)gridDim.x < n_items) {
+            const uint32_t *nsrc;
+            int nn;
+            piece_of(item + (int)gridDim.x, nsrc, nn);
+            if (nn > k) {
+                const uintptr_t a0 = (reinterpret_cast<uintptr_t>(nsrc) + 15u) & ~uintptr_t(15);
+                const uintptr_t a1 = reinterpret_cast<uintptr_t>(nsrc + nn) & ~uintptr_t(15);
+                constexpr uintptr_t kPiece = 16384;
+                for (uintptr_t a = a0 + (uintptr_t)tid * kPiece; a < a1; a += 32 * kPiece) {
+                    const uintptr_t e = a + kPiece < a1 ? a + kPiece : a1;
+                    prefetch_l2_bulk(reinterpret_cast<const void *>(a), (uint32_t)(e - a));
+                }
+            }
+        }
         if (n <= k) {
             if (p.final_stage) {   // every element fits the budget: all of them, in order
                 int32_t *out = p.blk_idx + (int64_t)i * k;
