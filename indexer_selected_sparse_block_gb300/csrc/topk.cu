@@ -8,11 +8,13 @@
 // llama.cpp PR #27970 "CUDA + ggml: add sparse-fa for DSV4/GLM" are padded the same way).
 //
 // Exact and deterministic without sorting.  A 1024-thread CTA takes a piece of at most 36864
-// elements: coalesced 16-byte loads stage it in shared memory, and each thread then holds R
-// consecutive elements in registers as order-preserving 32-bit keys.  The k-th largest of the
-// 1024 per-thread maxima is at most the k-th largest key T (the maxima are a subset), so the
-// floor of its histogram bin bounds T from below; the bins are 12-bit windows sized to the
-// range the maxima span, so the bound is tight.  Only the keys at or above it (k and a few
+// elements: coalesced 16-byte loads stage it in shared memory (each element loaded by exactly
+// one thread, which keeps the maximum of what it loaded), and each thread then reads R
+// consecutive elements back as order-preserving 32-bit keys.  The k-th largest of the 1024
+// per-thread maxima is at most the k-th largest key T (the maxima are keys of distinct
+// elements), so the floor of its histogram bin bounds T from below; the bins are 12-bit
+// windows sized to the range the maxima span, so the bound is tight.  While a piece is
+// selected, the CTA's next piece is prefetched into L2.  Only the keys at or above it (k and a few
 // per cent more on score rows) are compacted, in index order, into shared memory, where a
 // radix select whose 12-bit digit windows are again sized to the candidates' range finds T
 // (one pass for most rows, at most three).  A single block scan over the candidate list, of
