@@ -34,6 +34,11 @@ import torch
 from . import _binding as B
 
 
+# Pooled-key bytes per step of the exact scores (n_q * n_blk_max * 4 * d_idx) from which a
+# decode-like step takes the bounded selection by default.
+BOUNDED_MIN_BYTES = 96 << 20
+
+
 class SfaStep:
     def __init__(self, *, n_seq: int, n_tok_cap: int, n_q: int, h_q: int, h_kv: int, dkq: int,
                  dv: int, h_idx: int, d_idx: int, compress_ratio: int, indexer_top_k: int,
@@ -60,12 +65,18 @@ class SfaStep:
                 raise ValueError("cell_of must be an int32 [n_seq][n_tok_cap] tensor")
             if self.key_transform:
                 raise ValueError("the paged pool takes raw pooled keys (no key transform)")
-        # The bounded selection (hi-only scores + exact rescoring of the blocks the bounds
-        # cannot rule out) halves the pooled-key bytes of decode-like steps, where each query
+        # The bounded selection (cheap bound pass + exact rescoring of the blocks the bounds
+        # cannot rule out) cuts the pooled-key bytes of decode-like steps, where each query
         # streams its sequence's pooled keys; prefill tiles share those reads and take the
-        # exact scores directly.  Rows of at most 131072 blocks.
+        # exact scores directly.  Rows of at most 131072 blocks.  Its selection is a latency
+        # chain of ~20 us, which pays only once the exact pass would stream enough bytes:
+        # measured on GB300, the exact pair was faster up to 67 MB of pooled keys per step
+        # (16 queries x 8192 blocks: 48.1 against 50.2 us; one query x 1024 blocks: 31.5
+        # against 35.9 us) and slower from 268 MB (4 x 131072 blocks: 91 against 60.5 us).
         if bounded is None:
-            bounded = q_group <= 4 and n_blk_max <= B.SFA_REFINE_MAX_BLOCKS
+            exact_bytes = n_q * n_blk_max * 4 * d_idx
+            bounded = (q_group <= 4 and n_blk_max <= B.SFA_REFINE_MAX_BLOCKS
+                       and exact_bytes >= BOUNDED_MIN_BYTES)
         self.bounded = bool(bounded) and not self.dense
         if self.bounded and n_blk_max > B.SFA_REFINE_MAX_BLOCKS:
             raise ValueError(f"bounded selection takes rows of at most "

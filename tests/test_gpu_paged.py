@@ -266,7 +266,7 @@ def test_bad_cells_are_flagged_and_left_out(dev):
 
 
 # ------------------------------------------------------------------------------ whole step
-STEPS = [("decode_1x4096", None, {}),                                   # bounded selection
+STEPS = [("decode_1x4096", True, {}),                                   # bounded selection
          ("decode_32x131072", False, {"n_seq": 4, "depth": 20000}),    # exact, 4 sequences
          ("prefill_512x1000", None, {}),                                # below budget: dense
          ("decode_4x1048576", None, {"n_seq": 2, "depth": 70000})]      # separate V, cr 8

@@ -123,10 +123,13 @@ def _check_queries(w, case, step, queries=None, tol=TOL_BF16, window=0):
     return sum(1 for r in results if r[2])
 
 
-@pytest.mark.parametrize("bounded", [None, False])
+@pytest.mark.parametrize("bounded", [None, True, False])
 def test_decode_1x4096_all(dev, bounded):
+    """Six decode queries at depth 4096: the default (the exact pair at this size) and both
+    selections forced."""
     w = sfa.WORKLOADS["decode_1x4096"].with_(n_seq=6)
     case, step = _run(w, dev, bounded=bounded)
+    assert step.bounded == bool(bounded)
     _check_queries(w, case, step)
 
 
