@@ -692,10 +692,10 @@ __device__ void select_global_list(const uint32_t *bits, const int32_t *ids, int
 //      k_r-th largest group maximum, with quotas k_r proportional to the shares' groups and
 //      summing to at least k; L = min_r X_r is a lower bound of the k-th largest score;
 //   2. the candidates up_b >= L of the share, in ascending order; every block of the exact
-//      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k); their pooled
-//      rows are prefetched into L2 while the list is ordered;
-//   3. their exact scores from the hi + lo pooled keys (mma.sync, fp32 sums), written as
-//      keys with the block ids into the leader's candidate list at the share's offset;
+//      top k is one (s_b >= s_(k) >= L), and so is every block tied with s_(k);
+//   3. their exact scores from the hi + lo pooled keys (mma.sync, fp32 sums), by the share's
+//      own CTA, written as keys with the block ids into the leader's candidate list at the
+//      share's offset;
 //   4. the leader selects the top k of the list.
 // Lists longer than 4096 go through global memory (select_global_list).
 // A row's cluster: 4 CTAs for rows of up to one selection piece (36864 blocks), each taking
@@ -1034,44 +1034,34 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                 }
         }
         __syncthreads();
-        // ---- 3. exact scores of the candidates, split evenly over the cluster's CTAs (global
-        // index q in [0, total), ordered by share; CTA r takes [total r / CL, total (r + 1) / CL)
-        // and reads the ids of other shares from their CTAs' shared memory): a warp takes 8 at a
-        // time, every piece of their rows in flight at once
+        // ---- 3. exact scores of this share's candidates: a warp takes 8 at a time, every
+        // piece of their rows in flight at once.  (Spreading all shares' candidates evenly
+        // over the CTAs needs each share's list visible to the others first: one more cluster
+        // barrier, which cost more than the balance gained -- decode_32x131072's selection
+        // 26.9 -> 28.6 us, the 1M-token decode's 24.5 -> 26.5.)
         {
             constexpr int kTR = 8;
-            const int q0 = (int)((int64_t)total * rank / kCl);
-            const int q1 = (int)((int64_t)total * (rank + 1) / kCl);
-            const int nmine = q1 - q0;
-            int offs[kCl + 1];
-            offs[0] = 0;
-#pragma unroll
-            for (int r = 0; r < kCl; ++r) offs[r + 1] = offs[r] + lead.cnt[r];
+            const int32_t *lid = in_smem ? sh.cand_idx : gid + off;
             const __nv_bfloat16 *kseq = p.kbar + (int64_t)seq * p.kbar_seq_stride;
             const int g = lane >> 2;
-            for (int c0 = warp * kTR; c0 < nmine; c0 += kWarps * kTR) {
-                const bool live = c0 + g < nmine;
-                const int qa = q0 + c0 + (live ? g : 0);   // global index of this lane group's row
-                int ba;
-                if (in_smem) {
-                    int o = 0;   // the share holding qa
-#pragma unroll
-                    for (int r = 1; r < kCl; ++r) o += qa >= offs[r] ? 1 : 0;
-                    ba = cluster.map_shared_rank(sh.cand_idx, o)[qa - offs[o]];
-                } else {
-                    ba = gid[qa];
+            for (int c0 = warp * kTR; c0 < mine; c0 += kWarps * kTR) {
+                const int ra = c0 + g;
+                int ba = lid[ra < mine ? ra : c0];
+                if ((unsigned)ba >= (unsigned)B) {   // never a candidate: flagged, row 0 read
+                    if ((lane & 3) == 0) set_status(p.status, SFA_DEV_BAD_BLOCK);
+                    ba = 0;
                 }
                 float sa, unused;
                 const __nv_bfloat16 *ka = kseq + (int64_t)ba * 2 * D;
                 rescore_tile<D, kTR>(ka, ka, bs, H, sa, unused);
-                if ((lane & 3) == 0 && live) {
+                if ((lane & 3) == 0 && ra < mine) {
                     if (in_smem) {
-                        // rank 0's own list shares the leader's array with the result: the id
-                        // written at a position of it is the one already there
-                        lead.sh.cand_key[qa] = order_key(sa);
-                        lead.sh.cand_idx[qa] = ba;
+                        // the leader's own list is this array's head: the id written at a
+                        // position of it is the one already there
+                        lead.sh.cand_key[off + ra] = order_key(sa);
+                        lead.sh.cand_idx[off + ra] = ba;
                     } else {
-                        gbits[qa] = __float_as_uint(sa);
+                        gbits[off + ra] = __float_as_uint(sa);
                     }
                 }
             }
