@@ -16,7 +16,7 @@
 //   warp 0      TMA producer: one pipeline stage = one 128-row x 128-byte slab of Kbar
 //               (16 KB, 128-byte swizzle); a tile is 2 (d_idx 64) or 4 (d_idx 128) slabs
 //   warp 1      tensor-memory owner and single-thread MMA issuer (M = 128, N = q_tile*H pad 16)
-//   warps 2..5  epilogue (2..9 for wide tiles): tcgen05.ld (lane = block), ReLU . w, head
+//   warps 2..5  epilogue (2..13 for wide tiles): tcgen05.ld (lane = block), ReLU . w, head
 //               sum, coalesced stores
 // Two accumulator buffers in tensor memory let the epilogue of tile t overlap the MMAs of
 // tile t + 1; for narrow tiles the producer fills the pipeline before the rest of the set-up.
@@ -73,8 +73,8 @@ struct Layout {
 // bounded mode): K' = d_idx over hi only against q; the score from hi, less and plus its error
 // bound (from the norm of the hi row), gives the lower and upper bounds of the exact score
 // (see sfa_index_scores_bounded).  WIDE: tiles of more than 32 columns (prefill), one CTA per
-// SM, whose epilogue reads 64 accumulator columns per wait; narrow tiles (decode) run four
-// CTAs per SM and read 16 at a time.
+// SM with twelve epilogue warps and a five-stage ring; narrow tiles (decode) run four CTAs
+// per SM with four epilogue warps each.
 template <int KP, int H, bool HI, bool WIDE>
 __global__ void __launch_bounds__(Warps<WIDE>::kThreads, WIDE ? 1 : 4)
     index_score_kernel(const __grid_constant__ CUtensorMap kbar_map, const ScoreParams p) {
