@@ -280,13 +280,17 @@ def sfa_topk_workspace_bytes(n_q: int, n_blk_max: int, top_k: int) -> int:
 
 def sfa_topk_blocks(scores, q_pos, compress_ratio: int, top_k: int, n_blk_max: int, blk_idx,
                     n_sel, workspace=None, dev_status=None, stream=None):
-    """The top_k best blocks of each query (ascending, -1 padded) and their count."""
+    """The top_k best blocks of each query (ascending, -1 padded) and their count.  scores may
+    be a view whose rows are apart (score_stride = scores.stride(0)); each row contiguous."""
+    if scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be [n_q][>= n_blk_max] with contiguous rows")
     n_q = q_pos.shape[0]
     need = sfa_topk_workspace_bytes(n_q, n_blk_max, top_k)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_pos.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().sfa_topk_blocks(_p(scores), scores.stride(0), _p(q_pos), n_q, compress_ratio,
+    rc = lib().sfa_topk_blocks(_p(scores, strided=True), scores.stride(0), _p(q_pos), n_q,
+                               compress_ratio,
                                top_k, n_blk_max, _p(blk_idx), _p(n_sel), _p(workspace),
                                ws_bytes, _p(dev_status), _stream(stream))
     _check("sfa_topk_blocks", rc)

@@ -221,7 +221,6 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     constexpr int SP_PITCH = TT + 8;              // fp32 S-partial row pitch
     constexpr int P_PITCH = TT + 8;               // 16-bit P row pitch
     constexpr int TPR = kThreads / TT;            // copying threads per tile row
-    constexpr int SPT = TT / 8;                   // softmax columns per thread
     static_assert(TT == 16 || TT == 32, "tile sizes");
     constexpr int QKROW = q8_row_bytes(DKQ), QVROW = q8_row_bytes(DV);   // q8_0 rows (Q8)
     constexpr int STAGE_BYTES = Q8 ? TT * QKROW + (V_IS_K ? 0 : TT * QVROW)
@@ -250,9 +249,19 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     pdl_wait();   // global memory from here on
     const ListInfo L = list_info(p, i, lead && tid == 0);
     const int j0 = split * p.split_tokens;
-    const int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
+    int j1 = L.ok ? min(L.len, j0 + p.split_tokens) : 0;
+    // p.tail_fold: the splits cover the kept tokens only, and the last split also attends the
+    // tail (positions n_blk_tok .. len - 1, at most 15 tokens) as a 16-token tile loaded into
+    // the Q buffer at its start, so that no split spends a whole tile on a few tail tokens
+    int tail_n = 0;
+    if constexpr (!Q8 && V_IS_K && TT == 32) {
+        if (p.tail_fold && L.ok) {
+            j1 = max(j0, min(L.n_blk_tok, j0 + p.split_tokens));
+            if (split == p.n_split - 1) tail_n = min(L.len - L.n_blk_tok, 16);
+        }
+    }
 
-    if (j0 >= j1) {  // nothing to attend in this split
+    if (j0 >= j1 && tail_n == 0) {  // nothing to attend in this split
         if (p.cluster_merge) {   // it still takes its part in the cluster's merge
             if (tid < 16) {
                 sL[tid] = 0.f;
@@ -389,42 +398,39 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             ldsm_x4(q_base + r * KROW + swz(c, r) * 16, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
         }
     }
+    // the folded tail's rows into the Q buffer (free once every warp holds its fragments), laid
+    // out like a tile's rows, as the youngest copy group; rows past the tail are zero
+    if constexpr (!Q8 && V_IS_K && TT == 32) {
+        if (tail_n > 0) {
+            __syncthreads();
+            const uint32_t qs = smem_u32(sQ);
+            for (int e = tid; e < 16 * KCH; e += kThreads) {
+                const int r = e / KCH, c = e % KCH;
+                const int64_t row = r < tail_n ? kv_row(p, L.seq, L.tail0 + r) : -1;
+                const KElem *src = row >= 0 ? Kseq + row * p.k_tok_stride + c * 8 : Kseq;
+                cp_async16(qs + r * KROW + swz(c, r) * 16, src, row >= 0 ? 16u : 0u);
+            }
+            cp_async_commit();
+        }
+    }
 
     float o[NTV][4];
 #pragma unroll
     for (int n = 0; n < NTV; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;   // of row (tid >> 3), kept by its 8 threads
 
-    for (int t = 0; t < n_tiles; ++t) {
-        // tile t has landed once at most stages-2 younger groups are pending
-        cp_async_wait_n(p.stages - 2);
-        __syncthreads();
-        if (t + p.stages - 1 < n_tiles) issue_tile(t + p.stages - 1);
-        cp_async_commit();
-
-        const int st = t % p.stages;
-        if constexpr (Q8) {
-            // tile t from its q8_0 rows into the binary16 tile: each warp converts the K
-            // columns of its own head-dim slice (all it reads for S) and, with a separate V,
-            // the V columns of its value-dim slice; the block barrier after the S partials
-            // publishes the whole tile before any warp reads V columns of another's slice
-            const uint8_t *stg = sStage + (size_t)st * STAGE_BYTES;
-            bool ok = dequant_tile<DKQ, QKROW, TT, DKQ / 32>(stg, sDeq, warp * (DKQ / 32), lane, 32);
-            if constexpr (!V_IS_K)
-                ok &= dequant_tile<DV, QVROW, TT, DV / 32>(stg + TT * QKROW, sDeq + TT * KROW,
-                                                            warp * (DV / 32), lane, 32);
-            if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
-            __syncwarp();
-        }
-        const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
-        const uint32_t vbase = V_IS_K ? kbase : kbase + TT * KROW;
-
+    // One tile of NT tokens (NT = TT, or 16 for the folded tail) from K rows at kbase and V rows
+    // at vbase: S over this warp's head-dim slice, the online softmax, and O += P V over its
+    // value-dim slice.  tokv[c] < 0 leaves column c out of the softmax.
+    auto tile_step = [&](auto nt, const uint32_t kbase, const uint32_t vbase, const int *tokv) {
+        constexpr int NT = decltype(nt)::value;
+        constexpr int NSPT = NT / 8;   // softmax columns per thread
         // ---- S partial over this warp's head-dim slice
-        float acc[TT / 8][4];
+        float acc[NT / 8][4];
 #pragma unroll
-        for (int n = 0; n < TT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        for (int n = 0; n < NT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
-        for (int np = 0; np < TT / 16; ++np) {
+        for (int np = 0; np < NT / 16; ++np) {
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int kg = warp * KS + ks;
@@ -439,22 +445,22 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         }
         float *sp = sSP + warp * 16 * SP_PITCH;
 #pragma unroll
-        for (int n = 0; n < TT / 8; ++n) {
+        for (int n = 0; n < NT / 8; ++n) {
             *reinterpret_cast<float2 *>(sp + gq * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][0], acc[n][1]);
             *reinterpret_cast<float2 *>(sp + (gq + 8) * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][2], acc[n][3]);
         }
         __syncthreads();
 
-        // ---- online softmax: thread -> row tid/8, columns SPT*(tid%8) .. +SPT-1
+        // ---- online softmax: thread -> row tid/8, columns NSPT*(tid%8) .. +NSPT-1
         {
-            const int row = tid >> 3, c0 = (tid & 7) * SPT;
-            float s[SPT];
+            const int row = tid >> 3, c0 = (tid & 7) * NSPT;
+            float s[NSPT];
 #pragma unroll
-            for (int e = 0; e < SPT; ++e) s[e] = 0.f;
+            for (int e = 0; e < NSPT; ++e) s[e] = 0.f;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const float *src = sSP + (w * 16 + row) * SP_PITCH + c0;
-                if constexpr (SPT == 4) {
+                if constexpr (NSPT == 4) {
                     const float4 v = *reinterpret_cast<const float4 *>(src);
                     s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
                 } else {
@@ -464,8 +470,8 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             }
             float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < SPT; ++e) {
-                s[e] = sTok[st * TT + c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
+            for (int e = 0; e < NSPT; ++e) {
+                s[e] = tokv[c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, s[e]);
             }
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -473,9 +479,9 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
             const float m_new = fmaxf(m_run, mx);
             const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-            float ph[SPT], pl[SPT], rs = 0.f;
+            float ph[NSPT], pl[NSPT], rs = 0.f;
 #pragma unroll
-            for (int e = 0; e < SPT; ++e) {
+            for (int e = 0; e < NSPT; ++e) {
                 const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
                 ph[e] = round16<Q8>(pe);
                 pl[e] = pe - ph[e];
@@ -486,7 +492,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
             l_run = l_run * alpha + rs;
             m_run = m_new;
-            if constexpr (SPT == 4) {
+            if constexpr (NSPT == 4) {
                 *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
                     make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
                 *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
@@ -508,7 +514,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
             }
             const uint32_t pbase = smem_u32(sP);
 #pragma unroll
-            for (int ks = 0; ks < TT / 16; ++ks) {
+            for (int ks = 0; ks < NT / 16; ++ks) {
                 uint32_t pa[4], pb[4];
                 {
                     const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
@@ -530,6 +536,40 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
                 }
             }
         }
+    };
+
+    for (int t = 0; t < n_tiles; ++t) {
+        // tile t has landed once at most stages-2 younger groups are pending (and the folded
+        // tail's, while it is younger than tile t)
+        cp_async_wait_n(p.stages - 2 + (tail_n > 0 && t <= p.stages - 2 ? 1 : 0));
+        __syncthreads();
+        if (t + p.stages - 1 < n_tiles) issue_tile(t + p.stages - 1);
+        cp_async_commit();
+
+        const int st = t % p.stages;
+        if constexpr (Q8) {
+            // tile t from its q8_0 rows into the binary16 tile: each warp converts the K
+            // columns of its own head-dim slice (all it reads for S) and, with a separate V,
+            // the V columns of its value-dim slice; the block barrier after the S partials
+            // publishes the whole tile before any warp reads V columns of another's slice
+            const uint8_t *stg = sStage + (size_t)st * STAGE_BYTES;
+            bool ok = dequant_tile<DKQ, QKROW, TT, DKQ / 32>(stg, sDeq, warp * (DKQ / 32), lane, 32);
+            if constexpr (!V_IS_K)
+                ok &= dequant_tile<DV, QVROW, TT, DV / 32>(stg + TT * QKROW, sDeq + TT * KROW,
+                                                            warp * (DV / 32), lane, 32);
+            if (!ok) set_status(p.status, SFA_DEV_FP16_RANGE);
+            __syncwarp();
+        }
+        const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
+        const uint32_t vbase = V_IS_K ? kbase : kbase + TT * KROW;
+
+        tile_step(std::integral_constant<int, TT>{}, kbase, vbase, sTok + st * TT);
+    }
+    if (tail_n > 0) {   // the folded tail, its rows long since in the Q buffer
+        cp_async_wait<0>();
+        if (tid < 16) sTok[tid] = tid < tail_n ? 0 : -1;
+        __syncthreads();
+        tile_step(std::integral_constant<int, 16>{}, smem_u32(sQ), smem_u32(sQ), sTok);
     }
     cp_async_wait<0>();
 
@@ -1607,8 +1647,23 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
         return SFA_ERR_INVALID_ARG;
     if (n_q == 0) return SFA_OK;
     if (n_q > 65535 || h_kv > 65535 || n_kv_max > 0x7FFFFFFF) return SFA_ERR_UNSUPPORTED;
-    const AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, V != nullptr, n_kv_max, cr, dense,
-                                           cell_of != nullptr);
+    AttendPlan ap = make_attend_plan(dtype, n_q, h_kv, dkq, V != nullptr, n_kv_max, cr, dense,
+                                     cell_of != nullptr);
+    // The tail folded into the last split: the splits are planned over the kept tokens alone
+    // (top_k cr), so that a list of 512 blocks and a 3-token tail takes eight tiles per split
+    // instead of nine.  Only where the plan stays an in-cluster merge on the warp-level bf16
+    // kernel with V = K, and the tail is a plain suffix (no window) of at most 15 tokens.
+    int tail_fold = 0;
+    if (dtype == SFA_BF16 && !dense && !V && window == 0 && part == SFA_PART_ALL && cr >= 2 &&
+        cr <= 16 && ap.cluster_ns > 1 && !ap.use_tc && !ap.use_ws && ap.tt == 32) {
+        const int64_t n_kept = (int64_t)top_k * cr < n_kv_max ? (int64_t)top_k * cr : n_kv_max;
+        const AttendPlan f = make_attend_plan(dtype, n_q, h_kv, dkq, false, n_kept, cr, dense,
+                                              cell_of != nullptr);
+        if (n_kept < n_kv_max && f.cluster_ns > 1 && !f.use_tc && !f.use_ws && f.tt == 32) {
+            ap = f;
+            tail_fold = 1;
+        }
+    }
     const bool use_tc = ap.use_tc;
     SplitPlan sp = ap.sp;
     const int cluster_ns = ap.cluster_ns;
@@ -1640,6 +1695,7 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     p.n_kv_max = n_kv_max;
     p.window = window;
     p.part = part;
+    p.tail_fold = tail_fold;
     p.scale_log2 = scale * kLog2e;
     if (sp.n_split > 1) {
         const size_t n_rows = (size_t)n_q * h_q * sp.n_split;

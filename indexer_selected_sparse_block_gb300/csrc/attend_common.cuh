@@ -33,6 +33,8 @@ struct AttnParams {
     int64_t n_kv_max;    // the caller's bound on every list's length
     int64_t window;      // > 0: the window positions p - window + 1 .. p are attended too
     int part;            // SFA_PART_*: the whole list, its kept part, or its window part
+    int tail_fold;       // 1: the splits cover the kept tokens and the last one also the tail
+                         // (the warp-level bf16 kernel, V = K, in-cluster merge, no window)
     float scale_log2;
 };
 

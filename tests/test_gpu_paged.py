@@ -123,15 +123,21 @@ SHAPES = [(576, 512, True, 16, 1), (512, 512, False, 16, 2), (128, 128, False, 8
 
 @pytest.mark.parametrize("layout", ["pages", "cells"])
 @pytest.mark.parametrize("dkq,dv,v_is_k,h_q,h_kv", SHAPES)
-@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("mode", ["decode", "decode32", "prefill"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_gather_attend_paged(dev, layout, dkq, dv, v_is_k, h_q, h_kv, mode, dtype):
-    """Decode rows (2048 kept cells, split over a cluster) and prefill rows (one CTA each)."""
+    """Decode rows (2048 kept cells and a tail: 4 queries split over many CTAs and merged by a
+    second kernel; 32 queries split over an 8-CTA cluster, the tail folded into the last split
+    where V = K) and prefill rows (one CTA each)."""
     cr = 4
     if mode == "decode":
         n_seq, n_pos, top_k = 3, 2600, 512
         q_seq = np.array([0, 1, 2, 1], np.int32)
         q_pos = np.array([2599, 2100, 900, 2], np.int32)
+    elif mode == "decode32":
+        n_seq, n_pos, top_k = 3, 2600, 512
+        q_seq = (np.arange(32) % 3).astype(np.int32)
+        q_pos = np.array([2599, 2100, 900, 2, 2598, 2597, 1, 0] * 4, np.int32)
     else:
         n_seq, n_pos, top_k = 1, 700, 40
         q_seq = np.zeros(120, np.int32)

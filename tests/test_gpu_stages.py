@@ -125,12 +125,13 @@ def test_scores_flag_query_group_violation(dev):
 
 # ------------------------------------------------------------------------------------ top-k
 @pytest.mark.parametrize("top_k", [1, 7, 256, 512, 2048])
-@pytest.mark.parametrize("pattern", ["coarse", "continuous", "dup_at_cut"])
+@pytest.mark.parametrize("pattern", ["coarse", "continuous", "dup_at_cut", "odd_stride"])
 def test_topk_bit_exact(dev, top_k, pattern):
     """Kept sets equal the oracle's full sort exactly, for rows that fit the budget, rows of
     one chunk and rows cut into chunks; coarse values (many ties: the fallback radix select),
-    continuous values (the two-digit path) and continuous values with a run of exact ties
-    across the cut (ranked by index)."""
+    continuous values (the two-digit path), continuous values with a run of exact ties
+    across the cut (ranked by index), and continuous values in rows whose starts are not
+    16-byte aligned (a row pitch of n_blk_max + 1 scores: the staging's single-word head)."""
     g = torch.Generator().manual_seed(top_k * 3 + len(pattern))
     cr = 4
     Bs = [0, 1, top_k - 1, top_k, top_k + 1, 3000, 8192, 8193, 20000, 70000]
@@ -143,7 +144,7 @@ def test_topk_bit_exact(dev, top_k, pattern):
         vals = torch.round(raw * 4) / 4          # many exact ties
         vals[vals == 0] = -0.0                   # signed zeros must tie with +0.0
         vals[1::2, ::3] = 0.0
-    elif pattern == "continuous":
+    elif pattern in ("continuous", "odd_stride"):
         vals = torch.relu(raw) * 3 + torch.rand((n_q, n_blk_max), generator=g)
     else:
         vals = torch.relu(raw) * 3 + torch.rand((n_q, n_blk_max), generator=g)
@@ -153,7 +154,12 @@ def test_topk_bit_exact(dev, top_k, pattern):
                 cut = torch.sort(row, descending=True).values[top_k - 1].item()
                 idx = torch.randperm(b, generator=g)[:40]
                 row[idx] = cut                   # 40 exact copies of the cut value
-    scores = vals.to(dev)
+    if pattern == "odd_stride":
+        wide = torch.full((n_q, n_blk_max + 1), float("nan"), device=dev)
+        wide[:, :n_blk_max] = vals.to(dev)
+        scores = wide[:, :n_blk_max]
+    else:
+        scores = vals.to(dev)
     blk = torch.full((n_q, top_k), -9, dtype=torch.int32, device=dev)
     n_sel = torch.full((n_q,), -9, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
