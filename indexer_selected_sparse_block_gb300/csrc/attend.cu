@@ -16,7 +16,10 @@
 //   * O += P_hi V + P_lo V on tensor cores, the 512 value dims split over the 4 warps; V = K
 //     reuses the K tile in shared memory.
 // Decode has few queries, so each list is split over several CTAs (flash-decoding); the
-// partial (O, m, l) merge inside a thread-block cluster or through combine_kernel.  fp32 inputs
+// partial (O, m, l) merge inside a thread-block cluster or through combine_kernel.  With an
+// in-cluster merge and V = K, the splits cover the kept tokens only and the last one attends
+// the few tail tokens as a 16-token tile loaded into the Q buffer at its start (AttnParams::
+// tail_fold), so that no split spends a whole 32-token tile on them.  fp32 inputs
 // take a plain SIMT kernel with the same split/merge structure (accuracy reference path).
 #include <math.h>
 #include <stdlib.h>
