@@ -214,8 +214,9 @@ __host__ __device__ constexpr size_t mma_smem_bytes(int stages, int blk_list) {
 // to binary16, with Q converted to binary16 and every tensor-core product on binary16).
 // Tiles of TT tokens (16 or 32) stream through a ring of p.stages stages: tile t + stages - 1
 // is issued while tile t is scored, so stages - 1 tiles are in flight behind the one in use.
-template <int DKQ, int DV, bool V_IS_K, bool Q8, int TT>
+template <int DKQ, int DV, bool V_IS_K, bool Q8, int TT, bool FOLD = false>
 __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
+    static_assert(!FOLD || (!Q8 && V_IS_K && TT == 32), "the folded tail: bf16, V = K, TT 32");
     constexpr int KROW = DKQ * 2;                 // bytes of a K row in shared memory
     constexpr int VROW = V_IS_K ? KROW : DV * 2;  // bytes of a V row
     constexpr int KCH = DKQ / 8, VCH = DV / 8;    // 16-byte chunks per row
@@ -224,6 +225,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     constexpr int SP_PITCH = TT + 8;              // fp32 S-partial row pitch
     constexpr int P_PITCH = TT + 8;               // 16-bit P row pitch
     constexpr int TPR = kThreads / TT;            // copying threads per tile row
+    constexpr int SPT = TT / 8;                   // softmax columns per thread
     static_assert(TT == 16 || TT == 32, "tile sizes");
     constexpr int QKROW = q8_row_bytes(DKQ), QVROW = q8_row_bytes(DV);   // q8_0 rows (Q8)
     constexpr int STAGE_BYTES = Q8 ? TT * QKROW + (V_IS_K ? 0 : TT * QVROW)
@@ -257,7 +259,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     // tail (positions n_blk_tok .. len - 1, at most 15 tokens) as a 16-token tile loaded into
     // the Q buffer at its start, so that no split spends a whole tile on a few tail tokens
     int tail_n = 0;
-    if constexpr (!Q8 && V_IS_K && TT == 32) {
+    if constexpr (FOLD) {
         if (p.tail_fold && L.ok) {
             j1 = max(j0, min(L.n_blk_tok, j0 + p.split_tokens));
             if (split == p.n_split - 1) tail_n = min(L.len - L.n_blk_tok, 16);
@@ -403,7 +405,7 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     }
     // the folded tail's rows into the Q buffer (free once every warp holds its fragments), laid
     // out like a tile's rows, as the youngest copy group; rows past the tail are zero
-    if constexpr (!Q8 && V_IS_K && TT == 32) {
+    if constexpr (FOLD) {
         if (tail_n > 0) {
             __syncthreads();
             const uint32_t qs = smem_u32(sQ);
@@ -422,129 +424,9 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
     for (int n = 0; n < NTV; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;   // of row (tid >> 3), kept by its 8 threads
 
-    // One tile of NT tokens (NT = TT, or 16 for the folded tail) from K rows at kbase and V rows
-    // at vbase: S over this warp's head-dim slice, the online softmax, and O += P V over its
-    // value-dim slice.  tokv[c] < 0 leaves column c out of the softmax.
-    auto tile_step = [&](auto nt, const uint32_t kbase, const uint32_t vbase, const int *tokv) {
-        constexpr int NT = decltype(nt)::value;
-        constexpr int NSPT = NT / 8;   // softmax columns per thread
-        // ---- S partial over this warp's head-dim slice
-        float acc[NT / 8][4];
-#pragma unroll
-        for (int n = 0; n < NT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll
-        for (int np = 0; np < NT / 16; ++np) {
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int kg = warp * KS + ks;
-                const int mi = lane >> 3, r8 = lane & 7;
-                const int n = np * 16 + (mi >> 1) * 8 + r8;
-                const int c = kg * 2 + (mi & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + n * KROW + swz(c, n) * 16, b0, b1, b2, b3);
-                mma16816<Q8>(acc[2 * np], qa[ks], b0, b1);
-                mma16816<Q8>(acc[2 * np + 1], qa[ks], b2, b3);
-            }
-        }
-        float *sp = sSP + warp * 16 * SP_PITCH;
-#pragma unroll
-        for (int n = 0; n < NT / 8; ++n) {
-            *reinterpret_cast<float2 *>(sp + gq * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(sp + (gq + 8) * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][2], acc[n][3]);
-        }
-        __syncthreads();
-
-        // ---- online softmax: thread -> row tid/8, columns NSPT*(tid%8) .. +NSPT-1
-        {
-            const int row = tid >> 3, c0 = (tid & 7) * NSPT;
-            float s[NSPT];
-#pragma unroll
-            for (int e = 0; e < NSPT; ++e) s[e] = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float *src = sSP + (w * 16 + row) * SP_PITCH + c0;
-                if constexpr (NSPT == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src);
-                    s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
-                } else {
-                    const float2 v = *reinterpret_cast<const float2 *>(src);
-                    s[0] += v.x; s[1] += v.y;
-                }
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < NSPT; ++e) {
-                s[e] = tokv[c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[e]);
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-            float ph[NSPT], pl[NSPT], rs = 0.f;
-#pragma unroll
-            for (int e = 0; e < NSPT; ++e) {
-                const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
-                ph[e] = round16<Q8>(pe);
-                pl[e] = pe - ph[e];
-                rs += pe;
-            }
-            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
-            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
-            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
-            l_run = l_run * alpha + rs;
-            m_run = m_new;
-            if constexpr (NSPT == 4) {
-                *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
-                    make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
-                *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
-                    make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
-            } else {
-                *reinterpret_cast<uint32_t *>(sP + row * P_PITCH + c0) = pack16<Q8>(ph[0], ph[1]);
-                *reinterpret_cast<uint32_t *>(sP + (16 + row) * P_PITCH + c0) = pack16<Q8>(pl[0], pl[1]);
-            }
-            if ((tid & 7) == 0) sAlpha[row] = alpha;
-        }
-        __syncthreads();
-
-        // ---- O = O * alpha + P V over this warp's value-dim slice
-        {
-            const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
-#pragma unroll
-            for (int n = 0; n < NTV; ++n) {
-                o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
-            }
-            const uint32_t pbase = smem_u32(sP);
-#pragma unroll
-            for (int ks = 0; ks < NT / 16; ++ks) {
-                uint32_t pa[4], pb[4];
-                {
-                    const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
-                    const uint32_t a = pbase + r * (P_PITCH * 2) + col * 2;
-                    ldsm_x4(a, pa[0], pa[1], pa[2], pa[3]);
-                    ldsm_x4(a + 16 * P_PITCH * 2, pb[0], pb[1], pb[2], pb[3]);
-                }
-#pragma unroll
-                for (int np = 0; np < NTV / 2; ++np) {
-                    const int mi = lane >> 3, r8 = lane & 7;
-                    const int k = ks * 16 + (mi & 1) * 8 + r8;
-                    const int c = (warp * (DV / 4)) / 8 + np * 2 + (mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vbase + k * VROW + swz(c, k) * 16, b0, b1, b2, b3);
-                    mma16816<Q8>(o[2 * np], pa, b0, b1);
-                    mma16816<Q8>(o[2 * np + 1], pa, b2, b3);
-                    mma16816<Q8>(o[2 * np], pb, b0, b1);
-                    mma16816<Q8>(o[2 * np + 1], pb, b2, b3);
-                }
-            }
-        }
-    };
-
     for (int t = 0; t < n_tiles; ++t) {
-        // tile t has landed once at most stages-2 younger groups are pending (and the folded
-        // tail's, while it is younger than tile t)
-        cp_async_wait_n(p.stages - 2 + (tail_n > 0 && t <= p.stages - 2 ? 1 : 0));
+        // tile t has landed once at most stages-2 younger groups are pending
+        cp_async_wait_n(p.stages - 2 + (FOLD && tail_n > 0 && t <= p.stages - 2 ? 1 : 0));
         __syncthreads();
         if (t + p.stages - 1 < n_tiles) issue_tile(t + p.stages - 1);
         cp_async_commit();
@@ -566,13 +448,246 @@ __device__ __forceinline__ void attend_mma_body(const AttnParams &p) {
         const uint32_t kbase = Q8 ? smem_u32(sDeq) : smem_u32(sStage + (size_t)st * STAGE_BYTES);
         const uint32_t vbase = V_IS_K ? kbase : kbase + TT * KROW;
 
-        tile_step(std::integral_constant<int, TT>{}, kbase, vbase, sTok + st * TT);
-    }
-    if (tail_n > 0) {   // the folded tail, its rows long since in the Q buffer
-        cp_async_wait<0>();
-        if (tid < 16) sTok[tid] = tid < tail_n ? 0 : -1;
+        // ---- S partial over this warp's head-dim slice
+        float acc[TT / 8][4];
+#pragma unroll
+        for (int n = 0; n < TT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+        for (int np = 0; np < TT / 16; ++np) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int kg = warp * KS + ks;
+                const int mi = lane >> 3, r8 = lane & 7;
+                const int n = np * 16 + (mi >> 1) * 8 + r8;
+                const int c = kg * 2 + (mi & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + n * KROW + swz(c, n) * 16, b0, b1, b2, b3);
+                mma16816<Q8>(acc[2 * np], qa[ks], b0, b1);
+                mma16816<Q8>(acc[2 * np + 1], qa[ks], b2, b3);
+            }
+        }
+        float *sp = sSP + warp * 16 * SP_PITCH;
+#pragma unroll
+        for (int n = 0; n < TT / 8; ++n) {
+            *reinterpret_cast<float2 *>(sp + gq * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(sp + (gq + 8) * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][2], acc[n][3]);
+        }
         __syncthreads();
-        tile_step(std::integral_constant<int, 16>{}, smem_u32(sQ), smem_u32(sQ), sTok);
+
+        // ---- online softmax: thread -> row tid/8, columns SPT*(tid%8) .. +SPT-1
+        {
+            const int row = tid >> 3, c0 = (tid & 7) * SPT;
+            float s[SPT];
+#pragma unroll
+            for (int e = 0; e < SPT; ++e) s[e] = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float *src = sSP + (w * 16 + row) * SP_PITCH + c0;
+                if constexpr (SPT == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    s[0] += v.x; s[1] += v.y;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < SPT; ++e) {
+                s[e] = sTok[st * TT + c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[e]);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+            float ph[SPT], pl[SPT], rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < SPT; ++e) {
+                const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
+                ph[e] = round16<Q8>(pe);
+                pl[e] = pe - ph[e];
+                rs += pe;
+            }
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
+            l_run = l_run * alpha + rs;
+            m_run = m_new;
+            if constexpr (SPT == 4) {
+                *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
+                    make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
+                *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
+                    make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
+            } else {
+                *reinterpret_cast<uint32_t *>(sP + row * P_PITCH + c0) = pack16<Q8>(ph[0], ph[1]);
+                *reinterpret_cast<uint32_t *>(sP + (16 + row) * P_PITCH + c0) = pack16<Q8>(pl[0], pl[1]);
+            }
+            if ((tid & 7) == 0) sAlpha[row] = alpha;
+        }
+        __syncthreads();
+
+        // ---- O = O * alpha + P V over this warp's value-dim slice
+        {
+            const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
+#pragma unroll
+            for (int n = 0; n < NTV; ++n) {
+                o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
+            }
+            const uint32_t pbase = smem_u32(sP);
+#pragma unroll
+            for (int ks = 0; ks < TT / 16; ++ks) {
+                uint32_t pa[4], pb[4];
+                {
+                    const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
+                    const uint32_t a = pbase + r * (P_PITCH * 2) + col * 2;
+                    ldsm_x4(a, pa[0], pa[1], pa[2], pa[3]);
+                    ldsm_x4(a + 16 * P_PITCH * 2, pb[0], pb[1], pb[2], pb[3]);
+                }
+#pragma unroll
+                for (int np = 0; np < NTV / 2; ++np) {
+                    const int mi = lane >> 3, r8 = lane & 7;
+                    const int k = ks * 16 + (mi & 1) * 8 + r8;
+                    const int c = (warp * (DV / 4)) / 8 + np * 2 + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vbase + k * VROW + swz(c, k) * 16, b0, b1, b2, b3);
+                    mma16816<Q8>(o[2 * np], pa, b0, b1);
+                    mma16816<Q8>(o[2 * np + 1], pa, b2, b3);
+                    mma16816<Q8>(o[2 * np], pb, b0, b1);
+                    mma16816<Q8>(o[2 * np + 1], pb, b2, b3);
+                }
+            }
+        }
+    }
+    if constexpr (FOLD) {
+        if (tail_n > 0) {   // the folded tail, its rows long since in the Q buffer
+        // The loop's tile step for NT tokens from K rows at kbase and V rows at vbase (S over
+        // this warp's head-dim slice, the online softmax, O += P V over its value-dim slice;
+        // tokv[c] < 0 leaves column c out), here for the 16-token tail tile.  The loop keeps
+        // its own copy: routing it through this lambda made the plain kernel's dense prefill
+        // 1.3% slower (decode_32x131072 unchanged).
+        auto tile_step = [&](auto nt, const uint32_t kbase, const uint32_t vbase, const int *tokv) {
+            constexpr int NT = decltype(nt)::value;
+            constexpr int NSPT = NT / 8;   // softmax columns per thread
+            // ---- S partial over this warp's head-dim slice
+            float acc[NT / 8][4];
+    #pragma unroll
+            for (int n = 0; n < NT / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    #pragma unroll
+            for (int np = 0; np < NT / 16; ++np) {
+    #pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int kg = warp * KS + ks;
+                    const int mi = lane >> 3, r8 = lane & 7;
+                    const int n = np * 16 + (mi >> 1) * 8 + r8;
+                    const int c = kg * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbase + n * KROW + swz(c, n) * 16, b0, b1, b2, b3);
+                    mma16816<Q8>(acc[2 * np], qa[ks], b0, b1);
+                    mma16816<Q8>(acc[2 * np + 1], qa[ks], b2, b3);
+                }
+            }
+            float *sp = sSP + warp * 16 * SP_PITCH;
+    #pragma unroll
+            for (int n = 0; n < NT / 8; ++n) {
+                *reinterpret_cast<float2 *>(sp + gq * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][0], acc[n][1]);
+                *reinterpret_cast<float2 *>(sp + (gq + 8) * SP_PITCH + n * 8 + 2 * tq) = make_float2(acc[n][2], acc[n][3]);
+            }
+            __syncthreads();
+
+            // ---- online softmax: thread -> row tid/8, columns NSPT*(tid%8) .. +NSPT-1
+            {
+                const int row = tid >> 3, c0 = (tid & 7) * NSPT;
+                float s[NSPT];
+    #pragma unroll
+                for (int e = 0; e < NSPT; ++e) s[e] = 0.f;
+    #pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float *src = sSP + (w * 16 + row) * SP_PITCH + c0;
+                    if constexpr (NSPT == 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(src);
+                        s[0] += v.x; s[1] += v.y; s[2] += v.z; s[3] += v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2 *>(src);
+                        s[0] += v.x; s[1] += v.y;
+                    }
+                }
+                float mx = -INFINITY;
+    #pragma unroll
+                for (int e = 0; e < NSPT; ++e) {
+                    s[e] = tokv[c0 + e] >= 0 ? s[e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[e]);
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+                const float m_new = fmaxf(m_run, mx);
+                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+                float ph[NSPT], pl[NSPT], rs = 0.f;
+    #pragma unroll
+                for (int e = 0; e < NSPT; ++e) {
+                    const float pe = m_new == -INFINITY ? 0.f : exp2f(s[e] - m_new);
+                    ph[e] = round16<Q8>(pe);
+                    pl[e] = pe - ph[e];
+                    rs += pe;
+                }
+                rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
+                rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
+                rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 4);
+                l_run = l_run * alpha + rs;
+                m_run = m_new;
+                if constexpr (NSPT == 4) {
+                    *reinterpret_cast<uint2 *>(sP + row * P_PITCH + c0) =
+                        make_uint2(pack16<Q8>(ph[0], ph[1]), pack16<Q8>(ph[2], ph[3]));
+                    *reinterpret_cast<uint2 *>(sP + (16 + row) * P_PITCH + c0) =
+                        make_uint2(pack16<Q8>(pl[0], pl[1]), pack16<Q8>(pl[2], pl[3]));
+                } else {
+                    *reinterpret_cast<uint32_t *>(sP + row * P_PITCH + c0) = pack16<Q8>(ph[0], ph[1]);
+                    *reinterpret_cast<uint32_t *>(sP + (16 + row) * P_PITCH + c0) = pack16<Q8>(pl[0], pl[1]);
+                }
+                if ((tid & 7) == 0) sAlpha[row] = alpha;
+            }
+            __syncthreads();
+
+            // ---- O = O * alpha + P V over this warp's value-dim slice
+            {
+                const float a0 = sAlpha[gq], a1 = sAlpha[gq + 8];
+    #pragma unroll
+                for (int n = 0; n < NTV; ++n) {
+                    o[n][0] *= a0; o[n][1] *= a0; o[n][2] *= a1; o[n][3] *= a1;
+                }
+                const uint32_t pbase = smem_u32(sP);
+    #pragma unroll
+                for (int ks = 0; ks < NT / 16; ++ks) {
+                    uint32_t pa[4], pb[4];
+                    {
+                        const int r = lane & 15, col = ks * 16 + (lane >> 4) * 8;
+                        const uint32_t a = pbase + r * (P_PITCH * 2) + col * 2;
+                        ldsm_x4(a, pa[0], pa[1], pa[2], pa[3]);
+                        ldsm_x4(a + 16 * P_PITCH * 2, pb[0], pb[1], pb[2], pb[3]);
+                    }
+    #pragma unroll
+                    for (int np = 0; np < NTV / 2; ++np) {
+                        const int mi = lane >> 3, r8 = lane & 7;
+                        const int k = ks * 16 + (mi & 1) * 8 + r8;
+                        const int c = (warp * (DV / 4)) / 8 + np * 2 + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vbase + k * VROW + swz(c, k) * 16, b0, b1, b2, b3);
+                        mma16816<Q8>(o[2 * np], pa, b0, b1);
+                        mma16816<Q8>(o[2 * np + 1], pa, b2, b3);
+                        mma16816<Q8>(o[2 * np], pb, b0, b1);
+                        mma16816<Q8>(o[2 * np + 1], pb, b2, b3);
+                    }
+                }
+            }
+        };
+
+            cp_async_wait<0>();
+            if (tid < 16) sTok[tid] = tid < tail_n ? 0 : -1;
+            __syncthreads();
+            tile_step(std::integral_constant<int, 16>{}, smem_u32(sQ), smem_u32(sQ), sTok);
+        }
     }
     cp_async_wait<0>();
 
@@ -634,6 +749,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_bf16_kernel(const AttnPara
 template <int DKQ, int DV, bool V_IS_K, int TT>
 __global__ void __launch_bounds__(kThreads, 1) attend_q8_kernel(const AttnParams p) {
     attend_mma_body<DKQ, DV, V_IS_K, true, TT>(p);
+}
+// The bf16 kernel with the list's tail folded into the last split (AttnParams::tail_fold):
+// its own instance, so that the other plans keep the plain kernel's code and registers.
+template <int DKQ, int DV>
+__global__ void __launch_bounds__(kThreads, 1) attend_bf16_fold_kernel(const AttnParams p) {
+    attend_mma_body<DKQ, DV, true, false, 32, true>(p);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1482,12 +1603,16 @@ int launch_mma_shape(const AttnParams &p, dim3 grid, cudaStream_t st, int blk_li
     if (ring.smem > 227 * 1024) return SFA_ERR_UNSUPPORTED;
     AttnParams q = p;
     q.stages = ring.stages;
-    if (!ensure_max_dynamic_smem(mma_kernel<DKQ, DV, VK, Q8, TT>())) return SFA_ERR_CUDA;
+    auto kernel = mma_kernel<DKQ, DV, VK, Q8, TT>();
+    if constexpr (!Q8 && VK && TT == 32) {
+        if (q.tail_fold) kernel = attend_bf16_fold_kernel<DKQ, DV>;
+    }
+    if (q.tail_fold && kernel == mma_kernel<DKQ, DV, VK, Q8, TT>()) return SFA_ERR_UNSUPPORTED;
+    if (!ensure_max_dynamic_smem(kernel)) return SFA_ERR_CUDA;
     const cudaError_t e =
-        q.cluster_merge ? launch_pdl_cluster(mma_kernel<DKQ, DV, VK, Q8, TT>(), grid,
-                                             dim3(kThreads), ring.smem, st, q.n_split, q)
-                        : launch_pdl(mma_kernel<DKQ, DV, VK, Q8, TT>(), grid, dim3(kThreads),
-                                     ring.smem, st, q);
+        q.cluster_merge ? launch_pdl_cluster(kernel, grid, dim3(kThreads), ring.smem, st,
+                                             q.n_split, q)
+                        : launch_pdl(kernel, grid, dim3(kThreads), ring.smem, st, q);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return SFA_ERR_CUDA;
