@@ -1780,7 +1780,8 @@ int run_attend(const void *Q, const void *K, const void *V, int dtype, int n_seq
     // The tail folded into the last split: the splits are planned over the kept tokens alone
     // (top_k cr), so that a list of 512 blocks and a 3-token tail takes eight tiles per split
     // instead of nine.  Only where the plan stays an in-cluster merge on the warp-level bf16
-    // kernel with V = K, and the tail is a plain suffix (no window) of at most 15 tokens.
+    // kernel with V = K, and the tail is a plain suffix (no window) of at most 15 tokens.  (One-
+    // split prefill lists measured slower with it: pp2048's attention 905 -> 911 us.)
     int tail_fold = 0;
     if (dtype == SFA_BF16 && !dense && !V && window == 0 && part == SFA_PART_ALL && cr >= 2 &&
         cr <= 16 && ap.cluster_ns > 1 && !ap.use_tc && !ap.use_ws && ap.tt == 32) {
