@@ -89,6 +89,32 @@ def test_bounds_hold(dev, d_idx, h_idx):
         assert np.median(half) < 0.1 * np.median(np.abs(e[i, :B]) + 1e-30)
 
 
+@pytest.mark.parametrize("d_idx,h_idx", [(128, 8), (64, 16), (128, 4)])
+def test_bounds_hold_wide_tiles(dev, d_idx, h_idx):
+    """The bound pass on prefill-shaped query tiles (96 queries of one sequence: tiles of 16 or
+    32 queries, B operands of 128 or 256 columns, twelve epilogue warps): lower <= exact <=
+    upper on every visible block, nothing written past a query's blocks."""
+    cr, n_tok = 4, 6000
+    pos = list(range(5999 - 95, 6000))
+    X, qi, w, q_seq, q_pos, Kb = _case(dev, 5 + d_idx + h_idx, 1, n_tok, d_idx, h_idx, cr, pos)
+    n_q, n_blk_max = len(pos), 1500
+    exact = torch.full((n_q, n_blk_max), float("nan"), device=dev)
+    lower = torch.full_like(exact, float("nan"))
+    upper = torch.full_like(exact, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_index_scores(qi, w, q_seq, q_pos, Kb[0], cr, n_blk_max, exact, q_group=n_q,
+                         dev_status=status)
+    sfa.sfa_index_scores_bounded(qi, w, q_seq, q_pos, *Kb, cr, n_blk_max, lower, upper,
+                                 q_group=n_q, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    e, lo, up = np32(exact), np32(lower), np32(upper)
+    for i, p in enumerate(pos):
+        B = (p + 1) // cr
+        assert np.all(lo[i, :B] <= e[i, :B]) and np.all(e[i, :B] <= up[i, :B]), i
+        assert np.all(np.isnan(lo[i, B:])) and np.all(np.isnan(up[i, B:])), i
+
+
 @pytest.mark.parametrize("top_k", [1, 64, 512, 2048])
 def test_refine_follows_agreement_rule(dev, top_k):
     cr, d_idx, h_idx = 4, 128, 8
