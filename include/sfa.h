@@ -212,7 +212,9 @@ int sfa_topk_blocks(const float *scores, int64_t score_stride, const int32_t *q_
  * Limits: n_blk_max <= 131072 (each CTA of a row's cluster takes 3 rounds of 4096 blocks
  * up to 36864 blocks per row, 8 beyond); 1 <= top_k <= 2048; d_idx in {64, 128};
  * 1 <= h_idx <= 16.
- * Errors as the other entry points (host checks before any launch, SFA_DEV_* flags).
+ * Errors as the other entry points (host checks before any launch, SFA_DEV_* flags); a
+ * candidate id outside its row (which only inconsistent lower/upper arrays could produce) is
+ * not read and raises SFA_DEV_BAD_BLOCK.
  */
 int sfa_index_scores_bounded(const void *q_idx, const float *w, const int32_t *q_seq,
                              const int32_t *q_pos, int n_q, int q_group, int h_idx, int d_idx,
