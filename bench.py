@@ -559,6 +559,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--exact", action="store_true",
                     help="decode: exact scores + select instead of the bounded selection")
+    ap.add_argument("--bounded", action="store_true",
+                    help="decode: the bounded selection even below its default size (captures)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller runs for ncu captures)")
     ap.add_argument("--paged", action="store_true",
@@ -604,7 +606,10 @@ def main():
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
              torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
-    wb = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged, kv=args.kv)
+    if args.exact and args.bounded:
+        raise SystemExit("--exact and --bounded exclude each other")
+    sel_mode = False if args.exact else (True if args.bounded else None)
+    wb = Workbench(w, dev, bounded=sel_mode, paged=args.paged, kv=args.kv)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -726,7 +731,7 @@ def main():
 
     if not args.no_paged and not args.paged and rank == 0 and world == 1:
         # the same workload on a paged cache: the pool and the attention read through the map
-        wbp = Workbench(w, dev, bounded=False if args.exact else None, paged=True, kv=args.kv)
+        wbp = Workbench(w, dev, bounded=sel_mode, paged=True, kv=args.kv)
         sp, _ = measure(wbp, max(3, args.steps // 2), 3, flush, per_stage=False)
         _, stp = measure(wbp, 3, 3, flush, per_stage=True)
         msp = sum(sp) / len(sp)
@@ -740,7 +745,7 @@ def main():
 
     if not args.no_q8 and args.kv == "bf16" and rank == 0 and world == 1:
         # the same workload on q8_0 K/V caches: the attention gathers the quantized rows
-        wbq = Workbench(w, dev, bounded=False if args.exact else None, paged=args.paged, kv="q8_0")
+        wbq = Workbench(w, dev, bounded=sel_mode, paged=args.paged, kv="q8_0")
         sq, _ = measure(wbq, max(3, args.steps // 2), 3, flush, per_stage=False)
         _, stq = measure(wbq, 3, 3, flush, per_stage=True)
         msq = sum(sq) / len(sq)
@@ -765,7 +770,7 @@ def main():
         # pass and as the two parts combined by their log-sum-exp
         res, outs = {}, {}
         for mode in ("single", "split"):
-            wbw = Workbench(w, dev, bounded=False if args.exact else None, window=WINDOW,
+            wbw = Workbench(w, dev, bounded=sel_mode, window=WINDOW,
                             window_mode=mode)
             sw, _ = measure(wbw, max(3, args.steps // 2), 3, flush, per_stage=False)
             _, stw = measure(wbw, 3, 3, flush, per_stage=True)
