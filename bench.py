@@ -185,7 +185,7 @@ class Workbench:
     """Inputs, buffers and one step of the method for workload w on the current device."""
 
     def __init__(self, w, dev, bounded=None, paged=False, kv="bf16", window=0,
-                 window_mode="single"):
+                 window_mode="single", bound_pass=None):
         self.w, self.dev, self.paged, self.kv = w, dev, paged, kv
         self.case = sfa.make_case(w, device=dev)
         self.n_blk_max = w.n_tok // w.compress_ratio
@@ -215,7 +215,8 @@ class Workbench:
                                 compress_ratio=w.compress_ratio,
                                 indexer_top_k=w.indexer_top_k, n_blk_max=self.n_blk_max,
                                 q_group=w.n_q_per_seq, bounded=bounded, cell_of=self.cell_of,
-                                window=window, window_mode=window_mode, device=dev)
+                                window=window, window_mode=window_mode, bound_pass=bound_pass,
+                                device=dev)
         # the cache state before the step: every block completed by earlier tokens is pooled
         self.first_new_blk = w.depth // w.compress_ratio
         self.step.pool(self.case["X"], 0, self.first_new_blk)
@@ -561,6 +562,8 @@ def main():
                     help="decode: exact scores + select instead of the bounded selection")
     ap.add_argument("--bounded", action="store_true",
                     help="decode: the bounded selection even below its default size (captures)")
+    ap.add_argument("--bound-pass", default=None, choices=["i8", "hi"],
+                    help="the bounded selection's bound pass (default: i8 up to a budget of 1024)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="override the number of sequences (smaller runs for ncu captures)")
     ap.add_argument("--paged", action="store_true",
@@ -609,7 +612,8 @@ def main():
     if args.exact and args.bounded:
         raise SystemExit("--exact and --bounded exclude each other")
     sel_mode = False if args.exact else (True if args.bounded else None)
-    wb = Workbench(w, dev, bounded=sel_mode, paged=args.paged, kv=args.kv)
+    wb = Workbench(w, dev, bounded=sel_mode, paged=args.paged, kv=args.kv,
+                   bound_pass=args.bound_pass)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
