@@ -274,6 +274,39 @@ def test_gather_attend_cluster_merge(dev, n_q):
         assert np.abs(Ln[i] - rlse).max() < 2e-3, i
 
 
+@pytest.mark.parametrize("cr,top_k", [(8, 512), (16, 128)])
+def test_gather_attend_cluster_merge_long_tails(dev, cr, top_k):
+    """32 decode queries split over 8-CTA clusters with the tail folded into the last split, at
+    block sizes whose tails reach 7 and 15 tokens (every tail length occurs), against the
+    oracle."""
+    dkq, dv, h_q, h_kv = 576, 512, 16, 1
+    n_q, n_seq = 32, 4
+    n_tok = top_k * cr + 2 * cr
+    q_seq = (np.arange(n_q) % n_seq).astype(np.int32)
+    # full lists with every tail length, and a few short ones (later splits empty)
+    q_pos = np.array([top_k * cr + (i % cr) for i in range(24)] + [cr * 3 + 1, cr - 1, 5, 2,
+                     top_k * cr // 2 + 3, 0, 7, cr * 10 + cr - 2], np.int32)
+    Q, K, V = _attend_case(dev, dkq, dv, True, h_q, h_kv, n_seq, n_tok, q_seq, q_pos,
+                           torch.bfloat16, 31 + cr)
+    sel, n_sel = _random_selection(q_pos, cr, top_k, cr)
+    scale = 1.0 / math.sqrt(dkq)
+    O = torch.full((n_q, h_q, dv), float("nan"), device=dev)
+    lse = torch.full((n_q, h_q), float("nan"), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sfa.sfa_gather_attend(Q, K, V, torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_pos).to(dev),
+                          torch.from_numpy(sel).to(dev), torch.from_numpy(n_sel).to(dev), top_k,
+                          cr, scale, O, lse=lse, dev_status=status)
+    torch.cuda.synchronize()
+    assert sfa.sfa_read_device_status(status) == 0
+    Kn, Qn, On, Ln = np32(K), np32(Q), np32(O), np32(lse)
+    for i in range(n_q):
+        s, p = q_seq[i], int(q_pos[i])
+        msk = oracle.mask(p, cr, sel[i], int(n_sel[i]))
+        ref, rlse = oracle.attend(Qn[i], Kn[s], None, msk, scale, h_kv, dv=dv)
+        assert row_rel_err(On[i], ref).max() < TOL_BF16, i
+        assert np.abs(Ln[i] - rlse).max() < 2e-3, i
+
+
 @pytest.mark.parametrize("dkq,dv,v_is_k,h_q,h_kv", ATTN_SHAPES[:2])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_dense_attend_matches_oracle(dev, dkq, dv, v_is_k, h_q, h_kv, dtype):
