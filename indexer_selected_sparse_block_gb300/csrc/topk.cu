@@ -13,9 +13,9 @@
 // consecutive elements back as order-preserving 32-bit keys.  The k-th largest of the 1024
 // per-thread maxima is at most the k-th largest key T (the maxima are keys of distinct
 // elements), so the floor of its histogram bin bounds T from below; the bins are 12-bit
-// windows sized to the range the maxima span, so the bound is tight.  While a piece is
-// selected, the CTA's next piece is prefetched into L2.  Only the keys at or above it (k and a few
-// per cent more on score rows) are compacted, in index order, into shared memory, where a
+// windows sized to the range the maxima span, so the bound is tight (while a piece is
+// selected, the CTA's next piece is prefetched into L2).  Only the keys at or above it (k and
+// a few per cent more on score rows) are compacted, in index order, into shared memory, where a
 // radix select whose 12-bit digit windows are again sized to the candidates' range finds T
 // (one pass for most rows, at most three).  A single block scan over the candidate list, of
 // the counts above T and equal to T packed in one word, then gives every kept candidate its
@@ -138,10 +138,11 @@ __device__ __forceinline__ void clear_hist(Smem &sh, int nbins) {
 // Words [0, n) of src into dst (shared memory, 16-byte aligned), n <= R * kThreads: coalesced
 // 16-byte loads over the aligned body, single words at its two ends.  Each word is loaded by
 // exactly one thread; *mxf is the largest (NaN-skipping) of the scores this thread loaded and
-// *n_mine their count, so that the per-thread maxima are maxima of disjoint groups.
+// *n_mine their count, so that the per-thread maxima are maxima of disjoint groups.  Returns
+// the number of 16-byte vectors (threads below it hold at least four scores).
 template <int R>
-__device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t *dst,
-                                            float *mxf, int *n_mine) {
+__device__ __forceinline__ int stage_piece(const uint32_t *src, int n, uint32_t *dst,
+                                           float *mxf, int *n_mine) {
     const int tid = threadIdx.x;
     int head = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u)) & 15u) >> 2);
     head = head < n ? head : n;
@@ -197,6 +198,7 @@ __device__ __forceinline__ void stage_piece(const uint32_t *src, int n, uint32_t
             }
         }
     }
+    return nvec;
 }
 
 // Key of -inf: keys below it are NaN images only (order_key maps every NaN to 0).
@@ -537,13 +539,11 @@ __global__ void __launch_bounds__(kThreads, kPerSm) topk_stage_kernel(const Topk
         // ---- this thread's R consecutive elements, as keys (0 past the piece: never kept)
         float mxf;
         int n_mine;
-        stage_piece<R>(src, n, stg, &mxf, &n_mine);
+        const int nvec = stage_piece<R>(src, n, stg, &mxf, &n_mine);
         __syncthreads();
         const int e0 = tid * R;
         const int nv = n - e0 < 0 ? 0 : (n - e0 < R ? n - e0 : R);
-        // threads holding at least one 16-byte vector of the piece (stage_piece's split)
-        const int head = min((int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u)) & 15u) >> 2), n);
-        const int groups = min(kThreads, (n - head) >> 2);
+        const int groups = min(kThreads, nvec);   // threads holding a 16-byte vector each
         const Cut cut = select_cut<R>(stg, e0, nv, n, k, mxf, n_mine, groups, sh);
         if (cut.nc >= 0) {
             // ---- ascending write-out from the candidate list
