@@ -578,6 +578,8 @@ def main():
                     help="override the cache depth (smaller runs for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.exact and args.bounded:
+        ap.error("--exact and --bounded exclude each other")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -609,8 +611,6 @@ def main():
     flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev),
              torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev))
 
-    if args.exact and args.bounded:
-        raise SystemExit("--exact and --bounded exclude each other")
     sel_mode = False if args.exact else (True if args.bounded else None)
     wb = Workbench(w, dev, bounded=sel_mode, paged=args.paged, kv=args.kv,
                    bound_pass=args.bound_pass)

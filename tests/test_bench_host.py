@@ -42,3 +42,12 @@ def test_pooled_key_bytes():
     c = b.algorithmic(w, [1] * w.n_q, bounded="i8")
     assert c["kbar_bytes"] == w.n_q * nb * (w.d_idx + 8)           # codes + scale, bound factor
     assert c["score_bytes"] == a["score_bytes"]
+
+
+def test_conflicting_selection_flags_are_refused():
+    """--exact and --bounded together stop at argument parsing, before any device work."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--exact", "--bounded"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 2
+    assert "--exact and --bounded exclude each other" in r.stderr
