@@ -52,7 +52,7 @@ typedef struct CUstream_st *sfa_stream_t; /* identical to cudaStream_t */
 enum sfa_status {
     SFA_OK = 0,
     SFA_ERR_INVALID_ARG = 1, /* a pointer, size, stride or alignment the call cannot accept */
-    SFA_ERR_UNSUPPORTED = 2, /* a valid shape this build has no kernel for                */
+    SFA_ERR_UNSUPPORTED = 2, /* a valid shape the library has no kernel for               */
     SFA_ERR_CUDA = 3,        /* the CUDA runtime reported an error while enqueuing         */
     SFA_ERR_WORKSPACE = 4    /* the workspace is NULL or smaller than the size query says  */
 };

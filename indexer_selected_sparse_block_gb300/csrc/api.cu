@@ -85,7 +85,7 @@ extern "C" const char *sfa_status_string(int status) {
     switch (status) {
         case SFA_OK: return "SFA_OK";
         case SFA_ERR_INVALID_ARG: return "SFA_ERR_INVALID_ARG: an argument the call cannot accept";
-        case SFA_ERR_UNSUPPORTED: return "SFA_ERR_UNSUPPORTED: a shape this build has no kernel for";
+        case SFA_ERR_UNSUPPORTED: return "SFA_ERR_UNSUPPORTED: a shape the library has no kernel for";
         case SFA_ERR_CUDA: return "SFA_ERR_CUDA: the CUDA runtime reported an error";
         case SFA_ERR_WORKSPACE: return "SFA_ERR_WORKSPACE: workspace missing or too small";
         default: return "unknown sfa status";

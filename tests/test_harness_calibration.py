@@ -1,6 +1,6 @@
 """Calibration of the parity harness with planted mistakes.
 
-The GPU parity tests judge the library with two checks: the selection-agreement rule on the
+The GPU parity tests check the library in two ways: the selection-agreement rule on the
 kept blocks (``check_selection``) and the per-row relative error of the outputs
 (``row_rel_err`` against ``TOL_BF16``).  A harness that cannot fail proves nothing, so this
 file plants the plausible mistakes of the method -- a kept block swapped for the first one
