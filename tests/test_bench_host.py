@@ -51,3 +51,23 @@ def test_conflicting_selection_flags_are_refused():
                        capture_output=True, text=True, cwd=ROOT, timeout=300)
     assert r.returncode == 2
     assert "--exact and --bounded exclude each other" in r.stderr
+
+
+def test_traffic_records_name_existing_kernels():
+    """Each DRAM-traffic record the bench can report names a workload the bench knows, a source
+    file that defines the kernel it was taken on, and read + write bytes that add up."""
+    import json
+    import indexer_selected_sparse_block_gb300 as sfa
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    assert records
+    csrc = os.path.join(ROOT, "indexer_selected_sparse_block_gb300", "csrc")
+    for key, rec in records.items():
+        stage, workload = key.split("@")
+        assert stage in ("scores", "topk", "attend"), key
+        assert workload in sfa.WORKLOADS, key
+        with open(os.path.join(csrc, rec["source"])) as f:
+            src = f.read()
+        assert rec["kernel"].split("<")[0] in src, key
+        assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"], key
+        assert len(rec["src_sha256_16"]) == 16 and rec["command"].startswith("ncu "), key
