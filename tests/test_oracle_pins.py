@@ -543,6 +543,9 @@ MUTANTS = {
                             "const double p = (double)(b + pos_offset);"),
     "window_one_too_long": ("int64_t first = p - window + 1;", "int64_t first = p - window;"),
     "window_ignored": ("for (int64_t t = first; t <= p; ++t) mask[t] = 1;", ""),
+    "lse_without_max": ("if (lse) lse[h] = m + log(denom);", "if (lse) lse[h] = log(denom);"),
+    "kept_block_short_by_one": ("t < (int64_t)sel[i] * cr + cr; ++t) mask[t] = 1;",
+                                "t < (int64_t)sel[i] * cr + cr - 1; ++t) mask[t] = 1;"),
 }
 
 
