@@ -546,6 +546,10 @@ MUTANTS = {
     "lse_without_max": ("if (lse) lse[h] = m + log(denom);", "if (lse) lse[h] = log(denom);"),
     "kept_block_short_by_one": ("t < (int64_t)sel[i] * cr + cr; ++t) mask[t] = 1;",
                                 "t < (int64_t)sel[i] * cr + cr - 1; ++t) mask[t] = 1;"),
+    "one_head_weight": ("s += (double)w[j] * relu;", "s += (double)w[0] * relu;"),
+    "one_index_query": ("dot += (double)q_idx[j * d_idx + d] * kbar[b * d_idx + d];",
+                        "dot += (double)q_idx[d] * kbar[b * d_idx + d];"),
+    "kept_ids_unsorted": ("qsort(sel, (size_t)n_sel, sizeof(int32_t), ascending_i32);", ""),
 }
 
 
