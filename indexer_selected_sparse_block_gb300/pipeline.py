@@ -69,10 +69,10 @@ class SfaStep:
         # cannot rule out) cuts the pooled-key bytes of decode-like steps, where each query
         # streams its sequence's pooled keys; prefill tiles share those reads and take the
         # exact scores directly.  Rows of at most 131072 blocks.  Its selection is a latency
-        # chain of ~20 us, which pays only once the exact pass would stream enough bytes:
+        # chain of 22-27 us, which pays only once the exact pass would stream enough bytes:
         # measured on GB300, the exact pair was faster up to 67 MB of pooled keys per step
-        # (16 queries x 8192 blocks: 48.1 against 50.2 us; one query x 1024 blocks: 31.5
-        # against 35.9 us) and slower from 268 MB (4 x 131072 blocks: 91 against 60.5 us).
+        # (16 queries x 8192 blocks: 48.1 against 50.2 us; one query x 1024 blocks: 31.2
+        # against 35.9 us) and slower from 268 MB (4 x 131072 blocks: 91 against 59 us).
         if bounded is None:
             exact_bytes = n_q * n_blk_max * 4 * d_idx
             bounded = (q_group <= 4 and n_blk_max <= B.SFA_REFINE_MAX_BLOCKS
